@@ -1,0 +1,180 @@
+/*
+ * snack.h -- C ABI of the GB300 truly sparse linear layer.
+ *
+ * Source: "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks
+ * on GPU" (abstract).  The abstract describes a GPU layer that keeps and
+ * multiplies only the weights that exist (a COO SpMM kernel), computes its
+ * gradients without ever forming a dense weight, and lets the user rewire
+ * its connections during Dynamic Sparse Training.  This header makes those
+ * four operations concrete:
+ *
+ *   forward        Y[b,r]  = bias[r] + sum_{k: row[k]=r} val[k] * X[b,col[k]]
+ *   input grad     dX[b,c] = sum_{k: col[k]=c} val[k] * dY[b,row[k]]
+ *   weight grad    dW[k]   = sum_b dY[b,row[k]] * X[b,col[k]]  (stored positions only)
+ *                  db[r]   = sum_b dY[b,r]
+ *   restructure    prune the n_prune smallest |val|, regrow as many at uniformly
+ *                  random positions that were empty, value +0, re-sort the COO.
+ *
+ * Layout.  W is out_f x in_f, stored as row-sorted COO: int32 row[nnz] and
+ * col[nnz], strictly increasing in (row, col) (no duplicates), plus val[nnz]
+ * in fp32 or bf16.  X is [batch, in_f] and Y is [batch, out_f], row-major
+ * (torch Linear convention, Y = X W^T + b); dY and dX likewise.  bias, dW and
+ * db are fp32.  Accumulation is fp32 in every kernel.
+ *
+ * Memory ownership.  Every device buffer -- indices, values, activations,
+ * outputs, the plan and the workspaces -- is allocated and freed by the
+ * caller.  The library never allocates device memory.  A handle owns host
+ * metadata only; snack_destroy frees it and nothing else.
+ *
+ * Streams.  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream), except snack_create with validate != 0 and
+ * snack_restructure, which synchronise `stream` to read back a small count.
+ * A plan and a workspace may be used by one call in flight at a time.
+ *
+ * Errors.  Every entry point returns a snack_status.  Arguments are checked
+ * on the host before any launch; a failed launch or CUDA call returns
+ * SNACK_ERR_CUDA.  The library never aborts, exits or traps on the device.
+ *
+ * Plan contract.  snack_create derives a plan (row offsets, load-balanced
+ * tiles, a column-ordered view) from row/col.  row/col may change only through
+ * snack_restructure, which rebuilds the plan for the new pattern; the values
+ * may change freely between calls.  Passing a different pattern than the one
+ * the plan was built from gives undefined results (no fault: every index the
+ * kernels use is read from the plan, whose entries are in range).
+ */
+#ifndef SNACK_H
+#define SNACK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SNACK_VERSION 1
+
+/* Opaque layer handle (host memory only). */
+typedef struct snack_layer *snack_handle;
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *snack_stream_t;
+
+typedef enum snack_status {
+  SNACK_OK = 0,
+  SNACK_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, aliasing, batch > max_batch */
+  SNACK_ERR_UNSORTED = 2,     /* validation: (row, col) not strictly increasing */
+  SNACK_ERR_OUT_OF_RANGE = 3, /* validation: an index outside [0,out_f) x [0,in_f) */
+  SNACK_ERR_WORKSPACE = 4,    /* plan or workspace smaller than the size query returned */
+  SNACK_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+  SNACK_ERR_TIMEOUT = 6,      /* reserved for bounded device-side waits (none today) */
+  SNACK_ERR_UNSUPPORTED = 7,  /* e.g. val and act dtypes differ */
+  SNACK_ERR_NO_SPACE = 8      /* restructure: too few empty positions, or draw budget spent */
+} snack_status;
+
+typedef enum snack_dtype { SNACK_F32 = 0, SNACK_BF16 = 1 } snack_dtype;
+
+/*
+ * Sizes of the caller-allocated buffers for a layer.
+ *   plan_bytes       persistent plan, alive as long as the handle;
+ *   workspace_bytes  scratch for snack_create and for fwd / dx / dw with
+ *                    batch <= max_batch (contents need not survive calls).
+ * Limits: 1 <= out_f, in_f < 2^31; 0 <= nnz <= out_f*in_f and nnz < 2^31 - 1;
+ * 1 <= max_batch <= 65535.  val_t must equal act_t (fp32/fp32 or bf16/bf16).
+ * Either output pointer may be NULL.
+ */
+snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch,
+                               snack_dtype val_t, snack_dtype act_t, size_t *plan_bytes,
+                               size_t *workspace_bytes);
+
+/*
+ * Build a layer handle and its plan from the pattern row/col (device, nnz
+ * entries each, caller-owned; only read during the call).  `plan` (device,
+ * 256-byte aligned, plan_bytes >= the queried size) receives the plan;
+ * `ws` (device, 256-byte aligned) is scratch.  With validate != 0 the pattern
+ * is checked on the device (ranges, strict order) and the call synchronises
+ * `stream` to return SNACK_ERR_OUT_OF_RANGE or SNACK_ERR_UNSORTED; with
+ * validate == 0 an invalid pattern gives undefined results.
+ * The handle is bound to the CUDA device current at this call.
+ */
+snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f, int64_t nnz,
+                          int32_t max_batch, snack_dtype val_t, snack_dtype act_t,
+                          const int32_t *row, const int32_t *col, void *plan, size_t plan_bytes,
+                          void *ws, size_t ws_bytes, int validate, snack_stream_t stream);
+
+/*
+ * Forward (the SNACK-COO SpMM of the abstract, over stored weights only):
+ *   y[b, r] = bias[r] + sum_{k : row[k] = r} val[k] * x[b, col[k]]
+ * x [batch, in_f] and y [batch, out_f] in act dtype; bias fp32 [out_f] or
+ * NULL (zero).  0 <= batch <= max_batch.  y must not overlap x.  Rows without
+ * stored weights get bias[r].  Deterministic (no atomics on outputs).
+ */
+snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                            const void *x, int32_t batch, const float *bias, void *y, void *ws,
+                            size_t ws_bytes, snack_stream_t stream);
+
+/*
+ * Input gradient (transposed SpMM; the sparse backward pass of the abstract):
+ *   dx[b, c] = sum_{k : col[k] = c} val[k] * dy[b, row[k]]
+ * dy [batch, out_f], dx [batch, in_f] in act dtype; dx must not overlap dy.
+ * Deterministic.
+ */
+snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                           const void *dy, int32_t batch, void *dx, void *ws, size_t ws_bytes,
+                           snack_stream_t stream);
+
+/*
+ * Weight gradient at the stored positions only (sampled dense-dense product):
+ *   dw[k] = sum_b dy[b, row[k]] * x[b, col[k]]     fp32 [nnz]
+ *   db[r] = sum_b dy[b, r]                         fp32 [out_f], or NULL to skip
+ * x [batch, in_f], dy [batch, out_f] in act dtype.  Deterministic.
+ */
+snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *col, const void *x,
+                            const void *dy, int32_t batch, float *dw, float *db, void *ws,
+                            size_t ws_bytes, snack_stream_t stream);
+
+/*
+ * Workspace needed by snack_restructure for a given n_prune.
+ */
+snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, size_t *bytes);
+
+/*
+ * Dynamic Sparse Training restructure (the abstract's connection rewiring):
+ *  1. rank stored weights by (|val|, k) ascending, NaN above every number;
+ *     the first n_prune are pruned;
+ *  2. survivors keep order and value bits;
+ *  3. draws i = 0, 1, ... of SplitMix64 (state mix(seed ^ mix(step)),
+ *     advanced by 0x9E3779B97F4A7C15 before each draw) are mapped to
+ *     positions p_i = floor(u_i * out_f*in_f / 2^64); p_i is accepted when it
+ *     was empty before this call and is not already accepted; stop at n_prune;
+ *  4. regrown entries (p / in_f, p mod in_f) get value +0;
+ *  5. the output is survivors and regrown merged in (row, col) order.
+ * Outputs (device, nnz entries, must not overlap the inputs): row_out, col_out,
+ * val_out (val dtype), src_out (optional, NULL to skip): old index k of each
+ * survivor, -1 for a regrown entry.  The handle's plan is rebuilt for the new
+ * pattern; later calls must pass row_out/col_out.  Needs ws_bytes >=
+ * snack_restructure_workspace_size(h, n_prune).  Synchronises `stream` once per
+ * batch of draws (normally once).  Returns SNACK_ERR_NO_SPACE when fewer than
+ * n_prune positions are empty or the draw budget (sized in the workspace
+ * query: twice the expected number of draws plus 4096) runs out; the handle's
+ * plan is then unchanged.
+ */
+snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t *col,
+                               const void *val, int64_t n_prune, uint64_t seed, uint64_t step,
+                               int32_t *row_out, int32_t *col_out, void *val_out, int32_t *src_out,
+                               void *ws, size_t ws_bytes, snack_stream_t stream);
+
+/* Free the host-side handle (no device memory is touched). NULL is allowed. */
+void snack_destroy(snack_handle h);
+
+/* Static description of a status code. */
+const char *snack_status_string(snack_status st);
+
+/* SNACK_VERSION of the built library. */
+int snack_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNACK_H */

@@ -6,10 +6,10 @@
  * does, and the two share no code, headers or tables.
  *
  * Source: "Beyond Masked Sparsity: SNACK Enables Truly Sparse Neural Networks
- * on GPU" (abstract).  The abstract describes a layer that "stores and
- * computes only non-zero connections" in COO form, back-propagates entirely
- * in that sparse form, and restructures its connections for Dynamic Sparse
- * Training.  It prints no formula, so every function below writes out the
+ * on GPU" (abstract).  The abstract describes a layer that keeps only the
+ * weights that exist (COO) and computes with those alone, takes its
+ * gradients in that same sparse form, and rewires its connections during
+ * Dynamic Sparse Training.  It prints no formula, so every function below writes out the
  * plain definition of the operation its name gives:
  *
  *   W is out_f x in_f, held as COO triples (row[k], col[k], val[k]),

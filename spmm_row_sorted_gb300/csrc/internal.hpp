@@ -1,0 +1,78 @@
+// Host-side internals shared by the translation units of libsnack.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "spmm.cuh"
+
+namespace snack {
+
+// Device pointers into the caller's plan buffer.
+struct PlanPtrs {
+  int32_t *rp;       // [out_f + 1]   row offsets of the row-sorted COO
+  int32_t *tiles_f;  // [(nt_f + 1) * 2] forward merge-path split points
+  int32_t *cp;       // [in_f + 1]    column offsets of the column view
+  int32_t *tiles_t;  // [(nt_t + 1) * 2] input-gradient split points
+  int32_t *row_t;    // [nnz]         row of each column-view entry
+  int32_t *src_t;    // [nnz]         storage index of each column-view entry
+  uint32_t *flags;   // [64]          validation flags and small device scalars
+};
+
+struct PlanLayout {
+  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, total;
+  TileGeom gf, gt;
+};
+
+PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max);
+PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
+size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
+
+// Fill the plan for the pattern (row, col).  Asynchronous on s.
+cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
+                       const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s);
+
+// flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
+cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
+                             uint32_t *flag, cudaStream_t s);
+
+// Restructure driver (restructure.cu).
+struct RestructureArgs {
+  int32_t out_f, in_f;
+  int64_t nnz, n_prune;
+  snack_dtype val_t;
+  uint64_t seed, step;
+  const int32_t *row, *col;
+  const void *val;
+  const int32_t *rp_old;  // row offsets of the input pattern (from the plan)
+  int32_t *row_out, *col_out;
+  void *val_out;
+  int32_t *src_out;  // may be null
+};
+size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
+// Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
+snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// Host SplitMix64 (state increment and finaliser of Steele, Lea and Flood 2014).
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ULL;
+__host__ __device__ inline uint64_t sm64_finalise(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+}  // namespace snack
+
+struct snack_layer {
+  int device;
+  int32_t out_f, in_f;
+  int64_t nnz;
+  int32_t max_batch;
+  snack_dtype val_t, act_t;
+  snack::PlanLayout lay;
+  snack::PlanPtrs p;
+  size_t plan_bytes;
+  int num_sms;
+};

@@ -1,0 +1,455 @@
+// Dynamic Sparse Training restructure on the GPU (prune smallest |w|, regrow
+// at random empty positions with value +0, re-sort the COO).
+//
+//  1. prune set: radix select (8-bit digits, high to low) of the n_prune-th
+//     smallest magnitude key t; ties at t are pruned in storage order, so the
+//     pruned set is exactly the n_prune smallest (|w|, k);
+//  2. survivors: one scan of the packed pair (key > t, key == t) gives every
+//     survivor its output slot (stable compaction);
+//  3. regrow: draws i of SplitMix64 map to positions by multiply-high; a draw
+//     is a candidate when the position was empty (binary search in its old
+//     row), and is accepted when it is the first draw of its position -- a
+//     hash table keeps the minimum draw index per position (atomicMin, so the
+//     outcome does not depend on thread order); a scan over draw order keeps
+//     the first n_prune accepted.  Draws run in chunks until enough are
+//     accepted (one host read-back per chunk);
+//  4. regrown positions are radix sorted and merged with the survivors by
+//     position (merge path), writing row/col/val/src.
+// Every step is integer work, so the output is bit-exact with the sequential
+// definition.
+#include <math.h>
+
+#include "internal.hpp"
+#include "prims.cuh"
+
+namespace snack {
+
+namespace {
+
+constexpr uint64_t kEmpty = ~0ull;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeItems = 4;
+constexpr int kMergeTile = kMergeThreads * kMergeItems;
+
+struct SelState {
+  uint32_t prefix, mask, remaining, total;
+  uint32_t hist[256];
+};
+
+__device__ __forceinline__ uint32_t canon_mag(uint32_t m) { return m > 0x7F800000u ? 0x7F800001u : m; }
+
+template <typename TV>
+__device__ __forceinline__ uint32_t mag_key(const TV *val, int64_t k);
+template <>
+__device__ __forceinline__ uint32_t mag_key<float>(const float *val, int64_t k) {
+  return canon_mag(__float_as_uint(val[k]) & 0x7FFFFFFFu);
+}
+template <>
+__device__ __forceinline__ uint32_t mag_key<bf16>(const bf16 *val, int64_t k) {
+  uint32_t b = reinterpret_cast<const uint16_t *>(val)[k];
+  return canon_mag((b & 0x7FFFu) << 16);
+}
+
+template <typename TV>
+__global__ void k_sel_hist(const TV *__restrict__ val, int64_t nnz, SelState *st, int shift) {
+  __shared__ uint32_t h[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const uint32_t prefix = st->prefix, mask = st->mask;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < nnz; k += stride) {
+    uint32_t key = mag_key<TV>(val, k);
+    if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (h[i]) atomicAdd(&st->hist[i], h[i]);
+}
+
+__global__ void k_sel_pick(SelState *st, int shift) {
+  if (threadIdx.x == 0) {
+    uint32_t rem = st->remaining, cum = 0;
+    for (int d = 0; d < 256; ++d) {
+      uint32_t c = st->hist[d];
+      if (cum + c >= rem) {
+        st->prefix |= (uint32_t)d << shift;
+        st->mask |= 0xFFu << shift;
+        st->remaining = rem - cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) st->hist[i] = 0;
+}
+
+__global__ void k_sel_init(SelState *st, uint32_t n_prune) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) st->hist[i] = 0;
+  if (threadIdx.x == 0) {
+    st->prefix = 0;
+    st->mask = 0;
+    st->remaining = n_prune;
+    st->total = 0;
+  }
+}
+
+template <typename TV>
+struct KeepVal {
+  const TV *val;
+  const SelState *st;
+  __device__ uint64_t operator()(int64_t k) const {
+    uint32_t key = mag_key<TV>(val, k), t = st->prefix;
+    return (uint64_t)(key > t) | ((uint64_t)(key == t) << 32);
+  }
+};
+
+struct KeepOut {
+  const int32_t *row, *col;
+  int32_t in_f;
+  const SelState *st;
+  uint64_t *surv_pos;
+  uint32_t *surv_src;
+  __device__ void operator()(int64_t k, uint64_t ex, uint64_t v) const {
+    const uint32_t m = st->remaining;
+    const uint32_t gt = (uint32_t)ex, eq = (uint32_t)(ex >> 32);
+    const bool keep = (v & 1ull) || ((v >> 32) && eq >= m);
+    if (keep) {
+      uint32_t s = gt + (eq > m ? eq - m : 0u);
+      surv_pos[s] = (uint64_t)(uint32_t)row[k] * (uint64_t)in_f + (uint32_t)col[k];
+      surv_src[s] = (uint32_t)k;
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_t *mins, uint64_t mask, uint64_t p) {
+  uint64_t h = sm64_finalise(p) & mask;
+  for (uint64_t probe = 0; probe <= mask; ++probe) {
+    uint64_t k = keys[h];
+    if (k == p) return mins[h];
+    if (k == kEmpty) return 0xFFFFFFFFu;
+    h = (h + 1) & mask;
+  }
+  return 0xFFFFFFFFu;
+}
+
+__global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int32_t out_f,
+                       const int32_t *__restrict__ rp, const int32_t *__restrict__ col, uint64_t *__restrict__ cand,
+                       uint64_t *hkeys, uint32_t *hmin, uint64_t hmask, uint32_t *overflow) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
+    const uint64_t i = i0 + (uint64_t)idx;
+    const uint64_t u = sm64_finalise(base + (i + 1) * kGolden);
+    const uint64_t p = __umul64hi(u, n_pos);
+    const uint64_t r = p / (uint64_t)in_f;
+    const int32_t c = (int32_t)(p - r * (uint64_t)in_f);
+    int32_t lo = rp[r], hi = rp[r + 1];
+    while (lo < hi) {
+      int32_t mid = lo + (hi - lo) / 2;
+      if (col[mid] < c)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    const bool member = lo < rp[r + 1] && col[lo] == c;
+    if (member) {
+      cand[idx] = kEmpty;
+      continue;
+    }
+    cand[idx] = p;
+    uint64_t h = sm64_finalise(p) & hmask;
+    bool done = false;
+    for (uint64_t probe = 0; probe <= hmask; ++probe) {
+      unsigned long long prev =
+          atomicCAS(reinterpret_cast<unsigned long long *>(hkeys + h), (unsigned long long)kEmpty,
+                    (unsigned long long)p);
+      if (prev == kEmpty || prev == p) {
+        atomicMin(hmin + h, (uint32_t)i);
+        done = true;
+        break;
+      }
+      h = (h + 1) & hmask;
+    }
+    if (!done) atomicOr(overflow, 1u);
+    (void)out_f;
+  }
+}
+
+struct AcceptVal {
+  const uint64_t *cand, *hkeys;
+  const uint32_t *hmin;
+  uint64_t hmask, i0;
+  __device__ uint32_t operator()(int64_t idx) const {
+    uint64_t p = cand[idx];
+    if (p == kEmpty) return 0u;
+    return hash_min(hkeys, hmin, hmask, p) == (uint32_t)(i0 + (uint64_t)idx) ? 1u : 0u;
+  }
+};
+
+struct AcceptOut {
+  const uint64_t *cand;
+  uint64_t *grown;
+  int64_t before, n_prune;
+  __device__ void operator()(int64_t idx, uint32_t ex, uint32_t v) const {
+    if (v) {
+      int64_t q = before + (int64_t)ex;
+      if (q < n_prune) grown[q] = cand[idx];
+    }
+  }
+};
+
+__global__ void k_merge_part(const uint64_t *__restrict__ A, int64_t na, const uint64_t *__restrict__ B, int64_t nb,
+                             int64_t n_tiles, int64_t *__restrict__ part) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t > n_tiles) return;
+  int64_t d = t * kMergeTile;
+  if (d > na + nb) d = na + nb;
+  int64_t lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
+  while (lo < hi) {
+    int64_t mid = (lo + hi) >> 1;
+    if (A[mid] <= B[d - 1 - mid])
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  part[t] = lo;
+}
+
+template <typename TV>
+__global__ void __launch_bounds__(kMergeThreads)
+    k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
+            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, const TV *__restrict__ val,
+            int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
+            int32_t *__restrict__ src_out) {
+  __shared__ uint64_t sA[kMergeTile];
+  __shared__ uint64_t sB[kMergeTile];
+  __shared__ uint32_t sS[kMergeTile];
+  __shared__ int32_t oS[kMergeTile];
+  const int64_t t = blockIdx.x;
+  const int64_t n = na + nb;
+  const int64_t d0 = t * kMergeTile;
+  const int64_t d1 = d0 + kMergeTile < n ? d0 + kMergeTile : n;
+  const int64_t a0 = part[t], a1 = part[t + 1];
+  const int64_t b0 = d0 - a0, b1 = d1 - a1;
+  const int la = (int)(a1 - a0), lb = (int)(b1 - b0);
+  for (int q = threadIdx.x; q < la; q += kMergeThreads) {
+    sA[q] = A[a0 + q];
+    sS[q] = As[a0 + q];
+  }
+  for (int q = threadIdx.x; q < lb; q += kMergeThreads) sB[q] = B[b0 + q];
+  __syncthreads();
+  int ld = threadIdx.x * kMergeItems;
+  if (ld > la + lb) ld = la + lb;
+  int lo = ld > lb ? ld - lb : 0, hi = ld < la ? ld : la;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (sA[mid] <= sB[ld - 1 - mid])
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  int ai = lo, bi = ld - lo;
+  uint64_t pos[kMergeItems];
+  int32_t src[kMergeItems];
+#pragma unroll
+  for (int it = 0; it < kMergeItems; ++it) {
+    src[it] = -2;
+    if (ld + it >= la + lb) continue;
+    bool take_a = bi >= lb || (ai < la && sA[ai] <= sB[bi]);
+    if (take_a) {
+      pos[it] = sA[ai];
+      src[it] = (int32_t)sS[ai];
+      ++ai;
+    } else {
+      pos[it] = sB[bi];
+      src[it] = -1;
+      ++bi;
+    }
+  }
+  __syncthreads();
+  // stage rows / cols / sources in shared memory, then write coalesced
+#pragma unroll
+  for (int it = 0; it < kMergeItems; ++it)
+    if (src[it] != -2) {
+      uint64_t r = pos[it] / (uint64_t)in_f;
+      sA[ld + it] = r;
+      sB[ld + it] = pos[it] - r * (uint64_t)in_f;
+      oS[ld + it] = src[it];
+    }
+  __syncthreads();
+  for (int q = threadIdx.x; q < la + lb; q += kMergeThreads) {
+    int64_t o = d0 + q;
+    int32_t s = oS[q];
+    row_out[o] = (int32_t)sA[q];
+    col_out[o] = (int32_t)sB[q];
+    val_out[o] = s >= 0 ? val[s] : from_f32<TV>(0.f);
+    if (src_out) src_out[o] = s;
+  }
+}
+
+unsigned grid_for(int64_t n, int threads, int64_t cap = 65535 * 8) {
+  int64_t b = (n + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return (unsigned)b;
+}
+
+int bits_for(uint64_t v) {
+  int b = 0;
+  while (b < 64 && (v >> b) != 0) ++b;
+  return b;
+}
+
+// Expected number of draws to accept `need` distinct positions out of `empty`
+// empty ones, among n_pos equally likely positions: n_pos * (H(empty) -
+// H(empty - need)), using ln((e + 1/2) / (e - need + 1/2)) for the difference.
+double expected_draws(double n_pos, double empty, double need) {
+  if (need <= 0) return 0.0;
+  return n_pos * log((empty + 0.5) / (empty - need + 0.5));
+}
+
+struct RWs {
+  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, hkeys, hmin, radix, part, total;
+  int64_t d_max, cap, n_merge_tiles;
+};
+
+RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+  RWs w;
+  const double n_pos = (double)out_f * (double)in_f;
+  double e = expected_draws(n_pos, n_pos - (double)nnz, (double)n_prune);
+  double dm = n_prune > 0 ? ceil(2.0 * e) + 4096.0 : 0.0;
+  if (dm > 2147483647.0) dm = 2147483647.0;
+  w.d_max = (int64_t)dm;
+  int64_t cap = 16;
+  while (cap < 2 * w.d_max + 16) cap <<= 1;
+  w.cap = cap;
+  w.n_merge_tiles = (nnz + kMergeTile - 1) / kMergeTile;
+  const size_t n = (size_t)(nnz > 0 ? nnz : 1), np = (size_t)(n_prune > 0 ? n_prune : 1);
+  size_t o = 0;
+  w.state = o;
+  o += align_up(sizeof(SelState), kAlign);
+  w.scan = o;
+  int64_t scan_n = nnz > w.d_max ? nnz : w.d_max;
+  o += scan_temp_bytes<uint64_t>(scan_n > 0 ? scan_n : 1);
+  w.surv_pos = o;
+  o += align_up(8 * n, kAlign);
+  w.surv_src = o;
+  o += align_up(4 * n, kAlign);
+  w.grown_a = o;
+  o += align_up(8 * np, kAlign);
+  w.grown_b = o;
+  o += align_up(8 * np, kAlign);
+  w.cand = o;
+  o += align_up(8 * (size_t)(w.d_max > 0 ? w.d_max : 1), kAlign);
+  w.hkeys = o;
+  o += align_up(8 * (size_t)cap, kAlign);
+  w.hmin = o;
+  o += align_up(4 * (size_t)cap, kAlign);
+  w.radix = o;
+  o += radix_temp_bytes((int64_t)np);
+  w.part = o;
+  o += align_up(8 * (size_t)(w.n_merge_tiles + 1), kAlign);
+  w.total = o;
+  return w;
+}
+
+template <typename TV>
+snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+  const RWs W = rws_layout(a.out_f, a.in_f, a.nnz, a.n_prune);
+  if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  SelState *st = reinterpret_cast<SelState *>(b + W.state);
+  void *stemp = b + W.scan;
+  uint64_t *surv_pos = reinterpret_cast<uint64_t *>(b + W.surv_pos);
+  uint32_t *surv_src = reinterpret_cast<uint32_t *>(b + W.surv_src);
+  uint64_t *grown_a = reinterpret_cast<uint64_t *>(b + W.grown_a);
+  uint64_t *grown_b = reinterpret_cast<uint64_t *>(b + W.grown_b);
+  uint64_t *cand = reinterpret_cast<uint64_t *>(b + W.cand);
+  uint64_t *hkeys = reinterpret_cast<uint64_t *>(b + W.hkeys);
+  uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
+  int64_t *part = reinterpret_cast<int64_t *>(b + W.part);
+  const TV *val = reinterpret_cast<const TV *>(a.val);
+  const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
+  const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
+  cudaError_t e;
+#define SNACK_TRY(x)                       \
+  do {                                     \
+    e = (x);                               \
+    if (e != cudaSuccess) return SNACK_ERR_CUDA; \
+  } while (0)
+
+  // 1. prune threshold
+  k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
+  if (n_prune > 0) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      k_sel_hist<TV><<<grid_for(nnz, 256, 1184), 256, 0, s>>>(val, nnz, st, shift);
+      k_sel_pick<<<1, 256, 0, s>>>(st, shift);
+    }
+  }
+  SNACK_TRY(cudaGetLastError());
+  // 2. survivors
+  SNACK_TRY(scan_apply<uint64_t>(KeepVal<TV>{val, st}, nnz, KeepOut{a.row, a.col, a.in_f, st, surv_pos, surv_src},
+                                 (uint64_t *)nullptr, stemp, s));
+  // 3. regrow
+  if (n_prune > 0) {
+    SNACK_TRY(cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s));
+    SNACK_TRY(cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s));
+    const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
+    const double empty = (double)n_pos - (double)nnz;
+    int64_t done = 0, acc = 0;
+    uint32_t *d_total = &st->total;
+    uint32_t *d_overflow = &st->hist[0];  // hist is idle after the selection
+    SNACK_TRY(cudaMemsetAsync(d_overflow, 0, sizeof(uint32_t), s));
+    while (acc < n_prune) {
+      if (done >= W.d_max) return SNACK_ERR_NO_SPACE;
+      double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
+      int64_t m = (int64_t)ceil(want);
+      if (m > W.d_max - done) m = W.d_max - done;
+      k_draw<<<grid_for(m, 256), 256, 0, s>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
+                                              hkeys, hmin, (uint64_t)(W.cap - 1), d_overflow);
+      SNACK_TRY(cudaGetLastError());
+      SNACK_TRY(scan_apply<uint32_t>(AcceptVal{cand, hkeys, hmin, (uint64_t)(W.cap - 1), (uint64_t)done}, m,
+                                     AcceptOut{cand, grown_a, acc, n_prune}, d_total, stemp, s));
+      uint32_t h_total = 0, h_over = 0;
+      SNACK_TRY(cudaMemcpyAsync(&h_total, d_total, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+      SNACK_TRY(cudaMemcpyAsync(&h_over, d_overflow, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+      SNACK_TRY(cudaStreamSynchronize(s));
+      if (h_over) return SNACK_ERR_WORKSPACE;
+      acc += h_total;
+      done += m;
+    }
+  }
+  // 4. sort regrown positions, merge with survivors
+  const uint64_t *grown = grown_a;
+  if (n_prune > 1) {
+    bool second = false;
+    SNACK_TRY(radix_sort<uint64_t>(grown_a, nullptr, grown_b, nullptr, n_prune, bits_for(n_pos - 1), b + W.radix, s,
+                                   &second));
+    grown = second ? grown_b : grown_a;
+  }
+  if (nnz > 0) {
+    k_merge_part<<<grid_for(W.n_merge_tiles + 1, 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
+                                                                     W.n_merge_tiles, part);
+    k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
+        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, val, a.row_out, a.col_out,
+        reinterpret_cast<TV *>(a.val_out), a.src_out);
+  }
+  SNACK_TRY(cudaGetLastError());
+#undef SNACK_TRY
+  return SNACK_OK;
+}
+
+}  // namespace
+
+size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+  size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
+  size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
+  return r > p ? r : p;
+}
+
+snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+  if (a.val_t == SNACK_BF16) return restructure_impl<bf16>(a, ws, ws_bytes, s);
+  return restructure_impl<float>(a, ws, ws_bytes, s);
+}
+
+}  // namespace snack

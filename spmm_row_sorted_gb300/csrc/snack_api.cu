@@ -1,0 +1,380 @@
+// The C ABI of libsnack (declared in include/snack.h): argument checks on the
+// host, workspace carving, and dispatch to the kernels.  No device memory is
+// allocated here; every buffer comes from the caller.
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "internal.hpp"
+
+using namespace snack;
+
+namespace {
+
+struct DevGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DevGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      prev = -1;
+      ok = false;
+      return;
+    }
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DevGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return na && nb && x < y + nb && y < x + na;
+}
+
+inline bool dtype_ok(snack_dtype t) { return t == SNACK_F32 || t == SNACK_BF16; }
+
+struct SpmmWs {
+  size_t xt, carry, head, total;
+};
+
+SpmmWs spmm_ws(int32_t n_src, const TileGeom &tg, const BatchGeom &bg, size_t s_act, int batch) {
+  SpmmWs w;
+  size_t o = 0;
+  w.xt = o;
+  if (batch > 1) o += align_up((size_t)n_src * bg.ldx * s_act, kAlign);
+  w.carry = o;
+  o += align_up((size_t)bg.n_btiles * tg.n_tiles * bg.bt * 4, kAlign);
+  w.head = o;
+  o += align_up((size_t)bg.n_btiles * tg.n_tiles * bg.bt * 4, kAlign);
+  w.total = o;
+  return w;
+}
+
+struct DwWs {
+  size_t xt, dyt, total;
+};
+
+DwWs dw_ws(int32_t out_f, int32_t in_f, const BatchGeom &bg, size_t s_act, int batch) {
+  DwWs w;
+  size_t o = 0;
+  w.xt = o;
+  if (batch > 1) o += align_up((size_t)in_f * bg.ldx * s_act, kAlign);
+  w.dyt = o;
+  if (batch > 1) o += align_up((size_t)out_f * bg.ldx * s_act, kAlign);
+  w.total = o;
+  return w;
+}
+
+size_t ops_ws_bytes(int32_t out_f, int32_t in_f, int batch, snack_dtype act, const PlanLayout &lay) {
+  BatchGeom bg = batch_geom(batch, act);
+  size_t s = dtype_size(act);
+  size_t a = spmm_ws(in_f, lay.gf, bg, s, batch).total;
+  size_t b = spmm_ws(out_f, lay.gt, bg, s, batch).total;
+  size_t c = dw_ws(out_f, in_f, bg, s, batch).total;
+  size_t m = a > b ? a : b;
+  return m > c ? m : c;
+}
+
+snack_status check_shape(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t,
+                         snack_dtype act_t) {
+  if (out_f < 1 || in_f < 1 || nnz < 0 || nnz >= INT32_MAX) return SNACK_ERR_INVALID_ARG;
+  if ((uint64_t)nnz > (uint64_t)out_f * (uint64_t)in_f) return SNACK_ERR_INVALID_ARG;
+  if (max_batch < 1 || max_batch > 65535) return SNACK_ERR_INVALID_ARG;
+  if (!dtype_ok(val_t) || !dtype_ok(act_t)) return SNACK_ERR_INVALID_ARG;
+  if (val_t != act_t) return SNACK_ERR_UNSUPPORTED;
+  return SNACK_OK;
+}
+
+#define SNACK_CUDA(x)                              \
+  do {                                             \
+    if ((x) != cudaSuccess) return SNACK_ERR_CUDA; \
+  } while (0)
+
+template <typename T>
+snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const void *x, int32_t batch,
+                     const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s) {
+  BatchGeom bg = batch_geom(batch, h->act_t);
+  SpmmWs W = spmm_ws(h->in_f, h->lay.gf, bg, sizeof(T), batch);
+  if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  const T *xt = reinterpret_cast<const T *>(x);
+  if (batch > 1) {
+    T *xt_w = reinterpret_cast<T *>(b + W.xt);
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, xt_w, bg.ldx, s));
+    xt = xt_w;
+  }
+  SpmmParams p;
+  p.n_rows = h->out_f;
+  p.n_src = h->in_f;
+  p.ptr = h->p.rp;
+  p.tiles = h->p.tiles_f;
+  p.tg = h->lay.gf;
+  p.nnz = h->nnz;
+  p.idx = col;
+  p.val = val;
+  p.val_src = nullptr;
+  p.xt = xt;
+  p.bias = bias;
+  p.y = y;
+  p.batch = batch;
+  p.carry = reinterpret_cast<float *>(b + W.carry);
+  p.head = reinterpret_cast<float *>(b + W.head);
+  SNACK_CUDA(run_spmm<T>(p, bg, false, s));
+  return SNACK_OK;
+}
+
+template <typename T>
+snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t batch, void *dx, void *ws,
+                    size_t ws_bytes, cudaStream_t s) {
+  BatchGeom bg = batch_geom(batch, h->act_t);
+  SpmmWs W = spmm_ws(h->out_f, h->lay.gt, bg, sizeof(T), batch);
+  if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  const T *dyt = reinterpret_cast<const T *>(dy);
+  if (batch > 1) {
+    T *w = reinterpret_cast<T *>(b + W.xt);
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, w, bg.ldx, s));
+    dyt = w;
+  }
+  SpmmParams p;
+  p.n_rows = h->in_f;
+  p.n_src = h->out_f;
+  p.ptr = h->p.cp;
+  p.tiles = h->p.tiles_t;
+  p.tg = h->lay.gt;
+  p.nnz = h->nnz;
+  p.idx = h->p.row_t;
+  p.val = val;
+  p.val_src = h->p.src_t;
+  p.xt = dyt;
+  p.bias = nullptr;
+  p.y = dx;
+  p.batch = batch;
+  p.carry = reinterpret_cast<float *>(b + W.carry);
+  p.head = reinterpret_cast<float *>(b + W.head);
+  SNACK_CUDA(run_spmm<T>(p, bg, true, s));
+  return SNACK_OK;
+}
+
+template <typename T>
+snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, const void *x, const void *dy,
+                    int32_t batch, float *dw, float *db, void *ws, size_t ws_bytes, cudaStream_t s) {
+  BatchGeom bg = batch_geom(batch, h->act_t);
+  DwWs W = dw_ws(h->out_f, h->in_f, bg, sizeof(T), batch);
+  if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  const T *xt = reinterpret_cast<const T *>(x);
+  const T *dyt = reinterpret_cast<const T *>(dy);
+  if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
+  if (h->nnz == 0) return SNACK_OK;
+  if (batch > 1) {
+    T *a = reinterpret_cast<T *>(b + W.xt);
+    T *c = reinterpret_cast<T *>(b + W.dyt);
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, a, bg.ldx, s));
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, c, bg.ldx, s));
+    xt = a;
+    dyt = c;
+  }
+  SNACK_CUDA(run_sddmm<T>(h->nnz, row, col, h->out_f, h->in_f, xt, dyt, bg, dw, h->num_sms, s));
+  return SNACK_OK;
+}
+
+snack_status common_call_checks(snack_handle h, int32_t batch, void *ws) {
+  if (!h) return SNACK_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->max_batch) return SNACK_ERR_INVALID_ARG;
+  if (batch > 0 && (!ws || !aligned(ws, kAlign))) return SNACK_ERR_INVALID_ARG;
+  return SNACK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t,
+                               snack_dtype act_t, size_t *plan_bytes, size_t *workspace_bytes) {
+  snack_status st = check_shape(out_f, in_f, nnz, max_batch, val_t, act_t);
+  if (st != SNACK_OK) return st;
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, batch_geom(max_batch, act_t).bt);
+  if (plan_bytes) *plan_bytes = lay.total;
+  if (workspace_bytes) {
+    size_t a = ops_ws_bytes(out_f, in_f, max_batch, act_t, lay);
+    size_t b = plan_build_ws_bytes(out_f, in_f, nnz);
+    *workspace_bytes = a > b ? a : b;
+  }
+  return SNACK_OK;
+}
+
+snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch,
+                          snack_dtype val_t, snack_dtype act_t, const int32_t *row, const int32_t *col, void *plan,
+                          size_t plan_bytes, void *ws, size_t ws_bytes, int validate, snack_stream_t stream) {
+  if (!out_handle) return SNACK_ERR_INVALID_ARG;
+  *out_handle = nullptr;
+  snack_status st = check_shape(out_f, in_f, nnz, max_batch, val_t, act_t);
+  if (st != SNACK_OK) return st;
+  if (nnz > 0 && (!row || !col)) return SNACK_ERR_INVALID_ARG;
+  if (!plan || !aligned(plan, kAlign) || !ws || !aligned(ws, kAlign)) return SNACK_ERR_INVALID_ARG;
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, batch_geom(max_batch, act_t).bt);
+  if (plan_bytes < lay.total) return SNACK_ERR_WORKSPACE;
+  if (ws_bytes < plan_build_ws_bytes(out_f, in_f, nnz)) return SNACK_ERR_WORKSPACE;
+  int dev = 0;
+  SNACK_CUDA(cudaGetDevice(&dev));
+  int sms = 0;
+  SNACK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  PlanPtrs p = plan_ptrs(lay, plan);
+  if (validate) {
+    SNACK_CUDA(validate_pattern(out_f, in_f, nnz, row, col, p.flags, s));
+    uint32_t flag = 0;
+    SNACK_CUDA(cudaMemcpyAsync(&flag, p.flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    SNACK_CUDA(cudaStreamSynchronize(s));
+    if (flag & 1u) return SNACK_ERR_OUT_OF_RANGE;
+    if (flag & 2u) return SNACK_ERR_UNSORTED;
+  }
+  SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s));
+  snack_layer *h = new (std::nothrow) snack_layer;
+  if (!h) return SNACK_ERR_INVALID_ARG;
+  h->device = dev;
+  h->out_f = out_f;
+  h->in_f = in_f;
+  h->nnz = nnz;
+  h->max_batch = max_batch;
+  h->val_t = val_t;
+  h->act_t = act_t;
+  h->lay = lay;
+  h->p = p;
+  h->plan_bytes = plan_bytes;
+  h->num_sms = sms > 0 ? sms : 1;
+  *out_handle = h;
+  return SNACK_OK;
+}
+
+snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *x,
+                            int32_t batch, const float *bias, void *y, void *ws, size_t ws_bytes,
+                            snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  (void)row;
+  if (batch == 0) return SNACK_OK;
+  if (!x || !y || (h->nnz > 0 && (!col || !val))) return SNACK_ERR_INVALID_ARG;
+  const size_t s_act = dtype_size(h->act_t);
+  if (overlap(y, (size_t)batch * h->out_f * s_act, x, (size_t)batch * h->in_f * s_act)) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->act_t == SNACK_BF16) return run_fwd<bf16>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
+  return run_fwd<float>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
+}
+
+snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *dy,
+                           int32_t batch, void *dx, void *ws, size_t ws_bytes, snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  (void)row;
+  (void)col;
+  if (batch == 0) return SNACK_OK;
+  if (!dy || !dx || (h->nnz > 0 && !val)) return SNACK_ERR_INVALID_ARG;
+  const size_t s_act = dtype_size(h->act_t);
+  if (overlap(dx, (size_t)batch * h->in_f * s_act, dy, (size_t)batch * h->out_f * s_act)) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s);
+  return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s);
+}
+
+snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *col, const void *x, const void *dy,
+                            int32_t batch, float *dw, float *db, void *ws, size_t ws_bytes, snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  if (h->nnz > 0 && (!row || !col || !dw)) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (batch == 0) {  // empty sums
+    if (h->nnz > 0) SNACK_CUDA(cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)h->nnz, s));
+    if (db) SNACK_CUDA(cudaMemsetAsync(db, 0, sizeof(float) * (size_t)h->out_f, s));
+    return SNACK_OK;
+  }
+  if (!x || !dy) return SNACK_ERR_INVALID_ARG;
+  if (h->act_t == SNACK_BF16) return run_dw<bf16>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+  return run_dw<float>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+}
+
+snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, size_t *bytes) {
+  if (!h || !bytes || n_prune < 0 || n_prune > h->nnz) return SNACK_ERR_INVALID_ARG;
+  *bytes = restructure_ws_bytes(h->out_f, h->in_f, h->nnz, n_prune);
+  return SNACK_OK;
+}
+
+snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                               int64_t n_prune, uint64_t seed, uint64_t step, int32_t *row_out, int32_t *col_out,
+                               void *val_out, int32_t *src_out, void *ws, size_t ws_bytes, snack_stream_t stream) {
+  if (!h || n_prune < 0 || n_prune > h->nnz) return SNACK_ERR_INVALID_ARG;
+  const int64_t nnz = h->nnz;
+  if (!ws || !aligned(ws, kAlign)) return SNACK_ERR_INVALID_ARG;
+  if (nnz > 0 && (!row || !col || !val || !row_out || !col_out || !val_out)) return SNACK_ERR_INVALID_ARG;
+  const uint64_t n_pos = (uint64_t)h->out_f * (uint64_t)h->in_f;
+  if ((uint64_t)n_prune > n_pos - (uint64_t)nnz) return SNACK_ERR_NO_SPACE;
+  const size_t n4 = 4 * (size_t)nnz, nv = dtype_size(h->val_t) * (size_t)nnz;
+  const void *ins[3] = {row, col, val};
+  const size_t in_sz[3] = {n4, n4, nv};
+  const void *outs[4] = {row_out, col_out, val_out, src_out};
+  const size_t out_sz[4] = {n4, n4, nv, src_out ? n4 : 0};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], out_sz[i], ins[j], in_sz[j])) return SNACK_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], out_sz[i], outs[j], out_sz[j])) return SNACK_ERR_INVALID_ARG;
+  }
+  if (ws_bytes < restructure_ws_bytes(h->out_f, h->in_f, nnz, n_prune)) return SNACK_ERR_WORKSPACE;
+  if (nnz == 0) return SNACK_OK;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RestructureArgs a;
+  a.out_f = h->out_f;
+  a.in_f = h->in_f;
+  a.nnz = nnz;
+  a.n_prune = n_prune;
+  a.val_t = h->val_t;
+  a.seed = seed;
+  a.step = step;
+  a.row = row;
+  a.col = col;
+  a.val = val;
+  a.rp_old = h->p.rp;
+  a.row_out = row_out;
+  a.col_out = col_out;
+  a.val_out = val_out;
+  a.src_out = src_out;
+  snack_status st = run_restructure(a, ws, ws_bytes, s);
+  if (st != SNACK_OK) return st;
+  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s));
+  return SNACK_OK;
+}
+
+void snack_destroy(snack_handle h) { delete h; }
+
+const char *snack_status_string(snack_status st) {
+  switch (st) {
+    case SNACK_OK: return "ok";
+    case SNACK_ERR_INVALID_ARG: return "invalid argument";
+    case SNACK_ERR_UNSORTED: return "pattern not strictly increasing in (row, col)";
+    case SNACK_ERR_OUT_OF_RANGE: return "index out of range";
+    case SNACK_ERR_WORKSPACE: return "plan or workspace too small";
+    case SNACK_ERR_CUDA: return "CUDA error";
+    case SNACK_ERR_TIMEOUT: return "device wait timed out";
+    case SNACK_ERR_UNSUPPORTED: return "unsupported combination";
+    case SNACK_ERR_NO_SPACE: return "not enough empty positions or draw budget exhausted";
+  }
+  return "unknown status";
+}
+
+int snack_version(void) { return SNACK_VERSION; }
+
+}  // extern "C"

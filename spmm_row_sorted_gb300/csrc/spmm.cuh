@@ -1,0 +1,451 @@
+// SpMM over row-sorted COO (forward and input gradient), the weight-gradient
+// SDDMM, and the activation transposes they gather from.
+//
+// Work decomposition (forward; the input gradient runs the same kernel on the
+// column-ordered view of W):
+//  * The merge path of (row ends, stored weights) is cut into tiles of equal
+//    cost, a row end costing `row_weight` and a stored weight costing 1, so
+//    every tile has at most cost_per_tile weights AND a bounded number of rows
+//    whatever the row-length skew.  One CTA per (tile, batch tile).
+//  * Inside a CTA the tile is cut again into 8 equal-cost warp ranges.
+//  * A warp walks its rows.  Its 32 lanes form 32/G slots of G lanes; a slot
+//    takes one stored weight at a time and its G lanes each gather a 16-byte
+//    slice (V batch elements) of the transposed activation row Xt[col], so
+//    one weight's batch vector is read as whole 32-byte sectors.
+//  * Row sums reduce across slots with xor shuffles and land in shared
+//    memory; rows split between warps are combined in warp order, rows split
+//    between CTAs leave a partial ("carry" / "head") that a fix-up kernel adds
+//    in tile order.  No atomics on outputs: results are deterministic.
+//  * Outputs leave shared memory as contiguous runs of Y[b, r0:r1].
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace snack {
+
+constexpr int kSpmmThreads = 256;
+constexpr int kSpmmWarps = kSpmmThreads / 32;
+
+// Batch geometry of one call.
+struct BatchGeom {
+  int V;         // activation elements per lane slice (1, 4 or 8)
+  int G;         // lanes per stored weight (power of two <= 32)
+  int bt;        // batch elements per CTA = G * V
+  int n_btiles;  // CTAs along the batch
+  int ldx;       // row stride of the transposed activations (= n_btiles * bt; 1 when batch == 1)
+};
+
+inline BatchGeom batch_geom(int batch, snack_dtype act) {
+  BatchGeom g;
+  if (batch <= 1) {
+    g.V = 1;
+    g.G = 1;
+    g.bt = 1;
+    g.n_btiles = 1;
+    g.ldx = 1;
+    return g;
+  }
+  g.V = act == SNACK_BF16 ? 8 : 4;
+  int bp = (batch + g.V - 1) / g.V * g.V;
+  int lanes = bp / g.V;
+  int G = 1;
+  while (G < lanes && G < 32) G <<= 1;
+  g.G = G;
+  g.bt = G * g.V;
+  g.n_btiles = (bp + g.bt - 1) / g.bt;
+  g.ldx = g.n_btiles * g.bt;
+  return g;
+}
+
+// Tile geometry of one merge path (fixed per plan).
+struct TileGeom {
+  int32_t cost_per_tile;  // C
+  int32_t row_weight;     // w
+  int32_t n_tiles;
+  int32_t max_rows;       // rows a tile can touch, partial rows included
+};
+
+inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max) {
+  TileGeom t;
+  int c = 65536 / (bt_max > 0 ? bt_max : 1);
+  if (c < 256) c = 256;
+  if (c > 8192) c = 8192;
+  t.cost_per_tile = c;
+  // keep the staged rows of a tile within ~32 KB of shared memory
+  int rows_target = 32768 / ((bt_max + 1) * 4);
+  if (rows_target < 16) rows_target = 16;
+  int w = (c + rows_target - 1) / rows_target;
+  if (w < 2) w = 2;
+  t.row_weight = w;
+  int64_t total = (int64_t)w * n_rows + nnz;
+  int64_t nt = (total + c - 1) / c;
+  t.n_tiles = (int32_t)(nt > 0 ? nt : 1);
+  t.max_rows = (c + w - 1) / w + 2;
+  return t;
+}
+
+inline size_t spmm_smem_bytes(const TileGeom &tg, int bt) {
+  return (size_t)tg.max_rows * (bt + 1) * 4 + (size_t)kSpmmWarps * bt * 4 + (size_t)(tg.max_rows + 1) * 4 +
+         (size_t)(kSpmmWarps + 1) * 2 * 4;
+}
+
+struct SpmmParams {
+  int32_t n_rows;         // outputs per batch row (fwd: out_f, dx: in_f)
+  int32_t n_src;          // rows of the gathered operand (fwd: in_f, dx: out_f)
+  const int32_t *ptr;     // [n_rows + 1] segment offsets
+  const int32_t *tiles;   // [(n_tiles + 1) * 2] (row, nnz) split points
+  TileGeom tg;
+  int64_t nnz;
+  const int32_t *idx;     // [nnz] gather index (fwd: col, dx: row of the column view)
+  const void *val;        // [nnz] weights, storage order
+  const int32_t *val_src; // dx: storage index of each column-view entry; fwd: null
+  const void *xt;         // [n_src][ldx] transposed activations
+  const float *bias;      // [n_rows] or null
+  void *y;                // [batch][n_rows]
+  int32_t batch;
+  float *carry;           // [n_btiles][n_tiles][bt]
+  float *head;            // [n_btiles][n_tiles][bt]
+};
+
+// ------------------------------------------------------------------ kernels
+
+template <typename TA, typename TV, int V, int G, bool kGatherVal>
+__global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
+  constexpr int kSlots = 32 / G;
+  constexpr int kU = kSlots >= 8 ? 2 : 4;  // weights per slot in flight
+  extern __shared__ __align__(16) float smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane / G, g = lane % G;
+  const int t = blockIdx.x, bi = blockIdx.y;
+  const int bt = bg.bt;
+  const int b0 = bi * bt;
+  const int max_rows = P.tg.max_rows;
+  const int w = P.tg.row_weight;
+  const int ys_ld = bt + 1;
+  float *Ys = smem;
+  float *wcar = Ys + (size_t)max_rows * ys_ld;
+  int *rps = reinterpret_cast<int *>(wcar + kSpmmWarps * bt);
+  int *wsp = rps + max_rows + 1;
+
+  const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1];
+  int i1 = P.tiles[2 * t + 2];
+  const int j1 = P.tiles[2 * t + 3];
+  if (i1 - i0 + 1 > max_rows) i1 = i0 + max_rows - 1;  // defensive: never overrun shared memory
+  const int nr = i1 - i0 + 1;
+
+  for (int q = tid; q <= nr; q += kSpmmThreads) {
+    int r = i0 + q;
+    rps[q] = P.ptr[r < P.n_rows ? r : P.n_rows];
+  }
+  for (int b = tid; b < bt; b += kSpmmThreads) Ys[(size_t)(nr - 1) * ys_ld + b] = 0.f;
+  __syncthreads();
+
+  // warp ranges: equal cost slices of [c0, c1]
+  if (tid <= kSpmmWarps) {
+    const int64_t c0 = (int64_t)w * i0 + j0, c1 = (int64_t)w * i1 + j1;
+    const int64_t D = c0 + (c1 - c0) * tid / kSpmmWarps;
+    int lo = i0, hi = i1;
+    while (lo < hi) {
+      int mid = lo + (hi - lo + 1) / 2;
+      if ((int64_t)w * mid + rps[mid - i0] <= D)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    int64_t j = D - (int64_t)w * lo;
+    int64_t lim = rps[lo - i0 + 1];
+    if (j > lim) j = lim;
+    if (tid == kSpmmWarps) j = j1;
+    wsp[2 * tid] = lo;
+    wsp[2 * tid + 1] = (int)j;
+  }
+  __syncthreads();
+
+  const int wi0 = wsp[2 * warp], wj0 = wsp[2 * warp + 1];
+  const int wi1 = wsp[2 * warp + 2], wj1 = wsp[2 * warp + 3];
+  const TA *xt = reinterpret_cast<const TA *>(P.xt) + b0 + g * V;
+  const TV *val = reinterpret_cast<const TV *>(P.val);
+  const uint32_t src_max = (uint32_t)(P.n_src - 1);
+  const uint32_t nnz_max = (uint32_t)(P.nnz > 0 ? P.nnz - 1 : 0);
+
+  for (int i = wi0; i <= wi1; ++i) {
+    const int ps = max(rps[i - i0], wj0);
+    const int pe = i < wi1 ? rps[i - i0 + 1] : wj1;
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    for (int base = ps; base < pe; base += kSlots * kU) {
+      uint32_t c[kU];
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int k = base + u * kSlots + slot;
+        const bool ok = k < pe;
+        uint32_t cc = ok ? (uint32_t)ld_stream(P.idx + k) : 0u;
+        c[u] = cc < src_max ? cc : src_max;
+        float vv = 0.f;
+        if (ok) {
+          if (kGatherVal) {
+            uint32_t s = (uint32_t)ld_stream(P.val_src + k);
+            vv = to_f32(ld_keep(val + (s < nnz_max ? s : nnz_max)));
+          } else {
+            vv = to_f32(ld_stream(val + k));
+          }
+        }
+        v[u] = vv;
+      }
+      float x[kU][V];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) Slice<TA, V>::load(xt + (size_t)c[u] * bg.ldx, x[u]);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], x[u][e], acc[e]);
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (slot == 0) {
+      float *dst = i < wi1 ? Ys + (size_t)(i - i0) * ys_ld + g * V : wcar + warp * bt + g * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) dst[e] = acc[e];
+    }
+  }
+  __syncthreads();
+
+  // rows split between warps: add the carries in warp order
+  for (int b = tid; b < bt; b += kSpmmThreads) {
+#pragma unroll 1
+    for (int k = 0; k < kSpmmWarps; ++k) {
+      int r = wsp[2 * k + 2];
+      Ys[(size_t)(r - i0) * ys_ld + b] += wcar[k * bt + b];
+    }
+  }
+  __syncthreads();
+
+  const int nfin = nr - 1;  // rows i0 .. i1-1 end in this tile
+  const bool continued = rps[0] < j0;
+  const size_t slot_base = ((size_t)bi * P.tg.n_tiles + t) * bt;
+  if (i1 < P.n_rows)
+    for (int b = tid; b < bt; b += kSpmmThreads) P.carry[slot_base + b] = Ys[(size_t)(nr - 1) * ys_ld + b];
+  if (nfin >= 1 && continued)
+    for (int b = tid; b < bt; b += kSpmmThreads) P.head[slot_base + b] = Ys[b];
+  const int rs = continued ? 1 : 0;
+  const int nw = nfin - rs;
+  if (nw > 0) {
+    TA *y = reinterpret_cast<TA *>(P.y);
+    const int bmax = min(bt, P.batch - b0);
+    for (int b = warp; b < bmax; b += kSpmmWarps) {
+      TA *yrow = y + (size_t)(b0 + b) * P.n_rows + i0 + rs;
+      for (int q = lane; q < nw; q += 32) {
+        float s = Ys[(size_t)(q + rs) * ys_ld + b];
+        if (P.bias) s = P.bias[i0 + rs + q] + s;
+        yrow[q] = from_f32<TA>(s);
+      }
+    }
+  }
+}
+
+// Rows whose first stored weights sit in earlier tiles: bias + carries (tile
+// order) + head, written once.
+template <typename TA>
+__global__ void k_spmm_fixup(SpmmParams P, BatchGeom bg) {
+  const int t = blockIdx.x, bi = blockIdx.y;
+  const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1], i1 = P.tiles[2 * t + 2];
+  if (i1 <= i0 || i0 >= P.n_rows) return;
+  if (P.ptr[i0] >= j0) return;
+  int first = t - 1;
+  while (first > 0 && P.tiles[2 * first] == i0) --first;
+  const int bt = bg.bt, b0 = bi * bt;
+  TA *y = reinterpret_cast<TA *>(P.y);
+  for (int b = threadIdx.x; b < bt && b0 + b < P.batch; b += blockDim.x) {
+    float s = 0.f;
+    for (int u = first; u < t; ++u) s += P.carry[((size_t)bi * P.tg.n_tiles + u) * bt + b];
+    s += P.head[((size_t)bi * P.tg.n_tiles + t) * bt + b];
+    if (P.bias) s = P.bias[i0] + s;
+    y[(size_t)(b0 + b) * P.n_rows + i0] = from_f32<TA>(s);
+  }
+}
+
+// a [batch][n] -> at [n][ldx], zero-filled for b in [batch, ldx)
+template <typename T>
+__global__ void k_transpose(const T *__restrict__ a, int batch, int n, T *__restrict__ at, int ldx) {
+  __shared__ T tile[32][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int c0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int b = b0 + ty + 8 * j, c = c0 + tx;
+    T v = from_f32<T>(0.f);
+    if (b < batch && c < n) v = a[(size_t)b * n + c];
+    tile[ty + 8 * j][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int c = c0 + ty + 8 * j, b = b0 + tx;
+    if (c < n && b < ldx) at[(size_t)c * ldx + b] = tile[tx][ty + 8 * j];
+  }
+}
+
+// out[c] = sum_b a[b][c], b increasing
+template <typename T>
+__global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__restrict__ out) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  float s = 0.f;
+  for (int b = 0; b < batch; ++b) s += to_f32(a[(size_t)b * n + c]);
+  out[c] = s;
+}
+
+// dw[k] = sum_b dyt[row[k]][b] * xt[col[k]][b]
+template <typename TA, int V, int G>
+__global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__restrict__ row,
+                                               const int32_t *__restrict__ col, int32_t out_f, int32_t in_f,
+                                               const TA *__restrict__ xt, const TA *__restrict__ dyt, int ldx,
+                                               int n_chunks, float *__restrict__ dw) {
+  constexpr int kSlots = 32 / G;
+  constexpr int kU = kSlots >= 8 ? 2 : 4;
+  constexpr int kStep = kSlots * kU;
+  const int lane = threadIdx.x & 31;
+  const int slot = lane / G, g = lane % G;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const uint32_t rmax = (uint32_t)(out_f - 1), cmax = (uint32_t)(in_f - 1);
+  const int bt = G * V;
+  for (int64_t base = gw * kStep; base < nnz; base += nw * kStep) {
+    uint32_t r[kU], c[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      int64_t k = base + u * kSlots + slot;
+      bool ok = k < nnz;
+      uint32_t rr = ok ? (uint32_t)ld_stream(row + k) : 0u;
+      uint32_t cc = ok ? (uint32_t)ld_stream(col + k) : 0u;
+      r[u] = rr < rmax ? rr : rmax;
+      c[u] = cc < cmax ? cc : cmax;
+    }
+    float acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = 0.f;
+    for (int ch = 0; ch < n_chunks; ++ch) {
+      const int off = ch * bt + g * V;
+      float dyv[kU][V], xv[kU][V];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        Slice<TA, V>::load(dyt + (size_t)r[u] * ldx + off, dyv[u]);
+        Slice<TA, V>::load(xt + (size_t)c[u] * ldx + off, xv[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[u] = fmaf(dyv[u][e], xv[u][e], acc[u]);
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+    if (g == 0) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        int64_t k = base + u * kSlots + slot;
+        if (k < nnz) dw[k] = acc[u];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+template <typename TA, typename TV, int V, int G, bool kGV>
+cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
+  size_t smem = spmm_smem_bytes(p.tg, bg.bt);
+  auto kern = k_spmm_tiles<TA, TV, V, G, kGV>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(p.tg.n_tiles, bg.n_btiles);
+  kern<<<grid, kSpmmThreads, smem, s>>>(p, bg);
+  int fx = bg.bt < 32 ? 32 : (bg.bt > 256 ? 256 : bg.bt);
+  k_spmm_fixup<TA><<<grid, fx, 0, s>>>(p, bg);
+  return cudaGetLastError();
+}
+
+template <typename TA, typename TV, bool kGV>
+cudaError_t launch_spmm(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
+  constexpr int VV = ActTraits<TA>::kVec;
+  if (bg.V == 1) return launch_spmm_v<TA, TV, 1, 1, kGV>(p, bg, s);
+  switch (bg.G) {
+    case 1: return launch_spmm_v<TA, TV, VV, 1, kGV>(p, bg, s);
+    case 2: return launch_spmm_v<TA, TV, VV, 2, kGV>(p, bg, s);
+    case 4: return launch_spmm_v<TA, TV, VV, 4, kGV>(p, bg, s);
+    case 8: return launch_spmm_v<TA, TV, VV, 8, kGV>(p, bg, s);
+    case 16: return launch_spmm_v<TA, TV, VV, 16, kGV>(p, bg, s);
+    case 32: return launch_spmm_v<TA, TV, VV, 32, kGV>(p, bg, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename TA, int V, int G>
+cudaError_t launch_sddmm_v(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
+                           const TA *xt, const TA *dyt, const BatchGeom &bg, float *dw, int num_sms,
+                           cudaStream_t s) {
+  constexpr int kSlots = 32 / G;
+  constexpr int kStep = kSlots * (kSlots >= 8 ? 2 : 4);
+  int64_t groups = (nnz + kStep - 1) / kStep;  // one warp-iteration each
+  int64_t blocks = (groups + 7) / 8;
+  int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  int n_chunks = bg.ldx / bg.bt;
+  k_sddmm<TA, V, G><<<(unsigned)blocks, 256, 0, s>>>(nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks, dw);
+  return cudaGetLastError();
+}
+
+template <typename TA>
+cudaError_t launch_sddmm(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
+                         const TA *xt, const TA *dyt, const BatchGeom &bg, float *dw, int num_sms,
+                         cudaStream_t s) {
+  constexpr int VV = ActTraits<TA>::kVec;
+  if (nnz <= 0) return cudaSuccess;
+  if (bg.V == 1) return launch_sddmm_v<TA, 1, 1>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+  switch (bg.G) {
+    case 1: return launch_sddmm_v<TA, VV, 1>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+    case 2: return launch_sddmm_v<TA, VV, 2>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+    case 4: return launch_sddmm_v<TA, VV, 4>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+    case 8: return launch_sddmm_v<TA, VV, 8>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+    case 16: return launch_sddmm_v<TA, VV, 16>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+    case 32: return launch_sddmm_v<TA, VV, 32>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t launch_transpose(const T *a, int batch, int n, T *at, int ldx, cudaStream_t s) {
+  dim3 grid((n + 31) / 32, (ldx + 31) / 32);
+  k_transpose<T><<<grid, dim3(32, 8), 0, s>>>(a, batch, n, at, ldx);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_colsum(const T *a, int batch, int n, float *out, cudaStream_t s) {
+  k_colsum<T><<<(n + 255) / 256, 256, 0, s>>>(a, batch, n, out);
+  return cudaGetLastError();
+}
+
+// per-dtype entry points (explicitly instantiated in spmm_f32.cu / spmm_bf16.cu)
+template <typename T>
+cudaError_t run_spmm(const SpmmParams &p, const BatchGeom &bg, bool gather_val, cudaStream_t s);
+template <typename T>
+cudaError_t run_sddmm(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
+                      const T *xt, const T *dyt, const BatchGeom &bg, float *dw, int num_sms, cudaStream_t s);
+template <typename T>
+cudaError_t run_transpose(const T *a, int batch, int n, T *at, int ldx, cudaStream_t s);
+template <typename T>
+cudaError_t run_colsum(const T *a, int batch, int n, float *out, cudaStream_t s);
+
+}  // namespace snack

@@ -1,0 +1,28 @@
+// f32 instantiation of the SpMM / SDDMM / transpose launchers.
+#include "spmm.cuh"
+
+namespace snack {
+
+template <>
+cudaError_t run_spmm<float>(const SpmmParams &p, const BatchGeom &bg, bool gather_val, cudaStream_t s) {
+  return gather_val ? launch_spmm<float, float, true>(p, bg, s) : launch_spmm<float, float, false>(p, bg, s);
+}
+
+template <>
+cudaError_t run_sddmm<float>(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
+                          const float *xt, const float *dyt, const BatchGeom &bg, float *dw, int num_sms,
+                          cudaStream_t s) {
+  return launch_sddmm<float>(nnz, row, col, out_f, in_f, xt, dyt, bg, dw, num_sms, s);
+}
+
+template <>
+cudaError_t run_transpose<float>(const float *a, int batch, int n, float *at, int ldx, cudaStream_t s) {
+  return launch_transpose<float>(a, batch, n, at, ldx, s);
+}
+
+template <>
+cudaError_t run_colsum<float>(const float *a, int batch, int n, float *out, cudaStream_t s) {
+  return launch_colsum<float>(a, batch, n, out, s);
+}
+
+}  // namespace snack

@@ -1,0 +1,328 @@
+"""GPU parity: every op of the CUDA library, called through the C ABI, against
+the fp64 oracle on the same seeded inputs.
+
+Bar: fp32 |gpu - oracle| <= 1e-5 * T per output, bf16 (storage, fp32
+accumulation) <= 2e-3 * T, where T is the oracle's sum of |terms|; indices and
+restructure outputs bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from spmm_row_sorted_gb300 import build as snack_build
+from spmm_row_sorted_gb300 import snack
+from spmm_row_sorted_gb300 import workloads as wl
+
+from gpu_util import REL, act_tensor, assert_close_T, bits, f64, layer_tensors
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    snack_build.build()
+    snack.load()
+    oracle.set_threads(8)
+
+
+def run_layer_ops(layer: wl.Layer, acts: wl.Acts, ops=("fwd", "dx", "dw"), max_batch=None, with_bias=True):
+    row, col, val, bias = layer_tensors(layer)
+    B = acts.batch
+    L = snack.SparseLinear(layer.out_f, layer.in_f, row, col, val, bias if with_bias else None,
+                           max_batch=max_batch or max(B, 1), validate=True)
+    x = act_tensor(acts.x, acts.act_dtype)
+    dy = act_tensor(acts.dy, acts.act_dtype)
+    out = {}
+    if "fwd" in ops:
+        out["y"] = L.forward(x)
+    if "dx" in ops:
+        out["dx"] = L.grad_input(dy)
+    if "dw" in ops:
+        out["dw"], out["db"] = L.grad_weight(x, dy)
+    torch.cuda.synchronize()
+    L.close()
+    return out
+
+
+def check_layer_ops(layer: wl.Layer, acts: wl.Acts, ops=("fwd", "dx", "dw"), max_batch=None, with_bias=True,
+                    got=None):
+    got = got or run_layer_ops(layer, acts, ops, max_batch, with_bias)
+    rel = REL[layer.val_dtype]
+    v64 = oracle.as_f64(layer.val, layer.val_dtype)
+    x64 = oracle.as_f64(acts.x, acts.act_dtype)
+    dy64 = oracle.as_f64(acts.dy, acts.act_dtype)
+    b64 = oracle.as_f64(layer.bias) if with_bias else None
+    if "fwd" in ops:
+        y, t = oracle.fwd(layer.out_f, layer.in_f, layer.row, layer.col, v64, x64, b64)
+        assert_close_T(f64(got["y"]), y, t, rel, "fwd")
+    if "dx" in ops:
+        g, t = oracle.dx(layer.out_f, layer.in_f, layer.row, layer.col, v64, dy64)
+        assert_close_T(f64(got["dx"]), g, t, rel, "dx")
+    if "dw" in ops:
+        d, t, db = oracle.dw(layer.out_f, layer.in_f, layer.row, layer.col, x64, dy64)
+        assert_close_T(f64(got["dw"]), d, t, REL["f32"] if layer.val_dtype == "f32" else rel, "dw")
+        tdb = np.abs(dy64).sum(axis=0)
+        assert_close_T(f64(got["db"]), db, tdb, REL["f32"], "db")
+    return got
+
+
+# ---------------------------------------------------------------- small shapes, several tiles, ragged tails
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("batch", [1, 2, 3, 5, 8, 13, 32, 33, 64, 100, 130])
+def test_small_random(dtype, batch):
+    lay = wl.make_layer(97, 131, nnz=2500, val_std=0.5, val_dtype=dtype, seed=batch, bias="normal")
+    acts = wl.make_acts(batch, 131, 97, dtype, seed=batch)
+    check_layer_ops(lay, acts)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 37, 30), (37, 1, 20), (300, 4000, 60000), (4000, 300, 60000),
+                                   (33, 65, 0), (1000, 1000, 1000)])
+def test_shapes(dtype, shape):
+    out_f, in_f, nnz = shape
+    lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=0.3, val_dtype=dtype, seed=nnz + 7, bias="normal")
+    for batch in (1, 7, 32):
+        acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+        check_layer_ops(lay, acts)
+
+
+def test_one_row_holds_everything():
+    # a single row with 20000 weights: split across many tiles and warps
+    out_f, in_f = 50, 20000
+    row = np.full(in_f, 17, dtype=np.int32)
+    col = np.arange(in_f, dtype=np.int32)
+    val = wl.random_normal(in_f, seed=1, stream=0, std=0.1)
+    lay = wl.Layer(out_f, in_f, row, col, val, wl.random_normal(out_f, 1, 1), "f32")
+    for batch in (1, 4, 32, 40):
+        check_layer_ops(lay, wl.make_acts(batch, in_f, out_f, "f32", seed=batch))
+
+
+def test_zipf_rows_skew():
+    lay = wl.make_layer(2048, 3000, nnz=200000, zipf_s=1.2, val_dtype="f32", seed=3, bias="normal")
+    for batch in (1, 8, 32):
+        check_layer_ops(lay, wl.make_acts(batch, 3000, 2048, "f32", seed=batch))
+
+
+def test_empty_rows_and_columns():
+    # rows 0..99 and columns 0..49 and 150..199 empty
+    rng = np.random.default_rng(0)
+    pos = np.sort(rng.choice(100 * 100, 3000, replace=False))
+    row = (100 + pos // 100).astype(np.int32)
+    col = (50 + pos % 100).astype(np.int32)
+    val = wl.random_normal(3000, 2, 0)
+    lay = wl.Layer(250, 200, row, col, val, wl.random_normal(250, 2, 1), "f32")
+    for batch in (1, 6, 32):
+        check_layer_ops(lay, wl.make_acts(batch, 200, 250, "f32", seed=batch))
+
+
+def test_batch_smaller_than_max_batch_and_zero_batch():
+    lay = wl.make_layer(300, 200, nnz=5000, val_dtype="f32", seed=9, bias="normal")
+    for batch in (1, 3, 16):
+        check_layer_ops(lay, wl.make_acts(batch, 200, 300, "f32", seed=batch), max_batch=64)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(300, 200, row, col, val, bias, max_batch=64)
+    y = torch.empty((0, 300), device="cuda")
+    L.forward(torch.empty((0, 200), device="cuda"), out=y)
+    dw, db = L.grad_weight(torch.empty((0, 200), device="cuda"), torch.empty((0, 300), device="cuda"))
+    assert torch.all(dw == 0) and torch.all(db == 0)
+    L.close()
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_workload_c1():
+    c = wl.CONFIGS["c1"]
+    lay = wl.config_layer("c1")
+    check_layer_ops(lay, wl.make_acts(8, c["in_f"], c["out_f"], "f32"))
+
+
+@pytest.mark.parametrize("batch", [1, 16, 64])
+def test_workload_c2(batch):
+    lay = wl.config_layer("c2")
+    acts = wl.make_acts(batch, 4096, 4096, "bf16")
+    # one handle serves all three batches, as in single-stream inference
+    check_layer_ops(lay, acts, ops=("fwd",), max_batch=64)
+
+
+def test_workload_c3_layers():
+    for li in (0, 1):
+        lay = wl.config_layer("c3", layer_index=li)
+        check_layer_ops(lay, wl.make_acts(1024, lay.in_f, lay.out_f, "f32", seed=li))
+
+
+def test_workload_c4_ops_and_restructure():
+    lay = wl.config_layer("c4")
+    acts = wl.make_acts(32, 16384, 16384, "f32")
+    check_layer_ops(lay, acts)
+    n_prune = int(0.10 * lay.nnz)
+    restructure_and_check(lay, n_prune, seed=0, step=1, acts=acts)
+
+
+def test_workload_c5_sampled():
+    # 33.5M stored weights at batch 128: compare sampled batch rows / weights
+    lay = wl.config_layer("c5")
+    acts = wl.make_acts(128, 8192, 8192, "bf16")
+    got = run_layer_ops(lay, acts)
+    rel = REL["bf16"]
+    v64 = oracle.as_f64(lay.val, "bf16")
+    rows = np.array([0, 37, 127])
+    x64 = oracle.as_f64(acts.x, "bf16")[rows]
+    dy64 = oracle.as_f64(acts.dy, "bf16")[rows]
+    y, t = oracle.fwd(8192, 8192, lay.row, lay.col, v64, x64, oracle.as_f64(lay.bias))
+    assert_close_T(f64(got["y"])[rows], y, t, rel, "fwd c5")
+    g, t = oracle.dx(8192, 8192, lay.row, lay.col, v64, dy64)
+    assert_close_T(f64(got["dx"])[rows], g, t, rel, "dx c5")
+    ks = np.random.default_rng(0).choice(lay.nnz, 4096, replace=False)
+    d, t, _ = oracle.dw(8192, 8192, lay.row[ks], lay.col[ks], oracle.as_f64(acts.x, "bf16"),
+                        oracle.as_f64(acts.dy, "bf16"), want_db=False)
+    assert_close_T(f64(got["dw"])[ks], d, t, rel, "dw c5")
+
+
+# ---------------------------------------------------------------- restructure
+
+def restructure_and_check(lay: wl.Layer, n_prune: int, seed: int, step: int, acts=None):
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(lay.out_f, lay.in_f, row, col, val, bias, max_batch=acts.batch if acts else 8)
+    src = L.restructure(n_prune, seed, step)
+    torch.cuda.synchronize()
+    ro, co, so, _ = oracle.restructure(lay.out_f, lay.in_f, lay.row, lay.col, oracle.as_f64(lay.val, lay.val_dtype),
+                                       n_prune, seed, step)
+    assert np.array_equal(L.row.cpu().numpy(), ro), "row_out"
+    assert np.array_equal(L.col.cpu().numpy(), co), "col_out"
+    assert np.array_equal(src.cpu().numpy(), so.astype(np.int32)), "src_out"
+    vo = oracle.restructure_values(lay.val, so)
+    want_bits = vo.view(np.uint32) if lay.val_dtype == "f32" else vo.view(np.uint16)
+    assert np.array_equal(bits(L.val), want_bits), "val_out bits"
+    if acts is not None:  # the rebuilt plan serves the new pattern
+        new = wl.Layer(lay.out_f, lay.in_f, ro, co, vo, lay.bias, lay.val_dtype)
+        x = act_tensor(acts.x, acts.act_dtype)
+        dy = act_tensor(acts.dy, acts.act_dtype)
+        got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+        got["dw"], got["db"] = L.grad_weight(x, dy)
+        torch.cuda.synchronize()
+        check_layer_ops(new, acts, got=got)
+    L.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", [(8, 8, 20, 5), (1, 50, 10, 10), (40, 30, 600, 0), (40, 30, 600, 600),
+                                  (64, 64, 3000, 1000), (500, 700, 30000, 3000), (3, 3, 4, 4)])
+def test_restructure_small(dtype, case):
+    out_f, in_f, nnz, n_prune = case
+    lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=1.0, val_dtype=dtype, seed=nnz)
+    for seed, step in ((0, 0), (5, 123)):
+        restructure_and_check(lay, n_prune, seed, step, acts=wl.make_acts(4, in_f, out_f, dtype))
+
+
+def test_restructure_ties_zeros_nan():
+    lay = wl.make_layer(60, 70, nnz=2000, val_dtype="f32", seed=4)
+    v = np.round(lay.val * 50).astype(np.float32) / 50  # many exact ties
+    v[::7] = 0.0
+    v[3::11] = -0.0
+    v[5] = np.nan
+    lay.val = v
+    restructure_and_check(lay, 700, seed=9, step=2)
+
+
+def test_restructure_chain_of_steps():
+    lay = wl.make_layer(200, 300, nnz=6000, val_dtype="f32", seed=12)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(200, 300, row, col, val, bias, max_batch=8)
+    r, c, v = lay.row, lay.col, lay.val
+    for step in range(4):
+        L.restructure(600, 77, step)
+        r2, c2, s2, _ = oracle.restructure(200, 300, r, c, oracle.as_f64(v), 600, 77, step)
+        v2 = oracle.restructure_values(v, s2)
+        torch.cuda.synchronize()
+        assert np.array_equal(L.row.cpu().numpy(), r2) and np.array_equal(L.col.cpu().numpy(), c2)
+        assert np.array_equal(bits(L.val), v2.view(np.uint32))
+        r, c, v = r2, c2, v2
+    L.close()
+
+
+def test_restructure_no_space():
+    lay = wl.make_layer(4, 4, nnz=12, val_dtype="f32", seed=1)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(4, 4, row, col, val, bias, max_batch=1)
+    with pytest.raises(snack.SnackError) as e:
+        L.restructure(5, 0, 0)  # only 4 empty positions
+    assert e.value.status == 8
+    L.close()
+
+
+# ---------------------------------------------------------------- contracts
+
+def test_inputs_untouched_and_deterministic():
+    lay = wl.make_layer(777, 555, nnz=40000, zipf_s=1.1, val_dtype="f32", seed=2, bias="normal")
+    acts = wl.make_acts(32, 555, 777, "f32")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(777, 555, row, col, val, bias, max_batch=32)
+    x = act_tensor(acts.x, "f32")
+    dy = act_tensor(acts.dy, "f32")
+    keep = [t.clone() for t in (row, col, val, bias, x, dy)]
+    y1 = torch.full((32, 777), float("nan"), device="cuda")
+    dx1 = torch.full((32, 555), float("nan"), device="cuda")
+    L.forward(x, out=y1)
+    L.grad_input(dy, out=dx1)
+    dw1, db1 = L.grad_weight(x, dy)
+    y2, dx2 = L.forward(x), L.grad_input(dy)
+    dw2, db2 = L.grad_weight(x, dy)
+    torch.cuda.synchronize()
+    for a, b in zip(keep, (row, col, val, bias, x, dy)):
+        assert torch.equal(a, b)
+    assert not torch.isnan(y1).any() and not torch.isnan(dx1).any()  # every output written
+    assert torch.equal(y1, y2) and torch.equal(dx1, dx2) and torch.equal(dw1, dw2) and torch.equal(db1, db2)
+    L.close()
+
+
+def test_validation_errors():
+    row = torch.tensor([0, 2, 1], dtype=torch.int32, device="cuda")
+    col = torch.tensor([0, 0, 0], dtype=torch.int32, device="cuda")
+    val = torch.ones(3, device="cuda")
+    with pytest.raises(snack.SnackError) as e:
+        snack.SparseLinear(3, 3, row, col, val, validate=True)
+    assert e.value.status == 2
+    row = torch.tensor([0, 1, 5], dtype=torch.int32, device="cuda")
+    with pytest.raises(snack.SnackError) as e:
+        snack.SparseLinear(3, 3, row, col, val, validate=True)
+    assert e.value.status == 3
+
+
+def test_call_errors():
+    lay = wl.make_layer(30, 20, nnz=100, val_dtype="f32", seed=1)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(30, 20, row, col, val, bias, max_batch=4)
+    x = torch.zeros((8, 20), device="cuda")
+    with pytest.raises(snack.SnackError) as e:
+        L.forward(x)  # batch > max_batch
+    assert e.value.status == 1
+    y = torch.empty((2, 30), device="cuda")
+    with pytest.raises(snack.SnackError) as e:
+        snack.snack_spmm_fwd(L.handle, row, col, val, x[:2], 2, bias, y, L.ws[:256])
+    assert e.value.status == 4
+    buf = torch.zeros(4 * 30, device="cuda")
+    with pytest.raises(snack.SnackError) as e:  # y overlaps x
+        snack.snack_spmm_fwd(L.handle, row, col, val, buf[:40], 2, bias, buf[10:70], L.ws)
+    assert e.value.status == 1
+    L.close()
+
+
+def test_autograd_function():
+    lay = wl.make_layer(64, 48, nnz=700, val_dtype="f32", seed=3, bias="normal")
+    acts = wl.make_acts(8, 48, 64, "f32")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(64, 48, row, col, val.requires_grad_(True), bias, max_batch=8)
+    x = act_tensor(acts.x, "f32").requires_grad_(True)
+    g = act_tensor(acts.dy, "f32")
+    y = snack.sparse_linear(x, L)
+    y.backward(g)
+    torch.cuda.synchronize()
+    v64, x64, g64 = oracle.as_f64(lay.val), oracle.as_f64(acts.x), oracle.as_f64(acts.dy)
+    dx, t = oracle.dx(64, 48, lay.row, lay.col, v64, g64)
+    assert_close_T(f64(x.grad), dx, t, 1e-5, "autograd dx")
+    dw, t, _ = oracle.dw(64, 48, lay.row, lay.col, x64, g64)
+    assert_close_T(f64(L.val.grad), dw, t, 1e-5, "autograd dw")
+    L.close()
