@@ -1,0 +1,442 @@
+"""Benchmark of the truly sparse layer on GB300: one step = forward SpMM,
+input-gradient SpMM, weight-gradient SDDMM (+ bias gradient) and one DST
+restructure (prune 10 % smallest |w|, regrow at random empty positions) of a
+16384 x 16384 layer at 99 % sparsity with Zipf(1.2) row lengths, fp32, batch 32.
+
+Prints one JSON line.  `value` is algorithmic bytes per second over the step
+(bytes of indices + values + activations each op must move, summed over the
+four ops, divided by the device time of the step), inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, the machine's host cores) on the same
+workload and metric.  Under torchrun (N > 1) every rank runs an independent
+replica of the layer on its own GPU (no collective on the data path); rank 0
+prints the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SpMM fwd/dx/dw µs, GB/s and % of GB300 HBM roofline at 90–99% sparsity"
+WORKLOAD = ("16384x16384 sparse linear layer, 99% sparse (nnz 2,684,355, row lengths Zipf s=1.2), fp32 values "
+            "N(0,0.02), batch 32 fp32 X,dY ~ N(0,1); step = fwd + dX + dW/db + DST restructure "
+            "(prune 10% smallest |w| = 268,435, regrow as many at uniform empty positions)")
+OUT_F = IN_F = 16384
+BATCH = 32
+PRUNE_FRAC = 0.10
+N_COPIES = 8  # rotating layer copies: consecutive steps never find their inputs in L2
+
+
+def alg_bytes(nnz: int, batch: int, out_f: int, in_f: int, s_v: int = 4, s_x: int = 4) -> dict:
+    """Bytes each op must move at least (indices + values + activations once)."""
+    fwd = nnz * (8 + s_v) + batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
+    dx = nnz * (8 + s_v) + batch * out_f * s_x + batch * in_f * s_x
+    dw = nnz * (8 + 4) + batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
+    restructure = 2 * nnz * (8 + s_v) + 4 * nnz  # read old COO, write new COO + source map
+    return {"fwd": fwd, "dx": dx, "dw": dw, "restructure": restructure}
+
+
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "spmm_row_sorted_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(op: str):
+    """DRAM bytes per launch of `op` from the committed ncu summary, if the kernels are unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic_c4.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_digest()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("traffic:"):
+                try:
+                    d = json.loads(line[len("traffic:"):])
+                except ValueError:
+                    return None
+                if d.get("kernel_digest") == want and op in d.get("bytes_per_call", {}):
+                    return int(d["bytes_per_call"][op])
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_workload(seed: int):
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    lay = wl.make_layer(OUT_F, IN_F, density=0.01, val_std=0.02, val_dtype="f32", seed=seed, zipf_s=1.2)
+    acts = wl.make_acts(BATCH, IN_F, OUT_F, "f32", seed=seed)
+    return lay, acts
+
+
+def sub_layer(lay, r0: int, nrows: int):
+    """Rows [r0, r0+nrows) of the layer as a layer of their own (same columns)."""
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    lo, hi = np.searchsorted(lay.row, [r0, r0 + nrows])
+    return wl.Layer(nrows, lay.in_f, (lay.row[lo:hi] - r0).astype(np.int32), lay.col[lo:hi].copy(),
+                    lay.val[lo:hi].copy(), lay.bias[r0:r0 + nrows].copy(), lay.val_dtype)
+
+
+class OracleSampler:
+    """Times the fp64 oracle on row-block samples of the workload.
+
+    A sample is the sub-layer of `nrows` consecutive output rows (all input
+    columns, full batch); one sample step runs forward, input gradient, weight
+    gradient and a 10 % restructure of that sub-layer.  Its algorithmic bytes
+    follow the same formula as the GPU ops, so bytes/second compare directly.
+    """
+
+    def __init__(self, lay, acts):
+        import oracle
+
+        self.oracle = oracle
+        self.threads = os.cpu_count() or 1
+        oracle.set_threads(self.threads)
+        self.lay, self.acts = lay, acts
+        self.x64 = oracle.as_f64(acts.x)
+        self.dy64_full = oracle.as_f64(acts.dy)
+        self.cursor = 0
+
+    def step(self, nrows: int, step_index: int):
+        o = self.oracle
+        r0 = self.cursor
+        nrows = min(nrows, OUT_F - r0)
+        self.cursor = (r0 + nrows) % OUT_F
+        sub = sub_layer(self.lay, r0, nrows)
+        v64 = o.as_f64(sub.val)
+        dy64 = np.ascontiguousarray(self.dy64_full[:, r0:r0 + nrows])
+        n_prune = int(PRUNE_FRAC * sub.nnz)
+        t0 = time.perf_counter()
+        o.fwd(nrows, IN_F, sub.row, sub.col, v64, self.x64, o.as_f64(sub.bias))
+        o.dx(nrows, IN_F, sub.row, sub.col, v64, dy64)
+        o.dw(nrows, IN_F, sub.row, sub.col, self.x64, dy64)
+        o.restructure(nrows, IN_F, sub.row, sub.col, v64, n_prune, 0, step_index)
+        dt = time.perf_counter() - t0
+        return dt, sum(alg_bytes(sub.nnz, BATCH, nrows, IN_F).values()), nrows
+
+    def rows_for(self, seconds: float) -> int:
+        """Rows per sample so that one sample step takes about `seconds`."""
+        dt, _, n = self.step(1024, 0)
+        self.cursor = 0
+        rows = int(1024 * seconds / max(dt, 1e-6))
+        return max(16, min(OUT_F, rows))
+
+
+def time_oracle(lay, acts, seconds_total: float, steps: int, warmup: int):
+    s = OracleSampler(lay, acts)
+    rows = s.rows_for(seconds_total / max(1, steps + warmup))
+    for i in range(warmup):
+        s.step(rows, i)
+    tsum, bsum, rsum = 0.0, 0, 0
+    for i in range(steps):
+        dt, b, r = s.step(rows, warmup + i)
+        tsum += dt
+        bsum += b
+        rsum += r
+    sample = (f"{steps} sample steps of {rows} consecutive output rows x 16384 inputs each (fwd+dx+dw+restructure "
+              f"of that row block, batch 32), {rsum} rows in all, fp64 oracle on {s.threads} threads")
+    return bsum / tsum / 1e9, tsum / steps, sample, s.threads
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    lay, acts = make_workload(0)
+    value, sec, sample, threads = time_oracle(lay, acts, seconds_total=args.cpu_seconds_total, steps=args.steps,
+                                              warmup=args.warmup)
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from spmm_row_sorted_gb300 import build as snack_build
+    from spmm_row_sorted_gb300 import snack
+
+    snack_build.build()
+    snack.load()
+    lay, acts = make_workload(rank)
+    nnz = lay.nnz
+    n_prune = int(PRUNE_FRAC * nnz)
+    byts = alg_bytes(nnz, BATCH, OUT_F, IN_F)
+    step_bytes = sum(byts.values())
+
+    stream = torch.cuda.Stream(device=dev)
+    plan_b, ws_b = snack.snack_query_sizes(OUT_F, IN_F, nnz, BATCH, 0, 0)
+    copies = []
+    with torch.cuda.stream(stream):
+        row0 = torch.from_numpy(lay.row).to(dev)
+        col0 = torch.from_numpy(lay.col).to(dev)
+        val0 = torch.from_numpy(lay.val).to(dev)
+        bias = torch.from_numpy(lay.bias).to(dev)
+        x0 = torch.from_numpy(acts.x).to(dev)
+        dy0 = torch.from_numpy(acts.dy).to(dev)
+        for c in range(N_COPIES):
+            cp = {"row": [row0.clone(), torch.empty_like(row0)], "col": [col0.clone(), torch.empty_like(col0)],
+                  "val": [val0.clone(), torch.empty_like(val0)], "cur": 0, "src": torch.empty_like(row0),
+                  "x": x0.clone(), "dy": dy0.clone(), "bias": bias.clone(),
+                  "y": torch.empty((BATCH, OUT_F), device=dev), "dx": torch.empty((BATCH, IN_F), device=dev),
+                  "dw": torch.empty(nnz, device=dev), "db": torch.empty(OUT_F, device=dev),
+                  "plan": torch.empty(plan_b, dtype=torch.uint8, device=dev)}
+            copies.append(cp)
+        ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
+    stream.synchronize()
+    for cp in copies:
+        cp["h"] = snack.snack_create(OUT_F, IN_F, nnz, BATCH, 0, 0, cp["row"][0], cp["col"][0], cp["plan"], ws,
+                                     validate=True, stream=stream)
+    rws = max(snack.snack_restructure_workspace_size(copies[0]["h"], n_prune), ws_b)
+    ws = torch.empty(rws, dtype=torch.uint8, device=dev)
+    stream.synchronize()
+
+    def step(cp, i, ev=None):
+        cur = cp["cur"]
+        row, col, val = cp["row"][cur], cp["col"][cur], cp["val"][cur]
+        if ev is not None:
+            ev[0].record(stream)
+        snack.snack_spmm_fwd(cp["h"], row, col, val, cp["x"], BATCH, cp["bias"], cp["y"], ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        snack.snack_spmm_dx(cp["h"], row, col, val, cp["dy"], BATCH, cp["dx"], ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        snack.snack_sddmm_dw(cp["h"], row, col, cp["x"], cp["dy"], BATCH, cp["dw"], cp["db"], ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        nxt = 1 - cur
+        snack.snack_restructure(cp["h"], row, col, val, n_prune, 12345, i, cp["row"][nxt], cp["col"][nxt],
+                                cp["val"][nxt], cp["src"], ws, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        cp["cur"] = nxt
+
+    for i in range(args.warmup):
+        step(copies[i % N_COPIES], i)
+    stream.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(copies[i % N_COPIES], args.warmup + i, evs[i])
+        t_end.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ops = ["fwd", "dx", "dw", "restructure"]
+    op_ms = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+             for j, op in enumerate(ops)}
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    op_report = {}
+    for op in ops:
+        gbs = byts[op] / (op_ms[op] / 1e3) / 1e9
+        op_report[op] = {"us": op_ms[op] * 1e3, "alg_bytes": byts[op], "gbs": gbs, "frac": gbs / peak,
+                         "gflops": (2 * nnz * BATCH / (op_ms[op] / 1e3) / 1e9) if op != "restructure" else None}
+    dominant = max(ops, key=lambda o: op_ms[o])
+    roofline = {"bound": "hbm", "achieved": op_report[dominant]["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": op_report[dominant]["gbs"] / peak, "traffic": profiled_traffic(dominant),
+                "kernel": dominant, "peak_kind": peak_kind}
+
+    # end to end through the C ABI from pinned host buffers
+    e2e_steps = max(1, min(args.steps, 200))
+    hx = torch.from_numpy(acts.x).pin_memory()
+    hdy = torch.from_numpy(acts.dy).pin_memory()
+    hy = torch.empty((BATCH, OUT_F)).pin_memory()
+    hdx = torch.empty((BATCH, IN_F)).pin_memory()
+    hdw = torch.empty(nnz).pin_memory()
+    hdb = torch.empty(OUT_F).pin_memory()
+    h2d = hx.numel() * 4 + hdy.numel() * 4
+    d2h = (hy.numel() + hdx.numel() + hdw.numel() + hdb.numel()) * 4
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            cp = copies[i % N_COPIES]
+            cp["x"].copy_(hx, non_blocking=True)
+            cp["dy"].copy_(hdy, non_blocking=True)
+            step(cp, 10**6 + i)
+            hy.copy_(cp["y"], non_blocking=True)
+            hdx.copy_(cp["dx"], non_blocking=True)
+            hdw.copy_(cp["dw"], non_blocking=True)
+            hdb.copy_(cp["db"], non_blocking=True)
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    launches_per_step = 3 + 3 + 4 + restructure_launches()
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": f"inputs larger than L2: {N_COPIES} rotating layer copies",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "ops": op_report, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cval, _, sample, threads = time_oracle(lay, acts, seconds_total=args.cpu_seconds, steps=10, warmup=0)
+        line["cpu_baseline"] = {"value": cval, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample}
+    for cp in copies:
+        snack.snack_destroy(cp["h"])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def restructure_launches() -> int:
+    """Kernel launches of one restructure of the workload (one draw chunk)."""
+    select = 1 + 4 * 2
+    keep_scan = 3
+    draw_chunk = 1 + 3
+    sort_grown = 4 * (1 + 3 + 1)  # positions < 2^28: four 8-bit passes
+    merge = 2
+    plan = (1 + 3) + 1 + (1 + 3) + 1 + 1 + 2 * (1 + 3 + 1) + 1
+    return select + keep_scan + draw_chunk + sort_grown + merge + plan
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle time of the cpu_baseline sample")
+    ap.add_argument("--cpu-seconds-total", type=float, default=120.0,
+                    help="--impl reference: oracle time budget over all steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -8,6 +8,9 @@ from spmm_row_sorted_gb300 import workloads as wl
 
 # |gpu - oracle| <= REL * T per output, T = sum of |terms| (bias included).
 REL = {"f32": 1e-5, "bf16": 2e-3}
+# An output stored in bf16 is rounded once to nearest-even on top of that:
+# |bf16(y) - y| <= 2^-8 |y| (bf16 keeps 8 significant bits).
+BF16_STORE = 2.0 ** -8
 
 
 def act_tensor(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
@@ -36,10 +39,14 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int32).numpy().view(np.uint32)
 
 
-def assert_close_T(got: np.ndarray, ref: np.ndarray, T: np.ndarray, rel: float, what: str):
+def assert_close_T(got: np.ndarray, ref: np.ndarray, T: np.ndarray, rel: float, what: str,
+                   stored_bf16: bool = False):
+    """|got - ref| <= rel*T (+ 2^-8 |ref| when got was stored in bf16)."""
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     err = np.abs(got - ref)
     bound = rel * T
+    if stored_bf16:
+        bound = bound + BF16_STORE * np.abs(ref)
     bad = ~(err <= bound)
     both_nan = np.isnan(got) & np.isnan(ref)
     bad &= ~both_nan

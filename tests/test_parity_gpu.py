@@ -50,16 +50,17 @@ def check_layer_ops(layer: wl.Layer, acts: wl.Acts, ops=("fwd", "dx", "dw"), max
                     got=None):
     got = got or run_layer_ops(layer, acts, ops, max_batch, with_bias)
     rel = REL[layer.val_dtype]
+    bf = acts.act_dtype == "bf16"
     v64 = oracle.as_f64(layer.val, layer.val_dtype)
     x64 = oracle.as_f64(acts.x, acts.act_dtype)
     dy64 = oracle.as_f64(acts.dy, acts.act_dtype)
     b64 = oracle.as_f64(layer.bias) if with_bias else None
     if "fwd" in ops:
         y, t = oracle.fwd(layer.out_f, layer.in_f, layer.row, layer.col, v64, x64, b64)
-        assert_close_T(f64(got["y"]), y, t, rel, "fwd")
+        assert_close_T(f64(got["y"]), y, t, rel, "fwd", stored_bf16=bf)
     if "dx" in ops:
         g, t = oracle.dx(layer.out_f, layer.in_f, layer.row, layer.col, v64, dy64)
-        assert_close_T(f64(got["dx"]), g, t, rel, "dx")
+        assert_close_T(f64(got["dx"]), g, t, rel, "dx", stored_bf16=bf)
     if "dw" in ops:
         d, t, db = oracle.dw(layer.out_f, layer.in_f, layer.row, layer.col, x64, dy64)
         assert_close_T(f64(got["dw"]), d, t, REL["f32"] if layer.val_dtype == "f32" else rel, "dw")
@@ -172,9 +173,9 @@ def test_workload_c5_sampled():
     x64 = oracle.as_f64(acts.x, "bf16")[rows]
     dy64 = oracle.as_f64(acts.dy, "bf16")[rows]
     y, t = oracle.fwd(8192, 8192, lay.row, lay.col, v64, x64, oracle.as_f64(lay.bias))
-    assert_close_T(f64(got["y"])[rows], y, t, rel, "fwd c5")
+    assert_close_T(f64(got["y"])[rows], y, t, rel, "fwd c5", stored_bf16=True)
     g, t = oracle.dx(8192, 8192, lay.row, lay.col, v64, dy64)
-    assert_close_T(f64(got["dx"])[rows], g, t, rel, "dx c5")
+    assert_close_T(f64(got["dx"])[rows], g, t, rel, "dx c5", stored_bf16=True)
     ks = np.random.default_rng(0).choice(lay.nnz, 4096, replace=False)
     d, t, _ = oracle.dw(8192, 8192, lay.row[ks], lay.col[ks], oracle.as_f64(acts.x, "bf16"),
                         oracle.as_f64(acts.dy, "bf16"), want_db=False)
