@@ -70,12 +70,12 @@ struct TileGeom {
 
 inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max) {
   TileGeom t;
-  int c = 65536 / (bt_max > 0 ? bt_max : 1);
-  if (c < 256) c = 256;
+  int c = 32768 / (bt_max > 0 ? bt_max : 1);
+  if (c < 512) c = 512;
   if (c > 8192) c = 8192;
   t.cost_per_tile = c;
-  // keep the staged rows of a tile within ~32 KB of shared memory
-  int rows_target = 32768 / ((bt_max + 1) * 4);
+  // keep the staged rows of a tile within ~16 KB of shared memory
+  int rows_target = 16384 / ((bt_max + 1) * 4);
   if (rows_target < 16) rows_target = 16;
   int w = (c + rows_target - 1) / rows_target;
   if (w < 2) w = 2;
@@ -87,9 +87,12 @@ inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max) {
   return t;
 }
 
+// stored weights a tile can hold: cost C plus the part of a row end that did not fit
+inline __host__ __device__ int tile_stage_cap(const TileGeom &tg) { return tg.cost_per_tile + tg.row_weight; }
+
 inline size_t spmm_smem_bytes(const TileGeom &tg, int bt) {
   return (size_t)tg.max_rows * (bt + 1) * 4 + (size_t)kSpmmWarps * bt * 4 + (size_t)(tg.max_rows + 1) * 4 +
-         (size_t)(kSpmmWarps + 1) * 2 * 4;
+         (size_t)(kSpmmWarps + 1) * 2 * 4 + (size_t)tile_stage_cap(tg) * 8;
 }
 
 struct SpmmParams {
@@ -112,10 +115,17 @@ struct SpmmParams {
 
 // ------------------------------------------------------------------ kernels
 
+// Unroll: stored weights per slot in flight, keeping kU * V <= 32 gathered floats.
+template <int V, int G>
+struct SpmmUnroll {
+  static constexpr int kSlots = 32 / G;
+  static constexpr int value = kSlots >= 8 ? (V >= 8 ? 2 : 4) : (V >= 8 ? 4 : 8);
+};
+
 template <typename TA, typename TV, int V, int G, bool kGatherVal>
 __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
   constexpr int kSlots = 32 / G;
-  constexpr int kU = kSlots >= 8 ? 2 : 4;  // weights per slot in flight
+  constexpr int kU = SpmmUnroll<V, G>::value;
   extern __shared__ __align__(16) float smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = lane / G, g = lane % G;
@@ -124,16 +134,20 @@ __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, Batch
   const int b0 = bi * bt;
   const int max_rows = P.tg.max_rows;
   const int w = P.tg.row_weight;
+  const int cap = tile_stage_cap(P.tg);
   const int ys_ld = bt + 1;
   float *Ys = smem;
   float *wcar = Ys + (size_t)max_rows * ys_ld;
   int *rps = reinterpret_cast<int *>(wcar + kSpmmWarps * bt);
   int *wsp = rps + max_rows + 1;
+  uint32_t *s_idx = reinterpret_cast<uint32_t *>(wsp + 2 * (kSpmmWarps + 1));
+  float *s_val = reinterpret_cast<float *>(s_idx + cap);
 
   const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1];
   int i1 = P.tiles[2 * t + 2];
-  const int j1 = P.tiles[2 * t + 3];
+  int j1 = P.tiles[2 * t + 3];
   if (i1 - i0 + 1 > max_rows) i1 = i0 + max_rows - 1;  // defensive: never overrun shared memory
+  if (j1 - j0 > cap) j1 = j0 + cap;
   const int nr = i1 - i0 + 1;
 
   for (int q = tid; q <= nr; q += kSpmmThreads) {
@@ -141,6 +155,41 @@ __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, Batch
     rps[q] = P.ptr[r < P.n_rows ? r : P.n_rows];
   }
   for (int b = tid; b < bt; b += kSpmmThreads) Ys[(size_t)(nr - 1) * ys_ld + b] = 0.f;
+
+  // stage the tile's gather indices and weights (one memory round trip)
+  {
+    const TV *val = reinterpret_cast<const TV *>(P.val);
+    const uint32_t src_max = (uint32_t)(P.n_src - 1);
+    const uint32_t nnz_max = (uint32_t)(P.nnz > 0 ? P.nnz - 1 : 0);
+    const int nn = j1 - j0;
+    for (int q0 = 0; q0 < nn; q0 += 4 * kSpmmThreads) {
+      uint32_t cc[4];
+      float vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * kSpmmThreads + tid;
+        cc[u] = 0u;
+        vv[u] = 0.f;
+        if (q < nn) {
+          cc[u] = (uint32_t)ld_stream(P.idx + j0 + q);
+          if (kGatherVal) {
+            uint32_t sidx = (uint32_t)ld_stream(P.val_src + j0 + q);
+            vv[u] = to_f32(ld_keep(val + (sidx < nnz_max ? sidx : nnz_max)));
+          } else {
+            vv[u] = to_f32(ld_stream(val + j0 + q));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * kSpmmThreads + tid;
+        if (q < nn) {
+          s_idx[q] = cc[u] < src_max ? cc[u] : src_max;
+          s_val[q] = vv[u];
+        }
+      }
+    }
+  }
   __syncthreads();
 
   // warp ranges: equal cost slices of [c0, c1]
@@ -158,6 +207,8 @@ __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, Batch
     int64_t j = D - (int64_t)w * lo;
     int64_t lim = rps[lo - i0 + 1];
     if (j > lim) j = lim;
+    if (j > j1) j = j1;
+    if (j < j0) j = j0;
     if (tid == kSpmmWarps) j = j1;
     wsp[2 * tid] = lo;
     wsp[2 * tid + 1] = (int)j;
@@ -167,13 +218,10 @@ __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, Batch
   const int wi0 = wsp[2 * warp], wj0 = wsp[2 * warp + 1];
   const int wi1 = wsp[2 * warp + 2], wj1 = wsp[2 * warp + 3];
   const TA *xt = reinterpret_cast<const TA *>(P.xt) + b0 + g * V;
-  const TV *val = reinterpret_cast<const TV *>(P.val);
-  const uint32_t src_max = (uint32_t)(P.n_src - 1);
-  const uint32_t nnz_max = (uint32_t)(P.nnz > 0 ? P.nnz - 1 : 0);
 
   for (int i = wi0; i <= wi1; ++i) {
-    const int ps = max(rps[i - i0], wj0);
-    const int pe = i < wi1 ? rps[i - i0 + 1] : wj1;
+    const int ps = max(rps[i - i0], wj0) - j0;
+    const int pe = min(i < wi1 ? rps[i - i0 + 1] : wj1, j1) - j0;
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.f;
@@ -184,18 +232,8 @@ __global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, Batch
       for (int u = 0; u < kU; ++u) {
         const int k = base + u * kSlots + slot;
         const bool ok = k < pe;
-        uint32_t cc = ok ? (uint32_t)ld_stream(P.idx + k) : 0u;
-        c[u] = cc < src_max ? cc : src_max;
-        float vv = 0.f;
-        if (ok) {
-          if (kGatherVal) {
-            uint32_t s = (uint32_t)ld_stream(P.val_src + k);
-            vv = to_f32(ld_keep(val + (s < nnz_max ? s : nnz_max)));
-          } else {
-            vv = to_f32(ld_stream(val + k));
-          }
-        }
-        v[u] = vv;
+        c[u] = ok ? s_idx[k] : 0u;
+        v[u] = ok ? s_val[k] : 0.f;
       }
       float x[kU][V];
 #pragma unroll
@@ -302,31 +340,62 @@ __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__res
   out[c] = s;
 }
 
-// dw[k] = sum_b dyt[row[k]][b] * xt[col[k]][b]
+// dw[k] = sum_b dyt[row[k]][b] * xt[col[k]][b].  One CTA per chunk of at
+// most kDwChunk stored weights (fewer for wide batches, so the grid still
+// fills the GPU): indices staged in shared memory, results gathered in shared
+// memory and written back contiguously.
+constexpr int kDwChunk = 2048;
+
+template <int V, int G>
+struct DwUnroll {
+  static constexpr int kSlots = 32 / G;
+  static constexpr int value = V >= 8 ? 2 : (kSlots >= 8 && V >= 4 ? 2 : 4);
+};
+
 template <typename TA, int V, int G>
 __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__restrict__ row,
                                                const int32_t *__restrict__ col, int32_t out_f, int32_t in_f,
                                                const TA *__restrict__ xt, const TA *__restrict__ dyt, int ldx,
-                                               int n_chunks, float *__restrict__ dw) {
+                                               int n_chunks, int chunk, float *__restrict__ dw) {
   constexpr int kSlots = 32 / G;
-  constexpr int kU = kSlots >= 8 ? 2 : 4;
-  constexpr int kStep = kSlots * kU;
-  const int lane = threadIdx.x & 31;
+  constexpr int kU = DwUnroll<V, G>::value;
+  const int per_warp = (chunk + 7) / 8;
+  __shared__ uint32_t s_row[kDwChunk];
+  __shared__ uint32_t s_col[kDwChunk];
+  __shared__ float s_out[kDwChunk];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = lane / G, g = lane % G;
-  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t k0 = (int64_t)blockIdx.x * chunk;
+  const int n = (int)min((int64_t)chunk, nnz - k0);
   const uint32_t rmax = (uint32_t)(out_f - 1), cmax = (uint32_t)(in_f - 1);
+  for (int q0 = 0; q0 < n; q0 += 4 * 256) {
+    uint32_t rr[4], cc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int q = q0 + u * 256 + tid;
+      rr[u] = q < n ? (uint32_t)ld_stream(row + k0 + q) : 0u;
+      cc[u] = q < n ? (uint32_t)ld_stream(col + k0 + q) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int q = q0 + u * 256 + tid;
+      if (q < n) {
+        s_row[q] = rr[u] < rmax ? rr[u] : rmax;
+        s_col[q] = cc[u] < cmax ? cc[u] : cmax;
+      }
+    }
+  }
+  __syncthreads();
   const int bt = G * V;
-  for (int64_t base = gw * kStep; base < nnz; base += nw * kStep) {
+  const int wq0 = min(n, warp * per_warp), wq1 = min(n, wq0 + per_warp);
+  for (int base = wq0; base < wq1; base += kSlots * kU) {
     uint32_t r[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      int64_t k = base + u * kSlots + slot;
-      bool ok = k < nnz;
-      uint32_t rr = ok ? (uint32_t)ld_stream(row + k) : 0u;
-      uint32_t cc = ok ? (uint32_t)ld_stream(col + k) : 0u;
-      r[u] = rr < rmax ? rr : rmax;
-      c[u] = cc < cmax ? cc : cmax;
+      int q = base + u * kSlots + slot;
+      bool ok = q < wq1;
+      r[u] = ok ? s_row[q] : 0u;
+      c[u] = ok ? s_col[q] : 0u;
     }
     float acc[kU];
 #pragma unroll
@@ -351,11 +420,13 @@ __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__res
     if (g == 0) {
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        int64_t k = base + u * kSlots + slot;
-        if (k < nnz) dw[k] = acc[u];
+        int q = base + u * kSlots + slot;
+        if (q < wq1) s_out[q] = acc[u];
       }
     }
   }
+  __syncthreads();
+  for (int q = tid; q < n; q += 256) dw[k0 + q] = s_out[q];
 }
 
 // ------------------------------------------------------------------ host
@@ -394,15 +465,17 @@ template <typename TA, int V, int G>
 cudaError_t launch_sddmm_v(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
                            const TA *xt, const TA *dyt, const BatchGeom &bg, float *dw, int num_sms,
                            cudaStream_t s) {
-  constexpr int kSlots = 32 / G;
-  constexpr int kStep = kSlots * (kSlots >= 8 ? 2 : 4);
-  int64_t groups = (nnz + kStep - 1) / kStep;  // one warp-iteration each
-  int64_t blocks = (groups + 7) / 8;
-  int64_t cap = (int64_t)num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
+  // chunk: ~64K batch elements of work per CTA, at least two CTAs per SM
+  int64_t chunk = 65536 / (bg.ldx > 0 ? bg.ldx : 1);
+  int64_t fill = (nnz + 2 * (int64_t)num_sms - 1) / (2 * (int64_t)num_sms);
+  if (chunk > fill) chunk = fill;
+  chunk = (chunk + 63) / 64 * 64;
+  if (chunk < 64) chunk = 64;
+  if (chunk > kDwChunk) chunk = kDwChunk;
+  int64_t blocks = (nnz + chunk - 1) / chunk;
   int n_chunks = bg.ldx / bg.bt;
-  k_sddmm<TA, V, G><<<(unsigned)blocks, 256, 0, s>>>(nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks, dw);
+  k_sddmm<TA, V, G><<<(unsigned)blocks, 256, 0, s>>>(nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks,
+                                                     (int)chunk, dw);
   return cudaGetLastError();
 }
 
