@@ -114,6 +114,24 @@ snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *c
                             size_t ws_bytes, snack_stream_t stream);
 
 /*
+ * Forward without a workspace argument (the paper has no counterpart; this is
+ * a convenience of this library).  For callers that may not allocate device
+ * memory on their call path -- e.g. a plugin run from an inference engine's
+ * enqueue step, or a real-time loop whose memory is fixed at start-up -- and
+ * so cannot pass the scratch buffer snack_spmm_fwd takes.  Same arguments and
+ * result as snack_spmm_fwd; its scratch is a 32 MiB array inside the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits.  A call needing more scratch than that (large in_f * batch)
+ * returns SNACK_ERR_WORKSPACE before any launch.  The first call on a device
+ * looks up the array's device address (with that device current), so make it
+ * before any stream capture.  All calls share the array: calls that overlap on
+ * the GPU race, so order them (one stream, or events).  Allocates nothing.
+ */
+snack_status snack_spmm_fwd_noalloc(snack_handle h, const int32_t *row, const int32_t *col,
+                                    const void *val, const void *x, int32_t batch, const float *bias,
+                                    void *y, snack_stream_t stream);
+
+/*
  * Input gradient (transposed SpMM; the sparse backward pass of the abstract):
  *   dx[b, c] = sum_{k : col[k] = c} val[k] * dy[b, row[k]]
  * dy [batch, out_f], dx [batch, in_f] in act dtype; dx must not overlap dy.

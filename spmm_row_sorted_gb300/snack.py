@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "SNACK_OK", 1: "SNACK_ERR_INVALID_ARG", 2: "SNACK_ERR_UNSORTE
                 8: "SNACK_ERR_NO_SPACE"}
 SNACK_F32, SNACK_BF16 = 0, 1
 
-EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_dx", "snack_sddmm_dw",
+EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
+            "snack_sddmm_dw",
             "snack_restructure_workspace_size", "snack_restructure", "snack_destroy", "snack_status_string",
             "snack_version")
 
@@ -70,6 +71,8 @@ def load(path: Optional[str] = None):
         lib.snack_create.restype = st
         lib.snack_spmm_fwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         lib.snack_spmm_fwd.restype = st
+        lib.snack_spmm_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        lib.snack_spmm_fwd_noalloc.restype = st
         lib.snack_spmm_dx.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
         lib.snack_spmm_dx.restype = st
         lib.snack_sddmm_dw.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
@@ -141,6 +144,13 @@ def snack_spmm_fwd(h: int, row, col, val, x, batch: int, bias, y, ws, stream=Non
     _check("snack_spmm_fwd",
            load().snack_spmm_fwd(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), _ptr(x), batch, _ptr(bias),
                                  _ptr(y), _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
+
+
+def snack_spmm_fwd_noalloc(h: int, row, col, val, x, batch: int, bias, y, stream=None) -> None:
+    """Forward pass using the library's built-in scratch array (no workspace argument)."""
+    _check("snack_spmm_fwd_noalloc",
+           load().snack_spmm_fwd_noalloc(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), _ptr(x), batch,
+                                         _ptr(bias), _ptr(y), _stream(stream)))
 
 
 def snack_spmm_dx(h: int, row, col, val, dy, batch: int, dx, ws, stream=None) -> None:
