@@ -30,9 +30,12 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max);
 PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
-// Fill the plan for the pattern (row, col).  Asynchronous on s.
+// Fill the plan for the pattern (row, col).  Asynchronous on s.  rows_sorted
+// says the rows are known to be non-decreasing (a restructure's own output),
+// which allows the one-pass row offsets.
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
-                       const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s);
+                       const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
+                       bool rows_sorted);
 
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,

@@ -84,32 +84,58 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_spine(T *sums, int64_t nb
   if (threadIdx.x == 0 && total) *total = carry;
 }
 
-template <typename T, typename F, typename Out>
-__global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, int64_t n, const T *block_offs,
+// One padding element per 128 bytes keeps the blocked read (thread t reads
+// elements 8t..8t+7) free of bank conflicts.
+template <typename T>
+__device__ __forceinline__ int scan_pad(int e) {
+  return e + e / (int)(128 / sizeof(T));
+}
+
+// Payload loaded with the scanned value (before the block scan), so the
+// callback's operands do not cost a second memory round trip.
+struct NoPayload {
+  __device__ int operator()(int64_t) const { return 0; }
+};
+
+template <typename T, typename F, typename PL, typename Out>
+__global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t n, const T *block_offs,
                                                             Out out) {
-  __shared__ T tile[kScanTile];
+  constexpr int kPadded = kScanTile + kScanTile / (128 / sizeof(T));
+  __shared__ T tile[kPadded];
+  __shared__ T tile_ex[kPadded];
   const int64_t base = (int64_t)blockIdx.x * kScanTile;
+  T in[kScanItems];
+  decltype(pl(0)) pay[kScanItems];
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
-    int e = i * kScanThreads + threadIdx.x;
-    int64_t idx = base + e;
-    tile[e] = idx < n ? f(idx) : T(0);
+    int64_t idx = base + i * kScanThreads + threadIdx.x;
+    in[i] = idx < n ? f(idx) : T(0);
+    pay[i] = idx < n ? pl(idx) : decltype(pl(0))();
   }
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) tile[scan_pad<T>(i * kScanThreads + threadIdx.x)] = in[i];
   __syncthreads();
   T v[kScanItems];
   T s = 0;
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
-    v[i] = tile[threadIdx.x * kScanItems + i];
+    v[i] = tile[scan_pad<T>(threadIdx.x * kScanItems + i)];
     s += v[i];
   }
   __shared__ T tot;
   T ex = block_exclusive_scan<T>(s, &tot) + block_offs[blockIdx.x];
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
-    int64_t idx = base + threadIdx.x * kScanItems + i;
-    if (idx < n) out(idx, ex, v[i]);
+    tile_ex[scan_pad<T>(threadIdx.x * kScanItems + i)] = ex;
     ex += v[i];
+  }
+  __syncthreads();
+  // callbacks in striped order: consecutive threads touch consecutive elements
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int e = i * kScanThreads + threadIdx.x;
+    const int64_t idx = base + e;
+    if (idx < n) out(idx, tile_ex[scan_pad<T>(e)], in[i], pay[i]);
   }
 }
 
@@ -119,11 +145,11 @@ inline size_t scan_temp_bytes(int64_t n) {
   return align_up((size_t)(nb + 2) * sizeof(T), kAlign);
 }
 
-// Exclusive scan of f(0..n-1); calls out(i, exclusive_i, f(i)) for every i and
-// writes the total to *d_total (device pointer, may be null).  temp needs
-// scan_temp_bytes<T>(n).  Three launches on `stream`.
-template <typename T, typename F, typename Out>
-cudaError_t scan_apply(F f, int64_t n, Out out, T *d_total, void *temp, cudaStream_t stream) {
+// Exclusive scan of f(0..n-1); calls out(i, exclusive_i, f(i), pl(i)) for
+// every i and writes the total to *d_total (device pointer, may be null).
+// temp needs scan_temp_bytes<T>(n).  Three launches on `stream`.
+template <typename T, typename F, typename PL, typename Out>
+cudaError_t scan_apply_pl(F f, PL pl, int64_t n, Out out, T *d_total, void *temp, cudaStream_t stream) {
   int64_t nb = ceil_div(n > 0 ? n : 1, kScanTile);
   T *sums = reinterpret_cast<T *>(temp);
   if (n <= 0) {
@@ -132,45 +158,95 @@ cudaError_t scan_apply(F f, int64_t n, Out out, T *d_total, void *temp, cudaStre
   }
   k_scan_reduce<T, F><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, n, sums);
   k_scan_spine<T><<<1, kScanThreads, 0, stream>>>(sums, nb, d_total);
-  k_scan_down<T, F, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, n, sums, out);
+  k_scan_down<T, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out);
   return cudaGetLastError();
+}
+
+// Without payload: out(i, exclusive_i, f(i), 0).
+template <typename T, typename F, typename Out>
+cudaError_t scan_apply(F f, int64_t n, Out out, T *d_total, void *temp, cudaStream_t stream) {
+  return scan_apply_pl<T>(f, NoPayload{}, n, out, d_total, temp, stream);
 }
 
 // ------------------------------------------------------------- radix sort
 
 constexpr int kRadixThreads = 256;
-constexpr int kRadixItems = 16;  // per lane, striped within the warp
+constexpr int kRadixItems = 8;  // per lane, striped within the warp
 constexpr int kRadixWarps = kRadixThreads / 32;
-constexpr int kRadixTile = kRadixThreads * kRadixItems;  // 4096
+constexpr int kRadixTile = kRadixThreads * kRadixItems;  // 2048
 constexpr int kRadixBins = 256;
 
+// Sources and sinks of a radix pass: the first pass may generate its keys
+// (e.g. from a column array) and the last pass may write its own outputs.
 template <typename K>
-__global__ void __launch_bounds__(kRadixThreads) k_radix_hist(const K *keys, int64_t n, int shift,
-                                                              uint32_t *hist, int64_t nb) {
-  __shared__ uint32_t h[kRadixBins];
-  for (int i = threadIdx.x; i < kRadixBins; i += kRadixThreads) h[i] = 0;
-  __syncthreads();
+struct ArraySrc {
+  const K *k;
+  const uint32_t *v;
+  __device__ K key(int64_t i) const { return k[i]; }
+  __device__ uint32_t val(int64_t i) const { return v ? v[i] : 0u; }
+};
+
+// A sink may gather something per element first (load), all loads of a
+// thread in flight together, then write (put).
+template <typename K>
+struct ArrayDst {
+  K *k;
+  uint32_t *v;
+  __device__ int load(uint32_t) const { return 0; }
+  __device__ void put(uint32_t pos, K key, uint32_t val, int) const {
+    k[pos] = key;
+    if (v) v[pos] = val;
+  }
+};
+
+template <typename K, typename Src>
+__global__ void __launch_bounds__(kRadixThreads) k_radix_hist(Src src, int64_t n, int shift, uint32_t *hist,
+                                                              int64_t nb) {
+  __shared__ uint32_t h[kRadixWarps][kRadixBins];  // one histogram per warp: less atomic contention
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kRadixWarps * kRadixBins; i += kRadixThreads) (&h[0][0])[i] = 0;
   const int64_t base = (int64_t)blockIdx.x * kRadixTile;
-#pragma unroll 4
-  for (int i = 0; i < kRadixItems; ++i) {
+  K kk[kRadixItems];
+#pragma unroll
+  for (int i = 0; i < kRadixItems; ++i) {  // all loads in flight before any use
     int64_t idx = base + (int64_t)i * kRadixThreads + threadIdx.x;
-    if (idx < n) atomicAdd(&h[(uint32_t)(keys[idx] >> shift) & 0xFF], 1u);
+    kk[i] = idx < n ? src.key(idx) : K(0);
   }
   __syncthreads();
-  for (int d = threadIdx.x; d < kRadixBins; d += kRadixThreads) hist[(int64_t)d * nb + blockIdx.x] = h[d];
+#pragma unroll
+  for (int i = 0; i < kRadixItems; ++i) {
+    int64_t idx = base + (int64_t)i * kRadixThreads + threadIdx.x;
+    if (idx < n) atomicAdd(&h[warp][(uint32_t)(kk[i] >> shift) & 0xFF], 1u);
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < kRadixBins; d += kRadixThreads) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kRadixWarps; ++w) c += h[w][d];
+    hist[(int64_t)d * nb + blockIdx.x] = c;
+  }
 }
 
 // Stable scatter of one tile.  Warp w owns tile elements [w*512, w*512+512),
 // striped: item i of lane l is element w*512 + i*32 + l, so visiting items in
-// order and lanes in order visits elements in index order.
-template <typename K, bool kHasVal>
-__global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const K *kin, const uint32_t *vin,
-                                                                 K *kout, uint32_t *vout, int64_t n,
-                                                                 int shift, const uint32_t *offs,
-                                                                 int64_t nb) {
+// order and lanes in order visits elements in index order.  Each element gets
+// its rank inside the tile's digit-grouped order, the tile is rearranged in
+// shared memory, and each digit's run is written to its global slots by
+// consecutive threads (coalesced).
+template <typename K, typename Src, typename Dst>
+__global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(Src src, Dst dst, int64_t n, int shift,
+                                                                 const uint32_t *offs, int64_t nb) {
   __shared__ uint32_t cnt[kRadixWarps][kRadixBins];
+  __shared__ uint32_t dig_start[kRadixBins];
+  __shared__ uint32_t glob[kRadixBins];
+  __shared__ uint32_t tile_total;
+  extern __shared__ __align__(16) unsigned char rs_smem[];
+  K *s_key = reinterpret_cast<K *>(rs_smem);
+  uint32_t *s_val = reinterpret_cast<uint32_t *>(s_key + kRadixTile);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kRadixWarps * kRadixBins; i += kRadixThreads) (&cnt[0][0])[i] = 0;
+  for (int d = threadIdx.x; d < kRadixBins; d += kRadixThreads)
+    glob[d] = offs[(int64_t)d * nb + blockIdx.x];
   __syncthreads();
   const int64_t base = (int64_t)blockIdx.x * kRadixTile + (int64_t)warp * (kRadixItems * 32);
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -182,9 +258,13 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const K *kin, c
   for (int i = 0; i < kRadixItems; ++i) {
     int64_t idx = base + i * 32 + lane;
     bool ok = idx < n;
-    key[i] = ok ? kin[idx] : K(0);
-    if (kHasVal) val[i] = ok ? vin[idx] : 0u;
-    digit[i] = ok ? (int)((uint32_t)(key[i] >> shift) & 0xFF) : kRadixBins;  // sentinel bin
+    key[i] = ok ? src.key(idx) : K(0);
+    val[i] = ok ? src.val(idx) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < kRadixItems; ++i) {
+    int64_t idx = base + i * 32 + lane;
+    digit[i] = idx < n ? (int)((uint32_t)(key[i] >> shift) & 0xFF) : kRadixBins;  // sentinel bin
   }
 #pragma unroll
   for (int i = 0; i < kRadixItems; ++i) {
@@ -198,24 +278,52 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const K *kin, c
     __syncwarp();
   }
   __syncthreads();
-  // exclusive scan across warps, per digit
-  for (int d = threadIdx.x; d < kRadixBins; d += kRadixThreads) {
-    uint32_t run = 0;
+  // per digit: exclusive offsets across warps, and the digit's total in the tile
+  uint32_t tot = 0;
+  {
+    const int d = threadIdx.x;  // kRadixThreads == kRadixBins
 #pragma unroll
     for (int w = 0; w < kRadixWarps; ++w) {
       uint32_t c = cnt[w][d];
-      cnt[w][d] = run;
-      run += c;
+      cnt[w][d] = tot;
+      tot += c;
     }
+  }
+  {
+    __shared__ uint32_t scan_total;
+    uint32_t ex = block_exclusive_scan<uint32_t>(tot, &scan_total);
+    dig_start[threadIdx.x] = ex;
+    if (threadIdx.x == 0) tile_total = scan_total;
   }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < kRadixItems; ++i) {
     if (digit[i] < kRadixBins) {
-      uint32_t pos = offs[(int64_t)digit[i] * nb + blockIdx.x] + cnt[warp][digit[i]] + rank[i];
-      kout[pos] = key[i];
-      if (kHasVal) vout[pos] = val[i];
+      const uint32_t lpos = dig_start[digit[i]] + cnt[warp][digit[i]] + rank[i];
+      s_key[lpos] = key[i];
+      s_val[lpos] = val[i];
     }
+  }
+  __syncthreads();
+  const int m = (int)tile_total;
+  K ok[kRadixItems];
+  uint32_t ov[kRadixItems], opos[kRadixItems];
+  int oaux[kRadixItems];
+#pragma unroll
+  for (int i = 0; i < kRadixItems; ++i) {
+    const int e = i * kRadixThreads + threadIdx.x;
+    if (e < m) {
+      ok[i] = s_key[e];
+      ov[i] = s_val[e];
+      const uint32_t d = (uint32_t)(ok[i] >> shift) & 0xFF;
+      opos[i] = glob[d] + (uint32_t)e - dig_start[d];
+      oaux[i] = dst.load(ov[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kRadixItems; ++i) {
+    const int e = i * kRadixThreads + threadIdx.x;
+    if (e < m) dst.put(opos[i], ok[i], ov[i], oaux[i]);
   }
 }
 
@@ -225,7 +333,7 @@ struct HistRead {
 };
 struct WriteExcl32 {
   uint32_t *o;
-  __device__ void operator()(int64_t i, uint32_t ex, uint32_t) const { o[i] = ex; }
+  __device__ void operator()(int64_t i, uint32_t ex, uint32_t, int) const { o[i] = ex; }
 };
 
 inline size_t radix_temp_bytes(int64_t n) {
@@ -234,9 +342,57 @@ inline size_t radix_temp_bytes(int64_t n) {
   return 2 * h + scan_temp_bytes<uint32_t>(nb * kRadixBins);
 }
 
-// Stable sort by the low `bits` bits of the keys (bits <= 8*sizeof(K)).
-// Ping-pongs between (k0, v0) and (k1, v1); *in_second is set when the
-// result ends in (k1, v1).  v0/v1 may be null (keys only).
+template <typename K, typename Src, typename Dst>
+cudaError_t radix_pass(Src src, Dst dst, int64_t n, int shift, uint32_t *hist, uint32_t *offs, void *stemp,
+                       cudaStream_t stream) {
+  const int64_t nb = ceil_div(n, kRadixTile);
+  k_radix_hist<K, Src><<<(unsigned)nb, kRadixThreads, 0, stream>>>(src, n, shift, hist, nb);
+  cudaError_t e = scan_apply<uint32_t>(HistRead{hist}, nb * kRadixBins, WriteExcl32{offs}, (uint32_t *)nullptr,
+                                       stemp, stream);
+  if (e != cudaSuccess) return e;
+  const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
+  e = cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  k_radix_scatter<K, Src, Dst><<<(unsigned)nb, kRadixThreads, dyn, stream>>>(src, dst, n, shift, offs, nb);
+  return cudaGetLastError();
+}
+
+// Stable sort by the low `bits` bits of the keys, 8 bits per pass (at least
+// one pass).  The first pass reads `first`, the last writes `last`; passes in
+// between ping-pong between (k0, v0) and (k1, v1).
+template <typename K, typename Src0, typename DstLast>
+cudaError_t radix_sort_custom(Src0 first, DstLast last, int64_t n, int bits, K *k0, uint32_t *v0, K *k1,
+                              uint32_t *v1, void *temp, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t nb = ceil_div(n, kRadixTile);
+  uint8_t *t = reinterpret_cast<uint8_t *>(temp);
+  size_t hbytes = align_up((size_t)nb * kRadixBins * sizeof(uint32_t), kAlign);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(t);
+  uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
+  void *stemp = t + 2 * hbytes;
+  const int passes = bits <= 8 ? 1 : (bits + 7) / 8;
+  cudaError_t e = cudaSuccess;
+  if (passes == 1) return radix_pass<K>(first, last, n, 0, hist, offs, stemp, stream);
+  e = radix_pass<K>(first, ArrayDst<K>{k0, v0}, n, 0, hist, offs, stemp, stream);
+  if (e != cudaSuccess) return e;
+  K *ka = k0, *kb = k1;
+  uint32_t *va = v0, *vb = v1;
+  for (int p = 1; p < passes - 1; ++p) {
+    e = radix_pass<K>(ArraySrc<K>{ka, va}, ArrayDst<K>{kb, vb}, n, 8 * p, hist, offs, stemp, stream);
+    if (e != cudaSuccess) return e;
+    K *tk = ka;
+    ka = kb;
+    kb = tk;
+    uint32_t *tv = va;
+    va = vb;
+    vb = tv;
+  }
+  return radix_pass<K>(ArraySrc<K>{ka, va}, last, n, 8 * (passes - 1), hist, offs, stemp, stream);
+}
+
+// Stable sort by the low `bits` bits of the keys, ping-ponging between
+// (k0, v0) and (k1, v1) (v0/v1 may be null); *in_second is set when the
+// result ends in (k1, v1).
 template <typename K>
 cudaError_t radix_sort(K *k0, uint32_t *v0, K *k1, uint32_t *v1, int64_t n, int bits, void *temp,
                        cudaStream_t stream, bool *in_second) {
@@ -250,18 +406,9 @@ cudaError_t radix_sort(K *k0, uint32_t *v0, K *k1, uint32_t *v1, int64_t n, int 
   void *stemp = t + 2 * hbytes;
   K *ka = k0, *kb = k1;
   uint32_t *va = v0, *vb = v1;
-  const bool has_val = v0 != nullptr;
   for (int shift = 0; shift < bits; shift += 8) {
-    k_radix_hist<K><<<(unsigned)nb, kRadixThreads, 0, stream>>>(ka, n, shift, hist, nb);
-    cudaError_t e = scan_apply<uint32_t>(HistRead{hist}, nb * kRadixBins, WriteExcl32{offs},
-                                         (uint32_t *)nullptr, stemp, stream);
+    cudaError_t e = radix_pass<K>(ArraySrc<K>{ka, va}, ArrayDst<K>{kb, vb}, n, shift, hist, offs, stemp, stream);
     if (e != cudaSuccess) return e;
-    if (has_val)
-      k_radix_scatter<K, true><<<(unsigned)nb, kRadixThreads, 0, stream>>>(ka, va, kb, vb, n, shift,
-                                                                          offs, nb);
-    else
-      k_radix_scatter<K, false><<<(unsigned)nb, kRadixThreads, 0, stream>>>(ka, nullptr, kb, nullptr,
-                                                                           n, shift, offs, nb);
     K *tk = ka;
     ka = kb;
     kb = tk;
@@ -270,7 +417,7 @@ cudaError_t radix_sort(K *k0, uint32_t *v0, K *k1, uint32_t *v1, int64_t n, int 
     vb = tv;
     *in_second = !*in_second;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace snack

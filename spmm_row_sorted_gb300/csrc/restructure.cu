@@ -32,8 +32,9 @@ constexpr int kMergeItems = 4;
 constexpr int kMergeTile = kMergeThreads * kMergeItems;
 
 struct SelState {
-  uint32_t prefix, mask, remaining, total;
-  uint32_t hist[256];
+  uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
+  uint32_t overflow, pad[3];                   // overflow: a draw found the position table full
+  uint32_t hist[4][256];                       // one histogram per 8-bit digit, high digit first
 };
 
 __device__ __forceinline__ uint32_t canon_mag(uint32_t m) { return m > 0x7F800000u ? 0x7F800001u : m; }
@@ -50,47 +51,107 @@ __device__ __forceinline__ uint32_t mag_key<bf16>(const bf16 *val, int64_t k) {
   return canon_mag((b & 0x7FFFu) << 16);
 }
 
-template <typename TV>
-__global__ void k_sel_hist(const TV *__restrict__ val, int64_t nnz, SelState *st, int shift) {
-  __shared__ uint32_t h[256];
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
-  __syncthreads();
-  const uint32_t prefix = st->prefix, mask = st->mask;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < nnz; k += stride) {
-    uint32_t key = mag_key<TV>(val, k);
-    if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 0xFFu], 1u);
+// One warp: the digit d of `hist` where the running count first reaches rem,
+// and the count of smaller digits.
+__device__ void warp_pick(const uint32_t *hist, uint32_t rem, uint32_t *digit, uint32_t *before) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = hist[lane * 8 + i];
+    sum += h[i];
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    if (h[i]) atomicAdd(&st->hist[i], h[i]);
-}
-
-__global__ void k_sel_pick(SelState *st, int shift) {
-  if (threadIdx.x == 0) {
-    uint32_t rem = st->remaining, cum = 0;
-    for (int d = 0; d < 256; ++d) {
-      uint32_t c = st->hist[d];
-      if (cum + c >= rem) {
-        st->prefix |= (uint32_t)d << shift;
-        st->mask |= 0xFFu << shift;
-        st->remaining = rem - cum;
+  uint32_t inc = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t u = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += u;
+  }
+  const uint32_t ex = inc - sum;
+  const unsigned hit = __ballot_sync(0xffffffffu, inc >= rem && ex < rem);
+  const int src = hit ? __ffs(hit) - 1 : 31;
+  uint32_t dg = 255, bf = 0;
+  if (lane == src) {
+    uint32_t c = ex;
+    dg = lane * 8 + 7;
+    bf = c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c + h[i] >= rem) {
+        dg = lane * 8 + i;
+        bf = c;
         break;
       }
-      cum += c;
+      c += h[i];
+    }
+  }
+  *digit = __shfl_sync(0xffffffffu, dg, src);
+  *before = __shfl_sync(0xffffffffu, bf, src);
+}
+
+// prefix / mask / remaining after `passes` digits (one warp)
+__device__ void warp_replay(const SelState *st, int passes, uint32_t *prefix, uint32_t *mask, uint32_t *rem) {
+  uint32_t p = 0, m = 0, r = st->n_prune;
+  for (int q = 0; q < passes; ++q) {
+    uint32_t d, bf;
+    warp_pick(st->hist[q], r, &d, &bf);
+    const int shift = 24 - 8 * q;
+    p |= d << shift;
+    m |= 0xFFu << shift;
+    r -= bf;
+  }
+  *prefix = p;
+  *mask = m;
+  *rem = r;
+}
+
+template <typename TV>
+__global__ void __launch_bounds__(256) k_sel_hist(const TV *__restrict__ val, int64_t nnz, SelState *st, int pass) {
+  __shared__ uint32_t h[256];
+  __shared__ uint32_t s_prefix, s_mask;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  if (threadIdx.x < 32) {
+    uint32_t p, m, r;
+    warp_replay(st, pass, &p, &m, &r);
+    if (threadIdx.x == 0) {
+      s_prefix = p;
+      s_mask = m;
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) st->hist[i] = 0;
+  const uint32_t prefix = s_prefix, mask = s_mask;
+  const int shift = 24 - 8 * pass;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k0 < nnz; k0 += 4 * stride) {
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) key[u] = k0 + u * stride < nnz ? mag_key<TV>(val, k0 + u * stride) : 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (k0 + u * stride < nnz && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> shift) & 0xFFu], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (h[i]) atomicAdd(&st->hist[pass][i], h[i]);
+}
+
+__global__ void k_sel_final(SelState *st) {
+  uint32_t p, m, r;
+  warp_replay(st, 4, &p, &m, &r);
+  if (threadIdx.x == 0) {
+    st->prefix = p;
+    st->remaining = r;
+  }
 }
 
 __global__ void k_sel_init(SelState *st, uint32_t n_prune) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) st->hist[i] = 0;
+  for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&st->hist[0][0])[i] = 0;
   if (threadIdx.x == 0) {
     st->prefix = 0;
-    st->mask = 0;
-    st->remaining = n_prune;
+    st->remaining = 0;
+    st->n_prune = n_prune;
     st->total = 0;
+    st->overflow = 0;
   }
 }
 
@@ -104,19 +165,26 @@ struct KeepVal {
   }
 };
 
-struct KeepOut {
+// linear position row*in_f + col of stored weight k, loaded with the scan value
+struct PosPayload {
   const int32_t *row, *col;
   int32_t in_f;
+  __device__ uint64_t operator()(int64_t k) const {
+    return (uint64_t)(uint32_t)row[k] * (uint64_t)in_f + (uint32_t)col[k];
+  }
+};
+
+struct KeepOut {
   const SelState *st;
   uint64_t *surv_pos;
   uint32_t *surv_src;
-  __device__ void operator()(int64_t k, uint64_t ex, uint64_t v) const {
+  __device__ void operator()(int64_t k, uint64_t ex, uint64_t v, uint64_t pos) const {
     const uint32_t m = st->remaining;
     const uint32_t gt = (uint32_t)ex, eq = (uint32_t)(ex >> 32);
     const bool keep = (v & 1ull) || ((v >> 32) && eq >= m);
     if (keep) {
       uint32_t s = gt + (eq > m ? eq - m : 0u);
-      surv_pos[s] = (uint64_t)(uint32_t)row[k] * (uint64_t)in_f + (uint32_t)col[k];
+      surv_pos[s] = pos;
       surv_src[s] = (uint32_t)k;
     }
   }
@@ -175,61 +243,81 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
   }
 }
 
-struct AcceptVal {
-  const uint64_t *cand, *hkeys;
-  const uint32_t *hmin;
-  uint64_t hmask, i0;
-  __device__ uint32_t operator()(int64_t idx) const {
-    uint64_t p = cand[idx];
-    if (p == kEmpty) return 0u;
-    return hash_min(hkeys, hmin, hmask, p) == (uint32_t)(i0 + (uint64_t)idx) ? 1u : 0u;
+// flag[idx] = 1 when draw i0+idx found an empty position and is the first
+// draw of that position (its index is the minimum recorded for it)
+__global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0,
+                               const uint64_t *__restrict__ hkeys, const uint32_t *__restrict__ hmin, uint64_t hmask,
+                               uint32_t *__restrict__ flags) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
+    const uint64_t p = cand[idx];
+    flags[idx] = (p != kEmpty && hash_min(hkeys, hmin, hmask, p) == (uint32_t)(i0 + (uint64_t)idx)) ? 1u : 0u;
   }
+}
+
+struct FlagRead {
+  const uint32_t *f;
+  __device__ uint32_t operator()(int64_t i) const { return f[i]; }
+};
+
+struct CandPayload {
+  const uint64_t *cand;
+  __device__ uint64_t operator()(int64_t idx) const { return cand[idx]; }
 };
 
 struct AcceptOut {
-  const uint64_t *cand;
   uint64_t *grown;
   int64_t before, n_prune;
-  __device__ void operator()(int64_t idx, uint32_t ex, uint32_t v) const {
+  __device__ void operator()(int64_t idx, uint32_t ex, uint32_t v, uint64_t p) const {
     if (v) {
       int64_t q = before + (int64_t)ex;
-      if (q < n_prune) grown[q] = cand[idx];
+      if (q < n_prune) grown[q] = p;
     }
   }
 };
 
-__global__ void k_merge_part(const uint64_t *__restrict__ A, int64_t na, const uint64_t *__restrict__ B, int64_t nb,
-                             int64_t n_tiles, int64_t *__restrict__ part) {
-  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t > n_tiles) return;
-  int64_t d = t * kMergeTile;
-  if (d > na + nb) d = na + nb;
-  int64_t lo = d > nb ? d - nb : 0, hi = d < na ? d : na;
-  while (lo < hi) {
-    int64_t mid = (lo + hi) >> 1;
-    if (A[mid] <= B[d - 1 - mid])
-      lo = mid + 1;
-    else
-      hi = mid;
+// Number of A elements among the first d outputs of the merge (A first on
+// ties), by one warp: the predicate A[a] <= B[d-1-a] holds on a prefix of
+// candidate a, so each round probes 32 points and keeps the crossing.
+__device__ int64_t merge_split_warp(const uint64_t *A, int64_t na, const uint64_t *B, int64_t nb, int64_t d) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = d > nb ? d - nb : 0, hi = d < na ? d : na;  // answer in [lo, hi]
+  while (hi - lo > 32) {
+    const int64_t span = hi - lo;
+    const int64_t p = lo + span * (lane + 1) / 33;  // lo < p < hi
+    const bool ok = A[p] <= B[d - 1 - p];
+    const int cnt = __popc(__ballot_sync(0xffffffffu, ok));
+    const int64_t new_lo = cnt > 0 ? lo + span * cnt / 33 + 1 : lo;
+    const int64_t new_hi = cnt < 32 ? lo + span * (cnt + 1) / 33 : hi;
+    lo = new_lo;
+    hi = new_hi;
   }
-  part[t] = lo;
+  const int64_t a = lo + lane;
+  const bool ok = a < hi && A[a] <= B[d - 1 - a];
+  return lo + __popc(__ballot_sync(0xffffffffu, ok));
 }
 
 template <typename TV>
 __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
-            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, const TV *__restrict__ val,
+            int64_t nb, int32_t in_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
             int32_t *__restrict__ src_out) {
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];
   __shared__ int32_t oS[kMergeTile];
+  __shared__ int64_t s_split[2];
   const int64_t t = blockIdx.x;
   const int64_t n = na + nb;
   const int64_t d0 = t * kMergeTile;
   const int64_t d1 = d0 + kMergeTile < n ? d0 + kMergeTile : n;
-  const int64_t a0 = part[t], a1 = part[t + 1];
+  if (threadIdx.x < 64) {
+    const int64_t sp = merge_split_warp(A, na, B, nb, threadIdx.x < 32 ? d0 : d1);
+    if ((threadIdx.x & 31) == 0) s_split[threadIdx.x >> 5] = sp;
+  }
+  __syncthreads();
+  const int64_t a0 = s_split[0], a1 = s_split[1];
   const int64_t b0 = d0 - a0, b1 = d1 - a1;
   const int la = (int)(a1 - a0), lb = (int)(b1 - b0);
   for (int q = threadIdx.x; q < la; q += kMergeThreads) {
@@ -309,7 +397,7 @@ double expected_draws(double n_pos, double empty, double need) {
 }
 
 struct RWs {
-  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, hkeys, hmin, radix, part, total;
+  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, total;
   int64_t d_max, cap, n_merge_tiles;
 };
 
@@ -341,14 +429,14 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(8 * np, kAlign);
   w.cand = o;
   o += align_up(8 * (size_t)(w.d_max > 0 ? w.d_max : 1), kAlign);
+  w.flags = o;
+  o += align_up(4 * (size_t)(w.d_max > 0 ? w.d_max : 1), kAlign);
   w.hkeys = o;
   o += align_up(8 * (size_t)cap, kAlign);
   w.hmin = o;
   o += align_up(4 * (size_t)cap, kAlign);
   w.radix = o;
   o += radix_temp_bytes((int64_t)np);
-  w.part = o;
-  o += align_up(8 * (size_t)(w.n_merge_tiles + 1), kAlign);
   w.total = o;
   return w;
 }
@@ -367,7 +455,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   uint64_t *cand = reinterpret_cast<uint64_t *>(b + W.cand);
   uint64_t *hkeys = reinterpret_cast<uint64_t *>(b + W.hkeys);
   uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
-  int64_t *part = reinterpret_cast<int64_t *>(b + W.part);
+  uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
   const TV *val = reinterpret_cast<const TV *>(a.val);
   const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
   const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
@@ -378,18 +466,17 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     if (e != cudaSuccess) return SNACK_ERR_CUDA; \
   } while (0)
 
-  // 1. prune threshold
+  // 1. prune threshold: four 8-bit digit passes, high to low
   k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
   if (n_prune > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      k_sel_hist<TV><<<grid_for(nnz, 256, 1184), 256, 0, s>>>(val, nnz, st, shift);
-      k_sel_pick<<<1, 256, 0, s>>>(st, shift);
-    }
+    for (int pass = 0; pass < 4; ++pass)
+      k_sel_hist<TV><<<grid_for(nnz, 256, 1184), 256, 0, s>>>(val, nnz, st, pass);
+    k_sel_final<<<1, 32, 0, s>>>(st);
   }
   SNACK_TRY(cudaGetLastError());
   // 2. survivors
-  SNACK_TRY(scan_apply<uint64_t>(KeepVal<TV>{val, st}, nnz, KeepOut{a.row, a.col, a.in_f, st, surv_pos, surv_src},
-                                 (uint64_t *)nullptr, stemp, s));
+  SNACK_TRY(scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, a.in_f}, nnz,
+                                    KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s));
   // 3. regrow
   if (n_prune > 0) {
     SNACK_TRY(cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s));
@@ -398,8 +485,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     const double empty = (double)n_pos - (double)nnz;
     int64_t done = 0, acc = 0;
     uint32_t *d_total = &st->total;
-    uint32_t *d_overflow = &st->hist[0];  // hist is idle after the selection
-    SNACK_TRY(cudaMemsetAsync(d_overflow, 0, sizeof(uint32_t), s));
+    uint32_t *d_overflow = &st->overflow;
     while (acc < n_prune) {
       if (done >= W.d_max) return SNACK_ERR_NO_SPACE;
       double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
@@ -408,8 +494,10 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       k_draw<<<grid_for(m, 256), 256, 0, s>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
                                               hkeys, hmin, (uint64_t)(W.cap - 1), d_overflow);
       SNACK_TRY(cudaGetLastError());
-      SNACK_TRY(scan_apply<uint32_t>(AcceptVal{cand, hkeys, hmin, (uint64_t)(W.cap - 1), (uint64_t)done}, m,
-                                     AcceptOut{cand, grown_a, acc, n_prune}, d_total, stemp, s));
+      k_accept_flags<<<grid_for(m, 256), 256, 0, s>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
+                                                      flags);
+      SNACK_TRY(scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
+                                        d_total, stemp, s));
       uint32_t h_total = 0, h_over = 0;
       SNACK_TRY(cudaMemcpyAsync(&h_total, d_total, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
       SNACK_TRY(cudaMemcpyAsync(&h_over, d_overflow, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
@@ -428,10 +516,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     grown = second ? grown_b : grown_a;
   }
   if (nnz > 0) {
-    k_merge_part<<<grid_for(W.n_merge_tiles + 1, 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
-                                                                     W.n_merge_tiles, part);
     k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
-        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, val, a.row_out, a.col_out,
+        surv_pos, surv_src, n_surv, grown, n_prune, a.in_f, val, a.row_out, a.col_out,
         reinterpret_cast<TV *>(a.val_out), a.src_out);
   }
   SNACK_TRY(cudaGetLastError());

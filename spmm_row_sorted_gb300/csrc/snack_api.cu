@@ -235,7 +235,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
     if (flag & 1u) return SNACK_ERR_OUT_OF_RANGE;
     if (flag & 2u) return SNACK_ERR_UNSORTED;
   }
-  SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s));
+  SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s, false));
   snack_layer *h = new (std::nothrow) snack_layer;
   if (!h) return SNACK_ERR_INVALID_ARG;
   h->device = dev;
@@ -354,7 +354,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.src_out = src_out;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
-  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s));
+  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, true));
   return SNACK_OK;
 }
 
