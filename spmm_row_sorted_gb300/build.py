@@ -57,20 +57,27 @@ def _digest(extra_flags: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library if needed; return its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile and link the library if needed; return its path.
+
+    extra_flags (e.g. -D tuning macros) and out_dir build a separate copy
+    without touching the default library."""
     extra_flags = list(extra_flags or [])
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = out_dir or BUILD
+    lib_path = os.path.join(build_dir, "libsnack.so")
+    stamp_path = os.path.join(build_dir, "libsnack.stamp")
+    os.makedirs(build_dir, exist_ok=True)
     digest = _digest(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
-        with open(STAMP) as f:
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_path):
+        with open(stamp_path) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib_path
     nv = nvcc()
     objs = []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + f".{os.getpid()}.o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + f".{os.getpid()}.o")
         cmd = [nv, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -84,7 +91,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
     cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
@@ -96,10 +103,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             pass
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib_path)
+    with open(stamp_path, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -29,6 +29,16 @@ namespace snack {
 constexpr int kSpmmThreads = 256;
 constexpr int kSpmmWarps = kSpmmThreads / 32;
 
+// Resident CTAs per SM the tile kernel is compiled for (caps registers), and
+// the largest unroll depth (stored weights per slot in flight).  Defaults are
+// the fastest measured on GB300 for the 16384^2 / batch-32 layer.
+#ifndef SNACK_SPMM_MIN_CTAS
+#define SNACK_SPMM_MIN_CTAS 6
+#endif
+#ifndef SNACK_SPMM_UNROLL
+#define SNACK_SPMM_UNROLL 4
+#endif
+
 // Batch geometry of one call.
 struct BatchGeom {
   int V;         // activation elements per lane slice (1, 4 or 8)
@@ -119,11 +129,13 @@ struct SpmmParams {
 template <int V, int G>
 struct SpmmUnroll {
   static constexpr int kSlots = 32 / G;
-  static constexpr int value = kSlots >= 8 ? (V >= 8 ? 2 : 4) : (V >= 8 ? 4 : 8);
+  static constexpr int kMax = SNACK_SPMM_UNROLL;
+  static constexpr int base = kSlots >= 8 ? (V >= 8 ? 2 : 4) : (V >= 8 ? 4 : 8);
+  static constexpr int value = base < kMax ? base : kMax;
 };
 
 template <typename TA, typename TV, int V, int G, bool kGatherVal>
-__global__ void __launch_bounds__(kSpmmThreads) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
+__global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
   constexpr int kSlots = 32 / G;
   constexpr int kU = SpmmUnroll<V, G>::value;
   extern __shared__ __align__(16) float smem[];
