@@ -227,9 +227,10 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_hist(Src src, int64_t n
   }
 }
 
-// Stable scatter of one tile.  Warp w owns tile elements [w*512, w*512+512),
-// striped: item i of lane l is element w*512 + i*32 + l, so visiting items in
-// order and lanes in order visits elements in index order.  Each element gets
+// Stable scatter of one tile.  Warp w owns kRadixItems*32 consecutive tile
+// elements, striped: item i of lane l is element i*32 + l of that range, so
+// visiting items in order and lanes in order visits elements in index order.
+// Lanes with equal digits are found with one ballot per digit bit.  Each element gets
 // its rank inside the tile's digit-grouped order, the tile is rearranged in
 // shared memory, and each digit's run is written to its global slots by
 // consecutive threads (coalesced).
@@ -268,7 +269,14 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(Src src, Dst ds
   }
 #pragma unroll
   for (int i = 0; i < kRadixItems; ++i) {
-    unsigned peers = __match_any_sync(0xffffffffu, digit[i]);
+    // lanes holding the same digit (sentinel included), from nine ballots
+    unsigned peers = 0xffffffffu;
+#pragma unroll
+    for (int bit = 0; bit < 9; ++bit) {
+      const bool on = (digit[i] >> bit) & 1;
+      const unsigned bal = __ballot_sync(0xffffffffu, on);
+      peers &= on ? bal : ~bal;
+    }
     uint32_t before = (uint32_t)__popc(peers & lt_mask);
     uint32_t c = digit[i] < kRadixBins ? cnt[warp][digit[i]] : 0u;
     rank[i] = c + before;

@@ -107,9 +107,18 @@ __device__ void warp_replay(const SelState *st, int passes, uint32_t *prefix, ui
 
 template <typename TV>
 __global__ void __launch_bounds__(256) k_sel_hist(const TV *__restrict__ val, int64_t nnz, SelState *st, int pass) {
+  constexpr int kItems = 16;
   __shared__ uint32_t h[256];
   __shared__ uint32_t s_prefix, s_mask;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  const int shift = 24 - 8 * pass;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // the first chunk of keys is loaded before the previous digits are replayed,
+  // so the replay's global reads overlap the loads
+  uint32_t key[kItems];
+#pragma unroll
+  for (int u = 0; u < kItems; ++u) key[u] = first + u * stride < nnz ? mag_key<TV>(val, first + u * stride) : 0u;
   if (threadIdx.x < 32) {
     uint32_t p, m, r;
     warp_replay(st, pass, &p, &m, &r);
@@ -120,14 +129,14 @@ __global__ void __launch_bounds__(256) k_sel_hist(const TV *__restrict__ val, in
   }
   __syncthreads();
   const uint32_t prefix = s_prefix, mask = s_mask;
-  const int shift = 24 - 8 * pass;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t k0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k0 < nnz; k0 += 4 * stride) {
-    uint32_t key[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) key[u] = k0 + u * stride < nnz ? mag_key<TV>(val, k0 + u * stride) : 0u;
+  for (int u = 0; u < kItems; ++u)
+    if (first + u * stride < nnz && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> shift) & 0xFFu], 1u);
+  for (int64_t k0 = first + kItems * stride; k0 < nnz; k0 += kItems * stride) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kItems; ++u) key[u] = k0 + u * stride < nnz ? mag_key<TV>(val, k0 + u * stride) : 0u;
+#pragma unroll
+    for (int u = 0; u < kItems; ++u)
       if (k0 + u * stride < nnz && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> shift) & 0xFFu], 1u);
   }
   __syncthreads();
@@ -297,27 +306,32 @@ __device__ int64_t merge_split_warp(const uint64_t *A, int64_t na, const uint64_
   return lo + __popc(__ballot_sync(0xffffffffu, ok));
 }
 
+// part[t] = A elements among the first t*kMergeTile outputs, one warp per split
+__global__ void k_merge_splits(const uint64_t *__restrict__ A, int64_t na, const uint64_t *__restrict__ B, int64_t nb,
+                               int64_t n_tiles, int64_t *__restrict__ part) {
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t > n_tiles) return;
+  int64_t d = t * kMergeTile;
+  if (d > na + nb) d = na + nb;
+  const int64_t sp = merge_split_warp(A, na, B, nb, d);
+  if ((threadIdx.x & 31) == 0) part[t] = sp;
+}
+
 template <typename TV>
 __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
-            int64_t nb, int32_t in_f, const TV *__restrict__ val,
+            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
             int32_t *__restrict__ src_out) {
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];
   __shared__ int32_t oS[kMergeTile];
-  __shared__ int64_t s_split[2];
   const int64_t t = blockIdx.x;
   const int64_t n = na + nb;
   const int64_t d0 = t * kMergeTile;
   const int64_t d1 = d0 + kMergeTile < n ? d0 + kMergeTile : n;
-  if (threadIdx.x < 64) {
-    const int64_t sp = merge_split_warp(A, na, B, nb, threadIdx.x < 32 ? d0 : d1);
-    if ((threadIdx.x & 31) == 0) s_split[threadIdx.x >> 5] = sp;
-  }
-  __syncthreads();
-  const int64_t a0 = s_split[0], a1 = s_split[1];
+  const int64_t a0 = part[t], a1 = part[t + 1];
   const int64_t b0 = d0 - a0, b1 = d1 - a1;
   const int la = (int)(a1 - a0), lb = (int)(b1 - b0);
   for (int q = threadIdx.x; q < la; q += kMergeThreads) {
@@ -397,7 +411,7 @@ double expected_draws(double n_pos, double empty, double need) {
 }
 
 struct RWs {
-  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, total;
+  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, total;
   int64_t d_max, cap, n_merge_tiles;
 };
 
@@ -437,6 +451,8 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(4 * (size_t)cap, kAlign);
   w.radix = o;
   o += radix_temp_bytes((int64_t)np);
+  w.part = o;
+  o += align_up(8 * (size_t)(w.n_merge_tiles + 2), kAlign);
   w.total = o;
   return w;
 }
@@ -456,6 +472,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   uint64_t *hkeys = reinterpret_cast<uint64_t *>(b + W.hkeys);
   uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
   uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
+  int64_t *part = reinterpret_cast<int64_t *>(b + W.part);
   const TV *val = reinterpret_cast<const TV *>(a.val);
   const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
   const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
@@ -470,7 +487,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
   if (n_prune > 0) {
     for (int pass = 0; pass < 4; ++pass)
-      k_sel_hist<TV><<<grid_for(nnz, 256, 1184), 256, 0, s>>>(val, nnz, st, pass);
+      k_sel_hist<TV><<<grid_for((nnz + 15) / 16, 256, 1184), 256, 0, s>>>(val, nnz, st, pass);
     k_sel_final<<<1, 32, 0, s>>>(st);
   }
   SNACK_TRY(cudaGetLastError());
@@ -516,8 +533,10 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     grown = second ? grown_b : grown_a;
   }
   if (nnz > 0) {
+    k_merge_splits<<<grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
+                                                                              W.n_merge_tiles, part);
     k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
-        surv_pos, surv_src, n_surv, grown, n_prune, a.in_f, val, a.row_out, a.col_out,
+        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, val, a.row_out, a.col_out,
         reinterpret_cast<TV *>(a.val_out), a.src_out);
   }
   SNACK_TRY(cudaGetLastError());
