@@ -398,6 +398,112 @@ cudaError_t radix_sort_custom(Src0 first, DstLast last, int64_t n, int bits, K *
   return radix_pass<K>(ArraySrc<K>{ka, va}, last, n, 8 * (passes - 1), hist, offs, stemp, stream);
 }
 
+// ------------------------------------------------------------- bucket sort
+//
+// Sort n distinct 64-bit keys in [0, key_range): keys are spread over
+// equal-width buckets of the key range (about 16 keys per bucket for keys
+// drawn uniformly), each bucket is filled in arbitrary order with atomics, and
+// one warp per bucket then places every key by its rank within the bucket
+// (the number of smaller keys).  Distinct keys make the result unique.
+
+constexpr int kBucketTarget = 16;
+constexpr int kBucketSmem = 256;  // keys per warp ranked from shared memory
+
+__device__ __forceinline__ uint32_t bucket_of(uint64_t key, double scale, uint32_t nb) {
+  const double b = (double)key * scale;  // monotone in key
+  const uint32_t u = b < (double)nb ? (uint32_t)b : nb - 1;
+  return u;
+}
+
+static __global__ void k_bucket_count(const uint64_t *__restrict__ keys, int64_t n, double scale, uint32_t nb,
+                               uint32_t *__restrict__ counts) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    atomicAdd(&counts[bucket_of(keys[i], scale, nb)], 1u);
+}
+
+static __global__ void k_bucket_fill(const uint64_t *__restrict__ keys, int64_t n, double scale, uint32_t nb,
+                              const uint32_t *__restrict__ offs, uint32_t *__restrict__ fill,
+                              uint64_t *__restrict__ tmp) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const uint64_t k = keys[i];
+    const uint32_t b = bucket_of(k, scale, nb);
+    tmp[offs[b] + atomicAdd(&fill[b], 1u)] = k;
+  }
+}
+
+static __global__ void __launch_bounds__(256) k_bucket_rank(const uint64_t *__restrict__ tmp, const uint32_t *__restrict__ offs,
+                                                     uint32_t nb, uint64_t *__restrict__ out) {
+  __shared__ uint64_t s[8][kBucketSmem];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = (int64_t)blockIdx.x * 8 + warp;
+  if (b >= nb) return;
+  const uint32_t o = offs[b], L = offs[b + 1] - o;
+  if (L <= (uint32_t)kBucketSmem) {
+    for (uint32_t i = lane; i < L; i += 32) s[warp][i] = tmp[o + i];
+    __syncwarp();
+    for (uint32_t i = lane; i < L; i += 32) {
+      const uint64_t k = s[warp][i];
+      uint32_t r = 0;
+      for (uint32_t j = 0; j < L; ++j) r += s[warp][j] < k ? 1u : 0u;
+      out[o + r] = k;
+    }
+  } else {  // rare long bucket: rank from global memory
+    for (uint32_t i = lane; i < L; i += 32) {
+      const uint64_t k = tmp[o + i];
+      uint32_t r = 0;
+      for (uint32_t j = 0; j < L; ++j) r += tmp[o + j] < k ? 1u : 0u;
+      out[o + r] = k;
+    }
+  }
+}
+
+struct CountRead64 {
+  const uint32_t *c;
+  __device__ uint32_t operator()(int64_t i) const { return c[i]; }
+};
+struct WriteOffs {
+  uint32_t *o;
+  __device__ void operator()(int64_t i, uint32_t ex, uint32_t, int) const { o[i] = ex; }
+};
+
+inline uint32_t bucket_count_for(int64_t n) {
+  int64_t nb = n / kBucketTarget;
+  if (nb < 1) nb = 1;
+  if (nb > (1 << 24)) nb = 1 << 24;
+  return (uint32_t)nb;
+}
+
+inline size_t bucket_sort_temp_bytes(int64_t n) {
+  const uint32_t nb = bucket_count_for(n);
+  return 2 * align_up((size_t)(nb + 1) * 4, kAlign) + align_up((size_t)(n > 0 ? n : 1) * 8, kAlign) +
+         scan_temp_bytes<uint32_t>((int64_t)nb + 1);
+}
+
+// keys (n distinct, < key_range) -> out, ascending.  keys and out may not alias.
+inline cudaError_t bucket_sort_u64(const uint64_t *keys, int64_t n, uint64_t key_range, uint64_t *out, void *temp,
+                                   cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const uint32_t nb = bucket_count_for(n);
+  uint8_t *t = reinterpret_cast<uint8_t *>(temp);
+  const size_t cb = align_up((size_t)(nb + 1) * 4, kAlign);
+  uint32_t *offs = reinterpret_cast<uint32_t *>(t);
+  uint32_t *fill = reinterpret_cast<uint32_t *>(t + cb);
+  uint64_t *tmp = reinterpret_cast<uint64_t *>(t + 2 * cb);
+  void *stemp = t + 2 * cb + align_up((size_t)n * 8, kAlign);
+  const double scale = (double)nb / ((double)key_range + 1.0);
+  cudaError_t e = cudaMemsetAsync(offs, 0, 2 * cb, stream);  // counts and fill cursors
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((n + 255) / 256 < 65535 * 8 ? (n + 255) / 256 : 65535 * 8);
+  k_bucket_count<<<grid, 256, 0, stream>>>(keys, n, scale, nb, offs);
+  e = scan_apply<uint32_t>(CountRead64{offs}, (int64_t)nb, WriteOffs{offs}, offs + nb, stemp, stream);
+  if (e != cudaSuccess) return e;
+  k_bucket_fill<<<grid, 256, 0, stream>>>(keys, n, scale, nb, offs, fill, tmp);
+  k_bucket_rank<<<(nb + 7) / 8, 256, 0, stream>>>(tmp, offs, nb, out);
+  return cudaGetLastError();
+}
+
 // Stable sort by the low `bits` bits of the keys, ping-ponging between
 // (k0, v0) and (k1, v1) (v0/v1 may be null); *in_second is set when the
 // result ends in (k1, v1).

@@ -450,7 +450,7 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   w.hmin = o;
   o += align_up(4 * (size_t)cap, kAlign);
   w.radix = o;
-  o += radix_temp_bytes((int64_t)np);
+  o += bucket_sort_temp_bytes((int64_t)np);
   w.part = o;
   o += align_up(8 * (size_t)(w.n_merge_tiles + 2), kAlign);
   w.total = o;
@@ -524,13 +524,12 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       done += m;
     }
   }
-  // 4. sort regrown positions, merge with survivors
+  // 4. sort regrown positions (bucket sort: they are uniform over the empty
+  //    positions), merge with survivors
   const uint64_t *grown = grown_a;
   if (n_prune > 1) {
-    bool second = false;
-    SNACK_TRY(radix_sort<uint64_t>(grown_a, nullptr, grown_b, nullptr, n_prune, bits_for(n_pos - 1), b + W.radix, s,
-                                   &second));
-    grown = second ? grown_b : grown_a;
+    SNACK_TRY(bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s));
+    grown = grown_b;
   }
   if (nnz > 0) {
     k_merge_splits<<<grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
