@@ -142,6 +142,29 @@ snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *co
                            snack_stream_t stream);
 
 /*
+ * Forward with a GELU epilogue, for the sparse MLP block of the abstract's
+ * GPT-2 experiment (two sparse layers with GELU between them):
+ *   y_pre[b, r] = bias[r] + sum_{k : row[k] = r} val[k] * x[b, col[k]]
+ *   y[b, r]     = GELU(y_pre[b, r]) = y_pre * Phi(y_pre)   (exact erf form, fp32)
+ * y_pre (same shape and dtype as y) may be NULL; keep it when the backward
+ * pass needs GELU'.  y_pre and y must not overlap x or each other.
+ */
+snack_status snack_spmm_fwd_gelu(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                 const void *x, int32_t batch, const float *bias, void *y_pre, void *y, void *ws,
+                                 size_t ws_bytes, snack_stream_t stream);
+
+/*
+ * Input gradient through a GELU that preceded this layer:
+ *   dx[b, c] = GELU'(x_pre[b, c]) * sum_{k : col[k] = c} val[k] * dy[b, row[k]]
+ * x_pre [batch, in_f] is the pre-activation this layer's input came from (the
+ * y_pre of the previous layer's snack_spmm_fwd_gelu); GELU'(t) = Phi(t) +
+ * t phi(t).  dx must not overlap dy or x_pre.
+ */
+snack_status snack_spmm_dx_gelu(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                const void *dy, int32_t batch, const void *x_pre, void *dx, void *ws,
+                                size_t ws_bytes, snack_stream_t stream);
+
+/*
  * Weight gradient at the stored positions only (sampled dense-dense product):
  *   dw[k] = sum_b dy[b, row[k]] * x[b, col[k]]     fp32 [nnz]
  *   db[r] = sum_b dy[b, r]                         fp32 [out_f], or NULL to skip

@@ -97,7 +97,8 @@ snack_status check_shape(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_b
 
 template <typename T>
 snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const void *x, int32_t batch,
-                     const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s) {
+                     const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s, int act = kActNone,
+                     void *pre_out = nullptr) {
   BatchGeom bg = batch_geom(batch, h->act_t);
   SpmmWs W = spmm_ws(h->in_f, h->lay.gf, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
@@ -124,13 +125,16 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
   p.batch = batch;
   p.carry = reinterpret_cast<float *>(b + W.carry);
   p.head = reinterpret_cast<float *>(b + W.head);
+  p.act = act;
+  p.pre_in = nullptr;
+  p.pre_out = pre_out;
   SNACK_CUDA(run_spmm<T>(p, bg, false, s));
   return SNACK_OK;
 }
 
 template <typename T>
 snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t batch, void *dx, void *ws,
-                    size_t ws_bytes, cudaStream_t s) {
+                    size_t ws_bytes, cudaStream_t s, int act = kActNone, const void *pre_in = nullptr) {
   BatchGeom bg = batch_geom(batch, h->act_t);
   SpmmWs W = spmm_ws(h->out_f, h->lay.gt, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
@@ -157,6 +161,9 @@ snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t bat
   p.batch = batch;
   p.carry = reinterpret_cast<float *>(b + W.carry);
   p.head = reinterpret_cast<float *>(b + W.head);
+  p.act = act;
+  p.pre_in = pre_in;
+  p.pre_out = nullptr;
   SNACK_CUDA(run_spmm<T>(p, bg, true, s));
   return SNACK_OK;
 }
@@ -303,6 +310,44 @@ snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *c
   if (!x || !dy) return SNACK_ERR_INVALID_ARG;
   if (h->act_t == SNACK_BF16) return run_dw<bf16>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
   return run_dw<float>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+}
+
+snack_status snack_spmm_fwd_gelu(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                 const void *x, int32_t batch, const float *bias, void *y_pre, void *y, void *ws,
+                                 size_t ws_bytes, snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  (void)row;
+  if (batch == 0) return SNACK_OK;
+  if (!x || !y || (h->nnz > 0 && (!col || !val))) return SNACK_ERR_INVALID_ARG;
+  const size_t s_act = dtype_size(h->act_t);
+  const size_t ny = (size_t)batch * h->out_f * s_act, nx = (size_t)batch * h->in_f * s_act;
+  if (overlap(y, ny, x, nx) || (y_pre && (overlap(y_pre, ny, x, nx) || overlap(y_pre, ny, y, ny))))
+    return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->act_t == SNACK_BF16) return run_fwd<bf16>(h, col, val, x, batch, bias, y, ws, ws_bytes, s, kActGelu, y_pre);
+  return run_fwd<float>(h, col, val, x, batch, bias, y, ws, ws_bytes, s, kActGelu, y_pre);
+}
+
+snack_status snack_spmm_dx_gelu(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                const void *dy, int32_t batch, const void *x_pre, void *dx, void *ws, size_t ws_bytes,
+                                snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  (void)row;
+  (void)col;
+  if (batch == 0) return SNACK_OK;
+  if (!dy || !dx || !x_pre || (h->nnz > 0 && !val)) return SNACK_ERR_INVALID_ARG;
+  const size_t s_act = dtype_size(h->act_t);
+  const size_t nd = (size_t)batch * h->in_f * s_act, ny = (size_t)batch * h->out_f * s_act;
+  if (overlap(dx, nd, dy, ny) || overlap(dx, nd, x_pre, nd)) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
+  return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
 }
 
 snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, size_t *bytes) {

@@ -121,7 +121,32 @@ struct SpmmParams {
   int32_t batch;
   float *carry;           // [n_btiles][n_tiles][bt]
   float *head;            // [n_btiles][n_tiles][bt]
+  int32_t act;            // output epilogue: kActNone, kActGelu, kActGeluGrad
+  const void *pre_in;     // kActGeluGrad: pre-activation [batch][n_rows] (act dtype)
+  void *pre_out;          // kActGelu: pre-activation written here when non-null
 };
+
+// Output epilogues of the SpMM kernels.
+constexpr int kActNone = 0;
+constexpr int kActGelu = 1;      // y = GELU(s), s optionally kept in pre_out
+constexpr int kActGeluGrad = 2;  // y = s * GELU'(pre_in)
+
+// GELU in the exact (erf) form and its derivative Phi(x) + x phi(x).
+__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad_f(float x) {
+  return 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143267794f * expf(-0.5f * x * x);
+}
+
+// Final value of output (b, r) given its fp32 sum s (bias included).
+template <typename TA>
+__device__ __forceinline__ TA spmm_epilogue(const SpmmParams &P, float s, size_t off) {
+  if (P.act == kActGelu) {
+    if (P.pre_out) reinterpret_cast<TA *>(P.pre_out)[off] = from_f32<TA>(s);
+    return from_f32<TA>(gelu_f(s));
+  }
+  if (P.act == kActGeluGrad) return from_f32<TA>(s * gelu_grad_f(to_f32(reinterpret_cast<const TA *>(P.pre_in)[off])));
+  return from_f32<TA>(s);
+}
 
 // ------------------------------------------------------------------ kernels
 
@@ -290,11 +315,11 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
     TA *y = reinterpret_cast<TA *>(P.y);
     const int bmax = min(bt, P.batch - b0);
     for (int b = warp; b < bmax; b += kSpmmWarps) {
-      TA *yrow = y + (size_t)(b0 + b) * P.n_rows + i0 + rs;
+      const size_t rowoff = (size_t)(b0 + b) * P.n_rows + i0 + rs;
       for (int q = lane; q < nw; q += 32) {
         float s = Ys[(size_t)(q + rs) * ys_ld + b];
         if (P.bias) s = P.bias[i0 + rs + q] + s;
-        yrow[q] = from_f32<TA>(s);
+        y[rowoff + q] = spmm_epilogue<TA>(P, s, rowoff + q);
       }
     }
   }
@@ -317,7 +342,8 @@ __global__ void k_spmm_fixup(SpmmParams P, BatchGeom bg) {
     for (int u = first; u < t; ++u) s += P.carry[((size_t)bi * P.tg.n_tiles + u) * bt + b];
     s += P.head[((size_t)bi * P.tg.n_tiles + t) * bt + b];
     if (P.bias) s = P.bias[i0] + s;
-    y[(size_t)(b0 + b) * P.n_rows + i0] = from_f32<TA>(s);
+    const size_t off = (size_t)(b0 + b) * P.n_rows + i0;
+    y[off] = spmm_epilogue<TA>(P, s, off);
   }
 }
 

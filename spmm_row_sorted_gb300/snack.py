@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "SNACK_OK", 1: "SNACK_ERR_INVALID_ARG", 2: "SNACK_ERR_UNSORTE
 SNACK_F32, SNACK_BF16 = 0, 1
 
 EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
-            "snack_sddmm_dw",
+            "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw",
             "snack_restructure_workspace_size", "snack_restructure", "snack_destroy", "snack_status_string",
             "snack_version")
 
@@ -73,6 +73,10 @@ def load(path: Optional[str] = None):
         lib.snack_spmm_fwd.restype = st
         lib.snack_spmm_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp]
         lib.snack_spmm_fwd_noalloc.restype = st
+        lib.snack_spmm_fwd_gelu.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        lib.snack_spmm_fwd_gelu.restype = st
+        lib.snack_spmm_dx_gelu.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        lib.snack_spmm_dx_gelu.restype = st
         lib.snack_spmm_dx.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
         lib.snack_spmm_dx.restype = st
         lib.snack_sddmm_dw.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
@@ -159,6 +163,19 @@ def snack_spmm_dx(h: int, row, col, val, dy, batch: int, dx, ws, stream=None) ->
                                 _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
 
 
+def snack_spmm_fwd_gelu(h: int, row, col, val, x, batch: int, bias, y_pre, y, ws, stream=None) -> None:
+    _check("snack_spmm_fwd_gelu",
+           load().snack_spmm_fwd_gelu(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), _ptr(x), batch, _ptr(bias),
+                                      _ptr(y_pre), _ptr(y), _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
+
+
+def snack_spmm_dx_gelu(h: int, row, col, val, dy, batch: int, x_pre, dx, ws, stream=None) -> None:
+    _check("snack_spmm_dx_gelu",
+           load().snack_spmm_dx_gelu(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), _ptr(dy), batch,
+                                     _ptr(x_pre), _ptr(dx), _ptr(ws), 0 if ws is None else _nbytes(ws),
+                                     _stream(stream)))
+
+
 def snack_sddmm_dw(h: int, row, col, x, dy, batch: int, dw, db, ws, stream=None) -> None:
     _check("snack_sddmm_dw",
            load().snack_sddmm_dw(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(x), _ptr(dy), batch, _ptr(dw),
@@ -240,6 +257,22 @@ class SparseLinear:
         y = out if out is not None else torch.empty((x.shape[0], self.out_f), dtype=self.dtype, device=x.device)
         snack_spmm_fwd(self.handle, self.row, self.col, self.val, x, x.shape[0], self.bias, y, self.ws, stream)
         return y
+
+    def forward_gelu(self, x: torch.Tensor, keep_pre: bool = True, stream=None):
+        """GELU(x W^T + b); returns (y, pre) with pre None unless keep_pre."""
+        x = x.contiguous()
+        y = torch.empty((x.shape[0], self.out_f), dtype=self.dtype, device=x.device)
+        pre = torch.empty_like(y) if keep_pre else None
+        snack_spmm_fwd_gelu(self.handle, self.row, self.col, self.val, x, x.shape[0], self.bias, pre, y, self.ws,
+                            stream)
+        return y, pre
+
+    def grad_input_gelu(self, dy: torch.Tensor, x_pre: torch.Tensor, stream=None) -> torch.Tensor:
+        """(dy W) * GELU'(x_pre): the gradient at the pre-activation of this layer's input."""
+        dy, x_pre = dy.contiguous(), x_pre.contiguous()
+        dx = torch.empty((dy.shape[0], self.in_f), dtype=self.dtype, device=dy.device)
+        snack_spmm_dx_gelu(self.handle, self.row, self.col, self.val, dy, dy.shape[0], x_pre, dx, self.ws, stream)
+        return dx
 
     def grad_input(self, dy: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         dy = dy.contiguous()
