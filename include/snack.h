@@ -175,6 +175,20 @@ snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *c
                             size_t ws_bytes, snack_stream_t stream);
 
 /*
+ * The whole sparse backward pass in one call: the input gradient of
+ * snack_spmm_dx, the weight gradient of snack_sddmm_dw, and db (NULL to
+ * skip).  When one batch tile covers the batch (batch <= 128 for fp32, 256
+ * for bf16) the two gradients come from one pass over the column view: each
+ * gathered dY row slice is also dotted with the current column of X, so the
+ * index and value streams are read once.  Wider batches run the two kernels
+ * one after the other.  Outputs as in snack_spmm_dx / snack_sddmm_dw; dx must
+ * not overlap x or dy.  Deterministic.
+ */
+snack_status snack_backward(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                            const void *x, const void *dy, int32_t batch, void *dx, float *dw, float *db,
+                            void *ws, size_t ws_bytes, snack_stream_t stream);
+
+/*
  * Workspace needed by snack_restructure for a given n_prune.
  */
 snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, size_t *bytes);

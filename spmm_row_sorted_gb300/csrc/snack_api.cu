@@ -70,14 +70,36 @@ DwWs dw_ws(int32_t out_f, int32_t in_f, const BatchGeom &bg, size_t s_act, int b
   return w;
 }
 
+// fused backward: dY transposed + X transposed + the input-gradient tile partials
+struct BwdWs {
+  size_t dyt, xt, carry, head, total;
+};
+
+BwdWs bwd_ws(int32_t out_f, int32_t in_f, const TileGeom &gt, const BatchGeom &bg, size_t s_act, int batch) {
+  BwdWs w;
+  size_t o = 0;
+  w.dyt = o;
+  if (batch > 1) o += align_up((size_t)out_f * bg.ldx * s_act, kAlign);
+  w.xt = o;
+  if (batch > 1) o += align_up((size_t)in_f * bg.ldx * s_act, kAlign);
+  w.carry = o;
+  o += align_up((size_t)bg.n_btiles * gt.n_tiles * bg.bt * 4, kAlign);
+  w.head = o;
+  o += align_up((size_t)bg.n_btiles * gt.n_tiles * bg.bt * 4, kAlign);
+  w.total = o;
+  return w;
+}
+
 size_t ops_ws_bytes(int32_t out_f, int32_t in_f, int batch, snack_dtype act, const PlanLayout &lay) {
   BatchGeom bg = batch_geom(batch, act);
   size_t s = dtype_size(act);
   size_t a = spmm_ws(in_f, lay.gf, bg, s, batch).total;
   size_t b = spmm_ws(out_f, lay.gt, bg, s, batch).total;
   size_t c = dw_ws(out_f, in_f, bg, s, batch).total;
+  size_t d = bwd_ws(out_f, in_f, lay.gt, bg, s, batch).total;
   size_t m = a > b ? a : b;
-  return m > c ? m : c;
+  m = m > c ? m : c;
+  return m > d ? m : d;
 }
 
 snack_status check_shape(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t,
@@ -125,10 +147,12 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
   p.batch = batch;
   p.carry = reinterpret_cast<float *>(b + W.carry);
   p.head = reinterpret_cast<float *>(b + W.head);
+  p.xt_dw = nullptr;
+  p.dw = nullptr;
   p.act = act;
   p.pre_in = nullptr;
   p.pre_out = pre_out;
-  SNACK_CUDA(run_spmm<T>(p, bg, false, s));
+  SNACK_CUDA(run_spmm<T>(p, bg, false, false, s));
   return SNACK_OK;
 }
 
@@ -161,10 +185,12 @@ snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t bat
   p.batch = batch;
   p.carry = reinterpret_cast<float *>(b + W.carry);
   p.head = reinterpret_cast<float *>(b + W.head);
+  p.xt_dw = nullptr;
+  p.dw = nullptr;
   p.act = act;
   p.pre_in = pre_in;
   p.pre_out = nullptr;
-  SNACK_CUDA(run_spmm<T>(p, bg, true, s));
+  SNACK_CUDA(run_spmm<T>(p, bg, true, false, s));
   return SNACK_OK;
 }
 
@@ -188,6 +214,57 @@ snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, cons
     dyt = c;
   }
   SNACK_CUDA(run_sddmm<T>(h->nnz, row, col, h->out_f, h->in_f, xt, dyt, bg, dw, h->num_sms, s));
+  return SNACK_OK;
+}
+
+// Fused backward: one pass over the column view gives dX and dW (one batch
+// tile); wider batches run the input gradient and the SDDMM separately.
+template <typename T>
+snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *x,
+                     const void *dy, int32_t batch, void *dx, float *dw, float *db, void *ws, size_t ws_bytes,
+                     cudaStream_t s) {
+  BatchGeom bg = batch_geom(batch, h->act_t);
+  if (bg.n_btiles > 1 || h->nnz == 0) {
+    snack_status st = run_dx<T>(h, val, dy, batch, dx, ws, ws_bytes, s);
+    if (st != SNACK_OK) return st;
+    return run_dw<T>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+  }
+  BwdWs W = bwd_ws(h->out_f, h->in_f, h->lay.gt, bg, sizeof(T), batch);
+  if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  const T *dyt = reinterpret_cast<const T *>(dy);
+  const T *xt = reinterpret_cast<const T *>(x);
+  if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
+  if (batch > 1) {
+    T *a = reinterpret_cast<T *>(b + W.dyt);
+    T *c = reinterpret_cast<T *>(b + W.xt);
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, a, bg.ldx, s));
+    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, c, bg.ldx, s));
+    dyt = a;
+    xt = c;
+  }
+  SpmmParams p;
+  p.n_rows = h->in_f;
+  p.n_src = h->out_f;
+  p.ptr = h->p.cp;
+  p.tiles = h->p.tiles_t;
+  p.tg = h->lay.gt;
+  p.nnz = h->nnz;
+  p.idx = h->p.row_t;
+  p.val = val;
+  p.val_src = h->p.src_t;
+  p.xt = dyt;
+  p.bias = nullptr;
+  p.y = dx;
+  p.batch = batch;
+  p.carry = reinterpret_cast<float *>(b + W.carry);
+  p.head = reinterpret_cast<float *>(b + W.head);
+  p.xt_dw = xt;
+  p.dw = dw;
+  p.act = kActNone;
+  p.pre_in = nullptr;
+  p.pre_out = nullptr;
+  SNACK_CUDA(run_spmm<T>(p, bg, true, true, s));
   return SNACK_OK;
 }
 
@@ -348,6 +425,29 @@ snack_status snack_spmm_dx_gelu(snack_handle h, const int32_t *row, const int32_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
   return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
+}
+
+snack_status snack_backward(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *x,
+                            const void *dy, int32_t batch, void *dx, float *dw, float *db, void *ws, size_t ws_bytes,
+                            snack_stream_t stream) {
+  snack_status st = common_call_checks(h, batch, ws);
+  if (st != SNACK_OK) return st;
+  if (h->nnz > 0 && (!row || !col || !val || !dw)) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (batch == 0) {  // empty sums
+    if (h->nnz > 0) SNACK_CUDA(cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)h->nnz, s));
+    if (db) SNACK_CUDA(cudaMemsetAsync(db, 0, sizeof(float) * (size_t)h->out_f, s));
+    return SNACK_OK;
+  }
+  if (!x || !dy || !dx) return SNACK_ERR_INVALID_ARG;
+  const size_t s_act = dtype_size(h->act_t);
+  if (overlap(dx, (size_t)batch * h->in_f * s_act, dy, (size_t)batch * h->out_f * s_act) ||
+      overlap(dx, (size_t)batch * h->in_f * s_act, x, (size_t)batch * h->in_f * s_act))
+    return SNACK_ERR_INVALID_ARG;
+  if (h->act_t == SNACK_BF16) return run_bwd<bf16>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
+  return run_bwd<float>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
 }
 
 snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, size_t *bytes) {

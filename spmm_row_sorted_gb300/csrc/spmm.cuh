@@ -121,6 +121,8 @@ struct SpmmParams {
   int32_t batch;
   float *carry;           // [n_btiles][n_tiles][bt]
   float *head;            // [n_btiles][n_tiles][bt]
+  const void *xt_dw;      // fused backward: transposed X [n_rows][ldx] (dx mode, rows = input features)
+  float *dw;              // fused backward: weight gradient [nnz], written at storage index
   int32_t act;            // output epilogue: kActNone, kActGelu, kActGeluGrad
   const void *pre_in;     // kActGeluGrad: pre-activation [batch][n_rows] (act dtype)
   void *pre_out;          // kActGelu: pre-activation written here when non-null
@@ -159,7 +161,10 @@ struct SpmmUnroll {
   static constexpr int value = base < kMax ? base : kMax;
 };
 
-template <typename TA, typename TV, int V, int G, bool kGatherVal>
+// kFuseDw (column-view mode, one batch tile): each gathered dY row slice is
+// also dotted with the current column's X slice, giving dW at that entry's
+// storage index in the same pass.
+template <typename TA, typename TV, int V, int G, bool kGatherVal, bool kFuseDw>
 __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
   constexpr int kSlots = 32 / G;
   constexpr int kU = SpmmUnroll<V, G>::value;
@@ -179,6 +184,7 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
   int *wsp = rps + max_rows + 1;
   uint32_t *s_idx = reinterpret_cast<uint32_t *>(wsp + 2 * (kSpmmWarps + 1));
   float *s_val = reinterpret_cast<float *>(s_idx + cap);
+  uint32_t *s_src = reinterpret_cast<uint32_t *>(s_val + cap);  // kFuseDw only
 
   const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1];
   int i1 = P.tiles[2 * t + 2];
@@ -200,18 +206,20 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
     const uint32_t nnz_max = (uint32_t)(P.nnz > 0 ? P.nnz - 1 : 0);
     const int nn = j1 - j0;
     for (int q0 = 0; q0 < nn; q0 += 4 * kSpmmThreads) {
-      uint32_t cc[4];
+      uint32_t cc[4], ss[4];
       float vv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int q = q0 + u * kSpmmThreads + tid;
         cc[u] = 0u;
+        ss[u] = 0u;
         vv[u] = 0.f;
         if (q < nn) {
           cc[u] = (uint32_t)ld_stream(P.idx + j0 + q);
           if (kGatherVal) {
             uint32_t sidx = (uint32_t)ld_stream(P.val_src + j0 + q);
-            vv[u] = to_f32(ld_keep(val + (sidx < nnz_max ? sidx : nnz_max)));
+            ss[u] = sidx < nnz_max ? sidx : nnz_max;
+            vv[u] = to_f32(ld_keep(val + ss[u]));
           } else {
             vv[u] = to_f32(ld_stream(val + j0 + q));
           }
@@ -223,6 +231,7 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
         if (q < nn) {
           s_idx[q] = cc[u] < src_max ? cc[u] : src_max;
           s_val[q] = vv[u];
+          if (kFuseDw) s_src[q] = ss[u];
         }
       }
     }
@@ -262,6 +271,15 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    float xc[V];  // kFuseDw: this column's X slice
+    if (kFuseDw) {
+      const int ci = i < P.n_rows ? i : P.n_rows - 1;
+      if (ps < pe)
+        Slice<TA, V>::load(reinterpret_cast<const TA *>(P.xt_dw) + (size_t)ci * bg.ldx + b0 + g * V, xc);
+      else
+#pragma unroll
+        for (int e = 0; e < V; ++e) xc[e] = 0.f;
+    }
     for (int base = ps; base < pe; base += kSlots * kU) {
       uint32_t c[kU];
       float v[kU];
@@ -279,6 +297,26 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
       for (int u = 0; u < kU; ++u)
 #pragma unroll
         for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], x[u][e], acc[e]);
+      if (kFuseDw) {
+        float d[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          d[u] = 0.f;
+#pragma unroll
+          for (int e = 0; e < V; ++e) d[u] = fmaf(x[u][e], xc[e], d[u]);
+        }
+#pragma unroll
+        for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+          for (int u = 0; u < kU; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], off);
+        if (g == 0) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int k = base + u * kSlots + slot;
+            if (k < pe) P.dw[s_src[k]] = d[u];
+          }
+        }
+      }
     }
 #pragma unroll
     for (int off = G; off < 32; off <<= 1)
@@ -469,10 +507,10 @@ __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__res
 
 // ------------------------------------------------------------------ host
 
-template <typename TA, typename TV, int V, int G, bool kGV>
+template <typename TA, typename TV, int V, int G, bool kGV, bool kFuse>
 cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
-  size_t smem = spmm_smem_bytes(p.tg, bg.bt);
-  auto kern = k_spmm_tiles<TA, TV, V, G, kGV>;
+  size_t smem = spmm_smem_bytes(p.tg, bg.bt) + (kFuse ? (size_t)tile_stage_cap(p.tg) * 4 : 0);
+  auto kern = k_spmm_tiles<TA, TV, V, G, kGV, kFuse>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -484,17 +522,17 @@ cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t
   return cudaGetLastError();
 }
 
-template <typename TA, typename TV, bool kGV>
+template <typename TA, typename TV, bool kGV, bool kFuse>
 cudaError_t launch_spmm(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
   constexpr int VV = ActTraits<TA>::kVec;
-  if (bg.V == 1) return launch_spmm_v<TA, TV, 1, 1, kGV>(p, bg, s);
+  if (bg.V == 1) return launch_spmm_v<TA, TV, 1, 1, kGV, kFuse>(p, bg, s);
   switch (bg.G) {
-    case 1: return launch_spmm_v<TA, TV, VV, 1, kGV>(p, bg, s);
-    case 2: return launch_spmm_v<TA, TV, VV, 2, kGV>(p, bg, s);
-    case 4: return launch_spmm_v<TA, TV, VV, 4, kGV>(p, bg, s);
-    case 8: return launch_spmm_v<TA, TV, VV, 8, kGV>(p, bg, s);
-    case 16: return launch_spmm_v<TA, TV, VV, 16, kGV>(p, bg, s);
-    case 32: return launch_spmm_v<TA, TV, VV, 32, kGV>(p, bg, s);
+    case 1: return launch_spmm_v<TA, TV, VV, 1, kGV, kFuse>(p, bg, s);
+    case 2: return launch_spmm_v<TA, TV, VV, 2, kGV, kFuse>(p, bg, s);
+    case 4: return launch_spmm_v<TA, TV, VV, 4, kGV, kFuse>(p, bg, s);
+    case 8: return launch_spmm_v<TA, TV, VV, 8, kGV, kFuse>(p, bg, s);
+    case 16: return launch_spmm_v<TA, TV, VV, 16, kGV, kFuse>(p, bg, s);
+    case 32: return launch_spmm_v<TA, TV, VV, 32, kGV, kFuse>(p, bg, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -549,8 +587,10 @@ cudaError_t launch_colsum(const T *a, int batch, int n, float *out, cudaStream_t
 }
 
 // per-dtype entry points (explicitly instantiated in spmm_f32.cu / spmm_bf16.cu)
+// gather_val: column-view mode (input gradient); fuse_dw: also the weight
+// gradient (column-view mode with a single batch tile only)
 template <typename T>
-cudaError_t run_spmm(const SpmmParams &p, const BatchGeom &bg, bool gather_val, cudaStream_t s);
+cudaError_t run_spmm(const SpmmParams &p, const BatchGeom &bg, bool gather_val, bool fuse_dw, cudaStream_t s);
 template <typename T>
 cudaError_t run_sddmm(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
                       const T *xt, const T *dyt, const BatchGeom &bg, float *dw, int num_sms, cudaStream_t s);

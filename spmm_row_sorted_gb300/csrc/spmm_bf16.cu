@@ -4,8 +4,10 @@
 namespace snack {
 
 template <>
-cudaError_t run_spmm<bf16>(const SpmmParams &p, const BatchGeom &bg, bool gather_val, cudaStream_t s) {
-  return gather_val ? launch_spmm<bf16, bf16, true>(p, bg, s) : launch_spmm<bf16, bf16, false>(p, bg, s);
+cudaError_t run_spmm<bf16>(const SpmmParams &p, const BatchGeom &bg, bool gather_val, bool fuse_dw,
+                          cudaStream_t s) {
+  if (!gather_val) return launch_spmm<bf16, bf16, false, false>(p, bg, s);
+  return fuse_dw ? launch_spmm<bf16, bf16, true, true>(p, bg, s) : launch_spmm<bf16, bf16, true, false>(p, bg, s);
 }
 
 template <>

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "SNACK_OK", 1: "SNACK_ERR_INVALID_ARG", 2: "SNACK_ERR_UNSORTE
 SNACK_F32, SNACK_BF16 = 0, 1
 
 EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
-            "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw",
+            "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw", "snack_backward",
             "snack_restructure_workspace_size", "snack_restructure", "snack_destroy", "snack_status_string",
             "snack_version")
 
@@ -81,6 +81,8 @@ def load(path: Optional[str] = None):
         lib.snack_spmm_dx.restype = st
         lib.snack_sddmm_dw.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
         lib.snack_sddmm_dw.restype = st
+        lib.snack_backward.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        lib.snack_backward.restype = st
         lib.snack_restructure_workspace_size.argtypes = [vp, i64, ctypes.POINTER(sz)]
         lib.snack_restructure_workspace_size.restype = st
         lib.snack_restructure.argtypes = [vp, vp, vp, vp, i64, u64, u64, vp, vp, vp, vp, vp, sz, vp]
@@ -180,6 +182,13 @@ def snack_sddmm_dw(h: int, row, col, x, dy, batch: int, dw, db, ws, stream=None)
     _check("snack_sddmm_dw",
            load().snack_sddmm_dw(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(x), _ptr(dy), batch, _ptr(dw),
                                  _ptr(db), _ptr(ws), 0 if ws is None else _nbytes(ws), _stream(stream)))
+
+
+def snack_backward(h: int, row, col, val, x, dy, batch: int, dx, dw, db, ws, stream=None) -> None:
+    _check("snack_backward",
+           load().snack_backward(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), _ptr(x), _ptr(dy), batch,
+                                 _ptr(dx), _ptr(dw), _ptr(db), _ptr(ws), 0 if ws is None else _nbytes(ws),
+                                 _stream(stream)))
 
 
 def snack_restructure_workspace_size(h: int, n_prune: int) -> int:
@@ -286,6 +295,15 @@ class SparseLinear:
         db = torch.empty(self.out_f, dtype=torch.float32, device=x.device) if want_db else None
         snack_sddmm_dw(self.handle, self.row, self.col, x, dy, x.shape[0], dw, db, self.ws, stream)
         return dw, db
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, want_db: bool = True, stream=None):
+        """(dX, dW, db) in one call (fused single pass when the batch fits one tile)."""
+        x, dy = x.contiguous(), dy.contiguous()
+        dx = torch.empty((dy.shape[0], self.in_f), dtype=self.dtype, device=dy.device)
+        dw = torch.empty(self.nnz, dtype=torch.float32, device=x.device)
+        db = torch.empty(self.out_f, dtype=torch.float32, device=x.device) if want_db else None
+        snack_backward(self.handle, self.row, self.col, self.val, x, dy, x.shape[0], dx, dw, db, self.ws, stream)
+        return dx, dw, db
 
     def restructure(self, n_prune: int, seed: int, step: int, stream=None) -> torch.Tensor:
         """Prune/regrow in place of this layer's pattern; returns src index (-1 = regrown)."""
