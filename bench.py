@@ -36,8 +36,8 @@ if ROOT not in sys.path:
 
 METRIC = "SpMM fwd/dx/dw µs, GB/s and % of GB300 HBM roofline at 90–99% sparsity"
 WORKLOAD = ("16384x16384 sparse linear layer, 99% sparse (nnz 2,684,355, row lengths Zipf s=1.2), fp32 values "
-            "N(0,0.02), batch 32 fp32 X,dY ~ N(0,1); step = fwd + dX + dW/db + DST restructure "
-            "(prune 10% smallest |w| = 268,435, regrow as many at uniform empty positions)")
+            "N(0,0.02), batch 32 fp32 X,dY ~ N(0,1); step = fwd + backward (dX + dW + db in one fused pass) + "
+            "DST restructure (prune 10% smallest |w| = 268,435, regrow as many at uniform empty positions)")
 OUT_F = IN_F = 16384
 BATCH = 32
 PRUNE_FRAC = 0.10
@@ -45,12 +45,20 @@ N_COPIES = 8  # rotating layer copies: consecutive steps never find their inputs
 
 
 def alg_bytes(nnz: int, batch: int, out_f: int, in_f: int, s_v: int = 4, s_x: int = 4) -> dict:
-    """Bytes each op must move at least (indices + values + activations once)."""
+    """Bytes each op must move at least (indices + values + activations once).
+
+    fwd/dx/dw are the single ops; bwd is dx and dw together (snack_backward),
+    which reads the pattern and the values once: pattern + values + dW out +
+    X + dY in + dX out + db out."""
     fwd = nnz * (8 + s_v) + batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
     dx = nnz * (8 + s_v) + batch * out_f * s_x + batch * in_f * s_x
     dw = nnz * (8 + 4) + batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
+    bwd = nnz * (8 + s_v + 4) + 2 * batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
     restructure = 2 * nnz * (8 + s_v) + 4 * nnz  # read old COO, write new COO + source map
-    return {"fwd": fwd, "dx": dx, "dw": dw, "restructure": restructure}
+    return {"fwd": fwd, "dx": dx, "dw": dw, "bwd": bwd, "restructure": restructure}
+
+
+STEP_OPS = ("fwd", "bwd", "restructure")
 
 
 def measured_peak_gbs():
@@ -176,7 +184,8 @@ class OracleSampler:
     A sample is the sub-layer of `nrows` consecutive output rows (all input
     columns, full batch); one sample step runs forward, input gradient, weight
     gradient and a 10 % restructure of that sub-layer.  Its algorithmic bytes
-    follow the same formula as the GPU ops, so bytes/second compare directly.
+    follow the same formula as the GPU step (forward, backward, restructure),
+    so bytes/second compare directly.
     """
 
     def __init__(self, lay, acts):
@@ -205,7 +214,8 @@ class OracleSampler:
         o.dw(nrows, IN_F, sub.row, sub.col, self.x64, dy64)
         o.restructure(nrows, IN_F, sub.row, sub.col, v64, n_prune, 0, step_index)
         dt = time.perf_counter() - t0
-        return dt, sum(alg_bytes(sub.nnz, BATCH, nrows, IN_F).values()), nrows
+        b = alg_bytes(sub.nnz, BATCH, nrows, IN_F)
+        return dt, sum(b[op] for op in STEP_OPS), nrows
 
     def rows_for(self, seconds: float) -> int:
         """Rows per sample so that one sample step takes about `seconds`."""
@@ -269,7 +279,7 @@ def run_ours(args):
     nnz = lay.nnz
     n_prune = int(PRUNE_FRAC * nnz)
     byts = alg_bytes(nnz, BATCH, OUT_F, IN_F)
-    step_bytes = sum(byts.values())
+    step_bytes = sum(byts[op] for op in STEP_OPS)
 
     stream = torch.cuda.Stream(device=dev)
     plan_b, ws_b = snack.snack_query_sizes(OUT_F, IN_F, nnz, BATCH, 0, 0)
@@ -306,17 +316,15 @@ def run_ours(args):
         snack.snack_spmm_fwd(cp["h"], row, col, val, cp["x"], BATCH, cp["bias"], cp["y"], ws, stream)
         if ev is not None:
             ev[1].record(stream)
-        snack.snack_spmm_dx(cp["h"], row, col, val, cp["dy"], BATCH, cp["dx"], ws, stream)
+        snack.snack_backward(cp["h"], row, col, val, cp["x"], cp["dy"], BATCH, cp["dx"], cp["dw"], cp["db"], ws,
+                             stream)
         if ev is not None:
             ev[2].record(stream)
-        snack.snack_sddmm_dw(cp["h"], row, col, cp["x"], cp["dy"], BATCH, cp["dw"], cp["db"], ws, stream)
-        if ev is not None:
-            ev[3].record(stream)
         nxt = 1 - cur
         snack.snack_restructure(cp["h"], row, col, val, n_prune, 12345, i, cp["row"][nxt], cp["col"][nxt],
                                 cp["val"][nxt], cp["src"], ws, stream)
         if ev is not None:
-            ev[4].record(stream)
+            ev[3].record(stream)
         cp["cur"] = nxt
 
     if args.profile:  # untimed steps on one copy, for profilers (ncu -k ... -c ...)
@@ -330,7 +338,7 @@ def run_ours(args):
     for i in range(args.warmup):
         step(copies[i % N_COPIES], i)
     stream.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_OPS) + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -348,7 +356,7 @@ def run_ours(args):
         t = torch.tensor([elapsed_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    ops = ["fwd", "dx", "dw", "restructure"]
+    ops = list(STEP_OPS)
     op_ms = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
              for j, op in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps
@@ -357,8 +365,9 @@ def run_ours(args):
     op_report = {}
     for op in ops:
         gbs = byts[op] / (op_ms[op] / 1e3) / 1e9
+        flops = {"fwd": 2 * nnz * BATCH, "bwd": 4 * nnz * BATCH}.get(op)
         op_report[op] = {"us": op_ms[op] * 1e3, "alg_bytes": byts[op], "gbs": gbs, "frac": gbs / peak,
-                         "gflops": (2 * nnz * BATCH / (op_ms[op] / 1e3) / 1e9) if op != "restructure" else None}
+                         "gflops": (flops / (op_ms[op] / 1e3) / 1e9) if flops else None}
     dominant = max(ops, key=lambda o: op_ms[o])
     roofline = {"bound": "hbm", "achieved": op_report[dominant]["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": op_report[dominant]["gbs"] / peak, "traffic": profiled_traffic(dominant),
@@ -397,7 +406,7 @@ def run_ours(args):
     e2e = {"value": world * step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    launches_per_step = 3 + 3 + 4 + restructure_launches()
+    launches_per_step = 3 + 5 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: colsum, 2 transposes, tiles, fixup
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -419,12 +428,12 @@ def run_ours(args):
 
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
-    select = 1 + 4 * 2
+    select = 1 + 4 + 1  # init, four digit histograms, final pick
     keep_scan = 3
-    draw_chunk = 1 + 3
-    sort_grown = 4 * (1 + 3 + 1)  # positions < 2^28: four 8-bit passes
-    merge = 2
-    plan = (1 + 3) + 1 + (1 + 3) + 1 + 1 + 2 * (1 + 3 + 1) + 1
+    draw_chunk = 1 + 1 + 3  # draws, accept flags, scan
+    sort_grown = 1 + 3 + 1 + 1  # bucket count, scan, fill, rank
+    merge = 2  # split points, merge
+    plan = 1 + 1 + 2 * (1 + 3 + 1) + 1 + 1  # row offsets, tiles, two radix passes, column offsets, tiles
     return select + keep_scan + draw_chunk + sort_grown + merge + plan
 
 
