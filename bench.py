@@ -426,6 +426,361 @@ def run_ours(args):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# Per-workload sweep (--configs): every op of every workload, cold and warm,
+# beside same-run cuBLAS dense and Dense+Mask comparators and the oracle.
+# ----------------------------------------------------------------------------
+
+L2_BYTES = 129 * 2**20
+NOMINAL_HBM_GBS = 8000.0
+# fp32 FMA peak from unit counts and clock: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz
+FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+ACT_BYTES = {"f32": 4, "bf16": 2}
+
+
+def _dev_tensor(a, dtype: str, dev):
+    import torch
+
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+class _Timer:
+    """CUDA-event timing of an enqueue function on one stream: median over reps,
+    cold (a read of 2x L2 before every rep) or warm (back-to-back reps)."""
+
+    def __init__(self, torch, stream, dev):
+        self.torch, self.s = torch, stream
+        self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def graph(self, fn):
+        """fn captured in a CUDA graph (returns its replay), or fn itself if capture fails."""
+        torch = self.torch
+        with torch.cuda.stream(self.s):
+            fn()
+            fn()
+        self.s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g, stream=self.s):
+                fn()
+        except Exception:
+            torch.cuda.synchronize()
+            return fn, False
+        return g.replay, True
+
+    def time(self, run, reps: int, cold: bool) -> float:
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(self.s):
+            for _ in range(3):
+                run()
+            # hold the stream for a few ms so the host queues every rep before the
+            # first one runs: the events then time the device, not launch latency
+            torch.cuda._sleep(int(2e6 + 1e5 * reps))
+            for e0, e1 in evs:
+                if cold:
+                    torch.sum(self.flush, dim=0, out=self.flush_out)
+                e0.record(self.s)
+                run()
+                e1.record(self.s)
+        self.s.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+
+
+def _oracle_us(oracle, lay, x64, dy64, op: str, budget_terms: float = 3e7) -> tuple:
+    """Oracle time of `op` on the layer: the whole layer when nnz*batch is small,
+    else the first rows holding about budget_terms terms, scaled by nnz."""
+    batch = x64.shape[0]
+    frac = min(1.0, budget_terms / max(1.0, lay.nnz * batch))
+    if frac >= 1.0:
+        sub, dys = lay, dy64
+    else:
+        per_row = np.cumsum(np.bincount(lay.row, minlength=lay.out_f))
+        nrows = max(1, min(lay.out_f, int(np.searchsorted(per_row, lay.nnz * frac)) + 1))
+        sub = sub_layer(lay, 0, nrows)
+        dys = np.ascontiguousarray(dy64[:, :nrows])
+    v64 = oracle.as_f64(sub.val, sub.val_dtype)
+    t0 = time.perf_counter()
+    if op == "fwd":
+        oracle.fwd(sub.out_f, sub.in_f, sub.row, sub.col, v64, x64, oracle.as_f64(sub.bias))
+    elif op == "dx":
+        oracle.dx(sub.out_f, sub.in_f, sub.row, sub.col, v64, dys)
+    elif op == "dw":
+        oracle.dw(sub.out_f, sub.in_f, sub.row, sub.col, x64, dys)
+    elif op == "restructure":
+        oracle.restructure(sub.out_f, sub.in_f, sub.row, sub.col, v64, int(PRUNE_FRAC * sub.nnz), 0, 0)
+    dt = time.perf_counter() - t0
+    scale = lay.nnz / max(1, sub.nnz)
+    return dt * scale * 1e6, (sub.nnz == lay.nnz)
+
+
+def _layer_rows(name, lay, batch, ours, dense, mask, oracle_t, peak, cores):
+    """Result records of one layer at one batch."""
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    c = wl.CONFIGS[name]
+    s_v, s_x = ACT_BYTES[lay.val_dtype], ACT_BYTES[c["act_dtype"]]
+    byts = alg_bytes(lay.nnz, batch, lay.out_f, lay.in_f, s_v=s_v, s_x=s_x)
+    out = []
+    for op, t in ours.items():
+        cold, warm, graphed = t
+        flops = {"fwd": 2, "dx": 2, "dw": 2, "bwd": 4}.get(op, 0) * lay.nnz * batch
+        gbs = byts[op] / (cold * 1e-6) / 1e9
+        rec = {"config": name, "layer": f"{lay.out_f}x{lay.in_f}", "nnz": lay.nnz, "batch": batch, "op": op,
+               "dtype": lay.val_dtype, "us_cold": cold, "us_warm": warm, "graph": graphed,
+               "alg_bytes": byts[op], "gbs": gbs, "frac_measured": gbs / peak, "frac_nominal": gbs / NOMINAL_HBM_GBS,
+               "gflops": flops / (cold * 1e-6) / 1e9 if flops else None,
+               "frac_fma": (flops / (cold * 1e-6) / 1e12 / FMA_PEAK_TFLOPS) if flops else None,
+               "dense_us": dense.get(op), "dense_mask_us": mask.get(op),
+               "oracle_us": oracle_t.get(op, (None, None))[0], "oracle_full": oracle_t.get(op, (None, None))[1],
+               "oracle_cores": cores}
+        out.append(rec)
+    return out
+
+
+def _bench_layer(torch, F, snack, timer, name, lay, batch, ops, reps, dev, oracle, cores):
+    """Times our ops and the two dense comparators on one layer and batch."""
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    c = wl.CONFIGS[name]
+    act = c["act_dtype"]
+    tdt = torch.float32 if act == "f32" else torch.bfloat16
+    acts = wl.make_acts(batch, lay.in_f, lay.out_f, act, seed=0)
+    row = torch.from_numpy(lay.row).to(dev)
+    col = torch.from_numpy(lay.col).to(dev)
+    val = _dev_tensor(lay.val, lay.val_dtype, dev)
+    bias = torch.from_numpy(lay.bias).to(dev)
+    x = _dev_tensor(acts.x, act, dev)
+    dy = _dev_tensor(acts.dy, act, dev)
+    L = snack.SparseLinear(lay.out_f, lay.in_f, row, col, val, bias, max_batch=batch, validate=True)
+    y = torch.empty((batch, lay.out_f), dtype=tdt, device=dev)
+    dx = torch.empty((batch, lay.in_f), dtype=tdt, device=dev)
+    dw = torch.empty(lay.nnz, dtype=torch.float32, device=dev)
+    db = torch.empty(lay.out_f, dtype=torch.float32, device=dev)
+    h, ws = L.handle, L.ws
+    fns = {"fwd": lambda: snack.snack_spmm_fwd(h, row, col, val, x, batch, bias, y, ws),
+           "dx": lambda: snack.snack_spmm_dx(h, row, col, val, dy, batch, dx, ws),
+           "dw": lambda: snack.snack_sddmm_dw(h, row, col, x, dy, batch, dw, db, ws),
+           "bwd": lambda: snack.snack_backward(h, row, col, val, x, dy, batch, dx, dw, db, ws)}
+    ours = {}
+    for op in ops:
+        run, graphed = timer.graph(fns[op])
+        ours[op] = (timer.time(run, reps, True), timer.time(run, reps, False), graphed)
+    if "restructure" in c["ops"]:
+        n_prune = int(PRUNE_FRAC * lay.nnz)
+        rws = torch.empty(snack.snack_restructure_workspace_size(h, n_prune), dtype=torch.uint8, device=dev)
+        bufs = [(row, col, val), (torch.empty_like(row), torch.empty_like(col), torch.empty_like(val))]
+        src = torch.empty_like(row)
+        state = {"cur": 0, "i": 0}
+
+        def restructure():
+            a, b = bufs[state["cur"]], bufs[1 - state["cur"]]
+            snack.snack_restructure(h, a[0], a[1], a[2], n_prune, 12345, state["i"], b[0], b[1], b[2], src, rws)
+            state["cur"] ^= 1
+            state["i"] += 1
+
+        rr = max(20, reps // 4)
+        ours["restructure"] = (timer.time(restructure, rr, True), timer.time(restructure, rr, False), False)
+        if state["cur"] == 1:  # back on the first buffers
+            restructure()
+    # comparators: dense W (cuBLAS via F.linear / matmul) and Dense+Mask (W*M materialised every call)
+    dense, mask = {}, {}
+    Wd = torch.zeros((lay.out_f, lay.in_f), dtype=tdt, device=dev)
+    Wd[row.long(), col.long()] = val.to(tdt)
+    M = torch.zeros_like(Wd)
+    M[row.long(), col.long()] = 1
+    bias_t = bias.to(tdt)
+    dfns = {"fwd": (lambda: F.linear(x, Wd, bias_t), lambda: F.linear(x, Wd * M, bias_t)),
+            "dx": (lambda: dy @ Wd, lambda: dy @ (Wd * M)),
+            "dw": (lambda: dy.t() @ x, lambda: (dy.t() @ x) * M),
+            "bwd": (lambda: (dy @ Wd, dy.t() @ x), lambda: (dy @ (Wd * M), (dy.t() @ x) * M))}
+    for op in ops:
+        for store, idx in ((dense, 0), (mask, 1)):
+            run, _ = timer.graph(dfns[op][idx])
+            store[op] = timer.time(run, reps, True)
+    del Wd, M
+    oracle_t = {}
+    if oracle is not None:
+        x64, dy64 = oracle.as_f64(acts.x, act), oracle.as_f64(acts.dy, act)
+        for op in list(ops) + (["restructure"] if "restructure" in c["ops"] else []):
+            if op != "bwd":
+                oracle_t[op] = _oracle_us(oracle, lay, x64, dy64, op)
+    L.close()
+    return ours, dense, mask, oracle_t
+
+
+def _c3_step(torch, F, snack, timer, reps, dev):
+    """Full sparse-MLP training step (768 -> 3072 GELU -> 768, 1024 tokens): time and
+    peak device memory for ours, dense and Dense+Mask."""
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    l1, l2 = wl.config_layer("c3", layer_index=0), wl.config_layer("c3", layer_index=1)
+    batch = 1024
+    x_np = wl.make_acts(batch, 768, 3072, "f32", seed=5).x
+    dy_np = wl.make_acts(batch, 3072, 768, "f32", seed=6).dy
+    keep = {}
+
+    def measure(setup, graph=False):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        step = setup()
+        torch.cuda.synchronize()
+        persistent = torch.cuda.memory_allocated(dev) - base
+        torch.cuda.reset_peak_memory_stats(dev)
+        with torch.cuda.stream(timer.s):
+            step()
+        timer.s.synchronize()
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        r = {"us_warm": timer.time(step, reps, False), "persistent_bytes": persistent, "peak_bytes": peak}
+        if graph:
+            run, ok = timer.graph(step)
+            r["us_graph"] = timer.time(run, reps, False) if ok else None
+        return r
+
+    def ours_setup():
+        t = {}
+        for i, lay in enumerate((l1, l2)):
+            row = torch.from_numpy(lay.row).to(dev)
+            col = torch.from_numpy(lay.col).to(dev)
+            val = torch.from_numpy(lay.val).to(dev)
+            t[i] = snack.SparseLinear(lay.out_f, lay.in_f, row, col, val, torch.from_numpy(lay.bias).to(dev),
+                                      max_batch=batch)
+        t["x"] = torch.from_numpy(x_np).to(dev)
+        t["dy2"] = torch.from_numpy(dy_np).to(dev)
+
+        def step():
+            L1, L2 = t[0], t[1]
+            hh, pre = L1.forward_gelu(t["x"])
+            L2.forward(hh)
+            dy1 = L2.grad_input_gelu(t["dy2"], pre)
+            L2.grad_weight(hh, t["dy2"])
+            L1.backward(t["x"], dy1)
+
+        keep["ours"] = t
+        return step
+
+    def dense_setup(masked):
+        def setup():
+            ws = []
+            for lay in (l1, l2):
+                W = torch.zeros((lay.out_f, lay.in_f), device=dev)
+                W[torch.from_numpy(lay.row).to(dev).long(), torch.from_numpy(lay.col).to(dev).long()] = \
+                    torch.from_numpy(lay.val).to(dev)
+                M = (W != 0).float() if masked else None
+                ws.append((W.requires_grad_(True), M, torch.zeros(lay.out_f, device=dev, requires_grad=True)))
+            x = torch.from_numpy(x_np).to(dev).requires_grad_(True)
+            dy2 = torch.from_numpy(dy_np).to(dev)
+
+            def step():
+                (W1, M1, b1), (W2, M2, b2) = ws
+                hh = F.gelu(F.linear(x, W1 * M1 if masked else W1, b1))
+                y2 = F.linear(hh, W2 * M2 if masked else W2, b2)
+                y2.backward(dy2)
+                for p in (x, W1, W2, b1, b2):
+                    p.grad = None
+
+            keep["dense"] = (ws, x, dy2)
+            return step
+
+        return setup
+
+    res = {"ours": measure(ours_setup, graph=True)}
+    keep["ours"][0].close()
+    keep["ours"][1].close()
+    keep.clear()
+    res["dense"] = measure(dense_setup(False))
+    keep.clear()
+    res["dense_mask"] = measure(dense_setup(True))
+    keep.clear()
+    return res
+
+
+def run_configs(args):
+    import torch
+    import torch.nn.functional as F
+
+    from spmm_row_sorted_gb300 import build as snack_build
+    from spmm_row_sorted_gb300 import snack
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.backends.cuda.matmul.allow_tf32 = False
+    torch.backends.cudnn.allow_tf32 = False
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    snack_build.build()
+    snack.load()
+    peak, peak_kind = measured_peak_gbs()
+    oracle, cores = None, None
+    if not args.no_cpu_baseline:
+        import oracle as _oracle
+
+        oracle = _oracle
+        cores = os.cpu_count() or 1
+        oracle.set_threads(cores)
+    timer = _Timer(torch, torch.cuda.Stream(device=dev), dev)
+    names = args.configs.split(",") if args.configs != "all" else list(wl.CONFIGS)
+    records = []
+    with ClockSampler(0) as clk:
+        for name in names:
+            c = wl.CONFIGS[name]
+            layers = [wl.config_layer(name, layer_index=i) for i in range(len(c.get("layers", [None])))]
+            ops = ["fwd"] if c["ops"] == ("fwd",) else ["fwd", "dx", "dw", "bwd"]
+            for lay in layers:
+                for batch in c["batches"]:
+                    ours, dense, mask, ot = _bench_layer(torch, F, snack, timer, name, lay, batch, ops, args.reps,
+                                                         dev, oracle, cores)
+                    for rec in _layer_rows(name, lay, batch, ours, dense, mask, ot, peak, cores):
+                        records.append(rec)
+                        print(json.dumps(rec), flush=True)
+            if name == "c3":
+                rec = {"config": "c3", "op": "mlp_step", **_c3_step(torch, F, snack, timer, max(20, args.reps // 4),
+                                                                     dev)}
+                records.append(rec)
+                print(json.dumps(rec), flush=True)
+    clocks = clk.summary()
+    print(json.dumps({"clocks": clocks, "peak_gbs": peak, "peak_kind": peak_kind}), flush=True)
+    if args.configs_out:
+        with open(args.configs_out, "w") as f:
+            f.write(_configs_markdown(records, clocks, peak, peak_kind, cores))
+    return 0
+
+
+def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
+    def f(v, nd=1):
+        return "—" if v is None else f"{v:,.{nd}f}"
+
+    lines = ["| config | layer | batch | op | µs cold | µs warm | alg. MB | GB/s | % HBM (measured) | % of 8 TB/s | "
+             "GFLOP/s | cuBLAS dense µs | Dense+Mask µs | oracle µs |",
+             "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
+    step = None
+    for r in records:
+        if r.get("op") == "mlp_step":
+            step = r
+            continue
+        orc = f(r["oracle_us"], 0) + ("" if r["oracle_full"] in (None, True) else " (sampled)")
+        lines.append(f"| {r['config']} | {r['layer']} | {r['batch']} | {r['op']} | {f(r['us_cold'])} | "
+                     f"{f(r['us_warm'])} | {f(r['alg_bytes'] / 1e6, 2)} | {f(r['gbs'], 0)} | "
+                     f"{f(100 * r['frac_measured'])} | {f(100 * r['frac_nominal'])} | {f(r['gflops'], 0)} | "
+                     f"{f(r['dense_us'])} | {f(r['dense_mask_us'])} | {orc} |")
+    out = "\n".join(lines) + "\n"
+    if step:
+        out += ("\n| c3 MLP training step (both layers, fwd + dX + dW) | µs (warm, eager) | µs (CUDA graph) | "
+                "persistent MB | peak MB |\n|---|---|---|---|---|\n")
+        for k in ("ours", "dense", "dense_mask"):
+            v = step[k]
+            out += (f"| {k} | {f(v['us_warm'])} | {f(v.get('us_graph'))} | {f(v['persistent_bytes'] / 1e6, 2)} | "
+                    f"{f(v['peak_bytes'] / 1e6, 2)} |\n")
+    out += (f"\nPeak HBM {peak:,.0f} GB/s ({peak_kind}); fp32 FMA peak {FMA_PEAK_TFLOPS:.1f} TFLOP/s (units x clock); "
+            f"oracle on {cores} host threads; clocks {json.dumps(clocks)}\n")
+    return out
+
+
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
     select = 1 + 4 + 1  # init, four digit histograms, final pick
@@ -447,6 +802,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds-total", type=float, default=120.0,
                     help="--impl reference: oracle time budget over all steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default=None,
+                    help="per-workload sweep instead of the step bench: 'all' or a list like c1,c4")
+    ap.add_argument("--configs-out", default=None, help="--configs: also write a markdown table here")
+    ap.add_argument("--reps", type=int, default=200, help="--configs: timed reps per op")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps untimed on one layer copy and exit (for ncu captures)")
     args = ap.parse_args(argv)
@@ -454,6 +813,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_ours(args)
 
 
