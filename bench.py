@@ -783,7 +783,7 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
-    select = 1 + 4 + 1  # init, four digit histograms, final pick
+    select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
     keep_scan = 3
     draw_chunk = 1 + 1 + 3  # draws, accept flags, scan
     sort_grown = 1 + 3 + 1 + 1  # bucket count, scan, fill, rank

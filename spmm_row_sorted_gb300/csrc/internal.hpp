@@ -26,7 +26,7 @@ struct PlanLayout {
   TileGeom gf, gt;
 };
 
-PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max);
+PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles);
 PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
@@ -53,6 +53,8 @@ struct RestructureArgs {
   int32_t *row_out, *col_out;
   void *val_out;
   int32_t *src_out;  // may be null
+  uint32_t *host_counts;  // pinned host memory, 2 words: a draw chunk's accepted count and overflow flag
+  cudaEvent_t counts_ready;  // recorded after the copy into host_counts
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
@@ -78,4 +80,6 @@ struct snack_layer {
   snack::PlanPtrs p;
   size_t plan_bytes;
   int num_sms;
+  uint32_t *host_counts = nullptr;  // restructure read-back (pinned), made on first use
+  cudaEvent_t counts_ready = nullptr;
 };

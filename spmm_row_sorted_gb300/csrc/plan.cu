@@ -154,10 +154,10 @@ cudaError_t build_offsets(const int32_t *idx, int64_t nnz, int32_t n, int32_t *p
 
 }  // namespace
 
-PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max) {
+PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles) {
   PlanLayout L;
-  L.gf = tile_geom(out_f, nnz, bt_max);
-  L.gt = tile_geom(in_f, nnz, bt_max);
+  L.gf = tile_geom(out_f, nnz, bt_max, n_btiles);
+  L.gt = tile_geom(in_f, nnz, bt_max, n_btiles);
   size_t o = 0;
   L.off_rp = o;
   o += align_up(sizeof(int32_t) * ((size_t)out_f + 1), kAlign);

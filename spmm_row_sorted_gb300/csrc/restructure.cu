@@ -1,9 +1,9 @@
 // Dynamic Sparse Training restructure on the GPU (prune smallest |w|, regrow
 // at random empty positions with value +0, re-sort the COO).
 //
-//  1. prune set: radix select (8-bit digits, high to low) of the n_prune-th
-//     smallest magnitude key t; ties at t are pruned in storage order, so the
-//     pruned set is exactly the n_prune smallest (|w|, k);
+//  1. prune set: radix select (digits of 11, 10 and 10 bits, high to low) of
+//     the n_prune-th smallest magnitude key t; ties at t are pruned in
+//     storage order, so the pruned set is exactly the n_prune smallest (|w|, k);
 //  2. survivors: one scan of the packed pair (key > t, key == t) gives every
 //     survivor its output slot (stable compaction);
 //  3. regrow: draws i of SplitMix64 map to positions by multiply-high; a draw
@@ -12,8 +12,9 @@
 //     hash table keeps the minimum draw index per position (atomicMin, so the
 //     outcome does not depend on thread order); a scan over draw order keeps
 //     the first n_prune accepted.  Draws run in chunks until enough are
-//     accepted (one host read-back per chunk);
-//  4. regrown positions are radix sorted and merged with the survivors by
+//     accepted; the first chunk is queued before steps 1 and 2 and the host
+//     reads its count back while the device runs them;
+//  4. regrown positions are bucket sorted and merged with the survivors by
 //     position (merge path), writing row/col/val/src.
 // Every step is integer work, so the output is bit-exact with the sequential
 // definition.
@@ -33,8 +34,10 @@ constexpr int kMergeTile = kMergeThreads * kMergeItems;
 
 struct SelState {
   uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
-  uint32_t overflow, pad[3];                   // overflow: a draw found the position table full
-  uint32_t hist[4][256];                       // one histogram per 8-bit digit, high digit first
+  uint32_t overflow;                           // a draw found the position table full
+  uint32_t pfx, mask, rem;                     // select progress: digits fixed so far, ranks left within them
+  uint32_t arrive[4];                          // blocks finished per pass
+  uint32_t hist0[2048], hist1[1024], hist2[1024];  // digit histograms: key bits 30..20, 19..10, 9..0
 };
 
 __device__ __forceinline__ uint32_t canon_mag(uint32_t m) { return m > 0x7F800000u ? 0x7F800001u : m; }
@@ -51,116 +54,107 @@ __device__ __forceinline__ uint32_t mag_key<bf16>(const bf16 *val, int64_t k) {
   return canon_mag((b & 0x7FFFu) << 16);
 }
 
-// One warp: the digit d of `hist` where the running count first reaches rem,
-// and the count of smaller digits.
-__device__ void warp_pick(const uint32_t *hist, uint32_t rem, uint32_t *digit, uint32_t *before) {
-  const int lane = threadIdx.x & 31;
-  uint32_t h[8], sum = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    h[i] = hist[lane * 8 + i];
-    sum += h[i];
-  }
-  uint32_t inc = sum;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    uint32_t u = __shfl_up_sync(0xffffffffu, inc, d);
-    if (lane >= d) inc += u;
-  }
-  const uint32_t ex = inc - sum;
-  const unsigned hit = __ballot_sync(0xffffffffu, inc >= rem && ex < rem);
-  const int src = hit ? __ffs(hit) - 1 : 31;
-  uint32_t dg = 255, bf = 0;
-  if (lane == src) {
-    uint32_t c = ex;
-    dg = lane * 8 + 7;
-    bf = c;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (c + h[i] >= rem) {
-        dg = lane * 8 + i;
-        bf = c;
-        break;
-      }
-      c += h[i];
-    }
-  }
-  *digit = __shfl_sync(0xffffffffu, dg, src);
-  *before = __shfl_sync(0xffffffffu, bf, src);
-}
+template <int kPass>
+struct SelDigit {
+  static constexpr int kShift = kPass == 0 ? 20 : (kPass == 1 ? 10 : 0);
+  static constexpr int kBins = kPass == 0 ? 2048 : 1024;
+};
 
-// prefix / mask / remaining after `passes` digits (one warp)
-__device__ void warp_replay(const SelState *st, int passes, uint32_t *prefix, uint32_t *mask, uint32_t *rem) {
-  uint32_t p = 0, m = 0, r = st->n_prune;
-  for (int q = 0; q < passes; ++q) {
-    uint32_t d, bf;
-    warp_pick(st->hist[q], r, &d, &bf);
-    const int shift = 24 - 8 * q;
-    p |= d << shift;
-    m |= 0xFFu << shift;
-    r -= bf;
-  }
-  *prefix = p;
-  *mask = m;
-  *rem = r;
-}
-
-template <typename TV>
-__global__ void __launch_bounds__(256) k_sel_hist(const TV *__restrict__ val, int64_t nnz, SelState *st, int pass) {
+// One pass of the radix select over the 31-bit magnitude keys (digits of 11,
+// 10 and 10 bits, high first).  Every block histograms the digit of the keys
+// that match the digits fixed so far, adds its counts to the global
+// histogram, and the last block to finish picks the digit holding rank
+// `rem` (no extra launch, no waiting: the last arrival does the pick).
+template <typename TV, int kPass>
+__global__ void __launch_bounds__(256) k_sel_pass(const TV *__restrict__ val, int64_t nnz, SelState *st) {
   constexpr int kItems = 16;
-  __shared__ uint32_t h[256];
-  __shared__ uint32_t s_prefix, s_mask;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
-  const int shift = 24 - 8 * pass;
+  constexpr int kShift = SelDigit<kPass>::kShift, kBins = SelDigit<kPass>::kBins, kPer = kBins / 256;
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t s_scan[256];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // the first chunk of keys is loaded before the previous digits are replayed,
-  // so the replay's global reads overlap the loads
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + tid;
   uint32_t key[kItems];
 #pragma unroll
   for (int u = 0; u < kItems; ++u) key[u] = first + u * stride < nnz ? mag_key<TV>(val, first + u * stride) : 0u;
-  if (threadIdx.x < 32) {
-    uint32_t p, m, r;
-    warp_replay(st, pass, &p, &m, &r);
-    if (threadIdx.x == 0) {
-      s_prefix = p;
-      s_mask = m;
-    }
-  }
+  for (int i = tid; i < kBins; i += 256) h[i] = 0;
+  const uint32_t pfx = kPass ? st->pfx : 0u, mask = kPass ? st->mask : 0u;
   __syncthreads();
-  const uint32_t prefix = s_prefix, mask = s_mask;
 #pragma unroll
   for (int u = 0; u < kItems; ++u)
-    if (first + u * stride < nnz && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> shift) & 0xFFu], 1u);
+    if (first + u * stride < nnz && (key[u] & mask) == pfx) atomicAdd(&h[(key[u] >> kShift) & (kBins - 1)], 1u);
   for (int64_t k0 = first + kItems * stride; k0 < nnz; k0 += kItems * stride) {
 #pragma unroll
     for (int u = 0; u < kItems; ++u) key[u] = k0 + u * stride < nnz ? mag_key<TV>(val, k0 + u * stride) : 0u;
 #pragma unroll
     for (int u = 0; u < kItems; ++u)
-      if (k0 + u * stride < nnz && (key[u] & mask) == prefix) atomicAdd(&h[(key[u] >> shift) & 0xFFu], 1u);
+      if (k0 + u * stride < nnz && (key[u] & mask) == pfx) atomicAdd(&h[(key[u] >> kShift) & (kBins - 1)], 1u);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    if (h[i]) atomicAdd(&st->hist[pass][i], h[i]);
-}
-
-__global__ void k_sel_final(SelState *st) {
-  uint32_t p, m, r;
-  warp_replay(st, 4, &p, &m, &r);
-  if (threadIdx.x == 0) {
-    st->prefix = p;
-    st->remaining = r;
+  uint32_t *gh = kPass == 0 ? st->hist0 : (kPass == 1 ? st->hist1 : st->hist2);
+  for (int i = tid; i < kBins; i += 256)
+    if (h[i]) atomicAdd(&gh[i], h[i]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&st->arrive[kPass], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last block: exclusive scan of the global histogram, then the digit d at
+  // which the running count first reaches rem
+  const uint32_t rem = kPass ? st->rem : st->n_prune;
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    c[j] = __ldcg(&gh[tid * kPer + j]);
+    sum += c[j];
+  }
+  s_scan[tid] = sum;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    uint32_t v = tid >= off ? s_scan[tid - off] : 0u;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  uint32_t ex = s_scan[tid] - sum;
+  if (ex < rem && ex + sum >= rem) {
+#pragma unroll 1
+    for (int j = 0; j < kPer; ++j) {
+      if (ex + c[j] >= rem) {
+        const uint32_t d = (uint32_t)(tid * kPer + j);
+        const uint32_t np = pfx | (d << kShift), nm = mask | ((uint32_t)(kBins - 1) << kShift);
+        st->pfx = np;
+        st->mask = nm;
+        st->rem = rem - ex;
+        if (kPass == 2) {
+          st->prefix = np;
+          st->remaining = rem - ex;
+        }
+        break;
+      }
+      ex += c[j];
+    }
   }
 }
 
 __global__ void k_sel_init(SelState *st, uint32_t n_prune) {
-  for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&st->hist[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < 2048; i += blockDim.x) st->hist0[i] = 0;
+  for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
+    st->hist1[i] = 0;
+    st->hist2[i] = 0;
+  }
+  if (threadIdx.x < 4) st->arrive[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     st->prefix = 0;
     st->remaining = 0;
     st->n_prune = n_prune;
     st->total = 0;
     st->overflow = 0;
+    st->pfx = 0;
+    st->mask = 0;
+    st->rem = n_prune;
   }
 }
 
@@ -483,46 +477,59 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     if (e != cudaSuccess) return SNACK_ERR_CUDA; \
   } while (0)
 
-  // 1. prune threshold: four 8-bit digit passes, high to low
+  // The draws depend only on the old pattern, so they go first: the first
+  // chunk's accepted count is copied to pinned host memory, the prune select
+  // and the survivor scan are queued behind it, and the host waits only for
+  // that copy while the device goes on with the select.
   k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
+  SNACK_TRY(cudaGetLastError());
+  const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
+  const double empty = (double)n_pos - (double)nnz;
+  int64_t done = 0, acc = 0;
+  uint32_t *d_counts = &st->total;  // total, overflow: adjacent words
+  auto draw_chunk = [&](int64_t m) -> cudaError_t {
+    k_draw<<<grid_for(m, 256), 256, 0, s>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
+                                            hkeys, hmin, (uint64_t)(W.cap - 1), &st->overflow);
+    k_accept_flags<<<grid_for(m, 256), 256, 0, s>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
+                                                    flags);
+    cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
+                                              d_counts, stemp, s);
+    if (err != cudaSuccess) return err;
+    err = cudaMemcpyAsync(a.host_counts, d_counts, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) return err;
+    return cudaEventRecord(a.counts_ready, s);
+  };
+  auto chunk_size = [&]() -> int64_t {
+    double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
+    int64_t m = (int64_t)ceil(want);
+    return m > W.d_max - done ? W.d_max - done : m;
+  };
+  int64_t m = 0;
   if (n_prune > 0) {
-    for (int pass = 0; pass < 4; ++pass)
-      k_sel_hist<TV><<<grid_for((nnz + 15) / 16, 256, 1184), 256, 0, s>>>(val, nnz, st, pass);
-    k_sel_final<<<1, 32, 0, s>>>(st);
+    SNACK_TRY(cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s));
+    SNACK_TRY(cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s));
+    m = chunk_size();
+    SNACK_TRY(draw_chunk(m));
+    // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
+    const unsigned g = grid_for((nnz + 15) / 16, 256, 1184);
+    k_sel_pass<TV, 0><<<g, 256, 0, s>>>(val, nnz, st);
+    k_sel_pass<TV, 1><<<g, 256, 0, s>>>(val, nnz, st);
+    k_sel_pass<TV, 2><<<g, 256, 0, s>>>(val, nnz, st);
   }
   SNACK_TRY(cudaGetLastError());
   // 2. survivors
   SNACK_TRY(scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, a.in_f}, nnz,
                                     KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s));
-  // 3. regrow
-  if (n_prune > 0) {
-    SNACK_TRY(cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s));
-    SNACK_TRY(cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s));
-    const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
-    const double empty = (double)n_pos - (double)nnz;
-    int64_t done = 0, acc = 0;
-    uint32_t *d_total = &st->total;
-    uint32_t *d_overflow = &st->overflow;
-    while (acc < n_prune) {
-      if (done >= W.d_max) return SNACK_ERR_NO_SPACE;
-      double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
-      int64_t m = (int64_t)ceil(want);
-      if (m > W.d_max - done) m = W.d_max - done;
-      k_draw<<<grid_for(m, 256), 256, 0, s>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
-                                              hkeys, hmin, (uint64_t)(W.cap - 1), d_overflow);
-      SNACK_TRY(cudaGetLastError());
-      k_accept_flags<<<grid_for(m, 256), 256, 0, s>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
-                                                      flags);
-      SNACK_TRY(scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
-                                        d_total, stemp, s));
-      uint32_t h_total = 0, h_over = 0;
-      SNACK_TRY(cudaMemcpyAsync(&h_total, d_total, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
-      SNACK_TRY(cudaMemcpyAsync(&h_over, d_overflow, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
-      SNACK_TRY(cudaStreamSynchronize(s));
-      if (h_over) return SNACK_ERR_WORKSPACE;
-      acc += h_total;
-      done += m;
-    }
+  // 3. regrow: further chunks only when the first fell short (rare)
+  while (n_prune > 0) {
+    SNACK_TRY(cudaEventSynchronize(a.counts_ready));
+    if (a.host_counts[1]) return SNACK_ERR_WORKSPACE;
+    acc += a.host_counts[0];
+    done += m;
+    if (acc >= n_prune) break;
+    if (done >= W.d_max) return SNACK_ERR_NO_SPACE;
+    m = chunk_size();
+    SNACK_TRY(draw_chunk(m));
   }
   // 4. sort regrown positions (bucket sort: they are uniform over the empty
   //    positions), merge with survivors

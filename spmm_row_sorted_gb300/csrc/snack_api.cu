@@ -203,8 +203,10 @@ snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, cons
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   const T *xt = reinterpret_cast<const T *>(x);
   const T *dyt = reinterpret_cast<const T *>(dy);
-  if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
-  if (h->nnz == 0) return SNACK_OK;
+  if (h->nnz == 0) {
+    if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
+    return SNACK_OK;
+  }
   if (batch > 1) {
     T *a = reinterpret_cast<T *>(b + W.xt);
     T *c = reinterpret_cast<T *>(b + W.dyt);
@@ -213,6 +215,8 @@ snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, cons
     xt = a;
     dyt = c;
   }
+  // db from the feature-major dY (contiguous per output feature)
+  if (db) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
   SNACK_CUDA(run_sddmm<T>(h->nnz, row, col, h->out_f, h->in_f, xt, dyt, bg, dw, h->num_sms, s));
   return SNACK_OK;
 }
@@ -234,7 +238,6 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   const T *dyt = reinterpret_cast<const T *>(dy);
   const T *xt = reinterpret_cast<const T *>(x);
-  if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
   if (batch > 1) {
     T *a = reinterpret_cast<T *>(b + W.dyt);
     T *c = reinterpret_cast<T *>(b + W.xt);
@@ -243,6 +246,7 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
     dyt = a;
     xt = c;
   }
+  if (db) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
   SpmmParams p;
   p.n_rows = h->in_f;
   p.n_src = h->out_f;
@@ -283,7 +287,8 @@ snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t
                                snack_dtype act_t, size_t *plan_bytes, size_t *workspace_bytes) {
   snack_status st = check_shape(out_f, in_f, nnz, max_batch, val_t, act_t);
   if (st != SNACK_OK) return st;
-  PlanLayout lay = plan_layout(out_f, in_f, nnz, batch_geom(max_batch, act_t).bt);
+  const BatchGeom mbg = batch_geom(max_batch, act_t);
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles);
   if (plan_bytes) *plan_bytes = lay.total;
   if (workspace_bytes) {
     size_t a = ops_ws_bytes(out_f, in_f, max_batch, act_t, lay);
@@ -302,7 +307,8 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   if (st != SNACK_OK) return st;
   if (nnz > 0 && (!row || !col)) return SNACK_ERR_INVALID_ARG;
   if (!plan || !aligned(plan, kAlign) || !ws || !aligned(ws, kAlign)) return SNACK_ERR_INVALID_ARG;
-  PlanLayout lay = plan_layout(out_f, in_f, nnz, batch_geom(max_batch, act_t).bt);
+  const BatchGeom mbg = batch_geom(max_batch, act_t);
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles);
   if (plan_bytes < lay.total) return SNACK_ERR_WORKSPACE;
   if (ws_bytes < plan_build_ws_bytes(out_f, in_f, nnz)) return SNACK_ERR_WORKSPACE;
   int dev = 0;
@@ -497,13 +503,33 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.col_out = col_out;
   a.val_out = val_out;
   a.src_out = src_out;
+  if (!h->host_counts) {
+    void *hp = nullptr;
+    if (cudaHostAlloc(&hp, 2 * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) return SNACK_ERR_CUDA;
+    h->host_counts = reinterpret_cast<uint32_t *>(hp);
+  }
+  if (!h->counts_ready && cudaEventCreateWithFlags(&h->counts_ready, cudaEventDisableTiming) != cudaSuccess)
+    return SNACK_ERR_CUDA;
+  a.host_counts = h->host_counts;
+  a.counts_ready = h->counts_ready;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, true));
   return SNACK_OK;
 }
 
-void snack_destroy(snack_handle h) { delete h; }
+void snack_destroy(snack_handle h) {
+  if (!h) return;
+  if (h->counts_ready) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(h->device);
+    cudaEventDestroy(h->counts_ready);
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+  if (h->host_counts) cudaFreeHost(h->host_counts);
+  delete h;
+}
 
 const char *snack_status_string(snack_status st) {
   switch (st) {

@@ -78,19 +78,34 @@ struct TileGeom {
   int32_t max_rows;       // rows a tile can touch, partial rows included
 };
 
-inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max) {
+inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max, int n_btiles = 1) {
   TileGeom t;
   int c = 32768 / (bt_max > 0 ? bt_max : 1);
   if (c < 512) c = 512;
   if (c > 8192) c = 8192;
-  t.cost_per_tile = c;
   // keep the staged rows of a tile within ~16 KB of shared memory
   int rows_target = 16384 / ((bt_max + 1) * 4);
   if (rows_target < 16) rows_target = 16;
-  int w = (c + rows_target - 1) / rows_target;
-  if (w < 2) w = 2;
-  t.row_weight = w;
+  auto weight = [&](int cost) {
+    int w = (cost + rows_target - 1) / rows_target;
+    return w < 2 ? 2 : w;
+  };
+  int w = weight(c);
   int64_t total = (int64_t)w * n_rows + nnz;
+  // small layers: smaller tiles (down to 128 cost units) until the grid has
+  // about 1024 CTAs, so the work still spreads over every SM
+  const int64_t want = 1024 / (n_btiles > 0 ? n_btiles : 1) + 1;
+  if ((total + c - 1) / c < want) {
+    int64_t c2 = (total + want - 1) / want;
+    if (c2 < 128) c2 = 128;
+    if (c2 < c) {
+      c = (int)c2;
+      w = weight(c);
+      total = (int64_t)w * n_rows + nnz;
+    }
+  }
+  t.cost_per_tile = c;
+  t.row_weight = w;
   int64_t nt = (total + c - 1) / c;
   t.n_tiles = (int32_t)(nt > 0 ? nt : 1);
   t.max_rows = (c + w - 1) / w + 2;
@@ -416,6 +431,23 @@ __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__res
   out[c] = s;
 }
 
+// out[r] = sum_b at[r][b] over the feature-major copy (rows ldx apart): one
+// warp per row, lane-strided partial sums combined by a fixed shuffle tree,
+// so the result does not depend on scheduling.
+template <typename T>
+__global__ void __launch_bounds__(256) k_rowsum_t(const T *__restrict__ at, int ldx, int batch, int n,
+                                                  float *__restrict__ out) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const T *p = at + (size_t)r * ldx;
+  float s = 0.f;
+#pragma unroll 4
+  for (int b = lane; b < batch; b += 32) s += to_f32(p[b]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) out[r] = s;
+}
+
 // dw[k] = sum_b dyt[row[k]][b] * xt[col[k]][b].  One CTA per chunk of at
 // most kDwChunk stored weights (fewer for wide batches, so the grid still
 // fills the GPU): indices staged in shared memory, results gathered in shared
@@ -586,6 +618,12 @@ cudaError_t launch_colsum(const T *a, int batch, int n, float *out, cudaStream_t
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s) {
+  k_rowsum_t<T><<<(n + 7) / 8, 256, 0, s>>>(at, ldx, batch, n, out);
+  return cudaGetLastError();
+}
+
 // per-dtype entry points (explicitly instantiated in spmm_f32.cu / spmm_bf16.cu)
 // gather_val: column-view mode (input gradient); fuse_dw: also the weight
 // gradient (column-view mode with a single batch tile only)
@@ -598,5 +636,7 @@ template <typename T>
 cudaError_t run_transpose(const T *a, int batch, int n, T *at, int ldx, cudaStream_t s);
 template <typename T>
 cudaError_t run_colsum(const T *a, int batch, int n, float *out, cudaStream_t s);
+template <typename T>
+cudaError_t run_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s);
 
 }  // namespace snack

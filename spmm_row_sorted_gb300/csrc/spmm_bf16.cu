@@ -27,4 +27,9 @@ cudaError_t run_colsum<bf16>(const bf16 *a, int batch, int n, float *out, cudaSt
   return launch_colsum<bf16>(a, batch, n, out, s);
 }
 
+template <>
+cudaError_t run_rowsum_t<bf16>(const bf16 *at, int ldx, int batch, int n, float *out, cudaStream_t s) {
+  return launch_rowsum_t<bf16>(at, ldx, batch, n, out, s);
+}
+
 }  // namespace snack

@@ -27,4 +27,9 @@ cudaError_t run_colsum<float>(const float *a, int batch, int n, float *out, cuda
   return launch_colsum<float>(a, batch, n, out, s);
 }
 
+template <>
+cudaError_t run_rowsum_t<float>(const float *at, int ldx, int batch, int n, float *out, cudaStream_t s) {
+  return launch_rowsum_t<float>(at, ldx, batch, n, out, s);
+}
+
 }  // namespace snack
