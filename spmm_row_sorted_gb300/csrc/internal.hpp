@@ -30,12 +30,12 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
 PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
-// Fill the plan for the pattern (row, col).  Asynchronous on s.  rows_sorted
-// says the rows are known to be non-decreasing (a restructure's own output),
-// which allows the one-pass row offsets.
+// Fill the plan for the pattern (row, col).  Asynchronous on s.  rp_ready
+// says the row offsets p.rp are already in place (a restructure's merge
+// writes them).
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       bool rows_sorted);
+                       bool rp_ready);
 
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
@@ -50,6 +50,8 @@ struct RestructureArgs {
   const int32_t *row, *col;
   const void *val;
   const int32_t *rp_old;  // row offsets of the input pattern (from the plan)
+  int32_t *rp_new;        // row offsets of the output, written by the merge (may alias rp_old: the
+                          // draws that read rp_old are ordered before the merge on the stream)
   int32_t *row_out, *col_out;
   void *val_out;
   int32_t *src_out;  // may be null

@@ -225,17 +225,15 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz) { return bu
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       bool rows_sorted) {
+                       bool rp_ready) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
   void *stemp = b + W.scan;
   cudaError_t e;
 
-  // row offsets: one pass for a restructure's sorted output, counts otherwise
-  if (rows_sorted) {
-    k_offsets_sorted<int32_t><<<grid_for(nnz + 1, 256), 256, 0, s>>>(row, nnz, out_f, p.rp);
-  } else {
+  // row offsets: already written by a restructure's merge, counts otherwise
+  if (!rp_ready) {
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
   }

@@ -1,7 +1,8 @@
 // Device-wide building blocks used by the plan builder and the restructure:
 //  * scan_apply: exclusive prefix sum over a generated sequence f(i), then a
 //    per-element callback out(i, exclusive, value) -- reduce-then-scan in
-//    three launches, no inter-block waiting;
+//    two launches (each second-pass block sums the tile totals before it),
+//    no inter-block waiting;
 //  * radix_sort: stable LSD radix sort of 32/64-bit keys with an optional
 //    32-bit payload, 8-bit digits, per-warp stable ranking via match_any.
 // All results are deterministic.
@@ -53,6 +54,19 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T *total) {
   return excl;
 }
 
+// One padding element per 128 bytes keeps the blocked read (thread t reads
+// elements 8t..8t+7) free of bank conflicts.
+template <typename T>
+__device__ __forceinline__ int scan_pad(int e) {
+  return e + e / (int)(128 / sizeof(T));
+}
+
+// Payload loaded with the scanned value (before the block scan), so the
+// callback's operands do not cost a second memory round trip.
+struct NoPayload {
+  __device__ int operator()(int64_t) const { return 0; }
+};
+
 template <typename T, typename F>
 __global__ void __launch_bounds__(kScanThreads) k_scan_reduce(F f, int64_t n, T *block_sums) {
   const int64_t base = (int64_t)blockIdx.x * kScanTile;
@@ -84,25 +98,20 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_spine(T *sums, int64_t nb
   if (threadIdx.x == 0 && total) *total = carry;
 }
 
-// One padding element per 128 bytes keeps the blocked read (thread t reads
-// elements 8t..8t+7) free of bank conflicts.
-template <typename T>
-__device__ __forceinline__ int scan_pad(int e) {
-  return e + e / (int)(128 / sizeof(T));
-}
+// Up to this many tiles, every block of the second pass adds up the sums of
+// the tiles before it itself (no spine launch).
+constexpr int64_t kScanDirectTiles = 2048;
 
-// Payload loaded with the scanned value (before the block scan), so the
-// callback's operands do not cost a second memory round trip.
-struct NoPayload {
-  __device__ int operator()(int64_t) const { return 0; }
-};
-
-template <typename T, typename F, typename PL, typename Out>
-__global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t n, const T *block_offs,
-                                                            Out out) {
+// Second pass: block b scans its tile and runs the callbacks.  kDirect: its
+// prefix is the sum of block_sums[0..b) (and the last block writes the
+// total); otherwise block_sums already holds exclusive prefixes.
+template <typename T, bool kDirect, typename F, typename PL, typename Out>
+__global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t n, const T *block_sums, Out out,
+                                                            T *d_total) {
   constexpr int kPadded = kScanTile + kScanTile / (128 / sizeof(T));
   __shared__ T tile[kPadded];
   __shared__ T tile_ex[kPadded];
+  __shared__ T tot, pre_tot;
   const int64_t base = (int64_t)blockIdx.x * kScanTile;
   T in[kScanItems];
   decltype(pl(0)) pay[kScanItems];
@@ -112,18 +121,27 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t 
     in[i] = idx < n ? f(idx) : T(0);
     pay[i] = idx < n ? pl(idx) : decltype(pl(0))();
   }
+  T prefix;
+  if (kDirect) {
+    T ps = 0;
+    for (int64_t q = threadIdx.x; q < (int64_t)blockIdx.x; q += kScanThreads) ps += block_sums[q];
+    T ignored = block_exclusive_scan<T>(ps, &pre_tot);
+    (void)ignored;
+    prefix = pre_tot;
+  } else {
+    prefix = block_sums[blockIdx.x];
+  }
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) tile[scan_pad<T>(i * kScanThreads + threadIdx.x)] = in[i];
   __syncthreads();
   T v[kScanItems];
-  T s = 0;
+  T sum = 0;
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
     v[i] = tile[scan_pad<T>(threadIdx.x * kScanItems + i)];
-    s += v[i];
+    sum += v[i];
   }
-  __shared__ T tot;
-  T ex = block_exclusive_scan<T>(s, &tot) + block_offs[blockIdx.x];
+  T ex = block_exclusive_scan<T>(sum, &tot) + prefix;
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
     tile_ex[scan_pad<T>(threadIdx.x * kScanItems + i)] = ex;
@@ -137,6 +155,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t 
     const int64_t idx = base + e;
     if (idx < n) out(idx, tile_ex[scan_pad<T>(e)], in[i], pay[i]);
   }
+  if (kDirect && d_total && threadIdx.x == 0 && blockIdx.x == gridDim.x - 1) *d_total = prefix + tot;
 }
 
 template <typename T>
@@ -147,18 +166,23 @@ inline size_t scan_temp_bytes(int64_t n) {
 
 // Exclusive scan of f(0..n-1); calls out(i, exclusive_i, f(i), pl(i)) for
 // every i and writes the total to *d_total (device pointer, may be null).
-// temp needs scan_temp_bytes<T>(n).  Three launches on `stream`.
+// temp needs scan_temp_bytes<T>(n).  Reduce-then-scan: two launches on
+// `stream` (three above kScanDirectTiles tiles); no block waits on another.
 template <typename T, typename F, typename PL, typename Out>
 cudaError_t scan_apply_pl(F f, PL pl, int64_t n, Out out, T *d_total, void *temp, cudaStream_t stream) {
-  int64_t nb = ceil_div(n > 0 ? n : 1, kScanTile);
-  T *sums = reinterpret_cast<T *>(temp);
   if (n <= 0) {
     if (d_total) return cudaMemsetAsync(d_total, 0, sizeof(T), stream);
     return cudaSuccess;
   }
+  const int64_t nb = ceil_div(n, kScanTile);
+  T *sums = reinterpret_cast<T *>(temp);
   k_scan_reduce<T, F><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, n, sums);
-  k_scan_spine<T><<<1, kScanThreads, 0, stream>>>(sums, nb, d_total);
-  k_scan_down<T, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out);
+  if (nb <= kScanDirectTiles) {
+    k_scan_down<T, true, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out, d_total);
+  } else {
+    k_scan_spine<T><<<1, kScanThreads, 0, stream>>>(sums, nb, d_total);
+    k_scan_down<T, false, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out, d_total);
+  }
   return cudaGetLastError();
 }
 

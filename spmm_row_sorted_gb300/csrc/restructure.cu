@@ -78,9 +78,14 @@ __global__ void __launch_bounds__(256) k_sel_pass(const TV *__restrict__ val, in
   uint32_t key[kItems];
 #pragma unroll
   for (int u = 0; u < kItems; ++u) key[u] = first + u * stride < nnz ? mag_key<TV>(val, first + u * stride) : 0u;
+  __shared__ uint32_t s_pm[2];
   for (int i = tid; i < kBins; i += 256) h[i] = 0;
-  const uint32_t pfx = kPass ? st->pfx : 0u, mask = kPass ? st->mask : 0u;
+  if (tid == 0) {  // one load per block: the digits fixed by the previous pass
+    s_pm[0] = kPass ? st->pfx : 0u;
+    s_pm[1] = kPass ? st->mask : 0u;
+  }
   __syncthreads();
+  const uint32_t pfx = s_pm[0], mask = s_pm[1];
 #pragma unroll
   for (int u = 0; u < kItems; ++u)
     if (first + u * stride < nnz && (key[u] & mask) == pfx) atomicAdd(&h[(key[u] >> kShift) & (kBins - 1)], 1u);
@@ -163,7 +168,9 @@ struct KeepVal {
   const TV *val;
   const SelState *st;
   __device__ uint64_t operator()(int64_t k) const {
-    uint32_t key = mag_key<TV>(val, k), t = st->prefix;
+    // every element reads the threshold: through the read-only cache, so the
+    // SMs do not all queue on one L2 line
+    uint32_t key = mag_key<TV>(val, k), t = __ldg(&st->prefix);
     return (uint64_t)(key > t) | ((uint64_t)(key == t) << 32);
   }
 };
@@ -182,7 +189,7 @@ struct KeepOut {
   uint64_t *surv_pos;
   uint32_t *surv_src;
   __device__ void operator()(int64_t k, uint64_t ex, uint64_t v, uint64_t pos) const {
-    const uint32_t m = st->remaining;
+    const uint32_t m = __ldg(&st->remaining);
     const uint32_t gt = (uint32_t)ex, eq = (uint32_t)(ex >> 32);
     const bool keep = (v & 1ull) || ((v >> 32) && eq >= m);
     if (keep) {
@@ -314,9 +321,9 @@ __global__ void k_merge_splits(const uint64_t *__restrict__ A, int64_t na, const
 template <typename TV>
 __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
-            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, const TV *__restrict__ val,
+            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
-            int32_t *__restrict__ src_out) {
+            int32_t *__restrict__ src_out, int32_t *__restrict__ rp) {
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];
@@ -373,6 +380,16 @@ __global__ void __launch_bounds__(kMergeThreads)
       oS[ld + it] = src[it];
     }
   __syncthreads();
+  // row offsets of the output: rp[r] = o for the rows r in (row[o-1], row[o]];
+  // the row before the tile is that of the larger of the two inputs' last
+  // elements consumed by earlier tiles
+  int64_t r_before = -1;
+  if (d0 > 0) {
+    uint64_t last = 0;
+    if (a0 > 0) last = A[a0 - 1];
+    if (b0 > 0 && B[b0 - 1] > last) last = B[b0 - 1];
+    r_before = (int64_t)(last / (uint64_t)in_f);
+  }
   for (int q = threadIdx.x; q < la + lb; q += kMergeThreads) {
     int64_t o = d0 + q;
     int32_t s = oS[q];
@@ -380,6 +397,13 @@ __global__ void __launch_bounds__(kMergeThreads)
     col_out[o] = (int32_t)sB[q];
     val_out[o] = s >= 0 ? val[s] : from_f32<TV>(0.f);
     if (src_out) src_out[o] = s;
+    const int64_t r_cur = (int64_t)sA[q];
+    const int64_t r_prev = q > 0 ? (int64_t)sA[q - 1] : r_before;
+    for (int64_t r = r_prev + 1; r <= r_cur && r <= out_f; ++r) rp[r] = (int32_t)o;
+  }
+  if (d1 == n && threadIdx.x == 0) {  // rows after the last stored weight
+    const int64_t r_last = la + lb > 0 ? (int64_t)sA[la + lb - 1] : r_before;
+    for (int64_t r = r_last + 1; r <= out_f; ++r) rp[r] = (int32_t)n;
   }
 }
 
@@ -417,7 +441,7 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   if (dm > 2147483647.0) dm = 2147483647.0;
   w.d_max = (int64_t)dm;
   int64_t cap = 16;
-  while (cap < 2 * w.d_max + 16) cap <<= 1;
+  while (cap < w.d_max + w.d_max / 4 + 16) cap <<= 1;  // load factor below 0.8 even if every draw is made
   w.cap = cap;
   w.n_merge_tiles = (nnz + kMergeTile - 1) / kMergeTile;
   const size_t n = (size_t)(nnz > 0 ? nnz : 1), np = (size_t)(n_prune > 0 ? n_prune : 1);
@@ -542,8 +566,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     k_merge_splits<<<grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
     k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
-        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, val, a.row_out, a.col_out,
-        reinterpret_cast<TV *>(a.val_out), a.src_out);
+        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, a.out_f, val, a.row_out, a.col_out,
+        reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new);
   }
   SNACK_TRY(cudaGetLastError());
 #undef SNACK_TRY

@@ -499,6 +499,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.col = col;
   a.val = val;
   a.rp_old = h->p.rp;
+  a.rp_new = h->p.rp;
   a.row_out = row_out;
   a.col_out = col_out;
   a.val_out = val_out;
