@@ -57,6 +57,8 @@ struct RestructureArgs {
   int32_t *src_out;  // may be null
   uint32_t *host_counts;  // pinned host memory, 2 words: a draw chunk's accepted count and overflow flag
   cudaEvent_t counts_ready;  // recorded after the copy into host_counts
+  cudaStream_t aux;          // second stream of the handle (regrow branch)
+  cudaEvent_t ev_fork, ev_join;
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
@@ -84,4 +86,6 @@ struct snack_layer {
   int num_sms;
   uint32_t *host_counts = nullptr;  // restructure read-back (pinned), made on first use
   cudaEvent_t counts_ready = nullptr;
+  cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };

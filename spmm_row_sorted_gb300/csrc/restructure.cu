@@ -428,8 +428,13 @@ double expected_draws(double n_pos, double empty, double need) {
   return n_pos * log((empty + 0.5) / (empty - need + 0.5));
 }
 
+// Counters of the regrow branch (it runs beside the select on a second stream).
+struct DrawState {
+  uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
+};
+
 struct RWs {
-  size_t state, scan, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, total;
+  size_t state, dstate, scan, scan2, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, total;
   int64_t d_max, cap, n_merge_tiles;
 };
 
@@ -448,9 +453,12 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   size_t o = 0;
   w.state = o;
   o += align_up(sizeof(SelState), kAlign);
+  w.dstate = o;
+  o += align_up(sizeof(DrawState), kAlign);
   w.scan = o;
-  int64_t scan_n = nnz > w.d_max ? nnz : w.d_max;
-  o += scan_temp_bytes<uint64_t>(scan_n > 0 ? scan_n : 1);
+  o += scan_temp_bytes<uint64_t>(nnz > 0 ? nnz : 1);
+  w.scan2 = o;
+  o += scan_temp_bytes<uint32_t>(w.d_max > 0 ? w.d_max : 1);
   w.surv_pos = o;
   o += align_up(8 * n, kAlign);
   w.surv_src = o;
@@ -501,27 +509,37 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     if (e != cudaSuccess) return SNACK_ERR_CUDA; \
   } while (0)
 
-  // The draws depend only on the old pattern, so they go first: the first
-  // chunk's accepted count is copied to pinned host memory, the prune select
-  // and the survivor scan are queued behind it, and the host waits only for
-  // that copy while the device goes on with the select.
-  k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
-  SNACK_TRY(cudaGetLastError());
+  // Two branches meet at the merge: the regrow (draws, acceptance, sort of
+  // the grown positions) depends only on the old pattern and runs on the
+  // handle's second stream, beside the prune select and the survivor scan on
+  // the caller's stream.  The host reads back each draw chunk's accepted
+  // count (pinned memory, an event on the second stream) while the device
+  // goes on.  Every return after the fork joins the branches first, so no
+  // work on the second stream outlives the call's work on s.
+  cudaStream_t s2 = a.aux;
+  DrawState *ds = reinterpret_cast<DrawState *>(b + W.dstate);
+  void *stemp2 = b + W.scan2;
+  SNACK_TRY(cudaEventRecord(a.ev_fork, s));
+  SNACK_TRY(cudaStreamWaitEvent(s2, a.ev_fork, 0));
+  auto join = [&]() -> cudaError_t {
+    cudaError_t err = cudaEventRecord(a.ev_join, s2);
+    if (err != cudaSuccess) return err;
+    return cudaStreamWaitEvent(s, a.ev_join, 0);
+  };
   const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
   const double empty = (double)n_pos - (double)nnz;
   int64_t done = 0, acc = 0;
-  uint32_t *d_counts = &st->total;  // total, overflow: adjacent words
   auto draw_chunk = [&](int64_t m) -> cudaError_t {
-    k_draw<<<grid_for(m, 256), 256, 0, s>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
-                                            hkeys, hmin, (uint64_t)(W.cap - 1), &st->overflow);
-    k_accept_flags<<<grid_for(m, 256), 256, 0, s>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
-                                                    flags);
+    k_draw<<<grid_for(m, 256), 256, 0, s2>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
+                                             hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
+    k_accept_flags<<<grid_for(m, 256), 256, 0, s2>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
+                                                     flags);
     cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
-                                              d_counts, stemp, s);
+                                              &ds->total, stemp2, s2);
     if (err != cudaSuccess) return err;
-    err = cudaMemcpyAsync(a.host_counts, d_counts, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    err = cudaMemcpyAsync(a.host_counts, ds, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost, s2);
     if (err != cudaSuccess) return err;
-    return cudaEventRecord(a.counts_ready, s);
+    return cudaEventRecord(a.counts_ready, s2);
   };
   auto chunk_size = [&]() -> int64_t {
     double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
@@ -529,39 +547,67 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     return m > W.d_max - done ? W.d_max - done : m;
   };
   int64_t m = 0;
+  cudaError_t e2 = cudaSuccess;
   if (n_prune > 0) {
-    SNACK_TRY(cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s));
-    SNACK_TRY(cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s));
-    m = chunk_size();
-    SNACK_TRY(draw_chunk(m));
-    // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
+    e2 = cudaMemsetAsync(ds, 0, sizeof(DrawState), s2);
+    if (e2 == cudaSuccess) e2 = cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s2);
+    if (e2 == cudaSuccess) e2 = cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s2);
+    if (e2 == cudaSuccess) {
+      m = chunk_size();
+      e2 = draw_chunk(m);
+    }
+  }
+  // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
+  k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
+  if (n_prune > 0) {
     const unsigned g = grid_for((nnz + 15) / 16, 256, 1184);
     k_sel_pass<TV, 0><<<g, 256, 0, s>>>(val, nnz, st);
     k_sel_pass<TV, 1><<<g, 256, 0, s>>>(val, nnz, st);
     k_sel_pass<TV, 2><<<g, 256, 0, s>>>(val, nnz, st);
   }
-  SNACK_TRY(cudaGetLastError());
   // 2. survivors
-  SNACK_TRY(scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, a.in_f}, nnz,
-                                    KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s));
+  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, a.in_f}, nnz,
+                                KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s);
+  if (e != cudaSuccess || e2 != cudaSuccess) {
+    join();
+    return SNACK_ERR_CUDA;
+  }
   // 3. regrow: further chunks only when the first fell short (rare)
+  snack_status verdict = SNACK_OK;
   while (n_prune > 0) {
-    SNACK_TRY(cudaEventSynchronize(a.counts_ready));
-    if (a.host_counts[1]) return SNACK_ERR_WORKSPACE;
+    if (cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
+      verdict = SNACK_ERR_CUDA;
+      break;
+    }
+    if (a.host_counts[1]) {
+      verdict = SNACK_ERR_WORKSPACE;
+      break;
+    }
     acc += a.host_counts[0];
     done += m;
     if (acc >= n_prune) break;
-    if (done >= W.d_max) return SNACK_ERR_NO_SPACE;
+    if (done >= W.d_max) {
+      verdict = SNACK_ERR_NO_SPACE;
+      break;
+    }
     m = chunk_size();
-    SNACK_TRY(draw_chunk(m));
+    if (draw_chunk(m) != cudaSuccess) {
+      verdict = SNACK_ERR_CUDA;
+      break;
+    }
   }
   // 4. sort regrown positions (bucket sort: they are uniform over the empty
-  //    positions), merge with survivors
+  //    positions), then join and merge with the survivors
   const uint64_t *grown = grown_a;
-  if (n_prune > 1) {
-    SNACK_TRY(bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s));
+  if (verdict == SNACK_OK && n_prune > 1) {
+    if (bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s2) != cudaSuccess)
+      verdict = SNACK_ERR_CUDA;
     grown = grown_b;
   }
+  if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
+  if (verdict != SNACK_OK) return verdict;
   if (nnz > 0) {
     k_merge_splits<<<grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);

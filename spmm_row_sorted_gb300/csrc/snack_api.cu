@@ -511,8 +511,16 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   }
   if (!h->counts_ready && cudaEventCreateWithFlags(&h->counts_ready, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
+  if (!h->ev_fork && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess)
+    return SNACK_ERR_CUDA;
+  if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
+    return SNACK_ERR_CUDA;
+  if (!h->aux && cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess) return SNACK_ERR_CUDA;
   a.host_counts = h->host_counts;
   a.counts_ready = h->counts_ready;
+  a.aux = h->aux;
+  a.ev_fork = h->ev_fork;
+  a.ev_join = h->ev_join;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, true));
@@ -521,11 +529,17 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
 
 void snack_destroy(snack_handle h) {
   if (!h) return;
-  if (h->counts_ready) {
+  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join) {
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
-    cudaEventDestroy(h->counts_ready);
+    if (h->aux) {
+      cudaStreamSynchronize(h->aux);
+      cudaStreamDestroy(h->aux);
+    }
+    if (h->counts_ready) cudaEventDestroy(h->counts_ready);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     if (prev >= 0) cudaSetDevice(prev);
   }
   if (h->host_counts) cudaFreeHost(h->host_counts);
