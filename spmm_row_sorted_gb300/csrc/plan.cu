@@ -26,6 +26,17 @@ struct ColSrc {
   __device__ uint32_t val(int64_t i) const { return (uint32_t)i; }
 };
 
+// Column sort source with the row packed above the column (when both fit
+// in 32 bits): key = row << cbits | col, value = storage index.  Digits of
+// the column bits never see the row bits.
+struct ColRowSrc {
+  const int32_t *row, *col;
+  int32_t out_f, in_f;
+  int cbits;
+  __device__ uint32_t key(int64_t i) const { return (clamp_idx(row[i], out_f) << cbits) | clamp_idx(col[i], in_f); }
+  __device__ uint32_t val(int64_t i) const { return (uint32_t)i; }
+};
+
 // Last pass of the column sort writes the column view itself: the sorted
 // column (for the offsets), the storage index, and that entry's row.
 struct ColviewDst {
@@ -51,6 +62,159 @@ __global__ void k_count(const int32_t *__restrict__ idx, int64_t nnz, int32_t n,
     unsigned peers = __match_any_sync(0xffffffffu, key);
     int lane = threadIdx.x & 31;
     if (ok && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&counts[key], (uint32_t)__popc(peers));
+  }
+}
+
+// Second half of the column view for columns of 9..17 bits (and rows that
+// fit beside them in 32 bits).  The entries arrive as row << cbits | col,
+// grouped by the column's high 8 bits (a stable scatter, so storage order
+// within each group); block b sorts group b by the low `shift` bits,
+// stably, and writes the column view (row, storage index) and the column
+// offsets of its 2^shift columns.  The group is taken in chunks of
+// kRadixTile entries in storage order; warp w holds entries w*256.. of a
+// chunk, item i of lane l being entry i*32 + l of that range, so ranks from
+// ballots plus per-warp counts keep storage order within every column.
+constexpr int kColLowMax = 512;  // 2^shift bins at most
+
+__global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t *__restrict__ keys,
+                                                                  const uint32_t *__restrict__ vals, int64_t n,
+                                                                  int shift, int cbits,
+                                                                  const uint32_t *__restrict__ offs, int64_t nb,
+                                                                  int32_t in_f, int32_t *__restrict__ row_t,
+                                                                  int32_t *__restrict__ src_t, int32_t *__restrict__ cp) {
+  __shared__ uint32_t wc[kRadixWarps][kColLowMax];  // per-warp counts of a chunk, then local offsets
+  __shared__ uint32_t run[kColLowMax];              // next free global slot of each column
+  __shared__ uint32_t lstart[kColLowMax];           // start of each column's run inside the staged chunk
+  __shared__ uint32_t s_src[kRadixTile], s_row[kRadixTile];
+  __shared__ uint16_t s_col[kRadixTile];
+  const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int L = 1 << shift;
+  const uint32_t lmask = (uint32_t)(L - 1);
+  const int64_t start = offs[(int64_t)b * nb];
+  const int64_t end = b + 1 < kRadixBins ? (int64_t)offs[(int64_t)(b + 1) * nb] : n;
+  // column counts of the group, then exclusive offsets = column starts
+  for (int i = threadIdx.x; i < L; i += kRadixThreads) run[i] = 0;
+  __syncthreads();
+  for (int64_t k0 = start; k0 < end; k0 += (int64_t)kRadixThreads * kRadixItems) {
+    uint32_t kk[kRadixItems];  // all loads in flight before the atomics
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      const int64_t k = k0 + i * kRadixThreads + threadIdx.x;
+      kk[i] = k < end ? keys[k] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i)
+      if (k0 + i * kRadixThreads + threadIdx.x < end) atomicAdd(&run[kk[i] & lmask], 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // one warp scans the L counts in order
+    uint32_t carry = (uint32_t)start;
+    for (int c0 = 0; c0 < L; c0 += 32) {
+      const int c = c0 + lane;
+      const uint32_t v = c < L ? run[c] : 0u;
+      const uint32_t inc = warp_inclusive_scan(v);
+      if (c < L) {
+        run[c] = carry + inc - v;
+        const int64_t col = ((int64_t)b << shift) + c;
+        if (col < in_f) cp[col] = (int32_t)(carry + inc - v);
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  if (b == 0 && threadIdx.x == 0) cp[in_f] = (int32_t)n;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t nkey[kRadixItems], nsrc[kRadixItems];  // next chunk, loaded ahead
+  auto load = [&](int64_t c0) {
+    const int64_t wbase = c0 + (int64_t)warp * (kRadixItems * 32);
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      const int64_t k = wbase + i * 32 + lane;
+      const bool ok = k < end;
+      nkey[i] = ok ? keys[k] : 0u;
+      nsrc[i] = ok ? vals[k] : 0u;
+    }
+  };
+  load(start);
+  for (int64_t c0 = start; c0 < end; c0 += kRadixTile) {
+    const int m = (int)(end - c0 < kRadixTile ? end - c0 : kRadixTile);
+    uint32_t key[kRadixItems], src[kRadixItems];
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      key[i] = nkey[i];
+      src[i] = nsrc[i];
+    }
+    if (c0 + kRadixTile < end) load(c0 + kRadixTile);
+    __syncthreads();  // the previous chunk is done with wc, lstart and the staging arrays
+    for (int i = threadIdx.x; i < kRadixWarps * L; i += kRadixThreads) (&wc[0][0])[(i / L) * kColLowMax + i % L] = 0;
+    __syncthreads();
+    int dig[kRadixItems];
+    uint32_t rank[kRadixItems];
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      const int64_t k = c0 + (int64_t)warp * (kRadixItems * 32) + i * 32 + lane;
+      dig[i] = k < end ? (int)(key[i] & lmask) : L;  // L: sentinel for past the group
+    }
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      unsigned peers = 0xffffffffu;
+      for (int bit = 0; bit <= shift; ++bit) {  // shift + 1 bits cover the sentinel
+        const bool on = (dig[i] >> bit) & 1;
+        const unsigned bal = __ballot_sync(0xffffffffu, on);
+        peers &= on ? bal : ~bal;
+      }
+      const uint32_t c = dig[i] < L ? wc[warp][dig[i]] : 0u;
+      rank[i] = c + (uint32_t)__popc(peers & lt_mask);
+      __syncwarp();
+      if ((peers >> lane) == 1u && dig[i] < L) wc[warp][dig[i]] = c + (uint32_t)__popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // per column: its count in the chunk (kept in lstart for now) and the
+    // warps' exclusive offsets inside the column's run
+    for (int c = threadIdx.x; c < L; c += kRadixThreads) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kRadixWarps; ++w) {
+        const uint32_t x = wc[w][c];
+        wc[w][c] = t;
+        t += x;
+      }
+      lstart[c] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // exclusive scan of the chunk's column counts: run starts in the staging arrays
+      uint32_t carry = 0;
+      for (int cc = 0; cc < L; cc += 32) {
+        const int c = cc + lane;
+        const uint32_t v = c < L ? lstart[c] : 0u;
+        const uint32_t inc = warp_inclusive_scan(v);
+        if (c < L) lstart[c] = carry + inc - v;
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kRadixItems; ++i) {
+      if (dig[i] < L) {
+        const uint32_t lp = lstart[dig[i]] + wc[warp][dig[i]] + rank[i];
+        s_src[lp] = src[i];
+        s_row[lp] = key[i] >> cbits;
+        s_col[lp] = (uint16_t)dig[i];
+      }
+    }
+    __syncthreads();
+    // write the staged chunk in order: each column's run lands on consecutive slots
+    for (int e = threadIdx.x; e < m; e += kRadixThreads) {
+      const int c = s_col[e];
+      const uint32_t pos = run[c] + (uint32_t)e - lstart[c];
+      src_t[pos] = (int32_t)s_src[e];
+      row_t[pos] = (int32_t)s_row[e];
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < L; c += kRadixThreads) {  // advance each column by its count in the chunk
+      const uint32_t next = c + 1 < L ? lstart[c + 1] : (uint32_t)m;
+      run[c] += next - lstart[c];
+    }
   }
 }
 
@@ -241,14 +405,32 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
                                                                          gf.row_weight, gf.n_tiles, p.tiles_f);
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
-  if (nnz > 0) {
+  const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));
+  if (nnz > 0 && cbits > 8 && cbits - 8 <= 9 && cbits + rbits <= 32) {
+    // 9..17-bit columns: stable scatter of (row, col) by the column's high 8
+    // bits, then one block per group sorts by the low bits and writes the
+    // column offsets
+    uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
+    uint32_t *va = reinterpret_cast<uint32_t *>(b + W.vals_a);
+    const int shift = cbits - 8;
+    const int64_t nb = ceil_div(nnz, kRadixTile);
+    uint8_t *t = b + W.radix;
+    const size_t hbytes = align_up((size_t)nb * kRadixBins * sizeof(uint32_t), kAlign);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(t);
+    uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
+    e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
+                             offs, t + 2 * hbytes, s);
+    if (e != cudaSuccess) return e;
+    k_colview_bucket<<<kRadixBins, kRadixThreads, 0, s>>>(ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
+                                                          p.cp);
+  } else if (nnz > 0) {
     uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
     uint32_t *va = reinterpret_cast<uint32_t *>(b + W.vals_a);
     uint32_t *kb = reinterpret_cast<uint32_t *>(b + W.keys_b);
     uint32_t *vb = reinterpret_cast<uint32_t *>(b + W.vals_b);
     uint32_t *keys_out = reinterpret_cast<uint32_t *>(b + W.keys_out);
     e = radix_sort_custom<uint32_t>(ColSrc{col, in_f}, ColviewDst{keys_out, p.row_t, p.src_t, row, out_f}, nnz,
-                                    bits_for((uint64_t)(in_f - 1)), ka, va, kb, vb, b + W.radix, s);
+                                    cbits, ka, va, kb, vb, b + W.radix, s);
     if (e != cudaSuccess) return e;
     k_offsets_sorted<uint32_t><<<grid_for(nnz + 1, 256), 256, 0, s>>>(keys_out, nnz, in_f, p.cp);
   } else {
