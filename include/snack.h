@@ -24,12 +24,14 @@
  * Memory ownership.  Every device buffer -- indices, values, activations,
  * outputs, the plan and the workspaces -- is allocated and freed by the
  * caller.  The library never allocates device memory.  A handle owns host
- * metadata only; snack_destroy frees it and nothing else.
+ * metadata, and after its first restructure also a second CUDA stream, three
+ * events and 8 bytes of pinned host memory; snack_destroy frees them.
  *
  * Streams.  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
- * the legacy default stream), except snack_create with validate != 0 and
- * snack_restructure, which synchronise `stream` to read back a small count.
- * A plan and a workspace may be used by one call in flight at a time.
+ * the legacy default stream), except snack_create with validate != 0, which
+ * synchronises `stream`, and snack_restructure, which waits on the host for
+ * its draw count (see there).  A plan and a workspace may be used by one call
+ * in flight at a time.
  *
  * Errors.  Every entry point returns a snack_status.  Arguments are checked
  * on the host before any launch; a failed launch or CUDA call returns
@@ -68,7 +70,7 @@ typedef enum snack_status {
   SNACK_ERR_WORKSPACE = 4,    /* plan or workspace smaller than the size query returned */
   SNACK_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
   SNACK_ERR_TIMEOUT = 6,      /* reserved for bounded device-side waits (none today) */
-  SNACK_ERR_UNSUPPORTED = 7,  /* e.g. val and act dtypes differ */
+  SNACK_ERR_UNSUPPORTED = 7,  /* val and act dtypes differ, or max(out_f, in_f) x padded batch >= 2^32 */
   SNACK_ERR_NO_SPACE = 8      /* restructure: too few empty positions, or draw budget spent */
 } snack_status;
 
@@ -208,8 +210,12 @@ snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, s
  * val_out (val dtype), src_out (optional, NULL to skip): old index k of each
  * survivor, -1 for a regrown entry.  The handle's plan is rebuilt for the new
  * pattern; later calls must pass row_out/col_out.  Needs ws_bytes >=
- * snack_restructure_workspace_size(h, n_prune).  Synchronises `stream` once per
- * batch of draws (normally once).  Returns SNACK_ERR_NO_SPACE when fewer than
+ * snack_restructure_workspace_size(h, n_prune).  The regrow (draws,
+ * acceptance, sort of the new positions) runs on the handle's second stream,
+ * forked from and joined back into `stream`, concurrently with the prune
+ * select; the host waits once per batch of draws (normally once) for that
+ * batch's accepted count, while the device keeps working.  When the call
+ * returns, all its work is ordered on `stream`.  Returns SNACK_ERR_NO_SPACE when fewer than
  * n_prune positions are empty or the draw budget (sized in the workspace
  * query: twice the expected number of draws plus 4096) runs out; the handle's
  * plan is then unchanged.
@@ -219,7 +225,9 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
                                int32_t *row_out, int32_t *col_out, void *val_out, int32_t *src_out,
                                void *ws, size_t ws_bytes, snack_stream_t stream);
 
-/* Free the host-side handle (no device memory is touched). NULL is allowed. */
+/* Free the handle: its host memory, and the stream, events and pinned word of
+ * a handle that has restructured (waits for that stream).  No device memory
+ * of the caller is touched.  NULL is allowed. */
 void snack_destroy(snack_handle h);
 
 /* Static description of a status code. */

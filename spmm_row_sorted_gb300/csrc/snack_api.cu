@@ -109,6 +109,9 @@ snack_status check_shape(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_b
   if (max_batch < 1 || max_batch > 65535) return SNACK_ERR_INVALID_ARG;
   if (!dtype_ok(val_t) || !dtype_ok(act_t)) return SNACK_ERR_INVALID_ARG;
   if (val_t != act_t) return SNACK_ERR_UNSUPPORTED;
+  // the kernels address a feature's batch vector by a 32-bit element offset
+  const BatchGeom bg = batch_geom(max_batch, act_t);
+  if ((uint64_t)(out_f > in_f ? out_f : in_f) * (uint64_t)bg.ldx > 0xFFFFFFFFull) return SNACK_ERR_UNSUPPORTED;
   return SNACK_OK;
 }
 

@@ -33,7 +33,13 @@ constexpr int kSpmmWarps = kSpmmThreads / 32;
 // the largest unroll depth (stored weights per slot in flight).  Defaults are
 // the fastest measured on GB300 for the 16384^2 / batch-32 layer.
 #ifndef SNACK_SPMM_MIN_CTAS
-#define SNACK_SPMM_MIN_CTAS 6
+#define SNACK_SPMM_MIN_CTAS 5  // resident CTAs per SM the register budget is sized for
+#endif
+#ifndef SNACK_SPMM_MIN_CTAS_FUSED
+#define SNACK_SPMM_MIN_CTAS_FUSED 4  // the fused backward keeps more live values
+#endif
+#ifndef SNACK_TILE_COST
+#define SNACK_TILE_COST 65536  // tile cost C = SNACK_TILE_COST / batch tile width, clamped to [512, 8192]
 #endif
 #ifndef SNACK_SPMM_UNROLL
 #define SNACK_SPMM_UNROLL 4
@@ -80,7 +86,7 @@ struct TileGeom {
 
 inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max, int n_btiles = 1) {
   TileGeom t;
-  int c = 32768 / (bt_max > 0 ? bt_max : 1);
+  int c = SNACK_TILE_COST / (bt_max > 0 ? bt_max : 1);
   if (c < 512) c = 512;
   if (c > 8192) c = 8192;
   // keep the staged rows of a tile within ~16 KB of shared memory
@@ -114,10 +120,15 @@ inline TileGeom tile_geom(int32_t n_rows, int64_t nnz, int bt_max, int n_btiles 
 
 // stored weights a tile can hold: cost C plus the part of a row end that did not fit
 inline __host__ __device__ int tile_stage_cap(const TileGeom &tg) { return tg.cost_per_tile + tg.row_weight; }
+// The staged arrays run kStagePad entries past the tile (zero offsets and
+// weights), so the inner loop reads whole groups of slots without bounds
+// tests; weights past a row's end are masked to zero.
+constexpr int kStagePad = 256;  // >= slots per warp x weights per slot
+inline __host__ __device__ int tile_stage_len(const TileGeom &tg) { return tile_stage_cap(tg) + kStagePad; }
 
 inline size_t spmm_smem_bytes(const TileGeom &tg, int bt) {
   return (size_t)tg.max_rows * (bt + 1) * 4 + (size_t)kSpmmWarps * bt * 4 + (size_t)(tg.max_rows + 1) * 4 +
-         (size_t)(kSpmmWarps + 1) * 2 * 4 + (size_t)tile_stage_cap(tg) * 8;
+         (size_t)(kSpmmWarps + 1) * 2 * 4 + 8 + (size_t)tile_stage_len(tg) * 8;  // + 8: alignment of the staged pairs
 }
 
 struct SpmmParams {
@@ -180,7 +191,8 @@ struct SpmmUnroll {
 // also dotted with the current column's X slice, giving dW at that entry's
 // storage index in the same pass.
 template <typename TA, typename TV, int V, int G, bool kGatherVal, bool kFuseDw>
-__global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tiles(SpmmParams P, BatchGeom bg) {
+__global__ void __launch_bounds__(kSpmmThreads, kFuseDw ? SNACK_SPMM_MIN_CTAS_FUSED : SNACK_SPMM_MIN_CTAS)
+    k_spmm_tiles(SpmmParams P, BatchGeom bg) {
   constexpr int kSlots = 32 / G;
   constexpr int kU = SpmmUnroll<V, G>::value;
   extern __shared__ __align__(16) float smem[];
@@ -197,9 +209,10 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
   float *wcar = Ys + (size_t)max_rows * ys_ld;
   int *rps = reinterpret_cast<int *>(wcar + kSpmmWarps * bt);
   int *wsp = rps + max_rows + 1;
-  uint32_t *s_idx = reinterpret_cast<uint32_t *>(wsp + 2 * (kSpmmWarps + 1));
-  float *s_val = reinterpret_cast<float *>(s_idx + cap);
-  uint32_t *s_src = reinterpret_cast<uint32_t *>(s_val + cap);  // kFuseDw only
+  // s_iv: each weight's gather offset in elements (index * ldx) and its value bits
+  uint2 *s_iv = reinterpret_cast<uint2 *>(
+      (reinterpret_cast<uintptr_t>(wsp + 2 * (kSpmmWarps + 1)) + 7) & ~(uintptr_t)7);  // 8-byte aligned
+  uint32_t *s_src = reinterpret_cast<uint32_t *>(s_iv + cap + kStagePad);  // kFuseDw only
 
   const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1];
   int i1 = P.tiles[2 * t + 2];
@@ -244,11 +257,14 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
       for (int u = 0; u < 4; ++u) {
         const int q = q0 + u * kSpmmThreads + tid;
         if (q < nn) {
-          s_idx[q] = cc[u] < src_max ? cc[u] : src_max;
-          s_val[q] = vv[u];
+          s_iv[q] = make_uint2((cc[u] < src_max ? cc[u] : src_max) * (uint32_t)bg.ldx, __float_as_uint(vv[u]));
           if (kFuseDw) s_src[q] = ss[u];
         }
       }
+    }
+    for (int q = nn + tid; q < nn + kStagePad; q += kSpmmThreads) {
+      s_iv[q] = make_uint2(0u, 0u);
+      if (kFuseDw) s_src[q] = 0u;
     }
   }
   __syncthreads();
@@ -298,16 +314,20 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
     for (int base = ps; base < pe; base += kSlots * kU) {
       uint32_t c[kU];
       float v[kU];
+      const int k0 = base + slot;
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        const int k = base + u * kSlots + slot;
-        const bool ok = k < pe;
-        c[u] = ok ? s_idx[k] : 0u;
-        v[u] = ok ? s_val[k] : 0.f;
+        const uint2 iv = s_iv[k0 + u * kSlots];
+        c[u] = iv.x;
+        v[u] = __uint_as_float(iv.y);
+      }
+      if (base + kSlots * kU > pe) {  // last group of the row: weights past its end count zero
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = k0 + u * kSlots < pe ? v[u] : 0.f;
       }
       float x[kU][V];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) Slice<TA, V>::load(xt + (size_t)c[u] * bg.ldx, x[u]);
+      for (int u = 0; u < kU; ++u) Slice<TA, V>::load(xt + c[u], x[u]);
 #pragma unroll
       for (int u = 0; u < kU; ++u)
 #pragma unroll
@@ -320,15 +340,33 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
 #pragma unroll
           for (int e = 0; e < V; ++e) d[u] = fmaf(x[u][e], xc[e], d[u]);
         }
+        if constexpr (kU == 4 && G >= 4) {
+          // transposed reduction over the slot's G lanes: the first two steps
+          // halve the values each lane carries (4 -> 2 -> 1), so four
+          // shuffles (plus log2(G/4)) replace 4 * log2(G); lane g with
+          // g % (G/4) == 0 ends with the full sum of weight u = g / (G/4)
+          constexpr int h1 = G / 2, h2 = G / 4;
+          const bool up1 = (g & h1) != 0, up2 = (g & h2) != 0;
+          const float e0 = (up1 ? d[2] : d[0]) + __shfl_xor_sync(0xffffffffu, up1 ? d[0] : d[2], h1);
+          const float e1 = (up1 ? d[3] : d[1]) + __shfl_xor_sync(0xffffffffu, up1 ? d[1] : d[3], h1);
+          float f = (up2 ? e1 : e0) + __shfl_xor_sync(0xffffffffu, up2 ? e0 : e1, h2);
 #pragma unroll
-        for (int off = 1; off < G; off <<= 1)
+          for (int off = 1; off < h2; off <<= 1) f += __shfl_xor_sync(0xffffffffu, f, off);
+          if ((g & (h2 - 1)) == 0) {
+            const int k = base + ((up1 ? 2 : 0) + (up2 ? 1 : 0)) * kSlots + slot;
+            if (k < pe) P.dw[s_src[k]] = f;
+          }
+        } else {
 #pragma unroll
-          for (int u = 0; u < kU; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], off);
-        if (g == 0) {
+          for (int off = 1; off < G; off <<= 1)
 #pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int k = base + u * kSlots + slot;
-            if (k < pe) P.dw[s_src[k]] = d[u];
+            for (int u = 0; u < kU; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], off);
+          if (g == 0) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const int k = base + u * kSlots + slot;
+              if (k < pe) P.dw[s_src[k]] = d[u];
+            }
           }
         }
       }
@@ -367,12 +405,26 @@ __global__ void __launch_bounds__(kSpmmThreads, SNACK_SPMM_MIN_CTAS) k_spmm_tile
   if (nw > 0) {
     TA *y = reinterpret_cast<TA *>(P.y);
     const int bmax = min(bt, P.batch - b0);
-    for (int b = warp; b < bmax; b += kSpmmWarps) {
-      const size_t rowoff = (size_t)(b0 + b) * P.n_rows + i0 + rs;
-      for (int q = lane; q < nw; q += 32) {
-        float s = Ys[(size_t)(q + rs) * ys_ld + b];
-        if (P.bias) s = P.bias[i0 + rs + q] + s;
-        y[rowoff + q] = spmm_epilogue<TA>(P, s, rowoff + q);
+    if (nw <= 32) {  // a warp covers 32 / 2^lg batch rows of up to 2^lg outputs at once
+      const int lg = nw <= 1 ? 0 : 32 - __clz(nw - 1);
+      const int per = 32 >> lg, sub = lane >> lg, q = lane & ((1 << lg) - 1);
+      if (q < nw) {
+        const float bq = P.bias ? P.bias[i0 + rs + q] : 0.f;
+        for (int b = warp * per + sub; b < bmax; b += kSpmmWarps * per) {
+          const size_t off = (size_t)(b0 + b) * P.n_rows + i0 + rs + q;
+          float s = Ys[(size_t)(q + rs) * ys_ld + b];
+          if (P.bias) s = bq + s;
+          y[off] = spmm_epilogue<TA>(P, s, off);
+        }
+      }
+    } else {
+      for (int b = warp; b < bmax; b += kSpmmWarps) {
+        const size_t rowoff = (size_t)(b0 + b) * P.n_rows + i0 + rs;
+        for (int q = lane; q < nw; q += 32) {
+          float s = Ys[(size_t)(q + rs) * ys_ld + b];
+          if (P.bias) s = P.bias[i0 + rs + q] + s;
+          y[rowoff + q] = spmm_epilogue<TA>(P, s, rowoff + q);
+        }
       }
     }
   }
@@ -541,7 +593,7 @@ __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__res
 
 template <typename TA, typename TV, int V, int G, bool kGV, bool kFuse>
 cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
-  size_t smem = spmm_smem_bytes(p.tg, bg.bt) + (kFuse ? (size_t)tile_stage_cap(p.tg) * 4 : 0);
+  size_t smem = spmm_smem_bytes(p.tg, bg.bt) + (kFuse ? (size_t)tile_stage_len(p.tg) * 4 : 0);
   auto kern = k_spmm_tiles<TA, TV, V, G, kGV, kFuse>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
