@@ -37,6 +37,16 @@
  * on the host before any launch; a failed launch or CUDA call returns
  * SNACK_ERR_CUDA.  The library never aborts, exits or traps on the device.
  *
+ * Dense path.  A bf16 layer with at least a quarter of W stored, created with
+ * max_batch >= 32, runs calls with batch >= 32 as dense contractions: the
+ * stored weights are scattered into a dense bf16 copy of W in the workspace
+ * and the product runs on the tensor cores through cuBLASLt (the weight
+ * gradient is the dense dY^T X read back at the stored positions).
+ * snack_query_sizes then reports a workspace that holds the dense copy, the
+ * dense fp32 gradient and 32 MiB for cuBLASLt; a call given a smaller
+ * workspace takes the gather kernels instead.  The handle then also owns a
+ * cuBLASLt handle.  Results follow the same tolerance contract.
+ *
  * Plan contract.  snack_create derives a plan (row offsets, load-balanced
  * tiles, a column-ordered view) from row/col.  row/col may change only through
  * snack_restructure, which rebuilds the plan for the new pattern; the values

@@ -64,6 +64,13 @@ size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// Dense path for moderately sparse bf16 layers (dense.cu): used for calls
+// with batch >= kDenseMinBatch on layers with >= 25 % of W stored, when the
+// workspace holds the dense copy (snack_query_sizes reserves it).
+constexpr int kDenseMinBatch = 32;
+bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t);
+size_t dense_ws_bytes(int32_t out_f, int32_t in_f);
+
 // Host SplitMix64 (state increment and finaliser of Steele, Lea and Flood 2014).
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ULL;
 __host__ __device__ inline uint64_t sm64_finalise(uint64_t z) {
@@ -88,4 +95,17 @@ struct snack_layer {
   cudaEvent_t counts_ready = nullptr;
   cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  bool dense = false;   // the layer takes the dense path for wide batches
+  void *lt = nullptr;   // cuBLASLt handle of the dense path
 };
+
+namespace snack {
+bool dense_init(snack_layer *h);
+void dense_release(snack_layer *h);
+snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, const void *x, int32_t batch,
+                       const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s);
+snack_status dense_dx(snack_layer *h, const int32_t *col, const void *val, const void *dy, int32_t batch, void *dx,
+                      void *ws, size_t ws_bytes, cudaStream_t s);
+snack_status dense_dw(snack_layer *h, const int32_t *col, const void *x, const void *dy, int32_t batch, float *dw,
+                      float *db, void *ws, size_t ws_bytes, cudaStream_t s);
+}  // namespace snack

@@ -275,6 +275,11 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   return SNACK_OK;
 }
 
+// Dense path: a dense layer, a wide batch, and room for the dense copy.
+bool use_dense(snack_handle h, int32_t batch, size_t ws_bytes) {
+  return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f);
+}
+
 snack_status common_call_checks(snack_handle h, int32_t batch, void *ws) {
   if (!h) return SNACK_ERR_INVALID_ARG;
   if (batch < 0 || batch > h->max_batch) return SNACK_ERR_INVALID_ARG;
@@ -296,7 +301,9 @@ snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t
   if (workspace_bytes) {
     size_t a = ops_ws_bytes(out_f, in_f, max_batch, act_t, lay);
     size_t b = plan_build_ws_bytes(out_f, in_f, nnz);
-    *workspace_bytes = a > b ? a : b;
+    size_t c = dense_layer(out_f, in_f, nnz, max_batch, val_t) ? dense_ws_bytes(out_f, in_f) : 0;
+    a = a > b ? a : b;
+    *workspace_bytes = a > c ? a : c;
   }
   return SNACK_OK;
 }
@@ -342,6 +349,11 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   h->p = p;
   h->plan_bytes = plan_bytes;
   h->num_sms = sms > 0 ? sms : 1;
+  h->dense = dense_layer(out_f, in_f, nnz, max_batch, val_t);
+  if (h->dense && !dense_init(h)) {
+    delete h;
+    return SNACK_ERR_CUDA;
+  }
   *out_handle = h;
   return SNACK_OK;
 }
@@ -359,6 +371,7 @@ snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *c
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_dense(h, batch, ws_bytes)) return dense_fwd(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_fwd<bf16>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
   return run_fwd<float>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
 }
@@ -376,6 +389,7 @@ snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *co
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (col && use_dense(h, batch, ws_bytes)) return dense_dx(h, col, val, dy, batch, dx, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s);
   return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s);
 }
@@ -394,6 +408,7 @@ snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *c
     return SNACK_OK;
   }
   if (!x || !dy) return SNACK_ERR_INVALID_ARG;
+  if (use_dense(h, batch, ws_bytes)) return dense_dw(h, col, x, dy, batch, dw, db, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_dw<bf16>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
   return run_dw<float>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
 }
@@ -455,6 +470,10 @@ snack_status snack_backward(snack_handle h, const int32_t *row, const int32_t *c
   if (overlap(dx, (size_t)batch * h->in_f * s_act, dy, (size_t)batch * h->out_f * s_act) ||
       overlap(dx, (size_t)batch * h->in_f * s_act, x, (size_t)batch * h->in_f * s_act))
     return SNACK_ERR_INVALID_ARG;
+  if (use_dense(h, batch, ws_bytes)) {
+    snack_status r = dense_dx(h, col, val, dy, batch, dx, ws, ws_bytes, s);
+    return r != SNACK_OK ? r : dense_dw(h, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+  }
   if (h->act_t == SNACK_BF16) return run_bwd<bf16>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
   return run_bwd<float>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
 }
@@ -532,6 +551,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
 
 void snack_destroy(snack_handle h) {
   if (!h) return;
+  dense_release(h);
   if (h->counts_ready || h->aux || h->ev_fork || h->ev_join) {
     int prev = -1;
     cudaGetDevice(&prev);

@@ -372,3 +372,28 @@ def test_backward_equals_separate_calls_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(dx_f, dx_s) and torch.equal(db_f, db_s)
     L.close()
+
+
+# ---------------------------------------------------------------- dense path (bf16, >= 25 % stored, batch >= 32)
+
+@pytest.mark.parametrize("case", [(256, 384, 0.5, 64), (300, 515, 0.3, 33), (128, 128, 1.0, 32), (200, 264, 0.6, 130)])
+def test_dense_path_matches_oracle(case):
+    out_f, in_f, density, batch = case
+    lay = wl.make_layer(out_f, in_f, density=density, val_std=0.2, val_dtype="bf16", seed=out_f, bias="normal")
+    acts = wl.make_acts(batch, in_f, out_f, "bf16", seed=in_f)
+    check_layer_ops(lay, acts)
+    check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
+
+
+def test_dense_layer_narrow_batch_takes_gather_path():
+    # the same dense layer at batch 8 (below the dense path's minimum), built for batch 64
+    lay = wl.make_layer(256, 384, density=0.5, val_std=0.2, val_dtype="bf16", seed=3, bias="normal")
+    acts = wl.make_acts(8, 384, 256, "bf16", seed=3)
+    check_layer_ops(lay, acts, max_batch=64)
+
+
+def test_dense_path_after_restructure():
+    # the dense copy is rebuilt from the new pattern on every call
+    lay = wl.make_layer(192, 256, density=0.5, val_std=0.2, val_dtype="bf16", seed=9, bias="normal")
+    acts = wl.make_acts(48, 256, 192, "bf16", seed=9)
+    restructure_and_check(lay, int(0.1 * lay.nnz), seed=5, step=2, acts=acts)
