@@ -23,7 +23,8 @@ constexpr int kDensifyChunk = 8192;  // columns of one row staged in shared memo
 
 // Row r of the dense copy: zeros, then the row's stored weights at their
 // columns, written as whole 16-byte vectors.
-__global__ void __launch_bounds__(256) k_densify(const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
+template <typename I>
+__global__ void __launch_bounds__(256) k_densify(const int32_t *__restrict__ rp, const I *__restrict__ col,
                                                  const bf16 *__restrict__ val, int32_t in_f, bf16 *__restrict__ wd) {
   __shared__ __align__(16) bf16 row_buf[kDensifyChunk];
   const int r = blockIdx.x;
@@ -39,7 +40,7 @@ __global__ void __launch_bounds__(256) k_densify(const int32_t *__restrict__ rp,
 #pragma unroll
       for (int u = 0; u < 8; ++u) {  // all loads in flight before the stores
         const int64_t k = kb + u * (int64_t)blockDim.x;
-        c[u] = k < k1 ? col[k] - c0 : -1;
+        c[u] = k < k1 ? (int)col[k] - c0 : -1;
         v[u] = k < k1 ? val[k] : __float2bfloat16(0.f);
       }
 #pragma unroll
@@ -166,6 +167,15 @@ unsigned grid_of(int64_t n, int threads) {
   return (unsigned)b;
 }
 
+// the dense copy of W; columns from the plan's 16-bit copy when there is one
+void densify(const snack_layer *h, const int32_t *col, const void *val, bf16 *wd, cudaStream_t s) {
+  const bf16 *v = reinterpret_cast<const bf16 *>(val);
+  if (h->p.col16)
+    k_densify<uint16_t><<<h->out_f, 256, 0, s>>>(h->p.rp, h->p.col16, v, h->in_f, wd);
+  else
+    k_densify<int32_t><<<h->out_f, 256, 0, s>>>(h->p.rp, col, v, h->in_f, wd);
+}
+
 }  // namespace
 
 bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t) {
@@ -193,7 +203,7 @@ snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, cons
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   bf16 *wd = reinterpret_cast<bf16 *>(b + W.wd);
-  k_densify<<<h->out_f, 256, 0, s>>>(h->p.rp, col, reinterpret_cast<const bf16 *>(val), h->in_f, wd);
+  densify(h, col, val, wd, s);
   if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   // column-major: Y'(out x B) = Wd'(in x out)^T X'(in x B)
   if (lt_gemm(reinterpret_cast<cublasLtHandle_t>(h->lt), CUBLAS_OP_T, CUBLAS_OP_N, h->out_f, batch, h->in_f, wd,
@@ -213,7 +223,7 @@ snack_status dense_dx(snack_layer *h, const int32_t *col, const void *val, const
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   bf16 *wd = reinterpret_cast<bf16 *>(b + W.wd);
-  k_densify<<<h->out_f, 256, 0, s>>>(h->p.rp, col, reinterpret_cast<const bf16 *>(val), h->in_f, wd);
+  densify(h, col, val, wd, s);
   if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   // column-major: dX'(in x B) = Wd'(in x out) dY'(out x B)
   if (lt_gemm(reinterpret_cast<cublasLtHandle_t>(h->lt), CUBLAS_OP_N, CUBLAS_OP_N, h->in_f, batch, h->out_f, wd,

@@ -19,10 +19,13 @@ struct PlanPtrs {
   int32_t *row_t;    // [nnz]         row of each column-view entry
   int32_t *src_t;    // [nnz]         storage index of each column-view entry
   uint32_t *flags;   // [64]          validation flags and small device scalars
+  uint16_t *col16;   // [nnz]         16-bit copy of col (in_f <= 65536), else null
+  uint16_t *rowt16;  // [nnz]         16-bit copy of row_t (out_f <= 65536), else null
 };
 
 struct PlanLayout {
-  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, total;
+  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, total;
+  bool c16, r16;  // the 16-bit index copies exist
   TileGeom gf, gt;
 };
 
@@ -31,8 +34,8 @@ PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
 // Fill the plan for the pattern (row, col).  Asynchronous on s.  rp_ready
-// says the row offsets p.rp are already in place (a restructure's merge
-// writes them).
+// says the row offsets p.rp and the 16-bit column copy p.col16 are already in
+// place (a restructure's merge writes them).
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
                        bool rp_ready);
@@ -52,6 +55,7 @@ struct RestructureArgs {
   const int32_t *rp_old;  // row offsets of the input pattern (from the plan)
   int32_t *rp_new;        // row offsets of the output, written by the merge (may alias rp_old: the
                           // draws that read rp_old are ordered before the merge on the stream)
+  uint16_t *col16_new;    // 16-bit copy of col_out written by the merge, or null
   int32_t *row_out, *col_out;
   void *val_out;
   int32_t *src_out;  // may be null

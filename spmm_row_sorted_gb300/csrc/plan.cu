@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
                                                                   int shift, int cbits,
                                                                   const uint32_t *__restrict__ offs, int64_t nb,
                                                                   int32_t in_f, int32_t *__restrict__ row_t,
-                                                                  int32_t *__restrict__ src_t, int32_t *__restrict__ cp) {
+                                                                  int32_t *__restrict__ src_t, int32_t *__restrict__ cp,
+                                                                  uint16_t *__restrict__ rowt16) {
   __shared__ uint32_t wc[kRadixWarps][kColLowMax];  // per-warp counts of a chunk, then local offsets
   __shared__ uint32_t run[kColLowMax];              // next free global slot of each column
   __shared__ uint32_t lstart[kColLowMax];           // start of each column's run inside the staged chunk
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
       const uint32_t pos = run[c] + (uint32_t)e - lstart[c];
       src_t[pos] = (int32_t)s_src[e];
       row_t[pos] = (int32_t)s_row[e];
+      if (rowt16) rowt16[pos] = (uint16_t)s_row[e];
     }
     __syncthreads();
     for (int c = threadIdx.x; c < L; c += kRadixThreads) {  // advance each column by its count in the chunk
@@ -279,6 +281,17 @@ __global__ void k_offsets_sorted(const I *__restrict__ idx, int64_t nnz, int32_t
   }
 }
 
+// 16-bit copy of an index array whose values fit (the caller checks the
+// bound on the host): dst[k] = min(src[k], 65535) as uint16, clamped so a
+// bad input can never produce an index past the bound.
+__global__ void k_pack16(const int32_t *__restrict__ src, int64_t n, uint16_t *__restrict__ dst) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
+    const uint32_t v = (uint32_t)src[k];
+    dst[k] = (uint16_t)(v < 65535u ? v : 65535u);
+  }
+}
+
 __global__ void k_validate(const int32_t *__restrict__ row, const int32_t *__restrict__ col, int64_t nnz, int32_t out_f,
                            int32_t in_f, uint32_t *__restrict__ flag) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -337,6 +350,12 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
   o += align_up(sizeof(int32_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
   L.off_flags = o;
   o += align_up(sizeof(uint32_t) * 64, kAlign);
+  L.c16 = in_f <= 65536;
+  L.r16 = out_f <= 65536;
+  L.off_col16 = o;
+  if (L.c16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
+  L.off_rowt16 = o;
+  if (L.r16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
   L.total = o;
   return L;
 }
@@ -351,6 +370,8 @@ PlanPtrs plan_ptrs(const PlanLayout &L, void *base) {
   p.row_t = reinterpret_cast<int32_t *>(b + L.off_rowt);
   p.src_t = reinterpret_cast<int32_t *>(b + L.off_srct);
   p.flags = reinterpret_cast<uint32_t *>(b + L.off_flags);
+  p.col16 = L.c16 ? reinterpret_cast<uint16_t *>(b + L.off_col16) : nullptr;
+  p.rowt16 = L.r16 ? reinterpret_cast<uint16_t *>(b + L.off_rowt16) : nullptr;
   return p;
 }
 
@@ -396,7 +417,9 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   void *stemp = b + W.scan;
   cudaError_t e;
 
-  // row offsets: already written by a restructure's merge, counts otherwise
+  // row offsets and the 16-bit column copy: already written by a
+  // restructure's merge, made here otherwise
+  if (!rp_ready && p.col16 && nnz > 0) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, p.col16);
   if (!rp_ready) {
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
@@ -422,7 +445,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
                              offs, t + 2 * hbytes, s);
     if (e != cudaSuccess) return e;
     k_colview_bucket<<<kRadixBins, kRadixThreads, 0, s>>>(ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
-                                                          p.cp);
+                                                          p.cp, p.rowt16);
   } else if (nnz > 0) {
     uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
     uint32_t *va = reinterpret_cast<uint32_t *>(b + W.vals_a);
@@ -433,6 +456,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
                                     cbits, ka, va, kb, vb, b + W.radix, s);
     if (e != cudaSuccess) return e;
     k_offsets_sorted<uint32_t><<<grid_for(nnz + 1, 256), 256, 0, s>>>(keys_out, nnz, in_f, p.cp);
+    if (p.rowt16) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(p.row_t, nnz, p.rowt16);
   } else {
     k_offsets_sorted<int32_t><<<1, 256, 0, s>>>(col, 0, in_f, p.cp);
   }

@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
             int64_t nb, const int64_t *__restrict__ part, int32_t in_f, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
-            int32_t *__restrict__ src_out, int32_t *__restrict__ rp) {
+            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];
@@ -395,6 +395,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     int32_t s = oS[q];
     row_out[o] = (int32_t)sA[q];
     col_out[o] = (int32_t)sB[q];
+    if (col16) col16[o] = (uint16_t)sB[q];
     val_out[o] = s >= 0 ? val[s] : from_f32<TV>(0.f);
     if (src_out) src_out[o] = s;
     const int64_t r_cur = (int64_t)sA[q];
@@ -613,7 +614,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
                                                                               W.n_merge_tiles, part);
     k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
         surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, a.out_f, val, a.row_out, a.col_out,
-        reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new);
+        reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new, a.col16_new);
   }
   SNACK_TRY(cudaGetLastError());
 #undef SNACK_TRY

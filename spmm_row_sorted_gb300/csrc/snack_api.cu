@@ -142,6 +142,7 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
   p.tg = h->lay.gf;
   p.nnz = h->nnz;
   p.idx = col;
+  p.idx16 = h->p.col16;
   p.val = val;
   p.val_src = nullptr;
   p.xt = xt;
@@ -180,6 +181,7 @@ snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t bat
   p.tg = h->lay.gt;
   p.nnz = h->nnz;
   p.idx = h->p.row_t;
+  p.idx16 = h->p.rowt16;
   p.val = val;
   p.val_src = h->p.src_t;
   p.xt = dyt;
@@ -258,6 +260,7 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   p.tg = h->lay.gt;
   p.nnz = h->nnz;
   p.idx = h->p.row_t;
+  p.idx16 = h->p.rowt16;
   p.val = val;
   p.val_src = h->p.src_t;
   p.xt = dyt;
@@ -522,6 +525,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.val = val;
   a.rp_old = h->p.rp;
   a.rp_new = h->p.rp;
+  a.col16_new = h->p.col16;
   a.row_out = row_out;
   a.col_out = col_out;
   a.val_out = val_out;

@@ -139,6 +139,7 @@ struct SpmmParams {
   TileGeom tg;
   int64_t nnz;
   const int32_t *idx;     // [nnz] gather index (fwd: col, dx: row of the column view)
+  const uint16_t *idx16;  // [nnz] the same index in 16 bits (from the plan), or null
   const void *val;        // [nnz] weights, storage order
   const int32_t *val_src; // dx: storage index of each column-view entry; fwd: null
   const void *xt;         // [n_src][ldx] transposed activations
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kSpmmThreads, kFuseDw ? SNACK_SPMM_MIN_CTAS_FU
         ss[u] = 0u;
         vv[u] = 0.f;
         if (q < nn) {
-          cc[u] = (uint32_t)ld_stream(P.idx + j0 + q);
+          cc[u] = P.idx16 ? (uint32_t)ld_stream(P.idx16 + j0 + q) : (uint32_t)ld_stream(P.idx + j0 + q);
           if (kGatherVal) {
             uint32_t sidx = (uint32_t)ld_stream(P.val_src + j0 + q);
             ss[u] = sidx < nnz_max ? sidx : nnz_max;

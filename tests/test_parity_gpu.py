@@ -397,3 +397,17 @@ def test_dense_path_after_restructure():
     lay = wl.make_layer(192, 256, density=0.5, val_std=0.2, val_dtype="bf16", seed=9, bias="normal")
     acts = wl.make_acts(48, 256, 192, "bf16", seed=9)
     restructure_and_check(lay, int(0.1 * lay.nnz), seed=5, step=2, acts=acts)
+
+
+# ---------------------------------------------------------------- 16-bit index copies of the plan
+
+@pytest.mark.parametrize("shape", [(20, 70000, 3000), (70000, 20, 3000), (10, 140000, 2000), (65536, 65536, 4000)])
+def test_index_width_boundaries(shape):
+    # feature counts above 65536 keep 32-bit indices; 65536 itself uses the 16-bit copies;
+    # 140000 inputs also take the general column sort
+    out_f, in_f, nnz = shape
+    for dtype in ("f32", "bf16"):
+        lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=0.5, val_dtype=dtype, seed=nnz, bias="normal")
+        acts = wl.make_acts(9, in_f, out_f, dtype, seed=1)
+        check_layer_ops(lay, acts)
+    restructure_and_check(lay, nnz // 10, seed=1, step=1, acts=acts)
