@@ -406,7 +406,7 @@ def run_ours(args):
     e2e = {"value": world * step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    launches_per_step = 3 + 5 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: colsum, 2 transposes, tiles, fixup
+    launches_per_step = 3 + 5 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: 2 transposes, row sum, tiles, fixup
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -783,13 +783,13 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
+    draw_chunk = 1 + 1 + 2  # draws, accept flags, scan (second stream)
+    sort_grown = 1 + 2 + 1 + 1  # bucket count, scan, fill, rank (second stream)
     select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
-    keep_scan = 3
-    draw_chunk = 1 + 1 + 3  # draws, accept flags, scan
-    sort_grown = 1 + 3 + 1 + 1  # bucket count, scan, fill, rank
-    merge = 2  # split points, merge
-    plan = 1 + 1 + 2 * (1 + 3 + 1) + 1 + 1  # row offsets, tiles, two radix passes, column offsets, tiles
-    return select + keep_scan + draw_chunk + sort_grown + merge + plan
+    keep_scan = 2
+    merge = 2  # split points, merge (also writes the row offsets)
+    plan = 1 + (1 + 2 + 1) + 1 + 1  # row tiles, high-digit column scatter, per-group column sort, column tiles
+    return draw_chunk + sort_grown + select + keep_scan + merge + plan
 
 
 def main(argv=None):
