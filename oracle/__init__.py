@@ -83,6 +83,11 @@ def _load():
         lib.oracle_restructure.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
                                            _i32p, _i32p, _i64p]
         lib.oracle_restructure.restype = I64
+        lib.oracle_row_base.argtypes = [U64, U64, U64]
+        lib.oracle_row_base.restype = U64
+        lib.oracle_restructure_rows.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
+                                                _i32p, _i32p, _i64p]
+        lib.oracle_restructure_rows.restype = I64
         _lib = lib
         return lib
 
@@ -222,6 +227,38 @@ def restructure(out_f: int, in_f: int, row, col, val_f64: np.ndarray, n_prune: i
     if rc < 0:
         raise RestructureError(_RESTRUCTURE_ERRORS.get(int(rc), str(rc)))
     return ro, co, so, int(rc)
+
+
+def restructure_rows(out_f: int, in_f: int, row, col, val_f64: np.ndarray, n_per_row: int, seed: int,
+                     step: int, max_draws_per_row: Optional[int] = None):
+    """Per-row (constant fan-in) restructure: every row prunes min(n_per_row, its
+    length) smallest |w| and regrows as many columns of the same row that were
+    empty, from the row's own draw stream.
+
+    Returns (row_out, col_out, src_out, draws) as restructure() does; every row
+    keeps its count and its offsets.
+    """
+    row, col = _idx(row), _idx(col)
+    nnz = row.shape[0]
+    val_f64 = np.ascontiguousarray(val_f64, dtype=np.float64)
+    ro = np.empty(nnz, dtype=np.int32)
+    co = np.empty(nnz, dtype=np.int32)
+    so = np.empty(nnz, dtype=np.int64)
+    md = default_max_draws(n_per_row) if max_draws_per_row is None else int(max_draws_per_row)
+    rc = _load().oracle_restructure_rows(out_f, in_f, nnz, row, col, val_f64, int(n_per_row),
+                                         int(seed) & (2**64 - 1), int(step) & (2**64 - 1), md, ro, co, so)
+    if rc < 0:
+        raise RestructureError(_ROWS_ERRORS.get(int(rc), str(rc)))
+    return ro, co, so, int(rc)
+
+
+_ROWS_ERRORS = {-1: "pattern not valid row-sorted COO", -2: "n_per_row negative",
+                -3: "a row has fewer empty columns than it prunes", -4: "a row's draw budget is exhausted",
+                -5: "out of memory"}
+
+
+def row_base(seed: int, step: int, r: int) -> int:
+    return int(_load().oracle_row_base(int(seed) & (2**64 - 1), int(step) & (2**64 - 1), int(r)))
 
 
 def restructure_values(val_stored: np.ndarray, src_out: np.ndarray) -> np.ndarray:

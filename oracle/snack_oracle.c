@@ -403,3 +403,114 @@ done:
   free(acc.slot);
   return rc;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Per-row (constant fan-in) restructure: the structured DST variant in     */
+/* which every output row keeps its number of stored weights (Structured    */
+/* RigL imposes a constant fan-in; with equal row counts this preserves     */
+/* it).  Row r prunes its p_r = min(n_per_row, len_r) smallest |w| by      */
+/* (|w|, k) and regrows p_r columns of the same row that were empty before  */
+/* the call, drawn from the row's own stream:                               */
+/*   base_r = mix(seed ^ mix(step ^ (r * K))),  K = 0xD1B54A32D192ED03      */
+/*   draw i: u = mix(base_r + (i + 1) * gamma), column = floor(u * in_f / 2^64) */
+/* A draw is accepted when its column was empty in the row and is not       */
+/* already accepted; the row stops at p_r accepted (error when             */
+/* max_draws_per_row draws do not suffice).  Survivors and regrown columns  */
+/* are merged by column; row r's output stays at the row's input offsets.  */
+/* Row 0's stream is the unstructured restructure's stream, so a one-row    */
+/* layer gives the same result as oracle_restructure.                        */
+/*                                                                          */
+/* Returns the total number of draws, or a negative error: -1 bad pattern,  */
+/* -2 n_per_row negative, -3 a row has fewer empty columns than p_r,        */
+/* -4 a row's draw budget is exhausted, -5 out of memory.                   */
+
+static const uint64_t ROW_STREAM_K = 0xD1B54A32D192ED03ULL;
+
+uint64_t oracle_row_base(uint64_t seed, uint64_t step, uint64_t r) {
+  return oracle_splitmix64_mix(seed ^ oracle_splitmix64_mix(step ^ (r * ROW_STREAM_K)));
+}
+
+int64_t oracle_restructure_rows(int64_t out_f, int64_t in_f, int64_t nnz, const int32_t *row,
+                                const int32_t *col, const double *val, int64_t n_per_row, uint64_t seed,
+                                uint64_t step, int64_t max_draws_per_row, int32_t *row_out, int32_t *col_out,
+                                int64_t *src_out) {
+  if (oracle_check_coo(out_f, in_f, nnz, row, col) != 0) return -1;
+  if (n_per_row < 0) return -2;
+  int64_t *rp = (int64_t *)calloc((size_t)out_f + 1, sizeof(int64_t));
+  prune_key *keys = (prune_key *)malloc(sizeof(prune_key) * (size_t)(nnz > 0 ? nnz : 1));
+  unsigned char *pruned = (unsigned char *)calloc((size_t)(nnz > 0 ? nnz : 1), 1);
+  uint64_t *grown = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(nnz > 0 ? nnz : 1));
+  uint64_t *rowpos = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(nnz > 0 ? nnz : 1));
+  int64_t rc = -5, draws = 0;
+  if (!rp || !keys || !pruned || !grown || !rowpos) goto done;
+  for (int64_t k = 0; k < nnz; ++k) rp[row[k] + 1]++;
+  for (int64_t r = 0; r < out_f; ++r) rp[r + 1] += rp[r];
+  for (int64_t r = 0; r < out_f; ++r) {
+    const int64_t k0 = rp[r], len = rp[r + 1] - rp[r];
+    const int64_t p = n_per_row < len ? n_per_row : len;
+    if (p > in_f - len) {
+      rc = -3;
+      goto done;
+    }
+    /* prune: the p smallest (|w|, k) of the row */
+    for (int64_t j = 0; j < len; ++j) {
+      keys[j].is_nan = isnan(val[k0 + j]) ? 1 : 0;
+      keys[j].mag = keys[j].is_nan ? 0.0 : fabs(val[k0 + j]);
+      keys[j].k = k0 + j;
+    }
+    qsort(keys, (size_t)len, sizeof(prune_key), prune_key_cmp);
+    for (int64_t j = 0; j < p; ++j) pruned[keys[j].k] = 1;
+    /* regrow: the row's own draws; the old row's columns as sorted positions */
+    for (int64_t j = 0; j < len; ++j) rowpos[j] = (uint64_t)col[k0 + j];
+    uint64_t base = oracle_row_base(seed, step, (uint64_t)r);
+    int64_t n_acc = 0, i = 0;
+    while (n_acc < p) {
+      if (i >= max_draws_per_row) {
+        rc = -4;
+        goto done;
+      }
+      uint64_t u = oracle_splitmix64_mix(base + ((uint64_t)i + 1) * SM64_GAMMA);
+      uint64_t c = (uint64_t)(((unsigned __int128)u * (unsigned __int128)(uint64_t)in_f) >> 64);
+      ++i;
+      if (sorted_contains(rowpos, len, c)) continue;
+      int dup = 0;
+      for (int64_t a = 0; a < n_acc; ++a)
+        if (grown[a] == c) {
+          dup = 1;
+          break;
+        }
+      if (dup) continue;
+      grown[n_acc++] = c;
+    }
+    draws += i;
+    qsort(grown, (size_t)p, sizeof(uint64_t), cmp_u64);
+    /* merge the row's survivors with its regrown columns */
+    int64_t a = k0, g = 0, j = k0;
+    for (;;) {
+      while (a < k0 + len && pruned[a]) ++a;
+      int have_a = a < k0 + len, have_g = g < p;
+      if (!have_a && !have_g) break;
+      if (have_a && (!have_g || (uint64_t)col[a] < grown[g])) {
+        row_out[j] = (int32_t)r;
+        col_out[j] = col[a];
+        src_out[j] = a;
+        ++a;
+      } else {
+        row_out[j] = (int32_t)r;
+        col_out[j] = (int32_t)grown[g];
+        src_out[j] = -1;
+        ++g;
+      }
+      ++j;
+    }
+  }
+  rc = draws;
+
+done:
+  free(rp);
+  free(keys);
+  free(pruned);
+  free(grown);
+  free(rowpos);
+  return rc;
+}

@@ -131,6 +131,23 @@ def zipf_positions(out_f: int, in_f: int, nnz: int, s: float, seed: int) -> np.n
     return np.concatenate(parts)
 
 
+def fanin_positions(out_f: int, in_f: int, fan_in: int, seed: int) -> np.ndarray:
+    """Sorted linear positions with exactly fan_in uniform columns in every row
+    (constant fan-in, the layout of structured DST)."""
+    if fan_in > in_f:
+        raise ValueError("fan_in exceeds in_f")
+    rng = _rng(seed, _T_ZIPFCOL)
+    keys = rng.random((out_f, in_f)) if out_f * in_f <= (1 << 26) else None
+    parts = []
+    for r in range(out_f):
+        if keys is not None:
+            cols = np.sort(np.argpartition(keys[r], fan_in - 1)[:fan_in]) if fan_in > 0 else np.zeros(0, np.int64)
+        else:
+            cols = np.sort(rng.choice(in_f, size=fan_in, replace=False, shuffle=False))
+        parts.append(r * in_f + cols.astype(np.int64))
+    return np.concatenate(parts) if parts else np.zeros(0, dtype=np.int64)
+
+
 @dataclasses.dataclass
 class Layer:
     """One sparse layer: W (out_f x in_f) as row-sorted COO plus a bias."""
@@ -174,16 +191,20 @@ def _store(a32: np.ndarray, dtype: str) -> np.ndarray:
 
 def make_layer(out_f: int, in_f: int, *, nnz: Optional[int] = None, density: Optional[float] = None,
                val_std: float = 0.02, val_dtype: str = "f32", seed: int = 0,
-               zipf_s: Optional[float] = None, bias: str = "zeros") -> Layer:
-    """Seeded layer with uniform (or Zipf-row) positions and N(0, val_std) values."""
-    if nnz is None:
-        if density is None:
-            raise ValueError("give nnz or density")
-        nnz = nnz_for(out_f, in_f, density)
-    if zipf_s is None:
-        p = uniform_positions(out_f, in_f, nnz, seed)
+               zipf_s: Optional[float] = None, bias: str = "zeros", fan_in: Optional[int] = None) -> Layer:
+    """Seeded layer with uniform, Zipf-row or constant fan-in positions and N(0, val_std) values."""
+    if fan_in is not None:
+        nnz = out_f * fan_in
+        p = fanin_positions(out_f, in_f, fan_in, seed)
     else:
-        p = zipf_positions(out_f, in_f, nnz, zipf_s, seed)
+        if nnz is None:
+            if density is None:
+                raise ValueError("give nnz, density or fan_in")
+            nnz = nnz_for(out_f, in_f, density)
+        if zipf_s is None:
+            p = uniform_positions(out_f, in_f, nnz, seed)
+        else:
+            p = zipf_positions(out_f, in_f, nnz, zipf_s, seed)
     row = (p // in_f).astype(np.int32)
     col = (p % in_f).astype(np.int32)
     v = (_rng(seed, _T_VAL).standard_normal(nnz) * val_std).astype(np.float32)

@@ -26,6 +26,7 @@ import numpy as np
 import pytest
 
 import oracle
+from spmm_row_sorted_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -347,3 +348,136 @@ def test_thread_count_does_not_change_results():
     finally:
         oracle.set_threads(prev)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- per-row (constant fan-in) restructure
+
+def check_rows_invariants(out_f, in_f, row, col, val, n_per_row, ro, co, so):
+    nnz = row.shape[0]
+    assert np.array_equal(ro, row)  # every row keeps its count and offsets
+    rp = np.concatenate([[0], np.cumsum(np.bincount(row, minlength=out_f))]).astype(np.int64)
+    for r in range(out_f):
+        a, b = rp[r], rp[r + 1]
+        n = b - a
+        p = min(n_per_row, n)
+        cr, sr = co[a:b], so[a:b]
+        assert np.all(np.diff(cr) > 0)  # strictly increasing columns in the row
+        surv = sr[sr >= 0]
+        assert np.all((surv >= a) & (surv < b)) and np.all(np.diff(surv) > 0)
+        assert np.array_equal(cr[sr >= 0], col[surv])
+        assert (sr < 0).sum() == p
+        pruned = np.setdiff1d(np.arange(a, b), surv)
+        if p and surv.size:
+            assert max(prune_rank_key(val[k], k) for k in pruned) < min(prune_rank_key(val[k], k) for k in surv)
+        assert np.intersect1d(cr[sr < 0], col[a:b]).size == 0  # regrown only where the row was empty
+
+
+def test_rows_one_row_equals_unstructured():
+    # row 0's draw stream is the unstructured stream, so a one-row layer must
+    # give exactly the unstructured restructure's output
+    rng = np.random.default_rng(5)
+    for trial in range(100):
+        in_f = int(rng.integers(2, 300))
+        nnz = int(rng.integers(1, in_f))
+        _, col = rand_pattern(rng, 1, in_f, nnz)
+        row = np.zeros(nnz, np.int32)
+        val = rng.standard_normal(nnz)
+        n = int(rng.integers(0, min(nnz, in_f - nnz) + 1))
+        a = oracle.restructure(1, in_f, row, col, val, n, trial, 11)
+        b = oracle.restructure_rows(1, in_f, row, col, val, n, trial, 11)
+        for x, y in zip(a[:3], b[:3]):
+            assert np.array_equal(x, y)
+        assert a[3] == b[3]
+
+
+def test_rows_stream_base():
+    # base of row r: mix(seed ^ mix(step ^ r*K)); row 0 is the unstructured base
+    for seed, step in [(0, 0), (3, 9), (2**64 - 1, 2**40)]:
+        assert oracle.row_base(seed, step, 0) == oracle.splitmix64_mix(seed ^ oracle.splitmix64_mix(step))
+        k = 0xD1B54A32D192ED03
+        for r in (1, 2, 1000):
+            want = oracle.splitmix64_mix(seed ^ oracle.splitmix64_mix(step ^ ((r * k) & (2**64 - 1))))
+            assert oracle.row_base(seed, step, r) == want
+
+
+def test_rows_invariants_random():
+    rng = np.random.default_rng(33)
+    for trial in range(150):
+        out_f = int(rng.integers(1, 15))
+        in_f = int(rng.integers(2, 25))
+        if trial % 2:
+            lay = wl.make_layer(out_f, in_f, fan_in=int(rng.integers(0, in_f // 2 + 1)), seed=trial)
+            row, col = lay.row, lay.col
+        else:
+            row, col = rand_pattern(rng, out_f, in_f, int(rng.integers(0, out_f * in_f // 2 + 1)))
+        nnz = row.shape[0]
+        val = rng.standard_normal(nnz)
+        if nnz and trial % 3 == 0:
+            val = np.round(val)
+            val[rng.random(nnz) < 0.3] = -0.0
+        if nnz and trial % 5 == 0:
+            val[rng.integers(0, nnz)] = np.nan
+        lens = np.bincount(row, minlength=out_f)
+        room = int(np.min(in_f - lens)) if out_f else 0
+        n = int(rng.integers(0, room + 1))
+        ro, co, so, draws = oracle.restructure_rows(out_f, in_f, row, col, val, n, trial, 2)
+        check_rows_invariants(out_f, in_f, row, col, val, n, ro, co, so)
+
+
+def test_rows_every_3x3_pattern():
+    rng = np.random.default_rng(8)
+    for mask in range(512):
+        p = np.array([i for i in range(9) if (mask >> i) & 1], dtype=np.int64)
+        row, col = (p // 3).astype(np.int32), (p % 3).astype(np.int32)
+        val = np.round(rng.standard_normal(p.size) * 2) / 2
+        lens = np.bincount(row, minlength=3)
+        for n in range(0, 4):
+            if np.any(np.minimum(n, lens) > 3 - lens):
+                with pytest.raises(oracle.RestructureError):
+                    oracle.restructure_rows(3, 3, row, col, val, n, mask, n)
+                continue
+            ro, co, so, _ = oracle.restructure_rows(3, 3, row, col, val, n, mask, n)
+            check_rows_invariants(3, 3, row, col, val, n, ro, co, so)
+
+
+def test_rows_are_independent():
+    # a row's output depends on that row only (its values, columns and index)
+    rng = np.random.default_rng(2)
+    lay = wl.make_layer(12, 40, fan_in=10, seed=4)
+    val = rng.standard_normal(lay.nnz)
+    a = oracle.restructure_rows(12, 40, lay.row, lay.col, val, 3, 6, 1)
+    val2 = val.copy()
+    val2[lay.row == 5] = rng.standard_normal(10)
+    b = oracle.restructure_rows(12, 40, lay.row, lay.col, val2, 3, 6, 1)
+    other = lay.row != 5
+    for x, y in zip(a[:3], b[:3]):
+        assert np.array_equal(x[other], y[other])
+
+
+def test_rows_regrow_uniform_within_row():
+    # one row of 16 columns holding 6: each regrown column is uniform over the 10 empty ones
+    row = np.zeros(6, np.int32)
+    col = np.array([0, 3, 4, 8, 11, 15], np.int32)
+    val = np.arange(1.0, 7.0)
+    empty = [c for c in range(16) if c not in set(col.tolist())]
+    counts = dict.fromkeys(empty, 0)
+    n_seeds = 4000
+    for seed in range(n_seeds):
+        ro, co, so, _ = oracle.restructure_rows(1, 16, row, col, val, 2, seed, 3)
+        for c in co[so < 0].tolist():
+            counts[c] += 1
+    obs = np.array([counts[c] for c in empty], dtype=np.float64)
+    exp = n_seeds * 2 / len(empty)
+    chi2 = float(np.sum((obs - exp) ** 2 / exp))
+    assert chi2 < 45, chi2  # 9 dof: beyond p = 1e-6
+
+
+def test_rows_errors():
+    row = np.array([0, 0, 1], np.int32)
+    col = np.array([0, 1, 0], np.int32)
+    with pytest.raises(oracle.RestructureError):
+        oracle.restructure_rows(2, 2, row, col, np.ones(3), 1, 0, 0)  # row 0 has no empty column
+    with pytest.raises(oracle.RestructureError):
+        oracle.restructure_rows(2, 3, row, col, np.ones(3), -1, 0, 0)
+    with pytest.raises(oracle.RestructureError):
+        oracle.restructure_rows(2, 1000, row, col, np.ones(3), 1, 0, 0, max_draws_per_row=0)
