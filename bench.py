@@ -699,6 +699,51 @@ def _c3_step(torch, F, snack, timer, reps, dev):
     return res
 
 
+def _fanin_restructure(torch, snack, timer, dev, reps):
+    """The structured DST variant on a 16384 x 16384 layer with a constant fan-in of
+    164 (99 % sparse): per-row restructure (16 of every row's 164) beside the
+    unstructured restructure of the same layer (10 % of all weights)."""
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    lay = wl.make_layer(16384, 16384, fan_in=164, val_std=0.02, val_dtype="f32", seed=0)
+    row = torch.from_numpy(lay.row).to(dev)
+    col = torch.from_numpy(lay.col).to(dev)
+    val = torch.from_numpy(lay.val).to(dev)
+    L = snack.SparseLinear(16384, 16384, row, col, val, None, max_batch=32)
+    h = L.handle
+    n_rows = 16
+    n_prune = int(PRUNE_FRAC * lay.nnz)
+    ws = torch.empty(max(snack.snack_restructure_rows_workspace_size(h, n_rows),
+                         snack.snack_restructure_workspace_size(h, n_prune)), dtype=torch.uint8, device=dev)
+    bufs = [(row, col, val), (torch.empty_like(row), torch.empty_like(col), torch.empty_like(val))]
+    src = torch.empty_like(row)
+    state = {"cur": 0, "i": 0}
+
+    def per_row():
+        a, b = bufs[state["cur"]], bufs[1 - state["cur"]]
+        snack.snack_restructure_rows(h, a[0], a[1], a[2], n_rows, 12345, state["i"], b[0], b[1], b[2], src, ws)
+        state["cur"] ^= 1
+        state["i"] += 1
+
+    def unstructured():
+        a, b = bufs[state["cur"]], bufs[1 - state["cur"]]
+        snack.snack_restructure(h, a[0], a[1], a[2], n_prune, 12345, state["i"], b[0], b[1], b[2], src, ws)
+        state["cur"] ^= 1
+        state["i"] += 1
+
+    out = []
+    byts = alg_bytes(lay.nnz, 32, 16384, 16384)["restructure"]
+    for name, fn in (("restructure_rows", per_row), ("restructure", unstructured)):
+        us = timer.time(fn, reps, True)
+        out.append({"config": "c4-fanin", "layer": "16384x16384", "nnz": lay.nnz, "batch": 0, "op": name,
+                    "dtype": "f32", "us_cold": us, "us_warm": timer.time(fn, reps, False), "graph": False,
+                    "alg_bytes": byts, "gbs": byts / (us * 1e-6) / 1e9, "frac_measured": None, "frac_nominal": None,
+                    "gflops": None, "frac_fma": None, "dense_us": None, "dense_mask_us": None, "oracle_us": None,
+                    "oracle_full": None, "oracle_cores": None})
+    L.close()
+    return out
+
+
 def run_configs(args):
     import torch
     import torch.nn.functional as F
@@ -738,6 +783,12 @@ def run_configs(args):
                     for rec in _layer_rows(name, lay, batch, ours, dense, mask, ot, peak, cores):
                         records.append(rec)
                         print(json.dumps(rec), flush=True)
+            if name == "c4":
+                for rec in _fanin_restructure(torch, snack, timer, dev, max(20, args.reps // 4)):
+                    rec["frac_measured"] = rec["gbs"] / peak
+                    rec["frac_nominal"] = rec["gbs"] / NOMINAL_HBM_GBS
+                    records.append(rec)
+                    print(json.dumps(rec), flush=True)
             if name == "c3":
                 rec = {"config": "c3", "op": "mlp_step", **_c3_step(torch, F, snack, timer, max(20, args.reps // 4),
                                                                      dev)}

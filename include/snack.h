@@ -235,6 +235,37 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
                                int32_t *row_out, int32_t *col_out, void *val_out, int32_t *src_out,
                                void *ws, size_t ws_bytes, snack_stream_t stream);
 
+/*
+ * Workspace needed by snack_restructure_rows.
+ */
+snack_status snack_restructure_rows_workspace_size(snack_handle h, int64_t n_per_row, size_t *bytes);
+
+/*
+ * Per-row (constant fan-in) restructure, the structured DST variant: Structured
+ * RigL (in the pages' list of N:M sparsification work) keeps a constant fan-in;
+ * restructuring row by row with equal counts preserves it.  Row r prunes its
+ * p_r = min(n_per_row, length of row r) smallest (|val|, k), ranked as in
+ * snack_restructure, and regrows p_r columns of row r that were empty before
+ * the call, with value +0, from the row's own stream:
+ *   base_r = mix(seed ^ mix(step ^ (r * 0xD1B54A32D192ED03))),
+ *   draw i: u = mix(base_r + (i + 1) * 0x9E3779B97F4A7C15),
+ *   column  = floor(u * in_f / 2^64),
+ * accepting a draw whose column was empty in the row and is not yet accepted,
+ * until p_r are accepted (64 * n_per_row + 2^20 draws at most per row).  Row
+ * 0's stream is snack_restructure's stream.  Every row keeps its count and its
+ * offsets, so the outputs (same meaning and rules as snack_restructure) hold
+ * row r at the same index range as the input, and only the column view of the
+ * plan is rebuilt.  Needs ws_bytes >= snack_restructure_rows_workspace_size.
+ * Returns SNACK_ERR_UNSUPPORTED when n_per_row > 256 or in_f > 65536, and
+ * SNACK_ERR_NO_SPACE when a row has fewer empty columns than it prunes or runs
+ * out of draws (the outputs are then undefined and the plan is unchanged).
+ * The host waits once for the device's error word.
+ */
+snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                    int64_t n_per_row, uint64_t seed, uint64_t step, int32_t *row_out,
+                                    int32_t *col_out, void *val_out, int32_t *src_out, void *ws, size_t ws_bytes,
+                                    snack_stream_t stream);
+
 /* Free the handle: its host memory, and the stream, events and pinned word of
  * a handle that has restructured (waits for that stream).  No device memory
  * of the caller is touched.  NULL is allowed. */

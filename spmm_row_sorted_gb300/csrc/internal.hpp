@@ -33,12 +33,15 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
 PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
-// Fill the plan for the pattern (row, col).  Asynchronous on s.  rp_ready
-// says the row offsets p.rp and the 16-bit column copy p.col16 are already in
-// place (a restructure's merge writes them).
+// Fill the plan for the pattern (row, col).  Asynchronous on s.  `ready`
+// names what is already in place: kPlanNothingReady (create),
+// kPlanRowsReady (the row offsets and the 16-bit column copy, written by a
+// restructure's merge), kPlanRowTilesReady (also the forward tiles: a
+// per-row restructure keeps every row's offsets).
+constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       bool rp_ready);
+                       int ready);
 
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
@@ -74,6 +77,25 @@ snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes
 constexpr int kDenseMinBatch = 32;
 bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t);
 size_t dense_ws_bytes(int32_t out_f, int32_t in_f);
+
+// Per-row (constant fan-in) restructure (restructure.cu): rows keep their
+// counts and offsets; the plan's row offsets and forward tiles stay valid.
+struct RowsRestructureArgs {
+  int32_t out_f, in_f;
+  int64_t nnz, n_per_row;
+  snack_dtype val_t;
+  uint64_t seed, step;
+  const int32_t *rp, *col;
+  const void *val;
+  int32_t *row_out, *col_out;
+  void *val_out;
+  int32_t *src_out;   // may be null
+  uint16_t *col16;    // plan's 16-bit column copy, or null
+  uint32_t *err;      // device word: nonzero after the kernel when a row cannot be restructured
+};
+// SNACK_OK, SNACK_ERR_UNSUPPORTED (n_per_row > 256 or in_f > 65536) or SNACK_ERR_CUDA; row
+// failures are reported through *err.
+snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s);
 
 // Host SplitMix64 (state increment and finaliser of Steele, Lea and Flood 2014).
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ULL;

@@ -410,7 +410,7 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz) { return bu
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       bool rp_ready) {
+                       int ready) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
@@ -419,13 +419,14 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
 
   // row offsets and the 16-bit column copy: already written by a
   // restructure's merge, made here otherwise
-  if (!rp_ready && p.col16 && nnz > 0) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, p.col16);
-  if (!rp_ready) {
+  if (ready < kPlanRowsReady && p.col16 && nnz > 0) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, p.col16);
+  if (ready < kPlanRowsReady) {
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
   }
-  k_tiles<<<grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s>>>(p.rp, out_f, nnz, gf.cost_per_tile,
-                                                                         gf.row_weight, gf.n_tiles, p.tiles_f);
+  if (ready < kPlanRowTilesReady)
+    k_tiles<<<grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s>>>(p.rp, out_f, nnz, gf.cost_per_tile,
+                                                                           gf.row_weight, gf.n_tiles, p.tiles_f);
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
   const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));

@@ -621,12 +621,270 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   return SNACK_OK;
 }
 
+// ------------------------------------------------------------------------
+// Per-row (constant fan-in) restructure: every row prunes its
+// p = min(n_per_row, length) smallest (|w|, k) and regrows p columns of the
+// same row that were empty, from the row's own draw stream
+// (base_r = mix(seed ^ mix(step ^ r*K))), so row counts and offsets do not
+// change.  One warp per row:
+//  1. radix select of the row's p-th smallest magnitude key (four 8-bit
+//     digits, a 256-bin histogram per warp) and the number of ties to prune;
+//  2. draws in groups of 32: a draw is a candidate when its column was empty
+//     in the row (binary search) and is not yet accepted; the first
+//     occurrence in the group (match_any) in draw order is accepted until p;
+//  3. the accepted columns are sorted (bitonic, shared memory), each with
+//     the number of old entries left of it;
+//  4. one pass over the row: survivor s lands at s + (grown columns left of
+//     it), the pruned columns are listed; regrown g lands at
+//     g + (old entries left of it) - (pruned entries left of it).
+
+constexpr int kRowsWarps = 8;
+constexpr int kRowsMaxPrune = 256;  // per row
+constexpr uint64_t kRowStreamK = 0xD1B54A32D192ED03ull;
+
+struct RowsArgs {
+  const int32_t *rp, *col;
+  const void *val;
+  int32_t out_f, in_f, n_per_row;
+  uint64_t seed, step;
+  int64_t max_draws;
+  int32_t *row_out, *col_out;
+  void *val_out;
+  int32_t *src_out;
+  uint16_t *col16;
+  uint32_t *err;  // bit 0: a row has fewer empty columns than it prunes; bit 1: a row ran out of draws
+};
+
+// one warp: the digit d of hist (256 bins) where the running count reaches
+// rank rem (1-based), and the count below d
+__device__ void warp_pick256(const uint32_t *hist, uint32_t rem, uint32_t *digit, uint32_t *before) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = hist[lane * 8 + i];
+    sum += h[i];
+  }
+  uint32_t inc = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += u;
+  }
+  const uint32_t ex = inc - sum;
+  const unsigned hit = __ballot_sync(0xffffffffu, inc >= rem && ex < rem);
+  const int src = hit ? __ffs(hit) - 1 : 31;
+  uint32_t dg = 255, bf = 0;
+  if (lane == src) {
+    uint32_t c = ex;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      if (c + h[i] >= rem) {
+        dg = lane * 8 + i;
+        bf = c;
+        break;
+      }
+      c += h[i];
+    }
+  }
+  *digit = __shfl_sync(0xffffffffu, dg, src);
+  *before = __shfl_sync(0xffffffffu, bf, src);
+}
+
+// first index in a[0..n) with a[i] >= v (a ascending)
+template <typename P>
+__device__ __forceinline__ int lower_bound_by(P at, int n, uint32_t v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (at(mid) < v)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+template <typename TV>
+__global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A) {
+  __shared__ uint32_t s_hist[kRowsWarps][256];
+  __shared__ uint32_t s_gcol[kRowsWarps][kRowsMaxPrune];
+  __shared__ uint32_t s_glb[kRowsWarps][kRowsMaxPrune];
+  __shared__ uint32_t s_pcol[kRowsWarps][kRowsMaxPrune];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int r = blockIdx.x * kRowsWarps + w;
+  if (r >= A.out_f) return;
+  const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
+  const TV *val = reinterpret_cast<const TV *>(A.val);
+  TV *val_out = reinterpret_cast<TV *>(A.val_out);
+  const int64_t k0 = A.rp[r];
+  const int L = (int)(A.rp[r + 1] - k0);
+  const int p = A.n_per_row < L ? A.n_per_row : L;
+  if (p > A.in_f - L) {
+    if (lane == 0) atomicOr(A.err, 1u);
+    return;
+  }
+  const int32_t *crow = A.col + k0;
+  uint32_t *hist = s_hist[w], *gcol = s_gcol[w], *glb = s_glb[w], *pcol = s_pcol[w];
+
+  // 1. threshold key t of rank p and the ties to prune
+  uint32_t t = 0, remaining = 0;
+  if (p > 0) {
+    uint32_t pfx = 0, mask = 0, rem = (uint32_t)p;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
+      __syncwarp();
+      for (int j = lane; j < L; j += 32) {
+        const uint32_t key = mag_key<TV>(val, k0 + j);
+        if ((key & mask) == pfx) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
+      }
+      __syncwarp();
+      uint32_t d, before;
+      warp_pick256(hist, rem, &d, &before);
+      pfx |= d << shift;
+      mask |= 0xFFu << shift;
+      rem -= before;
+      __syncwarp();
+    }
+    t = pfx;
+    remaining = rem;
+  }
+
+  // 2. regrow draws, groups of 32 in draw order
+  int n_acc = 0;
+  if (p > 0) {
+    const uint64_t base = sm64_finalise(A.seed ^ sm64_finalise(A.step ^ ((uint64_t)r * kRowStreamK)));
+    for (int64_t i0 = 0; n_acc < p; i0 += 32) {
+      if (i0 >= A.max_draws) {
+        if (lane == 0) atomicOr(A.err, 2u);
+        return;
+      }
+      const int64_t i = i0 + lane;
+      const uint64_t u = sm64_finalise(base + ((uint64_t)i + 1) * kGolden);
+      const uint32_t c = (uint32_t)__umul64hi(u, (uint64_t)A.in_f);
+      const int lb = lower_bound_by([&](int m) { return (uint32_t)crow[m]; }, L, c);
+      bool cand = i < A.max_draws && !(lb < L && (uint32_t)crow[lb] == c);
+      for (int a = 0; cand && a < n_acc; ++a) cand = gcol[a] != c;
+      const unsigned peers = __match_any_sync(full, cand ? c : (0x80000000u | (uint32_t)lane));
+      const bool first = cand && (__ffs(peers) - 1) == lane;
+      const unsigned bal = __ballot_sync(full, first);
+      const int rank = __popc(bal & lt);
+      if (first && n_acc + rank < p) {
+        gcol[n_acc + rank] = c;
+        glb[n_acc + rank] = (uint32_t)lb;
+      }
+      n_acc = min(p, n_acc + __popc(bal));
+      __syncwarp();
+    }
+    // 3. sort the accepted columns (and their left counts) ascending
+    int n2 = 1;
+    while (n2 < p) n2 <<= 1;
+    for (int q = p + lane; q < n2; q += 32) {
+      gcol[q] = 0xFFFFFFFFu;
+      glb[q] = 0;
+    }
+    __syncwarp();
+    for (int size = 2; size <= n2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int q = lane; q < n2; q += 32) {
+          const int o = q ^ stride;
+          if (o > q) {
+            const bool up = (q & size) == 0;
+            const uint32_t a = gcol[q], b = gcol[o];
+            if ((a > b) == up) {
+              gcol[q] = b;
+              gcol[o] = a;
+              const uint32_t x = glb[q];
+              glb[q] = glb[o];
+              glb[o] = x;
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+
+  // 4. survivors in storage order; the pruned columns are listed in order
+  uint32_t carry_eq = 0, carry_keep = 0, n_pr = 0;
+  for (int j0 = 0; j0 < L; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < L;
+    const uint32_t key = in ? mag_key<TV>(val, k0 + j) : 0u;
+    const uint32_t c = in ? (uint32_t)crow[j] : 0u;
+    const bool eq = in && p > 0 && key == t;
+    const unsigned eqb = __ballot_sync(full, eq);
+    const uint32_t eq_rank = carry_eq + __popc(eqb & lt);
+    const bool keep = in && (p == 0 || key > t || (eq && eq_rank >= remaining));
+    const unsigned kb = __ballot_sync(full, keep), pb = __ballot_sync(full, in && !keep);
+    const uint32_t pos =
+        keep ? carry_keep + __popc(kb & lt) + (uint32_t)lower_bound_by([&](int m) { return gcol[m]; }, p, c) : 0u;
+    if (keep && pos < (uint32_t)L) {  // always true; the test keeps every store inside the row
+      const int64_t o = k0 + pos;
+      A.row_out[o] = r;
+      A.col_out[o] = (int32_t)c;
+      val_out[o] = val[k0 + j];
+      if (A.src_out) A.src_out[o] = (int32_t)(k0 + j);
+      if (A.col16) A.col16[o] = (uint16_t)c;
+    } else if (in && !keep && n_pr + __popc(pb & lt) < (uint32_t)kRowsMaxPrune) {
+      pcol[n_pr + __popc(pb & lt)] = c;
+    }
+    carry_eq += __popc(eqb);
+    carry_keep += __popc(kb);
+    n_pr += __popc(pb);
+  }
+  __syncwarp();
+  // 5. regrown entries
+  for (int g = lane; g < p; g += 32) {
+    const uint32_t c = gcol[g];
+    const int pl = lower_bound_by([&](int m) { return pcol[m]; }, (int)min(n_pr, (uint32_t)kRowsMaxPrune), c);
+    const int64_t off = g + (int64_t)glb[g] - pl;
+    if (off < 0 || off >= L) continue;  // never; keeps every store inside the row
+    const int64_t o = k0 + off;
+    A.row_out[o] = r;
+    A.col_out[o] = (int32_t)c;
+    val_out[o] = from_f32<TV>(0.f);
+    if (A.src_out) A.src_out[o] = -1;
+    if (A.col16) A.col16[o] = (uint16_t)c;
+  }
+}
+
 }  // namespace
 
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
   size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
   return r > p ? r : p;
+}
+
+snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) {
+  if (a.n_per_row > kRowsMaxPrune || a.in_f > 65536) return SNACK_ERR_UNSUPPORTED;
+  RowsArgs A;
+  A.rp = a.rp;
+  A.col = a.col;
+  A.val = a.val;
+  A.out_f = a.out_f;
+  A.in_f = a.in_f;
+  A.n_per_row = (int32_t)a.n_per_row;
+  A.seed = a.seed;
+  A.step = a.step;
+  A.max_draws = 64 * (int64_t)a.n_per_row + (1 << 20);
+  A.row_out = a.row_out;
+  A.col_out = a.col_out;
+  A.val_out = a.val_out;
+  A.src_out = a.src_out;
+  A.col16 = a.col16;
+  A.err = a.err;
+  if (cudaMemsetAsync(a.err, 0, sizeof(uint32_t), s) != cudaSuccess) return SNACK_ERR_CUDA;
+  const unsigned grid = (unsigned)((a.out_f + kRowsWarps - 1) / kRowsWarps);
+  if (a.val_t == SNACK_BF16)
+    k_restructure_rows<bf16><<<grid, kRowsWarps * 32, 0, s>>>(A);
+  else
+    k_restructure_rows<float><<<grid, kRowsWarps * 32, 0, s>>>(A);
+  if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
+  return SNACK_OK;
 }
 
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {

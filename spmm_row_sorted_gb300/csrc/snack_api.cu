@@ -278,6 +278,19 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   return SNACK_OK;
 }
 
+// Pinned host words and an event for reading small device results back
+// (made on a handle's first restructure).
+bool readback_ready(snack_handle h) {
+  if (!h->host_counts) {
+    void *hp = nullptr;
+    if (cudaHostAlloc(&hp, 2 * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) return false;
+    h->host_counts = reinterpret_cast<uint32_t *>(hp);
+  }
+  if (!h->counts_ready && cudaEventCreateWithFlags(&h->counts_ready, cudaEventDisableTiming) != cudaSuccess)
+    return false;
+  return true;
+}
+
 // Dense path: a dense layer, a wide batch, and room for the dense copy.
 bool use_dense(snack_handle h, int32_t batch, size_t ws_bytes) {
   return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f);
@@ -338,7 +351,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
     if (flag & 1u) return SNACK_ERR_OUT_OF_RANGE;
     if (flag & 2u) return SNACK_ERR_UNSORTED;
   }
-  SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s, false));
+  SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s, kPlanNothingReady));
   snack_layer *h = new (std::nothrow) snack_layer;
   if (!h) return SNACK_ERR_INVALID_ARG;
   h->device = dev;
@@ -530,13 +543,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.col_out = col_out;
   a.val_out = val_out;
   a.src_out = src_out;
-  if (!h->host_counts) {
-    void *hp = nullptr;
-    if (cudaHostAlloc(&hp, 2 * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) return SNACK_ERR_CUDA;
-    h->host_counts = reinterpret_cast<uint32_t *>(hp);
-  }
-  if (!h->counts_ready && cudaEventCreateWithFlags(&h->counts_ready, cudaEventDisableTiming) != cudaSuccess)
-    return SNACK_ERR_CUDA;
+  if (!readback_ready(h)) return SNACK_ERR_CUDA;
   if (!h->ev_fork && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
   if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
@@ -549,7 +556,68 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.ev_join = h->ev_join;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
-  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, true));
+  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady));
+  return SNACK_OK;
+}
+
+snack_status snack_restructure_rows_workspace_size(snack_handle h, int64_t n_per_row, size_t *bytes) {
+  if (!h || !bytes || n_per_row < 0) return SNACK_ERR_INVALID_ARG;
+  *bytes = kAlign + plan_build_ws_bytes(h->out_f, h->in_f, h->nnz);
+  return SNACK_OK;
+}
+
+snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
+                                    int64_t n_per_row, uint64_t seed, uint64_t step, int32_t *row_out,
+                                    int32_t *col_out, void *val_out, int32_t *src_out, void *ws, size_t ws_bytes,
+                                    snack_stream_t stream) {
+  if (!h || n_per_row < 0) return SNACK_ERR_INVALID_ARG;
+  if (n_per_row > 256 || h->in_f > 65536) return SNACK_ERR_UNSUPPORTED;
+  const int64_t nnz = h->nnz;
+  if (!ws || !aligned(ws, kAlign)) return SNACK_ERR_INVALID_ARG;
+  if (nnz > 0 && (!row || !col || !val || !row_out || !col_out || !val_out)) return SNACK_ERR_INVALID_ARG;
+  const size_t n4 = 4 * (size_t)nnz, nv = dtype_size(h->val_t) * (size_t)nnz;
+  const void *ins[3] = {row, col, val};
+  const size_t in_sz[3] = {n4, n4, nv};
+  const void *outs[4] = {row_out, col_out, val_out, src_out};
+  const size_t out_sz[4] = {n4, n4, nv, src_out ? n4 : 0};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(outs[i], out_sz[i], ins[j], in_sz[j])) return SNACK_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(outs[i], out_sz[i], outs[j], out_sz[j])) return SNACK_ERR_INVALID_ARG;
+  }
+  if (ws_bytes < kAlign + plan_build_ws_bytes(h->out_f, h->in_f, nnz)) return SNACK_ERR_WORKSPACE;
+  if (nnz == 0) return SNACK_OK;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  if (!readback_ready(h)) return SNACK_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *b = reinterpret_cast<uint8_t *>(ws);
+  RowsRestructureArgs a;
+  a.out_f = h->out_f;
+  a.in_f = h->in_f;
+  a.nnz = nnz;
+  a.n_per_row = n_per_row;
+  a.val_t = h->val_t;
+  a.seed = seed;
+  a.step = step;
+  a.rp = h->p.rp;
+  a.col = col;
+  a.val = val;
+  a.row_out = row_out;
+  a.col_out = col_out;
+  a.val_out = val_out;
+  a.src_out = src_out;
+  a.col16 = h->p.col16;
+  a.err = reinterpret_cast<uint32_t *>(b);
+  snack_status st = run_restructure_rows(a, s);
+  if (st != SNACK_OK) return st;
+  SNACK_CUDA(cudaMemcpyAsync(h->host_counts, a.err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+  SNACK_CUDA(cudaEventRecord(h->counts_ready, s));
+  SNACK_CUDA(cudaEventSynchronize(h->counts_ready));
+  if (h->host_counts[0]) return SNACK_ERR_NO_SPACE;
+  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, b + kAlign, s,
+                        kPlanRowTilesReady));
   return SNACK_OK;
 }
 

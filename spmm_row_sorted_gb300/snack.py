@@ -30,8 +30,8 @@ SNACK_F32, SNACK_BF16 = 0, 1
 
 EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
             "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw", "snack_backward",
-            "snack_restructure_workspace_size", "snack_restructure", "snack_destroy", "snack_status_string",
-            "snack_version")
+            "snack_restructure_workspace_size", "snack_restructure", "snack_restructure_rows_workspace_size",
+            "snack_restructure_rows", "snack_destroy", "snack_status_string", "snack_version")
 
 
 class SnackLibraryMissing(RuntimeError):
@@ -87,6 +87,10 @@ def load(path: Optional[str] = None):
         lib.snack_restructure_workspace_size.restype = st
         lib.snack_restructure.argtypes = [vp, vp, vp, vp, i64, u64, u64, vp, vp, vp, vp, vp, sz, vp]
         lib.snack_restructure.restype = st
+        lib.snack_restructure_rows_workspace_size.argtypes = [vp, i64, ctypes.POINTER(sz)]
+        lib.snack_restructure_rows_workspace_size.restype = st
+        lib.snack_restructure_rows.argtypes = [vp, vp, vp, vp, i64, u64, u64, vp, vp, vp, vp, vp, sz, vp]
+        lib.snack_restructure_rows.restype = st
         lib.snack_destroy.argtypes = [vp]
         lib.snack_destroy.restype = None
         lib.snack_status_string.argtypes = [st]
@@ -206,6 +210,21 @@ def snack_restructure(h: int, row, col, val, n_prune: int, seed: int, step: int,
                                     _ptr(val_out), _ptr(src_out), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
+def snack_restructure_rows_workspace_size(h: int, n_per_row: int) -> int:
+    b = ctypes.c_size_t(0)
+    _check("snack_restructure_rows_workspace_size",
+           load().snack_restructure_rows_workspace_size(ctypes.c_void_p(h), n_per_row, ctypes.byref(b)))
+    return b.value
+
+
+def snack_restructure_rows(h: int, row, col, val, n_per_row: int, seed: int, step: int, row_out, col_out, val_out,
+                           src_out, ws, stream=None) -> None:
+    _check("snack_restructure_rows",
+           load().snack_restructure_rows(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), n_per_row,
+                                         seed & (2**64 - 1), step & (2**64 - 1), _ptr(row_out), _ptr(col_out),
+                                         _ptr(val_out), _ptr(src_out), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
 def snack_destroy(h: int) -> None:
     load().snack_destroy(ctypes.c_void_p(h))
 
@@ -315,6 +334,19 @@ class SparseLinear:
         src_o = torch.empty_like(self.row)
         snack_restructure(self.handle, self.row, self.col, self.val, n_prune, seed, step, row_o, col_o, val_o,
                           src_o, ws, stream)
+        self.row, self.col, self.val = row_o, col_o, val_o
+        return src_o
+
+    def restructure_rows(self, n_per_row: int, seed: int, step: int, stream=None) -> torch.Tensor:
+        """Per-row (constant fan-in) prune/regrow in place; returns src index (-1 = regrown)."""
+        need = snack_restructure_rows_workspace_size(self.handle, n_per_row)
+        ws = self.ws if need <= _nbytes(self.ws) else torch.empty(need, dtype=torch.uint8, device=self.val.device)
+        row_o = torch.empty_like(self.row)
+        col_o = torch.empty_like(self.col)
+        val_o = torch.empty_like(self.val)
+        src_o = torch.empty_like(self.row)
+        snack_restructure_rows(self.handle, self.row, self.col, self.val, n_per_row, seed, step, row_o, col_o, val_o,
+                               src_o, ws, stream)
         self.row, self.col, self.val = row_o, col_o, val_o
         return src_o
 

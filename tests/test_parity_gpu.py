@@ -411,3 +411,104 @@ def test_index_width_boundaries(shape):
         acts = wl.make_acts(9, in_f, out_f, dtype, seed=1)
         check_layer_ops(lay, acts)
     restructure_and_check(lay, nnz // 10, seed=1, step=1, acts=acts)
+
+
+# ---------------------------------------------------------------- per-row (constant fan-in) restructure
+
+def restructure_rows_and_check(lay: wl.Layer, n_per_row: int, seed: int, step: int, acts=None):
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(lay.out_f, lay.in_f, row, col, val, bias, max_batch=acts.batch if acts else 8)
+    src = L.restructure_rows(n_per_row, seed, step)
+    torch.cuda.synchronize()
+    ro, co, so, _ = oracle.restructure_rows(lay.out_f, lay.in_f, lay.row, lay.col,
+                                            oracle.as_f64(lay.val, lay.val_dtype), n_per_row, seed, step)
+    assert np.array_equal(L.row.cpu().numpy(), ro), "row_out"
+    assert np.array_equal(L.col.cpu().numpy(), co), "col_out"
+    assert np.array_equal(src.cpu().numpy(), so.astype(np.int32)), "src_out"
+    vo = oracle.restructure_values(lay.val, so)
+    want_bits = vo.view(np.uint32) if lay.val_dtype == "f32" else vo.view(np.uint16)
+    assert np.array_equal(bits(L.val), want_bits), "val_out bits"
+    if acts is not None:  # the rebuilt column view serves the new pattern
+        new = wl.Layer(lay.out_f, lay.in_f, ro, co, vo, lay.bias, lay.val_dtype)
+        x = act_tensor(acts.x, acts.act_dtype)
+        dy = act_tensor(acts.dy, acts.act_dtype)
+        got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+        got["dw"], got["db"] = L.grad_weight(x, dy)
+        torch.cuda.synchronize()
+        check_layer_ops(new, acts, got=got)
+    L.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", [("fanin", 300, 500, 40, 4), ("fanin", 64, 1000, 300, 256), ("zipf", 400, 3000, 9000, 12),
+                                  ("uniform", 200, 333, 5000, 3), ("fanin", 50, 70, 10, 0)])
+def test_restructure_rows_matches_oracle(dtype, case):
+    kind, out_f, in_f, size, n = case
+    if kind == "fanin":
+        lay = wl.make_layer(out_f, in_f, fan_in=size, val_std=0.3, val_dtype=dtype, seed=out_f, bias="normal")
+    elif kind == "zipf":
+        lay = wl.make_layer(out_f, in_f, nnz=size, zipf_s=1.2, val_std=0.3, val_dtype=dtype, seed=out_f, bias="normal")
+    else:
+        lay = wl.make_layer(out_f, in_f, nnz=size, val_std=0.3, val_dtype=dtype, seed=out_f, bias="normal")
+    acts = wl.make_acts(16, in_f, out_f, dtype, seed=2)
+    restructure_rows_and_check(lay, n, seed=7, step=3, acts=acts)
+
+
+def test_restructure_rows_ties_nan_and_chain():
+    lay = wl.make_layer(40, 64, fan_in=16, val_std=1.0, val_dtype="f32", seed=3, bias="normal")
+    v = np.round(lay.val).astype(np.float32)
+    v[::7] = -0.0
+    v[5] = np.nan
+    lay.val = v
+    restructure_rows_and_check(lay, 5, seed=1, step=0)
+    # a chain of steps on one handle, against the oracle chain
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(40, 64, row, col, val, bias, max_batch=8)
+    r, c, vv = lay.row, lay.col, oracle.as_f64(lay.val)
+    for step in range(4):
+        L.restructure_rows(3, 11, step)
+        r, c, so, _ = oracle.restructure_rows(40, 64, r, c, vv, 3, 11, step)
+        vv = np.where(so >= 0, vv[np.maximum(so, 0)], 0.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(L.col.cpu().numpy(), c) and np.array_equal(L.row.cpu().numpy(), r)
+    L.close()
+
+
+def test_restructure_rows_workload_c4_fanin():
+    # 16384 x 16384 with a constant fan-in of 164 (99 % sparse), 10 % of every row per call
+    lay = wl.make_layer(16384, 16384, fan_in=164, val_std=0.02, val_dtype="f32", seed=0)
+    acts = wl.make_acts(32, 16384, 16384, "f32", seed=0)
+    restructure_rows_and_check(lay, 16, seed=12345, step=1, acts=acts)
+
+
+def test_restructure_rows_full_row_is_no_space_like_the_oracle():
+    # Zipf rows saturate: the longest row holds every column, so it cannot regrow
+    lay = wl.make_layer(400, 600, nnz=9000, zipf_s=1.2, val_std=0.3, val_dtype="f32", seed=400)
+    with pytest.raises(oracle.RestructureError):
+        oracle.restructure_rows(400, 600, lay.row, lay.col, oracle.as_f64(lay.val), 12, 7, 3)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(400, 600, row, col, val, bias, max_batch=4)
+    with pytest.raises(snack.SnackError) as e:
+        L.restructure_rows(12, 7, 3)
+    assert e.value.status == 8
+    L.close()
+
+
+def test_restructure_rows_errors():
+    lay = wl.make_layer(4, 8, fan_in=8, val_dtype="f32", seed=1)  # every row full
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(4, 8, row, col, val, bias, max_batch=4)
+    with pytest.raises(snack.SnackError) as e:
+        L.restructure_rows(1, 0, 0)
+    assert e.value.status == 8  # NO_SPACE
+    with pytest.raises(snack.SnackError) as e:
+        L.restructure_rows(257, 0, 0)
+    assert e.value.status == 7  # UNSUPPORTED
+    L.close()
+    wide = wl.make_layer(3, 70000, fan_in=5, val_dtype="f32", seed=1)
+    row, col, val, bias = layer_tensors(wide)
+    L = snack.SparseLinear(3, 70000, row, col, val, bias, max_batch=4)
+    with pytest.raises(snack.SnackError) as e:
+        L.restructure_rows(1, 0, 0)
+    assert e.value.status == 7
+    L.close()
