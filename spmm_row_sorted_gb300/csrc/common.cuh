@@ -17,6 +17,34 @@ __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + 
 
 typedef __nv_bfloat16 bf16;
 
+// ------------------------------------------------------- dependent launches
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization: its blocks may be scheduled while the kernel before it on
+// the stream is still draining, and its first instruction waits until that
+// kernel has completed and its writes are visible (griddepcontrol.wait).
+// Nothing a kernel does comes before that wait, so the stream order of
+// results is unchanged; what overlaps is the launch and block scheduling,
+// about 4 us per dependent launch on GB300 otherwise.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ---------------------------------------------------------------- loads
 
 // Streamed once: evict-first in L1 and L2.

@@ -10,7 +10,8 @@
 //   weight grad  G = dY^T X (fp32);                 dW[k] = G[row_k, col_k]
 //
 // Results equal the definitions up to the order of the fp32 sums, the same
-// contract as the gather kernels.
+// contract as the gather kernels.  The kernels here are launched plainly
+// (not as dependent launches): they sit next to cuBLASLt's GEMM.
 #include <cublasLt.h>
 
 #include "internal.hpp"
@@ -26,6 +27,7 @@ constexpr int kDensifyChunk = 8192;  // columns of one row staged in shared memo
 template <typename I>
 __global__ void __launch_bounds__(256) k_densify(const int32_t *__restrict__ rp, const I *__restrict__ col,
                                                  const bf16 *__restrict__ val, int32_t in_f, bf16 *__restrict__ wd) {
+  pdl_wait();
   __shared__ __align__(16) bf16 row_buf[kDensifyChunk];
   const int r = blockIdx.x;
   const int64_t k0 = rp[r], k1 = rp[r + 1];
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(256) k_densify(const int32_t *__restrict__ rp,
 // dW[k] = G[row_k][col_k], one block per row of G.
 __global__ void __launch_bounds__(256) k_gather_dw(const int32_t *__restrict__ rp, const int32_t *__restrict__ col,
                                                    const float *__restrict__ g, int32_t in_f, float *__restrict__ dw) {
+  pdl_wait();
   const int r = blockIdx.x;
   const float *gr = g + (size_t)r * in_f;
   const int64_t k1 = rp[r + 1];
@@ -85,6 +88,7 @@ __global__ void __launch_bounds__(256) k_gather_dw(const int32_t *__restrict__ r
 
 // y[b][r] += bias[r]
 __global__ void k_add_bias(bf16 *__restrict__ y, const float *__restrict__ bias, int batch, int n) {
+  pdl_wait();
   const int64_t total = (int64_t)batch * n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
     y[i] = __float2bfloat16(__bfloat162float(y[i]) + bias[i % n]);
@@ -92,6 +96,7 @@ __global__ void k_add_bias(bf16 *__restrict__ y, const float *__restrict__ bias,
 
 // db[r] = sum_b dy[b][r], b increasing
 __global__ void k_colsum_bf16(const bf16 *__restrict__ a, int batch, int n, float *__restrict__ out) {
+  pdl_wait();
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= n) return;
   float s = 0.f;
@@ -210,8 +215,7 @@ snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, cons
               h->in_f, x, h->in_f, y, h->out_f, CUDA_R_16BF, b + W.lt, s) != cudaSuccess)
     return SNACK_ERR_CUDA;
   if (bias) {
-    k_add_bias<<<grid_of((int64_t)batch * h->out_f, 256), 256, 0, s>>>(reinterpret_cast<bf16 *>(y), bias, batch,
-                                                                         h->out_f);
+    k_add_bias<<<grid_of((int64_t)batch * h->out_f, 256), 256, 0, s>>>(reinterpret_cast<bf16 *>(y), bias, batch, h->out_f);
     if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   }
   return SNACK_OK;

@@ -54,6 +54,7 @@ struct ColviewDst {
 
 // counts[clamp(idx[k])] += 1, aggregated over equal indices within a warp
 __global__ void k_count(const int32_t *__restrict__ idx, int64_t nnz, int32_t n, uint32_t *__restrict__ counts) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < nnz; base += stride) {
     int64_t k = base + threadIdx.x;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
                                                                   int32_t in_f, int32_t *__restrict__ row_t,
                                                                   int32_t *__restrict__ src_t, int32_t *__restrict__ cp,
                                                                   uint16_t *__restrict__ rowt16) {
+  pdl_wait();
   __shared__ uint32_t wc[kRadixWarps][kColLowMax];  // per-warp counts of a chunk, then local offsets
   __shared__ uint32_t run[kColLowMax];              // next free global slot of each column
   __shared__ uint32_t lstart[kColLowMax];           // start of each column's run inside the staged chunk
@@ -236,6 +238,7 @@ struct WriteOffsets {
 // so a 16K-row search takes three dependent rounds instead of fourteen.
 __global__ void k_tiles(const int32_t *__restrict__ ptr, int32_t n_rows, int64_t nnz, int32_t C, int32_t w,
                         int32_t n_tiles, int32_t *__restrict__ tiles) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t > n_tiles) return;
@@ -273,6 +276,7 @@ __global__ void k_tiles(const int32_t *__restrict__ ptr, int32_t n_rows, int64_t
 // atomics; indices are clamped, so writes stay in [0, n].
 template <typename I>
 __global__ void k_offsets_sorted(const I *__restrict__ idx, int64_t nnz, int32_t n, int32_t *__restrict__ ptr) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k <= nnz; k += stride) {
     const int r_prev = k > 0 ? (int)clamp_idx((int32_t)idx[k - 1], n) : -1;
@@ -285,6 +289,7 @@ __global__ void k_offsets_sorted(const I *__restrict__ idx, int64_t nnz, int32_t
 // bound on the host): dst[k] = min(src[k], 65535) as uint16, clamped so a
 // bad input can never produce an index past the bound.
 __global__ void k_pack16(const int32_t *__restrict__ src, int64_t n, uint16_t *__restrict__ dst) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
     const uint32_t v = (uint32_t)src[k];
@@ -294,6 +299,7 @@ __global__ void k_pack16(const int32_t *__restrict__ src, int64_t n, uint16_t *_
 
 __global__ void k_validate(const int32_t *__restrict__ row, const int32_t *__restrict__ col, int64_t nnz, int32_t out_f,
                            int32_t in_f, uint32_t *__restrict__ flag) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   uint32_t bad = 0;
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < nnz; k += stride) {
@@ -324,7 +330,7 @@ cudaError_t build_offsets(const int32_t *idx, int64_t nnz, int32_t n, int32_t *p
                           cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(uint32_t) * ((size_t)n + 1), s);
   if (e != cudaSuccess) return e;
-  if (nnz > 0) k_count<<<grid_for(nnz, 256), 256, 0, s>>>(idx, nnz, n, counts);
+  if (nnz > 0) launch_pdl(k_count, grid_for(nnz, 256), 256, 0, s, idx, nnz, n, counts);
   return scan_apply<uint32_t>(CountRead{counts, (int64_t)n}, (int64_t)n + 1, WriteOffsets{ptr}, (uint32_t *)nullptr,
                               stemp, s);
 }
@@ -419,13 +425,13 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
 
   // row offsets and the 16-bit column copy: already written by a
   // restructure's merge, made here otherwise
-  if (ready < kPlanRowsReady && p.col16 && nnz > 0) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(col, nnz, p.col16);
+  if (ready < kPlanRowsReady && p.col16 && nnz > 0) launch_pdl(k_pack16, grid_for(nnz, 256), 256, 0, s, col, nnz, p.col16);
   if (ready < kPlanRowsReady) {
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
   }
   if (ready < kPlanRowTilesReady)
-    k_tiles<<<grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s>>>(p.rp, out_f, nnz, gf.cost_per_tile,
+    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s, p.rp, out_f, nnz, gf.cost_per_tile,
                                                                            gf.row_weight, gf.n_tiles, p.tiles_f);
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
@@ -445,7 +451,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
                              offs, t + 2 * hbytes, s);
     if (e != cudaSuccess) return e;
-    k_colview_bucket<<<kRadixBins, kRadixThreads, 0, s>>>(ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
+    launch_pdl(k_colview_bucket, kRadixBins, kRadixThreads, 0, s, ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
                                                           p.cp, p.rowt16);
   } else if (nnz > 0) {
     uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
@@ -456,12 +462,12 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     e = radix_sort_custom<uint32_t>(ColSrc{col, in_f}, ColviewDst{keys_out, p.row_t, p.src_t, row, out_f}, nnz,
                                     cbits, ka, va, kb, vb, b + W.radix, s);
     if (e != cudaSuccess) return e;
-    k_offsets_sorted<uint32_t><<<grid_for(nnz + 1, 256), 256, 0, s>>>(keys_out, nnz, in_f, p.cp);
-    if (p.rowt16) k_pack16<<<grid_for(nnz, 256), 256, 0, s>>>(p.row_t, nnz, p.rowt16);
+    launch_pdl(k_offsets_sorted<uint32_t>, grid_for(nnz + 1, 256), 256, 0, s, keys_out, nnz, in_f, p.cp);
+    if (p.rowt16) launch_pdl(k_pack16, grid_for(nnz, 256), 256, 0, s, p.row_t, nnz, p.rowt16);
   } else {
-    k_offsets_sorted<int32_t><<<1, 256, 0, s>>>(col, 0, in_f, p.cp);
+    launch_pdl(k_offsets_sorted<int32_t>, 1, 256, 0, s, col, 0, in_f, p.cp);
   }
-  k_tiles<<<grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, s>>>(p.cp, in_f, nnz, gt.cost_per_tile,
+  launch_pdl(k_tiles, grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, s, p.cp, in_f, nnz, gt.cost_per_tile,
                                                                          gt.row_weight, gt.n_tiles, p.tiles_t);
   return cudaGetLastError();
 }
@@ -470,7 +476,7 @@ cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int
                              uint32_t *flag, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
-  if (nnz > 0) k_validate<<<grid_for(nnz, 256), 256, 0, s>>>(row, col, nnz, out_f, in_f, flag);
+  if (nnz > 0) launch_pdl(k_validate, grid_for(nnz, 256), 256, 0, s, row, col, nnz, out_f, in_f, flag);
   return cudaGetLastError();
 }
 

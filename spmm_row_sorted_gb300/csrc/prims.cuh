@@ -69,6 +69,7 @@ struct NoPayload {
 
 template <typename T, typename F>
 __global__ void __launch_bounds__(kScanThreads) k_scan_reduce(F f, int64_t n, T *block_sums) {
+  pdl_wait();
   const int64_t base = (int64_t)blockIdx.x * kScanTile;
   T s = 0;
 #pragma unroll
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_reduce(F f, int64_t n, T 
 // One block: exclusive scan of the block sums in place; grand total to *total.
 template <typename T>
 __global__ void __launch_bounds__(kScanThreads) k_scan_spine(T *sums, int64_t nb, T *total) {
+  pdl_wait();
   __shared__ T chunk_tot;
   T carry = 0;
   for (int64_t c = 0; c < nb; c += kScanThreads) {
@@ -108,6 +110,7 @@ constexpr int64_t kScanDirectTiles = 2048;
 template <typename T, bool kDirect, typename F, typename PL, typename Out>
 __global__ void __launch_bounds__(kScanThreads) k_scan_down(F f, PL pl, int64_t n, const T *block_sums, Out out,
                                                             T *d_total) {
+  pdl_wait();
   constexpr int kPadded = kScanTile + kScanTile / (128 / sizeof(T));
   __shared__ T tile[kPadded];
   __shared__ T tile_ex[kPadded];
@@ -176,12 +179,12 @@ cudaError_t scan_apply_pl(F f, PL pl, int64_t n, Out out, T *d_total, void *temp
   }
   const int64_t nb = ceil_div(n, kScanTile);
   T *sums = reinterpret_cast<T *>(temp);
-  k_scan_reduce<T, F><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, n, sums);
+  launch_pdl(k_scan_reduce<T, F>, (unsigned)nb, kScanThreads, 0, stream, f, n, sums);
   if (nb <= kScanDirectTiles) {
-    k_scan_down<T, true, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out, d_total);
+    launch_pdl(k_scan_down<T, true, F, PL, Out>, (unsigned)nb, kScanThreads, 0, stream, f, pl, n, sums, out, d_total);
   } else {
-    k_scan_spine<T><<<1, kScanThreads, 0, stream>>>(sums, nb, d_total);
-    k_scan_down<T, false, F, PL, Out><<<(unsigned)nb, kScanThreads, 0, stream>>>(f, pl, n, sums, out, d_total);
+    launch_pdl(k_scan_spine<T>, 1, kScanThreads, 0, stream, sums, nb, d_total);
+    launch_pdl(k_scan_down<T, false, F, PL, Out>, (unsigned)nb, kScanThreads, 0, stream, f, pl, n, sums, out, d_total);
   }
   return cudaGetLastError();
 }
@@ -226,6 +229,7 @@ struct ArrayDst {
 template <typename K, typename Src>
 __global__ void __launch_bounds__(kRadixThreads) k_radix_hist(Src src, int64_t n, int shift, uint32_t *hist,
                                                               int64_t nb) {
+  pdl_wait();
   __shared__ uint32_t h[kRadixWarps][kRadixBins];  // one histogram per warp: less atomic contention
   const int warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kRadixWarps * kRadixBins; i += kRadixThreads) (&h[0][0])[i] = 0;
@@ -261,6 +265,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_radix_hist(Src src, int64_t n
 template <typename K, typename Src, typename Dst>
 __global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(Src src, Dst dst, int64_t n, int shift,
                                                                  const uint32_t *offs, int64_t nb) {
+  pdl_wait();
   __shared__ uint32_t cnt[kRadixWarps][kRadixBins];
   __shared__ uint32_t dig_start[kRadixBins];
   __shared__ uint32_t glob[kRadixBins];
@@ -378,14 +383,14 @@ template <typename K, typename Src, typename Dst>
 cudaError_t radix_pass(Src src, Dst dst, int64_t n, int shift, uint32_t *hist, uint32_t *offs, void *stemp,
                        cudaStream_t stream) {
   const int64_t nb = ceil_div(n, kRadixTile);
-  k_radix_hist<K, Src><<<(unsigned)nb, kRadixThreads, 0, stream>>>(src, n, shift, hist, nb);
+  launch_pdl(k_radix_hist<K, Src>, (unsigned)nb, kRadixThreads, 0, stream, src, n, shift, hist, nb);
   cudaError_t e = scan_apply<uint32_t>(HistRead{hist}, nb * kRadixBins, WriteExcl32{offs}, (uint32_t *)nullptr,
                                        stemp, stream);
   if (e != cudaSuccess) return e;
   const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
   e = cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
-  k_radix_scatter<K, Src, Dst><<<(unsigned)nb, kRadixThreads, dyn, stream>>>(src, dst, n, shift, offs, nb);
+  launch_pdl(k_radix_scatter<K, Src, Dst>, (unsigned)nb, kRadixThreads, dyn, stream, src, dst, n, shift, offs, nb);
   return cudaGetLastError();
 }
 
@@ -441,6 +446,7 @@ __device__ __forceinline__ uint32_t bucket_of(uint64_t key, double scale, uint32
 
 static __global__ void k_bucket_count(const uint64_t *__restrict__ keys, int64_t n, double scale, uint32_t nb,
                                uint32_t *__restrict__ counts) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     atomicAdd(&counts[bucket_of(keys[i], scale, nb)], 1u);
@@ -449,6 +455,7 @@ static __global__ void k_bucket_count(const uint64_t *__restrict__ keys, int64_t
 static __global__ void k_bucket_fill(const uint64_t *__restrict__ keys, int64_t n, double scale, uint32_t nb,
                               const uint32_t *__restrict__ offs, uint32_t *__restrict__ fill,
                               uint64_t *__restrict__ tmp) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     const uint64_t k = keys[i];
@@ -459,6 +466,7 @@ static __global__ void k_bucket_fill(const uint64_t *__restrict__ keys, int64_t 
 
 static __global__ void __launch_bounds__(256) k_bucket_rank(const uint64_t *__restrict__ tmp, const uint32_t *__restrict__ offs,
                                                      uint32_t nb, uint64_t *__restrict__ out) {
+  pdl_wait();
   __shared__ uint64_t s[8][kBucketSmem];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = (int64_t)blockIdx.x * 8 + warp;
@@ -520,11 +528,11 @@ inline cudaError_t bucket_sort_u64(const uint64_t *keys, int64_t n, uint64_t key
   cudaError_t e = cudaMemsetAsync(offs, 0, 2 * cb, stream);  // counts and fill cursors
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n + 255) / 256 < 65535 * 8 ? (n + 255) / 256 : 65535 * 8);
-  k_bucket_count<<<grid, 256, 0, stream>>>(keys, n, scale, nb, offs);
+  launch_pdl(k_bucket_count, grid, 256, 0, stream, keys, n, scale, nb, offs);
   e = scan_apply<uint32_t>(CountRead64{offs}, (int64_t)nb, WriteOffs{offs}, offs + nb, stemp, stream);
   if (e != cudaSuccess) return e;
-  k_bucket_fill<<<grid, 256, 0, stream>>>(keys, n, scale, nb, offs, fill, tmp);
-  k_bucket_rank<<<(nb + 7) / 8, 256, 0, stream>>>(tmp, offs, nb, out);
+  launch_pdl(k_bucket_fill, grid, 256, 0, stream, keys, n, scale, nb, offs, fill, tmp);
+  launch_pdl(k_bucket_rank, (nb + 7) / 8, 256, 0, stream, tmp, offs, nb, out);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ struct SelDigit {
 // `rem` (no extra launch, no waiting: the last arrival does the pick).
 template <typename TV, int kPass>
 __global__ void __launch_bounds__(256) k_sel_pass(const TV *__restrict__ val, int64_t nnz, SelState *st) {
+  pdl_wait();
   constexpr int kItems = 16;
   constexpr int kShift = SelDigit<kPass>::kShift, kBins = SelDigit<kPass>::kBins, kPer = kBins / 256;
   __shared__ uint32_t h[kBins];
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(256) k_sel_pass(const TV *__restrict__ val, in
 }
 
 __global__ void k_sel_init(SelState *st, uint32_t n_prune) {
+  pdl_wait();
   for (int i = threadIdx.x; i < 2048; i += blockDim.x) st->hist0[i] = 0;
   for (int i = threadIdx.x; i < 1024; i += blockDim.x) {
     st->hist1[i] = 0;
@@ -214,6 +216,7 @@ __device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_
 __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int32_t out_f,
                        const int32_t *__restrict__ rp, const int32_t *__restrict__ col, uint64_t *__restrict__ cand,
                        uint64_t *hkeys, uint32_t *hmin, uint64_t hmask, uint32_t *overflow) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
     const uint64_t i = i0 + (uint64_t)idx;
@@ -258,6 +261,7 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
 __global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0,
                                const uint64_t *__restrict__ hkeys, const uint32_t *__restrict__ hmin, uint64_t hmask,
                                uint32_t *__restrict__ flags) {
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
     const uint64_t p = cand[idx];
@@ -310,6 +314,7 @@ __device__ int64_t merge_split_warp(const uint64_t *A, int64_t na, const uint64_
 // part[t] = A elements among the first t*kMergeTile outputs, one warp per split
 __global__ void k_merge_splits(const uint64_t *__restrict__ A, int64_t na, const uint64_t *__restrict__ B, int64_t nb,
                                int64_t n_tiles, int64_t *__restrict__ part) {
+  pdl_wait();
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t > n_tiles) return;
   int64_t d = t * kMergeTile;
@@ -324,6 +329,7 @@ __global__ void __launch_bounds__(kMergeThreads)
             int64_t nb, const int64_t *__restrict__ part, int32_t in_f, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
             int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
+  pdl_wait();
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];
@@ -531,9 +537,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   const double empty = (double)n_pos - (double)nnz;
   int64_t done = 0, acc = 0;
   auto draw_chunk = [&](int64_t m) -> cudaError_t {
-    k_draw<<<grid_for(m, 256), 256, 0, s2>>>(base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
+    launch_pdl(k_draw, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
                                              hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
-    k_accept_flags<<<grid_for(m, 256), 256, 0, s2>>>(cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
+    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
                                                      flags);
     cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
                                               &ds->total, stemp2, s2);
@@ -559,12 +565,12 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     }
   }
   // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
-  k_sel_init<<<1, 256, 0, s>>>(st, (uint32_t)n_prune);
+  launch_pdl(k_sel_init, 1, 256, 0, s, st, (uint32_t)n_prune);
   if (n_prune > 0) {
     const unsigned g = grid_for((nnz + 15) / 16, 256, 1184);
-    k_sel_pass<TV, 0><<<g, 256, 0, s>>>(val, nnz, st);
-    k_sel_pass<TV, 1><<<g, 256, 0, s>>>(val, nnz, st);
-    k_sel_pass<TV, 2><<<g, 256, 0, s>>>(val, nnz, st);
+    launch_pdl(k_sel_pass<TV, 0>, g, 256, 0, s, val, nnz, st);
+    launch_pdl(k_sel_pass<TV, 1>, g, 256, 0, s, val, nnz, st);
+    launch_pdl(k_sel_pass<TV, 2>, g, 256, 0, s, val, nnz, st);
   }
   // 2. survivors
   e = cudaGetLastError();
@@ -610,9 +616,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
   if (verdict != SNACK_OK) return verdict;
   if (nnz > 0) {
-    k_merge_splits<<<grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s>>>(surv_pos, n_surv, grown, n_prune,
+    launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
-    k_merge<TV><<<(unsigned)W.n_merge_tiles, kMergeThreads, 0, s>>>(
+    launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, 
         surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, a.out_f, val, a.row_out, a.col_out,
         reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new, a.col16_new);
   }
@@ -707,6 +713,7 @@ __device__ __forceinline__ int lower_bound_by(P at, int n, uint32_t v) {
 
 template <typename TV>
 __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A) {
+  pdl_wait();
   __shared__ uint32_t s_hist[kRowsWarps][256];
   __shared__ uint32_t s_gcol[kRowsWarps][kRowsMaxPrune];
   __shared__ uint32_t s_glb[kRowsWarps][kRowsMaxPrune];
@@ -880,9 +887,9 @@ snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) 
   if (cudaMemsetAsync(a.err, 0, sizeof(uint32_t), s) != cudaSuccess) return SNACK_ERR_CUDA;
   const unsigned grid = (unsigned)((a.out_f + kRowsWarps - 1) / kRowsWarps);
   if (a.val_t == SNACK_BF16)
-    k_restructure_rows<bf16><<<grid, kRowsWarps * 32, 0, s>>>(A);
+    launch_pdl(k_restructure_rows<bf16>, grid, kRowsWarps * 32, 0, s, A);
   else
-    k_restructure_rows<float><<<grid, kRowsWarps * 32, 0, s>>>(A);
+    launch_pdl(k_restructure_rows<float>, grid, kRowsWarps * 32, 0, s, A);
   if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   return SNACK_OK;
 }

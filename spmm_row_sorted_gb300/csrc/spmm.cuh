@@ -194,6 +194,7 @@ struct SpmmUnroll {
 template <typename TA, typename TV, int V, int G, bool kGatherVal, bool kFuseDw>
 __global__ void __launch_bounds__(kSpmmThreads, kFuseDw ? SNACK_SPMM_MIN_CTAS_FUSED : SNACK_SPMM_MIN_CTAS)
     k_spmm_tiles(SpmmParams P, BatchGeom bg) {
+  pdl_wait();
   constexpr int kSlots = 32 / G;
   constexpr int kU = SpmmUnroll<V, G>::value;
   extern __shared__ __align__(16) float smem[];
@@ -435,6 +436,7 @@ __global__ void __launch_bounds__(kSpmmThreads, kFuseDw ? SNACK_SPMM_MIN_CTAS_FU
 // order) + head, written once.
 template <typename TA>
 __global__ void k_spmm_fixup(SpmmParams P, BatchGeom bg) {
+  pdl_wait();
   const int t = blockIdx.x, bi = blockIdx.y;
   const int i0 = P.tiles[2 * t], j0 = P.tiles[2 * t + 1], i1 = P.tiles[2 * t + 2];
   if (i1 <= i0 || i0 >= P.n_rows) return;
@@ -456,6 +458,7 @@ __global__ void k_spmm_fixup(SpmmParams P, BatchGeom bg) {
 // a [batch][n] -> at [n][ldx], zero-filled for b in [batch, ldx)
 template <typename T>
 __global__ void k_transpose(const T *__restrict__ a, int batch, int n, T *__restrict__ at, int ldx) {
+  pdl_wait();
   __shared__ T tile[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int c0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
@@ -477,6 +480,7 @@ __global__ void k_transpose(const T *__restrict__ a, int batch, int n, T *__rest
 // out[c] = sum_b a[b][c], b increasing
 template <typename T>
 __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__restrict__ out) {
+  pdl_wait();
   int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= n) return;
   float s = 0.f;
@@ -490,6 +494,7 @@ __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__res
 template <typename T>
 __global__ void __launch_bounds__(256) k_rowsum_t(const T *__restrict__ at, int ldx, int batch, int n,
                                                   float *__restrict__ out) {
+  pdl_wait();
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= n) return;
   const T *p = at + (size_t)r * ldx;
@@ -518,6 +523,7 @@ __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__res
                                                const int32_t *__restrict__ col, int32_t out_f, int32_t in_f,
                                                const TA *__restrict__ xt, const TA *__restrict__ dyt, int ldx,
                                                int n_chunks, int chunk, float *__restrict__ dw) {
+  pdl_wait();
   constexpr int kSlots = 32 / G;
   constexpr int kU = DwUnroll<V, G>::value;
   const int per_warp = (chunk + 7) / 8;
@@ -601,9 +607,9 @@ cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t
     if (e != cudaSuccess) return e;
   }
   dim3 grid(p.tg.n_tiles, bg.n_btiles);
-  kern<<<grid, kSpmmThreads, smem, s>>>(p, bg);
+  launch_pdl(kern, grid, kSpmmThreads, smem, s, p, bg);
   int fx = bg.bt < 32 ? 32 : (bg.bt > 256 ? 256 : bg.bt);
-  k_spmm_fixup<TA><<<grid, fx, 0, s>>>(p, bg);
+  launch_pdl(k_spmm_fixup<TA>, grid, fx, 0, s, p, bg);
   return cudaGetLastError();
 }
 
@@ -635,7 +641,7 @@ cudaError_t launch_sddmm_v(int64_t nnz, const int32_t *row, const int32_t *col, 
   if (chunk > kDwChunk) chunk = kDwChunk;
   int64_t blocks = (nnz + chunk - 1) / chunk;
   int n_chunks = bg.ldx / bg.bt;
-  k_sddmm<TA, V, G><<<(unsigned)blocks, 256, 0, s>>>(nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks,
+  launch_pdl(k_sddmm<TA, V, G>, (unsigned)blocks, 256, 0, s, nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks,
                                                      (int)chunk, dw);
   return cudaGetLastError();
 }
@@ -661,19 +667,19 @@ cudaError_t launch_sddmm(int64_t nnz, const int32_t *row, const int32_t *col, in
 template <typename T>
 cudaError_t launch_transpose(const T *a, int batch, int n, T *at, int ldx, cudaStream_t s) {
   dim3 grid((n + 31) / 32, (ldx + 31) / 32);
-  k_transpose<T><<<grid, dim3(32, 8), 0, s>>>(a, batch, n, at, ldx);
+  launch_pdl(k_transpose<T>, grid, dim3(32, 8), 0, s, a, batch, n, at, ldx);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_colsum(const T *a, int batch, int n, float *out, cudaStream_t s) {
-  k_colsum<T><<<(n + 255) / 256, 256, 0, s>>>(a, batch, n, out);
+  launch_pdl(k_colsum<T>, (n + 255) / 256, 256, 0, s, a, batch, n, out);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s) {
-  k_rowsum_t<T><<<(n + 7) / 8, 256, 0, s>>>(at, ldx, batch, n, out);
+  launch_pdl(k_rowsum_t<T>, (n + 7) / 8, 256, 0, s, at, ldx, batch, n, out);
   return cudaGetLastError();
 }
 
