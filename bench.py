@@ -406,7 +406,7 @@ def run_ours(args):
     e2e = {"value": world * step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    launches_per_step = 3 + 5 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: 2 transposes, row sum, tiles, fixup
+    launches_per_step = 3 + 3 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: both transposes (+ db), tiles, fixup
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",

@@ -212,16 +212,20 @@ snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, cons
     if (db) SNACK_CUDA(run_colsum<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, db, s));
     return SNACK_OK;
   }
+  bool db_done = false;
   if (batch > 1) {
     T *a = reinterpret_cast<T *>(b + W.xt);
     T *c = reinterpret_cast<T *>(b + W.dyt);
-    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, a, bg.ldx, s));
-    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, c, bg.ldx, s));
+    TransposePair<T> tp{reinterpret_cast<const T *>(dy), reinterpret_cast<const T *>(x), c, a, h->out_f, h->in_f,
+                        bg.ldx <= 32 ? db : nullptr};
+    SNACK_CUDA(run_transpose2<T>(tp, batch, bg.ldx, s));
+    db_done = tp.db0 != nullptr;
     xt = a;
     dyt = c;
   }
-  // db from the feature-major dY (contiguous per output feature)
-  if (db) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
+  // db from the feature-major dY (contiguous per output feature), unless the
+  // transpose already summed a single batch tile
+  if (db && !db_done) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
   SNACK_CUDA(run_sddmm<T>(h->nnz, row, col, h->out_f, h->in_f, xt, dyt, bg, dw, h->num_sms, s));
   return SNACK_OK;
 }
@@ -243,15 +247,18 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   const T *dyt = reinterpret_cast<const T *>(dy);
   const T *xt = reinterpret_cast<const T *>(x);
+  bool db_done = false;
   if (batch > 1) {
     T *a = reinterpret_cast<T *>(b + W.dyt);
     T *c = reinterpret_cast<T *>(b + W.xt);
-    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, a, bg.ldx, s));
-    SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, c, bg.ldx, s));
+    TransposePair<T> tp{reinterpret_cast<const T *>(dy), reinterpret_cast<const T *>(x), a, c, h->out_f, h->in_f,
+                        bg.ldx <= 32 ? db : nullptr};
+    SNACK_CUDA(run_transpose2<T>(tp, batch, bg.ldx, s));
+    db_done = tp.db0 != nullptr;
     dyt = a;
     xt = c;
   }
-  if (db) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
+  if (db && !db_done) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
   SpmmParams p;
   p.n_rows = h->in_f;
   p.n_src = h->out_f;

@@ -477,6 +477,49 @@ __global__ void k_transpose(const T *__restrict__ a, int batch, int n, T *__rest
   }
 }
 
+// Two transposes in one launch (blockIdx.z picks the matrix): a0 [batch][n0]
+// -> at0 [n0][ldx] and a1 [batch][n1] -> at1 [n1][ldx].  When the whole
+// batch fits one 32-row tile, the blocks of the first matrix also write its
+// column sums db0[c] = sum_b a0[b][c] (b increasing) from the staged tile.
+template <typename T>
+struct TransposePair {
+  const T *a0, *a1;
+  T *at0, *at1;
+  int n0, n1;
+  float *db0;  // or null
+};
+
+template <typename T>
+__global__ void k_transpose2(TransposePair<T> tp, int batch, int ldx) {
+  pdl_wait();
+  __shared__ T tile[32][33];
+  const bool second = blockIdx.z == 1;
+  const T *a = second ? tp.a1 : tp.a0;
+  T *at = second ? tp.at1 : tp.at0;
+  const int n = second ? tp.n1 : tp.n0;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int c0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
+  if (c0 >= n) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int b = b0 + ty + 8 * j, c = c0 + tx;
+    T v = from_f32<T>(0.f);
+    if (b < batch && c < n) v = a[(size_t)b * n + c];
+    tile[ty + 8 * j][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int c = c0 + ty + 8 * j, b = b0 + tx;
+    if (c < n && b < ldx) at[(size_t)c * ldx + b] = tile[tx][ty + 8 * j];
+  }
+  if (!second && tp.db0 && gridDim.y == 1 && ty == 0 && c0 + tx < n) {
+    float s = 0.f;
+    for (int b = 0; b < batch; ++b) s += to_f32(tile[b][tx]);
+    tp.db0[c0 + tx] = s;
+  }
+}
+
 // out[c] = sum_b a[b][c], b increasing
 template <typename T>
 __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__restrict__ out) {
@@ -678,6 +721,14 @@ cudaError_t launch_colsum(const T *a, int batch, int n, float *out, cudaStream_t
 }
 
 template <typename T>
+cudaError_t launch_transpose2(const TransposePair<T> &tp, int batch, int ldx, cudaStream_t s) {
+  const int n = tp.n0 > tp.n1 ? tp.n0 : tp.n1;
+  dim3 grid((n + 31) / 32, (ldx + 31) / 32, 2);
+  launch_pdl(k_transpose2<T>, grid, dim3(32, 8), 0, s, tp, batch, ldx);
+  return cudaGetLastError();
+}
+
+template <typename T>
 cudaError_t launch_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s) {
   launch_pdl(k_rowsum_t<T>, (n + 7) / 8, 256, 0, s, at, ldx, batch, n, out);
   return cudaGetLastError();
@@ -697,5 +748,7 @@ template <typename T>
 cudaError_t run_colsum(const T *a, int batch, int n, float *out, cudaStream_t s);
 template <typename T>
 cudaError_t run_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s);
+template <typename T>
+cudaError_t run_transpose2(const TransposePair<T> &tp, int batch, int ldx, cudaStream_t s);
 
 }  // namespace snack

@@ -32,4 +32,9 @@ cudaError_t run_rowsum_t<bf16>(const bf16 *at, int ldx, int batch, int n, float 
   return launch_rowsum_t<bf16>(at, ldx, batch, n, out, s);
 }
 
+template <>
+cudaError_t run_transpose2<bf16>(const TransposePair<bf16> &tp, int batch, int ldx, cudaStream_t s) {
+  return launch_transpose2<bf16>(tp, batch, ldx, s);
+}
+
 }  // namespace snack

@@ -32,4 +32,9 @@ cudaError_t run_rowsum_t<float>(const float *at, int ldx, int batch, int n, floa
   return launch_rowsum_t<float>(at, ldx, batch, n, out, s);
 }
 
+template <>
+cudaError_t run_transpose2<float>(const TransposePair<float> &tp, int batch, int ldx, cudaStream_t s) {
+  return launch_transpose2<float>(tp, batch, ldx, s);
+}
+
 }  // namespace snack
