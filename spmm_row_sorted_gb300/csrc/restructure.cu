@@ -269,6 +269,18 @@ __global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uin
   }
 }
 
+// grown[q] = n_pos + q for the slots the first draw chunk left empty, so a
+// sort queued before the host has seen the chunk's count still sorts n_prune
+// distinct keys (those slots are sorted again once more chunks fill them)
+__global__ void k_fill_tail(uint64_t *__restrict__ grown, const uint32_t *__restrict__ total, int64_t n_prune,
+                            uint64_t n_pos) {
+  pdl_wait();
+  const int64_t t0 = *total;
+  for (int64_t q = t0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n_prune;
+       q += (int64_t)gridDim.x * blockDim.x)
+    grown[q] = n_pos + (uint64_t)q;
+}
+
 struct FlagRead {
   const uint32_t *f;
   __device__ uint32_t operator()(int64_t i) const { return f[i]; }
@@ -555,6 +567,19 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   };
   int64_t m = 0;
   cudaError_t e2 = cudaSuccess;
+  // When at least twice n_prune positions are empty the first chunk is all but
+  // certain to accept enough, so the sort of the regrown positions is queued
+  // right behind it, before the host has read the count (and redone if more
+  // chunks turn out to be needed).
+  const bool speculative = n_prune > 1 && (double)n_pos - (double)nnz >= 2.0 * (double)n_prune;
+  auto sort_grown = [&](bool first_chunk_only) -> cudaError_t {
+    if (!first_chunk_only)  // every slot filled by accepted draws
+      return bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s2);
+    launch_pdl(k_fill_tail, grid_for(n_prune, 256, 1184), 256, 0, s2, grown_a, &ds->total, n_prune, n_pos);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return bucket_sort_u64(grown_a, n_prune, n_pos + (uint64_t)n_prune - 1, grown_b, b + W.radix, s2);
+  };
   if (n_prune > 0) {
     e2 = cudaMemsetAsync(ds, 0, sizeof(DrawState), s2);
     if (e2 == cudaSuccess) e2 = cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s2);
@@ -563,6 +588,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       m = chunk_size();
       e2 = draw_chunk(m);
     }
+    if (e2 == cudaSuccess && speculative) e2 = sort_grown(true);
   }
   // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
   launch_pdl(k_sel_init, 1, 256, 0, s, st, (uint32_t)n_prune);
@@ -583,6 +609,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   }
   // 3. regrow: further chunks only when the first fell short (rare)
   snack_status verdict = SNACK_OK;
+  bool resort = !speculative;
   while (n_prune > 0) {
     if (cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
       verdict = SNACK_ERR_CUDA;
@@ -600,6 +627,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       break;
     }
     m = chunk_size();
+    resort = true;
     if (draw_chunk(m) != cudaSuccess) {
       verdict = SNACK_ERR_CUDA;
       break;
@@ -607,12 +635,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   }
   // 4. sort regrown positions (bucket sort: they are uniform over the empty
   //    positions), then join and merge with the survivors
-  const uint64_t *grown = grown_a;
-  if (verdict == SNACK_OK && n_prune > 1) {
-    if (bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s2) != cudaSuccess)
-      verdict = SNACK_ERR_CUDA;
-    grown = grown_b;
-  }
+  const uint64_t *grown = n_prune > 1 ? grown_b : grown_a;
+  if (verdict == SNACK_OK && n_prune > 1 && resort && sort_grown(false) != cudaSuccess) verdict = SNACK_ERR_CUDA;
   if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
   if (verdict != SNACK_OK) return verdict;
   if (nnz > 0) {
