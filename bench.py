@@ -835,7 +835,7 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
     draw_chunk = 1 + 1 + 2  # draws, accept flags, scan (second stream)
-    sort_grown = 1 + 2 + 1 + 1  # bucket count, scan, fill, rank (second stream)
+    sort_grown = 1 + 1 + 2 + 1 + 1  # sentinel tail, bucket count, scan, fill, rank (second stream)
     select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
     keep_scan = 2
     merge = 2  # split points, merge (also writes the row offsets)
