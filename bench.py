@@ -161,6 +161,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest replica's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every replica moves its own bytes in the slowest replica's time."""
+    return world * bytes_per_step_per_rank / (ms_per_step / 1e3) / 1e9
+
+
 def make_workload(seed: int):
     from spmm_row_sorted_gb300 import workloads as wl
 
@@ -351,16 +367,12 @@ def run_ours(args):
         t_end.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ops = list(STEP_OPS)
     op_ms = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
              for j, op in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes * args.steps / (elapsed_ms / 1e3) / 1e9
+    value = job_throughput(step_bytes, world, elapsed_ms / args.steps)
     peak, peak_kind = measured_peak_gbs()
     op_report = {}
     for op in ops:
@@ -398,12 +410,8 @@ def run_ours(args):
             hdb.copy_(cp["db"], non_blocking=True)
     e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * step_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e = {"value": job_throughput(step_bytes, world, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     launches_per_step = 3 + 3 + restructure_launches()  # fwd: transpose, tiles, fixup; bwd: both transposes (+ db), tiles, fixup
