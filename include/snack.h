@@ -77,7 +77,7 @@ typedef enum snack_status {
   SNACK_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad size, aliasing, batch > max_batch */
   SNACK_ERR_UNSORTED = 2,     /* validation: (row, col) not strictly increasing */
   SNACK_ERR_OUT_OF_RANGE = 3, /* validation: an index outside [0,out_f) x [0,in_f) */
-  SNACK_ERR_WORKSPACE = 4,    /* plan or workspace smaller than the size query returned */
+  SNACK_ERR_WORKSPACE = 4,    /* plan or workspace smaller than the call needs (the queried sizes always do) */
   SNACK_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
   SNACK_ERR_TIMEOUT = 6,      /* reserved for bounded device-side waits (none today) */
   SNACK_ERR_UNSUPPORTED = 7,  /* val and act dtypes differ, or max(out_f, in_f) x padded batch >= 2^32 */
@@ -91,6 +91,12 @@ typedef enum snack_dtype { SNACK_F32 = 0, SNACK_BF16 = 1 } snack_dtype;
  *   plan_bytes       persistent plan, alive as long as the handle;
  *   workspace_bytes  scratch for snack_create and for fwd / dx / dw with
  *                    batch <= max_batch (contents need not survive calls).
+ *                    Calls with batch <= 8 whose gathered operand (x for the
+ *                    forward, dy for the gradients) fits 96 KB at the batch
+ *                    rounded up to 1, 2, 4 or 8 run one small-batch kernel
+ *                    that uses none of it; other calls check ws_bytes against
+ *                    what they use and return SNACK_ERR_WORKSPACE before any
+ *                    launch when it is short.
  * Limits: 1 <= out_f, in_f < 2^31; 0 <= nnz <= out_f*in_f and nnz < 2^31 - 1;
  * 1 <= max_batch <= 65535.  val_t must equal act_t (fp32/fp32 or bf16/bf16).
  * Either output pointer may be NULL.

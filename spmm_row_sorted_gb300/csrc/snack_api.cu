@@ -120,10 +120,47 @@ snack_status check_shape(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_b
     if ((x) != cudaSuccess) return SNACK_ERR_CUDA; \
   } while (0)
 
+// Column-view parameters of the small-batch path: rows are the input
+// features, the gathered operand is dY [batch][out_f].
+SpmmParams small_colview_params(snack_handle h, const void *val, const void *dy, int32_t batch, void *dx) {
+  SpmmParams p = {};
+  p.n_rows = h->in_f;
+  p.n_src = h->out_f;
+  p.ptr = h->p.cp;
+  p.nnz = h->nnz;
+  p.idx = h->p.row_t;
+  p.idx16 = h->p.rowt16;
+  p.val = val;
+  p.val_src = h->p.src_t;
+  p.xt = dy;
+  p.y = dx;
+  p.batch = batch;
+  p.act = kActNone;
+  return p;
+}
+
 template <typename T>
 snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const void *x, int32_t batch,
                      const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s, int act = kActNone,
                      void *pre_out = nullptr) {
+  if (small_path_ok(batch, h->in_f, sizeof(T))) {  // one launch, X read batch-major
+    SpmmParams p = {};
+    p.n_rows = h->out_f;
+    p.n_src = h->in_f;
+    p.ptr = h->p.rp;
+    p.nnz = h->nnz;
+    p.idx = col;
+    p.idx16 = h->p.col16;
+    p.val = val;
+    p.xt = x;
+    p.bias = bias;
+    p.y = y;
+    p.batch = batch;
+    p.act = act;
+    p.pre_out = pre_out;
+    SNACK_CUDA(run_spmm_small<T>(p, false, false, h->num_sms, s));
+    return SNACK_OK;
+  }
   BatchGeom bg = batch_geom(batch, h->act_t);
   SpmmWs W = spmm_ws(h->in_f, h->lay.gf, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
@@ -134,7 +171,7 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
     SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(x), batch, h->in_f, xt_w, bg.ldx, s));
     xt = xt_w;
   }
-  SpmmParams p;
+  SpmmParams p = {};
   p.n_rows = h->out_f;
   p.n_src = h->in_f;
   p.ptr = h->p.rp;
@@ -163,6 +200,13 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
 template <typename T>
 snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t batch, void *dx, void *ws,
                     size_t ws_bytes, cudaStream_t s, int act = kActNone, const void *pre_in = nullptr) {
+  if (small_path_ok(batch, h->out_f, sizeof(T))) {  // one launch over the column view, dY read batch-major
+    SpmmParams p = small_colview_params(h, val, dy, batch, dx);
+    p.act = act;
+    p.pre_in = pre_in;
+    SNACK_CUDA(run_spmm_small<T>(p, true, false, h->num_sms, s));
+    return SNACK_OK;
+  }
   BatchGeom bg = batch_geom(batch, h->act_t);
   SpmmWs W = spmm_ws(h->out_f, h->lay.gt, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
@@ -173,7 +217,7 @@ snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t bat
     SNACK_CUDA(run_transpose<T>(reinterpret_cast<const T *>(dy), batch, h->out_f, w, bg.ldx, s));
     dyt = w;
   }
-  SpmmParams p;
+  SpmmParams p = {};
   p.n_rows = h->in_f;
   p.n_src = h->out_f;
   p.ptr = h->p.cp;
@@ -202,6 +246,19 @@ snack_status run_dx(snack_handle h, const void *val, const void *dy, int32_t bat
 template <typename T>
 snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, const void *x, const void *dy,
                     int32_t batch, float *dw, float *db, void *ws, size_t ws_bytes, cudaStream_t s) {
+  if (small_dw_flat_ok(batch, h->nnz)) {  // one flat pass over the stored weights
+    SNACK_CUDA(run_sddmm_small<T>(h->nnz, row, col, h->out_f, h->in_f, reinterpret_cast<const T *>(x),
+                                  reinterpret_cast<const T *>(dy), batch, dw, db, h->num_sms, s));
+    return SNACK_OK;
+  }
+  if (small_path_ok(batch, h->out_f, sizeof(T))) {  // the column-view pass with dW and db only
+    SpmmParams p = small_colview_params(h, nullptr, dy, batch, nullptr);
+    p.xt_dw = x;
+    p.dw = dw;
+    p.db = db;
+    SNACK_CUDA(run_spmm_small<T>(p, true, true, h->num_sms, s));
+    return SNACK_OK;
+  }
   BatchGeom bg = batch_geom(batch, h->act_t);
   DwWs W = dw_ws(h->out_f, h->in_f, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
@@ -236,6 +293,14 @@ template <typename T>
 snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *x,
                      const void *dy, int32_t batch, void *dx, float *dw, float *db, void *ws, size_t ws_bytes,
                      cudaStream_t s) {
+  if (small_path_ok(batch, h->out_f, sizeof(T))) {  // dX, dW and db in one launch
+    SpmmParams p = small_colview_params(h, val, dy, batch, dx);
+    p.xt_dw = x;
+    p.dw = dw;
+    p.db = db;
+    SNACK_CUDA(run_spmm_small<T>(p, true, true, h->num_sms, s));
+    return SNACK_OK;
+  }
   BatchGeom bg = batch_geom(batch, h->act_t);
   if (bg.n_btiles > 1 || h->nnz == 0) {
     snack_status st = run_dx<T>(h, val, dy, batch, dx, ws, ws_bytes, s);
@@ -259,7 +324,7 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
     xt = c;
   }
   if (db && !db_done) SNACK_CUDA(run_rowsum_t<T>(dyt, batch > 1 ? bg.ldx : 1, batch, h->out_f, db, s));
-  SpmmParams p;
+  SpmmParams p = {};
   p.n_rows = h->in_f;
   p.n_src = h->out_f;
   p.ptr = h->p.cp;

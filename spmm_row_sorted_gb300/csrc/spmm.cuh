@@ -153,6 +153,7 @@ struct SpmmParams {
   int32_t act;            // output epilogue: kActNone, kActGelu, kActGeluGrad
   const void *pre_in;     // kActGeluGrad: pre-activation [batch][n_rows] (act dtype)
   void *pre_out;          // kActGelu: pre-activation written here when non-null
+  float *db;              // small-batch fused backward: bias gradient [n_src], or null
 };
 
 // Output epilogues of the SpMM kernels.
@@ -750,5 +751,24 @@ template <typename T>
 cudaError_t run_rowsum_t(const T *at, int ldx, int batch, int n, float *out, cudaStream_t s);
 template <typename T>
 cudaError_t run_transpose2(const TransposePair<T> &tp, int batch, int ldx, cudaStream_t s);
+
+// Small-batch path (spmm_small.cu): batch <= kSmallMaxBatch, the gathered
+// operand read batch-major (no transposed copy), one launch per call.  In
+// column-view mode with fuse_dw it also writes dw at storage index and, when
+// p.db is set, the bias gradient; p.y == null skips the input gradient.
+constexpr int kSmallMaxBatch = 8;
+constexpr size_t kSmallMaxStage = 96 * 1024;  // bytes of the operand copy a CTA stages
+int small_batch_width(int batch);
+bool small_path_ok(int batch, int n_src, size_t elem);
+template <typename T>
+cudaError_t run_spmm_small(const SpmmParams &p, bool gather_val, bool fuse_dw, int num_sms, cudaStream_t s);
+// Weight gradient alone on a small layer at small batch: a flat pass over
+// the stored weights (no row structure, no transposed copies) when nnz times
+// the padded batch width is at most kSmallDwFlatLoads.
+constexpr int64_t kSmallDwFlatLoads = int64_t(1) << 22;
+bool small_dw_flat_ok(int batch, int64_t nnz);
+template <typename T>
+cudaError_t run_sddmm_small(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
+                            const T *x, const T *dy, int batch, float *dw, float *db, int num_sms, cudaStream_t s);
 
 }  // namespace snack

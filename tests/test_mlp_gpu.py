@@ -48,7 +48,7 @@ def check_gelu_close(got, ref, t, what):
     assert np.all(err <= bound), f"{what}: worst err/bound {float(np.max(err / np.maximum(bound, 1e-300))):.3f}"
 
 
-@pytest.mark.parametrize("batch", [1024, 37])
+@pytest.mark.parametrize("batch", [1024, 37, 8, 3])
 def test_sparse_mlp_training_step(batch):
     l1 = wl.config_layer("c3", layer_index=0)  # 3072 x 768
     l2 = wl.config_layer("c3", layer_index=1)  # 768 x 3072
@@ -108,10 +108,11 @@ def test_sparse_mlp_training_step(batch):
     L2.close()
 
 
-def test_gelu_epilogue_bf16_and_no_pre():
+@pytest.mark.parametrize("batch", [16, 4])
+def test_gelu_epilogue_bf16_and_no_pre(batch):
     lay = wl.make_layer(300, 200, nnz=6000, val_std=0.2, val_dtype="bf16", seed=8, bias="normal")
-    acts = wl.make_acts(16, 200, 300, "bf16", seed=8)
-    L = make(lay, 16)
+    acts = wl.make_acts(batch, 200, 300, "bf16", seed=8)
+    L = make(lay, batch)
     x = act_tensor(acts.x, "bf16")
     y, pre = L.forward_gelu(x, keep_pre=False)
     assert pre is None

@@ -300,10 +300,17 @@ def test_call_errors():
     with pytest.raises(snack.SnackError) as e:
         L.forward(x)  # batch > max_batch
     assert e.value.status == 1
-    y = torch.empty((2, 30), device="cuda")
+    # a short workspace: batch 16 takes the tile kernels, which need scratch
+    L16 = snack.SparseLinear(30, 20, row, col, val, bias, max_batch=16)
+    x16 = torch.zeros((16, 20), device="cuda")
+    y16 = torch.empty((16, 30), device="cuda")
     with pytest.raises(snack.SnackError) as e:
-        snack.snack_spmm_fwd(L.handle, row, col, val, x[:2], 2, bias, y, L.ws[:256])
+        snack.snack_spmm_fwd(L16.handle, row, col, val, x16, 16, bias, y16, L16.ws[:256])
     assert e.value.status == 4
+    L16.close()
+    # batch 2 runs the small-batch kernel, which uses no workspace
+    y = torch.empty((2, 30), device="cuda")
+    snack.snack_spmm_fwd(L.handle, row, col, val, x[:2], 2, bias, y, L.ws[:256])
     buf = torch.zeros(4 * 30, device="cuda")
     with pytest.raises(snack.SnackError) as e:  # y overlaps x
         snack.snack_spmm_fwd(L.handle, row, col, val, buf[:40], 2, bias, buf[10:70], L.ws)
@@ -357,14 +364,15 @@ def test_backward_workloads_c1_c4():
         check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
 
 
-def test_backward_equals_separate_calls_bitwise():
+@pytest.mark.parametrize("batch", [32, 5])
+def test_backward_equals_separate_calls_bitwise(batch):
     # dX and db come from the same kernels and tiles as the separate calls, so
     # they are bit-identical; dW may differ in summation order (checked above
-    # against the oracle)
+    # against the oracle).  Batch 5 runs the small-batch path.
     lay = wl.make_layer(300, 400, nnz=20000, val_dtype="f32", seed=4, bias="normal")
-    acts = wl.make_acts(32, 400, 300, "f32", seed=4)
+    acts = wl.make_acts(batch, 400, 300, "f32", seed=4)
     row, col, val, bias = layer_tensors(lay)
-    L = snack.SparseLinear(300, 400, row, col, val, bias, max_batch=32)
+    L = snack.SparseLinear(300, 400, row, col, val, bias, max_batch=batch)
     x, dy = act_tensor(acts.x, "f32"), act_tensor(acts.dy, "f32")
     dx_f, dw_f, db_f = L.backward(x, dy)
     dx_s = L.grad_input(dy)
@@ -372,6 +380,49 @@ def test_backward_equals_separate_calls_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(dx_f, dx_s) and torch.equal(db_f, db_s)
     L.close()
+
+
+# ---------------------------------------------------------------- small-batch path (batch <= 8)
+
+# The small-batch kernels stage the gathered operand (X, or dY for the column
+# view) whole in shared memory when it fits in 96 KB at the padded batch width
+# (1, 2, 4 or 8); wider operands take the tile kernels.  Cases on both sides of
+# that limit, for every op.
+@pytest.mark.parametrize("dtype,batch,feat", [("f32", 8, 3072), ("f32", 8, 3073), ("f32", 4, 6144), ("f32", 3, 6145),
+                                              ("bf16", 8, 6144), ("bf16", 6, 6145), ("bf16", 2, 24576),
+                                              ("f32", 1, 40000)])
+def test_small_batch_stage_limit(dtype, batch, feat):
+    other = 97
+    for out_f, in_f in ((other, feat), (feat, other)):
+        lay = wl.make_layer(out_f, in_f, nnz=min(60000, out_f * in_f // 3), val_std=0.3, val_dtype=dtype,
+                            seed=feat + batch, bias="normal")
+        acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+        check_layer_ops(lay, acts)
+        check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
+
+
+@pytest.mark.parametrize("dtype,batch", [("f32", 8), ("bf16", 6)])
+def test_small_batch_weight_gradient_paths(dtype, batch):
+    # dW alone: a flat pass while nnz * padded batch <= 2^22, the column-view
+    # pass (dW and db only) above that
+    for nnz in (30000, 700000):
+        lay = wl.make_layer(1500, 3000, nnz=nnz, val_std=0.3, val_dtype=dtype, seed=nnz, bias="normal")
+        acts = wl.make_acts(batch, 3000, 1500, dtype, seed=batch)
+        check_layer_ops(lay, acts, ops=("dw",))
+
+
+def test_small_batch_skewed_rows_and_empty_layer():
+    # Zipf rows: whole rows per CTA, so the longest row sets one CTA's length
+    lay = wl.make_layer(1500, 2000, nnz=150000, zipf_s=1.3, val_std=0.3, val_dtype="f32", seed=12, bias="normal")
+    for batch in (1, 2, 7):
+        acts = wl.make_acts(batch, 2000, 1500, "f32", seed=batch)
+        check_layer_ops(lay, acts)
+        check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
+    empty = wl.make_layer(40, 70, nnz=0, val_dtype="f32", seed=1, bias="normal")
+    for batch in (1, 8):
+        acts = wl.make_acts(batch, 70, 40, "f32", seed=batch)
+        check_layer_ops(empty, acts)
+        check_layer_ops(empty, acts, ops=("dx", "dw"), got=run_backward(empty, acts))
 
 
 # ---------------------------------------------------------------- dense path (bf16, >= 25 % stored, batch >= 32)
