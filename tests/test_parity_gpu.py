@@ -382,6 +382,34 @@ def test_backward_equals_separate_calls_bitwise(batch):
     L.close()
 
 
+# ---------------------------------------------------------------- rows split between CTAs
+
+def test_split_rows_repeat_calls_bitwise():
+    # Long Zipf rows span many tiles, whose partials are combined in tile
+    # order: repeated calls with 1, 2 and 3 batch tiles on one handle give
+    # bit-identical results, and match the oracle.
+    lay = wl.make_layer(700, 9000, nnz=400000, zipf_s=1.4, val_std=0.3, val_dtype="f32", seed=21, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(700, 9000, row, col, val, bias, max_batch=300)
+    first = {}
+    for rep in range(3):
+        for batch in (300, 130, 40):
+            acts = wl.make_acts(batch, 9000, 700, "f32", seed=batch)
+            x, dy = act_tensor(acts.x, "f32"), act_tensor(acts.dy, "f32")
+            y = L.forward(x)
+            dx = L.grad_input(dy)
+            dx_f, dw_f, db_f = L.backward(x, dy)
+            torch.cuda.synchronize()
+            got = [t.clone() for t in (y, dx, dx_f, dw_f, db_f)]
+            if rep == 0:
+                first[batch] = got
+                check_layer_ops(lay, acts, ops=("fwd", "dx"), got={"y": y, "dx": dx})
+            else:
+                for a, b in zip(got, first[batch]):
+                    assert torch.equal(a, b)
+    L.close()
+
+
 # ---------------------------------------------------------------- small-batch path (batch <= 8)
 
 # The small-batch kernels stage the gathered operand (X, or dY for the column
