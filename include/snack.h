@@ -25,7 +25,7 @@
  * outputs, the plan and the workspaces -- is allocated and freed by the
  * caller.  The library never allocates device memory.  A handle owns host
  * metadata, and after its first restructure also a second CUDA stream, three
- * events and 8 bytes of pinned host memory; snack_destroy frees them.
+ * events and 16 bytes of mapped pinned host memory; snack_destroy frees them.
  *
  * Streams.  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), except snack_create with validate != 0, which

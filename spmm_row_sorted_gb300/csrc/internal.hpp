@@ -62,8 +62,9 @@ struct RestructureArgs {
   int32_t *row_out, *col_out;
   void *val_out;
   int32_t *src_out;  // may be null
-  uint32_t *host_counts;  // pinned host memory, 2 words: a draw chunk's accepted count and overflow flag
-  cudaEvent_t counts_ready;  // recorded after the copy into host_counts
+  uint32_t *host_counts;  // pinned, mapped host memory, 4 words: a draw chunk's accepted count, table and bucket overflow
+  uint32_t *counts_dev;   // the same words' device address (written by a kernel, no copy)
+  cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
   cudaStream_t aux;          // second stream of the handle (regrow branch)
   cudaEvent_t ev_fork, ev_join;
 };
@@ -117,7 +118,8 @@ struct snack_layer {
   snack::PlanPtrs p;
   size_t plan_bytes;
   int num_sms;
-  uint32_t *host_counts = nullptr;  // restructure read-back (pinned), made on first use
+  uint32_t *host_counts = nullptr;  // restructure read-back (pinned, mapped), made on first use
+  uint32_t *host_counts_dev = nullptr;  // its device address
   cudaEvent_t counts_ready = nullptr;
   cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;

@@ -14,8 +14,12 @@
 //     the first n_prune accepted.  Draws run in chunks until enough are
 //     accepted; the first chunk is queued before steps 1 and 2 and the host
 //     reads its count back while the device runs them;
-//  4. regrown positions are bucket sorted and merged with the survivors by
-//     position (merge path), writing row/col/val/src.
+//  4. regrown positions are sorted: the accept scan drops each accepted
+//     position into an equal-width bucket of the position range, one block
+//     turns the bucket counts into offsets and one warp per bucket places its
+//     positions by rank (a general sort takes over after extra draw chunks or
+//     a full bucket); then they are merged with the survivors by position
+//     (merge path), writing row/col/val/src.
 // Every step is integer work, so the output is bit-exact with the sequential
 // definition.
 #include <math.h>
@@ -269,18 +273,6 @@ __global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uin
   }
 }
 
-// grown[q] = n_pos + q for the slots the first draw chunk left empty, so a
-// sort queued before the host has seen the chunk's count still sorts n_prune
-// distinct keys (those slots are sorted again once more chunks fill them)
-__global__ void k_fill_tail(uint64_t *__restrict__ grown, const uint32_t *__restrict__ total, int64_t n_prune,
-                            uint64_t n_pos) {
-  pdl_wait();
-  const int64_t t0 = *total;
-  for (int64_t q = t0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n_prune;
-       q += (int64_t)gridDim.x * blockDim.x)
-    grown[q] = n_pos + (uint64_t)q;
-}
-
 struct FlagRead {
   const uint32_t *f;
   __device__ uint32_t operator()(int64_t i) const { return f[i]; }
@@ -291,16 +283,135 @@ struct CandPayload {
   __device__ uint64_t operator()(int64_t idx) const { return cand[idx]; }
 };
 
+// Accepted draws in draw order: slot q of the regrown list, and -- for the
+// sort -- a slot in the position's bucket (equal-width buckets of the
+// position range, kBktCap slots each, filled in any order; a full bucket
+// raises `bovf` and the caller sorts the list the general way instead).
+constexpr int kBktTarget = 64;  // positions expected per bucket
+constexpr int kBktCap = 256;    // slots per bucket
+
 struct AcceptOut {
   uint64_t *grown;
   int64_t before, n_prune;
+  uint32_t *bcnt;     // [nb] positions placed per bucket
+  uint64_t *bslots;   // [nb][kBktCap]
+  double scale;       // bucket = floor(p * scale)
+  uint32_t nb;
+  uint32_t *bovf;
   __device__ void operator()(int64_t idx, uint32_t ex, uint32_t v, uint64_t p) const {
     if (v) {
       int64_t q = before + (int64_t)ex;
-      if (q < n_prune) grown[q] = p;
+      if (q < n_prune) {
+        grown[q] = p;
+        const uint32_t bk = bucket_of(p, scale, nb);
+        const uint32_t slot = atomicAdd(&bcnt[bk], 1u);
+        if (slot < (uint32_t)kBktCap)
+          bslots[(size_t)bk * kBktCap + slot] = p;
+        else
+          atomicOr(bovf, 1u);
+      }
     }
   }
 };
+
+// Counters of the regrow branch (it runs beside the select on a second stream).
+struct DrawState {
+  uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
+  uint32_t bucket_overflow;  // a sort bucket of the regrown positions ran out of slots
+};
+
+// Bucket offsets: exclusive prefix of min(count, kBktCap) over the nb
+// buckets, one block of light threads (it runs beside the other stream's
+// kernels): each thread sums a contiguous run of counts, 16 loads in flight
+// per round, the block scans the sums, and the thread writes its run's
+// offsets; offs[nb] = the number of positions placed.  Thread 0 first copies
+// the draw chunk's counters to the host's mapped words (the accept scan that
+// wrote them precedes this kernel), so the host reads them with no copy on
+// the stream.
+constexpr int kBktScanThreads = 1024;
+__global__ void __launch_bounds__(kBktScanThreads) k_bkt_scan(const uint32_t *__restrict__ bcnt, uint32_t nb,
+                                                              uint32_t *__restrict__ offs, const DrawState *ds,
+                                                              volatile uint32_t *host_words) {
+  pdl_wait();
+  __shared__ uint32_t s_warp[kBktScanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    host_words[0] = ds->total;
+    host_words[1] = ds->overflow;
+    host_words[2] = ds->bucket_overflow;
+  }
+  const uint32_t per = (nb + kBktScanThreads - 1) / kBktScanThreads;
+  const uint32_t b0 = min((uint32_t)tid * per, nb), b1 = min(b0 + per, nb);
+  uint32_t sum = 0;
+  for (uint32_t i0 = b0; i0 < b1; i0 += 16) {
+    uint32_t c[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i] = i0 + i < b1 ? min(__ldg(&bcnt[i0 + i]), (uint32_t)kBktCap) : 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum += c[i];
+  }
+  const uint32_t inc = warp_inclusive_scan(sum);
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) s_warp[lane] = warp_inclusive_scan(s_warp[lane]);
+  __syncthreads();
+  uint32_t run = inc - sum + (warp > 0 ? s_warp[warp - 1] : 0u);
+  for (uint32_t i0 = b0; i0 < b1; i0 += 16) {
+    uint32_t c[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) c[i] = i0 + i < b1 ? min(__ldg(&bcnt[i0 + i]), (uint32_t)kBktCap) : 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i0 + i < b1) offs[i0 + i] = run;
+      run += c[i];
+    }
+  }
+  if (tid == kBktScanThreads - 1) offs[nb] = run;
+}
+
+// Start of a restructure's regrow branch: counters and bucket counts to zero,
+// the position table to empty (one launch instead of four fills).
+__global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t *__restrict__ hmin, int64_t cap,
+                          uint32_t *__restrict__ bcnt, int64_t nb) {
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i0 == 0) {
+    ds->total = 0u;
+    ds->overflow = 0u;
+    ds->bucket_overflow = 0u;
+  }
+  for (int64_t i = i0; i < cap; i += stride) {
+    hkeys[i] = kEmpty;
+    hmin[i] = 0xFFFFFFFFu;
+  }
+  for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
+}
+
+// One warp per bucket: each position's rank among its bucket's (distinct)
+// positions gives its place in the sorted list.  Slots past the placed
+// positions get n_pos + q, larger than every position, in order.
+__global__ void __launch_bounds__(256) k_bkt_rank(const uint64_t *__restrict__ bslots, const uint32_t *__restrict__ bcnt,
+                                                  const uint32_t *__restrict__ offs, uint32_t nb, int64_t n,
+                                                  uint64_t n_pos, uint64_t *__restrict__ out) {
+  pdl_wait();
+  __shared__ uint64_t sk[8][kBktCap];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t tot = offs[nb];
+  for (int64_t q = tot + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x)
+    out[q] = n_pos + (uint64_t)q;
+  const int64_t b = (int64_t)blockIdx.x * 8 + warp;
+  if (b >= nb) return;
+  const uint32_t L = min(bcnt[b], (uint32_t)kBktCap), o = offs[b];
+  for (uint32_t i = lane; i < L; i += 32) sk[warp][i] = bslots[(size_t)b * kBktCap + i];
+  __syncwarp();
+  for (uint32_t i = lane; i < L; i += 32) {
+    const uint64_t k = sk[warp][i];
+    uint32_t r = 0;
+    for (uint32_t j = 0; j < L; ++j) r += sk[warp][j] < k ? 1u : 0u;
+    out[o + r] = k;
+  }
+}
 
 // Number of A elements among the first d outputs of the merge (A first on
 // ties), by one warp: the predicate A[a] <= B[d-1-a] holds on a prefix of
@@ -447,14 +558,11 @@ double expected_draws(double n_pos, double empty, double need) {
   return n_pos * log((empty + 0.5) / (empty - need + 0.5));
 }
 
-// Counters of the regrow branch (it runs beside the select on a second stream).
-struct DrawState {
-  uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
-};
-
 struct RWs {
-  size_t state, dstate, scan, scan2, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, total;
+  size_t state, dstate, scan, scan2, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, bcnt,
+      boffs, bslots, total;
   int64_t d_max, cap, n_merge_tiles;
+  uint32_t n_bkt;  // sort buckets of the regrown positions
 };
 
 RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
@@ -498,6 +606,13 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += bucket_sort_temp_bytes((int64_t)np);
   w.part = o;
   o += align_up(8 * (size_t)(w.n_merge_tiles + 2), kAlign);
+  w.n_bkt = (uint32_t)((int64_t)np / kBktTarget > 0 ? (int64_t)np / kBktTarget : 1);
+  w.bcnt = o;
+  o += align_up(4 * ((size_t)w.n_bkt + 1), kAlign);
+  w.boffs = o;
+  o += align_up(4 * ((size_t)w.n_bkt + 1), kAlign);
+  w.bslots = o;
+  o += align_up(8 * (size_t)w.n_bkt * kBktCap, kAlign);
   w.total = o;
   return w;
 }
@@ -518,6 +633,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
   uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
   int64_t *part = reinterpret_cast<int64_t *>(b + W.part);
+  uint32_t *bcnt = reinterpret_cast<uint32_t *>(b + W.bcnt);
+  uint32_t *boffs = reinterpret_cast<uint32_t *>(b + W.boffs);
+  uint64_t *bslots = reinterpret_cast<uint64_t *>(b + W.bslots);
   const TV *val = reinterpret_cast<const TV *>(a.val);
   const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
   const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
@@ -531,9 +649,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // Two branches meet at the merge: the regrow (draws, acceptance, sort of
   // the grown positions) depends only on the old pattern and runs on the
   // handle's second stream, beside the prune select and the survivor scan on
-  // the caller's stream.  The host reads back each draw chunk's accepted
-  // count (pinned memory, an event on the second stream) while the device
-  // goes on.  Every return after the fork joins the branches first, so no
+  // the caller's stream.  The host reads each draw chunk's accepted count
+  // from mapped pinned words that a kernel writes (an event on the second
+  // stream marks them ready) while the device goes on.  Every return after the fork joins the branches first, so no
   // work on the second stream outlives the call's work on s.
   cudaStream_t s2 = a.aux;
   DrawState *ds = reinterpret_cast<DrawState *>(b + W.dstate);
@@ -546,6 +664,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     return cudaStreamWaitEvent(s, a.ev_join, 0);
   };
   const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
+  const double bscale = (double)W.n_bkt / (double)n_pos;  // regrown positions are < n_pos
   const double empty = (double)n_pos - (double)nnz;
   int64_t done = 0, acc = 0;
   auto draw_chunk = [&](int64_t m) -> cudaError_t {
@@ -553,10 +672,11 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
                                              hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
     launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
                                                      flags);
-    cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune},
-                                              &ds->total, stemp2, s2);
+    const AcceptOut out{grown_a, acc, n_prune, bcnt, bslots, bscale, W.n_bkt, &ds->bucket_overflow};
+    cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, out, &ds->total, stemp2, s2);
     if (err != cudaSuccess) return err;
-    err = cudaMemcpyAsync(a.host_counts, ds, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost, s2);
+    launch_pdl(k_bkt_scan, 1, kBktScanThreads, 0, s2, bcnt, W.n_bkt, boffs, (const DrawState *)ds, a.counts_dev);
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     return cudaEventRecord(a.counts_ready, s2);
   };
@@ -572,18 +692,20 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // right behind it, before the host has read the count (and redone if more
   // chunks turn out to be needed).
   const bool speculative = n_prune > 1 && (double)n_pos - (double)nnz >= 2.0 * (double)n_prune;
+  // The first chunk's accepted positions already sit in their buckets
+  // (AcceptOut): bucket offsets, then a rank inside each bucket, with slots
+  // the chunk left empty filled past n_pos.  After more chunks, or when a
+  // bucket overflowed, the whole list is sorted the general way.
   auto sort_grown = [&](bool first_chunk_only) -> cudaError_t {
     if (!first_chunk_only)  // every slot filled by accepted draws
       return bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s2);
-    launch_pdl(k_fill_tail, grid_for(n_prune, 256, 1184), 256, 0, s2, grown_a, &ds->total, n_prune, n_pos);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    return bucket_sort_u64(grown_a, n_prune, n_pos + (uint64_t)n_prune - 1, grown_b, b + W.radix, s2);
+    launch_pdl(k_bkt_rank, (W.n_bkt + 7) / 8, 256, 0, s2, bslots, bcnt, boffs, W.n_bkt, n_prune, n_pos, grown_b);
+    return cudaGetLastError();
   };
   if (n_prune > 0) {
-    e2 = cudaMemsetAsync(ds, 0, sizeof(DrawState), s2);
-    if (e2 == cudaSuccess) e2 = cudaMemsetAsync(hkeys, 0xFF, 8 * (size_t)W.cap, s2);
-    if (e2 == cudaSuccess) e2 = cudaMemsetAsync(hmin, 0xFF, 4 * (size_t)W.cap, s2);
+    launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, hkeys, hmin, (int64_t)W.cap, bcnt,
+               (int64_t)W.n_bkt);
+    e2 = cudaGetLastError();
     if (e2 == cudaSuccess) {
       m = chunk_size();
       e2 = draw_chunk(m);
@@ -621,6 +743,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     }
     acc += a.host_counts[0];
     done += m;
+    if (a.host_counts[2]) resort = true;  // a bucket overflowed: sort the list the general way
     if (acc >= n_prune) break;
     if (done >= W.d_max) {
       verdict = SNACK_ERR_NO_SPACE;

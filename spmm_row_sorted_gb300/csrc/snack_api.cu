@@ -353,10 +353,15 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
 // Pinned host words and an event for reading small device results back
 // (made on a handle's first restructure).
 bool readback_ready(snack_handle h) {
-  if (!h->host_counts) {
-    void *hp = nullptr;
-    if (cudaHostAlloc(&hp, 2 * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess) return false;
+  if (!h->host_counts) {  // mapped, so a kernel writes the words and the host reads them with no copy
+    void *hp = nullptr, *dp = nullptr;
+    if (cudaHostAlloc(&hp, 4 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess) return false;
+    if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess || !dp) {
+      cudaFreeHost(hp);
+      return false;
+    }
     h->host_counts = reinterpret_cast<uint32_t *>(hp);
+    h->host_counts_dev = reinterpret_cast<uint32_t *>(dp);
   }
   if (!h->counts_ready && cudaEventCreateWithFlags(&h->counts_ready, cudaEventDisableTiming) != cudaSuccess)
     return false;
@@ -620,8 +625,16 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
     return SNACK_ERR_CUDA;
   if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
-  if (!h->aux && cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess) return SNACK_ERR_CUDA;
+  if (!h->aux) {
+    // The regrow branch (draws, acceptance, sort) is the longer of the two
+    // that meet at the merge: its stream gets the highest priority, so its
+    // blocks are scheduled ahead of the select's when both wait for SMs.
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SNACK_ERR_CUDA;
+    if (cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess) return SNACK_ERR_CUDA;
+  }
   a.host_counts = h->host_counts;
+  a.counts_dev = h->host_counts_dev;
   a.counts_ready = h->counts_ready;
   a.aux = h->aux;
   a.ev_fork = h->ev_fork;

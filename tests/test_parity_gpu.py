@@ -228,6 +228,22 @@ def test_restructure_ties_zeros_nan():
     restructure_and_check(lay, 700, seed=9, step=2)
 
 
+def test_restructure_crowded_empties_general_sort():
+    # Every empty position sits in the last row, so the regrown positions all
+    # land in one bucket of the position range: the bucket overflows and the
+    # regrown list is sorted the general way.  Output still bit-exact.
+    out_f, in_f = 64, 512
+    full = np.arange(63 * in_f, dtype=np.int64)
+    rng = np.random.default_rng(5)
+    tail = 63 * in_f + np.sort(rng.choice(in_f, 100, replace=False))
+    p = np.concatenate([full, tail])
+    val = wl.random_normal(p.size, seed=5, stream=0, std=0.3)
+    lay = wl.Layer(out_f, in_f, (p // in_f).astype(np.int32), (p % in_f).astype(np.int32), val,
+                   wl.random_normal(out_f, 5, 1), "f32")
+    for step in range(3):
+        restructure_and_check(lay, 200, seed=11, step=step)
+
+
 def test_restructure_chain_of_steps():
     lay = wl.make_layer(200, 300, nnz=6000, val_dtype="f32", seed=12)
     row, col, val, bias = layer_tensors(lay)
