@@ -39,9 +39,11 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 // restructure's merge), kPlanRowTilesReady (also the forward tiles: a
 // per-row restructure keeps every row's offsets).
 constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
+// With `aux` (and two events), the forward tiles are cut on that stream,
+// beside the column view on s, and s waits for them before returning.
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready);
+                       int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr);
 
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,

@@ -416,7 +416,7 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz) { return bu
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready) {
+                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
@@ -430,9 +430,30 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
   }
-  if (ready < kPlanRowTilesReady)
+  const bool fork = aux && ev_a && ev_b && ready == kPlanRowsReady;
+  if (fork) {  // the forward tiles need only the row offsets: cut them beside the column view
+    e = cudaEventRecord(ev_a, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, ev_a, 0);
+    if (e != cudaSuccess) return e;
+    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, aux, p.rp, out_f, nnz,
+               gf.cost_per_tile, gf.row_weight, gf.n_tiles, p.tiles_f);
+    e = cudaEventRecord(ev_b, aux);
+    if (e != cudaSuccess) {
+      cudaStreamWaitEvent(s, ev_a, 0);
+      return e;
+    }
+  } else if (ready < kPlanRowTilesReady) {
     launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s, p.rp, out_f, nnz, gf.cost_per_tile,
                                                                            gf.row_weight, gf.n_tiles, p.tiles_f);
+  }
+  // every return from here on joins the forward tiles first
+  auto joined = [&](cudaError_t err) -> cudaError_t {
+    if (fork) {
+      cudaError_t j = cudaStreamWaitEvent(s, ev_b, 0);
+      if (err == cudaSuccess) err = j;
+    }
+    return err;
+  };
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
   const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));
@@ -450,7 +471,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
     e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
                              offs, t + 2 * hbytes, s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return joined(e);
     launch_pdl(k_colview_bucket, kRadixBins, kRadixThreads, 0, s, ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
                                                           p.cp, p.rowt16);
   } else if (nnz > 0) {
@@ -461,7 +482,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     uint32_t *keys_out = reinterpret_cast<uint32_t *>(b + W.keys_out);
     e = radix_sort_custom<uint32_t>(ColSrc{col, in_f}, ColviewDst{keys_out, p.row_t, p.src_t, row, out_f}, nnz,
                                     cbits, ka, va, kb, vb, b + W.radix, s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return joined(e);
     launch_pdl(k_offsets_sorted<uint32_t>, grid_for(nnz + 1, 256), 256, 0, s, keys_out, nnz, in_f, p.cp);
     if (p.rowt16) launch_pdl(k_pack16, grid_for(nnz, 256), 256, 0, s, p.row_t, nnz, p.rowt16);
   } else {
@@ -469,7 +490,7 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   }
   launch_pdl(k_tiles, grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, s, p.cp, in_f, nnz, gt.cost_per_tile,
                                                                          gt.row_weight, gt.n_tiles, p.tiles_t);
-  return cudaGetLastError();
+  return joined(cudaGetLastError());
 }
 
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,

@@ -181,12 +181,14 @@ struct KeepVal {
   }
 };
 
-// linear position row*in_f + col of stored weight k, loaded with the scan value
+// position key (row << cbits) | col of stored weight k, loaded with the scan
+// value; keys order positions as row * in_f + col does, and split with a
+// shift and a mask
 struct PosPayload {
   const int32_t *row, *col;
-  int32_t in_f;
+  int cbits;
   __device__ uint64_t operator()(int64_t k) const {
-    return (uint64_t)(uint32_t)row[k] * (uint64_t)in_f + (uint32_t)col[k];
+    return ((uint64_t)(uint32_t)row[k] << cbits) | (uint32_t)col[k];
   }
 };
 
@@ -217,7 +219,7 @@ __device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_
   return 0xFFFFFFFFu;
 }
 
-__global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int32_t out_f,
+__global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int cbits,
                        const int32_t *__restrict__ rp, const int32_t *__restrict__ col, uint64_t *__restrict__ cand,
                        uint64_t *hkeys, uint32_t *hmin, uint64_t hmask, uint32_t *overflow) {
   pdl_wait();
@@ -241,14 +243,15 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
       cand[idx] = kEmpty;
       continue;
     }
-    cand[idx] = p;
-    uint64_t h = sm64_finalise(p) & hmask;
+    const uint64_t key = (r << cbits) | (uint32_t)c;  // position key of the draw
+    cand[idx] = key;
+    uint64_t h = sm64_finalise(key) & hmask;
     bool done = false;
     for (uint64_t probe = 0; probe <= hmask; ++probe) {
       unsigned long long prev =
           atomicCAS(reinterpret_cast<unsigned long long *>(hkeys + h), (unsigned long long)kEmpty,
-                    (unsigned long long)p);
-      if (prev == kEmpty || prev == p) {
+                    (unsigned long long)key);
+      if (prev == kEmpty || prev == key) {
         atomicMin(hmin + h, (uint32_t)i);
         done = true;
         break;
@@ -256,7 +259,6 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
       h = (h + 1) & hmask;
     }
     if (!done) atomicOr(overflow, 1u);
-    (void)out_f;
   }
 }
 
@@ -390,16 +392,16 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
 
 // One warp per bucket: each position's rank among its bucket's (distinct)
 // positions gives its place in the sorted list.  Slots past the placed
-// positions get n_pos + q, larger than every position, in order.
+// positions get key_space + q, larger than every position key, in order.
 __global__ void __launch_bounds__(256) k_bkt_rank(const uint64_t *__restrict__ bslots, const uint32_t *__restrict__ bcnt,
                                                   const uint32_t *__restrict__ offs, uint32_t nb, int64_t n,
-                                                  uint64_t n_pos, uint64_t *__restrict__ out) {
+                                                  uint64_t key_space, uint64_t *__restrict__ out) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tot = offs[nb];
   for (int64_t q = tot + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x)
-    out[q] = n_pos + (uint64_t)q;
+    out[q] = key_space + (uint64_t)q;
   const int64_t b = (int64_t)blockIdx.x * 8 + warp;
   if (b >= nb) return;
   const uint32_t L = min(bcnt[b], (uint32_t)kBktCap), o = offs[b];
@@ -449,7 +451,7 @@ __global__ void k_merge_splits(const uint64_t *__restrict__ A, int64_t na, const
 template <typename TV>
 __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
-            int64_t nb, const int64_t *__restrict__ part, int32_t in_f, int32_t out_f, const TV *__restrict__ val,
+            int64_t nb, const int64_t *__restrict__ part, int cbits, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
             int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
   pdl_wait();
@@ -459,6 +461,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ int32_t oS[kMergeTile];
   const int64_t t = blockIdx.x;
   const int64_t n = na + nb;
+  const uint64_t cmask = (1ull << cbits) - 1ull;
   const int64_t d0 = t * kMergeTile;
   const int64_t d1 = d0 + kMergeTile < n ? d0 + kMergeTile : n;
   const int64_t a0 = part[t], a1 = part[t + 1];
@@ -503,9 +506,8 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
   for (int it = 0; it < kMergeItems; ++it)
     if (src[it] != -2) {
-      uint64_t r = pos[it] / (uint64_t)in_f;
-      sA[ld + it] = r;
-      sB[ld + it] = pos[it] - r * (uint64_t)in_f;
+      sA[ld + it] = pos[it] >> cbits;
+      sB[ld + it] = pos[it] & cmask;
       oS[ld + it] = src[it];
     }
   __syncthreads();
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     uint64_t last = 0;
     if (a0 > 0) last = A[a0 - 1];
     if (b0 > 0 && B[b0 - 1] > last) last = B[b0 - 1];
-    r_before = (int64_t)(last / (uint64_t)in_f);
+    r_before = (int64_t)(last >> cbits);
   }
   for (int q = threadIdx.x; q < la + lb; q += kMergeThreads) {
     int64_t o = d0 + q;
@@ -639,6 +641,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   const TV *val = reinterpret_cast<const TV *>(a.val);
   const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
   const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
+  // positions travel as keys (row << cbits) | col: same order as row * in_f + col
+  const int cbits = bits_for((uint64_t)(a.in_f - 1));
+  const uint64_t key_space = (uint64_t)a.out_f << cbits;
   cudaError_t e;
 #define SNACK_TRY(x)                       \
   do {                                     \
@@ -664,11 +669,11 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     return cudaStreamWaitEvent(s, a.ev_join, 0);
   };
   const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
-  const double bscale = (double)W.n_bkt / (double)n_pos;  // regrown positions are < n_pos
+  const double bscale = (double)W.n_bkt / (double)key_space;  // position keys are < key_space
   const double empty = (double)n_pos - (double)nnz;
   int64_t done = 0, acc = 0;
   auto draw_chunk = [&](int64_t m) -> cudaError_t {
-    launch_pdl(k_draw, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, a.out_f, a.rp_old, a.col, cand,
+    launch_pdl(k_draw, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, a.rp_old, a.col, cand,
                                              hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
     launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
                                                      flags);
@@ -694,12 +699,12 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   const bool speculative = n_prune > 1 && (double)n_pos - (double)nnz >= 2.0 * (double)n_prune;
   // The first chunk's accepted positions already sit in their buckets
   // (AcceptOut): bucket offsets, then a rank inside each bucket, with slots
-  // the chunk left empty filled past n_pos.  After more chunks, or when a
+  // the chunk left empty filled past key_space.  After more chunks, or when a
   // bucket overflowed, the whole list is sorted the general way.
   auto sort_grown = [&](bool first_chunk_only) -> cudaError_t {
     if (!first_chunk_only)  // every slot filled by accepted draws
-      return bucket_sort_u64(grown_a, n_prune, n_pos - 1, grown_b, b + W.radix, s2);
-    launch_pdl(k_bkt_rank, (W.n_bkt + 7) / 8, 256, 0, s2, bslots, bcnt, boffs, W.n_bkt, n_prune, n_pos, grown_b);
+      return bucket_sort_u64(grown_a, n_prune, key_space - 1, grown_b, b + W.radix, s2);
+    launch_pdl(k_bkt_rank, (W.n_bkt + 7) / 8, 256, 0, s2, bslots, bcnt, boffs, W.n_bkt, n_prune, key_space, grown_b);
     return cudaGetLastError();
   };
   if (n_prune > 0) {
@@ -723,7 +728,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // 2. survivors
   e = cudaGetLastError();
   if (e == cudaSuccess)
-    e = scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, a.in_f}, nnz,
+    e = scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, cbits}, nnz,
                                 KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s);
   if (e != cudaSuccess || e2 != cudaSuccess) {
     join();
@@ -766,7 +771,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
     launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, 
-        surv_pos, surv_src, n_surv, grown, n_prune, part, a.in_f, a.out_f, val, a.row_out, a.col_out,
+        surv_pos, surv_src, n_surv, grown, n_prune, part, cbits, a.out_f, val, a.row_out, a.col_out,
         reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new, a.col16_new);
   }
   SNACK_TRY(cudaGetLastError());

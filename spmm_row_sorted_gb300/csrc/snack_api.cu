@@ -641,7 +641,8 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.ev_join = h->ev_join;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
-  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady));
+  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
+                        h->aux, h->ev_fork, h->ev_join));
   return SNACK_OK;
 }
 
