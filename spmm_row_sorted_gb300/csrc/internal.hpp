@@ -41,9 +41,19 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
 // With `aux` (and two events), the forward tiles are cut on that stream,
 // beside the column view on s, and s waits for them before returning.
+// `col_hist`, when set, is the column view's first-level tile histogram
+// already made by the kernel that wrote row/col (see colview_digits).
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr);
+                       int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr,
+                       const uint32_t *col_hist = nullptr);
+
+// The column view's first level scatters (row, col) by the column's high 8
+// bits when 9..17-bit columns and row + column bits fit 32: then *shift =
+// column bits - 8 and the digit of an entry is (col >> shift) & 0xFF, per
+// tile of 2048 entries (the histogram is digit-major: [256][tiles]).
+bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
+size_t colview_hist_bytes(int64_t nnz);
 
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
@@ -71,6 +81,11 @@ struct RestructureArgs {
   cudaEvent_t ev_fork, ev_join;
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
+// Whether a restructure's merge also makes the column view's first-level
+// histogram (colview_digits holds and something is pruned), and where it
+// leaves it: pass ws + colview_hist_offset to build_plan.
+bool merge_makes_col_hist(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune, int *shift);
+size_t colview_hist_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 

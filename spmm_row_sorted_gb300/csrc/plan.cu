@@ -414,9 +414,20 @@ BuildWs build_ws_layout(int32_t out_f, int32_t in_f, int64_t nnz) {
 
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz) { return build_ws_layout(out_f, in_f, nnz).total; }
 
+bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift) {
+  const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));
+  const bool ok = nnz > 0 && cbits > 8 && cbits - 8 <= 9 && cbits + rbits <= 32;
+  if (shift) *shift = ok ? cbits - 8 : 0;
+  return ok;
+}
+
+size_t colview_hist_bytes(int64_t nnz) {
+  return align_up((size_t)ceil_div(nnz > 0 ? nnz : 1, kRadixTile) * kRadixBins * sizeof(uint32_t), kAlign);
+}
+
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b) {
+                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, const uint32_t *col_hist) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
@@ -456,8 +467,8 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   };
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
-  const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));
-  if (nnz > 0 && cbits > 8 && cbits - 8 <= 9 && cbits + rbits <= 32) {
+  const int cbits = bits_for((uint64_t)(in_f - 1));
+  if (colview_digits(out_f, in_f, nnz, nullptr)) {
     // 9..17-bit columns: stable scatter of (row, col) by the column's high 8
     // bits, then one block per group sorts by the low bits and writes the
     // column offsets
@@ -469,8 +480,12 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     const size_t hbytes = align_up((size_t)nb * kRadixBins * sizeof(uint32_t), kAlign);
     uint32_t *hist = reinterpret_cast<uint32_t *>(t);
     uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
-    e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
-                             offs, t + 2 * hbytes, s);
+    if (col_hist)
+      e = radix_pass_prehist<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz,
+                                       shift, col_hist, offs, t + 2 * hbytes, s);
+    else
+      e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
+                               offs, t + 2 * hbytes, s);
     if (e != cudaSuccess) return joined(e);
     launch_pdl(k_colview_bucket, kRadixBins, kRadixThreads, 0, s, ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
                                                           p.cp, p.rowt16);

@@ -394,6 +394,22 @@ cudaError_t radix_pass(Src src, Dst dst, int64_t n, int shift, uint32_t *hist, u
   return cudaGetLastError();
 }
 
+// The same pass when another kernel already wrote the tile histograms
+// (hist[d * nb + tile] for tiles of kRadixTile elements, digit (key >> shift) & 0xFF).
+template <typename K, typename Src, typename Dst>
+cudaError_t radix_pass_prehist(Src src, Dst dst, int64_t n, int shift, const uint32_t *hist, uint32_t *offs,
+                               void *stemp, cudaStream_t stream) {
+  const int64_t nb = ceil_div(n, kRadixTile);
+  cudaError_t e = scan_apply<uint32_t>(HistRead{hist}, nb * kRadixBins, WriteExcl32{offs}, (uint32_t *)nullptr,
+                                       stemp, stream);
+  if (e != cudaSuccess) return e;
+  const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
+  e = cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  launch_pdl(k_radix_scatter<K, Src, Dst>, (unsigned)nb, kRadixThreads, dyn, stream, src, dst, n, shift, offs, nb);
+  return cudaGetLastError();
+}
+
 // Stable sort by the low `bits` bits of the keys, 8 bits per pass (at least
 // one pass).  The first pass reads `first`, the last writes `last`; passes in
 // between ping-pong between (k0, v0) and (k1, v1).

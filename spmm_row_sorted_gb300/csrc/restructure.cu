@@ -35,6 +35,7 @@ constexpr uint64_t kEmpty = ~0ull;
 constexpr int kMergeThreads = 256;
 constexpr int kMergeItems = 4;
 constexpr int kMergeTile = kMergeThreads * kMergeItems;
+static_assert(2 * kMergeTile == kRadixTile, "two merge tiles make one tile of the column view's first radix pass");
 
 struct SelState {
   uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
@@ -371,10 +372,11 @@ __global__ void __launch_bounds__(kBktScanThreads) k_bkt_scan(const uint32_t *__
   if (tid == kBktScanThreads - 1) offs[nb] = run;
 }
 
-// Start of a restructure's regrow branch: counters and bucket counts to zero,
-// the position table to empty (one launch instead of four fills).
+// Start of a restructure's regrow branch: counters, bucket counts and the
+// merge's column histogram to zero, the position table to empty (one launch
+// instead of five fills).
 __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t *__restrict__ hmin, int64_t cap,
-                          uint32_t *__restrict__ bcnt, int64_t nb) {
+                          uint32_t *__restrict__ bcnt, int64_t nb, uint32_t *__restrict__ chist, int64_t n_chist) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -388,6 +390,7 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
     hmin[i] = 0xFFFFFFFFu;
   }
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
+  for (int64_t i = i0; i < n_chist; i += stride) chist[i] = 0u;
 }
 
 // One warp per bucket: each position's rank among its bucket's (distinct)
@@ -453,12 +456,14 @@ __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
             int64_t nb, const int64_t *__restrict__ part, int cbits, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
-            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
+            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16,
+            uint32_t *__restrict__ chist, int64_t cnb, int cshift) {
   pdl_wait();
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
-  __shared__ uint32_t sS[kMergeTile];
-  __shared__ int32_t oS[kMergeTile];
+  __shared__ uint32_t sS[kMergeTile];  // survivor sources; then the output sources (oS)
+  __shared__ uint32_t s_hist[kRadixBins];
+  int32_t *oS = reinterpret_cast<int32_t *>(sS);
   const int64_t t = blockIdx.x;
   const int64_t n = na + nb;
   const uint64_t cmask = (1ull << cbits) - 1ull;
@@ -472,6 +477,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     sS[q] = As[a0 + q];
   }
   for (int q = threadIdx.x; q < lb; q += kMergeThreads) sB[q] = B[b0 + q];
+  if (chist)
+    for (int d = threadIdx.x; d < kRadixBins; d += kMergeThreads) s_hist[d] = 0u;
   __syncthreads();
   int ld = threadIdx.x * kMergeItems;
   if (ld > la + lb) ld = la + lb;
@@ -502,15 +509,22 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
   }
   __syncthreads();
-  // stage rows / cols / sources in shared memory, then write coalesced
+  // stage rows / cols / sources in shared memory, then write coalesced; with
+  // chist (zeroed beforehand), count each output column's high digit into the
+  // column view's first radix pass, whose tiles are two merge tiles
 #pragma unroll
   for (int it = 0; it < kMergeItems; ++it)
     if (src[it] != -2) {
+      const uint64_t c = pos[it] & cmask;
       sA[ld + it] = pos[it] >> cbits;
-      sB[ld + it] = pos[it] & cmask;
+      sB[ld + it] = c;
       oS[ld + it] = src[it];
+      if (chist) atomicAdd(&s_hist[(uint32_t)(c >> cshift) & 0xFFu], 1u);
     }
   __syncthreads();
+  if (chist)
+    for (int d = threadIdx.x; d < kRadixBins; d += kMergeThreads)
+      if (s_hist[d]) atomicAdd(&chist[(int64_t)d * cnb + (t >> 1)], s_hist[d]);
   // row offsets of the output: rp[r] = o for the rows r in (row[o-1], row[o]];
   // the row before the tile is that of the larger of the two inputs' last
   // elements consumed by earlier tiles
@@ -644,6 +658,13 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // positions travel as keys (row << cbits) | col: same order as row * in_f + col
   const int cbits = bits_for((uint64_t)(a.in_f - 1));
   const uint64_t key_space = (uint64_t)a.out_f << cbits;
+  // the merge also makes the column view's first-level histogram (zeroed by
+  // the regrow branch's init kernel, so only when something is pruned)
+  int cshift = 0;
+  uint32_t *chist = merge_makes_col_hist(a.out_f, a.in_f, nnz, n_prune, &cshift)
+                        ? reinterpret_cast<uint32_t *>(b + colview_hist_offset(a.out_f, a.in_f, nnz, n_prune))
+                        : nullptr;
+  const int64_t n_chist = chist ? ceil_div(nnz, kRadixTile) * kRadixBins : 0;
   cudaError_t e;
 #define SNACK_TRY(x)                       \
   do {                                     \
@@ -709,7 +730,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   };
   if (n_prune > 0) {
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, hkeys, hmin, (int64_t)W.cap, bcnt,
-               (int64_t)W.n_bkt);
+               (int64_t)W.n_bkt, chist, n_chist);
     e2 = cudaGetLastError();
     if (e2 == cudaSuccess) {
       m = chunk_size();
@@ -770,9 +791,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   if (nnz > 0) {
     launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
-    launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, 
-        surv_pos, surv_src, n_surv, grown, n_prune, part, cbits, a.out_f, val, a.row_out, a.col_out,
-        reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new, a.col16_new);
+    launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, surv_pos, surv_src, n_surv, grown, n_prune,
+               part, cbits, a.out_f, val, a.row_out, a.col_out, reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new,
+               a.col16_new, chist, ceil_div(nnz, kRadixTile), cshift);
   }
   SNACK_TRY(cudaGetLastError());
 #undef SNACK_TRY
@@ -1012,10 +1033,21 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
 
 }  // namespace
 
-size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+bool merge_makes_col_hist(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune, int *shift) {
+  return n_prune > 0 && colview_digits(out_f, in_f, nnz, shift);
+}
+
+// The merge's column histogram sits past both the restructure's own scratch
+// and the plan rebuild's, so the rebuild can read it while reusing the rest.
+size_t colview_hist_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
   size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
-  return r > p ? r : p;
+  return align_up(r > p ? r : p, kAlign);
+}
+
+size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+  return colview_hist_offset(out_f, in_f, nnz, n_prune) +
+         (colview_digits(out_f, in_f, nnz, nullptr) ? colview_hist_bytes(nnz) : 0);
 }
 
 snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) {

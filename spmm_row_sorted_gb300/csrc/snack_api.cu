@@ -641,8 +641,13 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.ev_join = h->ev_join;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
+  const uint32_t *col_hist =
+      merge_makes_col_hist(h->out_f, h->in_f, nnz, n_prune, nullptr)
+          ? reinterpret_cast<const uint32_t *>(reinterpret_cast<uint8_t *>(ws) +
+                                               colview_hist_offset(h->out_f, h->in_f, nnz, n_prune))
+          : nullptr;
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
-                        h->aux, h->ev_fork, h->ev_join));
+                        h->aux, h->ev_fork, h->ev_join, col_hist));
   return SNACK_OK;
 }
 
