@@ -77,9 +77,10 @@ __global__ void k_count(const int32_t *__restrict__ idx, int64_t nnz, int32_t n,
 // ballots plus per-warp counts keep storage order within every column.
 constexpr int kColLowMax = 512;  // 2^shift bins at most
 
+template <int kShift>
 __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t *__restrict__ keys,
                                                                   const uint32_t *__restrict__ vals, int64_t n,
-                                                                  int shift, int cbits,
+                                                                  int cbits,
                                                                   const uint32_t *__restrict__ offs, int64_t nb,
                                                                   int32_t in_f, int32_t *__restrict__ row_t,
                                                                   int32_t *__restrict__ src_t, int32_t *__restrict__ cp,
@@ -91,8 +92,9 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
   __shared__ uint32_t s_src[kRadixTile], s_row[kRadixTile];
   __shared__ uint16_t s_col[kRadixTile];
   const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int L = 1 << shift;
-  const uint32_t lmask = (uint32_t)(L - 1);
+  constexpr int shift = kShift;  // low column bits sorted here (the group holds 2^shift columns)
+  constexpr int L = 1 << shift;
+  constexpr uint32_t lmask = (uint32_t)(L - 1);
   const int64_t start = offs[(int64_t)b * nb];
   const int64_t end = b + 1 < kRadixBins ? (int64_t)offs[(int64_t)(b + 1) * nb] : n;
   // column counts of the group, then exclusive offsets = column starts
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
     }
     if (c0 + kRadixTile < end) load(c0 + kRadixTile);
     __syncthreads();  // the previous chunk is done with wc, lstart and the staging arrays
-    for (int i = threadIdx.x; i < kRadixWarps * L; i += kRadixThreads) (&wc[0][0])[(i / L) * kColLowMax + i % L] = 0;
+    for (int i = threadIdx.x; i < kRadixWarps * L; i += kRadixThreads) wc[i >> shift][i & (L - 1)] = 0;
     __syncthreads();
     int dig[kRadixItems];
     uint32_t rank[kRadixItems];
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
 #pragma unroll
     for (int i = 0; i < kRadixItems; ++i) {
       unsigned peers = 0xffffffffu;
+#pragma unroll
       for (int bit = 0; bit <= shift; ++bit) {  // shift + 1 bits cover the sentinel
         const bool on = (dig[i] >> bit) & 1;
         const unsigned bal = __ballot_sync(0xffffffffu, on);
@@ -414,6 +417,32 @@ BuildWs build_ws_layout(int32_t out_f, int32_t in_f, int64_t nnz) {
 
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz) { return build_ws_layout(out_f, in_f, nnz).total; }
 
+namespace {
+template <int kShift>
+cudaError_t launch_cvb(const uint32_t *ka, const uint32_t *va, int64_t nnz, int cbits, const uint32_t *offs, int64_t nb,
+                       int32_t in_f, const PlanPtrs &p, cudaStream_t s) {
+  launch_pdl(k_colview_bucket<kShift>, kRadixBins, kRadixThreads, 0, s, ka, va, nnz, cbits, offs, nb, in_f, p.row_t,
+             p.src_t, p.cp, p.rowt16);
+  return cudaGetLastError();
+}
+// the group kernel for 1..9 low column bits
+cudaError_t launch_colview_bucket(int shift, const uint32_t *ka, const uint32_t *va, int64_t nnz, int cbits,
+                                  const uint32_t *offs, int64_t nb, int32_t in_f, const PlanPtrs &p, cudaStream_t s) {
+  switch (shift) {
+    case 1: return launch_cvb<1>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 2: return launch_cvb<2>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 3: return launch_cvb<3>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 4: return launch_cvb<4>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 5: return launch_cvb<5>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 6: return launch_cvb<6>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 7: return launch_cvb<7>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 8: return launch_cvb<8>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    case 9: return launch_cvb<9>(ka, va, nnz, cbits, offs, nb, in_f, p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+}  // namespace
+
 bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift) {
   const int cbits = bits_for((uint64_t)(in_f - 1)), rbits = bits_for((uint64_t)(out_f - 1));
   const bool ok = nnz > 0 && cbits > 8 && cbits - 8 <= 9 && cbits + rbits <= 32;
@@ -487,8 +516,8 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
       e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
                                offs, t + 2 * hbytes, s);
     if (e != cudaSuccess) return joined(e);
-    launch_pdl(k_colview_bucket, kRadixBins, kRadixThreads, 0, s, ka, va, nnz, shift, cbits, offs, nb, in_f, p.row_t, p.src_t,
-                                                          p.cp, p.rowt16);
+    e = launch_colview_bucket(shift, ka, va, nnz, cbits, offs, nb, in_f, p, s);
+    if (e != cudaSuccess) return joined(e);
   } else if (nnz > 0) {
     uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
     uint32_t *va = reinterpret_cast<uint32_t *>(b + W.vals_a);
