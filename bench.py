@@ -842,12 +842,12 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk)."""
-    draw_chunk = 1 + 1 + 2  # draws, accept flags, scan (second stream)
-    sort_grown = 1 + 1 + 2 + 1 + 1  # sentinel tail, bucket count, scan, fill, rank (second stream)
+    draw_chunk = 1 + 1 + 1 + 2 + 1  # init, draws, accept flags, scan (+ bucket fill), bucket offsets (second stream)
+    sort_grown = 1  # rank inside each bucket (second stream)
     select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
     keep_scan = 2
-    merge = 2  # split points, merge (also writes the row offsets)
-    plan = 1 + (1 + 2 + 1) + 1 + 1  # row tiles, high-digit column scatter, per-group column sort, column tiles
+    merge = 2  # split points, merge (also writes the row offsets and the column digit counts)
+    plan = 1 + (2 + 1) + 1 + 1  # row tiles (second stream), column digit scan + scatter, per-group column sort, column tiles
     return draw_chunk + sort_grown + select + keep_scan + merge + plan
 
 
