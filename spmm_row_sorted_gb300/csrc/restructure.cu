@@ -464,6 +464,8 @@ __global__ void __launch_bounds__(kMergeThreads)
   __shared__ uint32_t sS[kMergeTile];  // survivor sources; then the output sources (oS)
   __shared__ uint32_t s_hist[kRadixBins];
   int32_t *oS = reinterpret_cast<int32_t *>(sS);
+  // after the merge, the two key arrays hold the outputs' rows and columns as 32-bit words
+  uint32_t *oR = reinterpret_cast<uint32_t *>(sA), *oC = reinterpret_cast<uint32_t *>(sB);
   const int64_t t = blockIdx.x;
   const int64_t n = na + nb;
   const uint64_t cmask = (1ull << cbits) - 1ull;
@@ -515,9 +517,9 @@ __global__ void __launch_bounds__(kMergeThreads)
 #pragma unroll
   for (int it = 0; it < kMergeItems; ++it)
     if (src[it] != -2) {
-      const uint64_t c = pos[it] & cmask;
-      sA[ld + it] = pos[it] >> cbits;
-      sB[ld + it] = c;
+      const uint32_t c = (uint32_t)(pos[it] & cmask);
+      oR[ld + it] = (uint32_t)(pos[it] >> cbits);
+      oC[ld + it] = c;
       oS[ld + it] = src[it];
       if (chist) atomicAdd(&s_hist[(uint32_t)(c >> cshift) & 0xFFu], 1u);
     }
@@ -528,28 +530,29 @@ __global__ void __launch_bounds__(kMergeThreads)
   // row offsets of the output: rp[r] = o for the rows r in (row[o-1], row[o]];
   // the row before the tile is that of the larger of the two inputs' last
   // elements consumed by earlier tiles
-  int64_t r_before = -1;
+  int r_before = -1;
   if (d0 > 0) {
     uint64_t last = 0;
     if (a0 > 0) last = A[a0 - 1];
     if (b0 > 0 && B[b0 - 1] > last) last = B[b0 - 1];
-    r_before = (int64_t)(last >> cbits);
+    r_before = (int)(last >> cbits);
   }
   for (int q = threadIdx.x; q < la + lb; q += kMergeThreads) {
-    int64_t o = d0 + q;
-    int32_t s = oS[q];
-    row_out[o] = (int32_t)sA[q];
-    col_out[o] = (int32_t)sB[q];
-    if (col16) col16[o] = (uint16_t)sB[q];
+    const int64_t o = d0 + q;
+    const int32_t s = oS[q];
+    const uint32_t rr = oR[q], cc = oC[q];
+    row_out[o] = (int32_t)rr;
+    col_out[o] = (int32_t)cc;
+    if (col16) col16[o] = (uint16_t)cc;
     val_out[o] = s >= 0 ? val[s] : from_f32<TV>(0.f);
     if (src_out) src_out[o] = s;
-    const int64_t r_cur = (int64_t)sA[q];
-    const int64_t r_prev = q > 0 ? (int64_t)sA[q - 1] : r_before;
-    for (int64_t r = r_prev + 1; r <= r_cur && r <= out_f; ++r) rp[r] = (int32_t)o;
+    const int r_cur = (int)rr;
+    const int r_prev = q > 0 ? (int)oR[q - 1] : r_before;
+    for (int r = r_prev + 1; r <= r_cur && r <= out_f; ++r) rp[r] = (int32_t)o;
   }
   if (d1 == n && threadIdx.x == 0) {  // rows after the last stored weight
-    const int64_t r_last = la + lb > 0 ? (int64_t)sA[la + lb - 1] : r_before;
-    for (int64_t r = r_last + 1; r <= out_f; ++r) rp[r] = (int32_t)n;
+    const int64_t r_last = la + lb > 0 ? (int64_t)oR[la + lb - 1] : r_before;
+    for (int64_t r = r_last + 1; r <= out_f; ++r) rp[r] = (int32_t)n;  // 64-bit: out_f may be 2^31 - 1
   }
 }
 
