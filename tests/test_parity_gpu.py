@@ -316,14 +316,14 @@ def test_call_errors():
     with pytest.raises(snack.SnackError) as e:
         L.forward(x)  # batch > max_batch
     assert e.value.status == 1
-    # a short workspace: batch 16 takes the tile kernels, which need scratch
-    L16 = snack.SparseLinear(30, 20, row, col, val, bias, max_batch=16)
-    x16 = torch.zeros((16, 20), device="cuda")
-    y16 = torch.empty((16, 30), device="cuda")
+    # a short workspace: batch 32 takes the tile kernels, which need scratch
+    L32 = snack.SparseLinear(30, 20, row, col, val, bias, max_batch=32)
+    x32 = torch.zeros((32, 20), device="cuda")
+    y32 = torch.empty((32, 30), device="cuda")
     with pytest.raises(snack.SnackError) as e:
-        snack.snack_spmm_fwd(L16.handle, row, col, val, x16, 16, bias, y16, L16.ws[:256])
+        snack.snack_spmm_fwd(L32.handle, row, col, val, x32, 32, bias, y32, L32.ws[:256])
     assert e.value.status == 4
-    L16.close()
+    L32.close()
     # batch 2 runs the small-batch kernel, which uses no workspace
     y = torch.empty((2, 30), device="cuda")
     snack.snack_spmm_fwd(L.handle, row, col, val, x[:2], 2, bias, y, L.ws[:256])
@@ -430,11 +430,12 @@ def test_split_rows_repeat_calls_bitwise():
 
 # The small-batch kernels stage the gathered operand (X, or dY for the column
 # view) whole in shared memory when it fits in 96 KB at the padded batch width
-# (1, 2, 4 or 8); wider operands take the tile kernels.  Cases on both sides of
-# that limit, for every op.
+# (1, 2, 4 or 8); wider operands, and batches above 8, take the tile kernels.
+# Cases on both sides of that limit, for every op.
 @pytest.mark.parametrize("dtype,batch,feat", [("f32", 8, 3072), ("f32", 8, 3073), ("f32", 4, 6144), ("f32", 3, 6145),
                                               ("bf16", 8, 6144), ("bf16", 6, 6145), ("bf16", 2, 24576),
-                                              ("f32", 1, 40000)])
+                                              ("f32", 1, 40000), ("bf16", 16, 5120), ("bf16", 16, 5121),
+                                              ("f32", 12, 2560), ("f32", 9, 2561)])
 def test_small_batch_stage_limit(dtype, batch, feat):
     other = 97
     for out_f, in_f in ((other, feat), (feat, other)):
