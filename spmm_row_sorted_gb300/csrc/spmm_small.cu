@@ -381,18 +381,42 @@ int small_rows_per_cta(K kern, size_t smem, int n_rows, int num_sms) {
   return (int)R;
 }
 
+// Host-side state a launch would otherwise query every call: the largest
+// dynamic shared memory granted to the kernel so far, and the rows per CTA
+// last derived for a (device, shared memory, rows) triple.  Per host thread.
+struct SmallLaunchCache {
+  size_t granted = 0;
+  int dev = -1, n_rows = -1, num_sms = -1, R = 0;
+  size_t smem = 0;
+};
+
 template <typename TA, typename TV, int kB, bool kStage, bool kGV, bool kFuse>
 cudaError_t launch_small_s(const SpmmParams &p, int num_sms, cudaStream_t s) {
   auto kern = k_spmm_small<TA, TV, kB, kStage, kGV, kFuse>;
+  thread_local SmallLaunchCache cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (cache.dev != dev) cache = SmallLaunchCache{0, dev};
   const size_t smem_max = small_smem_bytes(p.n_src, kB, sizeof(TA), 64, kStage);
-  if (smem_max > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+  auto fused = k_spmm_small<TA, TV, kB, kStage, true, true>;  // sizes the column-view calls' CTAs
+  if (smem_max > 48 * 1024 && smem_max > cache.granted) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+    if (e == cudaSuccess && kGV)  // the occupancy query below must see the same limit
+      e = cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
     if (e != cudaSuccess) return e;
+    cache.granted = smem_max;
   }
   // the column-view calls size their CTAs by the fused kernel, so dX comes
   // out of the same row partition (and summation order) with or without dW
-  const int R = kGV ? small_rows_per_cta(k_spmm_small<TA, TV, kB, kStage, true, true>, smem_max, p.n_rows, num_sms)
-                    : small_rows_per_cta(kern, smem_max, p.n_rows, num_sms);
+  if (cache.smem != smem_max || cache.n_rows != p.n_rows || cache.num_sms != num_sms) {
+    cache.R = kGV ? small_rows_per_cta(fused, smem_max, p.n_rows, num_sms)
+                  : small_rows_per_cta(kern, smem_max, p.n_rows, num_sms);
+    cache.smem = smem_max;
+    cache.n_rows = p.n_rows;
+    cache.num_sms = num_sms;
+  }
+  const int R = cache.R;
   const size_t smem = small_smem_bytes(p.n_src, kB, sizeof(TA), R, kStage);
   const unsigned grid = (unsigned)((p.n_rows + R - 1) / R);
   launch_pdl(kern, grid, kSmallThreads, smem, s, p, R);

@@ -380,15 +380,17 @@ def test_backward_workloads_c1_c4():
         check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
 
 
-@pytest.mark.parametrize("batch", [32, 5])
-def test_backward_equals_separate_calls_bitwise(batch):
+@pytest.mark.parametrize("batch,out_f,in_f,nnz", [(32, 300, 400, 20000), (5, 300, 400, 20000),
+                                                  (8, 3000, 600, 900000)])
+def test_backward_equals_separate_calls_bitwise(batch, out_f, in_f, nnz):
     # dX and db come from the same kernels and tiles as the separate calls, so
     # they are bit-identical; dW may differ in summation order (checked above
-    # against the oracle).  Batch 5 runs the small-batch path.
-    lay = wl.make_layer(300, 400, nnz=20000, val_dtype="f32", seed=4, bias="normal")
-    acts = wl.make_acts(batch, 400, 300, "f32", seed=4)
+    # against the oracle).  Batches 5 and 8 run the small-batch path; the last
+    # case stages 94 KB of dY per CTA (above the default 48 KB limit).
+    lay = wl.make_layer(out_f, in_f, nnz=nnz, val_dtype="f32", seed=4, bias="normal")
+    acts = wl.make_acts(batch, in_f, out_f, "f32", seed=4)
     row, col, val, bias = layer_tensors(lay)
-    L = snack.SparseLinear(300, 400, row, col, val, bias, max_batch=batch)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=batch)
     x, dy = act_tensor(acts.x, "f32"), act_tensor(acts.dy, "f32")
     dx_f, dw_f, db_f = L.backward(x, dy)
     dx_s = L.grad_input(dy)
