@@ -872,9 +872,10 @@ def restructure_launches() -> int:
     sort_grown = 1  # rank inside each bucket (second stream)
     select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
     keep_scan = 2
-    merge = 2  # split points, merge (also writes the row offsets and the column digit counts)
-    plan = 1 + (2 + 1) + 1 + 1  # row tiles (second stream), column digit scan + scatter, per-group column sort, column tiles
-    return draw_chunk + sort_grown + select + keep_scan + merge + plan
+    merge = 2  # split points, merge (also writes the row offsets)
+    col_offsets = 1 + 2  # column digit histogram from the split points + its scan (second stream, beside the merge)
+    plan = 1 + 1 + 1 + 1  # row tiles (second stream), column scatter, per-group column sort, column tiles
+    return draw_chunk + sort_grown + select + keep_scan + merge + col_offsets + plan
 
 
 def main(argv=None):

@@ -24,7 +24,7 @@
  * Memory ownership.  Every device buffer -- indices, values, activations,
  * outputs, the plan and the workspaces -- is allocated and freed by the
  * caller.  The library never allocates device memory.  A handle owns host
- * metadata, and after its first restructure also a second CUDA stream, three
+ * metadata, and after its first restructure also a second CUDA stream, four
  * events and 16 bytes of mapped pinned host memory; snack_destroy frees them.
  *
  * Streams.  Every call is asynchronous on `stream` (a cudaStream_t; NULL is

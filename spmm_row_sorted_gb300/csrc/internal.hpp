@@ -41,12 +41,13 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
 // With `aux` (and two events), the forward tiles are cut on that stream,
 // beside the column view on s, and s waits for them before returning.
-// `col_hist`, when set, is the column view's first-level tile histogram
-// already made by the kernel that wrote row/col (see colview_digits).
+// `col_offs`, when set, are the column view's first-level scatter offsets
+// (digit-major, see colview_digits) already made on another stream: s waits
+// for `col_ready` and the rebuild only scatters.
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
                        int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr,
-                       const uint32_t *col_hist = nullptr);
+                       const uint32_t *col_offs = nullptr, cudaEvent_t col_ready = nullptr);
 
 // The column view's first level scatters (row, col) by the column's high 8
 // bits when 9..17-bit columns and row + column bits fit 32: then *shift =
@@ -79,13 +80,14 @@ struct RestructureArgs {
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
   cudaStream_t aux;          // second stream of the handle (regrow branch)
   cudaEvent_t ev_fork, ev_join;
+  cudaEvent_t ev_col;  // recorded on aux once the column view's first-level offsets are made
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
-// Whether a restructure's merge also makes the column view's first-level
-// histogram (colview_digits holds and something is pruned), and where it
-// leaves it: pass ws + colview_hist_offset to build_plan.
-bool merge_makes_col_hist(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune, int *shift);
-size_t colview_hist_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
+// Whether a restructure makes the column view's first-level offsets beside
+// its merge (colview_digits holds), and where it leaves them: pass
+// ws + colview_offs_offset to build_plan with the handle's ev_col.
+bool restructure_makes_col_offs(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
+size_t colview_offs_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 
@@ -139,7 +141,7 @@ struct snack_layer {
   uint32_t *host_counts_dev = nullptr;  // its device address
   cudaEvent_t counts_ready = nullptr;
   cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_col = nullptr;
   bool dense = false;   // the layer takes the dense path for wide batches
   void *lt = nullptr;   // cuBLASLt handle of the dense path
 };

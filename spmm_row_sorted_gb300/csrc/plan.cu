@@ -456,7 +456,8 @@ size_t colview_hist_bytes(int64_t nnz) {
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, const uint32_t *col_hist) {
+                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, const uint32_t *col_offs,
+                       cudaEvent_t col_ready) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
@@ -508,13 +509,17 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     uint8_t *t = b + W.radix;
     const size_t hbytes = align_up((size_t)nb * kRadixBins * sizeof(uint32_t), kAlign);
     uint32_t *hist = reinterpret_cast<uint32_t *>(t);
-    uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
-    if (col_hist)
-      e = radix_pass_prehist<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz,
-                                       shift, col_hist, offs, t + 2 * hbytes, s);
-    else
+    const uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
+    if (col_offs) {  // offsets made beside the restructure's merge: wait for them, then scatter
+      e = col_ready ? cudaStreamWaitEvent(s, col_ready, 0) : cudaSuccess;
+      if (e == cudaSuccess)
+        e = radix_scatter_only<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz,
+                                         shift, col_offs, s);
+      offs = col_offs;
+    } else {
       e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
-                               offs, t + 2 * hbytes, s);
+                               reinterpret_cast<uint32_t *>(t + hbytes), t + 2 * hbytes, s);
+    }
     if (e != cudaSuccess) return joined(e);
     e = launch_colview_bucket(shift, ka, va, nnz, cbits, offs, nb, in_f, p, s);
     if (e != cudaSuccess) return joined(e);

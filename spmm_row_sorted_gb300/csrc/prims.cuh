@@ -394,17 +394,14 @@ cudaError_t radix_pass(Src src, Dst dst, int64_t n, int shift, uint32_t *hist, u
   return cudaGetLastError();
 }
 
-// The same pass when another kernel already wrote the tile histograms
-// (hist[d * nb + tile] for tiles of kRadixTile elements, digit (key >> shift) & 0xFF).
+// The scatter half of a pass, when the digit-major offsets (exclusive scan of
+// the tile histograms, tiles of kRadixTile elements) were made elsewhere.
 template <typename K, typename Src, typename Dst>
-cudaError_t radix_pass_prehist(Src src, Dst dst, int64_t n, int shift, const uint32_t *hist, uint32_t *offs,
-                               void *stemp, cudaStream_t stream) {
+cudaError_t radix_scatter_only(Src src, Dst dst, int64_t n, int shift, const uint32_t *offs, cudaStream_t stream) {
   const int64_t nb = ceil_div(n, kRadixTile);
-  cudaError_t e = scan_apply<uint32_t>(HistRead{hist}, nb * kRadixBins, WriteExcl32{offs}, (uint32_t *)nullptr,
-                                       stemp, stream);
-  if (e != cudaSuccess) return e;
   const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
-  e = cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   launch_pdl(k_radix_scatter<K, Src, Dst>, (unsigned)nb, kRadixThreads, dyn, stream, src, dst, n, shift, offs, nb);
   return cudaGetLastError();

@@ -37,6 +37,38 @@ constexpr int kMergeItems = 4;
 constexpr int kMergeTile = kMergeThreads * kMergeItems;
 static_assert(2 * kMergeTile == kRadixTile, "two merge tiles make one tile of the column view's first radix pass");
 
+// The column view's first-level tile histogram of the merged pattern, from
+// the merge's split points alone (beside the merge, on the other stream):
+// radix tile t holds the outputs of merge tiles 2t and 2t+1, i.e. survivor
+// keys A[a0, a1) and regrown keys B[d0 - a0, d1 - a1); each output's digit is
+// its column's high 8 bits.  Every bin is written (digit-major [256][tiles]).
+__global__ void __launch_bounds__(256) k_col_hist(const uint64_t *__restrict__ A, const uint64_t *__restrict__ B,
+                                                  const int64_t *__restrict__ part, int64_t n_merge_tiles, int64_t n,
+                                                  int cbits, int cshift, uint32_t *__restrict__ chist, int64_t cnb) {
+  pdl_wait();
+  __shared__ uint32_t h[8][kRadixBins];  // one histogram per warp: less atomic contention
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 8 * kRadixBins; i += 256) (&h[0][0])[i] = 0u;
+  __syncthreads();
+  const int64_t t = blockIdx.x;
+  const int64_t d0 = t * kRadixTile, d1 = d0 + kRadixTile < n ? d0 + kRadixTile : n;
+  const int64_t m1 = 2 * t + 2 < n_merge_tiles ? 2 * t + 2 : n_merge_tiles;
+  const int64_t a0 = part[2 * t], a1 = part[m1];
+  const int64_t b0 = d0 - a0, b1 = d1 - a1;
+  const uint64_t cmask = (1ull << cbits) - 1ull;
+  for (int64_t q = a0 + threadIdx.x; q < a1; q += 256)
+    atomicAdd(&h[warp][(uint32_t)((A[q] & cmask) >> cshift) & 0xFFu], 1u);
+  for (int64_t q = b0 + threadIdx.x; q < b1; q += 256)
+    atomicAdd(&h[warp][(uint32_t)((B[q] & cmask) >> cshift) & 0xFFu], 1u);
+  __syncthreads();
+  for (int d = threadIdx.x; d < kRadixBins; d += 256) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) c += h[w][d];
+    chist[(int64_t)d * cnb + t] = c;
+  }
+}
+
 struct SelState {
   uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
   uint32_t overflow;                           // a draw found the position table full
@@ -372,11 +404,10 @@ __global__ void __launch_bounds__(kBktScanThreads) k_bkt_scan(const uint32_t *__
   if (tid == kBktScanThreads - 1) offs[nb] = run;
 }
 
-// Start of a restructure's regrow branch: counters, bucket counts and the
-// merge's column histogram to zero, the position table to empty (one launch
-// instead of five fills).
+// Start of a restructure's regrow branch: counters and bucket counts to zero,
+// the position table to empty (one launch instead of four fills).
 __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t *__restrict__ hmin, int64_t cap,
-                          uint32_t *__restrict__ bcnt, int64_t nb, uint32_t *__restrict__ chist, int64_t n_chist) {
+                          uint32_t *__restrict__ bcnt, int64_t nb) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -390,7 +421,6 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
     hmin[i] = 0xFFFFFFFFu;
   }
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
-  for (int64_t i = i0; i < n_chist; i += stride) chist[i] = 0u;
 }
 
 // One warp per bucket: each position's rank among its bucket's (distinct)
@@ -456,13 +486,11 @@ __global__ void __launch_bounds__(kMergeThreads)
     k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
             int64_t nb, const int64_t *__restrict__ part, int cbits, int32_t out_f, const TV *__restrict__ val,
             int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
-            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16,
-            uint32_t *__restrict__ chist, int64_t cnb, int cshift) {
+            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
   pdl_wait();
   __shared__ uint64_t sA[kMergeTile];
   __shared__ uint64_t sB[kMergeTile];
   __shared__ uint32_t sS[kMergeTile];  // survivor sources; then the output sources (oS)
-  __shared__ uint32_t s_hist[kRadixBins];
   int32_t *oS = reinterpret_cast<int32_t *>(sS);
   // after the merge, the two key arrays hold the outputs' rows and columns as 32-bit words
   uint32_t *oR = reinterpret_cast<uint32_t *>(sA), *oC = reinterpret_cast<uint32_t *>(sB);
@@ -479,8 +507,6 @@ __global__ void __launch_bounds__(kMergeThreads)
     sS[q] = As[a0 + q];
   }
   for (int q = threadIdx.x; q < lb; q += kMergeThreads) sB[q] = B[b0 + q];
-  if (chist)
-    for (int d = threadIdx.x; d < kRadixBins; d += kMergeThreads) s_hist[d] = 0u;
   __syncthreads();
   int ld = threadIdx.x * kMergeItems;
   if (ld > la + lb) ld = la + lb;
@@ -511,9 +537,7 @@ __global__ void __launch_bounds__(kMergeThreads)
     }
   }
   __syncthreads();
-  // stage rows / cols / sources in shared memory, then write coalesced; with
-  // chist (zeroed beforehand), count each output column's high digit into the
-  // column view's first radix pass, whose tiles are two merge tiles
+  // stage rows / cols / sources in shared memory, then write coalesced
 #pragma unroll
   for (int it = 0; it < kMergeItems; ++it)
     if (src[it] != -2) {
@@ -521,12 +545,8 @@ __global__ void __launch_bounds__(kMergeThreads)
       oR[ld + it] = (uint32_t)(pos[it] >> cbits);
       oC[ld + it] = c;
       oS[ld + it] = src[it];
-      if (chist) atomicAdd(&s_hist[(uint32_t)(c >> cshift) & 0xFFu], 1u);
     }
   __syncthreads();
-  if (chist)
-    for (int d = threadIdx.x; d < kRadixBins; d += kMergeThreads)
-      if (s_hist[d]) atomicAdd(&chist[(int64_t)d * cnb + (t >> 1)], s_hist[d]);
   // row offsets of the output: rp[r] = o for the rows r in (row[o-1], row[o]];
   // the row before the tile is that of the larger of the two inputs' last
   // elements consumed by earlier tiles
@@ -603,8 +623,9 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(sizeof(DrawState), kAlign);
   w.scan = o;
   o += scan_temp_bytes<uint64_t>(nnz > 0 ? nnz : 1);
-  w.scan2 = o;
-  o += scan_temp_bytes<uint32_t>(w.d_max > 0 ? w.d_max : 1);
+  w.scan2 = o;  // the accept scan, then the column histogram's scan
+  const int64_t col_scan = ceil_div(nnz > 0 ? nnz : 1, kRadixTile) * kRadixBins;
+  o += scan_temp_bytes<uint32_t>(w.d_max > col_scan ? w.d_max : col_scan);
   w.surv_pos = o;
   o += align_up(8 * n, kAlign);
   w.surv_src = o;
@@ -661,13 +682,13 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // positions travel as keys (row << cbits) | col: same order as row * in_f + col
   const int cbits = bits_for((uint64_t)(a.in_f - 1));
   const uint64_t key_space = (uint64_t)a.out_f << cbits;
-  // the merge also makes the column view's first-level histogram (zeroed by
-  // the regrow branch's init kernel, so only when something is pruned)
+  // the column view's first-level histogram and offsets are made from the
+  // merge's split points on the second stream, beside the merge
   int cshift = 0;
-  uint32_t *chist = merge_makes_col_hist(a.out_f, a.in_f, nnz, n_prune, &cshift)
-                        ? reinterpret_cast<uint32_t *>(b + colview_hist_offset(a.out_f, a.in_f, nnz, n_prune))
-                        : nullptr;
-  const int64_t n_chist = chist ? ceil_div(nnz, kRadixTile) * kRadixBins : 0;
+  const bool col_offs = restructure_makes_col_offs(a.out_f, a.in_f, nnz, &cshift);
+  const int64_t cnb = ceil_div(nnz, kRadixTile);
+  uint32_t *coffs = reinterpret_cast<uint32_t *>(b + colview_offs_offset(a.out_f, a.in_f, nnz, n_prune));
+  uint32_t *chist = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(coffs) + colview_hist_bytes(nnz));
   cudaError_t e;
 #define SNACK_TRY(x)                       \
   do {                                     \
@@ -733,7 +754,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   };
   if (n_prune > 0) {
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, hkeys, hmin, (int64_t)W.cap, bcnt,
-               (int64_t)W.n_bkt, chist, n_chist);
+               (int64_t)W.n_bkt);
     e2 = cudaGetLastError();
     if (e2 == cudaSuccess) {
       m = chunk_size();
@@ -794,9 +815,22 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   if (nnz > 0) {
     launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
+    if (col_offs) {  // fork: the column histogram and its scan beside the merge
+      SNACK_TRY(cudaEventRecord(a.ev_fork, s));
+      SNACK_TRY(cudaStreamWaitEvent(s2, a.ev_fork, 0));
+      launch_pdl(k_col_hist, (unsigned)cnb, 256, 0, s2, (const uint64_t *)surv_pos, grown, (const int64_t *)part,
+                 W.n_merge_tiles, nnz, cbits, cshift, chist, cnb);
+      e = scan_apply<uint32_t>(HistRead{chist}, cnb * kRadixBins, WriteExcl32{coffs}, (uint32_t *)nullptr, stemp2, s2);
+      cudaError_t er = cudaEventRecord(a.ev_col, s2);  // build_plan waits for it before its scatter
+      if (e == cudaSuccess) e = er;
+      if (e != cudaSuccess) {
+        cudaStreamWaitEvent(s, a.ev_col, 0);
+        return SNACK_ERR_CUDA;
+      }
+    }
     launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, surv_pos, surv_src, n_surv, grown, n_prune,
                part, cbits, a.out_f, val, a.row_out, a.col_out, reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new,
-               a.col16_new, chist, ceil_div(nnz, kRadixTile), cshift);
+               a.col16_new);
   }
   SNACK_TRY(cudaGetLastError());
 #undef SNACK_TRY
@@ -1036,21 +1070,22 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
 
 }  // namespace
 
-bool merge_makes_col_hist(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune, int *shift) {
-  return n_prune > 0 && colview_digits(out_f, in_f, nnz, shift);
+bool restructure_makes_col_offs(int32_t out_f, int32_t in_f, int64_t nnz, int *shift) {
+  return colview_digits(out_f, in_f, nnz, shift);
 }
 
-// The merge's column histogram sits past both the restructure's own scratch
-// and the plan rebuild's, so the rebuild can read it while reusing the rest.
-size_t colview_hist_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+// The column offsets (and the histogram behind them) sit past both the
+// restructure's own scratch and the plan rebuild's, so the rebuild can read
+// them while reusing the rest.
+size_t colview_offs_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
   size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
   return align_up(r > p ? r : p, kAlign);
 }
 
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
-  return colview_hist_offset(out_f, in_f, nnz, n_prune) +
-         (colview_digits(out_f, in_f, nnz, nullptr) ? colview_hist_bytes(nnz) : 0);
+  return colview_offs_offset(out_f, in_f, nnz, n_prune) +
+         (colview_digits(out_f, in_f, nnz, nullptr) ? 2 * colview_hist_bytes(nnz) : 0);
 }
 
 snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) {

@@ -625,6 +625,8 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
     return SNACK_ERR_CUDA;
   if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
+  if (!h->ev_col && cudaEventCreateWithFlags(&h->ev_col, cudaEventDisableTiming) != cudaSuccess)
+    return SNACK_ERR_CUDA;
   if (!h->aux) {
     // The regrow branch (draws, acceptance, sort) is the longer of the two
     // that meet at the merge: its stream gets the highest priority, so its
@@ -639,15 +641,16 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.aux = h->aux;
   a.ev_fork = h->ev_fork;
   a.ev_join = h->ev_join;
+  a.ev_col = h->ev_col;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
   if (st != SNACK_OK) return st;
-  const uint32_t *col_hist =
-      merge_makes_col_hist(h->out_f, h->in_f, nnz, n_prune, nullptr)
+  const uint32_t *col_offs =
+      restructure_makes_col_offs(h->out_f, h->in_f, nnz, nullptr)
           ? reinterpret_cast<const uint32_t *>(reinterpret_cast<uint8_t *>(ws) +
-                                               colview_hist_offset(h->out_f, h->in_f, nnz, n_prune))
+                                               colview_offs_offset(h->out_f, h->in_f, nnz, n_prune))
           : nullptr;
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
-                        h->aux, h->ev_fork, h->ev_join, col_hist));
+                        h->aux, h->ev_fork, h->ev_join, col_offs, h->ev_col));
   return SNACK_OK;
 }
 
@@ -715,7 +718,7 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
 void snack_destroy(snack_handle h) {
   if (!h) return;
   dense_release(h);
-  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join) {
+  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join || h->ev_col) {
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
@@ -726,6 +729,7 @@ void snack_destroy(snack_handle h) {
     if (h->counts_ready) cudaEventDestroy(h->counts_ready);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->ev_col) cudaEventDestroy(h->ev_col);
     if (prev >= 0) cudaSetDevice(prev);
   }
   if (h->host_counts) cudaFreeHost(h->host_counts);
