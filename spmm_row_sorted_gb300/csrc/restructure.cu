@@ -322,8 +322,8 @@ struct CandPayload {
 // sort -- a slot in the position's bucket (equal-width buckets of the
 // position range, kBktCap slots each, filled in any order; a full bucket
 // raises `bovf` and the caller sorts the list the general way instead).
-constexpr int kBktTarget = 64;  // positions expected per bucket
-constexpr int kBktCap = 256;    // slots per bucket
+constexpr int kBktTarget = 32;  // positions expected per bucket
+constexpr int kBktCap = 128;    // slots per bucket
 
 struct AcceptOut {
   uint64_t *grown;
