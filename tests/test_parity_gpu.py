@@ -211,7 +211,7 @@ def restructure_and_check(lay: wl.Layer, n_prune: int, seed: int, step: int, act
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", [(8, 8, 20, 5), (1, 50, 10, 10), (40, 30, 600, 0), (40, 30, 600, 600),
                                   (64, 64, 3000, 1000), (500, 700, 30000, 3000), (3, 3, 4, 4),
-                                  (300, 700, 20000, 0), (300, 700, 20000, 1)])
+                                  (300, 700, 20000, 0), (300, 700, 20000, 1), (50, 1, 20, 5), (7, 3, 10, 5)])
 def test_restructure_small(dtype, case):
     out_f, in_f, nnz, n_prune = case
     lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=1.0, val_dtype=dtype, seed=nnz)
