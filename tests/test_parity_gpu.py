@@ -503,12 +503,14 @@ def test_dense_path_after_restructure():
 @pytest.mark.parametrize("shape", [(20, 70000, 3000), (70000, 20, 3000), (10, 140000, 2000), (65536, 65536, 4000)])
 def test_index_width_boundaries(shape):
     # feature counts above 65536 keep 32-bit indices; 65536 itself uses the 16-bit copies;
-    # 140000 inputs also take the general column sort
+    # 140000 inputs also take the general column sort.  Batch 9 runs the tile kernels,
+    # batch 1 the small-batch kernels.
     out_f, in_f, nnz = shape
     for dtype in ("f32", "bf16"):
         lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=0.5, val_dtype=dtype, seed=nnz, bias="normal")
-        acts = wl.make_acts(9, in_f, out_f, dtype, seed=1)
-        check_layer_ops(lay, acts)
+        for batch in (1, 9):
+            acts = wl.make_acts(batch, in_f, out_f, dtype, seed=1)
+            check_layer_ops(lay, acts)
     restructure_and_check(lay, nnz // 10, seed=1, step=1, acts=acts)
 
 
