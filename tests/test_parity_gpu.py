@@ -219,6 +219,44 @@ def test_restructure_small(dtype, case):
         restructure_and_check(lay, n_prune, seed, step, acts=wl.make_acts(4, in_f, out_f, dtype))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", [(500, 700, 30000, 3000, None), (64, 64, 3000, 1000, None), (7, 3, 10, 5, None),
+                                  (2000, 3000, 200000, 20000, 1.2), (70000, 20, 3000, 300, None),
+                                  (40, 30, 600, 0, None)])
+def test_restructure_chain_plan_equals_fresh(dtype, case):
+    # The restructure rebuilds the handle's plan in place (row offsets and the
+    # 16-bit columns from its merge, the column view's first-level offsets made
+    # beside the merge).  After three restructures in a row the COO still
+    # matches the oracle, and every op on the handle is bit-identical to the
+    # same op on a new handle made for the final pattern, at a small-batch and
+    # at a tile-path batch: same column view, storage indices and tiles.
+    out_f, in_f, nnz, n_prune, zipf = case
+    lay = wl.make_layer(out_f, in_f, nnz=nnz, zipf_s=zipf, val_std=0.5, val_dtype=dtype, seed=7, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    mb = 32
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=mb)
+    r, c, v = lay.row, lay.col, lay.val
+    for step in range(3):
+        src = L.restructure(n_prune, seed=2, step=step)
+        torch.cuda.synchronize()
+        r, c, so, _ = oracle.restructure(out_f, in_f, r, c, oracle.as_f64(v, dtype), n_prune, 2, step)
+        v = oracle.restructure_values(v, so)
+        assert np.array_equal(L.row.cpu().numpy(), r) and np.array_equal(L.col.cpu().numpy(), c), step
+        assert np.array_equal(src.cpu().numpy(), so.astype(np.int32)), step
+        assert np.array_equal(bits(L.val), v.view(np.uint32) if dtype == "f32" else v.view(np.uint16)), step
+    F = snack.SparseLinear(out_f, in_f, L.row.clone(), L.col.clone(), L.val.clone(), bias, max_batch=mb)
+    for batch in (4, mb):
+        acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+        x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
+        for M in (L, F):
+            M.out = (M.forward(x), M.grad_input(dy), *M.grad_weight(x, dy), *M.backward(x, dy))
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(L.out, F.out)):
+            assert torch.equal(a, b), (batch, i)
+    F.close()
+    L.close()
+
+
 def test_restructure_ties_zeros_nan():
     lay = wl.make_layer(60, 70, nnz=2000, val_dtype="f32", seed=4)
     v = np.round(lay.val * 50).astype(np.float32) / 50  # many exact ties
