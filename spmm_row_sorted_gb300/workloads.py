@@ -148,6 +148,19 @@ def fanin_positions(out_f: int, in_f: int, fan_in: int, seed: int) -> np.ndarray
     return np.concatenate(parts) if parts else np.zeros(0, dtype=np.int64)
 
 
+def diagonal_positions(out_f: int, in_f: int, n_diag: int, seed: int) -> np.ndarray:
+    """Sorted linear positions on n_diag wrapped diagonals: row r holds the
+    columns (r + o) mod in_f for n_diag distinct offsets o drawn uniformly from
+    [0, in_f) (a diagonal sparsity pattern; every row holds n_diag weights, and
+    every column too when out_f == in_f)."""
+    if n_diag > in_f:
+        raise ValueError("n_diag exceeds in_f")
+    offs = _rng(seed, _T_AUX).choice(in_f, size=n_diag, replace=False).astype(np.int64)
+    r = np.arange(out_f, dtype=np.int64)[:, None]
+    cols = np.sort((r + offs[None, :]) % in_f, axis=1)
+    return (r * in_f + cols).reshape(-1)
+
+
 @dataclasses.dataclass
 class Layer:
     """One sparse layer: W (out_f x in_f) as row-sorted COO plus a bias."""
@@ -191,11 +204,16 @@ def _store(a32: np.ndarray, dtype: str) -> np.ndarray:
 
 def make_layer(out_f: int, in_f: int, *, nnz: Optional[int] = None, density: Optional[float] = None,
                val_std: float = 0.02, val_dtype: str = "f32", seed: int = 0,
-               zipf_s: Optional[float] = None, bias: str = "zeros", fan_in: Optional[int] = None) -> Layer:
-    """Seeded layer with uniform, Zipf-row or constant fan-in positions and N(0, val_std) values."""
+               zipf_s: Optional[float] = None, bias: str = "zeros", fan_in: Optional[int] = None,
+               diagonals: Optional[int] = None) -> Layer:
+    """Seeded layer with uniform, Zipf-row, constant fan-in or wrapped-diagonal
+    positions and N(0, val_std) values."""
     if fan_in is not None:
         nnz = out_f * fan_in
         p = fanin_positions(out_f, in_f, fan_in, seed)
+    elif diagonals is not None:
+        nnz = out_f * diagonals
+        p = diagonal_positions(out_f, in_f, diagonals, seed)
     else:
         if nnz is None:
             if density is None:

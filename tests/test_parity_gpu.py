@@ -613,6 +613,22 @@ def test_restructure_rows_ties_nan_and_chain():
     L.close()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1024, 1024, 51), (768, 3072, 31), (3072, 768, 8), (300, 7000, 3)])
+def test_diagonal_patterns(dtype, shape):
+    # A diagonal sparsity pattern (wrapped diagonals, the same column offsets
+    # in every row) is an ordinary row-sorted COO pattern: every op matches the
+    # oracle at a small-batch and a tile-path batch, and both restructures
+    # (unstructured and per-row) stay bit-exact on it.
+    out_f, in_f, n_diag = shape
+    lay = wl.make_layer(out_f, in_f, diagonals=n_diag, val_std=0.5, val_dtype=dtype, seed=n_diag, bias="normal")
+    for batch in (4, 32):
+        check_layer_ops(lay, wl.make_acts(batch, in_f, out_f, dtype, seed=batch))
+    acts = wl.make_acts(8, in_f, out_f, dtype, seed=3)
+    restructure_and_check(lay, lay.nnz // 10, seed=4, step=1, acts=acts)
+    restructure_rows_and_check(lay, max(1, n_diag // 4), seed=4, step=1, acts=acts)
+
+
 def test_restructure_rows_workload_c4_fanin():
     # 16384 x 16384 with a constant fan-in of 164 (99 % sparse), 10 % of every row per call
     lay = wl.make_layer(16384, 16384, fan_in=164, val_std=0.02, val_dtype="f32", seed=0)

@@ -48,3 +48,16 @@ def test_small_zipf_layer_positions():
     pos = lay.row.astype(np.int64) * 48 + lay.col
     assert lay.nnz == 600 and np.all(np.diff(pos) > 0)
     assert lay.row.min() >= 0 and lay.row.max() < 64 and lay.col.max() < 48
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 5), (48, 200, 7), (300, 40, 40), (1, 9, 3)])
+def test_diagonal_layer_positions(shape):
+    out_f, in_f, n_diag = shape
+    lay = w.make_layer(out_f, in_f, diagonals=n_diag, seed=2)
+    pos = lay.row.astype(np.int64) * in_f + lay.col
+    assert lay.nnz == out_f * n_diag and np.all(np.diff(pos) > 0)
+    # every row holds the same set of offsets (col - row) mod in_f
+    offs = ((lay.col.astype(np.int64) - lay.row) % in_f).reshape(out_f, n_diag)
+    assert np.all(np.sort(offs, axis=1) == np.sort(offs[0]))
+    if out_f == in_f:
+        assert np.all(np.bincount(lay.col, minlength=in_f) == n_diag)
