@@ -56,6 +56,9 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
 bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
 size_t colview_hist_bytes(int64_t nnz);
 
+// dst[i] = (uint16_t)src[i] for i < n (the plan's 16-bit index copies); nothing when dst is null.
+cudaError_t pack16(const int32_t *src, int64_t n, uint16_t *dst, cudaStream_t s);
+
 // flags[0] |= 1 (index out of range), |= 2 (not strictly increasing).
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                              uint32_t *flag, cudaStream_t s);

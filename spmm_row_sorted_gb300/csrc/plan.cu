@@ -542,6 +542,11 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   return joined(cudaGetLastError());
 }
 
+cudaError_t pack16(const int32_t *src, int64_t n, uint16_t *dst, cudaStream_t s) {
+  if (n > 0 && dst) launch_pdl(k_pack16, grid_for(n, 256), 256, 0, s, src, n, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t validate_pattern(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                              uint32_t *flag, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);

@@ -709,7 +709,12 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
   SNACK_CUDA(cudaMemcpyAsync(h->host_counts, a.err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
   SNACK_CUDA(cudaEventRecord(h->counts_ready, s));
   SNACK_CUDA(cudaEventSynchronize(h->counts_ready));
-  if (h->host_counts[0]) return SNACK_ERR_NO_SPACE;
+  if (h->host_counts[0]) {
+    // the rows that finished wrote their new columns into the plan's 16-bit
+    // copy: put back the input's, so the plan still serves (row, col)
+    SNACK_CUDA(pack16(col, nnz, h->p.col16, s));
+    return SNACK_ERR_NO_SPACE;
+  }
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, b + kAlign, s,
                         kPlanRowTilesReady));
   return SNACK_OK;

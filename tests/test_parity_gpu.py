@@ -646,6 +646,14 @@ def test_restructure_rows_full_row_is_no_space_like_the_oracle():
     with pytest.raises(snack.SnackError) as e:
         L.restructure_rows(12, 7, 3)
     assert e.value.status == 8
+    # the other rows were restructured on the device before the error was
+    # seen; the handle still serves the input pattern
+    acts = wl.make_acts(4, 600, 400, "f32", seed=2)
+    x, dy = act_tensor(acts.x, "f32"), act_tensor(acts.dy, "f32")
+    got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+    got["dw"], got["db"] = L.grad_weight(x, dy)
+    torch.cuda.synchronize()
+    check_layer_ops(lay, acts, got=got)
     L.close()
 
 
