@@ -33,6 +33,13 @@
  * its draw count (see there).  A plan and a workspace may be used by one call
  * in flight at a time.
  *
+ * Host threads.  Issue the calls for one device from one host thread at a
+ * time (or under a lock).  The launchers raise a kernel's dynamic
+ * shared-memory limit to what the call needs.  Two threads that launch the
+ * same kernel for layers of different sizes at the same moment can lower
+ * that limit under each other.  One launch then fails with SNACK_ERR_CUDA;
+ * memory is never touched out of bounds.
+ *
  * Errors.  Every entry point returns a snack_status.  Arguments are checked
  * on the host before any launch; a failed launch or CUDA call returns
  * SNACK_ERR_CUDA.  The library never aborts, exits or traps on the device.
