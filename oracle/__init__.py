@@ -39,14 +39,18 @@ _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _f64p_opt = ctypes.c_void_p
 
 
+def compile_library(src: str, out: str) -> None:
+    """gcc with the oracle's portable flags (no -march): C source -> shared library."""
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", "-fno-fast-math", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle library with gcc (portable flags; no -march)."""
+    """Compile the oracle library (once, and again when the source changes)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
-               "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_library(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -56,40 +60,44 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
-        I64, U64, I32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
-        lib.oracle_set_threads.argtypes = [I32]
-        lib.oracle_get_threads.restype = I32
-        lib.oracle_check_coo.argtypes = [I64, I64, I64, _i32p, _i32p]
-        lib.oracle_check_coo.restype = I32
-        lib.oracle_fwd.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, _f64p, _f64p_opt, _f64p, _f64p_opt]
-        lib.oracle_fwd.restype = I32
-        lib.oracle_dx.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, _f64p, _f64p, _f64p_opt]
-        lib.oracle_dx.restype = I32
-        lib.oracle_dw.argtypes = [I64, I64, I64, _i32p, _i32p, I64, _f64p, _f64p, _f64p, _f64p_opt, _f64p_opt]
-        lib.oracle_dw.restype = I32
-        lib.oracle_gelu.argtypes = [ctypes.c_double]
-        lib.oracle_gelu.restype = ctypes.c_double
-        lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
-        lib.oracle_gelu_grad.restype = ctypes.c_double
-        lib.oracle_gelu_vec.argtypes = [I64, _f64p, _f64p]
-        lib.oracle_gelu_grad_vec.argtypes = [I64, _f64p, _f64p]
-        lib.oracle_splitmix64_mix.argtypes = [U64]
-        lib.oracle_splitmix64_mix.restype = U64
-        lib.oracle_regrow_base.argtypes = [U64, U64]
-        lib.oracle_regrow_base.restype = U64
-        lib.oracle_regrow_draw.argtypes = [U64, U64, U64, U64]
-        lib.oracle_regrow_draw.restype = U64
-        lib.oracle_restructure.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
-                                           _i32p, _i32p, _i64p]
-        lib.oracle_restructure.restype = I64
-        lib.oracle_row_base.argtypes = [U64, U64, U64]
-        lib.oracle_row_base.restype = U64
-        lib.oracle_restructure_rows.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
-                                                _i32p, _i32p, _i64p]
-        lib.oracle_restructure_rows.restype = I64
-        _lib = lib
-        return lib
+        _lib = bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def bind(lib):
+    """Declare the C signatures on a loaded oracle library; returns it."""
+    I64, U64, I32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
+    lib.oracle_set_threads.argtypes = [I32]
+    lib.oracle_get_threads.restype = I32
+    lib.oracle_check_coo.argtypes = [I64, I64, I64, _i32p, _i32p]
+    lib.oracle_check_coo.restype = I32
+    lib.oracle_fwd.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, _f64p, _f64p_opt, _f64p, _f64p_opt]
+    lib.oracle_fwd.restype = I32
+    lib.oracle_dx.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, _f64p, _f64p, _f64p_opt]
+    lib.oracle_dx.restype = I32
+    lib.oracle_dw.argtypes = [I64, I64, I64, _i32p, _i32p, I64, _f64p, _f64p, _f64p, _f64p_opt, _f64p_opt]
+    lib.oracle_dw.restype = I32
+    lib.oracle_gelu.argtypes = [ctypes.c_double]
+    lib.oracle_gelu.restype = ctypes.c_double
+    lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
+    lib.oracle_gelu_grad.restype = ctypes.c_double
+    lib.oracle_gelu_vec.argtypes = [I64, _f64p, _f64p]
+    lib.oracle_gelu_grad_vec.argtypes = [I64, _f64p, _f64p]
+    lib.oracle_splitmix64_mix.argtypes = [U64]
+    lib.oracle_splitmix64_mix.restype = U64
+    lib.oracle_regrow_base.argtypes = [U64, U64]
+    lib.oracle_regrow_base.restype = U64
+    lib.oracle_regrow_draw.argtypes = [U64, U64, U64, U64]
+    lib.oracle_regrow_draw.restype = U64
+    lib.oracle_restructure.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
+                                       _i32p, _i32p, _i64p]
+    lib.oracle_restructure.restype = I64
+    lib.oracle_row_base.argtypes = [U64, U64, U64]
+    lib.oracle_row_base.restype = U64
+    lib.oracle_restructure_rows.argtypes = [I64, I64, I64, _i32p, _i32p, _f64p, I64, U64, U64, I64,
+                                            _i32p, _i32p, _i64p]
+    lib.oracle_restructure_rows.restype = I64
+    return lib
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -187,6 +195,11 @@ def gelu_grad(x: np.ndarray) -> np.ndarray:
 
 def splitmix64_mix(z: int) -> int:
     return int(_load().oracle_splitmix64_mix(int(z) & (2**64 - 1)))
+
+
+def regrow_base(seed: int, step: int) -> int:
+    """State before the first draw of (seed, step)."""
+    return int(_load().oracle_regrow_base(seed, step))
 
 
 def regrow_draw(seed: int, step: int, i: int, n_pos: int) -> int:

@@ -222,6 +222,20 @@ def test_splitmix64_known_answers():
         assert oracle.splitmix64_mix((n * gamma) % 2**64) == want
 
 
+def test_draw_stream_is_splitmix64_from_state_zero():
+    # Seed 0 at step 0 gives the base state mix(0 ^ mix(0)) = 0 (the finaliser
+    # maps 0 to 0), so draw i must be output i + 1 of SplitMix64 started from
+    # state 0 -- the published known answers -- and with n_pos = 2^63 the
+    # multiply-high reduction keeps its top 63 bits.  This pins the stream's
+    # increment, its one-step offset and its base state.
+    with open(os.path.join(GOLDEN, "splitmix64_kat.txt")) as f:
+        kat = [int(line, 16) for line in f if line.strip() and not line.startswith("#")]
+    assert oracle.regrow_base(0, 0) == 0
+    for i, want in enumerate(kat):
+        assert oracle.regrow_draw(0, 0, i, 2**63) == want >> 1
+        assert oracle.regrow_draw(0, 0, i, 2**64 - 1) == (want * (2**64 - 1)) >> 64
+
+
 def test_multiply_high_reduction():
     # floor(u * 2^k / 2^64) is u >> (64-k); so draws for n_pos = 2^k are the top
     # bits of draws for n_pos = 2^63, shifted.
