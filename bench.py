@@ -154,6 +154,80 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class NvmlClockSampler:
+    """Polls NVML (libnvidia-ml through ctypes, read-only queries) every
+    `period_s` from a background thread during the timed region: the SM
+    clock, its maximum and the active clock-event reasons.  A region of a
+    few milliseconds still gets samples, which nvidia-smi's 100 ms loop
+    cannot give.  Falls back to no samples when NVML is missing."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device_index: int, period_s: float = 0.0005):
+        import ctypes
+
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.handle = None
+        self._stop = threading.Event()
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            import torch
+
+            pr = torch.cuda.get_device_properties(torch_device_index)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+            h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                raise OSError("handle")
+            self.handle = h
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            self.handle = None
+
+    def _run(self):
+        import ctypes
+
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                r = rs.value if self._reasons(self.handle, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(mhz.value), int(r)))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.handle is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.handle is not None:
+            self._stop.set()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(m for m, _ in self.samples), "reasons": reasons, "samples": len(self.samples),
+                "source": f"nvml, every {self.period * 1e3:.1f} ms during the timed region"}
+
+
+def clock_sampler(index: int):
+    """NVML sampler when NVML loads, else the nvidia-smi one."""
+    s = NvmlClockSampler(index)
+    return s if s.handle is not None else ClockSampler(index)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -358,7 +432,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -878,6 +952,93 @@ def restructure_launches() -> int:
     return draw_chunk + sort_grown + select + keep_scan + merge + col_offsets + plan
 
 
+# ----------------------------------------------------------------------------
+# Gather ceiling (--gather-ceiling): how fast can the SM bring one 128-byte
+# batch vector per stored weight to the FMA units, by each route, on the
+# 16384^2 Zipf layer at batch 32 fp32?  Probes in probe/gather_probe.cu.
+# ----------------------------------------------------------------------------
+
+PROBE_KINDS = {0: "LDG.128 gather through L1", 1: "TMA tile::gather4 into a shared-memory ring",
+               2: "1-D bulk copy per weight into a shared-memory ring", 3: "random 4-byte loads val[perm[k]]",
+               4: "random 4-byte stores dst[perm[k]]", 5: "sequential read of col + val"}
+
+
+def run_gather_ceiling(args):
+    import ctypes
+
+    import torch
+
+    from spmm_row_sorted_gb300 import build as snack_build
+
+    lib = ctypes.CDLL(snack_build.build_probe())
+    lib.probe_gather.restype = ctypes.c_int
+    lib.probe_gather.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                 ctypes.c_int, ctypes.c_void_p]
+    lib.probe_out_elems.restype = ctypes.c_int64
+    lib.probe_out_elems.argtypes = [ctypes.c_int, ctypes.c_int]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lay, acts = make_workload(0)
+    nnz = lay.nnz
+    perm = np.lexsort((lay.row, lay.col)).astype(np.int32)  # storage index of each entry in column order
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    xt = torch.from_numpy(np.ascontiguousarray(acts.x.T)).to(dev).contiguous()  # [16384][32] feature-major
+    col = torch.from_numpy(lay.col).to(dev)
+    val = torch.from_numpy(lay.val).to(dev)
+    pm = torch.from_numpy(perm).to(dev)
+    dst = torch.empty(nnz, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(int(lib.probe_out_elems(1, 64 * sms)), device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    flush_out = torch.empty((), device=dev)
+    records = []
+    sweeps = {0: (2, 4, 8, 16), 1: (1, 2, 4, 6), 2: (1, 2, 4, 6), 3: (4, 8, 16), 4: (4, 8, 16), 5: (4, 8, 16)}
+    for kind, mults in sweeps.items():
+        best = None
+        for m in mults:
+            grid = m * sms
+
+            def launch():
+                rc = lib.probe_gather(kind, xt.data_ptr(), IN_F, col.data_ptr(), val.data_ptr(), pm.data_ptr(), nnz,
+                                      out.data_ptr(), dst.data_ptr(), err.data_ptr(), grid, stream.cuda_stream)
+                if rc != 0:
+                    raise RuntimeError(f"probe {kind} failed: {rc}")
+
+            ts = []
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    launch()
+                for _ in range(args.reps):
+                    torch.sum(flush, dim=0, out=flush_out)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    launch()
+                    e1.record(stream)
+                    ts.append((e0, e1))
+            stream.synchronize()
+            us = statistics.median(a.elapsed_time(b) for a, b in ts) * 1e3
+            if best is None or us < best[1]:
+                best = (grid, us)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"probe {kind} reported a wait that ran out: {int(err.item())}")
+        grid, us = best
+        rec = {"kind": kind, "route": PROBE_KINDS[kind], "grid": grid, "us": us, "weights_per_us": nnz / us}
+        if kind <= 2:
+            rec["gathered_GBs"] = nnz * 128 / (us * 1e-6) / 1e9
+        elif kind <= 4:
+            rec["sectors_per_us"] = nnz / us
+        else:
+            rec["GBs"] = nnz * 8 / (us * 1e-6) / 1e9
+        records.append(rec)
+        print(json.dumps(rec), flush=True)
+    byts = alg_bytes(nnz, BATCH, OUT_F, IN_F)
+    print(json.dumps({"what": "gather ceiling, 16384^2 Zipf layer, batch 32 fp32, cold L2 (2x L2 read between reps)",
+                      "nnz": nnz, "fwd_alg_bytes": byts["fwd"], "records": records}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -892,6 +1053,8 @@ def main(argv=None):
                     help="per-workload sweep instead of the step bench: 'all' or a list like c1,c4")
     ap.add_argument("--configs-out", default=None, help="--configs: also write a markdown table here")
     ap.add_argument("--reps", type=int, default=200, help="--configs: timed reps per op")
+    ap.add_argument("--gather-ceiling", action="store_true",
+                    help="time the gather-route probes on the 16384^2 layer at batch 32 and exit")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps untimed on one layer copy and exit (for ncu captures)")
     args = ap.parse_args(argv)
@@ -899,6 +1062,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.gather_ceiling:
+        return run_gather_ceiling(args)
     if args.configs:
         return run_configs(args)
     return run_ours(args)

@@ -110,5 +110,35 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     return lib_path
 
 
+PROBE_SRC = os.path.join(HERE, "probe", "gather_probe.cu")
+
+
+def build_probe(force: bool = False) -> str:
+    """Compile the gather-throughput probes (bench.py --gather-ceiling) into
+    _build/libsnack_probe.so; not part of libsnack."""
+    os.makedirs(BUILD, exist_ok=True)
+    lib_path = os.path.join(BUILD, "libsnack_probe.so")
+    stamp_path = os.path.join(BUILD, "libsnack_probe.stamp")
+    h = hashlib.sha256()
+    with open(PROBE_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(platform.machine().encode())
+    digest = h.hexdigest()
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_path):
+        with open(stamp_path) as f:
+            if f.read().strip() == digest:
+                return lib_path
+    tmp = lib_path + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, "-shared", "-cudart", "shared", "-o", tmp, PROBE_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on the probe:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib_path)
+    with open(stamp_path, "w") as f:
+        f.write(digest)
+    return lib_path
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

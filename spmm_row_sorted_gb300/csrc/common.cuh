@@ -45,6 +45,20 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// ------------------------------------------------ shared-memory limits
+//
+// A kernel's dynamic shared-memory limit (cudaFuncAttributeMaxDynamicSharedMemorySize)
+// is process-wide per device.  Every launcher raises it through this one
+// call: a table keyed by (device, kernel), under a lock, records the largest
+// limit granted so far and the attribute is only ever raised, so host threads
+// launching the same kernel for layers of different sizes, or one launcher
+// that also sizes another kernel, never lower a limit another launch needs.
+cudaError_t raise_smem_limit(const void *kernel, size_t bytes);
+template <typename... KArgs>
+inline cudaError_t raise_smem_limit(void (*kernel)(KArgs...), size_t bytes) {
+  return raise_smem_limit(reinterpret_cast<const void *>(kernel), bytes);
+}
+
 // ---------------------------------------------------------------- loads
 
 // Streamed once: evict-first in L1 and L2.

@@ -86,12 +86,14 @@ __global__ void __launch_bounds__(256) k_gather_dw(const int32_t *__restrict__ r
   }
 }
 
-// y[b][r] += bias[r]
-__global__ void k_add_bias(bf16 *__restrict__ y, const float *__restrict__ bias, int batch, int n) {
+// y[b][r] = bf16(acc[b][r] + bias[r]): the fp32 product and the bias are
+// added before the one rounding to bf16
+__global__ void k_bias_round(const float *__restrict__ acc, const float *__restrict__ bias, int batch, int n,
+                             bf16 *__restrict__ y) {
   pdl_wait();
   const int64_t total = (int64_t)batch * n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = __float2bfloat16(__bfloat162float(y[i]) + bias[i % n]);
+    y[i] = __float2bfloat16_rn(bias[i % n] + acc[i]);
 }
 
 // db[r] = sum_b dy[b][r], b increasing
@@ -110,13 +112,15 @@ struct DenseWs {
   size_t wd, g, lt, total;
 };
 
-DenseWs dense_ws(int32_t out_f, int32_t in_f) {
+// wd: the dense bf16 W; g: the dense fp32 weight gradient, or the forward's
+// fp32 sums [batch][out_f] before the bias (so at least max_batch columns)
+DenseWs dense_ws(int32_t out_f, int32_t in_f, int32_t max_batch) {
   DenseWs w;
   size_t o = 0;
   w.wd = o;
   o += align_up((size_t)out_f * in_f * sizeof(bf16), kAlign);
   w.g = o;
-  o += align_up((size_t)out_f * in_f * sizeof(float), kAlign);
+  o += align_up((size_t)out_f * (in_f > max_batch ? in_f : max_batch) * sizeof(float), kAlign);
   w.lt = o;
   o += kLtWorkspace;
   w.total = o;
@@ -188,7 +192,7 @@ bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, sn
          (int64_t)out_f * in_f <= ((int64_t)1 << 31);
 }
 
-size_t dense_ws_bytes(int32_t out_f, int32_t in_f) { return dense_ws(out_f, in_f).total; }
+size_t dense_ws_bytes(int32_t out_f, int32_t in_f, int32_t max_batch) { return dense_ws(out_f, in_f, max_batch).total; }
 
 bool dense_init(snack_layer *h) {
   cublasLtHandle_t lt = nullptr;
@@ -204,18 +208,24 @@ void dense_release(snack_layer *h) {
 
 snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, const void *x, int32_t batch,
                        const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s) {
-  const DenseWs W = dense_ws(h->out_f, h->in_f);
+  const DenseWs W = dense_ws(h->out_f, h->in_f, h->max_batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   bf16 *wd = reinterpret_cast<bf16 *>(b + W.wd);
   densify(h, col, val, wd, s);
   if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
-  // column-major: Y'(out x B) = Wd'(in x out)^T X'(in x B)
+  // column-major: Y'(out x B) = Wd'(in x out)^T X'(in x B).  Without a bias
+  // the GEMM rounds its fp32 sums to bf16 once; with one, it writes the fp32
+  // sums (into the fp32 gradient buffer, unused by the forward) and the bias
+  // is added before the single rounding.
+  float *acc = reinterpret_cast<float *>(b + W.g);
   if (lt_gemm(reinterpret_cast<cublasLtHandle_t>(h->lt), CUBLAS_OP_T, CUBLAS_OP_N, h->out_f, batch, h->in_f, wd,
-              h->in_f, x, h->in_f, y, h->out_f, CUDA_R_16BF, b + W.lt, s) != cudaSuccess)
+              h->in_f, x, h->in_f, bias ? (void *)acc : y, h->out_f, bias ? CUDA_R_32F : CUDA_R_16BF, b + W.lt,
+              s) != cudaSuccess)
     return SNACK_ERR_CUDA;
   if (bias) {
-    k_add_bias<<<grid_of((int64_t)batch * h->out_f, 256), 256, 0, s>>>(reinterpret_cast<bf16 *>(y), bias, batch, h->out_f);
+    k_bias_round<<<grid_of((int64_t)batch * h->out_f, 256), 256, 0, s>>>(acc, bias, batch, h->out_f,
+                                                                         reinterpret_cast<bf16 *>(y));
     if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   }
   return SNACK_OK;
@@ -223,7 +233,7 @@ snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, cons
 
 snack_status dense_dx(snack_layer *h, const int32_t *col, const void *val, const void *dy, int32_t batch, void *dx,
                       void *ws, size_t ws_bytes, cudaStream_t s) {
-  const DenseWs W = dense_ws(h->out_f, h->in_f);
+  const DenseWs W = dense_ws(h->out_f, h->in_f, h->max_batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   bf16 *wd = reinterpret_cast<bf16 *>(b + W.wd);
@@ -238,7 +248,7 @@ snack_status dense_dx(snack_layer *h, const int32_t *col, const void *val, const
 
 snack_status dense_dw(snack_layer *h, const int32_t *col, const void *x, const void *dy, int32_t batch, float *dw,
                       float *db, void *ws, size_t ws_bytes, cudaStream_t s) {
-  const DenseWs W = dense_ws(h->out_f, h->in_f);
+  const DenseWs W = dense_ws(h->out_f, h->in_f, h->max_batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   float *g = reinterpret_cast<float *>(b + W.g);

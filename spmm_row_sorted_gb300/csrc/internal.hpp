@@ -99,7 +99,7 @@ snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes
 // workspace holds the dense copy (snack_query_sizes reserves it).
 constexpr int kDenseMinBatch = 32;
 bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t);
-size_t dense_ws_bytes(int32_t out_f, int32_t in_f);
+size_t dense_ws_bytes(int32_t out_f, int32_t in_f, int32_t max_batch);
 
 // Per-row (constant fan-in) restructure (restructure.cu): rows keep their
 // counts and offsets; the plan's row offsets and forward tiles stay valid.

@@ -388,7 +388,7 @@ cudaError_t radix_pass(Src src, Dst dst, int64_t n, int shift, uint32_t *hist, u
                                        stemp, stream);
   if (e != cudaSuccess) return e;
   const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
-  e = cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  e = raise_smem_limit(k_radix_scatter<K, Src, Dst>, dyn);
   if (e != cudaSuccess) return e;
   launch_pdl(k_radix_scatter<K, Src, Dst>, (unsigned)nb, kRadixThreads, dyn, stream, src, dst, n, shift, offs, nb);
   return cudaGetLastError();
@@ -400,8 +400,7 @@ template <typename K, typename Src, typename Dst>
 cudaError_t radix_scatter_only(Src src, Dst dst, int64_t n, int shift, const uint32_t *offs, cudaStream_t stream) {
   const int64_t nb = ceil_div(n, kRadixTile);
   const size_t dyn = (size_t)kRadixTile * (sizeof(K) + sizeof(uint32_t));
-  cudaError_t e =
-      cudaFuncSetAttribute(k_radix_scatter<K, Src, Dst>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  cudaError_t e = raise_smem_limit(k_radix_scatter<K, Src, Dst>, dyn);
   if (e != cudaSuccess) return e;
   launch_pdl(k_radix_scatter<K, Src, Dst>, (unsigned)nb, kRadixThreads, dyn, stream, src, dst, n, shift, offs, nb);
   return cudaGetLastError();

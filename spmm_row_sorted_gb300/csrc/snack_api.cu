@@ -4,11 +4,33 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 
 #include "internal.hpp"
 
 using namespace snack;
+
+namespace snack {
+
+cudaError_t raise_smem_limit(const void *kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;  // within the default limit of every kernel
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, size_t> granted;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t &g = granted[std::make_pair(dev, kernel)];
+  if (g >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) g = bytes;
+  return e;
+}
+
+}  // namespace snack
 
 namespace {
 
@@ -370,7 +392,7 @@ bool readback_ready(snack_handle h) {
 
 // Dense path: a dense layer, a wide batch, and room for the dense copy.
 bool use_dense(snack_handle h, int32_t batch, size_t ws_bytes) {
-  return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f);
+  return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f, h->max_batch);
 }
 
 snack_status common_call_checks(snack_handle h, int32_t batch, void *ws) {
@@ -394,7 +416,7 @@ snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t
   if (workspace_bytes) {
     size_t a = ops_ws_bytes(out_f, in_f, max_batch, act_t, lay);
     size_t b = plan_build_ws_bytes(out_f, in_f, nnz);
-    size_t c = dense_layer(out_f, in_f, nnz, max_batch, val_t) ? dense_ws_bytes(out_f, in_f) : 0;
+    size_t c = dense_layer(out_f, in_f, nnz, max_batch, val_t) ? dense_ws_bytes(out_f, in_f, max_batch) : 0;
     a = a > b ? a : b;
     *workspace_bytes = a > c ? a : c;
   }

@@ -23,10 +23,13 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // The array's name is only a host-side stand-in in host code; its device
-// address is looked up once per device, with that device current.
-std::once_flag g_once[kMaxDevices];
+// address is looked up per device, with that device current, and kept once
+// a lookup succeeds.  A failed lookup (a leftover error from earlier work, or
+// a first call made during stream capture) is not remembered: the next call
+// on that device tries again.
+std::mutex g_mu[kMaxDevices];
 void *g_scratch[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+bool g_have[kMaxDevices];
 
 struct CurrentDevice {
   int prev = -1;
@@ -49,16 +52,24 @@ extern "C" snack_status snack_spmm_fwd_noalloc(snack_handle h, const int32_t *ro
   if (!h) return SNACK_ERR_INVALID_ARG;
   const int dev = h->device;
   if (dev < 0 || dev >= kMaxDevices) return SNACK_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
   {
-    CurrentDevice cur(dev);
-    if (!cur.ok) return SNACK_ERR_CUDA;
-    std::call_once(g_once[dev], [dev] {
-      g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch[dev], g_noalloc_scratch);
-    });
+    std::lock_guard<std::mutex> lock(g_mu[dev]);
+    if (!g_have[dev]) {
+      CurrentDevice cur(dev);
+      if (!cur.ok) return SNACK_ERR_CUDA;
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();  // do not leave the failed lookup's error for the next CUDA call
+        return SNACK_ERR_CUDA;
+      }
+      g_scratch[dev] = ptr;
+      g_have[dev] = true;
+    }
+    scratch = g_scratch[dev];
   }
-  if (g_scratch_err[dev] != cudaSuccess || !g_scratch[dev]) return SNACK_ERR_CUDA;
   // snack_spmm_fwd checks the scratch size this call needs against the
   // array's size and returns SNACK_ERR_WORKSPACE, before any launch, when it
   // does not fit.
-  return snack_spmm_fwd(h, row, col, val, x, batch, bias, y, g_scratch[dev], kNoAllocScratchBytes, stream);
+  return snack_spmm_fwd(h, row, col, val, x, batch, bias, y, scratch, kNoAllocScratchBytes, stream);
 }

@@ -646,10 +646,8 @@ template <typename TA, typename TV, int V, int G, bool kGV, bool kFuse>
 cudaError_t launch_spmm_v(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s) {
   size_t smem = spmm_smem_bytes(p.tg, bg.bt) + (kFuse ? (size_t)tile_stage_len(p.tg) * 4 : 0);
   auto kern = k_spmm_tiles<TA, TV, V, G, kGV, kFuse>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = raise_smem_limit(kern, smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.tg.n_tiles, bg.n_btiles);
   launch_pdl(kern, grid, kSpmmThreads, smem, s, p, bg);
   int fx = bg.bt < 32 ? 32 : (bg.bt > 256 ? 256 : bg.bt);

@@ -381,11 +381,11 @@ int small_rows_per_cta(K kern, size_t smem, int n_rows, int num_sms) {
   return (int)R;
 }
 
-// Host-side state a launch would otherwise query every call: the largest
-// dynamic shared memory granted to the kernel so far, and the rows per CTA
-// last derived for a (device, shared memory, rows) triple.  Per host thread.
+// Host-side state a launch would otherwise query every call: the rows per
+// CTA last derived for a (device, shared memory, rows) triple.  Per host
+// thread.  Shared-memory limits live in the process-wide table of
+// raise_smem_limit, which only ever raises them.
 struct SmallLaunchCache {
-  size_t granted = 0;
   int dev = -1, n_rows = -1, num_sms = -1, R = 0;
   size_t smem = 0;
 };
@@ -397,16 +397,16 @@ cudaError_t launch_small_s(const SpmmParams &p, int num_sms, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (cache.dev != dev) cache = SmallLaunchCache{0, dev};
+  if (cache.dev != dev) {
+    cache = SmallLaunchCache{};
+    cache.dev = dev;
+  }
   const size_t smem_max = small_smem_bytes(p.n_src, kB, sizeof(TA), 64, kStage);
   auto fused = k_spmm_small<TA, TV, kB, kStage, true, true>;  // sizes the column-view calls' CTAs
-  if (smem_max > 48 * 1024 && smem_max > cache.granted) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
-    if (e == cudaSuccess && kGV)  // the occupancy query below must see the same limit
-      e = cudaFuncSetAttribute(fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
-    if (e != cudaSuccess) return e;
-    cache.granted = smem_max;
-  }
+  e = raise_smem_limit(kern, smem_max);
+  if (e == cudaSuccess && kGV)  // the occupancy query below must see a limit that fits smem_max
+    e = raise_smem_limit(fused, smem_max);
+  if (e != cudaSuccess) return e;
   // the column-view calls size their CTAs by the fused kernel, so dX comes
   // out of the same row partition (and summation order) with or without dW
   if (cache.smem != smem_max || cache.n_rows != p.n_rows || cache.num_sms != num_sms) {

@@ -211,6 +211,50 @@ def test_gelu_pins():
     np.testing.assert_allclose(oracle.gelu_grad(xs), tx.grad.numpy(), rtol=1e-13, atol=1e-14)
 
 
+def test_mlp_step_against_dense_autograd():
+    # The sparse MLP step (two sparse layers with GELU between them) against a
+    # dense two-layer network in fp64 with the same weights at the stored
+    # positions and zeros elsewhere, differentiated by torch autograd for the
+    # loss L = sum(dY2 * Y2): every forward value and every gradient the step
+    # returns (dW at the stored positions only).
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(17)
+    batch, d0, d1, d2 = 5, 9, 14, 7
+    layers = []
+    for o, i, nnz in ((d1, d0, 60), (d2, d1, 50)):
+        p = np.sort(rng.choice(o * i, nnz, replace=False))
+        layers.append((o, i, (p // i).astype(np.int32), (p % i).astype(np.int32), rng.standard_normal(nnz),
+                       rng.standard_normal(o)))
+    x = rng.standard_normal((batch, d0))
+    dy2 = rng.standard_normal((batch, d2))
+    got = oracle.mlp_step(layers[0], layers[1], x, dy2)
+
+    def dense(lay):
+        o, i, r, c, v, b = lay
+        w = np.zeros((o, i))
+        w[r, c] = v
+        return torch.tensor(w, requires_grad=True), torch.tensor(b, requires_grad=True)
+
+    (w1, b1), (w2, b2) = dense(layers[0]), dense(layers[1])
+    xt = torch.tensor(x, requires_grad=True)
+    y1 = xt @ w1.T + b1
+    y1.retain_grad()
+    h = torch.nn.functional.gelu(y1, approximate="none")
+    h.retain_grad()
+    y2 = h @ w2.T + b2
+    (torch.tensor(dy2) * y2).sum().backward()
+    tol = dict(rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got["y1"], y1.detach().numpy(), **tol)
+    np.testing.assert_allclose(got["h"], h.detach().numpy(), **tol)
+    np.testing.assert_allclose(got["y2"], y2.detach().numpy(), **tol)
+    np.testing.assert_allclose(got["dh"], h.grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dy1"], y1.grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dx"], xt.grad.numpy(), **tol)
+    for name, (o, i, r, c, v, b), w, bb in (("1", layers[0], w1, b1), ("2", layers[1], w2, b2)):
+        np.testing.assert_allclose(got["dw" + name], w.grad.numpy()[r, c], **tol)
+        np.testing.assert_allclose(got["db" + name], bb.grad.numpy(), **tol)
+
+
 # ---------------------------------------------------------------- restructure
 
 

@@ -1,12 +1,15 @@
 """The allocation-free forward entry point, snack_spmm_fwd_noalloc.
 
-Callers that may not allocate device memory on their call path (an engine
-plugin's enqueue step, a real-time loop with a fixed memory budget) cannot
-pass the workspace snack_spmm_fwd needs; this entry point uses a scratch array
-built into the library instead.  The test calls it through the C ABI twice in
-a row and checks both results against the workspace entry point, within the
-same T-scaled bound as the other parity tests, and checks that a call needing
-more than the built-in scratch is rejected.
+Some callers cannot allocate device memory where they call the forward pass:
+a plugin run from an inference engine's enqueue step, or a real-time loop
+whose memory is fixed at start-up.  They cannot pass the workspace that
+snack_spmm_fwd takes, so this entry point uses a scratch array built into the
+library instead.  The tests call it through the C ABI twice in a row and check
+that both results are bit-identical to the workspace entry point's (the same
+kernels run on the same inputs) and within the parity bound of the oracle;
+that a moderately sparse bf16 layer, which takes the tensor-core path, also
+matches the oracle; and that a call needing more than the built-in scratch is
+rejected before anything is launched.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -23,7 +26,7 @@ from spmm_row_sorted_gb300 import build as snack_build
 from spmm_row_sorted_gb300 import snack
 from spmm_row_sorted_gb300 import workloads as wl
 
-from gpu_util import REL, act_tensor, assert_close_T, f64, layer_tensors
+from gpu_util import ACC_REL, act_tensor, assert_close_T, f64, layer_tensors
 
 pytestmark = pytest.mark.gpu
 
@@ -34,30 +37,42 @@ def lib():
     return snack.load()
 
 
-@pytest.mark.parametrize("dtype,batch", [("f32", 32), ("bf16", 16)])
-def test_noalloc_matches_workspace_entry_point(lib, dtype, batch):
-    lay = wl.make_layer(700, 900, nnz=40000, zipf_s=1.1, val_std=0.3, val_dtype=dtype, seed=5, bias="normal")
-    acts = wl.make_acts(batch, 900, 700, dtype, seed=5)
+def call_noalloc(lib, L, row, col, val, x, batch, bias, y):
+    stream = torch.cuda.current_stream()
+    return lib.snack_spmm_fwd_noalloc(ctypes.c_void_p(L.handle), ctypes.c_void_p(row.data_ptr()),
+                                      ctypes.c_void_p(col.data_ptr()), ctypes.c_void_p(val.data_ptr()),
+                                      ctypes.c_void_p(x.data_ptr()), batch, ctypes.c_void_p(bias.data_ptr()),
+                                      ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+
+
+@pytest.mark.parametrize("dtype,batch,density", [("f32", 32, None), ("bf16", 16, None), ("bf16", 64, 0.5)])
+def test_noalloc_matches_workspace_entry_point(lib, dtype, batch, density):
+    out_f, in_f = 700, 900
+    if density is None:
+        lay = wl.make_layer(out_f, in_f, nnz=40000, zipf_s=1.1, val_std=0.3, val_dtype=dtype, seed=5, bias="normal")
+    else:  # half of W stored, bf16, batch >= 32: the moderately sparse (tensor-core) path
+        lay = wl.make_layer(out_f, in_f, density=density, val_std=0.1, val_dtype=dtype, seed=5, bias="normal")
+    acts = wl.make_acts(batch, in_f, out_f, dtype, seed=5)
     row, col, val, bias = layer_tensors(lay)
-    L = snack.SparseLinear(700, 900, row, col, val, bias, max_batch=batch)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=batch)
     x = act_tensor(acts.x, dtype)
     y_ws = L.forward(x)
-    stream = torch.cuda.current_stream()
     outs = []
     for _ in range(2):  # two calls in a row share the built-in scratch
         y = torch.full_like(y_ws, float("nan"))
-        st = lib.snack_spmm_fwd_noalloc(ctypes.c_void_p(L.handle), ctypes.c_void_p(row.data_ptr()),
-                                        ctypes.c_void_p(col.data_ptr()), ctypes.c_void_p(val.data_ptr()),
-                                        ctypes.c_void_p(x.data_ptr()), batch, ctypes.c_void_p(bias.data_ptr()),
-                                        ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+        st = call_noalloc(lib, L, row, col, val, x, batch, bias, y)
         assert st == 0, snack.snack_status_string(st)
         outs.append(y)
     torch.cuda.synchronize()
-    _, t = oracle.fwd(700, 900, lay.row, lay.col, oracle.as_f64(lay.val, dtype), oracle.as_f64(acts.x, dtype),
-                      oracle.as_f64(lay.bias))
-    ref = f64(y_ws)
+    ref, t = oracle.fwd(out_f, in_f, lay.row, lay.col, oracle.as_f64(lay.val, dtype), oracle.as_f64(acts.x, dtype),
+                        oracle.as_f64(lay.bias))
+    assert_close_T(f64(y_ws), ref, t, ACC_REL, "workspace fwd", stored_bf16=dtype == "bf16")
     for y in outs:
-        assert_close_T(f64(y), ref, t, REL[dtype], "noalloc vs workspace fwd", stored_bf16=dtype == "bf16")
+        # the two calls run the same kernels on the same inputs
+        assert torch.equal(y, outs[0]), "two noalloc calls in a row differ"
+        if density is None:  # the workspace call runs the same kernels too
+            assert torch.equal(y, y_ws), "noalloc differs from the workspace entry point"
+        assert_close_T(f64(y), ref, t, ACC_REL, "noalloc fwd", stored_bf16=dtype == "bf16")
     L.close()
 
 
