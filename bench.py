@@ -54,7 +54,7 @@ def alg_bytes(nnz: int, batch: int, out_f: int, in_f: int, s_v: int = 4, s_x: in
     dx = nnz * (8 + s_v) + batch * out_f * s_x + batch * in_f * s_x
     dw = nnz * (8 + 4) + batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
     bwd = nnz * (8 + s_v + 4) + 2 * batch * in_f * s_x + batch * out_f * s_x + 4 * out_f
-    restructure = 2 * nnz * (8 + s_v) + 4 * nnz  # read old COO, write new COO + source map
+    restructure = 2 * nnz * (8 + s_v)  # read the old COO, write the new one (the 4 B/weight source map not counted)
     return {"fwd": fwd, "dx": dx, "dw": dw, "bwd": bwd, "restructure": restructure}
 
 
@@ -154,72 +154,98 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+NVML_POLL = r"""
+import ctypes, sys, time
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+if nv.nvmlInit_v2() != 0:
+    sys.exit(1)
+h = ctypes.c_void_p()
+if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(sys.argv[1].encode()), ctypes.byref(h)) != 0:
+    sys.exit(1)
+mx = ctypes.c_uint()
+nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+period = float(sys.argv[2])
+mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+print("max", mx.value, flush=True)
+while True:
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+        r = rs.value if reasons(h, ctypes.byref(rs)) == 0 else 0
+        print(time.monotonic(), mhz.value, r, flush=True)
+    time.sleep(period)
+"""
+
+
 class NvmlClockSampler:
     """Polls NVML (libnvidia-ml through ctypes, read-only queries) every
-    `period_s` from a background thread during the timed region: the SM
-    clock, its maximum and the active clock-event reasons.  A region of a
-    few milliseconds still gets samples, which nvidia-smi's 100 ms loop
-    cannot give.  Falls back to no samples when NVML is missing."""
+    `period_s` from a separate process: the SM clock, its maximum and the
+    active clock-event reasons.  The samples whose time falls inside the timed
+    region are kept, so a region of a few milliseconds still gets samples
+    (nvidia-smi's loop gives one per 100 ms); polling from another process
+    leaves the launching thread alone.  No samples when NVML is missing."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, torch_device_index: int, period_s: float = 0.0005):
-        import ctypes
-
         self.period = period_s
-        self.samples = []
+        self.rows = []
         self.max_mhz = None
-        self.handle = None
-        self._stop = threading.Event()
+        self.proc = None
+        self.t0 = self.t1 = None
         try:
-            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
-            if self.nv.nvmlInit_v2() != 0:
-                raise OSError("nvmlInit")
             import torch
 
             pr = torch.cuda.get_device_properties(torch_device_index)
-            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
-            h = ctypes.c_void_p()
-            if self.nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
-                raise OSError("handle")
-            self.handle = h
-            mx = ctypes.c_uint()
-            if self.nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
-                self.max_mhz = float(mx.value)
-            self._reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+            self.ok = True
         except Exception:
-            self.handle = None
+            self.ok = False
 
-    def _run(self):
-        import ctypes
+    @property
+    def handle(self):
+        return self.ok or None
 
-        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self._stop.is_set():
-            if self.nv.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
-                r = rs.value if self._reasons(self.handle, ctypes.byref(rs)) == 0 else 0
-                self.samples.append((float(mhz.value), int(r)))
-            time.sleep(self.period)
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = line.split()
+            if parts and parts[0] == "max":
+                self.max_mhz = float(parts[1])
+                self.ready.set()
+            elif len(parts) == 3:
+                self.rows.append((float(parts[0]), float(parts[1]), int(parts[2])))
 
     def __enter__(self):
-        if self.handle is not None:
-            self.thread = threading.Thread(target=self._run, daemon=True)
+        if self.ok:
+            self.ready = threading.Event()
+            self.proc = subprocess.Popen([sys.executable, "-c", NVML_POLL, self.bus, str(self.period)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            self.ready.wait(timeout=10)
+            time.sleep(0.005)
+        self.t0 = time.monotonic()
         return self
 
     def __exit__(self, *exc):
-        if self.handle is not None:
-            self._stop.set()
+        self.t1 = time.monotonic()
+        if self.proc is not None:
+            time.sleep(0.002)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
             self.thread.join(timeout=2)
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
-        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
-        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                "sm_mhz_min": min(m for m, _ in self.samples), "reasons": reasons, "samples": len(self.samples),
-                "source": f"nvml, every {self.period * 1e3:.1f} ms during the timed region"}
+        inside = [(m, r) for t, m, r in self.rows if self.t0 is not None and self.t0 <= t <= self.t1]
+        src = f"nvml from a separate process every {self.period * 1e3:.1f} ms, samples inside the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": src}
+        reasons = sorted({n for _, r in inside for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in inside), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(m for m, _ in inside), "reasons": reasons, "samples": len(inside), "source": src}
 
 
 def clock_sampler(index: int):
@@ -438,13 +464,35 @@ def run_ours(args):
         t_start.record(stream)
         for i in range(args.steps):
             step(copies[i % N_COPIES], args.warmup + i, evs[i])
+        for cp in copies:  # column-view rebuilds still running on the handles' second streams
+            snack.snack_wait_plan(cp["h"], stream)
         t_end.record(stream)
         stream.synchronize()
     torch.cuda.synchronize()
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ops = list(STEP_OPS)
-    op_ms = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
-             for j, op in enumerate(ops)}
+    # Per-op breakdown, outside the timed region: the column-view rebuild a
+    # restructure leaves on its handle's second stream overlaps the next
+    # step's forward in the timed loop, so there the op events do not isolate
+    # the ops.  Here every op starts after all earlier work, and the
+    # restructure's time runs until its rebuild has finished as well.
+    n_bd = max(1, min(args.steps, 100))
+    bd = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_bd)]
+    for i in range(n_bd):
+        cp = copies[i % N_COPIES]
+        for c2 in copies:
+            snack.snack_wait_plan(c2["h"], stream)
+        e = bd[i]
+        step(cp, 2 * 10**6 + i, e[:4])
+        snack.snack_wait_plan(cp["h"], stream)
+        e[4].record(stream)
+    stream.synchronize()
+    op_ms = {"fwd": statistics.mean(e[0].elapsed_time(e[1]) for e in bd),
+             "bwd": statistics.mean(e[1].elapsed_time(e[2]) for e in bd),
+             "restructure": statistics.mean(e[2].elapsed_time(e[4]) for e in bd)}
+    restructure_on_stream_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in bd)
+    overlapped_ms = {op: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                     for j, op in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps
     value = job_throughput(step_bytes, world, elapsed_ms / args.steps)
     peak, peak_kind = measured_peak_gbs()
@@ -453,11 +501,20 @@ def run_ours(args):
         gbs = byts[op] / (op_ms[op] / 1e3) / 1e9
         flops = {"fwd": 2 * nnz * BATCH, "bwd": 4 * nnz * BATCH}.get(op)
         op_report[op] = {"us": op_ms[op] * 1e3, "alg_bytes": byts[op], "gbs": gbs, "frac": gbs / peak,
-                         "gflops": (flops / (op_ms[op] / 1e3) / 1e9) if flops else None}
+                         "gflops": (flops / (op_ms[op] / 1e3) / 1e9) if flops else None,
+                         "us_in_timed_loop": overlapped_ms[op] * 1e3}
+    op_report["restructure"]["us_until_return"] = restructure_on_stream_ms * 1e3
     dominant = max(ops, key=lambda o: op_ms[o])
+    launches = {"fwd": 3, "bwd": 3, "restructure": restructure_launches()}
     roofline = {"bound": "hbm", "achieved": op_report[dominant]["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": op_report[dominant]["gbs"] / peak, "traffic": profiled_traffic(dominant),
-                "kernel": dominant, "peak_kind": peak_kind}
+                "kernel": f"op {dominant} ({launches[dominant]} launches; the op with the largest time share)",
+                "peak_kind": peak_kind,
+                # the largest single kernel of the step is the fused backward's tile kernel; its op time
+                # (both transposes, the tiles, the fix-up) bounds the kernel's time from above
+                "largest_kernel": {"name": "k_spmm_tiles<float, float, 4, 8, 1, 1> (fused backward, dX + dW)",
+                                   "achieved_op": op_report["bwd"]["gbs"], "frac_op": op_report["bwd"]["frac"],
+                                   "alg_bytes": byts["bwd"]}}
 
     # end to end through the C ABI from pinned host buffers: every step's inputs
     # go host -> device and its results device -> host inside the timed region,
@@ -508,6 +565,8 @@ def run_ours(args):
     for d in drained:
         if d is not None:
             stream.wait_event(d)
+    for cp in copies:
+        snack.snack_wait_plan(cp["h"], stream)
     e1.record(stream)
     stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)

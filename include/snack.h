@@ -31,14 +31,20 @@
  * the legacy default stream), except snack_create with validate != 0, which
  * synchronises `stream`, and snack_restructure, which waits on the host for
  * its draw count (see there).  A plan and a workspace may be used by one call
- * in flight at a time.
+ * in flight at a time.  After snack_restructure the rebuild of the plan's
+ * column view may still be running on the handle's second stream; every call
+ * that reads the column view (snack_spmm_dx, snack_spmm_dx_gelu,
+ * snack_sddmm_dw, snack_backward and both restructures) first makes its
+ * stream wait for it, so results never depend on the timing.  The forward
+ * reads only the row half of the plan and does not wait.  snack_wait_plan
+ * orders any stream after that rebuild.
  *
- * Host threads.  Issue the calls for one device from one host thread at a
- * time (or under a lock).  The launchers raise a kernel's dynamic
- * shared-memory limit to what the call needs.  Two threads that launch the
- * same kernel for layers of different sizes at the same moment can lower
- * that limit under each other.  One launch then fails with SNACK_ERR_CUDA;
- * memory is never touched out of bounds.
+ * Host threads.  Calls may come from several host threads.  The launchers
+ * raise a kernel's dynamic shared-memory limit (a per-process, per-device
+ * setting) through one table kept under a lock, and never lower it, so
+ * threads launching one kernel for layers of different sizes do not disturb
+ * each other.  Calls on one handle, plan or workspace must still be ordered
+ * (one call in flight at a time, see Streams).
  *
  * Errors.  Every entry point returns a snack_status.  Arguments are checked
  * on the host before any launch; a failed launch or CUDA call returns
@@ -104,6 +110,10 @@ typedef enum snack_dtype { SNACK_F32 = 0, SNACK_BF16 = 1 } snack_dtype;
  *                    that uses none of it; other calls check ws_bytes against
  *                    what they use and return SNACK_ERR_WORKSPACE before any
  *                    launch when it is short.
+ * For layers whose column view is rebuilt after the call returns (256 <
+ * in_f <= 131072 and row plus column index bits <= 32), plan_bytes also holds
+ * that rebuild's scratch (8 bytes per stored weight and two small tables), so
+ * it never uses the caller's workspace.
  * Limits: 1 <= out_f, in_f < 2^31; 0 <= nnz <= out_f*in_f and nnz < 2^31 - 1;
  * 1 <= max_batch <= 65535.  val_t must equal act_t (fp32/fp32 or bf16/bf16).
  * Either output pointer may be NULL.
@@ -238,7 +248,15 @@ snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, s
  * forked from and joined back into `stream`, concurrently with the prune
  * select; the host waits once per batch of draws (normally once) for that
  * batch's accepted count, while the device keeps working.  When the call
- * returns, all its work is ordered on `stream`.  Returns SNACK_ERR_NO_SPACE when fewer than
+ * returns, the new COO, the source map and the row half of the plan are
+ * ordered on `stream`; the workspace is free for the next call at once.  For
+ * layers with the deferred scratch in their plan (see snack_query_sizes) the
+ * column view is rebuilt from row_out/col_out on the handle's second stream
+ * after `stream`'s work, overlapping whatever the caller queues next; the
+ * calls that read it wait for it (see Streams), snack_wait_plan orders a
+ * stream after it, and snack_destroy waits for it.  row_out and col_out must
+ * not change while it runs (they are the layer's pattern from now on).
+ * Returns SNACK_ERR_NO_SPACE when fewer than
  * n_prune positions are empty or the draw budget (sized in the workspace
  * query: twice the expected number of draws plus 4096) runs out; the handle's
  * plan is then unchanged.
@@ -279,9 +297,19 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
                                     int32_t *col_out, void *val_out, int32_t *src_out, void *ws, size_t ws_bytes,
                                     snack_stream_t stream);
 
+/*
+ * Order `stream` after every plan rebuild of the handle that may still be
+ * running on its second stream (the column view of the last
+ * snack_restructure); returns at once, asynchronous like every call.  Use it
+ * before timing, freeing or reading anything that the rebuild touches (the
+ * plan; row_out/col_out of the last restructure).  A handle that has not
+ * restructured has nothing pending.
+ */
+snack_status snack_wait_plan(snack_handle h, snack_stream_t stream);
+
 /* Free the handle: its host memory, and the stream, events and pinned word of
- * a handle that has restructured (waits for that stream).  No device memory
- * of the caller is touched.  NULL is allowed. */
+ * a handle that has restructured (waits for that stream, so for any pending
+ * plan rebuild).  No device memory of the caller is touched.  NULL is allowed. */
 void snack_destroy(snack_handle h);
 
 /* Static description of a status code. */

@@ -21,11 +21,20 @@ struct PlanPtrs {
   uint32_t *flags;   // [64]          validation flags and small device scalars
   uint16_t *col16;   // [nnz]         16-bit copy of col (in_f <= 65536), else null
   uint16_t *rowt16;  // [nnz]         16-bit copy of row_t (out_f <= 65536), else null
+  // Scratch of the column view's rebuild after a restructure, which runs on
+  // the handle's second stream after the call has returned (so it cannot use
+  // the caller's workspace); present when colview_digits holds, else null.
+  uint32_t *cv_keys;  // [nnz] first-level scatter: packed (row, col) keys
+  uint32_t *cv_vals;  // [nnz] and their storage indices
+  uint32_t *cv_offs;  // digit-major first-level scatter offsets (colview_hist_bytes)
+  uint32_t *cv_hist;  // their tile histogram (colview_hist_bytes)
 };
 
 struct PlanLayout {
-  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, total;
+  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cvk, off_cvv,
+      off_cvo, off_cvh, total;
   bool c16, r16;  // the 16-bit index copies exist
+  bool cv;        // the deferred column-view rebuild's scratch exists
   TileGeom gf, gt;
 };
 
@@ -39,15 +48,19 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 // restructure's merge), kPlanRowTilesReady (also the forward tiles: a
 // per-row restructure keeps every row's offsets).
 constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
-// With `aux` (and two events), the forward tiles are cut on that stream,
-// beside the column view on s, and s waits for them before returning.
-// `col_offs`, when set, are the column view's first-level scatter offsets
-// (digit-major, see colview_digits) already made on another stream: s waits
-// for `col_ready` and the rebuild only scatters.
+// With `aux` (and two events) after a restructure (kPlanRowsReady):
+//  * when the plan has the deferred scratch (PlanPtrs::cv_*), the forward
+//    tiles are cut on s and the column view is rebuilt on `aux` after s's
+//    work so far (ev_a), from the first-level offsets that the restructure
+//    left in cv_offs on `aux`; ev_b is recorded on `aux` when it is done and
+//    s does NOT wait for it (*deferred is set): the calls that read the column
+//    view wait for ev_b;
+//  * otherwise the forward tiles are cut on `aux` beside the column view on
+//    s, and s waits for them before returning.
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
                        int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr,
-                       const uint32_t *col_offs = nullptr, cudaEvent_t col_ready = nullptr);
+                       bool *deferred = nullptr);
 
 // The column view's first level scatters (row, col) by the column's high 8
 // bits when 9..17-bit columns and row + column bits fit 32: then *shift =
@@ -83,14 +96,12 @@ struct RestructureArgs {
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
   cudaStream_t aux;          // second stream of the handle (regrow branch)
   cudaEvent_t ev_fork, ev_join;
-  cudaEvent_t ev_col;  // recorded on aux once the column view's first-level offsets are made
+  // When set (colview_digits holds), the column view's first-level histogram
+  // and offsets of the new pattern are made into these plan arrays on `aux`,
+  // beside the merge, for the column-view rebuild that follows on `aux`.
+  uint32_t *cv_offs, *cv_hist;
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
-// Whether a restructure makes the column view's first-level offsets beside
-// its merge (colview_digits holds), and where it leaves them: pass
-// ws + colview_offs_offset to build_plan with the handle's ev_col.
-bool restructure_makes_col_offs(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
-size_t colview_offs_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 
@@ -144,7 +155,12 @@ struct snack_layer {
   uint32_t *host_counts_dev = nullptr;  // its device address
   cudaEvent_t counts_ready = nullptr;
   cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_col = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // The column view of the last restructure is rebuilt on `aux` after the
+  // call returns; ev_colview marks its end and the calls that read the
+  // column view make their stream wait for it.
+  cudaEvent_t ev_colview = nullptr;
+  bool colview_pending = false;
   bool dense = false;   // the layer takes the dense path for wide batches
   void *lt = nullptr;   // cuBLASLt handle of the dense path
 };

@@ -365,6 +365,18 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
   if (L.c16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
   L.off_rowt16 = o;
   if (L.r16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
+  L.cv = colview_digits(out_f, in_f, nnz, nullptr);
+  L.off_cvk = L.off_cvv = L.off_cvo = L.off_cvh = o;
+  if (L.cv) {
+    L.off_cvk = o;
+    o += align_up(sizeof(uint32_t) * (size_t)nnz, kAlign);
+    L.off_cvv = o;
+    o += align_up(sizeof(uint32_t) * (size_t)nnz, kAlign);
+    L.off_cvo = o;
+    o += colview_hist_bytes(nnz);
+    L.off_cvh = o;
+    o += colview_hist_bytes(nnz);
+  }
   L.total = o;
   return L;
 }
@@ -381,6 +393,10 @@ PlanPtrs plan_ptrs(const PlanLayout &L, void *base) {
   p.flags = reinterpret_cast<uint32_t *>(b + L.off_flags);
   p.col16 = L.c16 ? reinterpret_cast<uint16_t *>(b + L.off_col16) : nullptr;
   p.rowt16 = L.r16 ? reinterpret_cast<uint16_t *>(b + L.off_rowt16) : nullptr;
+  p.cv_keys = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvk) : nullptr;
+  p.cv_vals = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvv) : nullptr;
+  p.cv_offs = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvo) : nullptr;
+  p.cv_hist = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvh) : nullptr;
   return p;
 }
 
@@ -456,13 +472,14 @@ size_t colview_hist_bytes(int64_t nnz) {
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, const uint32_t *col_offs,
-                       cudaEvent_t col_ready) {
+                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, bool *deferred) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
   void *stemp = b + W.scan;
   cudaError_t e;
+  if (deferred) *deferred = false;
+  const int cbits = bits_for((uint64_t)(in_f - 1));
 
   // row offsets and the 16-bit column copy: already written by a
   // restructure's merge, made here otherwise
@@ -471,7 +488,33 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
     if (e != cudaSuccess) return e;
   }
-  const bool fork = aux && ev_a && ev_b && ready == kPlanRowsReady;
+  const bool restructured = aux && ev_a && ev_b && ready == kPlanRowsReady;
+  int dshift = 0;
+  if (restructured && p.cv_keys && colview_digits(out_f, in_f, nnz, &dshift)) {
+    // The forward reads only the row half of the plan: cut its tiles here,
+    // and rebuild the column view on `aux` after the call returns, from the
+    // first-level offsets the restructure left in cv_offs on `aux`.
+    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s, p.rp, out_f, nnz, gf.cost_per_tile,
+               gf.row_weight, gf.n_tiles, p.tiles_f);
+    e = cudaEventRecord(ev_a, s);  // after the merge wrote (row, col)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, ev_a, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t nb = ceil_div(nnz, kRadixTile);
+    e = radix_scatter_only<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{p.cv_keys, p.cv_vals},
+                                     nnz, dshift, p.cv_offs, aux);
+    if (e == cudaSuccess) e = launch_colview_bucket(dshift, p.cv_keys, p.cv_vals, nnz, cbits, p.cv_offs, nb, in_f, p, aux);
+    if (e == cudaSuccess) {
+      launch_pdl(k_tiles, grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, aux, p.cp, in_f, nnz,
+                 gt.cost_per_tile, gt.row_weight, gt.n_tiles, p.tiles_t);
+      e = cudaGetLastError();
+    }
+    cudaError_t r = cudaEventRecord(ev_b, aux);
+    if (e == cudaSuccess) e = r;
+    if (e == cudaSuccess && deferred) *deferred = true;
+    if (e != cudaSuccess) cudaStreamWaitEvent(s, ev_b, 0);
+    return e;
+  }
+  const bool fork = restructured;
   if (fork) {  // the forward tiles need only the row offsets: cut them beside the column view
     e = cudaEventRecord(ev_a, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, ev_a, 0);
@@ -497,7 +540,6 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   };
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
-  const int cbits = bits_for((uint64_t)(in_f - 1));
   if (colview_digits(out_f, in_f, nnz, nullptr)) {
     // 9..17-bit columns: stable scatter of (row, col) by the column's high 8
     // bits, then one block per group sorts by the low bits and writes the
@@ -510,16 +552,8 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     const size_t hbytes = align_up((size_t)nb * kRadixBins * sizeof(uint32_t), kAlign);
     uint32_t *hist = reinterpret_cast<uint32_t *>(t);
     const uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
-    if (col_offs) {  // offsets made beside the restructure's merge: wait for them, then scatter
-      e = col_ready ? cudaStreamWaitEvent(s, col_ready, 0) : cudaSuccess;
-      if (e == cudaSuccess)
-        e = radix_scatter_only<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz,
-                                         shift, col_offs, s);
-      offs = col_offs;
-    } else {
-      e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
-                               reinterpret_cast<uint32_t *>(t + hbytes), t + 2 * hbytes, s);
-    }
+    e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
+                             reinterpret_cast<uint32_t *>(t + hbytes), t + 2 * hbytes, s);
     if (e != cudaSuccess) return joined(e);
     e = launch_colview_bucket(shift, ka, va, nnz, cbits, offs, nb, in_f, p, s);
     if (e != cudaSuccess) return joined(e);

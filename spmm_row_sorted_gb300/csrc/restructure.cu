@@ -685,10 +685,10 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // the column view's first-level histogram and offsets are made from the
   // merge's split points on the second stream, beside the merge
   int cshift = 0;
-  const bool col_offs = restructure_makes_col_offs(a.out_f, a.in_f, nnz, &cshift);
+  const bool col_offs = a.cv_offs && a.cv_hist && colview_digits(a.out_f, a.in_f, nnz, &cshift);
   const int64_t cnb = ceil_div(nnz, kRadixTile);
-  uint32_t *coffs = reinterpret_cast<uint32_t *>(b + colview_offs_offset(a.out_f, a.in_f, nnz, n_prune));
-  uint32_t *chist = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(coffs) + colview_hist_bytes(nnz));
+  uint32_t *coffs = a.cv_offs;
+  uint32_t *chist = a.cv_hist;
   cudaError_t e;
 #define SNACK_TRY(x)                       \
   do {                                     \
@@ -815,22 +815,24 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   if (nnz > 0) {
     launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
                                                                               W.n_merge_tiles, part);
-    if (col_offs) {  // fork: the column histogram and its scan beside the merge
+    if (col_offs) {  // fork: the column histogram and its scan beside the merge, into the plan, for the
+                     // column-view rebuild that follows on the second stream
       SNACK_TRY(cudaEventRecord(a.ev_fork, s));
       SNACK_TRY(cudaStreamWaitEvent(s2, a.ev_fork, 0));
       launch_pdl(k_col_hist, (unsigned)cnb, 256, 0, s2, (const uint64_t *)surv_pos, grown, (const int64_t *)part,
                  W.n_merge_tiles, nnz, cbits, cshift, chist, cnb);
       e = scan_apply<uint32_t>(HistRead{chist}, cnb * kRadixBins, WriteExcl32{coffs}, (uint32_t *)nullptr, stemp2, s2);
-      cudaError_t er = cudaEventRecord(a.ev_col, s2);  // build_plan waits for it before its scatter
-      if (e == cudaSuccess) e = er;
       if (e != cudaSuccess) {
-        cudaStreamWaitEvent(s, a.ev_col, 0);
+        join();
         return SNACK_ERR_CUDA;
       }
     }
     launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, surv_pos, surv_src, n_surv, grown, n_prune,
                part, cbits, a.out_f, val, a.row_out, a.col_out, reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new,
                a.col16_new);
+    // the column histogram read the merge's inputs and scanned in the
+    // workspace: it is ordered on s before the call returns
+    if (col_offs) SNACK_TRY(join());
   }
   SNACK_TRY(cudaGetLastError());
 #undef SNACK_TRY
@@ -1070,22 +1072,13 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
 
 }  // namespace
 
-bool restructure_makes_col_offs(int32_t out_f, int32_t in_f, int64_t nnz, int *shift) {
-  return colview_digits(out_f, in_f, nnz, shift);
-}
-
-// The column offsets (and the histogram behind them) sit past both the
-// restructure's own scratch and the plan rebuild's, so the rebuild can read
-// them while reusing the rest.
-size_t colview_offs_offset(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
+// The restructure's own scratch, or the plan rebuild's when that is larger
+// (the rebuild runs on the caller's stream for layers whose column view is
+// not rebuilt on the second stream).
+size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
   size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
   return align_up(r > p ? r : p, kAlign);
-}
-
-size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
-  return colview_offs_offset(out_f, in_f, nnz, n_prune) +
-         (colview_digits(out_f, in_f, nnz, nullptr) ? 2 * colview_hist_bytes(nnz) : 0);
 }
 
 snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) {

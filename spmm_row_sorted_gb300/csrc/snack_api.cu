@@ -395,6 +395,13 @@ bool use_dense(snack_handle h, int32_t batch, size_t ws_bytes) {
   return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f, h->max_batch);
 }
 
+// The column view of a restructured handle may still be rebuilding on the
+// handle's second stream: order `s` after it.  The forward reads only the
+// row half of the plan and does not wait.
+bool wait_colview(snack_handle h, cudaStream_t s) {
+  return !h->colview_pending || cudaStreamWaitEvent(s, h->ev_colview, 0) == cudaSuccess;
+}
+
 snack_status common_call_checks(snack_handle h, int32_t batch, void *ws) {
   if (!h) return SNACK_ERR_INVALID_ARG;
   if (batch < 0 || batch > h->max_batch) return SNACK_ERR_INVALID_ARG;
@@ -504,6 +511,7 @@ snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *co
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   if (col && use_dense(h, batch, ws_bytes)) return dense_dx(h, col, val, dy, batch, dx, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s);
   return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s);
@@ -517,6 +525,7 @@ snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *c
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   if (batch == 0) {  // empty sums
     if (h->nnz > 0) SNACK_CUDA(cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)h->nnz, s));
     if (db) SNACK_CUDA(cudaMemsetAsync(db, 0, sizeof(float) * (size_t)h->out_f, s));
@@ -562,6 +571,7 @@ snack_status snack_spmm_dx_gelu(snack_handle h, const int32_t *row, const int32_
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
   return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s, kActGeluGrad, x_pre);
 }
@@ -575,6 +585,7 @@ snack_status snack_backward(snack_handle h, const int32_t *row, const int32_t *c
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   if (batch == 0) {  // empty sums
     if (h->nnz > 0) SNACK_CUDA(cudaMemsetAsync(dw, 0, sizeof(float) * (size_t)h->nnz, s));
     if (db) SNACK_CUDA(cudaMemsetAsync(db, 0, sizeof(float) * (size_t)h->out_f, s));
@@ -624,6 +635,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   RestructureArgs a;
   a.out_f = h->out_f;
   a.in_f = h->in_f;
@@ -647,7 +659,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
     return SNACK_ERR_CUDA;
   if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
-  if (!h->ev_col && cudaEventCreateWithFlags(&h->ev_col, cudaEventDisableTiming) != cudaSuccess)
+  if (!h->ev_colview && cudaEventCreateWithFlags(&h->ev_colview, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
   if (!h->aux) {
     // The regrow branch (draws, acceptance, sort) is the longer of the two
@@ -663,17 +675,24 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.aux = h->aux;
   a.ev_fork = h->ev_fork;
   a.ev_join = h->ev_join;
-  a.ev_col = h->ev_col;
+  a.cv_offs = h->p.cv_offs;
+  a.cv_hist = h->p.cv_hist;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
-  if (st != SNACK_OK) return st;
-  const uint32_t *col_offs =
-      restructure_makes_col_offs(h->out_f, h->in_f, nnz, nullptr)
-          ? reinterpret_cast<const uint32_t *>(reinterpret_cast<uint8_t *>(ws) +
-                                               colview_offs_offset(h->out_f, h->in_f, nnz, n_prune))
-          : nullptr;
-  SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
-                        h->aux, h->ev_fork, h->ev_join, col_offs, h->ev_col));
-  return SNACK_OK;
+  if (st == SNACK_OK) {
+    bool deferred = false;
+    if (build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
+                   h->aux, h->ev_fork, h->ev_colview, &deferred) != cudaSuccess)
+      st = SNACK_ERR_CUDA;
+  }
+  // Whatever is still queued on the second stream (the column-view rebuild,
+  // or work an error left behind) is what the column-view readers wait for.
+  if (cudaEventRecord(h->ev_colview, h->aux) != cudaSuccess) {
+    cudaStreamSynchronize(h->aux);
+    h->colview_pending = false;
+    return SNACK_ERR_CUDA;
+  }
+  h->colview_pending = true;
+  return st;
 }
 
 snack_status snack_restructure_rows_workspace_size(snack_handle h, int64_t n_per_row, size_t *bytes) {
@@ -708,6 +727,7 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
   if (!g.ok) return SNACK_ERR_CUDA;
   if (!readback_ready(h)) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   RowsRestructureArgs a;
   a.out_f = h->out_f;
@@ -742,10 +762,17 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
   return SNACK_OK;
 }
 
+snack_status snack_wait_plan(snack_handle h, snack_stream_t stream) {
+  if (!h) return SNACK_ERR_INVALID_ARG;
+  DevGuard g(h->device);
+  if (!g.ok) return SNACK_ERR_CUDA;
+  return wait_colview(h, reinterpret_cast<cudaStream_t>(stream)) ? SNACK_OK : SNACK_ERR_CUDA;
+}
+
 void snack_destroy(snack_handle h) {
   if (!h) return;
   dense_release(h);
-  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join || h->ev_col) {
+  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join || h->ev_colview) {
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
@@ -756,7 +783,7 @@ void snack_destroy(snack_handle h) {
     if (h->counts_ready) cudaEventDestroy(h->counts_ready);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
-    if (h->ev_col) cudaEventDestroy(h->ev_col);
+    if (h->ev_colview) cudaEventDestroy(h->ev_colview);
     if (prev >= 0) cudaSetDevice(prev);
   }
   if (h->host_counts) cudaFreeHost(h->host_counts);

@@ -31,7 +31,7 @@ SNACK_F32, SNACK_BF16 = 0, 1
 EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
             "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw", "snack_backward",
             "snack_restructure_workspace_size", "snack_restructure", "snack_restructure_rows_workspace_size",
-            "snack_restructure_rows", "snack_destroy", "snack_status_string", "snack_version")
+            "snack_restructure_rows", "snack_wait_plan", "snack_destroy", "snack_status_string", "snack_version")
 
 
 class SnackLibraryMissing(RuntimeError):
@@ -91,6 +91,8 @@ def load(path: Optional[str] = None):
         lib.snack_restructure_rows_workspace_size.restype = st
         lib.snack_restructure_rows.argtypes = [vp, vp, vp, vp, i64, u64, u64, vp, vp, vp, vp, vp, sz, vp]
         lib.snack_restructure_rows.restype = st
+        lib.snack_wait_plan.argtypes = [vp, vp]
+        lib.snack_wait_plan.restype = st
         lib.snack_destroy.argtypes = [vp]
         lib.snack_destroy.restype = None
         lib.snack_status_string.argtypes = [st]
@@ -223,6 +225,10 @@ def snack_restructure_rows(h: int, row, col, val, n_per_row: int, seed: int, ste
            load().snack_restructure_rows(ctypes.c_void_p(h), _ptr(row), _ptr(col), _ptr(val), n_per_row,
                                          seed & (2**64 - 1), step & (2**64 - 1), _ptr(row_out), _ptr(col_out),
                                          _ptr(val_out), _ptr(src_out), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def snack_wait_plan(h: int, stream=None) -> None:
+    _check("snack_wait_plan", load().snack_wait_plan(ctypes.c_void_p(h), _stream(stream)))
 
 
 def snack_destroy(h: int) -> None:

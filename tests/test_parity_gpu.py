@@ -290,6 +290,43 @@ def test_restructure_chain_plan_equals_fresh(dtype, case):
     L.close()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_restructure_deferred_column_view(dtype):
+    # After a restructure the column view is rebuilt on the handle's second
+    # stream once the call has returned.  Its scratch lives in the plan: the
+    # workspace is overwritten right after the call, the forward runs at once
+    # (it does not wait), and the column-view readers run on another stream
+    # (they wait for the rebuild through the handle's event); every result
+    # matches the oracle on the new pattern, at a small-batch and a tile batch.
+    out_f, in_f, nnz = 3000, 5000, 300000
+    lay = wl.make_layer(out_f, in_f, nnz=nnz, zipf_s=1.1, val_std=0.3, val_dtype=dtype, seed=8, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=32)
+    ro, co, so, _ = oracle.restructure(out_f, in_f, lay.row, lay.col, oracle.as_f64(lay.val, dtype), 30000, 3, 4)
+    new = wl.Layer(out_f, in_f, ro, co, oracle.restructure_values(lay.val, so), lay.bias, dtype)
+    other = torch.cuda.Stream()
+    for batch in (4, 32):
+        acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+        x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
+        M = snack.SparseLinear(out_f, in_f, row.clone(), col.clone(), val.clone(), bias, max_batch=32)
+        M.restructure(30000, seed=3, step=4)
+        M.ws.fill_(255)  # the rebuild must not read the caller's workspace
+        got = {"y": M.forward(x)}
+        other.wait_stream(torch.cuda.current_stream())  # inputs and the new COO, not the rebuild
+        with torch.cuda.stream(other):
+            got["dx"] = M.grad_input(dy, stream=other)
+            got["dw"], got["db"] = M.grad_weight(x, dy, stream=other)
+            bdx, bdw, bdb = M.backward(x, dy, stream=other)
+        other.synchronize()
+        torch.cuda.synchronize()
+        assert np.array_equal(M.row.cpu().numpy(), ro) and np.array_equal(M.col.cpu().numpy(), co)
+        check_layer_ops(new, acts, got=got)
+        check_layer_ops(new, acts, ops=("dx", "dw"), got={"dx": bdx, "dw": bdw, "db": bdb})
+        snack.snack_wait_plan(M.handle)
+        M.close()
+    L.close()
+
+
 def test_restructure_ties_zeros_nan():
     lay = wl.make_layer(60, 70, nnz=2000, val_dtype="f32", seed=4)
     v = np.round(lay.val * 50).astype(np.float32) / 50  # many exact ties
