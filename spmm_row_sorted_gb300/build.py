@@ -1,8 +1,8 @@
 """Build libsnack.so (the CUDA library behind include/snack.h) in-tree.
 
 Each ``csrc/*.cu`` compiles in parallel for sm_103a only, then links into
-``_build/libsnack.so`` against the shared CUDA runtime and cuBLASLt (the
-dense path's GEMM).  A stamp keyed on the
+``_build/libsnack.so`` against the shared CUDA runtime (no other library).
+A stamp keyed on the
 sources, flags and host machine decides when to rebuild, so a library built
 on another architecture is never reused.
 """
@@ -94,7 +94,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         objs = list(ex.map(compile_one, srcs))
     tmp = lib_path + f".tmp{os.getpid()}"
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
-    cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublasLt",
+    cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     for o in objs:

@@ -28,17 +28,22 @@ struct PlanPtrs {
   uint32_t *cv_vals;  // [nnz] and their storage indices
   uint32_t *cv_offs;  // digit-major first-level scatter offsets (colview_hist_bytes)
   uint32_t *cv_hist;  // their tile histogram (colview_hist_bytes)
+  // Moderately sparse bf16 layers (dense_layer): per 64-column block and row,
+  // the stored-position mask (u64) and the storage index of the block's
+  // first stored weight (dense.cu, build_tables); else null.
+  void *tables;
 };
 
 struct PlanLayout {
   size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cvk, off_cvv,
-      off_cvo, off_cvh, total;
+      off_cvo, off_cvh, off_tab, total;
   bool c16, r16;  // the 16-bit index copies exist
   bool cv;        // the deferred column-view rebuild's scratch exists
+  bool dense;     // the tensor-core path's mask and offset tables exist
   TileGeom gf, gt;
 };
 
-PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles);
+PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles, bool dense);
 PlanPtrs plan_ptrs(const PlanLayout &lay, void *base);
 size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 
@@ -105,12 +110,19 @@ size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
 snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
 
-// Dense path for moderately sparse bf16 layers (dense.cu): used for calls
-// with batch >= kDenseMinBatch on layers with >= 25 % of W stored, when the
-// workspace holds the dense copy (snack_query_sizes reserves it).
+// Tensor-core path for moderately sparse bf16 layers (dense.cu): layers with
+// >= 25 % of W stored, feature counts multiples of 8 and <= 65536, created
+// with max_batch >= kDenseMinBatch; used for calls with batch >=
+// kDenseMinBatch whose activations are 16-byte aligned and whose workspace
+// holds the path's scratch (snack_query_sizes reserves it).
 constexpr int kDenseMinBatch = 32;
 bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t);
-size_t dense_ws_bytes(int32_t out_f, int32_t in_f, int32_t max_batch);
+size_t dense_table_bytes(int32_t out_f, int32_t in_f);
+cudaError_t build_tables(const int32_t *rp, const uint16_t *col16, int32_t out_f, int32_t in_f, void *tables,
+                         cudaStream_t s);
+// scratch of one call at `batch` on a device with num_sms SMs (a larger
+// num_sms never needs less)
+size_t dense_ws_bytes(int32_t out_f, int32_t in_f, int32_t batch, int num_sms);
 
 // Per-row (constant fan-in) restructure (restructure.cu): rows keep their
 // counts and offsets; the plan's row offsets and forward tiles stay valid.
@@ -161,17 +173,15 @@ struct snack_layer {
   // column view make their stream wait for it.
   cudaEvent_t ev_colview = nullptr;
   bool colview_pending = false;
-  bool dense = false;   // the layer takes the dense path for wide batches
-  void *lt = nullptr;   // cuBLASLt handle of the dense path
+  bool dense = false;   // the layer takes the tensor-core path for wide batches
 };
 
 namespace snack {
-bool dense_init(snack_layer *h);
-void dense_release(snack_layer *h);
-snack_status dense_fwd(snack_layer *h, const int32_t *col, const void *val, const void *x, int32_t batch,
-                       const float *bias, void *y, void *ws, size_t ws_bytes, cudaStream_t s);
-snack_status dense_dx(snack_layer *h, const int32_t *col, const void *val, const void *dy, int32_t batch, void *dx,
-                      void *ws, size_t ws_bytes, cudaStream_t s);
-snack_status dense_dw(snack_layer *h, const int32_t *col, const void *x, const void *dy, int32_t batch, float *dw,
-                      float *db, void *ws, size_t ws_bytes, cudaStream_t s);
+bool dense_call_ok(const snack_layer *h, int32_t batch, const void *act, size_t ws_bytes);
+snack_status dense_fwd(snack_layer *h, const void *val, const void *x, int32_t batch, const float *bias, void *y,
+                       void *ws, size_t ws_bytes, cudaStream_t s);
+snack_status dense_dx(snack_layer *h, const void *val, const void *dy, int32_t batch, void *dx, void *ws,
+                      size_t ws_bytes, cudaStream_t s);
+snack_status dense_dw(snack_layer *h, const void *x, const void *dy, int32_t batch, float *dw, float *db, void *ws,
+                      size_t ws_bytes, cudaStream_t s);
 }  // namespace snack

@@ -340,7 +340,7 @@ cudaError_t build_offsets(const int32_t *idx, int64_t nnz, int32_t n, int32_t *p
 
 }  // namespace
 
-PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles) {
+PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int n_btiles, bool dense) {
   PlanLayout L;
   L.gf = tile_geom(out_f, nnz, bt_max, n_btiles);
   L.gt = tile_geom(in_f, nnz, bt_max, n_btiles);
@@ -377,6 +377,9 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
     L.off_cvh = o;
     o += colview_hist_bytes(nnz);
   }
+  L.dense = dense;
+  L.off_tab = o;
+  if (dense) o += dense_table_bytes(out_f, in_f);
   L.total = o;
   return L;
 }
@@ -397,6 +400,7 @@ PlanPtrs plan_ptrs(const PlanLayout &L, void *base) {
   p.cv_vals = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvv) : nullptr;
   p.cv_offs = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvo) : nullptr;
   p.cv_hist = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvh) : nullptr;
+  p.tables = L.dense ? reinterpret_cast<void *>(b + L.off_tab) : nullptr;
   return p;
 }
 
@@ -486,6 +490,11 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   if (ready < kPlanRowsReady && p.col16 && nnz > 0) launch_pdl(k_pack16, grid_for(nnz, 256), 256, 0, s, col, nnz, p.col16);
   if (ready < kPlanRowsReady) {
     e = build_offsets(row, nnz, out_f, p.rp, counts, stemp, s);
+    if (e != cudaSuccess) return e;
+  }
+  // the tensor-core path's per-(block, row) masks and offsets, from the row half
+  if (p.tables && p.col16) {
+    e = build_tables(p.rp, p.col16, out_f, in_f, p.tables, s);
     if (e != cudaSuccess) return e;
   }
   const bool restructured = aux && ev_a && ev_b && ready == kPlanRowsReady;

@@ -390,10 +390,6 @@ bool readback_ready(snack_handle h) {
   return true;
 }
 
-// Dense path: a dense layer, a wide batch, and room for the dense copy.
-bool use_dense(snack_handle h, int32_t batch, size_t ws_bytes) {
-  return h->dense && batch >= kDenseMinBatch && ws_bytes >= dense_ws_bytes(h->out_f, h->in_f, h->max_batch);
-}
 
 // The column view of a restructured handle may still be rebuilding on the
 // handle's second stream: order `s` after it.  The forward reads only the
@@ -418,12 +414,13 @@ snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t
   snack_status st = check_shape(out_f, in_f, nnz, max_batch, val_t, act_t);
   if (st != SNACK_OK) return st;
   const BatchGeom mbg = batch_geom(max_batch, act_t);
-  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles);
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles, dense_layer(out_f, in_f, nnz, max_batch, val_t));
   if (plan_bytes) *plan_bytes = lay.total;
   if (workspace_bytes) {
     size_t a = ops_ws_bytes(out_f, in_f, max_batch, act_t, lay);
     size_t b = plan_build_ws_bytes(out_f, in_f, nnz);
-    size_t c = dense_layer(out_f, in_f, nnz, max_batch, val_t) ? dense_ws_bytes(out_f, in_f, max_batch) : 0;
+    // the tensor-core path's scratch at max_batch on any GPU (more SMs never need less)
+    size_t c = dense_layer(out_f, in_f, nnz, max_batch, val_t) ? dense_ws_bytes(out_f, in_f, max_batch, 1 << 20) : 0;
     a = a > b ? a : b;
     *workspace_bytes = a > c ? a : c;
   }
@@ -440,7 +437,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   if (nnz > 0 && (!row || !col)) return SNACK_ERR_INVALID_ARG;
   if (!plan || !aligned(plan, kAlign) || !ws || !aligned(ws, kAlign)) return SNACK_ERR_INVALID_ARG;
   const BatchGeom mbg = batch_geom(max_batch, act_t);
-  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles);
+  PlanLayout lay = plan_layout(out_f, in_f, nnz, mbg.bt, mbg.n_btiles, dense_layer(out_f, in_f, nnz, max_batch, val_t));
   if (plan_bytes < lay.total) return SNACK_ERR_WORKSPACE;
   if (ws_bytes < plan_build_ws_bytes(out_f, in_f, nnz)) return SNACK_ERR_WORKSPACE;
   int dev = 0;
@@ -471,11 +468,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   h->p = p;
   h->plan_bytes = plan_bytes;
   h->num_sms = sms > 0 ? sms : 1;
-  h->dense = dense_layer(out_f, in_f, nnz, max_batch, val_t);
-  if (h->dense && !dense_init(h)) {
-    delete h;
-    return SNACK_ERR_CUDA;
-  }
+  h->dense = lay.dense;
   *out_handle = h;
   return SNACK_OK;
 }
@@ -493,7 +486,7 @@ snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *c
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (use_dense(h, batch, ws_bytes)) return dense_fwd(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
+  if (dense_call_ok(h, batch, x, ws_bytes)) return dense_fwd(h, val, x, batch, bias, y, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_fwd<bf16>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
   return run_fwd<float>(h, col, val, x, batch, bias, y, ws, ws_bytes, s);
 }
@@ -512,7 +505,7 @@ snack_status snack_spmm_dx(snack_handle h, const int32_t *row, const int32_t *co
   if (!g.ok) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
-  if (col && use_dense(h, batch, ws_bytes)) return dense_dx(h, col, val, dy, batch, dx, ws, ws_bytes, s);
+  if (dense_call_ok(h, batch, dy, ws_bytes)) return dense_dx(h, val, dy, batch, dx, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_dx<bf16>(h, val, dy, batch, dx, ws, ws_bytes, s);
   return run_dx<float>(h, val, dy, batch, dx, ws, ws_bytes, s);
 }
@@ -532,7 +525,7 @@ snack_status snack_sddmm_dw(snack_handle h, const int32_t *row, const int32_t *c
     return SNACK_OK;
   }
   if (!x || !dy) return SNACK_ERR_INVALID_ARG;
-  if (use_dense(h, batch, ws_bytes)) return dense_dw(h, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+  if (dense_call_ok(h, batch, dy, ws_bytes)) return dense_dw(h, x, dy, batch, dw, db, ws, ws_bytes, s);
   if (h->act_t == SNACK_BF16) return run_dw<bf16>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
   return run_dw<float>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
 }
@@ -596,9 +589,9 @@ snack_status snack_backward(snack_handle h, const int32_t *row, const int32_t *c
   if (overlap(dx, (size_t)batch * h->in_f * s_act, dy, (size_t)batch * h->out_f * s_act) ||
       overlap(dx, (size_t)batch * h->in_f * s_act, x, (size_t)batch * h->in_f * s_act))
     return SNACK_ERR_INVALID_ARG;
-  if (use_dense(h, batch, ws_bytes)) {
-    snack_status r = dense_dx(h, col, val, dy, batch, dx, ws, ws_bytes, s);
-    return r != SNACK_OK ? r : dense_dw(h, col, x, dy, batch, dw, db, ws, ws_bytes, s);
+  if (dense_call_ok(h, batch, dy, ws_bytes)) {
+    snack_status r = dense_dx(h, val, dy, batch, dx, ws, ws_bytes, s);
+    return r != SNACK_OK ? r : dense_dw(h, x, dy, batch, dw, db, ws, ws_bytes, s);
   }
   if (h->act_t == SNACK_BF16) return run_bwd<bf16>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
   return run_bwd<float>(h, row, col, val, x, dy, batch, dx, dw, db, ws, ws_bytes, s);
@@ -771,7 +764,6 @@ snack_status snack_wait_plan(snack_handle h, snack_stream_t stream) {
 
 void snack_destroy(snack_handle h) {
   if (!h) return;
-  dense_release(h);
   if (h->counts_ready || h->aux || h->ev_fork || h->ev_join || h->ev_colview) {
     int prev = -1;
     cudaGetDevice(&prev);

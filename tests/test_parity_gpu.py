@@ -583,7 +583,11 @@ def test_small_batch_skewed_rows_and_empty_layer():
 
 # ---------------------------------------------------------------- dense path (bf16, >= 25 % stored, batch >= 32)
 
-@pytest.mark.parametrize("case", [(256, 384, 0.5, 64), (300, 515, 0.3, 33), (128, 128, 1.0, 32), (200, 264, 0.6, 130)])
+# (out_f, in_f, density, batch): one and several M tiles, a partial last M
+# tile (out_f 8, 200), one partial K chunk (in_f 8), K split across CTAs
+# (2048 inputs), batch tiles of 48, 64, 144 and 2 x 256 (batch 300).
+@pytest.mark.parametrize("case", [(256, 384, 0.5, 64), (320, 520, 0.3, 33), (128, 128, 1.0, 32), (200, 264, 0.6, 130),
+                                  (8, 64, 0.5, 40), (136, 8, 0.5, 300), (1000, 2048, 0.26, 256)])
 def test_dense_path_matches_oracle(case):
     out_f, in_f, density, batch = case
     lay = wl.make_layer(out_f, in_f, density=density, val_std=0.2, val_dtype="bf16", seed=out_f, bias="normal")

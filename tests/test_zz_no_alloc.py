@@ -47,7 +47,7 @@ def call_noalloc(lib, L, row, col, val, x, batch, bias, y):
 
 @pytest.mark.parametrize("dtype,batch,density", [("f32", 32, None), ("bf16", 16, None), ("bf16", 64, 0.5)])
 def test_noalloc_matches_workspace_entry_point(lib, dtype, batch, density):
-    out_f, in_f = 700, 900
+    out_f, in_f = (700, 900) if density is None else (704, 896)
     if density is None:
         lay = wl.make_layer(out_f, in_f, nnz=40000, zipf_s=1.1, val_std=0.3, val_dtype=dtype, seed=5, bias="normal")
     else:  # half of W stored, bf16, batch >= 32: the moderately sparse (tensor-core) path
@@ -67,11 +67,8 @@ def test_noalloc_matches_workspace_entry_point(lib, dtype, batch, density):
     ref, t = oracle.fwd(out_f, in_f, lay.row, lay.col, oracle.as_f64(lay.val, dtype), oracle.as_f64(acts.x, dtype),
                         oracle.as_f64(lay.bias))
     assert_close_T(f64(y_ws), ref, t, ACC_REL, "workspace fwd", stored_bf16=dtype == "bf16")
-    for y in outs:
-        # the two calls run the same kernels on the same inputs
-        assert torch.equal(y, outs[0]), "two noalloc calls in a row differ"
-        if density is None:  # the workspace call runs the same kernels too
-            assert torch.equal(y, y_ws), "noalloc differs from the workspace entry point"
+    for y in outs:  # the same kernels on the same inputs: bit-identical
+        assert torch.equal(y, y_ws), "noalloc differs from the workspace entry point"
         assert_close_T(f64(y), ref, t, ACC_REL, "noalloc fwd", stored_bf16=dtype == "bf16")
     L.close()
 
