@@ -50,15 +50,18 @@
  * on the host before any launch; a failed launch or CUDA call returns
  * SNACK_ERR_CUDA.  The library never aborts, exits or traps on the device.
  *
- * Dense path.  A bf16 layer with at least a quarter of W stored, created with
- * max_batch >= 32, runs calls with batch >= 32 as dense contractions: the
- * stored weights are scattered into a dense bf16 copy of W in the workspace
- * and the product runs on the tensor cores through cuBLASLt (the weight
- * gradient is the dense dY^T X read back at the stored positions).
- * snack_query_sizes then reports a workspace that holds the dense copy, the
- * dense fp32 gradient and 32 MiB for cuBLASLt; a call given a smaller
- * workspace takes the gather kernels instead.  The handle then also owns a
- * cuBLASLt handle.  Results follow the same tolerance contract.
+ * Tensor-core path.  A bf16 layer with at least 8 % of W stored, out_f and
+ * in_f multiples of 8 and at most 65536, created with max_batch >= 16, runs
+ * calls with batch >= 16 (activations 16-byte aligned) as dense contractions
+ * on the tensor cores (tcgen05), never densifying W in memory: each CTA
+ * builds W tiles in shared memory from a per-(64-column block, row) mask and
+ * value-offset table that the plan keeps, and multiplies them with activation
+ * tiles brought in by TMA; the weight gradient is read back from the
+ * accumulators at the stored positions only.  snack_query_sizes reserves the
+ * tables in the plan and the path's scratch (split-K partial sums and
+ * transposed activations) in the workspace; a call given a smaller workspace
+ * takes the gather kernels instead.  Results follow the same tolerance
+ * contract.
  *
  * Plan contract.  snack_create derives a plan (row offsets, load-balanced
  * tiles, a column-ordered view) from row/col.  row/col may change only through
@@ -157,7 +160,11 @@ snack_status snack_spmm_fwd(snack_handle h, const int32_t *row, const int32_t *c
  * result as snack_spmm_fwd; its scratch is a 32 MiB array inside the
  * library's device image, held by every GPU that loads the library until the
  * process exits.  A call needing more scratch than that (large in_f * batch)
- * returns SNACK_ERR_WORKSPACE before any launch.  The first call on a device
+ * returns SNACK_ERR_WORKSPACE before any launch.  The call takes the path
+ * snack_spmm_fwd would take with a 32 MiB workspace: a layer on the
+ * tensor-core path whose scratch for this batch exceeds it runs on the gather
+ * kernels instead (same results within the tolerance contract, not bit for
+ * bit).  The first call on a device
  * looks up the array's device address (with that device current), so make it
  * before any stream capture.  All calls share the array: calls that overlap on
  * the GPU race, so order them (one stream, or events).  Allocates nothing.

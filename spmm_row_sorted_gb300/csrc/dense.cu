@@ -682,7 +682,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 }  // namespace
 
 bool dense_layer(int32_t out_f, int32_t in_f, int64_t nnz, int32_t max_batch, snack_dtype val_t) {
-  return val_t == SNACK_BF16 && max_batch >= kDenseMinBatch && (double)nnz >= 0.25 * (double)out_f * (double)in_f &&
+  return val_t == SNACK_BF16 && max_batch >= kDenseMinBatch && (double)nnz >= kDenseMinDensity * (double)out_f * (double)in_f &&
          out_f % 8 == 0 && in_f % 8 == 0 && out_f <= 65536 && in_f <= 65536;
 }
 
