@@ -686,9 +686,7 @@ def _oracle_us(oracle, lay, x64, dy64, op: str, budget_terms: float = 3e7) -> tu
 
 def _layer_rows(name, lay, batch, ours, dense, mask, oracle_t, peak, cores):
     """Result records of one layer at one batch."""
-    from spmm_row_sorted_gb300 import workloads as wl
-
-    c = wl.CONFIGS[name]
+    c = _config(name)
     s_v, s_x = ACT_BYTES[lay.val_dtype], ACT_BYTES[c["act_dtype"]]
     byts = alg_bytes(lay.nnz, batch, lay.out_f, lay.in_f, s_v=s_v, s_x=s_x)
     out = []
@@ -708,11 +706,24 @@ def _layer_rows(name, lay, batch, ours, dense, mask, oracle_t, peak, cores):
     return out
 
 
+# The 16384^2 layer with a constant fan-in of 164 (99 % sparse), as the
+# structured DST variant keeps it: not one of the five workloads, timed in the
+# c4 sweep beside them.
+FANIN_CONFIG = dict(name="16384x16384 constant fan-in 164 (99%), fp32, batch 32", out_f=16384, in_f=16384,
+                    val_dtype="f32", act_dtype="f32", batches=(32,), ops=("fwd", "dx", "dw"))
+
+
+def _config(name):
+    from spmm_row_sorted_gb300 import workloads as wl
+
+    return FANIN_CONFIG if name == "c4-fanin" else wl.CONFIGS[name]
+
+
 def _bench_layer(torch, F, snack, timer, name, lay, batch, ops, reps, dev, oracle, cores):
     """Times our ops and the two dense comparators on one layer and batch."""
     from spmm_row_sorted_gb300 import workloads as wl
 
-    c = wl.CONFIGS[name]
+    c = _config(name)
     act = c["act_dtype"]
     tdt = torch.float32 if act == "f32" else torch.bfloat16
     acts = wl.make_acts(batch, lay.in_f, lay.out_f, act, seed=0)
@@ -925,8 +936,12 @@ def run_configs(args):
     torch.backends.cudnn.allow_tf32 = False
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    snack_build.build()
-    snack.load()
+    if args.no_fan_in_path:  # a copy of the library whose constant-fan-in layers take the general kernels
+        snack.load(snack_build.build(extra_flags=["-DSNACK_NO_FAN_IN_PATH"],
+                                     out_dir=os.path.join(ROOT, "spmm_row_sorted_gb300", "_build", "no_fan_in")))
+    else:
+        snack_build.build()
+        snack.load()
     peak, peak_kind = measured_peak_gbs()
     oracle, cores = None, None
     if not args.no_cpu_baseline:
@@ -940,8 +955,11 @@ def run_configs(args):
     records = []
     with ClockSampler(0) as clk:
         for name in names:
-            c = wl.CONFIGS[name]
-            layers = [wl.config_layer(name, layer_index=i) for i in range(len(c.get("layers", [None])))]
+            c = _config(name)
+            if name == "c4-fanin":
+                layers = [wl.make_layer(16384, 16384, fan_in=164, val_std=0.02, val_dtype="f32", seed=0)]
+            else:
+                layers = [wl.config_layer(name, layer_index=i) for i in range(len(c.get("layers", [None])))]
             ops = ["fwd"] if c["ops"] == ("fwd",) else ["fwd", "dx", "dw", "bwd"]
             for lay in layers:
                 for batch in c["batches"]:
@@ -1112,6 +1130,8 @@ def main(argv=None):
                     help="per-workload sweep instead of the step bench: 'all' or a list like c1,c4")
     ap.add_argument("--configs-out", default=None, help="--configs: also write a markdown table here")
     ap.add_argument("--reps", type=int, default=200, help="--configs: timed reps per op")
+    ap.add_argument("--no-fan-in-path", action="store_true",
+                    help="--configs: time a library copy built without the constant-fan-in forward (for comparison)")
     ap.add_argument("--gather-ceiling", action="store_true",
                     help="time the gather-route probes on the 16384^2 layer at batch 32 and exit")
     ap.add_argument("--profile", action="store_true",

@@ -132,7 +132,11 @@ snack_status snack_query_sizes(int32_t out_f, int32_t in_f, int64_t nnz, int32_t
  * `ws` (device, 256-byte aligned) is scratch.  With validate != 0 the pattern
  * is checked on the device (ranges, strict order) and the call synchronises
  * `stream` to return SNACK_ERR_OUT_OF_RANGE or SNACK_ERR_UNSORTED; with
- * validate == 0 an invalid pattern gives undefined results.
+ * validate == 0 an invalid pattern gives undefined results.  When nnz is a
+ * multiple of out_f the call also checks on the device whether every row
+ * holds nnz / out_f stored weights (a constant fan-in, as Structured RigL
+ * keeps and snack_restructure_rows preserves) and synchronises `stream` once
+ * to read the answer; such layers run their forward with whole rows per warp.
  * The handle is bound to the CUDA device current at this call.
  */
 snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f, int64_t nnz,

@@ -74,6 +74,9 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
 bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
 size_t colview_hist_bytes(int64_t nnz);
 
+// *flag = 1 unless rp[r] == r * K for every r <= out_f (a constant fan-in of K).
+cudaError_t check_fan_in(const int32_t *rp, int32_t out_f, int32_t K, uint32_t *flag, cudaStream_t s);
+
 // dst[i] = (uint16_t)src[i] for i < n (the plan's 16-bit index copies); nothing when dst is null.
 cudaError_t pack16(const int32_t *src, int64_t n, uint16_t *dst, cudaStream_t s);
 
@@ -184,6 +187,7 @@ struct snack_layer {
   cudaEvent_t ev_colview = nullptr;
   bool colview_pending = false;
   bool dense = false;   // the layer takes the tensor-core path for wide batches
+  int32_t fan_in = 0;   // K when every row holds K stored weights (rows at r * K), else 0
 };
 
 namespace snack {

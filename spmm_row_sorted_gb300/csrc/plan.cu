@@ -585,6 +585,20 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
   return joined(cudaGetLastError());
 }
 
+// *flag |= 1 when some row r does not start at r * K (K stored weights per row)
+__global__ void k_check_fan_in(const int32_t *__restrict__ rp, int32_t out_f, int32_t K, uint32_t *flag) {
+  pdl_wait();
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r <= out_f && rp[r] != (int64_t)r * K) atomicOr(flag, 1u);
+}
+
+cudaError_t check_fan_in(const int32_t *rp, int32_t out_f, int32_t K, uint32_t *flag, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  launch_pdl(k_check_fan_in, grid_for((int64_t)out_f + 1, 256), 256, 0, s, rp, out_f, K, flag);
+  return cudaGetLastError();
+}
+
 cudaError_t pack16(const int32_t *src, int64_t n, uint16_t *dst, cudaStream_t s) {
   if (n > 0 && dst) launch_pdl(k_pack16, grid_for(n, 256), 256, 0, s, src, n, dst);
   return cudaGetLastError();

@@ -215,6 +215,10 @@ snack_status run_fwd(snack_handle h, const int32_t *col, const void *val, const 
   p.act = act;
   p.pre_in = nullptr;
   p.pre_out = pre_out;
+  if (h->fan_in > 0) {  // constant fan-in: whole rows per warp, no split rows
+    SNACK_CUDA(run_ell<T>(p, bg, h->fan_in, s));
+    return SNACK_OK;
+  }
   SNACK_CUDA(run_spmm<T>(p, bg, false, false, s));
   return SNACK_OK;
 }
@@ -455,6 +459,19 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
     if (flag & 2u) return SNACK_ERR_UNSORTED;
   }
   SNACK_CUDA(build_plan(out_f, in_f, nnz, row, col, p, lay.gf, lay.gt, ws, s, kPlanNothingReady));
+  // a constant fan-in (every row K stored weights) lets the forward take whole
+  // rows per warp: checked on the device and read back once
+  int32_t fan_in = 0;
+#ifndef SNACK_NO_FAN_IN_PATH  // a comparison build: every layer takes the general kernels
+  if (nnz > 0 && nnz % out_f == 0) {
+    const int32_t K = (int32_t)(nnz / out_f);
+    SNACK_CUDA(check_fan_in(p.rp, out_f, K, p.flags + 1, s));
+    uint32_t bad = 1;
+    SNACK_CUDA(cudaMemcpyAsync(&bad, p.flags + 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    SNACK_CUDA(cudaStreamSynchronize(s));
+    fan_in = bad ? 0 : K;
+  }
+#endif
   snack_layer *h = new (std::nothrow) snack_layer;
   if (!h) return SNACK_ERR_INVALID_ARG;
   h->device = dev;
@@ -469,6 +486,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   h->plan_bytes = plan_bytes;
   h->num_sms = sms > 0 ? sms : 1;
   h->dense = lay.dense;
+  h->fan_in = fan_in;
   *out_handle = h;
   return SNACK_OK;
 }
@@ -671,6 +689,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.cv_offs = h->p.cv_offs;
   a.cv_hist = h->p.cv_hist;
   snack_status st = run_restructure(a, ws, ws_bytes, s);
+  if (st == SNACK_OK) h->fan_in = 0;  // regrowth lands in any row: row counts change
   if (st == SNACK_OK) {
     bool deferred = false;
     if (build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,

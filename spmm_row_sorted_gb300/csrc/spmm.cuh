@@ -640,6 +640,167 @@ __global__ void __launch_bounds__(256) k_sddmm(int64_t nnz, const int32_t *__res
   for (int q = tid; q < n; q += 256) dw[k0 + q] = s_out[q];
 }
 
+// Weight gradient in storage (row) order when one batch tile covers the
+// batch: a slot keeps the dY slice of its current row in registers and
+// reloads it only when its next stored weight starts a new row, so each
+// stored weight gathers one activation slice (X[col]) instead of two.
+// Chunks, staging and output as in k_sddmm.
+template <typename TA, int V, int G>
+__global__ void __launch_bounds__(256) k_sddmm_rows(int64_t nnz, const int32_t *__restrict__ row,
+                                                    const int32_t *__restrict__ col, int32_t out_f, int32_t in_f,
+                                                    const TA *__restrict__ xt, const TA *__restrict__ dyt, int ldx,
+                                                    int chunk, float *__restrict__ dw) {
+  pdl_wait();
+  constexpr int kSlots = 32 / G;
+  constexpr int kU = DwUnroll<V, G>::value;
+  const int per_warp = (chunk + 7) / 8;
+  __shared__ uint32_t s_row[kDwChunk];
+  __shared__ uint32_t s_col[kDwChunk];
+  __shared__ float s_out[kDwChunk];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane / G, g = lane % G;
+  const int64_t k0 = (int64_t)blockIdx.x * chunk;
+  const int n = (int)min((int64_t)chunk, nnz - k0);
+  const uint32_t rmax = (uint32_t)(out_f - 1), cmax = (uint32_t)(in_f - 1);
+  for (int q0 = 0; q0 < n; q0 += 4 * 256) {
+    uint32_t rr[4], cc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int q = q0 + u * 256 + tid;
+      rr[u] = q < n ? (uint32_t)ld_stream(row + k0 + q) : 0u;
+      cc[u] = q < n ? (uint32_t)ld_stream(col + k0 + q) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int q = q0 + u * 256 + tid;
+      if (q < n) {
+        s_row[q] = rr[u] < rmax ? rr[u] : rmax;
+        s_col[q] = cc[u] < cmax ? cc[u] : cmax;
+      }
+    }
+  }
+  __syncthreads();
+  const int wq0 = min(n, warp * per_warp), wq1 = min(n, wq0 + per_warp);
+  uint32_t cur = 0xFFFFFFFFu;  // the row whose dY slice dyv holds
+  float dyv[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) dyv[e] = 0.f;
+  const TA *xb = xt + g * V;
+  const TA *db = dyt + g * V;
+  for (int base = wq0; base < wq1; base += kSlots * kU) {
+    uint32_t c[kU];
+    float xv[kU][V];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int q = base + u * kSlots + slot;
+      c[u] = q < wq1 ? s_col[q] : 0u;
+      Slice<TA, V>::load(xb + (size_t)c[u] * ldx, xv[u]);
+    }
+    float acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int q = base + u * kSlots + slot;
+      const uint32_t r = q < wq1 ? s_row[q] : cur;
+      if (r != cur) {  // the G lanes of a slot take this branch together
+        Slice<TA, V>::load(db + (size_t)r * ldx, dyv);
+        cur = r;
+      }
+      acc[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[u] = fmaf(dyv[e], xv[u][e], acc[u]);
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+    if (g == 0) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int q = base + u * kSlots + slot;
+        if (q < wq1) s_out[q] = acc[u];
+      }
+    }
+  }
+  __syncthreads();
+  for (int q = tid; q < n; q += 256) dw[k0 + q] = s_out[q];
+}
+
+// Forward of a layer with a constant fan-in (every row holds K stored
+// weights, rows at k = r K): kEllRows whole rows per CTA, a warp per row at a
+// time, no merge-path search, no split rows, no fix-up.  The warp loads its
+// row's indices and weights 32 at a time (one per lane), slots of G lanes
+// take them in turn and gather their Xt slices; the row sums reduce across
+// slots into shared memory, and outputs leave as contiguous runs of Y[b, r0:].
+constexpr int kEllRows = 32;
+constexpr int kEllThreads = 256;
+
+template <typename TA, typename TV, int V, int G>
+__global__ void __launch_bounds__(kEllThreads) k_ell_fwd(SpmmParams P, BatchGeom bg, int32_t K) {
+  pdl_wait();
+  constexpr int kSlots = 32 / G;
+  constexpr int kSteps = 32 / kSlots;           // slot steps per group of 32 stored weights
+  constexpr int kU = kSteps < 4 ? kSteps : 4;   // steps in flight
+  extern __shared__ __align__(16) float ys[];  // [kEllRows][bt + 1]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slot = lane / G, g = lane % G;
+  const int bt = bg.bt, ys_ld = bt + 1;
+  const int r0 = blockIdx.x * kEllRows, b0 = blockIdx.y * bt;
+  const TA *xt = reinterpret_cast<const TA *>(P.xt) + b0 + g * V;
+  const TV *val = reinterpret_cast<const TV *>(P.val);
+  const uint32_t src_max = (uint32_t)(P.n_src - 1);
+  for (int rr = warp; rr < kEllRows; rr += kEllThreads / 32) {
+    const int r = r0 + rr;
+    if (r >= P.n_rows) break;
+    const int64_t k0 = (int64_t)r * K, k1 = k0 + K;
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    for (int64_t kb = k0; kb < k1; kb += 32) {
+      const int64_t k = kb + lane;
+      uint32_t c = 0u;
+      float v = 0.f;
+      if (k < k1) {
+        c = P.idx16 ? (uint32_t)ld_stream(P.idx16 + k) : (uint32_t)ld_stream(P.idx + k);
+        c = c < src_max ? c : src_max;
+        v = to_f32(ld_stream(val + k));
+      }
+#pragma unroll
+      for (int s0 = 0; s0 < kSteps; s0 += kU) {
+        float x[kU][V], vv[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int e = (s0 + u) * kSlots + slot;  // < 32
+          const uint32_t cc = __shfl_sync(0xffffffffu, c, e);
+          vv[u] = __shfl_sync(0xffffffffu, v, e);
+          Slice<TA, V>::load(xt + (size_t)cc * bg.ldx, x[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int e = 0; e < V; ++e) acc[e] = fmaf(vv[u], x[u][e], acc[e]);
+      }
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (slot == 0)
+#pragma unroll
+      for (int e = 0; e < V; ++e) ys[rr * ys_ld + g * V + e] = acc[e];
+  }
+  __syncthreads();
+  TA *y = reinterpret_cast<TA *>(P.y);
+  const int nr = min(kEllRows, P.n_rows - r0);
+  const int bmax = min(bt, P.batch - b0);
+  for (int i = threadIdx.x; i < nr * bmax; i += kEllThreads) {
+    const int b = i / nr, q = i % nr;  // consecutive threads: consecutive outputs of one batch row
+    float s = ys[q * ys_ld + b];
+    if (P.bias) s = P.bias[r0 + q] + s;
+    const size_t off = (size_t)(b0 + b) * P.n_rows + r0 + q;
+    y[off] = spmm_epilogue<TA>(P, s, off);
+  }
+}
+
 // ------------------------------------------------------------------ host
 
 template <typename TA, typename TV, int V, int G, bool kGV, bool kFuse>
@@ -670,6 +831,31 @@ cudaError_t launch_spmm(const SpmmParams &p, const BatchGeom &bg, cudaStream_t s
   return cudaErrorInvalidValue;
 }
 
+template <typename TA, typename TV, int V, int G>
+cudaError_t launch_ell_v(const SpmmParams &p, const BatchGeom &bg, int32_t K, cudaStream_t s) {
+  const size_t smem = (size_t)kEllRows * (bg.bt + 1) * sizeof(float);
+  cudaError_t e = raise_smem_limit(k_ell_fwd<TA, TV, V, G>, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.n_rows + kEllRows - 1) / kEllRows), bg.n_btiles);
+  launch_pdl(k_ell_fwd<TA, TV, V, G>, grid, kEllThreads, smem, s, p, bg, K);
+  return cudaGetLastError();
+}
+
+template <typename TA, typename TV>
+cudaError_t launch_ell(const SpmmParams &p, const BatchGeom &bg, int32_t K, cudaStream_t s) {
+  constexpr int VV = ActTraits<TA>::kVec;
+  if (bg.V == 1) return launch_ell_v<TA, TV, 1, 1>(p, bg, K, s);
+  switch (bg.G) {
+    case 1: return launch_ell_v<TA, TV, VV, 1>(p, bg, K, s);
+    case 2: return launch_ell_v<TA, TV, VV, 2>(p, bg, K, s);
+    case 4: return launch_ell_v<TA, TV, VV, 4>(p, bg, K, s);
+    case 8: return launch_ell_v<TA, TV, VV, 8>(p, bg, K, s);
+    case 16: return launch_ell_v<TA, TV, VV, 16>(p, bg, K, s);
+    case 32: return launch_ell_v<TA, TV, VV, 32>(p, bg, K, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <typename TA, int V, int G>
 cudaError_t launch_sddmm_v(int64_t nnz, const int32_t *row, const int32_t *col, int32_t out_f, int32_t in_f,
                            const TA *xt, const TA *dyt, const BatchGeom &bg, float *dw, int num_sms,
@@ -683,8 +869,12 @@ cudaError_t launch_sddmm_v(int64_t nnz, const int32_t *row, const int32_t *col, 
   if (chunk > kDwChunk) chunk = kDwChunk;
   int64_t blocks = (nnz + chunk - 1) / chunk;
   int n_chunks = bg.ldx / bg.bt;
-  launch_pdl(k_sddmm<TA, V, G>, (unsigned)blocks, 256, 0, s, nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks,
-                                                     (int)chunk, dw);
+  if (n_chunks == 1)  // one batch tile: each slot keeps its row's dY slice
+    launch_pdl(k_sddmm_rows<TA, V, G>, (unsigned)blocks, 256, 0, s, nnz, row, col, out_f, in_f, xt, dyt, bg.ldx,
+               (int)chunk, dw);
+  else
+    launch_pdl(k_sddmm<TA, V, G>, (unsigned)blocks, 256, 0, s, nnz, row, col, out_f, in_f, xt, dyt, bg.ldx, n_chunks,
+               (int)chunk, dw);
   return cudaGetLastError();
 }
 
@@ -743,6 +933,9 @@ cudaError_t run_sddmm(int64_t nnz, const int32_t *row, const int32_t *col, int32
                       const T *xt, const T *dyt, const BatchGeom &bg, float *dw, int num_sms, cudaStream_t s);
 template <typename T>
 cudaError_t run_transpose(const T *a, int batch, int n, T *at, int ldx, cudaStream_t s);
+// forward of a constant-fan-in layer (K stored weights in every row)
+template <typename T>
+cudaError_t run_ell(const SpmmParams &p, const BatchGeom &bg, int32_t K, cudaStream_t s);
 template <typename T>
 cudaError_t run_colsum(const T *a, int batch, int n, float *out, cudaStream_t s);
 template <typename T>

@@ -18,6 +18,11 @@ cudaError_t run_sddmm<bf16>(int64_t nnz, const int32_t *row, const int32_t *col,
 }
 
 template <>
+cudaError_t run_ell<bf16>(const SpmmParams &p, const BatchGeom &bg, int32_t K, cudaStream_t s) {
+  return launch_ell<bf16, bf16>(p, bg, K, s);
+}
+
+template <>
 cudaError_t run_transpose<bf16>(const bf16 *a, int batch, int n, bf16 *at, int ldx, cudaStream_t s) {
   return launch_transpose<bf16>(a, batch, n, at, ldx, s);
 }

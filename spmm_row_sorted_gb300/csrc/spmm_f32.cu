@@ -18,6 +18,11 @@ cudaError_t run_sddmm<float>(int64_t nnz, const int32_t *row, const int32_t *col
 }
 
 template <>
+cudaError_t run_ell<float>(const SpmmParams &p, const BatchGeom &bg, int32_t K, cudaStream_t s) {
+  return launch_ell<float, float>(p, bg, K, s);
+}
+
+template <>
 cudaError_t run_transpose<float>(const float *a, int batch, int n, float *at, int ldx, cudaStream_t s) {
   return launch_transpose<float>(a, batch, n, at, ldx, s);
 }

@@ -641,6 +641,31 @@ def test_index_width_boundaries(shape):
     restructure_and_check(lay, nnz // 10, seed=1, step=1, acts=acts)
 
 
+# ---------------------------------------------------------------- constant fan-in forward
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", [(300, 700, 37, 9), (1000, 500, 1, 33), (64, 4000, 400, 130), (2000, 3000, 30, 300),
+                                  (8, 64, 48, 16)])
+def test_constant_fan_in_forward(dtype, case):
+    # Every row holds K stored weights: the forward takes whole rows per warp
+    # (no merge path, no split rows); batches above 8 take that kernel, every
+    # op still matches the oracle, and so does the same layer after a per-row
+    # restructure (which keeps the fan-in).
+    out_f, in_f, K, batch = case
+    lay = wl.make_layer(out_f, in_f, fan_in=K, val_std=0.3, val_dtype=dtype, seed=K + batch, bias="normal")
+    acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+    check_layer_ops(lay, acts)
+    restructure_rows_and_check(lay, max(1, K // 4), seed=3, step=2, acts=acts)
+
+
+def test_row_count_multiple_of_out_f_without_constant_fan_in():
+    # nnz = 3 * out_f but the rows differ in length: the tile kernels run
+    lay = wl.make_layer(500, 700, nnz=1500, zipf_s=1.1, val_std=0.3, val_dtype="f32", seed=5, bias="normal")
+    assert len(set(np.bincount(lay.row, minlength=500).tolist())) > 1
+    for batch in (9, 32):
+        check_layer_ops(lay, wl.make_acts(batch, 700, 500, "f32", seed=batch))
+
+
 # ---------------------------------------------------------------- per-row (constant fan-in) restructure
 
 def restructure_rows_and_check(lay: wl.Layer, n_per_row: int, seed: int, step: int, acts=None):
