@@ -516,16 +516,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc(const __grid_constant__ CUte
   if (warp == 0) tmem_dealloc(tmem, tcols);
 }
 
-// y[b][o] = bf16((bias[o]) + sum_s part[s][b][o]), s ascending
-__global__ void k_tc_finish(const float *__restrict__ part, int n_split, int batch, int n_out,
-                            const float *__restrict__ bias, bf16 *__restrict__ y) {
+// y[b][o] = bf16((bias[o]) + sum_s part[s][b][o]), s ascending; four outputs
+// per thread (n_out is a multiple of 8, so a group never crosses a row)
+__global__ void __launch_bounds__(256) k_tc_finish(const float *__restrict__ part, int n_split, int batch, int n_out,
+                                                   const float *__restrict__ bias, bf16 *__restrict__ y) {
   pdl_wait();
-  const int64_t total = (int64_t)batch * n_out;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    float s = part[i];
-    for (int k = 1; k < n_split; ++k) s += part[(size_t)k * total + i];
-    if (bias) s = bias[i % n_out] + s;
-    y[i] = __float2bfloat16_rn(s);
+  const int64_t total = (int64_t)batch * n_out, groups = total / 4;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += (int64_t)gridDim.x * blockDim.x) {
+    float4 a = __ldcs(reinterpret_cast<const float4 *>(part) + g);
+    for (int k = 1; k < n_split; ++k) {
+      const float4 c = __ldcs(reinterpret_cast<const float4 *>(part + (size_t)k * total) + g);
+      a.x += c.x;
+      a.y += c.y;
+      a.z += c.z;
+      a.w += c.w;
+    }
+    if (bias) {  // the caller's bias and output need only their element alignment
+      const float *bb = bias + (g * 4) % n_out;
+      a.x = bb[0] + a.x;
+      a.y = bb[1] + a.y;
+      a.z = bb[2] + a.z;
+      a.w = bb[3] + a.w;
+    }
+    bf16 *yo = y + g * 4;
+    yo[0] = __float2bfloat16_rn(a.x);
+    yo[1] = __float2bfloat16_rn(a.y);
+    yo[2] = __float2bfloat16_rn(a.z);
+    yo[3] = __float2bfloat16_rn(a.w);
   }
 }
 
@@ -756,7 +773,7 @@ snack_status dense_fwd(snack_layer *h, const void *val, const void *x, int32_t b
     return SNACK_ERR_CUDA;
   if (launch_tc<kModeFwd>(mx, mx, mm, mk, a, h->num_sms, s) != cudaSuccess) return SNACK_ERR_CUDA;
   if (a.n_split > 1) {
-    launch_pdl(k_tc_finish, grid_of((int64_t)batch * h->out_f, 256), 256, 0, s, (const float *)a.part, a.n_split, batch,
+    launch_pdl(k_tc_finish, grid_of((int64_t)batch * h->out_f / 4, 256), 256, 0, s, (const float *)a.part, a.n_split, batch,
                h->out_f, bias, a.out);
     if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   }
@@ -790,7 +807,7 @@ snack_status dense_dx(snack_layer *h, const void *val, const void *dy, int32_t b
     return SNACK_ERR_CUDA;
   if (launch_tc<kModeDx>(md, md, mm, mk, a, h->num_sms, s) != cudaSuccess) return SNACK_ERR_CUDA;
   if (a.n_split > 1) {
-    launch_pdl(k_tc_finish, grid_of((int64_t)batch * h->in_f, 256), 256, 0, s, (const float *)a.part, a.n_split, batch,
+    launch_pdl(k_tc_finish, grid_of((int64_t)batch * h->in_f / 4, 256), 256, 0, s, (const float *)a.part, a.n_split, batch,
                h->in_f, (const float *)nullptr, a.out);
     if (cudaGetLastError() != cudaSuccess) return SNACK_ERR_CUDA;
   }
