@@ -509,6 +509,68 @@ def test_backward_equals_separate_calls_bitwise(batch, out_f, in_f, nnz):
     L.close()
 
 
+# ---------------------------------------------------------------- shared-memory limits
+
+def _staged_layers():
+    # batch 8 fp32, column view: dY of 3000 outputs staged (94 KB per CTA) and of 2000 outputs
+    # (62.5 KB), both above the 48 KB default limit, through the same small-batch kernels
+    big = wl.make_layer(3000, 600, nnz=900000, val_dtype="f32", seed=4, bias="normal")
+    small = wl.make_layer(2000, 600, nnz=600000, val_dtype="f32", seed=5, bias="normal")
+    return big, small
+
+
+def test_shared_memory_limits_only_rise():
+    # One thread: a backward on the big layer raises the fused kernel's limit, an input
+    # gradient on the smaller layer must not lower it, and the big layer's backward runs
+    # again with the same bits; then two host threads drive the two layers at once.
+    import threading
+
+    big, small = _staged_layers()
+    acts_b = wl.make_acts(8, 600, 3000, "f32", seed=6)
+    acts_s = wl.make_acts(8, 600, 2000, "f32", seed=7)
+
+    def make(lay):
+        row, col, val, bias = layer_tensors(lay)
+        return snack.SparseLinear(lay.out_f, lay.in_f, row, col, val, bias, max_batch=8)
+
+    B, S = make(big), make(small)
+    xb, dyb = act_tensor(acts_b.x, "f32"), act_tensor(acts_b.dy, "f32")
+    xs, dys = act_tensor(acts_s.x, "f32"), act_tensor(acts_s.dy, "f32")
+    first = [t.clone() for t in B.backward(xb, dyb)]
+    dx_s = S.grad_input(dys)
+    again = B.backward(xb, dyb)
+    torch.cuda.synchronize()
+    for a, b in zip(first, again):
+        assert torch.equal(a, b)
+    check_layer_ops(big, acts_b, ops=("dx", "dw"), got={"dx": first[0], "dw": first[1], "db": first[2]})
+    check_layer_ops(small, acts_s, ops=("dx",), got={"dx": dx_s})
+    ref_s = dx_s.clone()
+
+    errors = []
+
+    def drive(layer, x, dy, want, kind):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(20):
+                    got = layer.backward(x, dy, stream=st)[0] if kind == "bwd" else layer.grad_input(dy, stream=st)
+                st.synchronize()
+                if not torch.equal(got, want):
+                    errors.append(kind + " differs")
+        except Exception as e:  # a launch refused for a lowered limit surfaces here
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=drive, args=(B, xb, dyb, first[0], "bwd")),
+               threading.Thread(target=drive, args=(S, xs, dys, ref_s, "dx"))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    B.close()
+    S.close()
+
+
 # ---------------------------------------------------------------- rows split between CTAs
 
 def test_split_rows_repeat_calls_bitwise():
