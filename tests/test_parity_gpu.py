@@ -673,6 +673,28 @@ def test_dense_path_bias_rounded_once():
     check_layer_ops(lay, acts, ops=("fwd",))
 
 
+@pytest.mark.parametrize("case", [(136, 200, 0.9, 16), (64, 264, 0.97, 255), (128, 384, 0.5, 256), (72, 136, 0.5, 257),
+                                  (128, 8192, 0.3, 32), (8192, 128, 0.3, 32)])
+def test_dense_path_tiles_and_splits(case):
+    # Nearly full 64-column blocks whose runs start at odd storage indices (the
+    # value loads straddle words), batch tiles at the edges (16, 255, 256, 257),
+    # one output tile with K split 8 ways (128 x 8192) and the input gradient's
+    # long K (8192 x 128): every op against the oracle.
+    out_f, in_f, density, batch = case
+    lay = wl.make_layer(out_f, in_f, density=density, val_std=0.2, val_dtype="bf16", seed=out_f + batch,
+                        bias="normal")
+    acts = wl.make_acts(batch, in_f, out_f, "bf16", seed=batch)
+    check_layer_ops(lay, acts)
+    check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
+
+
+def test_dense_path_after_per_row_restructure():
+    # the per-row restructure rewrites the columns of every row: the masks and
+    # value offsets of the tensor-core path are rebuilt from them
+    lay = wl.make_layer(128, 256, fan_in=96, val_std=0.2, val_dtype="bf16", seed=12, bias="normal")
+    restructure_rows_and_check(lay, 20, seed=6, step=1, acts=wl.make_acts(40, 256, 128, "bf16", seed=4))
+
+
 def test_dense_layer_narrow_batch_takes_gather_path():
     # the same dense layer at batch 8 (below the dense path's minimum), built for batch 64
     lay = wl.make_layer(256, 384, density=0.5, val_std=0.2, val_dtype="bf16", seed=3, bias="normal")
