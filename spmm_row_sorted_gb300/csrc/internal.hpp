@@ -21,13 +21,20 @@ struct PlanPtrs {
   uint32_t *flags;   // [64]          validation flags and small device scalars
   uint16_t *col16;   // [nnz]         16-bit copy of col (in_f <= 65536), else null
   uint16_t *rowt16;  // [nnz]         16-bit copy of row_t (out_f <= 65536), else null
-  // Scratch of the column view's rebuild after a restructure, which runs on
-  // the handle's second stream after the call has returned (so it cannot use
-  // the caller's workspace); present when colview_digits holds, else null.
-  uint32_t *cv_keys;  // [nnz] first-level scatter: packed (row, col) keys
-  uint32_t *cv_vals;  // [nnz] and their storage indices
-  uint32_t *cv_offs;  // digit-major first-level scatter offsets (colview_hist_bytes)
-  uint32_t *cv_hist;  // their tile histogram (colview_hist_bytes)
+  // Incremental update of the column view after a restructure (present when
+  // the row and column bits fit 31 together): a second column view, written
+  // by the update while the current one is read (the handle swaps the two
+  // when the update is queued), and the update's scratch, which must outlive
+  // the call because the update runs on the handle's second stream.
+  int32_t *cp_alt, *tiles_t_alt, *row_t_alt, *src_t_alt;
+  uint16_t *rowt16_alt;
+  uint32_t *newidx;   // [nnz] output index of each stored weight (~0u: pruned)
+  uint32_t *gq;       // [cv_pmax] output index of each regrown weight, by acceptance rank
+  uint32_t *gc_key;   // [cv_pmax] regrown positions in column order, col << rbits | row
+  uint32_t *gc_q;     // [cv_pmax] and their acceptance ranks
+  uint64_t *cv_sums;  // kept entries per column-view tile (scan_temp_bytes<uint64_t>(nnz))
+  void *cv_bnd;       // bounds of the update's tiles of kScanTile entries (32 bytes per tile, and one more)
+  int64_t cv_pmax;    // most weights a restructure may prune and still update (else rebuild)
   // Moderately sparse bf16 layers (dense_layer): per 64-column block and row,
   // the stored-position mask (u64) and the storage index of the block's
   // first stored weight (dense.cu, build_tables); else null.
@@ -35,10 +42,11 @@ struct PlanPtrs {
 };
 
 struct PlanLayout {
-  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cvk, off_cvv,
-      off_cvo, off_cvh, off_tab, total;
+  size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cpa, off_tta,
+      off_rowta, off_srcta, off_rowt16a, off_newidx, off_gq, off_gck, off_gcq, off_cvs, off_cvb, off_tab, total;
   bool c16, r16;  // the 16-bit index copies exist
-  bool cv;        // the deferred column-view rebuild's scratch exists
+  bool cv;        // the second column view and the incremental update's scratch exist
+  int64_t cv_pmax;
   bool dense;     // the tensor-core path's mask and offset tables exist
   TileGeom gf, gt;
 };
@@ -51,28 +59,26 @@ size_t plan_build_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz);
 // names what is already in place: kPlanNothingReady (create),
 // kPlanRowsReady (the row offsets and the 16-bit column copy, written by a
 // restructure's merge), kPlanRowTilesReady (also the forward tiles: a
-// per-row restructure keeps every row's offsets).
+// per-row restructure keeps every row's offsets).  With colview = false the
+// column view is left alone (a restructure updates it itself).
 constexpr int kPlanNothingReady = 0, kPlanRowsReady = 1, kPlanRowTilesReady = 2;
-// With `aux` (and two events) after a restructure (kPlanRowsReady):
-//  * when the plan has the deferred scratch (PlanPtrs::cv_*), the forward
-//    tiles are cut on s and the column view is rebuilt on `aux` after s's
-//    work so far (ev_a), from the first-level offsets that the restructure
-//    left in cv_offs on `aux`; ev_b is recorded on `aux` when it is done and
-//    s does NOT wait for it (*deferred is set): the calls that read the column
-//    view wait for ev_b;
-//  * otherwise the forward tiles are cut on `aux` beside the column view on
-//    s, and s waits for them before returning.
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux = nullptr, cudaEvent_t ev_a = nullptr, cudaEvent_t ev_b = nullptr,
-                       bool *deferred = nullptr);
+                       int ready, bool colview = true);
+
+// Merge-path split points of a row- or column-offset array (k_tiles).
+cudaError_t cut_tiles(const int32_t *ptr, int32_t n_rows, int64_t nnz, const TileGeom &g, int32_t *tiles,
+                      cudaStream_t s);
+
+// The second column view and the update's scratch exist when both index
+// widths fit 31 bits together; the update takes up to a quarter of nnz.
+bool colview_update_ok(int32_t out_f, int32_t in_f, int64_t nnz);
 
 // The column view's first level scatters (row, col) by the column's high 8
 // bits when 9..17-bit columns and row + column bits fit 32: then *shift =
 // column bits - 8 and the digit of an entry is (col >> shift) & 0xFF, per
 // tile of 2048 entries (the histogram is digit-major: [256][tiles]).
 bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift);
-size_t colview_hist_bytes(int64_t nnz);
 
 // *flag = 1 unless rp[r] == r * K for every r <= out_f (a constant fan-in of K).
 cudaError_t check_fan_in(const int32_t *rp, int32_t out_f, int32_t K, uint32_t *flag, cudaStream_t s);
@@ -92,26 +98,28 @@ struct RestructureArgs {
   uint64_t seed, step;
   const int32_t *row, *col;
   const void *val;
-  const int32_t *rp_old;  // row offsets of the input pattern (from the plan)
-  int32_t *rp_new;        // row offsets of the output, written by the merge (may alias rp_old: the
-                          // draws that read rp_old are ordered before the merge on the stream)
-  uint16_t *col16_new;    // 16-bit copy of col_out written by the merge, or null
   int32_t *row_out, *col_out;
   void *val_out;
   int32_t *src_out;  // may be null
+  // The plan of the input pattern: the draws read its row offsets and 16-bit
+  // columns, the merge rewrites them (and the forward tiles) for the output;
+  // when `update` is set the column view is updated into the plan's second
+  // view on `aux` after the call returns (the caller then swaps the views),
+  // else it is rebuilt on s.
+  const PlanPtrs *plan;
+  TileGeom gf, gt;
+  bool update;
   uint32_t *host_counts;  // pinned, mapped host memory, 4 words: a draw chunk's accepted count, table and bucket overflow
   uint32_t *counts_dev;   // the same words' device address (written by a kernel, no copy)
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
-  cudaStream_t aux;          // second stream of the handle (regrow branch)
+  cudaStream_t aux;          // second stream of the handle (regrow branch, column-view update)
   cudaEvent_t ev_fork, ev_join;
-  // When set (colview_digits holds), the column view's first-level histogram
-  // and offsets of the new pattern are made into these plan arrays on `aux`,
-  // beside the merge, for the column-view rebuild that follows on `aux`.
-  uint32_t *cv_offs, *cv_hist;
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
-// Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA.
-snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
+// Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA;
+// *updated is set when the column view was queued into the plan's second
+// view (the caller swaps the views).
+snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s, bool *updated);
 
 // Tensor-core path for moderately sparse bf16 layers (dense.cu): layers with
 // >= 8 % of W stored, feature counts multiples of 8 and <= 65536, created
@@ -181,7 +189,7 @@ struct snack_layer {
   cudaEvent_t counts_ready = nullptr;
   cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  // The column view of the last restructure is rebuilt on `aux` after the
+  // The column view of the last restructure is updated on `aux` after the
   // call returns; ev_colview marks its end and the calls that read the
   // column view make their stream wait for it.
   cudaEvent_t ev_colview = nullptr;

@@ -365,17 +365,34 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
   if (L.c16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
   L.off_rowt16 = o;
   if (L.r16) o += align_up(sizeof(uint16_t) * (size_t)(nnz > 0 ? nnz : 1), kAlign);
-  L.cv = colview_digits(out_f, in_f, nnz, nullptr);
-  L.off_cvk = L.off_cvv = L.off_cvo = L.off_cvh = o;
+  L.cv = colview_update_ok(out_f, in_f, nnz);
+  L.cv_pmax = L.cv ? (nnz + 3) / 4 : 0;
+  L.off_cpa = L.off_tta = L.off_rowta = L.off_srcta = L.off_rowt16a = L.off_newidx = L.off_gq = L.off_gck =
+      L.off_gcq = L.off_cvs = L.off_cvb = o;
   if (L.cv) {
-    L.off_cvk = o;
-    o += align_up(sizeof(uint32_t) * (size_t)nnz, kAlign);
-    L.off_cvv = o;
-    o += align_up(sizeof(uint32_t) * (size_t)nnz, kAlign);
-    L.off_cvo = o;
-    o += colview_hist_bytes(nnz);
-    L.off_cvh = o;
-    o += colview_hist_bytes(nnz);
+    const size_t n = (size_t)nnz, pm = (size_t)L.cv_pmax;
+    L.off_cpa = o;
+    o += align_up(sizeof(int32_t) * ((size_t)in_f + 1), kAlign);
+    L.off_tta = o;
+    o += align_up(sizeof(int32_t) * 2 * ((size_t)L.gt.n_tiles + 1), kAlign);
+    L.off_rowta = o;
+    o += align_up(sizeof(int32_t) * n, kAlign);
+    L.off_srcta = o;
+    o += align_up(sizeof(int32_t) * n, kAlign);
+    L.off_rowt16a = o;
+    if (L.r16) o += align_up(sizeof(uint16_t) * n, kAlign);
+    L.off_newidx = o;
+    o += align_up(sizeof(uint32_t) * n, kAlign);
+    L.off_gq = o;
+    o += align_up(sizeof(uint32_t) * pm, kAlign);
+    L.off_gck = o;
+    o += align_up(sizeof(uint32_t) * pm, kAlign);
+    L.off_gcq = o;
+    o += align_up(sizeof(uint32_t) * pm, kAlign);
+    L.off_cvs = o;
+    o += scan_temp_bytes<uint64_t>(nnz);
+    L.off_cvb = o;
+    o += align_up(32 * (size_t)(ceil_div(nnz, kScanTile) + 1), kAlign);
   }
   L.dense = dense;
   L.off_tab = o;
@@ -396,10 +413,18 @@ PlanPtrs plan_ptrs(const PlanLayout &L, void *base) {
   p.flags = reinterpret_cast<uint32_t *>(b + L.off_flags);
   p.col16 = L.c16 ? reinterpret_cast<uint16_t *>(b + L.off_col16) : nullptr;
   p.rowt16 = L.r16 ? reinterpret_cast<uint16_t *>(b + L.off_rowt16) : nullptr;
-  p.cv_keys = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvk) : nullptr;
-  p.cv_vals = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvv) : nullptr;
-  p.cv_offs = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvo) : nullptr;
-  p.cv_hist = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvh) : nullptr;
+  p.cp_alt = L.cv ? reinterpret_cast<int32_t *>(b + L.off_cpa) : nullptr;
+  p.tiles_t_alt = L.cv ? reinterpret_cast<int32_t *>(b + L.off_tta) : nullptr;
+  p.row_t_alt = L.cv ? reinterpret_cast<int32_t *>(b + L.off_rowta) : nullptr;
+  p.src_t_alt = L.cv ? reinterpret_cast<int32_t *>(b + L.off_srcta) : nullptr;
+  p.rowt16_alt = L.cv && L.r16 ? reinterpret_cast<uint16_t *>(b + L.off_rowt16a) : nullptr;
+  p.newidx = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_newidx) : nullptr;
+  p.gq = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gq) : nullptr;
+  p.gc_key = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gck) : nullptr;
+  p.gc_q = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gcq) : nullptr;
+  p.cv_sums = L.cv ? reinterpret_cast<uint64_t *>(b + L.off_cvs) : nullptr;
+  p.cv_bnd = L.cv ? reinterpret_cast<void *>(b + L.off_cvb) : nullptr;
+  p.cv_pmax = L.cv_pmax;
   p.tables = L.dense ? reinterpret_cast<void *>(b + L.off_tab) : nullptr;
   return p;
 }
@@ -470,19 +495,25 @@ bool colview_digits(int32_t out_f, int32_t in_f, int64_t nnz, int *shift) {
   return ok;
 }
 
-size_t colview_hist_bytes(int64_t nnz) {
-  return align_up((size_t)ceil_div(nnz > 0 ? nnz : 1, kRadixTile) * kRadixBins * sizeof(uint32_t), kAlign);
+bool colview_update_ok(int32_t out_f, int32_t in_f, int64_t nnz) {
+  return nnz > 0 && bits_for((uint64_t)(in_f - 1)) + bits_for((uint64_t)(out_f - 1)) <= 31;
+}
+
+cudaError_t cut_tiles(const int32_t *ptr, int32_t n_rows, int64_t nnz, const TileGeom &g, int32_t *tiles,
+                      cudaStream_t s) {
+  launch_pdl(k_tiles, grid_for(32 * ((int64_t)g.n_tiles + 1), 256), 256, 0, s, ptr, n_rows, nnz, g.cost_per_tile,
+             g.row_weight, g.n_tiles, tiles);
+  return cudaGetLastError();
 }
 
 cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *row, const int32_t *col,
                        const PlanPtrs &p, const TileGeom &gf, const TileGeom &gt, void *ws, cudaStream_t s,
-                       int ready, cudaStream_t aux, cudaEvent_t ev_a, cudaEvent_t ev_b, bool *deferred) {
+                       int ready, bool colview) {
   BuildWs W = build_ws_layout(out_f, in_f, nnz);
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   uint32_t *counts = reinterpret_cast<uint32_t *>(b + W.counts);
   void *stemp = b + W.scan;
   cudaError_t e;
-  if (deferred) *deferred = false;
   const int cbits = bits_for((uint64_t)(in_f - 1));
 
   // row offsets and the 16-bit column copy: already written by a
@@ -497,56 +528,11 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     e = build_tables(p.rp, p.col16, out_f, in_f, p.tables, s);
     if (e != cudaSuccess) return e;
   }
-  const bool restructured = aux && ev_a && ev_b && ready == kPlanRowsReady;
-  int dshift = 0;
-  if (restructured && p.cv_keys && colview_digits(out_f, in_f, nnz, &dshift)) {
-    // The forward reads only the row half of the plan: cut its tiles here,
-    // and rebuild the column view on `aux` after the call returns, from the
-    // first-level offsets the restructure left in cv_offs on `aux`.
-    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s, p.rp, out_f, nnz, gf.cost_per_tile,
-               gf.row_weight, gf.n_tiles, p.tiles_f);
-    e = cudaEventRecord(ev_a, s);  // after the merge wrote (row, col)
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, ev_a, 0);
+  if (ready < kPlanRowTilesReady) {
+    e = cut_tiles(p.rp, out_f, nnz, gf, p.tiles_f, s);
     if (e != cudaSuccess) return e;
-    const int64_t nb = ceil_div(nnz, kRadixTile);
-    e = radix_scatter_only<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{p.cv_keys, p.cv_vals},
-                                     nnz, dshift, p.cv_offs, aux);
-    if (e == cudaSuccess) e = launch_colview_bucket(dshift, p.cv_keys, p.cv_vals, nnz, cbits, p.cv_offs, nb, in_f, p, aux);
-    if (e == cudaSuccess) {
-      launch_pdl(k_tiles, grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, aux, p.cp, in_f, nnz,
-                 gt.cost_per_tile, gt.row_weight, gt.n_tiles, p.tiles_t);
-      e = cudaGetLastError();
-    }
-    cudaError_t r = cudaEventRecord(ev_b, aux);
-    if (e == cudaSuccess) e = r;
-    if (e == cudaSuccess && deferred) *deferred = true;
-    if (e != cudaSuccess) cudaStreamWaitEvent(s, ev_b, 0);
-    return e;
   }
-  const bool fork = restructured;
-  if (fork) {  // the forward tiles need only the row offsets: cut them beside the column view
-    e = cudaEventRecord(ev_a, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, ev_a, 0);
-    if (e != cudaSuccess) return e;
-    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, aux, p.rp, out_f, nnz,
-               gf.cost_per_tile, gf.row_weight, gf.n_tiles, p.tiles_f);
-    e = cudaEventRecord(ev_b, aux);
-    if (e != cudaSuccess) {
-      cudaStreamWaitEvent(s, ev_a, 0);
-      return e;
-    }
-  } else if (ready < kPlanRowTilesReady) {
-    launch_pdl(k_tiles, grid_for(32 * ((int64_t)gf.n_tiles + 1), 256), 256, 0, s, p.rp, out_f, nnz, gf.cost_per_tile,
-                                                                           gf.row_weight, gf.n_tiles, p.tiles_f);
-  }
-  // every return from here on joins the forward tiles first
-  auto joined = [&](cudaError_t err) -> cudaError_t {
-    if (fork) {
-      cudaError_t j = cudaStreamWaitEvent(s, ev_b, 0);
-      if (err == cudaSuccess) err = j;
-    }
-    return err;
-  };
+  if (!colview) return cudaGetLastError();
   // column view: stable sort by column (rows stay in order within a column);
   // column offsets from the sorted keys
   if (colview_digits(out_f, in_f, nnz, nullptr)) {
@@ -563,9 +549,9 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     const uint32_t *offs = reinterpret_cast<uint32_t *>(t + hbytes);
     e = radix_pass<uint32_t>(ColRowSrc{row, col, out_f, in_f, cbits}, ArrayDst<uint32_t>{ka, va}, nnz, shift, hist,
                              reinterpret_cast<uint32_t *>(t + hbytes), t + 2 * hbytes, s);
-    if (e != cudaSuccess) return joined(e);
+    if (e != cudaSuccess) return e;
     e = launch_colview_bucket(shift, ka, va, nnz, cbits, offs, nb, in_f, p, s);
-    if (e != cudaSuccess) return joined(e);
+    if (e != cudaSuccess) return e;
   } else if (nnz > 0) {
     uint32_t *ka = reinterpret_cast<uint32_t *>(b + W.keys_a);
     uint32_t *va = reinterpret_cast<uint32_t *>(b + W.vals_a);
@@ -574,15 +560,13 @@ cudaError_t build_plan(int32_t out_f, int32_t in_f, int64_t nnz, const int32_t *
     uint32_t *keys_out = reinterpret_cast<uint32_t *>(b + W.keys_out);
     e = radix_sort_custom<uint32_t>(ColSrc{col, in_f}, ColviewDst{keys_out, p.row_t, p.src_t, row, out_f}, nnz,
                                     cbits, ka, va, kb, vb, b + W.radix, s);
-    if (e != cudaSuccess) return joined(e);
+    if (e != cudaSuccess) return e;
     launch_pdl(k_offsets_sorted<uint32_t>, grid_for(nnz + 1, 256), 256, 0, s, keys_out, nnz, in_f, p.cp);
     if (p.rowt16) launch_pdl(k_pack16, grid_for(nnz, 256), 256, 0, s, p.row_t, nnz, p.rowt16);
   } else {
     launch_pdl(k_offsets_sorted<int32_t>, 1, 256, 0, s, col, 0, in_f, p.cp);
   }
-  launch_pdl(k_tiles, grid_for(32 * ((int64_t)gt.n_tiles + 1), 256), 256, 0, s, p.cp, in_f, nnz, gt.cost_per_tile,
-                                                                         gt.row_weight, gt.n_tiles, p.tiles_t);
-  return joined(cudaGetLastError());
+  return cut_tiles(p.cp, in_f, nnz, gt, p.tiles_t, s);
 }
 
 // *flag |= 1 when some row r does not start at r * K (K stored weights per row)

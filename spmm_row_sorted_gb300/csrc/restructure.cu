@@ -3,23 +3,32 @@
 //
 //  1. prune set: radix select (digits of 11, 10 and 10 bits, high to low) of
 //     the n_prune-th smallest magnitude key t; ties at t are pruned in
-//     storage order, so the pruned set is exactly the n_prune smallest (|w|, k);
-//  2. survivors: one scan of the packed pair (key > t, key == t) gives every
-//     survivor its output slot (stable compaction);
-//  3. regrow: draws i of SplitMix64 map to positions by multiply-high; a draw
-//     is a candidate when the position was empty (binary search in its old
-//     row), and is accepted when it is the first draw of its position -- a
-//     hash table keeps the minimum draw index per position (atomicMin, so the
-//     outcome does not depend on thread order); a scan over draw order keeps
-//     the first n_prune accepted.  Draws run in chunks until enough are
-//     accepted; the first chunk is queued before steps 1 and 2 and the host
-//     reads its count back while the device runs them;
-//  4. regrown positions are sorted: the accept scan drops each accepted
-//     position into an equal-width bucket of the position range, one block
-//     turns the bucket counts into offsets and one warp per bucket places its
-//     positions by rank (a general sort takes over after extra draw chunks or
-//     a full bucket); then they are merged with the survivors by position
-//     (merge path), writing row/col/val/src.
+//     storage order, so the pruned set is exactly the n_prune smallest
+//     (|w|, k); one more pass counts, per tile of stored weights, those above
+//     t and those equal to it;
+//  2. regrow, on the handle's second stream beside step 1: draws i of
+//     SplitMix64 map to positions by multiply-high; a draw is a candidate when
+//     the position was empty (binary search in its old row), and is accepted
+//     when it is the first draw of its position -- a hash table keeps the
+//     minimum draw index per position (atomicMin, so the outcome does not
+//     depend on thread order); a scan over draw order keeps the first n_prune
+//     accepted and drops each into an equal-width bucket of the position range
+//     (and, when the column view is updated, of the column-major range); one
+//     warp per bucket ranks its positions, giving the regrown positions sorted
+//     in row order (and in column order);
+//  3. one pass merges the survivors with the regrown positions: tile t of the
+//     stored weights owns the regrown positions from its first key up to the
+//     next tile's, so a survivor lands at (survivors before it) + (regrown
+//     below it) and a regrown position at (its rank) + (survivors below it);
+//     the same pass writes the row offsets and the 16-bit columns;
+//  4. the column view is updated the same way on the second stream after the
+//     call returns: the current view's kept entries (column order) merged with
+//     the regrown positions in column order, into the plan's second view.
+// Steps 3 and 4 are queued before the host has read how many draws the first
+// chunk accepted, behind a device flag that step 2 sets only when the chunk
+// sufficed; when it did not (rare: more draws are needed, or a bucket ran
+// over) the flagged passes write nothing, and the host queues the remaining
+// draws, a general sort and the passes again.
 // Every step is integer work, so the output is bit-exact with the sequential
 // definition.
 #include <math.h>
@@ -32,42 +41,6 @@ namespace snack {
 namespace {
 
 constexpr uint64_t kEmpty = ~0ull;
-constexpr int kMergeThreads = 256;
-constexpr int kMergeItems = 4;
-constexpr int kMergeTile = kMergeThreads * kMergeItems;
-static_assert(2 * kMergeTile == kRadixTile, "two merge tiles make one tile of the column view's first radix pass");
-
-// The column view's first-level tile histogram of the merged pattern, from
-// the merge's split points alone (beside the merge, on the other stream):
-// radix tile t holds the outputs of merge tiles 2t and 2t+1, i.e. survivor
-// keys A[a0, a1) and regrown keys B[d0 - a0, d1 - a1); each output's digit is
-// its column's high 8 bits.  Every bin is written (digit-major [256][tiles]).
-__global__ void __launch_bounds__(256) k_col_hist(const uint64_t *__restrict__ A, const uint64_t *__restrict__ B,
-                                                  const int64_t *__restrict__ part, int64_t n_merge_tiles, int64_t n,
-                                                  int cbits, int cshift, uint32_t *__restrict__ chist, int64_t cnb) {
-  pdl_wait();
-  __shared__ uint32_t h[8][kRadixBins];  // one histogram per warp: less atomic contention
-  const int warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < 8 * kRadixBins; i += 256) (&h[0][0])[i] = 0u;
-  __syncthreads();
-  const int64_t t = blockIdx.x;
-  const int64_t d0 = t * kRadixTile, d1 = d0 + kRadixTile < n ? d0 + kRadixTile : n;
-  const int64_t m1 = 2 * t + 2 < n_merge_tiles ? 2 * t + 2 : n_merge_tiles;
-  const int64_t a0 = part[2 * t], a1 = part[m1];
-  const int64_t b0 = d0 - a0, b1 = d1 - a1;
-  const uint64_t cmask = (1ull << cbits) - 1ull;
-  for (int64_t q = a0 + threadIdx.x; q < a1; q += 256)
-    atomicAdd(&h[warp][(uint32_t)((A[q] & cmask) >> cshift) & 0xFFu], 1u);
-  for (int64_t q = b0 + threadIdx.x; q < b1; q += 256)
-    atomicAdd(&h[warp][(uint32_t)((B[q] & cmask) >> cshift) & 0xFFu], 1u);
-  __syncthreads();
-  for (int d = threadIdx.x; d < kRadixBins; d += 256) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) c += h[w][d];
-    chist[(int64_t)d * cnb + t] = c;
-  }
-}
 
 struct SelState {
   uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
@@ -214,32 +187,6 @@ struct KeepVal {
   }
 };
 
-// position key (row << cbits) | col of stored weight k, loaded with the scan
-// value; keys order positions as row * in_f + col does, and split with a
-// shift and a mask
-struct PosPayload {
-  const int32_t *row, *col;
-  int cbits;
-  __device__ uint64_t operator()(int64_t k) const {
-    return ((uint64_t)(uint32_t)row[k] << cbits) | (uint32_t)col[k];
-  }
-};
-
-struct KeepOut {
-  const SelState *st;
-  uint64_t *surv_pos;
-  uint32_t *surv_src;
-  __device__ void operator()(int64_t k, uint64_t ex, uint64_t v, uint64_t pos) const {
-    const uint32_t m = __ldg(&st->remaining);
-    const uint32_t gt = (uint32_t)ex, eq = (uint32_t)(ex >> 32);
-    const bool keep = (v & 1ull) || ((v >> 32) && eq >= m);
-    if (keep) {
-      uint32_t s = gt + (eq > m ? eq - m : 0u);
-      surv_pos[s] = pos;
-      surv_src[s] = (uint32_t)k;
-    }
-  }
-};
 
 __device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_t *mins, uint64_t mask, uint64_t p) {
   uint64_t h = sm64_finalise(p) & mask;
@@ -252,8 +199,18 @@ __device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_
   return 0xFFFFFFFFu;
 }
 
+
+__device__ __forceinline__ uint32_t mag_of(float v) { return canon_mag(__float_as_uint(v) & 0x7FFFFFFFu); }
+__device__ __forceinline__ uint32_t mag_of(bf16 v) {
+  return canon_mag(((uint32_t)__bfloat16_as_ushort(v) & 0x7FFFu) << 16);
+}
+
+// A draw: position by multiply-high of SplitMix64 output i, empty test by a
+// binary search of its column in the old row (CI: the plan's 16-bit column
+// copy, or the 32-bit columns), insertion into the position table.
+template <typename CI>
 __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int cbits,
-                       const int32_t *__restrict__ rp, const int32_t *__restrict__ col, uint64_t *__restrict__ cand,
+                       const int32_t *__restrict__ rp, const CI *__restrict__ col, uint64_t *__restrict__ cand,
                        uint64_t *hkeys, uint32_t *hmin, uint64_t hmask, uint32_t *overflow) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -264,14 +221,15 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
     const uint64_t r = p / (uint64_t)in_f;
     const int32_t c = (int32_t)(p - r * (uint64_t)in_f);
     int32_t lo = rp[r], hi = rp[r + 1];
+    const int32_t end = hi;
     while (lo < hi) {
       int32_t mid = lo + (hi - lo) / 2;
-      if (col[mid] < c)
+      if ((int32_t)col[mid] < c)
         lo = mid + 1;
       else
         hi = mid;
     }
-    const bool member = lo < rp[r + 1] && col[lo] == c;
+    const bool member = lo < end && (int32_t)col[lo] == c;
     if (member) {
       cand[idx] = kEmpty;
       continue;
@@ -295,8 +253,9 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
   }
 }
 
-// flag[idx] = 1 when draw i0+idx found an empty position and is the first
-// draw of that position (its index is the minimum recorded for it)
+// flag[idx] = 1 when draw i0 + idx found an empty position and is that
+// position's first draw (the minimum index recorded for it); one thread per
+// draw, so the table lookups of all draws are in flight at once
 __global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0,
                                const uint64_t *__restrict__ hkeys, const uint32_t *__restrict__ hmin, uint64_t hmask,
                                uint32_t *__restrict__ flags) {
@@ -318,94 +277,94 @@ struct CandPayload {
   __device__ uint64_t operator()(int64_t idx) const { return cand[idx]; }
 };
 
-// Accepted draws in draw order: slot q of the regrown list, and -- for the
-// sort -- a slot in the position's bucket (equal-width buckets of the
-// position range, kBktCap slots each, filled in any order; a full bucket
-// raises `bovf` and the caller sorts the list the general way instead).
-constexpr int kBktTarget = 32;  // positions expected per bucket
-constexpr int kBktCap = 128;    // slots per bucket
+constexpr int kBktTarget = 64;               // positions expected per bucket
+constexpr int kBktCap = 256;                 // slots per bucket
+constexpr uint32_t kBktMaxBuckets = 16384;   // more buckets: the regrown positions take the general sort
 
+// Equal-width buckets of a key range, filled in any order (atomic slots);
+// each key keeps its acceptance rank.  The bucket of a key is the high word
+// of key * mult, mult = floor(2^64 * nb / range): monotone in the key and
+// below nb.  Counters sit one per 32-byte sector (kCntStride words apart), so
+// the atomics on neighbouring buckets do not queue on one sector.
+constexpr int kCntStride = 8;
+struct BucketSet {
+  uint32_t *cnt;  // [nb * kCntStride] keys dropped per bucket
+  uint64_t *key;  // [nb][kBktCap]
+  uint32_t *q;    // [nb][kBktCap]
+  uint64_t mult;
+  uint32_t nb;    // 0: not used
+  __device__ uint32_t count(uint32_t b) const { return min(__ldg(&cnt[(size_t)b * kCntStride]), (uint32_t)kBktCap); }
+  __device__ void place(uint64_t k, uint32_t qq, uint32_t *ovf) const {
+    const uint32_t b = (uint32_t)__umul64hi(k, mult);
+    const uint32_t slot = atomicAdd(&cnt[(size_t)b * kCntStride], 1u);
+    if (slot < (uint32_t)kBktCap) {
+      key[(size_t)b * kBktCap + slot] = k;
+      q[(size_t)b * kBktCap + slot] = qq;
+    } else {
+      atomicOr(ovf, 1u);
+    }
+  }
+};
+
+uint64_t bucket_mult(uint32_t nb, uint64_t range) {
+  const unsigned __int128 m = ((unsigned __int128)nb << 64) / (unsigned __int128)range;
+  return m >> 64 ? ~0ull : (uint64_t)m;
+}
+
+// column-major key col << rbits | row of a row-major key row << cbits | col
+__device__ __forceinline__ uint64_t col_major(uint64_t p, int cbits, int rbits) {
+  return ((p & ((1ull << cbits) - 1ull)) << rbits) | (p >> cbits);
+}
+
+// Accepted draws in draw order: rank q among the accepted; the first n_prune
+// are the regrown positions, grown[q].
 struct AcceptOut {
   uint64_t *grown;
   int64_t before, n_prune;
-  uint32_t *bcnt;     // [nb] positions placed per bucket
-  uint64_t *bslots;   // [nb][kBktCap]
-  double scale;       // bucket = floor(p * scale)
-  uint32_t nb;
-  uint32_t *bovf;
-  __device__ void operator()(int64_t idx, uint32_t ex, uint32_t v, uint64_t p) const {
-    if (v) {
-      int64_t q = before + (int64_t)ex;
-      if (q < n_prune) {
-        grown[q] = p;
-        const uint32_t bk = bucket_of(p, scale, nb);
-        const uint32_t slot = atomicAdd(&bcnt[bk], 1u);
-        if (slot < (uint32_t)kBktCap)
-          bslots[(size_t)bk * kBktCap + slot] = p;
-        else
-          atomicOr(bovf, 1u);
-      }
-    }
+  __device__ void operator()(int64_t, uint32_t ex, uint32_t v, uint64_t p) const {
+    if (!v) return;
+    const int64_t q = before + (int64_t)ex;
+    if (q < n_prune) grown[q] = p;
   }
 };
 
 // Counters of the regrow branch (it runs beside the select on a second stream).
 struct DrawState {
   uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
-  uint32_t bucket_overflow;  // a sort bucket of the regrown positions ran out of slots
+  uint32_t bucket_overflow;  // a row-order bucket of the regrown positions ran out of slots
+  uint32_t col_overflow;     // a column-order bucket did
+  uint32_t lists_ok;         // the row-order list is complete: the merge may write
+  uint32_t col_ok;           // and the column-order list: the column-view update may write
 };
 
-// Bucket offsets: exclusive prefix of min(count, kBktCap) over the nb
-// buckets, one block of light threads (it runs beside the other stream's
-// kernels): each thread sums a contiguous run of counts, 16 loads in flight
-// per round, the block scans the sums, and the thread writes its run's
-// offsets; offs[nb] = the number of positions placed.  Thread 0 first copies
-// the draw chunk's counters to the host's mapped words (the accept scan that
-// wrote them precedes this kernel), so the host reads them with no copy on
-// the stream.
-constexpr int kBktScanThreads = 1024;
-__global__ void __launch_bounds__(kBktScanThreads) k_bkt_scan(const uint32_t *__restrict__ bcnt, uint32_t nb,
-                                                              uint32_t *__restrict__ offs, const DrawState *ds,
-                                                              volatile uint32_t *host_words) {
+// The lists' verdict and, with host_words, the chunk's counters to the host's
+// mapped words.
+__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made) {
+  const uint32_t tot = ds->total, ovf = ds->overflow, bovf = ds->bucket_overflow, covf = ds->col_overflow;
+  if (host_words) {
+    volatile uint32_t *hw = host_words;
+    hw[0] = tot;
+    hw[1] = ovf;
+    hw[2] = bovf;
+    hw[3] = covf;
+  }
+  const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf;
+  ds->lists_ok = ok ? 1u : 0u;
+  ds->col_ok = ok && !covf ? 1u : 0u;
+}
+
+__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made) {
   pdl_wait();
-  __shared__ uint32_t s_warp[kBktScanThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    host_words[0] = ds->total;
-    host_words[1] = ds->overflow;
-    host_words[2] = ds->bucket_overflow;
-  }
-  const uint32_t per = (nb + kBktScanThreads - 1) / kBktScanThreads;
-  const uint32_t b0 = min((uint32_t)tid * per, nb), b1 = min(b0 + per, nb);
-  uint32_t sum = 0;
-  for (uint32_t i0 = b0; i0 < b1; i0 += 16) {
-    uint32_t c[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) c[i] = i0 + i < b1 ? min(__ldg(&bcnt[i0 + i]), (uint32_t)kBktCap) : 0u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sum += c[i];
-  }
-  const uint32_t inc = warp_inclusive_scan(sum);
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  if (warp == 0) s_warp[lane] = warp_inclusive_scan(s_warp[lane]);
-  __syncthreads();
-  uint32_t run = inc - sum + (warp > 0 ? s_warp[warp - 1] : 0u);
-  for (uint32_t i0 = b0; i0 < b1; i0 += 16) {
-    uint32_t c[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) c[i] = i0 + i < b1 ? min(__ldg(&bcnt[i0 + i]), (uint32_t)kBktCap) : 0u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i0 + i < b1) offs[i0 + i] = run;
-      run += c[i];
-    }
-  }
-  if (tid == kBktScanThreads - 1) offs[nb] = run;
+  publish(ds, n_prune, host_words, made != 0);
+}
+
+__global__ void k_set_word(uint32_t *w, uint32_t v) {
+  pdl_wait();
+  *w = v;
 }
 
 // Start of a restructure's regrow branch: counters and bucket counts to zero,
-// the position table to empty (one launch instead of four fills).
+// the position table to empty (one launch instead of several fills).
 __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t *__restrict__ hmin, int64_t cap,
                           uint32_t *__restrict__ bcnt, int64_t nb) {
   pdl_wait();
@@ -415,6 +374,9 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
     ds->total = 0u;
     ds->overflow = 0u;
     ds->bucket_overflow = 0u;
+    ds->col_overflow = 0u;
+    ds->lists_ok = 0u;
+    ds->col_ok = 0u;
   }
   for (int64_t i = i0; i < cap; i += stride) {
     hkeys[i] = kEmpty;
@@ -423,157 +385,584 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
 }
 
-// One warp per bucket: each position's rank among its bucket's (distinct)
-// positions gives its place in the sorted list.  Slots past the placed
-// positions get key_space + q, larger than every position key, in order.
-__global__ void __launch_bounds__(256) k_bkt_rank(const uint64_t *__restrict__ bslots, const uint32_t *__restrict__ bcnt,
-                                                  const uint32_t *__restrict__ offs, uint32_t nb, int64_t n,
-                                                  uint64_t key_space, uint64_t *__restrict__ out) {
+// The first chunk's regrown positions into one order's buckets (row order:
+// the key itself; column order: col << rbits | row), one thread per
+// position, so all atomics are in flight at once.
+__global__ void k_place(const uint64_t *__restrict__ grown, const DrawState *ds, int64_t n_prune, BucketSet bs,
+                        int col_order, int cbits, int rbits, uint32_t *bovf) {
+  pdl_wait();
+  const int64_t n = min((int64_t)ds->total, n_prune);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
+    const uint64_t p = grown[q];
+    bs.place(col_order ? col_major(p, cbits, rbits) : p, (uint32_t)q, bovf);
+  }
+}
+
+struct RankDst {
+  uint64_t *key64;  // row order: 64-bit keys, or
+  uint32_t *key32;  // column order: 32-bit keys
+  uint32_t *q;      // acceptance ranks
+};
+
+// A sorted list from the first chunk's buckets, one warp per bucket: the
+// bucket's first slot is the number of keys in the buckets before it (its
+// block adds up those counts), and each key lands at its rank among the
+// bucket's keys (all distinct).  Block 0 first sets the lists' verdict (and,
+// with host_words, publishes the chunk's counters).
+__global__ void __launch_bounds__(256) k_bkt_rank(BucketSet S, RankDst D, int64_t n_prune, DrawState *ds,
+                                                  uint32_t *host_words, bool k32) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
+  __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tot = offs[nb];
-  for (int64_t q = tot + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x)
-    out[q] = key_space + (uint64_t)q;
-  const int64_t b = (int64_t)blockIdx.x * 8 + warp;
-  if (b >= nb) return;
-  const uint32_t L = min(bcnt[b], (uint32_t)kBktCap), o = offs[b];
-  for (uint32_t i = lane; i < L; i += 32) sk[warp][i] = bslots[(size_t)b * kBktCap + i];
+  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true);
+  const uint32_t b0 = blockIdx.x * 8;
+  uint32_t part = 0;
+  for (uint32_t i0 = threadIdx.x; i0 < b0; i0 += 256 * 8) {  // eight loads in flight per round
+    uint32_t c[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) c[u] = i0 + u * 256 < b0 ? S.count(i0 + u * 256) : 0u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part += c[u];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(0xffffffffu, part, o);
+  if (lane == 0) s_red[warp] = part;
+  __syncthreads();
+  uint32_t before = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) before += s_red[w];
+  const uint32_t b = b0 + warp;
+  if (b >= S.nb) return;
+  for (uint32_t w = 0; w < (uint32_t)warp; ++w) before += S.count(b0 + w);
+  const uint32_t L = S.count(b);
+  const size_t sb = (size_t)b * kBktCap;
+  for (uint32_t i = lane; i < L; i += 32) sk[warp][i] = S.key[sb + i];
   __syncwarp();
   for (uint32_t i = lane; i < L; i += 32) {
     const uint64_t k = sk[warp][i];
     uint32_t r = 0;
-    for (uint32_t j = 0; j < L; ++j) r += sk[warp][j] < k ? 1u : 0u;
-    out[o + r] = k;
+    if (k32) {  // keys below 2^32: compare the low words
+      const uint32_t *s32 = reinterpret_cast<const uint32_t *>(sk[warp]);
+      const uint32_t k_lo = (uint32_t)k;
+      for (uint32_t j = 0; j < L; ++j) r += s32[2 * j] < k_lo ? 1u : 0u;
+    } else {
+      for (uint32_t j = 0; j < L; ++j) r += sk[warp][j] < k ? 1u : 0u;
+    }
+    const int64_t dst = (int64_t)before + r;
+    if (dst < n_prune) {  // always, unless a bucket ran over (then the lists are discarded)
+      if (D.key64)
+        D.key64[dst] = k;
+      else
+        D.key32[dst] = (uint32_t)k;
+      D.q[dst] = S.q[sb + i];
+    }
   }
 }
 
-// Number of A elements among the first d outputs of the merge (A first on
-// ties), by one warp: the predicate A[a] <= B[d-1-a] holds on a prefix of
-// candidate a, so each round probes 32 points and keeps the crossing.
-__device__ int64_t merge_split_warp(const uint64_t *A, int64_t na, const uint64_t *B, int64_t nb, int64_t d) {
+// Sources of the general sort of the regrown positions (acceptance rank as
+// the payload): row order, and column order.
+struct GrownRowSrc {
+  const uint64_t *grown;
+  __device__ uint64_t key(int64_t q) const { return grown[q]; }
+  __device__ uint32_t val(int64_t q) const { return (uint32_t)q; }
+};
+struct GrownColSrc {
+  const uint64_t *grown;
+  int cbits, rbits;
+  __device__ uint32_t key(int64_t q) const { return (uint32_t)col_major(grown[q], cbits, rbits); }
+  __device__ uint32_t val(int64_t q) const { return (uint32_t)q; }
+};
+
+// ---------------------------------------------------------------------------
+// Merge of the kept elements of a sorted stream with a sorted list.
+//
+// The stream holds n elements with strictly increasing keys; each has a
+// packed count g | e << 16 (the scan tile sums pack g | e << 32): kept
+// (g = 1), or a tie (e = 1) -- the first m ties in stream order are dropped,
+// the rest kept.  The list's keys increase strictly and none equals a stream
+// key.  Output index of a kept element: (kept elements before it) + (list
+// keys below its key); of list entry j: j + (kept elements below it).  Tile
+// t of the stream (kMkTile elements) owns the list keys from its first key up
+// to the next tile's first key (tile 0 from the start, the last tile to the
+// end): every list entry is written by one tile, and a tile's outputs are one
+// contiguous range.  Major offsets (rows, or columns): off[M] = outputs whose
+// major index (key >> minor_bits) is below M, written by the tile after
+// whose element major M starts.
+//
+// A block loads its tile striped (coalesced), scans the counts and walks the
+// tile against its list slice blocked (thread t: elements 8t .. 8t+7, one
+// binary search and then forward steps), and writes striped again, each
+// element's output index passed through shared memory.
+
+constexpr int kMkThreads = 256, kMkItems = 8, kMkTile = kMkThreads * kMkItems;
+static_assert(kMkTile == kScanTile, "a tile's keep counts are one scan tile's sum");
+constexpr int kMkListCap = 2048;                       // list keys of a tile staged in shared memory
+constexpr int kMkXWords = kMkTile + kMkTile / 32 + 1;  // padded local counts, index kMkTile included
+__device__ __forceinline__ int mk_pad(int e) { return e + (e >> 5); }
+// Tile arrays are read both striped (thread t: t, t + 256, ...) and blocked
+// (thread t: 8t .. 8t+7); one pad word per 32 words keeps both free of bank
+// conflicts (one 8-byte pad per 16 keys for 64-bit keys).
+template <typename K>
+__device__ __forceinline__ int kpad(int e) {
+  return sizeof(K) == 4 ? e + (e >> 5) : e + (e >> 4);
+}
+template <typename K>
+__host__ __device__ constexpr int kpad_words(int n) {
+  return sizeof(K) == 4 ? n + n / 32 + 1 : n + n / 16 + 1;
+}
+template <typename K>
+struct PadKeys {  // sK[e] through the padded index
+  K *p;
+  __device__ K &operator[](int e) const { return p[kpad<K>(e)]; }
+};
+
+// Bounds of tile t: its first key and the list keys below it (tile n_tiles:
+// key ~0, every list key), and the policy's note on the first element (the
+// column view: its column).
+struct MkBound {
+  uint64_t key;
+  int64_t lo;
+  uint32_t aux, pad;
+};
+static_assert(sizeof(MkBound) <= 32, "the plan reserves 32 bytes per tile bound");
+
+struct MkArgs {
+  int64_t n, n_list;
+  int64_t n_out;          // output slots (every index written is checked against it)
+  const MkBound *bnd;     // [n_tiles + 1]
+  const uint64_t *sums;   // per-tile packed keep counts (kDirect), or their exclusive prefixes
+  const uint32_t *guard;  // when set and zero, every block returns at once
+  int minor_bits;
+  int64_t n_major;
+  int32_t *off;  // [n_major + 1]
+};
+
+// number of entries of an ascending sequence at(0..n) below v, by one warp:
+// each round probes 32 evenly spaced entries and keeps the bracket of the
+// crossing (the probes below v are a prefix)
+template <typename F>
+__device__ int64_t lb_warp(F at, int64_t n, uint64_t v) {
   const int lane = threadIdx.x & 31;
-  int64_t lo = d > nb ? d - nb : 0, hi = d < na ? d : na;  // answer in [lo, hi]
+  int64_t lo = 0, hi = n;  // answer in [lo, hi]
   while (hi - lo > 32) {
     const int64_t span = hi - lo;
-    const int64_t p = lo + span * (lane + 1) / 33;  // lo < p < hi
-    const bool ok = A[p] <= B[d - 1 - p];
-    const int cnt = __popc(__ballot_sync(0xffffffffu, ok));
+    const bool below = at(lo + span * (lane + 1) / 33) < v;  // probes strictly inside [lo, hi)
+    const int cnt = __popc(__ballot_sync(0xffffffffu, below));
     const int64_t new_lo = cnt > 0 ? lo + span * cnt / 33 + 1 : lo;
     const int64_t new_hi = cnt < 32 ? lo + span * (cnt + 1) / 33 : hi;
     lo = new_lo;
     hi = new_hi;
   }
-  const int64_t a = lo + lane;
-  const bool ok = a < hi && A[a] <= B[d - 1 - a];
-  return lo + __popc(__ballot_sync(0xffffffffu, ok));
+  const bool below = lo + lane < hi && at(lo + lane) < v;
+  return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
-// part[t] = A elements among the first t*kMergeTile outputs, one warp per split
-__global__ void k_merge_splits(const uint64_t *__restrict__ A, int64_t na, const uint64_t *__restrict__ B, int64_t nb,
-                               int64_t n_tiles, int64_t *__restrict__ part) {
-  pdl_wait();
-  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t > n_tiles) return;
-  int64_t d = t * kMergeTile;
-  if (d > na + nb) d = na + nb;
-  const int64_t sp = merge_split_warp(A, na, B, nb, d);
-  if ((threadIdx.x & 31) == 0) part[t] = sp;
-}
-
-template <typename TV>
-__global__ void __launch_bounds__(kMergeThreads)
-    k_merge(const uint64_t *__restrict__ A, const uint32_t *__restrict__ As, int64_t na, const uint64_t *__restrict__ B,
-            int64_t nb, const int64_t *__restrict__ part, int cbits, int32_t out_f, const TV *__restrict__ val,
-            int32_t *__restrict__ row_out, int32_t *__restrict__ col_out, TV *__restrict__ val_out,
-            int32_t *__restrict__ src_out, int32_t *__restrict__ rp, uint16_t *__restrict__ col16) {
-  pdl_wait();
-  __shared__ uint64_t sA[kMergeTile];
-  __shared__ uint64_t sB[kMergeTile];
-  __shared__ uint32_t sS[kMergeTile];  // survivor sources; then the output sources (oS)
-  int32_t *oS = reinterpret_cast<int32_t *>(sS);
-  // after the merge, the two key arrays hold the outputs' rows and columns as 32-bit words
-  uint32_t *oR = reinterpret_cast<uint32_t *>(sA), *oC = reinterpret_cast<uint32_t *>(sB);
-  const int64_t t = blockIdx.x;
-  const int64_t n = na + nb;
-  const uint64_t cmask = (1ull << cbits) - 1ull;
-  const int64_t d0 = t * kMergeTile;
-  const int64_t d1 = d0 + kMergeTile < n ? d0 + kMergeTile : n;
-  const int64_t a0 = part[t], a1 = part[t + 1];
-  const int64_t b0 = d0 - a0, b1 = d1 - a1;
-  const int la = (int)(a1 - a0), lb = (int)(b1 - b0);
-  for (int q = threadIdx.x; q < la; q += kMergeThreads) {
-    sA[q] = A[a0 + q];
-    sS[q] = As[a0 + q];
-  }
-  for (int q = threadIdx.x; q < lb; q += kMergeThreads) sB[q] = B[b0 + q];
-  __syncthreads();
-  int ld = threadIdx.x * kMergeItems;
-  if (ld > la + lb) ld = la + lb;
-  int lo = ld > lb ? ld - lb : 0, hi = ld < la ? ld : la;
+// number of entries of an ascending sequence at(0..n) below v
+template <typename F, typename V>
+__device__ __forceinline__ int lb_seq(F at, int n, V v) {
+  int lo = 0, hi = n;
   while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (sA[mid] <= sB[ld - 1 - mid])
+    const int mid = (lo + hi) >> 1;
+    if (at(mid) < v)
       lo = mid + 1;
     else
       hi = mid;
   }
-  int ai = lo, bi = ld - lo;
-  uint64_t pos[kMergeItems];
-  int32_t src[kMergeItems];
+  return lo;
+}
+
+template <class Pol>
+constexpr size_t mk_smem_bytes() {
+  using K = typename Pol::Key;
+  return sizeof(K) * (kpad_words<K>(kMkTile + 1) + kMkListCap) +
+         sizeof(uint32_t) * (kMkXWords + (kMkXWords & 1) + kMkXWords + (kMkXWords & 1)) + sizeof(uint16_t) * kMkListCap +
+         sizeof(typename Pol::Shared);
+}
+
+// Tile bounds, one warp per tile t in [0, n_tiles], all at once (so the merge
+// blocks start with their bounds instead of searching the list themselves).
+template <class Pol>
+__global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd) {
+  pdl_wait();
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t > n_tiles) return;
+  MkBound r{~0ull, n_list, 0u, 0u};
+  if (t < n_tiles) {
+    r.key = pol.key_at_warp(t * (int64_t)kMkTile, &r.aux);
+    r.lo = t == 0 ? 0 : lb_warp([&](int64_t j) { return pol.list_key(j); }, n_list, r.key);
+  }
+  if ((threadIdx.x & 31) == 0) bnd[t] = r;
+}
+
+template <class Pol, bool kDirect>
+__global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a) {
+  using K = typename Pol::Key;
+  extern __shared__ __align__(16) uint8_t mk_smem[];
+  // tile keys (padded index; [len] = the next tile's first key, or the maximum)
+  K *sKp = reinterpret_cast<K *>(mk_smem);
+  K *sL = sKp + kpad_words<K>(kMkTile + 1);                      // the tile's list keys
+  uint32_t *sX = reinterpret_cast<uint32_t *>(sL + kMkListCap);  // local exclusive counts (padded)
+  uint32_t *sPos = sX + kMkXWords + (kMkXWords & 1);             // output index of each element, padded (~0u: dropped)
+  uint16_t *sP = reinterpret_cast<uint16_t *>(sPos + kMkXWords + (kMkXWords & 1));  // elements below each list key
+  const PadKeys<K> sK{sKp};
+  typename Pol::Shared &ps = *reinterpret_cast<typename Pol::Shared *>(sP + kMkListCap);
+  __shared__ uint64_t s_pre;
+  __shared__ uint64_t s_red[kMkThreads / 32];
+  __shared__ uint32_t s_tot;
+  pdl_wait();
+  // every load of the tile's inputs is issued before the first wait on one
+  const uint32_t go = a.guard ? *reinterpret_cast<const volatile uint32_t *>(a.guard) : 1u;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t b = blockIdx.x, base = b * (int64_t)kMkTile;
+  const int len = (int)(a.n - base < kMkTile ? a.n - base : kMkTile);
+  const bool last = b == (int64_t)gridDim.x - 1;
+  const MkBound bd0 = a.bnd[b], bd1 = a.bnd[b + 1];
+  const uint32_t m = pol.ties_dropped();
+  typename Pol::Item it[kMkItems];
+  uint32_t fl[kMkItems];
+  pol.load(base, len, last, bd0.aux, bd1.aux, it, fl, sK, ps);
+  uint64_t part = 0;
+  if (kDirect) {
+    for (int64_t q0 = tid; q0 < b; q0 += kMkThreads * 8) {  // eight loads in flight per round
+      uint64_t c[8];
 #pragma unroll
-  for (int it = 0; it < kMergeItems; ++it) {
-    src[it] = -2;
-    if (ld + it >= la + lb) continue;
-    bool take_a = bi >= lb || (ai < la && sA[ai] <= sB[bi]);
-    if (take_a) {
-      pos[it] = sA[ai];
-      src[it] = (int32_t)sS[ai];
-      ++ai;
+      for (int u = 0; u < 8; ++u) c[u] = q0 + u * kMkThreads < b ? a.sums[q0 + u * kMkThreads] : 0ull;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) part += c[u];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(0xffffffffu, part, o);
+    if (lane == 0) s_red[warp] = part;
+  }
+#pragma unroll
+  for (int i = 0; i < kMkItems; ++i) sX[mk_pad(i * kMkThreads + tid)] = fl[i];
+  if (go == 0u) return;  // a speculative launch whose lists were not made: write nothing
+  if (tid == 0) sK[len] = (K)bd1.key;
+  __syncthreads();
+  if (tid == 0) {
+    uint64_t p = 0;
+    if (kDirect) {
+#pragma unroll
+      for (int w = 0; w < kMkThreads / 32; ++w) p += s_red[w];
     } else {
-      pos[it] = sB[bi];
-      src[it] = -1;
-      ++bi;
+      p = a.sums[b];
     }
+    s_pre = p;
   }
-  __syncthreads();
-  // stage rows / cols / sources in shared memory, then write coalesced
+  pol.keys_blocked(base, len, last, bd0.aux, bd1.aux, sK, ps);
+  {  // exclusive scan of the packed counts in element order
+    uint32_t v[kMkItems], tsum = 0;
 #pragma unroll
-  for (int it = 0; it < kMergeItems; ++it)
-    if (src[it] != -2) {
-      const uint32_t c = (uint32_t)(pos[it] & cmask);
-      oR[ld + it] = (uint32_t)(pos[it] >> cbits);
-      oC[ld + it] = c;
-      oS[ld + it] = src[it];
+    for (int i = 0; i < kMkItems; ++i) {
+      v[i] = sX[mk_pad(tid * kMkItems + i)];
+      tsum += v[i];
     }
+    uint32_t ex = block_exclusive_scan<uint32_t>(tsum, &s_tot);
+#pragma unroll
+    for (int i = 0; i < kMkItems; ++i) {
+      sX[mk_pad(tid * kMkItems + i)] = ex;
+      ex += v[i];
+    }
+    if (tid == 0) sX[mk_pad(kMkTile)] = s_tot;
+  }
+  const int64_t lo = bd0.lo, cnt = bd1.lo - bd0.lo;
+  const bool lsm = cnt <= kMkListCap;
+  if (lsm)
+    for (int j = tid; j < (int)cnt; j += kMkThreads) sL[j] = (K)pol.list_key(lo + j);
   __syncthreads();
-  // row offsets of the output: rp[r] = o for the rows r in (row[o-1], row[o]];
-  // the row before the tile is that of the larger of the two inputs' last
-  // elements consumed by earlier tiles
-  int r_before = -1;
-  if (d0 > 0) {
-    uint64_t last = 0;
-    if (a0 > 0) last = A[a0 - 1];
-    if (b0 > 0 && B[b0 - 1] > last) last = B[b0 - 1];
-    r_before = (int)(last >> cbits);
+  const uint32_t preG = (uint32_t)s_pre, preE = (uint32_t)(s_pre >> 32), lo32 = (uint32_t)lo;
+  auto surv = [&](uint32_t x) -> uint32_t {  // kept elements before a local index, from its exclusive count
+    const uint32_t g = preG + (x & 0xFFFFu), e = preE + (x >> 16);
+    return g + (e > m ? e - m : 0u);
+  };
+  const int mb = a.minor_bits;
+  const uint32_t nmaj = (uint32_t)a.n_major;
+  // the blocked walk; with the slice in shared memory it also records, per
+  // list key, the elements below it
+  auto walk = [&](auto lkey, int n_l, bool record) {
+    if (b == 0) {  // list keys below the tile's first element: no element below them
+      const int j00 = lb_seq(lkey, n_l, sK[0]);
+      if (record)
+        for (int j = tid; j < j00; j += kMkThreads) sP[j] = 0;
+      if (tid == 0) {  // majors up to the first element's (no kept element before them)
+        const int64_t maj0 = min((int64_t)(sK[0] >> mb), a.n_major);
+        int jj = 0;
+        for (int64_t M = 0; M <= maj0; ++M) {
+          const K mk = (K)((uint64_t)M << mb);
+          while (jj < n_l && lkey(jj) < mk) ++jj;
+          a.off[M] = (int32_t)jj;
+        }
+      }
+    }
+    const int e0 = tid * kMkItems;
+    if (e0 >= len) return;
+    const int e1 = min(e0 + kMkItems, len);
+    int j = lb_seq(lkey, n_l, sK[e0]);
+    uint32_t x = sX[mk_pad(e0)];
+    for (int e = e0; e < e1; ++e) {
+      const K key = sK[e];
+      while (j < n_l && lkey(j) < key) {
+        if (record) sP[j] = (uint16_t)e;
+        ++j;
+      }
+      const uint32_t xn = sX[mk_pad(e + 1)];
+      const uint32_t d = xn - x;  // this element's own counts
+      const bool keep = (d & 0xFFFFu) || ((d >> 16) && preE + (x >> 16) >= m);
+      sPos[mk_pad(e)] = keep ? surv(x) + lo32 + (uint32_t)j : ~0u;
+      const uint32_t maj = (uint32_t)(key >> mb);
+      const uint32_t nxt = min(e + 1 == len && last ? nmaj : (uint32_t)(sK[e + 1] >> mb), nmaj);
+      if (nxt > maj) {  // majors that start after this element
+        const uint32_t sv = surv(xn) + lo32;
+        int jj = j;
+        for (uint32_t M = maj + 1; M <= nxt; ++M) {
+          const K mk = (K)M << mb;
+          while (jj < n_l && lkey(jj) < mk) ++jj;
+          a.off[M] = (int32_t)(sv + (uint32_t)jj);
+        }
+      }
+      x = xn;
+    }
+    const K nkey = sK[e1];  // the next element, or the next tile's first key
+    while (j < n_l && lkey(j) < nkey) {
+      if (record) sP[j] = (uint16_t)e1;
+      ++j;
+    }
+  };
+  if (lsm)
+    walk([&](int j) -> K { return sL[j]; }, (int)cnt, true);
+  else  // a list slice larger than shared memory (regrown positions crowded into one tile's range)
+    walk([&](int j) -> K { return (K)pol.list_key(lo + j); }, (int)cnt, false);
+  __syncthreads();
+  // kept and dropped elements, striped (coalesced writes)
+#pragma unroll
+  for (int i = 0; i < kMkItems; ++i) {
+    const int e = i * kMkThreads + tid;
+    if (e < len) {
+      const uint32_t pos = sPos[mk_pad(e)];
+      if (pos != ~0u) {
+        if ((int64_t)pos < a.n_out) pol.write_kept(it[i], base + e, pos, sK[e]);
+      } else {
+        pol.write_dropped(it[i], base + e);
+      }
+    }
   }
-  for (int q = threadIdx.x; q < la + lb; q += kMergeThreads) {
-    const int64_t o = d0 + q;
-    const int32_t s = oS[q];
-    const uint32_t rr = oR[q], cc = oC[q];
-    row_out[o] = (int32_t)rr;
-    col_out[o] = (int32_t)cc;
-    if (col16) col16[o] = (uint16_t)cc;
-    val_out[o] = s >= 0 ? val[s] : from_f32<TV>(0.f);
-    if (src_out) src_out[o] = s;
-    const int r_cur = (int)rr;
-    const int r_prev = q > 0 ? (int)oR[q - 1] : r_before;
-    for (int r = r_prev + 1; r <= r_cur && r <= out_f; ++r) rp[r] = (int32_t)o;
+  // the tile's list entries
+  for (int j = tid; j < (int)cnt; j += kMkThreads) {
+    const K key = lsm ? sL[j] : (K)pol.list_key(lo + j);
+    const int p = lsm ? (int)sP[j] : lb_seq([&](int i) { return sK[i]; }, len, key);
+    const uint32_t pos = lo32 + (uint32_t)j + surv(sX[mk_pad(p)]);
+    if ((int64_t)pos < a.n_out) pol.write_list(lo + j, key, pos);
   }
-  if (d1 == n && threadIdx.x == 0) {  // rows after the last stored weight
-    const int64_t r_last = la + lb > 0 ? (int64_t)oR[la + lb - 1] : r_before;
-    for (int64_t r = r_last + 1; r <= out_f; ++r) rp[r] = (int32_t)n;  // 64-bit: out_f may be 2^31 - 1
+}
+
+// The stored weights (row order) merged with the regrown positions: writes
+// the output pattern, values (+0 for the regrown), sources (-1 for the
+// regrown), 16-bit columns, and -- for the column-view update -- the output
+// index of every old weight (~0u when pruned) and of every regrown position
+// (by acceptance rank).  K: 32-bit keys when row and column bits fit 31.
+template <typename TV, typename K>
+struct RowPol {
+  using Key = K;
+  const int32_t *row, *col;
+  const TV *val;
+  const SelState *st;
+  int cbits;
+  const uint64_t *B;   // regrown positions, row order
+  const uint32_t *Bq;  // their acceptance ranks
+  int32_t *row_out, *col_out;
+  TV *val_out;
+  int32_t *src_out;  // or null
+  uint16_t *col16;   // or null
+  uint32_t *newidx;  // or null
+  uint32_t *gq;      // or null
+  struct Shared {
+    uint32_t unused;
+  };
+  struct Item {
+    TV v;
+  };
+  __device__ uint32_t ties_dropped() const { return st->remaining; }
+  __device__ void load(int64_t base, int len, bool, uint32_t, uint32_t, Item (&it)[kMkItems], uint32_t (&fl)[kMkItems],
+                       const PadKeys<K> &sK, Shared &) const {
+    const uint32_t t = st->prefix;
+    uint32_t r[kMkItems], c[kMkItems];
+#pragma unroll
+    for (int i = 0; i < kMkItems; ++i) {
+      const int e = i * kMkThreads + threadIdx.x;
+      if (e < len) {
+        r[i] = (uint32_t)ld_stream(row + base + e);
+        c[i] = (uint32_t)ld_stream(col + base + e);
+        it[i].v = ld_stream(val + base + e);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMkItems; ++i) {
+      const int e = i * kMkThreads + threadIdx.x;
+      fl[i] = 0u;
+      if (e < len) {
+        sK[e] = ((K)r[i] << cbits) | (K)c[i];
+        const uint32_t mk = mag_of(it[i].v);
+        fl[i] = (mk > t ? 1u : 0u) | (mk == t ? 0x10000u : 0u);
+      }
+    }
   }
+  __device__ void keys_blocked(int64_t, int, bool, uint32_t, uint32_t, const PadKeys<K> &, Shared &) const {}
+  __device__ uint64_t key_at_warp(int64_t k, uint32_t *) const {
+    return ((uint64_t)(uint32_t)row[k] << cbits) | (uint32_t)col[k];
+  }
+  __device__ uint64_t list_key(int64_t j) const { return B[j]; }
+  __device__ void write_kept(const Item &x, int64_t k, uint32_t pos, K key) const {
+    const uint32_t c = (uint32_t)(key & (((K)1 << cbits) - 1));
+    row_out[pos] = (int32_t)(key >> cbits);
+    col_out[pos] = (int32_t)c;
+    val_out[pos] = x.v;
+    if (src_out) src_out[pos] = (int32_t)k;
+    if (col16) col16[pos] = (uint16_t)c;
+    if (newidx) newidx[k] = pos;
+  }
+  __device__ void write_dropped(const Item &, int64_t k) const {
+    if (newidx) newidx[k] = ~0u;
+  }
+  __device__ void write_list(int64_t j, K key, uint32_t pos) const {
+    const uint32_t c = (uint32_t)(key & (((K)1 << cbits) - 1));
+    row_out[pos] = (int32_t)(key >> cbits);
+    col_out[pos] = (int32_t)c;
+    val_out[pos] = from_f32<TV>(0.f);
+    if (src_out) src_out[pos] = -1;
+    if (col16) col16[pos] = (uint16_t)c;
+    if (gq) gq[Bq[j]] = pos;
+  }
+};
+
+// The current column view (column order: rows, storage indices, column
+// offsets) merged with the regrown positions in column order (col << rbits |
+// row, 32-bit), into the second view: kept entries take their weight's new
+// storage index, regrown ones theirs.
+struct ColPol {
+  using Key = uint32_t;
+  const int32_t *cp;       // [in_f + 1] current column offsets
+  const int32_t *row_t;    // current rows in column order
+  const uint16_t *rowt16;  // or null
+  const int32_t *src_t;    // current storage indices in column order
+  const uint32_t *newidx;
+  int rbits;
+  int32_t in_f;
+  const uint32_t *gc_key, *gc_q, *gq;
+  int32_t *row_t_new, *src_t_new;
+  uint16_t *rowt16_new;  // or null
+  static constexpr int kCpCap = 1024;  // column offsets of a tile staged in shared memory
+  struct Shared {
+    int32_t cp[kCpCap];
+  };
+  struct Item {
+    uint32_t nk;
+  };
+  __device__ uint32_t ties_dropped() const { return 0u; }
+  // rows into sK (the columns follow, blocked), the tile's column offsets
+  // cp[c0 .. c1 + 1] into shared memory, each entry's weight's new index
+  __device__ void load(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next, Item (&it)[kMkItems],
+                       uint32_t (&fl)[kMkItems], const PadKeys<uint32_t> &sK, Shared &ps) const {
+    const int64_t ncp = (int64_t)(last ? (uint32_t)in_f - 1 : c_next) - c0 + 2;
+    if (ncp <= kCpCap)
+      for (int i = threadIdx.x; i < ncp; i += kMkThreads) ps.cp[i] = cp[c0 + i];
+    uint32_t src[kMkItems];
+#pragma unroll
+    for (int i = 0; i < kMkItems; ++i) {
+      const int e = i * kMkThreads + threadIdx.x;
+      if (e < len) {
+        src[i] = (uint32_t)ld_stream(src_t + base + e);
+        sK[e] = rowt16 ? (uint32_t)ld_stream(rowt16 + base + e) : (uint32_t)ld_stream(row_t + base + e);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMkItems; ++i) {
+      const int e = i * kMkThreads + threadIdx.x;
+      fl[i] = 0u;
+      if (e < len) {
+        it[i].nk = newidx[src[i]];
+        fl[i] = it[i].nk != ~0u ? 1u : 0u;
+      }
+    }
+  }
+  // columns, blocked (thread t: entries 8t .. 8t+7): one search, then forward steps
+  __device__ void keys_blocked(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next,
+                               const PadKeys<uint32_t> &sK, Shared &ps) const {
+    const int64_t ncp = (int64_t)(last ? (uint32_t)in_f - 1 : c_next) - c0 + 2;
+    const bool sm = ncp <= kCpCap;
+    auto cpx = [&](int64_t x) -> int64_t { return sm ? ps.cp[x] : cp[c0 + x]; };
+    const int e0 = threadIdx.x * kMkItems;
+    if (e0 >= len) return;
+    const int e1 = min(e0 + kMkItems, len);
+    int64_t lo = 0, hi = ncp - 1;  // last x with cpx(x) <= base + e0, in [0, ncp - 2]
+    while (hi - lo > 1) {
+      const int64_t md = (lo + hi) >> 1;
+      if (cpx(md) <= base + e0)
+        lo = md;
+      else
+        hi = md;
+    }
+    for (int e = e0; e < e1; ++e) {
+      while (cpx(lo + 1) <= base + e) ++lo;
+      sK[e] |= (c0 + (uint32_t)lo) << rbits;
+    }
+  }
+  // column of entry e: the number of columns c >= 1 whose offset cp[c] is at most e
+  __device__ uint64_t key_at_warp(int64_t e, uint32_t *aux) const {
+    const uint32_t c =
+        (uint32_t)lb_warp([&](int64_t j) { return (uint64_t)(uint32_t)cp[j + 1]; }, in_f, (uint64_t)e + 1);
+    *aux = c;
+    const uint32_t r = rowt16 ? (uint32_t)rowt16[e] : (uint32_t)row_t[e];
+    return ((uint64_t)c << rbits) | r;
+  }
+  __device__ uint64_t list_key(int64_t j) const { return gc_key[j]; }
+  __device__ void write_kept(const Item &x, int64_t, uint32_t pos, uint32_t key) const {
+    const uint32_t r = key & ((1u << rbits) - 1u);
+    row_t_new[pos] = (int32_t)r;
+    src_t_new[pos] = (int32_t)x.nk;
+    if (rowt16_new) rowt16_new[pos] = (uint16_t)r;
+  }
+  __device__ void write_dropped(const Item &, int64_t) const {}
+  __device__ void write_list(int64_t j, uint32_t key, uint32_t pos) const {
+    const uint32_t r = key & ((1u << rbits) - 1u);
+    row_t_new[pos] = (int32_t)r;
+    src_t_new[pos] = (int32_t)gq[gc_q[j]];
+    if (rowt16_new) rowt16_new[pos] = (uint16_t)r;
+  }
+};
+
+// a column-view entry is kept when its weight survived
+struct ColKeep {
+  const int32_t *src_t;
+  const uint32_t *newidx;
+  __device__ uint64_t operator()(int64_t e) const { return newidx[src_t[e]] != ~0u ? 1ull : 0ull; }
+};
+
+// per-tile packed keep counts of f; exclusive prefixes in place when there are
+// more tiles than each merge block adds up itself
+template <typename F>
+cudaError_t keep_sums(F f, int64_t n, uint64_t *sums, cudaStream_t s, bool *direct) {
+  const int64_t nb = ceil_div(n, kScanTile);
+  launch_pdl(k_scan_reduce<uint64_t, F>, (unsigned)nb, kScanThreads, 0, s, f, n, sums);
+  *direct = nb <= kScanDirectTiles;
+  if (!*direct) launch_pdl(k_scan_spine<uint64_t>, 1, kScanThreads, 0, s, sums, nb, (uint64_t *)nullptr);
+  return cudaGetLastError();
+}
+
+template <class Pol>
+cudaError_t launch_merge(const Pol &pol, const MkArgs &a, bool direct, cudaStream_t s) {
+  constexpr size_t dyn = mk_smem_bytes<Pol>();
+  const unsigned grid = (unsigned)ceil_div(a.n, kMkTile);
+  cudaError_t e;
+  if (direct) {
+    e = raise_smem_limit(k_merge_kept<Pol, true>, dyn);
+    if (e == cudaSuccess) e = launch_pdl(k_merge_kept<Pol, true>, grid, kMkThreads, dyn, s, pol, a);
+  } else {
+    e = raise_smem_limit(k_merge_kept<Pol, false>, dyn);
+    if (e == cudaSuccess) e = launch_pdl(k_merge_kept<Pol, false>, grid, kMkThreads, dyn, s, pol, a);
+  }
+  return e;
 }
 
 unsigned grid_for(int64_t n, int threads, int64_t cap = 65535 * 8) {
@@ -598,10 +987,10 @@ double expected_draws(double n_pos, double empty, double need) {
 }
 
 struct RWs {
-  size_t state, dstate, scan, scan2, surv_pos, surv_src, grown_a, grown_b, cand, flags, hkeys, hmin, radix, part, bcnt,
-      boffs, bslots, total;
-  int64_t d_max, cap, n_merge_tiles;
-  uint32_t n_bkt;  // sort buckets of the regrown positions
+  size_t state, dstate, sums, scan2, grown_a, B, Bq, cand, flags, hkeys, hmin, bcnt, bnd, bkey, bq, rk0, rv0, rk1,
+      rv1, rtemp, plan, total;
+  int64_t d_max, cap;
+  uint32_t n_bkt;  // buckets per order (row, column)
 };
 
 RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
@@ -614,155 +1003,253 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   int64_t cap = 16;
   while (cap < w.d_max + w.d_max / 4 + 16) cap <<= 1;  // load factor below 0.8 even if every draw is made
   w.cap = cap;
-  w.n_merge_tiles = (nnz + kMergeTile - 1) / kMergeTile;
-  const size_t n = (size_t)(nnz > 0 ? nnz : 1), np = (size_t)(n_prune > 0 ? n_prune : 1);
+  const size_t np = (size_t)(n_prune > 0 ? n_prune : 1), dmx = (size_t)(w.d_max > 0 ? w.d_max : 1);
+  w.n_bkt = (uint32_t)((int64_t)np / kBktTarget > 0 ? (int64_t)np / kBktTarget : 1);
+  if (w.n_bkt > (1u << 30)) w.n_bkt = 1u << 30;
   size_t o = 0;
   w.state = o;
   o += align_up(sizeof(SelState), kAlign);
   w.dstate = o;
   o += align_up(sizeof(DrawState), kAlign);
-  w.scan = o;
+  w.sums = o;
   o += scan_temp_bytes<uint64_t>(nnz > 0 ? nnz : 1);
-  w.scan2 = o;  // the accept scan, then the column histogram's scan
-  const int64_t col_scan = ceil_div(nnz > 0 ? nnz : 1, kRadixTile) * kRadixBins;
-  o += scan_temp_bytes<uint32_t>(w.d_max > col_scan ? w.d_max : col_scan);
-  w.surv_pos = o;
-  o += align_up(8 * n, kAlign);
-  w.surv_src = o;
-  o += align_up(4 * n, kAlign);
+  w.scan2 = o;
+  o += scan_temp_bytes<uint32_t>((int64_t)dmx);
   w.grown_a = o;
   o += align_up(8 * np, kAlign);
-  w.grown_b = o;
+  w.B = o;
   o += align_up(8 * np, kAlign);
+  w.Bq = o;
+  o += align_up(4 * np, kAlign);
   w.cand = o;
-  o += align_up(8 * (size_t)(w.d_max > 0 ? w.d_max : 1), kAlign);
+  o += align_up(8 * dmx, kAlign);
   w.flags = o;
-  o += align_up(4 * (size_t)(w.d_max > 0 ? w.d_max : 1), kAlign);
+  o += align_up(4 * dmx, kAlign);
   w.hkeys = o;
   o += align_up(8 * (size_t)cap, kAlign);
   w.hmin = o;
   o += align_up(4 * (size_t)cap, kAlign);
-  w.radix = o;
-  o += bucket_sort_temp_bytes((int64_t)np);
-  w.part = o;
-  o += align_up(8 * (size_t)(w.n_merge_tiles + 2), kAlign);
-  w.n_bkt = (uint32_t)((int64_t)np / kBktTarget > 0 ? (int64_t)np / kBktTarget : 1);
-  w.bcnt = o;
-  o += align_up(4 * ((size_t)w.n_bkt + 1), kAlign);
-  w.boffs = o;
-  o += align_up(4 * ((size_t)w.n_bkt + 1), kAlign);
-  w.bslots = o;
-  o += align_up(8 * (size_t)w.n_bkt * kBktCap, kAlign);
+  const bool bk = w.n_bkt <= kBktMaxBuckets;
+  w.bcnt = o;  // both orders' bucket counts, one launch clears them
+  if (bk) o += align_up(4 * 2 * (size_t)w.n_bkt * kCntStride, kAlign);
+  w.bnd = o;  // tile bounds of the merge
+  o += align_up(sizeof(MkBound) * (size_t)(ceil_div(nnz > 0 ? nnz : 1, kMkTile) + 1), kAlign);
+  // the buckets' slots, or (the general sort) its key / rank buffers
+  const size_t region = o;
+  w.bkey = o;
+  if (bk) o += align_up(8 * 2 * (size_t)w.n_bkt * kBktCap, kAlign);
+  w.bq = o;
+  if (bk) o += align_up(4 * 2 * (size_t)w.n_bkt * kBktCap, kAlign);
+  const size_t bucket_end = o;
+  o = region;
+  w.rk0 = o;
+  o += align_up(8 * np, kAlign);
+  w.rv0 = o;
+  o += align_up(4 * np, kAlign);
+  w.rk1 = o;
+  o += align_up(8 * np, kAlign);
+  w.rv1 = o;
+  o += align_up(4 * np, kAlign);
+  w.rtemp = o;
+  o += radix_temp_bytes((int64_t)np);
+  if (o < bucket_end) o = bucket_end;
+  w.plan = o;  // a plan rebuild's scratch (layers without the column-view update)
+  o += plan_build_ws_bytes(out_f, in_f, nnz);
   w.total = o;
   return w;
 }
 
 template <typename TV>
-snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s, bool *updated) {
+  *updated = false;
   const RWs W = rws_layout(a.out_f, a.in_f, a.nnz, a.n_prune);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
   SelState *st = reinterpret_cast<SelState *>(b + W.state);
-  void *stemp = b + W.scan;
-  uint64_t *surv_pos = reinterpret_cast<uint64_t *>(b + W.surv_pos);
-  uint32_t *surv_src = reinterpret_cast<uint32_t *>(b + W.surv_src);
+  DrawState *ds = reinterpret_cast<DrawState *>(b + W.dstate);
+  uint64_t *sums = reinterpret_cast<uint64_t *>(b + W.sums);
+  void *stemp2 = b + W.scan2;
   uint64_t *grown_a = reinterpret_cast<uint64_t *>(b + W.grown_a);
-  uint64_t *grown_b = reinterpret_cast<uint64_t *>(b + W.grown_b);
+  uint64_t *B = reinterpret_cast<uint64_t *>(b + W.B);
+  uint32_t *Bq = reinterpret_cast<uint32_t *>(b + W.Bq);
   uint64_t *cand = reinterpret_cast<uint64_t *>(b + W.cand);
+  uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
   uint64_t *hkeys = reinterpret_cast<uint64_t *>(b + W.hkeys);
   uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
-  uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
-  int64_t *part = reinterpret_cast<int64_t *>(b + W.part);
   uint32_t *bcnt = reinterpret_cast<uint32_t *>(b + W.bcnt);
-  uint32_t *boffs = reinterpret_cast<uint32_t *>(b + W.boffs);
-  uint64_t *bslots = reinterpret_cast<uint64_t *>(b + W.bslots);
+  const PlanPtrs &pl = *a.plan;
   const TV *val = reinterpret_cast<const TV *>(a.val);
-  const int64_t nnz = a.nnz, n_prune = a.n_prune, n_surv = nnz - n_prune;
+  const int64_t nnz = a.nnz, n_prune = a.n_prune;
   const uint64_t n_pos = (uint64_t)a.out_f * (uint64_t)a.in_f;
   // positions travel as keys (row << cbits) | col: same order as row * in_f + col
-  const int cbits = bits_for((uint64_t)(a.in_f - 1));
+  const int cbits = bits_for((uint64_t)(a.in_f - 1)), rbits = bits_for((uint64_t)(a.out_f - 1));
   const uint64_t key_space = (uint64_t)a.out_f << cbits;
-  // the column view's first-level histogram and offsets are made from the
-  // merge's split points on the second stream, beside the merge
-  int cshift = 0;
-  const bool col_offs = a.cv_offs && a.cv_hist && colview_digits(a.out_f, a.in_f, nnz, &cshift);
-  const int64_t cnb = ceil_div(nnz, kRadixTile);
-  uint32_t *coffs = a.cv_offs;
-  uint32_t *chist = a.cv_hist;
+  const int kbits = cbits + rbits;
+  const bool update = a.update && pl.newidx && kbits <= 32 && n_prune <= pl.cv_pmax;
+  const bool buckets = n_prune > 0 && W.n_bkt <= kBktMaxBuckets;
+  BucketSet br{}, bc{};
+  if (buckets) {
+    uint64_t *bkey = reinterpret_cast<uint64_t *>(b + W.bkey);
+    uint32_t *bq = reinterpret_cast<uint32_t *>(b + W.bq);
+    const size_t per = (size_t)W.n_bkt * kBktCap;
+    br = BucketSet{bcnt, bkey, bq, bucket_mult(W.n_bkt, key_space), W.n_bkt};
+    if (update)
+      bc = BucketSet{bcnt + (size_t)W.n_bkt * kCntStride, bkey + per, bq + per,
+                     bucket_mult(W.n_bkt, (uint64_t)a.in_f << rbits), W.n_bkt};
+  }
   cudaError_t e;
-#define SNACK_TRY(x)                       \
-  do {                                     \
-    e = (x);                               \
+#define SNACK_TRY(x)                             \
+  do {                                           \
+    e = (x);                                     \
     if (e != cudaSuccess) return SNACK_ERR_CUDA; \
   } while (0)
 
   // Two branches meet at the merge: the regrow (draws, acceptance, sort of
-  // the grown positions) depends only on the old pattern and runs on the
-  // handle's second stream, beside the prune select and the survivor scan on
-  // the caller's stream.  The host reads each draw chunk's accepted count
-  // from mapped pinned words that a kernel writes (an event on the second
-  // stream marks them ready) while the device goes on.  Every return after the fork joins the branches first, so no
-  // work on the second stream outlives the call's work on s.
+  // the regrown positions) depends only on the old pattern and runs on the
+  // handle's second stream, beside the prune select on the caller's stream.
+  // The host reads each draw chunk's accepted count from mapped pinned words
+  // that a kernel writes (an event marks them ready).
   cudaStream_t s2 = a.aux;
-  DrawState *ds = reinterpret_cast<DrawState *>(b + W.dstate);
-  void *stemp2 = b + W.scan2;
-  SNACK_TRY(cudaEventRecord(a.ev_fork, s));
-  SNACK_TRY(cudaStreamWaitEvent(s2, a.ev_fork, 0));
+  auto fork = [&]() -> cudaError_t {
+    cudaError_t err = cudaEventRecord(a.ev_fork, s);
+    return err != cudaSuccess ? err : cudaStreamWaitEvent(s2, a.ev_fork, 0);
+  };
   auto join = [&]() -> cudaError_t {
     cudaError_t err = cudaEventRecord(a.ev_join, s2);
-    if (err != cudaSuccess) return err;
-    return cudaStreamWaitEvent(s, a.ev_join, 0);
+    return err != cudaSuccess ? err : cudaStreamWaitEvent(s, a.ev_join, 0);
   };
+  SNACK_TRY(fork());
   const uint64_t base = sm64_finalise(a.seed ^ sm64_finalise(a.step));
-  const double bscale = (double)W.n_bkt / (double)key_space;  // position keys are < key_space
   const double empty = (double)n_pos - (double)nnz;
   int64_t done = 0, acc = 0;
-  auto draw_chunk = [&](int64_t m) -> cudaError_t {
-    launch_pdl(k_draw, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, a.rp_old, a.col, cand,
-                                             hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
-    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin, (uint64_t)(W.cap - 1),
-                                                     flags);
-    const AcceptOut out{grown_a, acc, n_prune, bcnt, bslots, bscale, W.n_bkt, &ds->bucket_overflow};
-    cudaError_t err = scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, out, &ds->total, stemp2, s2);
-    if (err != cudaSuccess) return err;
-    launch_pdl(k_bkt_scan, 1, kBktScanThreads, 0, s2, bcnt, W.n_bkt, boffs, (const DrawState *)ds, a.counts_dev);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    return cudaEventRecord(a.counts_ready, s2);
+  auto draw_chunk = [&](int64_t m, bool first) -> cudaError_t {
+    if (pl.col16)
+      launch_pdl(k_draw<uint16_t>, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, pl.rp,
+                 (const uint16_t *)pl.col16, cand, hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
+    else
+      launch_pdl(k_draw<int32_t>, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, pl.rp,
+                 a.col, cand, hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
+    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin,
+               (uint64_t)(W.cap - 1), flags);
+    cudaError_t err =
+        scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune}, &ds->total,
+                                stemp2, s2);
+    if (err != cudaSuccess || !first || !buckets) return err;
+    launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds, n_prune,
+               br, 0, cbits, rbits, &ds->bucket_overflow);
+    return cudaGetLastError();
   };
   auto chunk_size = [&]() -> int64_t {
     double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
     int64_t m = (int64_t)ceil(want);
     return m > W.d_max - done ? W.d_max - done : m;
   };
-  int64_t m = 0;
-  cudaError_t e2 = cudaSuccess;
-  // When at least twice n_prune positions are empty the first chunk is all but
-  // certain to accept enough, so the sort of the regrown positions is queued
-  // right behind it, before the host has read the count (and redone if more
-  // chunks turn out to be needed).
-  const bool speculative = n_prune > 1 && (double)n_pos - (double)nnz >= 2.0 * (double)n_prune;
-  // The first chunk's accepted positions already sit in their buckets
-  // (AcceptOut): bucket offsets, then a rank inside each bucket, with slots
-  // the chunk left empty filled past key_space.  After more chunks, or when a
-  // bucket overflowed, the whole list is sorted the general way.
-  auto sort_grown = [&](bool first_chunk_only) -> cudaError_t {
-    if (!first_chunk_only)  // every slot filled by accepted draws
-      return bucket_sort_u64(grown_a, n_prune, key_space - 1, grown_b, b + W.radix, s2);
-    launch_pdl(k_bkt_rank, (W.n_bkt + 7) / 8, 256, 0, s2, bslots, bcnt, boffs, W.n_bkt, n_prune, key_space, grown_b);
-    return cudaGetLastError();
+  // general sorts of the n_prune regrown positions: row order, column order
+  uint64_t *rk0 = reinterpret_cast<uint64_t *>(b + W.rk0), *rk1 = reinterpret_cast<uint64_t *>(b + W.rk1);
+  uint32_t *rv0 = reinterpret_cast<uint32_t *>(b + W.rv0), *rv1 = reinterpret_cast<uint32_t *>(b + W.rv1);
+  auto sort_rows_general = [&]() -> cudaError_t {
+    return radix_sort_custom<uint64_t>(GrownRowSrc{grown_a}, ArrayDst<uint64_t>{B, Bq}, n_prune, kbits, rk0, rv0, rk1,
+                                       rv1, b + W.rtemp, s2);
   };
+  auto sort_cols_general = [&]() -> cudaError_t {
+    if (!update) return cudaSuccess;
+    return radix_sort_custom<uint32_t>(GrownColSrc{grown_a, cbits, rbits}, ArrayDst<uint32_t>{pl.gc_key, pl.gc_q},
+                                       n_prune, kbits, reinterpret_cast<uint32_t *>(rk0), rv0,
+                                       reinterpret_cast<uint32_t *>(rk1), rv1, b + W.rtemp, s2);
+  };
+  const int64_t n_tiles = ceil_div(nnz, kMkTile);
+  const uint32_t *row_guard = n_prune > 0 ? &ds->lists_ok : nullptr;
+  const uint32_t *col_guard = n_prune > 0 ? &ds->col_ok : nullptr;
+  // 3: the merge (after s waits for the row-order list) and the plan's row half
+  bool row_direct = true;  // set with the keep counts below, before the first call
+  auto queue_rows = [&]() -> cudaError_t {
+    const MkBound *rbnd = reinterpret_cast<MkBound *>(b + W.bnd);
+    const uint32_t *nix = nullptr;
+    cudaError_t err;
+    auto run = [&](auto rpol) -> cudaError_t {
+      using P = decltype(rpol);
+      launch_pdl(k_bounds<P>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s, rpol, n_prune, n_tiles,
+                 const_cast<MkBound *>(rbnd));
+      cudaError_t r = cudaGetLastError();
+      return r != cudaSuccess ? r
+                              : launch_merge(rpol, MkArgs{nnz, n_prune, nnz, rbnd, sums, row_guard, cbits, a.out_f, pl.rp},
+                                             row_direct, s);
+    };
+    (void)nix;
+    TV *vo = reinterpret_cast<TV *>(a.val_out);
+    uint32_t *ni = update ? pl.newidx : nullptr, *gq = update ? pl.gq : nullptr;
+    if (kbits <= 31)
+      err = run(RowPol<TV, uint32_t>{a.row, a.col, val, st, cbits, B, Bq, a.row_out, a.col_out, vo, a.src_out,
+                                     pl.col16, ni, gq});
+    else
+      err = run(RowPol<TV, uint64_t>{a.row, a.col, val, st, cbits, B, Bq, a.row_out, a.col_out, vo, a.src_out,
+                                     pl.col16, ni, gq});
+    if (err != cudaSuccess) return err;
+    return build_plan(a.out_f, a.in_f, nnz, a.row_out, a.col_out, pl, a.gf, a.gt, b + W.plan, s, kPlanRowsReady,
+                      !update);
+  };
+  // 4: the column-view update, on s2 after s's work so far
+  auto queue_cols = [&]() -> cudaError_t {
+    cudaError_t err = fork();
+    if (err != cudaSuccess) return err;
+    const ColPol cpol{pl.cp, pl.row_t, pl.rowt16, pl.src_t, pl.newidx, rbits, a.in_f, pl.gc_key, pl.gc_q, pl.gq,
+                      pl.row_t_alt, pl.src_t_alt, pl.rowt16_alt};
+    MkBound *cbnd = reinterpret_cast<MkBound *>(pl.cv_bnd);
+    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s2, cpol, n_prune, n_tiles, cbnd);
+    bool cdirect = true;
+    err = keep_sums(ColKeep{pl.src_t, pl.newidx}, nnz, pl.cv_sums, s2, &cdirect);
+    if (err != cudaSuccess) return err;
+    err = launch_merge(cpol, MkArgs{nnz, n_prune, nnz, cbnd, pl.cv_sums, col_guard, rbits, a.in_f, pl.cp_alt},
+                       cdirect, s2);
+    if (err != cudaSuccess) return err;
+    return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s2);
+  };
+  auto mark = [&]() -> cudaError_t { return cudaEventRecord(a.ev_join, s2); };  // s joins s2 here
+  auto wait_mark = [&]() -> cudaError_t { return cudaStreamWaitEvent(s, a.ev_join, 0); };
+
+  // 2. regrow, first chunk, and its sorted lists (on s2): the row-order list
+  //    is what the merge waits for; the column-order list is made after it,
+  //    beside the merge
+  int64_t m = 0;
+  e = cudaSuccess;
   if (n_prune > 0) {
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, hkeys, hmin, (int64_t)W.cap, bcnt,
-               (int64_t)W.n_bkt);
-    e2 = cudaGetLastError();
-    if (e2 == cudaSuccess) {
-      m = chunk_size();
-      e2 = draw_chunk(m);
+               (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0));
+    m = chunk_size();
+    e = draw_chunk(m, true);
+    if (e == cudaSuccess) {
+      const bool k32 = kbits <= 32;
+      if (buckets) {
+        launch_pdl(k_bkt_rank, (br.nb + 7) / 8, 256, 0, s2, br, RankDst{B, nullptr, Bq}, n_prune, ds,
+                   update ? (uint32_t *)nullptr : a.counts_dev, k32);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = mark();
+        if (e == cudaSuccess && update) {
+          launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds,
+                     n_prune, bc, 1, cbits, rbits, &ds->col_overflow);
+          launch_pdl(k_bkt_rank, (bc.nb + 7) / 8, 256, 0, s2, bc, RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds,
+                     a.counts_dev, true);
+          e = cudaGetLastError();
+        }
+      } else {
+        e = sort_rows_general();
+        if (e == cudaSuccess) e = sort_cols_general();
+        if (e == cudaSuccess) {
+          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1);
+          e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) e = mark();
+      }
     }
-    if (e2 == cudaSuccess && speculative) e2 = sort_grown(true);
+    if (e == cudaSuccess) e = cudaEventRecord(a.counts_ready, s2);
+  } else {
+    e = mark();
   }
-  // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low
+  if (e != cudaSuccess) {
+    join();
+    return SNACK_ERR_CUDA;
+  }
+  // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low; keep counts per tile
   launch_pdl(k_sel_init, 1, 256, 0, s, st, (uint32_t)n_prune);
   if (n_prune > 0) {
     const unsigned g = grid_for((nnz + 15) / 16, 256, 1184);
@@ -770,75 +1257,89 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     launch_pdl(k_sel_pass<TV, 1>, g, 256, 0, s, val, nnz, st);
     launch_pdl(k_sel_pass<TV, 2>, g, 256, 0, s, val, nnz, st);
   }
-  // 2. survivors
-  e = cudaGetLastError();
-  if (e == cudaSuccess)
-    e = scan_apply_pl<uint64_t>(KeepVal<TV>{val, st}, PosPayload{a.row, a.col, cbits}, nnz,
-                                KeepOut{st, surv_pos, surv_src}, (uint64_t *)nullptr, stemp, s);
-  if (e != cudaSuccess || e2 != cudaSuccess) {
+  e = keep_sums(KeepVal<TV>{val, st}, nnz, sums, s, &row_direct);
+  // With the update, 3 and 4 are queued at once behind the lists' flags (they
+  // write nothing unless the first chunk's lists came out whole); a plan
+  // rebuild on s cannot be undone, so without the update they wait for the
+  // host's verdict.
+  if (e == cudaSuccess && update) e = wait_mark();
+  if (e == cudaSuccess && update) e = queue_rows();
+  if (e == cudaSuccess && update) e = queue_cols();
+  if (e != cudaSuccess) {
     join();
     return SNACK_ERR_CUDA;
   }
-  // 3. regrow: further chunks only when the first fell short (rare)
   snack_status verdict = SNACK_OK;
-  bool resort = !speculative;
-  while (n_prune > 0) {
+  bool rows_queued = update, cols_queued = update;
+  if (n_prune > 0) {
     if (cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
-      verdict = SNACK_ERR_CUDA;
-      break;
+      join();
+      return SNACK_ERR_CUDA;
     }
-    if (a.host_counts[1]) {
-      verdict = SNACK_ERR_WORKSPACE;
-      break;
+    if (a.host_counts[1]) {  // the position table ran full (nothing of the output was written)
+      join();
+      return SNACK_ERR_WORKSPACE;
     }
-    acc += a.host_counts[0];
-    done += m;
-    if (a.host_counts[2]) resort = true;  // a bucket overflowed: sort the list the general way
-    if (acc >= n_prune) break;
-    if (done >= W.d_max) {
-      verdict = SNACK_ERR_NO_SPACE;
-      break;
-    }
-    m = chunk_size();
-    resort = true;
-    if (draw_chunk(m) != cudaSuccess) {
-      verdict = SNACK_ERR_CUDA;
-      break;
-    }
-  }
-  // 4. sort regrown positions (bucket sort: they are uniform over the empty
-  //    positions), then join and merge with the survivors
-  const uint64_t *grown = n_prune > 1 ? grown_b : grown_a;
-  if (verdict == SNACK_OK && n_prune > 1 && resort && sort_grown(false) != cudaSuccess) verdict = SNACK_ERR_CUDA;
-  if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
-  if (verdict != SNACK_OK) return verdict;
-  if (nnz > 0) {
-    launch_pdl(k_merge_splits, grid_for(32 * (W.n_merge_tiles + 1), 256), 256, 0, s, surv_pos, n_surv, grown, n_prune,
-                                                                              W.n_merge_tiles, part);
-    if (col_offs) {  // fork: the column histogram and its scan beside the merge, into the plan, for the
-                     // column-view rebuild that follows on the second stream
-      SNACK_TRY(cudaEventRecord(a.ev_fork, s));
-      SNACK_TRY(cudaStreamWaitEvent(s2, a.ev_fork, 0));
-      launch_pdl(k_col_hist, (unsigned)cnb, 256, 0, s2, (const uint64_t *)surv_pos, grown, (const int64_t *)part,
-                 W.n_merge_tiles, nnz, cbits, cshift, chist, cnb);
-      e = scan_apply<uint32_t>(HistRead{chist}, cnb * kRadixBins, WriteExcl32{coffs}, (uint32_t *)nullptr, stemp2, s2);
-      if (e != cudaSuccess) {
-        join();
-        return SNACK_ERR_CUDA;
+    acc = a.host_counts[0] < (uint32_t)n_prune ? (int64_t)a.host_counts[0] : n_prune;
+    done = m;
+    if (acc < n_prune || a.host_counts[2]) {
+      // the first chunk fell short or a row-order bucket ran over: more draws
+      // (after everything queued so far), the general sorts, and 3 and 4 again
+      rows_queued = cols_queued = false;
+      SNACK_TRY(fork());
+      while (acc < n_prune) {
+        if (done >= W.d_max) {
+          verdict = SNACK_ERR_NO_SPACE;
+          break;
+        }
+        m = chunk_size();
+        if (draw_chunk(m, false) != cudaSuccess) {
+          verdict = SNACK_ERR_CUDA;
+          break;
+        }
+        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0);
+        if (cudaGetLastError() != cudaSuccess || cudaEventRecord(a.counts_ready, s2) != cudaSuccess ||
+            cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
+          verdict = SNACK_ERR_CUDA;
+          break;
+        }
+        if (a.host_counts[1]) {
+          verdict = SNACK_ERR_WORKSPACE;
+          break;
+        }
+        acc += a.host_counts[0];
+        done += m;
       }
+      if (verdict == SNACK_OK && (sort_rows_general() != cudaSuccess || sort_cols_general() != cudaSuccess))
+        verdict = SNACK_ERR_CUDA;
+      if (verdict == SNACK_OK) {
+        launch_pdl(k_set_word, 1, 1, 0, s2, &ds->lists_ok, 1u);
+        launch_pdl(k_set_word, 1, 1, 0, s2, &ds->col_ok, 1u);
+        if (cudaGetLastError() != cudaSuccess) verdict = SNACK_ERR_CUDA;
+      }
+      if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
+      if (verdict != SNACK_OK) return verdict;
+    } else if (update && a.host_counts[3]) {
+      // only a column-order bucket ran over: the merge has written the
+      // output; the column-order list the general way and 4 again
+      cols_queued = false;
+      SNACK_TRY(fork());
+      SNACK_TRY(sort_cols_general());
+      launch_pdl(k_set_word, 1, 1, 0, s2, &ds->col_ok, 1u);
+      SNACK_TRY(cudaGetLastError());
     }
-    launch_pdl(k_merge<TV>, (unsigned)W.n_merge_tiles, kMergeThreads, 0, s, surv_pos, surv_src, n_surv, grown, n_prune,
-               part, cbits, a.out_f, val, a.row_out, a.col_out, reinterpret_cast<TV *>(a.val_out), a.src_out, a.rp_new,
-               a.col16_new);
-    // the column histogram read the merge's inputs and scanned in the
-    // workspace: it is ordered on s before the call returns
-    if (col_offs) SNACK_TRY(join());
   }
-  SNACK_TRY(cudaGetLastError());
+  if (!rows_queued) {
+    SNACK_TRY(wait_mark());
+    SNACK_TRY(queue_rows());
+  }
+  if (update && !cols_queued) SNACK_TRY(queue_cols());
+  *updated = update;
 #undef SNACK_TRY
   return SNACK_OK;
 }
 
+// ------------------------------------------------------------------------
 // ------------------------------------------------------------------------
 // Per-row (constant fan-in) restructure: every row prunes its
 // p = min(n_per_row, length) smallest (|w|, k) and regrows p columns of the
@@ -1072,13 +1573,8 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
 
 }  // namespace
 
-// The restructure's own scratch, or the plan rebuild's when that is larger
-// (the rebuild runs on the caller's stream for layers whose column view is
-// not rebuilt on the second stream).
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
-  size_t r = rws_layout(out_f, in_f, nnz, n_prune).total;
-  size_t p = plan_build_ws_bytes(out_f, in_f, nnz);
-  return align_up(r > p ? r : p, kAlign);
+  return align_up(rws_layout(out_f, in_f, nnz, n_prune).total, kAlign);
 }
 
 snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) {
@@ -1109,9 +1605,9 @@ snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) 
   return SNACK_OK;
 }
 
-snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s) {
-  if (a.val_t == SNACK_BF16) return restructure_impl<bf16>(a, ws, ws_bytes, s);
-  return restructure_impl<float>(a, ws, ws_bytes, s);
+snack_status run_restructure(const RestructureArgs &a, void *ws, size_t ws_bytes, cudaStream_t s, bool *updated) {
+  if (a.val_t == SNACK_BF16) return restructure_impl<bf16>(a, ws, ws_bytes, s, updated);
+  return restructure_impl<float>(a, ws, ws_bytes, s, updated);
 }
 
 }  // namespace snack

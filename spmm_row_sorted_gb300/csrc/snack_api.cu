@@ -658,13 +658,14 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.row = row;
   a.col = col;
   a.val = val;
-  a.rp_old = h->p.rp;
-  a.rp_new = h->p.rp;
-  a.col16_new = h->p.col16;
   a.row_out = row_out;
   a.col_out = col_out;
   a.val_out = val_out;
   a.src_out = src_out;
+  a.plan = &h->p;
+  a.gf = h->lay.gf;
+  a.gt = h->lay.gt;
+  a.update = h->lay.cv && n_prune <= h->lay.cv_pmax;
   if (!readback_ready(h)) return SNACK_ERR_CUDA;
   if (!h->ev_fork && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
@@ -686,17 +687,17 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.aux = h->aux;
   a.ev_fork = h->ev_fork;
   a.ev_join = h->ev_join;
-  a.cv_offs = h->p.cv_offs;
-  a.cv_hist = h->p.cv_hist;
-  snack_status st = run_restructure(a, ws, ws_bytes, s);
+  bool updated = false;
+  snack_status st = run_restructure(a, ws, ws_bytes, s, &updated);
   if (st == SNACK_OK) h->fan_in = 0;  // regrowth lands in any row: row counts change
-  if (st == SNACK_OK) {
-    bool deferred = false;
-    if (build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, ws, s, kPlanRowsReady,
-                   h->aux, h->ev_fork, h->ev_colview, &deferred) != cudaSuccess)
-      st = SNACK_ERR_CUDA;
+  if (updated) {  // the new column view is being written into the second view: it becomes the current one
+    std::swap(h->p.cp, h->p.cp_alt);
+    std::swap(h->p.tiles_t, h->p.tiles_t_alt);
+    std::swap(h->p.row_t, h->p.row_t_alt);
+    std::swap(h->p.src_t, h->p.src_t_alt);
+    std::swap(h->p.rowt16, h->p.rowt16_alt);
   }
-  // Whatever is still queued on the second stream (the column-view rebuild,
+  // Whatever is still queued on the second stream (the column-view update,
   // or work an error left behind) is what the column-view readers wait for.
   if (cudaEventRecord(h->ev_colview, h->aux) != cudaSuccess) {
     cudaStreamSynchronize(h->aux);

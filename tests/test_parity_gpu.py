@@ -244,7 +244,8 @@ def restructure_and_check(lay: wl.Layer, n_prune: int, seed: int, step: int, act
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", [(8, 8, 20, 5), (1, 50, 10, 10), (40, 30, 600, 0), (40, 30, 600, 600),
                                   (64, 64, 3000, 1000), (500, 700, 30000, 3000), (3, 3, 4, 4),
-                                  (300, 700, 20000, 0), (300, 700, 20000, 1), (50, 1, 20, 5), (7, 3, 10, 5)])
+                                  (300, 700, 20000, 0), (300, 700, 20000, 1), (50, 1, 20, 5), (7, 3, 10, 5),
+                                  (70000, 70000, 30000, 3000)])
 def test_restructure_small(dtype, case):
     out_f, in_f, nnz, n_prune = case
     lay = wl.make_layer(out_f, in_f, nnz=nnz, val_std=1.0, val_dtype=dtype, seed=nnz)
@@ -255,11 +256,14 @@ def test_restructure_small(dtype, case):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", [(500, 700, 30000, 3000, None), (64, 64, 3000, 1000, None), (7, 3, 10, 5, None),
                                   (2000, 3000, 200000, 20000, 1.2), (70000, 20, 3000, 300, None),
-                                  (40, 30, 600, 0, None)])
+                                  (40, 30, 600, 0, None), (70000, 70000, 30000, 3000, None),
+                                  (300, 400, 40000, 20000, None)])
 def test_restructure_chain_plan_equals_fresh(dtype, case):
-    # The restructure rebuilds the handle's plan in place (row offsets and the
-    # 16-bit columns from its merge, the column view's first-level offsets made
-    # beside the merge).  After three restructures in a row the COO still
+    # The restructure rebuilds the handle's plan in place: row offsets and the
+    # 16-bit columns from its merge, and the column view updated into the
+    # plan's second view (row and column bits within 32, at most a quarter of
+    # the weights pruned) or rebuilt (70000^2; half pruned).  After three
+    # restructures in a row the COO still
     # matches the oracle, and every op on the handle is bit-identical to the
     # same op on a new handle made for the final pattern, at a small-batch and
     # at a tile-path batch: same column view, storage indices and tiles.
@@ -351,6 +355,66 @@ def test_restructure_crowded_empties_general_sort():
                    wl.random_normal(out_f, 5, 1), "f32")
     for step in range(3):
         restructure_and_check(lay, 200, seed=11, step=step)
+
+
+def test_restructure_bucket_overflow_general_sort():
+    # 1500 regrown positions, all in the last row of a 64 x 4096 layer: they
+    # crowd two of the 23 equal-width buckets (256 slots each), the buckets
+    # run over, and the lists come from the general sort (queued after the
+    # host reads the verdict); the merge passes queued before it write nothing.
+    out_f, in_f = 64, 4096
+    rng = np.random.default_rng(6)
+    tail = 63 * in_f + np.sort(rng.choice(in_f, 1000, replace=False))
+    p = np.concatenate([np.arange(63 * in_f, dtype=np.int64), tail])
+    val = wl.random_normal(p.size, seed=6, stream=0, std=0.3)
+    lay = wl.Layer(out_f, in_f, (p // in_f).astype(np.int32), (p % in_f).astype(np.int32), val,
+                   wl.random_normal(out_f, 6, 1), "f32")
+    restructure_and_check(lay, 1500, seed=3, step=1, acts=wl.make_acts(8, in_f, out_f, "f32"))
+
+
+def first_chunk_draws(n_pos: int, nnz: int, n_prune: int) -> int:
+    # the library's first draw chunk: 1.1 x the expected draws + 1024
+    empty = n_pos - nnz
+    return int(np.ceil(1.1 * n_pos * np.log((empty + 0.5) / (empty - n_prune + 0.5)) + 1024.0))
+
+
+def test_restructure_extra_draw_chunks():
+    # Regrowing every empty position of a 100 x 100 layer: for some seeds the
+    # first chunk of draws misses a position (the oracle needs more draws than
+    # the chunk holds), the merge passes queued behind the lists' flag write
+    # nothing, and the host draws more chunks and sorts the general way.  Both
+    # outcomes are bit-exact.
+    lay = wl.make_layer(100, 100, nnz=9000, val_dtype="f32", seed=13)
+    m1 = first_chunk_draws(10000, 9000, 1000)
+    short, full = [], []
+    for seed in range(40):
+        draws = oracle.restructure(100, 100, lay.row, lay.col, oracle.as_f64(lay.val), 1000, seed, 0)[3]
+        (short if draws > m1 else full).append(seed)
+    assert short and full, (short, full)
+    for seed in short[:3] + full[:1]:
+        restructure_and_check(lay, 1000, seed=seed, step=0, acts=wl.make_acts(8, 100, 100, "f32"))
+
+
+def test_restructure_large_prune_general_sort_column_view():
+    # 1.1M regrown positions: more buckets than the bucket sort takes, so the
+    # first chunk's lists come from the general sort (speculatively, before the
+    # host's verdict); the column view is updated from them.  The COO is
+    # bit-exact and the input gradient through the updated view equals a fresh
+    # handle's bit for bit.
+    out_f = in_f = 20000
+    lay = wl.make_layer(out_f, in_f, nnz=4_500_000, val_std=0.1, val_dtype="f32", seed=14)
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=8)
+    src = L.restructure(1_100_000, 5, 9)
+    torch.cuda.synchronize()
+    ro, co, so, _ = oracle.restructure(out_f, in_f, lay.row, lay.col, oracle.as_f64(lay.val), 1_100_000, 5, 9)
+    assert np.array_equal(L.row.cpu().numpy(), ro) and np.array_equal(L.col.cpu().numpy(), co)
+    assert np.array_equal(src.cpu().numpy(), so.astype(np.int32))
+    F = snack.SparseLinear(out_f, in_f, L.row.clone(), L.col.clone(), L.val.clone(), bias, max_batch=8)
+    dy = act_tensor(wl.make_acts(8, in_f, out_f, "f32").dy, "f32")
+    assert torch.equal(L.grad_input(dy), F.grad_input(dy))
+    F.close()
+    L.close()
 
 
 def test_restructure_chain_of_steps():
