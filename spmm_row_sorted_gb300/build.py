@@ -90,18 +90,21 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         return obj
 
     srcs = sources()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(compile_one, srcs))
+    planned = [os.path.join(build_dir, os.path.basename(src)[:-3] + f".{os.getpid()}.o") for src in srcs]
     tmp = lib_path + f".tmp{os.getpid()}"
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
-    cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-           "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    for o in objs:
-        try:
-            os.remove(o)
-        except OSError:
-            pass
+    try:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+            objs = list(ex.map(compile_one, srcs))
+        cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nv)), "lib64")
+        cmd = [nv, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+               "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+    finally:  # no object file outlives the build, failed or not
+        for o in planned:
+            try:
+                os.remove(o)
+            except OSError:
+                pass
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, lib_path)

@@ -41,6 +41,11 @@ struct PlanPtrs {
   void *tables;
 };
 
+// Words of PlanPtrs::flags: [0] pattern validation, [1] constant fan-in check,
+// [kPlanFlagLookBack] set when a column-view update gave up waiting for a
+// predecessor tile's counts.
+constexpr int kPlanFlagLookBack = 2;
+
 struct PlanLayout {
   size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cpa, off_tta,
       off_rowta, off_srcta, off_rowt16a, off_newidx, off_gq, off_gck, off_gcq, off_cvs, off_cvb, off_tab, total;
@@ -109,7 +114,8 @@ struct RestructureArgs {
   const PlanPtrs *plan;
   TileGeom gf, gt;
   bool update;
-  uint32_t *host_counts;  // pinned, mapped host memory, 4 words: a draw chunk's accepted count, table and bucket overflow
+  uint32_t *host_counts;  // pinned, mapped host memory, 8 words: a draw chunk's accepted count, table and bucket
+                          // overflows, and the plan's look-back error
   uint32_t *counts_dev;   // the same words' device address (written by a kernel, no copy)
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
   cudaStream_t aux;          // second stream of the handle (regrow branch, column-view update)

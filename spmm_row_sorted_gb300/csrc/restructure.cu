@@ -47,6 +47,7 @@ struct SelState {
   uint32_t overflow;                           // a draw found the position table full
   uint32_t pfx, mask, rem;                     // select progress: digits fixed so far, ranks left within them
   uint32_t arrive[4];                          // blocks finished per pass
+  uint32_t n_cand;                             // keys in the first digit's bucket (the candidates)
   uint32_t hist0[2048], hist1[1024], hist2[1024];  // digit histograms: key bits 30..20, 19..10, 9..0
 };
 
@@ -172,6 +173,162 @@ __global__ void k_sel_init(SelState *st, uint32_t n_prune) {
     st->pfx = 0;
     st->mask = 0;
     st->rem = n_prune;
+    st->n_cand = 0;
+  }
+}
+
+// Second pass of the two-pass select, one block per scan tile (2048 stored
+// weights): the tile's keys above the first digit's bucket are counted (its
+// keep count so far, sums[t]), and the keys in the bucket are listed as
+// candidates, key << 32 | storage index (one list append per block).
+template <typename TV>
+__global__ void __launch_bounds__(kScanThreads) k_sel_bucket(const TV *__restrict__ val, int64_t nnz, SelState *st,
+                                                             uint64_t *__restrict__ sums, uint64_t *__restrict__ cand) {
+  pdl_wait();
+  __shared__ uint32_t s_above[kScanThreads / 32], s_cnt[kScanThreads / 32];
+  __shared__ uint32_t s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t base = (int64_t)blockIdx.x * kScanTile;
+  const uint32_t d0 = st->pfx >> 20;
+  uint32_t key[kScanItems];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t k = base + i * kScanThreads + tid;
+    key[i] = k < nnz ? mag_key<TV>(val, k) : 0u;
+  }
+  uint32_t n_above = 0, n_mine = 0;
+  unsigned bal[kScanItems];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t k = base + i * kScanThreads + tid;
+    const bool in = k < nnz;
+    n_above += in && (key[i] >> 20) > d0 ? 1u : 0u;
+    bal[i] = __ballot_sync(0xffffffffu, in && (key[i] >> 20) == d0);
+    n_mine += (uint32_t)__popc(bal[i]);  // the warp's candidates (same in every lane)
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n_above += __shfl_down_sync(0xffffffffu, n_above, o);
+  if (lane == 0) {
+    s_above[warp] = n_above;
+    s_cnt[warp] = n_mine;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t ta = 0, tc = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+      ta += s_above[w];
+      const uint32_t c = s_cnt[w];
+      s_cnt[w] = tc;  // the warp's first slot within the block's run
+      tc += c;
+    }
+    sums[blockIdx.x] = ta;
+    s_base = tc ? atomicAdd(&st->n_cand, tc) : 0u;
+  }
+  __syncthreads();
+  uint32_t at = s_base + s_cnt[warp];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    if ((bal[i] >> lane) & 1u)
+      cand[at + __popc(bal[i] & ((1u << lane) - 1u))] = ((uint64_t)key[i] << 32) | (uint32_t)(base + i * kScanThreads + tid);
+    at += (uint32_t)__popc(bal[i]);
+  }
+}
+
+// A digit pass of the select over the candidate list (bits 19..10, then
+// 9..0, of the keys matching the digits fixed so far): per-block histograms
+// (equal bins of a warp added once), added to the global one; the last block
+// to finish picks the digit that holds rank rem (as the first pass does).
+constexpr int kSelCandBlocks = 304;
+template <int kPass>
+__global__ void __launch_bounds__(256) k_sel_cand(const uint64_t *__restrict__ cand, SelState *st) {
+  pdl_wait();
+  constexpr int kShift = kPass == 1 ? 10 : 0, kBins = 1024, kPer = kBins / 256;
+  __shared__ uint32_t h[kBins];
+  __shared__ uint32_t s_scan[256];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t nc = st->n_cand, pfx = st->pfx, mask = st->mask;
+  for (int i = tid; i < kBins; i += 256) h[i] = 0u;
+  __syncthreads();
+  const uint32_t stride = gridDim.x * 256u;
+  for (uint32_t i0 = blockIdx.x * 256u; i0 < nc; i0 += stride) {  // whole warps per round (ballots below)
+    const uint32_t i = i0 + tid;
+    const uint32_t key = i < nc ? (uint32_t)(cand[i] >> 32) : 0u;
+    const bool on = i < nc && (key & mask) == pfx;
+    const uint32_t bin = on ? (key >> kShift) & (kBins - 1) : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (on && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  }
+  __syncthreads();
+  uint32_t *gh = kPass == 1 ? st->hist1 : st->hist2;
+  for (int i = tid; i < kBins; i += 256)
+    if (h[i]) atomicAdd(&gh[i], h[i]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&st->arrive[kPass], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const uint32_t rem = st->rem;
+  uint32_t c[kPer], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    c[j] = __ldcg(&gh[tid * kPer + j]);
+    sum += c[j];
+  }
+  s_scan[tid] = sum;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const uint32_t v = tid >= off ? s_scan[tid - off] : 0u;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  uint32_t ex = s_scan[tid] - sum;
+  if (ex < rem && ex + sum >= rem) {
+#pragma unroll 1
+    for (int j = 0; j < kPer; ++j) {
+      if (ex + c[j] >= rem) {
+        const uint32_t d = (uint32_t)(tid * kPer + j);
+        st->pfx = pfx | (d << kShift);
+        st->mask = mask | ((uint32_t)(kBins - 1) << kShift);
+        st->rem = rem - ex;
+        if (kPass == 2) {
+          st->prefix = pfx | (d << kShift);
+          st->remaining = rem - ex;
+        }
+        break;
+      }
+      ex += c[j];
+    }
+  }
+}
+
+// The tiles' keep counts: each candidate above the threshold t adds one kept
+// weight to its tile, each equal to t one tie.  Candidates were listed a
+// tile at a time, so a warp's lanes of one tile add their counts at once.
+__global__ void __launch_bounds__(256) k_sel_tiles(const uint64_t *__restrict__ cand, const SelState *st,
+                                                   uint64_t *__restrict__ sums) {
+  pdl_wait();
+  const uint32_t nc = st->n_cand, t = st->prefix;
+  const int lane = threadIdx.x & 31;
+  const uint32_t stride = gridDim.x * 256u;
+  for (uint32_t i0 = blockIdx.x * 256u; i0 < nc; i0 += stride) {  // whole warps per round (ballots below)
+    const uint32_t i = i0 + threadIdx.x;
+    uint32_t key = 0, tile = 0xFFFFFFFFu;
+    if (i < nc) {
+      const uint64_t cw = cand[i];
+      key = (uint32_t)(cw >> 32);
+      tile = (uint32_t)cw / kScanTile;
+    }
+    const bool gt = i < nc && key > t, eq = i < nc && key == t;
+    const unsigned gtm = __ballot_sync(0xffffffffu, gt), eqm = __ballot_sync(0xffffffffu, eq);
+    const unsigned peers = __match_any_sync(0xffffffffu, (gt || eq) ? tile : 0xFFFFFFFFu);
+    if ((gt || eq) && (peers & ((1u << lane) - 1u)) == 0u) {
+      const uint64_t add = (uint64_t)__popc(peers & gtm) | ((uint64_t)__popc(peers & eqm) << 32);
+      atomicAdd(reinterpret_cast<unsigned long long *>(&sums[tile]), add);
+    }
   }
 }
 
@@ -188,30 +345,71 @@ struct KeepVal {
 };
 
 
-__device__ __forceinline__ uint32_t hash_min(const uint64_t *keys, const uint32_t *mins, uint64_t mask, uint64_t p) {
-  uint64_t h = sm64_finalise(p) & mask;
-  for (uint64_t probe = 0; probe <= mask; ++probe) {
-    uint64_t k = keys[h];
-    if (k == p) return mins[h];
-    if (k == kEmpty) return 0xFFFFFFFFu;
-    h = (h + 1) & mask;
+// Position table: the first (smallest) draw index of every drawn empty
+// position, open addressing with linear probing.  Packed (positions below
+// 2^32): one 64-bit word per slot, position << 32 | draw index, so a first
+// insertion is one compare-and-swap and a repeat one atomicMin on the same
+// word; otherwise 64-bit positions and 32-bit minima in two arrays.
+struct PosTable {
+  uint64_t *keys;
+  uint32_t *mins;  // unused when packed
+  uint64_t mask;
+  bool packed;
+  __device__ bool insert(uint64_t key, uint32_t i) const {
+    uint64_t h = sm64_finalise(key) & mask;
+    if (packed) {
+      const unsigned long long w = (key << 32) | i;  // never kEmpty: i < 2^32 - 1
+      for (uint64_t probe = 0; probe <= mask; ++probe) {
+        const unsigned long long prev =
+            atomicCAS(reinterpret_cast<unsigned long long *>(keys + h), (unsigned long long)kEmpty, w);
+        if (prev == kEmpty) return true;
+        if ((prev >> 32) == key) {
+          atomicMin(reinterpret_cast<unsigned long long *>(keys + h), w);
+          return true;
+        }
+        h = (h + 1) & mask;
+      }
+      return false;
+    }
+    for (uint64_t probe = 0; probe <= mask; ++probe) {
+      const unsigned long long prev = atomicCAS(reinterpret_cast<unsigned long long *>(keys + h),
+                                                (unsigned long long)kEmpty, (unsigned long long)key);
+      if (prev == kEmpty || prev == key) {
+        atomicMin(mins + h, i);
+        return true;
+      }
+      h = (h + 1) & mask;
+    }
+    return false;
   }
-  return 0xFFFFFFFFu;
-}
-
+  __device__ uint32_t min_of(uint64_t key) const {
+    uint64_t h = sm64_finalise(key) & mask;
+    for (uint64_t probe = 0; probe <= mask; ++probe) {
+      const uint64_t k = keys[h];
+      if (k == kEmpty) return 0xFFFFFFFFu;
+      if (packed) {
+        if ((k >> 32) == key) return (uint32_t)k;
+      } else if (k == key) {
+        return mins[h];
+      }
+      h = (h + 1) & mask;
+    }
+    return 0xFFFFFFFFu;
+  }
+};
 
 __device__ __forceinline__ uint32_t mag_of(float v) { return canon_mag(__float_as_uint(v) & 0x7FFFFFFFu); }
 __device__ __forceinline__ uint32_t mag_of(bf16 v) {
   return canon_mag(((uint32_t)__bfloat16_as_ushort(v) & 0x7FFFu) << 16);
 }
 
-// A draw: position by multiply-high of SplitMix64 output i, empty test by a
-// binary search of its column in the old row (CI: the plan's 16-bit column
-// copy, or the 32-bit columns), insertion into the position table.
+// A draw: position by multiply-high of SplitMix64 output i; empty test by a
+// binary search of its column in the old row, over the plan's 16-bit column
+// copy or the 32-bit columns (CI); insertion into the position table.
 template <typename CI>
 __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, int32_t in_f, int cbits,
                        const int32_t *__restrict__ rp, const CI *__restrict__ col, uint64_t *__restrict__ cand,
-                       uint64_t *hkeys, uint32_t *hmin, uint64_t hmask, uint32_t *overflow) {
+                       PosTable tab, uint32_t *overflow) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
@@ -223,7 +421,7 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
     int32_t lo = rp[r], hi = rp[r + 1];
     const int32_t end = hi;
     while (lo < hi) {
-      int32_t mid = lo + (hi - lo) / 2;
+      const int32_t mid = lo + (hi - lo) / 2;
       if ((int32_t)col[mid] < c)
         lo = mid + 1;
       else
@@ -236,34 +434,20 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
     }
     const uint64_t key = (r << cbits) | (uint32_t)c;  // position key of the draw
     cand[idx] = key;
-    uint64_t h = sm64_finalise(key) & hmask;
-    bool done = false;
-    for (uint64_t probe = 0; probe <= hmask; ++probe) {
-      unsigned long long prev =
-          atomicCAS(reinterpret_cast<unsigned long long *>(hkeys + h), (unsigned long long)kEmpty,
-                    (unsigned long long)key);
-      if (prev == kEmpty || prev == key) {
-        atomicMin(hmin + h, (uint32_t)i);
-        done = true;
-        break;
-      }
-      h = (h + 1) & hmask;
-    }
-    if (!done) atomicOr(overflow, 1u);
+    if (!tab.insert(key, (uint32_t)i)) atomicOr(overflow, 1u);
   }
 }
 
 // flag[idx] = 1 when draw i0 + idx found an empty position and is that
 // position's first draw (the minimum index recorded for it); one thread per
 // draw, so the table lookups of all draws are in flight at once
-__global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0,
-                               const uint64_t *__restrict__ hkeys, const uint32_t *__restrict__ hmin, uint64_t hmask,
+__global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0, PosTable tab,
                                uint32_t *__restrict__ flags) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
     const uint64_t p = cand[idx];
-    flags[idx] = (p != kEmpty && hash_min(hkeys, hmin, hmask, p) == (uint32_t)(i0 + (uint64_t)idx)) ? 1u : 0u;
+    flags[idx] = (p != kEmpty && tab.min_of(p) == (uint32_t)(i0 + (uint64_t)idx)) ? 1u : 0u;
   }
 }
 
@@ -338,8 +522,10 @@ struct DrawState {
 };
 
 // The lists' verdict and, with host_words, the chunk's counters to the host's
-// mapped words.
-__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made) {
+// mapped words, with the plan's look-back error word (set by an earlier
+// column-view update that gave up waiting; read and cleared here).
+__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made,
+                                        uint32_t *lb_err) {
   const uint32_t tot = ds->total, ovf = ds->overflow, bovf = ds->bucket_overflow, covf = ds->col_overflow;
   if (host_words) {
     volatile uint32_t *hw = host_words;
@@ -347,15 +533,17 @@ __device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t
     hw[1] = ovf;
     hw[2] = bovf;
     hw[3] = covf;
+    hw[4] = lb_err ? *lb_err : 0u;
+    if (lb_err) *lb_err = 0u;
   }
   const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf;
   ds->lists_ok = ok ? 1u : 0u;
   ds->col_ok = ok && !covf ? 1u : 0u;
 }
 
-__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made) {
+__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made, uint32_t *lb_err) {
   pdl_wait();
-  publish(ds, n_prune, host_words, made != 0);
+  publish(ds, n_prune, host_words, made != 0, lb_err);
 }
 
 __global__ void k_set_word(uint32_t *w, uint32_t v) {
@@ -365,8 +553,7 @@ __global__ void k_set_word(uint32_t *w, uint32_t v) {
 
 // Start of a restructure's regrow branch: counters and bucket counts to zero,
 // the position table to empty (one launch instead of several fills).
-__global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t *__restrict__ hmin, int64_t cap,
-                          uint32_t *__restrict__ bcnt, int64_t nb) {
+__global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bcnt, int64_t nb) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -378,9 +565,10 @@ __global__ void k_rs_init(DrawState *ds, uint64_t *__restrict__ hkeys, uint32_t 
     ds->lists_ok = 0u;
     ds->col_ok = 0u;
   }
+  const int64_t cap = (int64_t)tab.mask + 1;
   for (int64_t i = i0; i < cap; i += stride) {
-    hkeys[i] = kEmpty;
-    hmin[i] = 0xFFFFFFFFu;
+    tab.keys[i] = kEmpty;
+    if (!tab.packed) tab.mins[i] = 0xFFFFFFFFu;
   }
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
 }
@@ -411,12 +599,12 @@ struct RankDst {
 // bucket's keys (all distinct).  Block 0 first sets the lists' verdict (and,
 // with host_words, publishes the chunk's counters).
 __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet S, RankDst D, int64_t n_prune, DrawState *ds,
-                                                  uint32_t *host_words, bool k32) {
+                                                  uint32_t *host_words, bool k32, uint32_t *lb_err) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true);
+  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true, lb_err);
   const uint32_t b0 = blockIdx.x * 8;
   uint32_t part = 0;
   for (uint32_t i0 = threadIdx.x; i0 < b0; i0 += 256 * 8) {  // eight loads in flight per round
@@ -532,12 +720,26 @@ struct MkArgs {
   int64_t n, n_list;
   int64_t n_out;          // output slots (every index written is checked against it)
   const MkBound *bnd;     // [n_tiles + 1]
-  const uint64_t *sums;   // per-tile packed keep counts (kDirect), or their exclusive prefixes
+  const uint64_t *sums;   // per-tile packed keep counts (kMkDirect), or their exclusive prefixes (kMkGiven)
   const uint32_t *guard;  // when set and zero, every block returns at once
   int minor_bits;
   int64_t n_major;
   int32_t *off;  // [n_major + 1]
+  // kMkLookBack: tiles are taken in ticket order and each block finds the
+  // counts before its tile from its predecessors' published totals
+  uint64_t *status;  // [n_tiles], zero before the launch
+  uint32_t *ticket;  // zero before the launch
+  uint32_t *err;     // set when a wait for a predecessor gave up (never expected)
 };
+
+// How a merge block learns the keep counts before its tile.
+constexpr int kMkGiven = 0, kMkDirect = 1, kMkLookBack = 2;
+// Look-back words: flag in bits 62..63 (1: the tile's own total, 2: the total
+// of all tiles up to and including it), kept and tie counts in 31 bits each.
+constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
+constexpr uint32_t kLbMaxSpins = 1u << 20;  // about 0.1 s of polling before a wait gives up
+__device__ __forceinline__ uint64_t lb_pack(uint64_t x) { return (x & 0x7FFFFFFFull) | ((x >> 32) << 31); }
+__device__ __forceinline__ uint64_t lb_unpack(uint64_t v) { return (v & 0x7FFFFFFFull) | (((v >> 31) & 0x7FFFFFFFull) << 32); }
 
 // number of entries of an ascending sequence at(0..n) below v, by one warp:
 // each round probes 32 evenly spaced entries and keeps the bracket of the
@@ -576,18 +778,22 @@ __device__ __forceinline__ int lb_seq(F at, int n, V v) {
 template <class Pol>
 constexpr size_t mk_smem_bytes() {
   using K = typename Pol::Key;
-  return sizeof(K) * (kpad_words<K>(kMkTile + 1) + kMkListCap) +
-         sizeof(uint32_t) * (kMkXWords + (kMkXWords & 1) + kMkXWords + (kMkXWords & 1)) + sizeof(uint16_t) * kMkListCap +
-         sizeof(typename Pol::Shared);
+  return sizeof(K) * (kpad_words<K>(kMkTile + 1) + kMkListCap) + sizeof(uint64_t) * kpad_words<uint64_t>(kMkTile + 1) +
+         sizeof(uint16_t) * kMkListCap + sizeof(typename Pol::Shared);
 }
 
 // Tile bounds, one warp per tile t in [0, n_tiles], all at once (so the merge
-// blocks start with their bounds instead of searching the list themselves).
+// blocks start with their bounds instead of searching the list themselves);
+// for a look-back merge also its per-tile words and ticket, cleared.
 template <class Pol>
-__global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd) {
+__global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd, uint64_t *status, uint32_t *ticket) {
   pdl_wait();
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t > n_tiles) return;
+  if (status && (threadIdx.x & 31) == 0) {  // a look-back merge's per-tile words and ticket, cleared
+    if (t < n_tiles) status[t] = 0ull;
+    if (t == 0) *ticket = 0u;
+  }
   MkBound r{~0ull, n_list, 0u, 0u};
   if (t < n_tiles) {
     r.key = pol.key_at_warp(t * (int64_t)kMkTile, &r.aux);
@@ -596,26 +802,38 @@ __global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd)
   if ((threadIdx.x & 31) == 0) bnd[t] = r;
 }
 
-template <class Pol, bool kDirect>
+// Each element's 64-bit count: bits 0..15 kept (unless a tie), 16..31 tie,
+// 32..47 list keys placed right after it.  After the exclusive scan, the
+// fields at element e count the kept elements, ties and list keys of the tile
+// below e's key (list keys below the tile's first element are counted apart).
+template <class Pol, int kMode>
 __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a) {
+  constexpr bool kDirect = kMode == kMkDirect;
   using K = typename Pol::Key;
   extern __shared__ __align__(16) uint8_t mk_smem[];
-  // tile keys (padded index; [len] = the next tile's first key, or the maximum)
-  K *sKp = reinterpret_cast<K *>(mk_smem);
-  K *sL = sKp + kpad_words<K>(kMkTile + 1);                      // the tile's list keys
-  uint32_t *sX = reinterpret_cast<uint32_t *>(sL + kMkListCap);  // local exclusive counts (padded)
-  uint32_t *sPos = sX + kMkXWords + (kMkXWords & 1);             // output index of each element, padded (~0u: dropped)
-  uint16_t *sP = reinterpret_cast<uint16_t *>(sPos + kMkXWords + (kMkXWords & 1));  // elements below each list key
+  uint64_t *sX = reinterpret_cast<uint64_t *>(mk_smem);                    // counts (padded), then exclusive sums
+  K *sKp = reinterpret_cast<K *>(sX + kpad_words<uint64_t>(kMkTile + 1));  // tile keys (padded)
+  K *sL = sKp + kpad_words<K>(kMkTile + 1);                                // the tile's list keys
+  uint16_t *sPj = reinterpret_cast<uint16_t *>(sL + kMkListCap);          // elements below each list key
+  typename Pol::Shared &ps = *reinterpret_cast<typename Pol::Shared *>(sPj + kMkListCap);
   const PadKeys<K> sK{sKp};
-  typename Pol::Shared &ps = *reinterpret_cast<typename Pol::Shared *>(sP + kMkListCap);
   __shared__ uint64_t s_pre;
   __shared__ uint64_t s_red[kMkThreads / 32];
-  __shared__ uint32_t s_tot;
+  __shared__ uint64_t s_tot;
+  __shared__ uint32_t s_c00;
+  __shared__ int64_t s_tile;
   pdl_wait();
   // every load of the tile's inputs is issued before the first wait on one
   const uint32_t go = a.guard ? *reinterpret_cast<const volatile uint32_t *>(a.guard) : 1u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t b = blockIdx.x, base = b * (int64_t)kMkTile;
+  int64_t b = blockIdx.x;
+  if (kMode == kMkLookBack) {  // tiles in ticket order: every tile before this one has a block running
+    if (go == 0u) return;
+    if (tid == 0) s_tile = atomicAdd(a.ticket, 1u);
+    __syncthreads();
+    b = s_tile;
+  }
+  const int64_t base = b * (int64_t)kMkTile;
   const int len = (int)(a.n - base < kMkTile ? a.n - base : kMkTile);
   const bool last = b == (int64_t)gridDim.x - 1;
   const MkBound bd0 = a.bnd[b], bd1 = a.bnd[b + 1];
@@ -623,6 +841,10 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
   typename Pol::Item it[kMkItems];
   uint32_t fl[kMkItems];
   pol.load(base, len, last, bd0.aux, bd1.aux, it, fl, sK, ps);
+  const int64_t lo = bd0.lo, cnt = bd1.lo - bd0.lo;
+  const bool lsm = cnt <= kMkListCap;
+  if (lsm)
+    for (int j = tid; j < (int)cnt; j += kMkThreads) sL[j] = (K)pol.list_key(lo + j);
   uint64_t part = 0;
   if (kDirect) {
     for (int64_t q0 = tid; q0 < b; q0 += kMkThreads * 8) {  // eight loads in flight per round
@@ -637,11 +859,18 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
     if (lane == 0) s_red[warp] = part;
   }
 #pragma unroll
-  for (int i = 0; i < kMkItems; ++i) sX[mk_pad(i * kMkThreads + tid)] = fl[i];
+  for (int i = 0; i < kMkItems; ++i) {
+    const int e = i * kMkThreads + tid;
+    sX[kpad<uint64_t>(e)] = fl[i];
+  }
   if (go == 0u) return;  // a speculative launch whose lists were not made: write nothing
-  if (tid == 0) sK[len] = (K)bd1.key;
-  __syncthreads();
   if (tid == 0) {
+    sK[len] = (K)bd1.key;
+    sX[kpad<uint64_t>(kMkTile)] = 0ull;
+    s_c00 = 0u;
+  }
+  __syncthreads();
+  if (tid == 0 && kMode != kMkLookBack) {
     uint64_t p = 0;
     if (kDirect) {
 #pragma unroll
@@ -651,108 +880,112 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
     }
     s_pre = p;
   }
-  pol.keys_blocked(base, len, last, bd0.aux, bd1.aux, sK, ps);
-  {  // exclusive scan of the packed counts in element order
-    uint32_t v[kMkItems], tsum = 0;
+  if (pol.keys_blocked(base, len, last, bd0.aux, bd1.aux, sK, ps)) __syncthreads();
+  auto lkey = [&](int j) -> K { return lsm ? sL[j] : (K)pol.list_key(lo + j); };
+  auto lb_keys = [&](K v) -> int { return lb_seq([&](int i) { return sK[i]; }, len, v); };
+  // each list key after the last element below it
+  for (int j = tid; j < (int)cnt; j += kMkThreads) {
+    const int p = lb_keys(lkey(j));
+    if (lsm) sPj[j] = (uint16_t)p;
+    if (p > 0)
+      atomicAdd(reinterpret_cast<unsigned long long *>(&sX[kpad<uint64_t>(p - 1)]), 1ull << 32);
+    else
+      atomicAdd(&s_c00, 1u);
+  }
+  __syncthreads();
+  {  // exclusive scan of the counts in element order (thread t: elements 8t .. 8t+7)
+    uint64_t v[kMkItems], tsum = 0;
 #pragma unroll
     for (int i = 0; i < kMkItems; ++i) {
-      v[i] = sX[mk_pad(tid * kMkItems + i)];
+      v[i] = sX[kpad<uint64_t>(tid * kMkItems + i)];
       tsum += v[i];
     }
-    uint32_t ex = block_exclusive_scan<uint32_t>(tsum, &s_tot);
+    uint64_t ex = block_exclusive_scan<uint64_t>(tsum, &s_tot);
 #pragma unroll
     for (int i = 0; i < kMkItems; ++i) {
-      sX[mk_pad(tid * kMkItems + i)] = ex;
+      sX[kpad<uint64_t>(tid * kMkItems + i)] = ex;
       ex += v[i];
     }
-    if (tid == 0) sX[mk_pad(kMkTile)] = s_tot;
+    if (tid == 0) sX[kpad<uint64_t>(kMkTile)] = s_tot;
   }
-  const int64_t lo = bd0.lo, cnt = bd1.lo - bd0.lo;
-  const bool lsm = cnt <= kMkListCap;
-  if (lsm)
-    for (int j = tid; j < (int)cnt; j += kMkThreads) sL[j] = (K)pol.list_key(lo + j);
+  if (kMode == kMkLookBack && warp == 0) {
+    // publish this tile's kept and tie counts, then add up the predecessors'
+    // going back from the nearest, 32 tiles at a time, until a tile whose
+    // total includes everything before it
+    const uint64_t agg = lb_pack((s_tot & 0xFFFFull) | (((s_tot >> 16) & 0xFFFFull) << 32));
+    if (lane == 0) *reinterpret_cast<volatile uint64_t *>(&a.status[b]) = (b == 0 ? kLbInclusive : kLbAggregate) | agg;
+    uint64_t excl = 0;
+    int64_t i = b - 1;
+    uint32_t spins = 0;
+    while (i >= 0) {
+      const int64_t idx = i - lane;
+      const uint64_t v = idx >= 0 ? *reinterpret_cast<const volatile uint64_t *>(&a.status[idx]) : kLbInclusive;
+      const unsigned incl = __ballot_sync(0xffffffffu, (v >> 62) == 2u);
+      const int first = incl ? __ffs(incl) - 1 : 31;
+      const unsigned upto = first == 31 ? 0xffffffffu : ((2u << first) - 1u);  // lanes 0 .. first
+      const unsigned missing = __ballot_sync(0xffffffffu, (v >> 62) == 0u) & upto;
+      if (missing) {
+        if (++spins > kLbMaxSpins) {  // give up (the counts are then wrong; the error word says so)
+          if (lane == 0) atomicOr(a.err, 1u);
+          break;
+        }
+        __nanosleep(64);
+        continue;
+      }
+      uint64_t val = (unsigned)lane <= (unsigned)first ? (v & kLbValue) : 0ull;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) val += __shfl_down_sync(0xffffffffu, val, o);
+      excl += __shfl_sync(0xffffffffu, val, 0);
+      if (incl) break;
+      i -= 32;
+    }
+    if (lane == 0) {
+      if (b > 0) *reinterpret_cast<volatile uint64_t *>(&a.status[b]) = kLbInclusive | ((excl + agg) & kLbValue);
+      s_pre = lb_unpack(excl);
+    }
+  }
   __syncthreads();
-  const uint32_t preG = (uint32_t)s_pre, preE = (uint32_t)(s_pre >> 32), lo32 = (uint32_t)lo;
-  auto surv = [&](uint32_t x) -> uint32_t {  // kept elements before a local index, from its exclusive count
-    const uint32_t g = preG + (x & 0xFFFFu), e = preE + (x >> 16);
+  const uint32_t preG = (uint32_t)s_pre, preE = (uint32_t)(s_pre >> 32), lo32 = (uint32_t)lo, c00 = s_c00;
+  auto surv = [&](uint64_t x) -> uint32_t {  // kept elements below, from an exclusive count
+    const uint32_t g = preG + (uint32_t)(x & 0xFFFFu), e = preE + (uint32_t)((x >> 16) & 0xFFFFu);
     return g + (e > m ? e - m : 0u);
   };
+  auto below = [&](uint64_t x) -> uint32_t { return c00 + (uint32_t)((x >> 32) & 0xFFFFu); };  // list keys below
   const int mb = a.minor_bits;
   const uint32_t nmaj = (uint32_t)a.n_major;
-  // the blocked walk; with the slice in shared memory it also records, per
-  // list key, the elements below it
-  auto walk = [&](auto lkey, int n_l, bool record) {
-    if (b == 0) {  // list keys below the tile's first element: no element below them
-      const int j00 = lb_seq(lkey, n_l, sK[0]);
-      if (record)
-        for (int j = tid; j < j00; j += kMkThreads) sP[j] = 0;
-      if (tid == 0) {  // majors up to the first element's (no kept element before them)
-        const int64_t maj0 = min((int64_t)(sK[0] >> mb), a.n_major);
-        int jj = 0;
-        for (int64_t M = 0; M <= maj0; ++M) {
-          const K mk = (K)((uint64_t)M << mb);
-          while (jj < n_l && lkey(jj) < mk) ++jj;
-          a.off[M] = (int32_t)jj;
-        }
-      }
-    }
-    const int e0 = tid * kMkItems;
-    if (e0 >= len) return;
-    const int e1 = min(e0 + kMkItems, len);
-    int j = lb_seq(lkey, n_l, sK[e0]);
-    uint32_t x = sX[mk_pad(e0)];
-    for (int e = e0; e < e1; ++e) {
-      const K key = sK[e];
-      while (j < n_l && lkey(j) < key) {
-        if (record) sP[j] = (uint16_t)e;
-        ++j;
-      }
-      const uint32_t xn = sX[mk_pad(e + 1)];
-      const uint32_t d = xn - x;  // this element's own counts
-      const bool keep = (d & 0xFFFFu) || ((d >> 16) && preE + (x >> 16) >= m);
-      sPos[mk_pad(e)] = keep ? surv(x) + lo32 + (uint32_t)j : ~0u;
-      const uint32_t maj = (uint32_t)(key >> mb);
-      const uint32_t nxt = min(e + 1 == len && last ? nmaj : (uint32_t)(sK[e + 1] >> mb), nmaj);
-      if (nxt > maj) {  // majors that start after this element
-        const uint32_t sv = surv(xn) + lo32;
-        int jj = j;
-        for (uint32_t M = maj + 1; M <= nxt; ++M) {
-          const K mk = (K)M << mb;
-          while (jj < n_l && lkey(jj) < mk) ++jj;
-          a.off[M] = (int32_t)(sv + (uint32_t)jj);
-        }
-      }
-      x = xn;
-    }
-    const K nkey = sK[e1];  // the next element, or the next tile's first key
-    while (j < n_l && lkey(j) < nkey) {
-      if (record) sP[j] = (uint16_t)e1;
-      ++j;
-    }
-  };
-  if (lsm)
-    walk([&](int j) -> K { return sL[j]; }, (int)cnt, true);
-  else  // a list slice larger than shared memory (regrown positions crowded into one tile's range)
-    walk([&](int j) -> K { return (K)pol.list_key(lo + j); }, (int)cnt, false);
-  __syncthreads();
-  // kept and dropped elements, striped (coalesced writes)
+  // kept and dropped elements, striped (coalesced writes), and the offsets of
+  // the majors that start after each element
 #pragma unroll
   for (int i = 0; i < kMkItems; ++i) {
     const int e = i * kMkThreads + tid;
     if (e < len) {
-      const uint32_t pos = sPos[mk_pad(e)];
-      if (pos != ~0u) {
-        if ((int64_t)pos < a.n_out) pol.write_kept(it[i], base + e, pos, sK[e]);
+      const uint64_t x = sX[kpad<uint64_t>(e)];
+      const uint32_t keep = (fl[i] & 0xFFFFu) | ((fl[i] >> 16) & (preE + (uint32_t)((x >> 16) & 0xFFFFu) >= m ? 1u : 0u));
+      const K key = sK[e];
+      if (keep) {
+        const uint32_t pos = surv(x) + lo32 + below(x);
+        if ((int64_t)pos < a.n_out) pol.write_kept(it[i], base + e, pos, key);
       } else {
         pol.write_dropped(it[i], base + e);
       }
+      const uint32_t maj = (uint32_t)(key >> mb);
+      const uint32_t nxt = e + 1 == len && last ? nmaj : min((uint32_t)(sK[e + 1] >> mb), nmaj);
+      if (nxt > maj) {
+        const uint32_t sv = surv(sX[kpad<uint64_t>(e + 1)]) + lo32;
+        for (uint32_t M = maj + 1; M <= nxt; ++M)
+          a.off[M] = (int32_t)(sv + (uint32_t)lb_seq(lkey, (int)cnt, (K)M << mb));
+      }
     }
+  }
+  if (b == 0) {  // majors up to the first element's: no kept element before them
+    const uint32_t maj0 = min((uint32_t)(sK[0] >> mb), nmaj);
+    for (uint32_t M = tid; M <= maj0; M += kMkThreads) a.off[M] = (int32_t)lb_seq(lkey, (int)cnt, (K)M << mb);
   }
   // the tile's list entries
   for (int j = tid; j < (int)cnt; j += kMkThreads) {
-    const K key = lsm ? sL[j] : (K)pol.list_key(lo + j);
-    const int p = lsm ? (int)sP[j] : lb_seq([&](int i) { return sK[i]; }, len, key);
-    const uint32_t pos = lo32 + (uint32_t)j + surv(sX[mk_pad(p)]);
+    const K key = lkey(j);
+    const int p = lsm ? (int)sPj[j] : lb_keys(key);
+    const uint32_t pos = lo32 + (uint32_t)j + surv(sX[kpad<uint64_t>(p)]);
     if ((int64_t)pos < a.n_out) pol.write_list(lo + j, key, pos);
   }
 }
@@ -808,7 +1041,9 @@ struct RowPol {
       }
     }
   }
-  __device__ void keys_blocked(int64_t, int, bool, uint32_t, uint32_t, const PadKeys<K> &, Shared &) const {}
+  __device__ bool keys_blocked(int64_t, int, bool, uint32_t, uint32_t, const PadKeys<K> &, Shared &) const {
+    return false;
+  }
   __device__ uint64_t key_at_warp(int64_t k, uint32_t *) const {
     return ((uint64_t)(uint32_t)row[k] << cbits) | (uint32_t)col[k];
   }
@@ -886,14 +1121,15 @@ struct ColPol {
       }
     }
   }
-  // columns, blocked (thread t: entries 8t .. 8t+7): one search, then forward steps
-  __device__ void keys_blocked(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next,
+  // columns, blocked (thread t: entries 8t .. 8t+7): one search, then forward
+  // steps; the block synchronises after it
+  __device__ bool keys_blocked(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next,
                                const PadKeys<uint32_t> &sK, Shared &ps) const {
     const int64_t ncp = (int64_t)(last ? (uint32_t)in_f - 1 : c_next) - c0 + 2;
     const bool sm = ncp <= kCpCap;
     auto cpx = [&](int64_t x) -> int64_t { return sm ? ps.cp[x] : cp[c0 + x]; };
     const int e0 = threadIdx.x * kMkItems;
-    if (e0 >= len) return;
+    if (e0 >= len) return true;
     const int e1 = min(e0 + kMkItems, len);
     int64_t lo = 0, hi = ncp - 1;  // last x with cpx(x) <= base + e0, in [0, ncp - 2]
     while (hi - lo > 1) {
@@ -907,6 +1143,7 @@ struct ColPol {
       while (cpx(lo + 1) <= base + e) ++lo;
       sK[e] |= (c0 + (uint32_t)lo) << rbits;
     }
+    return true;
   }
   // column of entry e: the number of columns c >= 1 whose offset cp[c] is at most e
   __device__ uint64_t key_at_warp(int64_t e, uint32_t *aux) const {
@@ -932,13 +1169,6 @@ struct ColPol {
   }
 };
 
-// a column-view entry is kept when its weight survived
-struct ColKeep {
-  const int32_t *src_t;
-  const uint32_t *newidx;
-  __device__ uint64_t operator()(int64_t e) const { return newidx[src_t[e]] != ~0u ? 1ull : 0ull; }
-};
-
 // per-tile packed keep counts of f; exclusive prefixes in place when there are
 // more tiles than each merge block adds up itself
 template <typename F>
@@ -950,19 +1180,20 @@ cudaError_t keep_sums(F f, int64_t n, uint64_t *sums, cudaStream_t s, bool *dire
   return cudaGetLastError();
 }
 
-template <class Pol>
-cudaError_t launch_merge(const Pol &pol, const MkArgs &a, bool direct, cudaStream_t s) {
+template <class Pol, int kMode>
+cudaError_t launch_merge_mode(const Pol &pol, const MkArgs &a, cudaStream_t s) {
   constexpr size_t dyn = mk_smem_bytes<Pol>();
-  const unsigned grid = (unsigned)ceil_div(a.n, kMkTile);
-  cudaError_t e;
-  if (direct) {
-    e = raise_smem_limit(k_merge_kept<Pol, true>, dyn);
-    if (e == cudaSuccess) e = launch_pdl(k_merge_kept<Pol, true>, grid, kMkThreads, dyn, s, pol, a);
-  } else {
-    e = raise_smem_limit(k_merge_kept<Pol, false>, dyn);
-    if (e == cudaSuccess) e = launch_pdl(k_merge_kept<Pol, false>, grid, kMkThreads, dyn, s, pol, a);
-  }
+  cudaError_t e = raise_smem_limit(k_merge_kept<Pol, kMode>, dyn);
+  if (e == cudaSuccess)
+    e = launch_pdl(k_merge_kept<Pol, kMode>, (unsigned)ceil_div(a.n, kMkTile), kMkThreads, dyn, s, pol, a);
   return e;
+}
+
+template <class Pol>
+cudaError_t launch_merge(const Pol &pol, const MkArgs &a, int mode, cudaStream_t s) {
+  if (mode == kMkDirect) return launch_merge_mode<Pol, kMkDirect>(pol, a, s);
+  if (mode == kMkLookBack) return launch_merge_mode<Pol, kMkLookBack>(pol, a, s);
+  return launch_merge_mode<Pol, kMkGiven>(pol, a, s);
 }
 
 unsigned grid_for(int64_t n, int threads, int64_t cap = 65535 * 8) {
@@ -987,9 +1218,10 @@ double expected_draws(double n_pos, double empty, double need) {
 }
 
 struct RWs {
-  size_t state, dstate, sums, scan2, grown_a, B, Bq, cand, flags, hkeys, hmin, bcnt, bnd, bkey, bq, rk0, rv0, rk1,
-      rv1, rtemp, plan, total;
+  size_t state, dstate, sums, above, scand, scan2, grown_a, B, Bq, cand, flags, hkeys, hmin, bcnt, bnd, bkey, bq, rk0,
+      rv0, rk1, rv1, rtemp, plan, total;
   int64_t d_max, cap;
+  bool packed;     // positions below 2^32: one 64-bit word per table slot
   uint32_t n_bkt;  // buckets per order (row, column)
 };
 
@@ -1013,6 +1245,9 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(sizeof(DrawState), kAlign);
   w.sums = o;
   o += scan_temp_bytes<uint64_t>(nnz > 0 ? nnz : 1);
+  w.above = o;
+  w.scand = o;  // the keys in the select's first-digit bucket
+  if (n_prune > 0) o += align_up(8 * (size_t)(nnz > 0 ? nnz : 1), kAlign);
   w.scan2 = o;
   o += scan_temp_bytes<uint32_t>((int64_t)dmx);
   w.grown_a = o;
@@ -1025,10 +1260,11 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(8 * dmx, kAlign);
   w.flags = o;
   o += align_up(4 * dmx, kAlign);
+  w.packed = ((uint64_t)out_f << bits_for((uint64_t)(in_f - 1))) <= (1ull << 32);
   w.hkeys = o;
   o += align_up(8 * (size_t)cap, kAlign);
   w.hmin = o;
-  o += align_up(4 * (size_t)cap, kAlign);
+  if (!w.packed) o += align_up(4 * (size_t)cap, kAlign);
   const bool bk = w.n_bkt <= kBktMaxBuckets;
   w.bcnt = o;  // both orders' bucket counts, one launch clears them
   if (bk) o += align_up(4 * 2 * (size_t)w.n_bkt * kCntStride, kAlign);
@@ -1074,8 +1310,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   uint32_t *Bq = reinterpret_cast<uint32_t *>(b + W.Bq);
   uint64_t *cand = reinterpret_cast<uint64_t *>(b + W.cand);
   uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
-  uint64_t *hkeys = reinterpret_cast<uint64_t *>(b + W.hkeys);
-  uint32_t *hmin = reinterpret_cast<uint32_t *>(b + W.hmin);
+  const PosTable tab{reinterpret_cast<uint64_t *>(b + W.hkeys), reinterpret_cast<uint32_t *>(b + W.hmin),
+                     (uint64_t)(W.cap - 1), W.packed};
   uint32_t *bcnt = reinterpret_cast<uint32_t *>(b + W.bcnt);
   const PlanPtrs &pl = *a.plan;
   const TV *val = reinterpret_cast<const TV *>(a.val);
@@ -1125,12 +1361,11 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   auto draw_chunk = [&](int64_t m, bool first) -> cudaError_t {
     if (pl.col16)
       launch_pdl(k_draw<uint16_t>, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, pl.rp,
-                 (const uint16_t *)pl.col16, cand, hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
+                 (const uint16_t *)pl.col16, cand, tab, &ds->overflow);
     else
       launch_pdl(k_draw<int32_t>, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, pl.rp,
-                 a.col, cand, hkeys, hmin, (uint64_t)(W.cap - 1), &ds->overflow);
-    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, hkeys, hmin,
-               (uint64_t)(W.cap - 1), flags);
+                 a.col, cand, tab, &ds->overflow);
+    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, tab, flags);
     cudaError_t err =
         scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune}, &ds->total,
                                 stemp2, s2);
@@ -1160,6 +1395,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   const int64_t n_tiles = ceil_div(nnz, kMkTile);
   const uint32_t *row_guard = n_prune > 0 ? &ds->lists_ok : nullptr;
   const uint32_t *col_guard = n_prune > 0 ? &ds->col_ok : nullptr;
+  uint32_t *lb_err = pl.flags + kPlanFlagLookBack;
   // 3: the merge (after s waits for the row-order list) and the plan's row half
   bool row_direct = true;  // set with the keep counts below, before the first call
   auto queue_rows = [&]() -> cudaError_t {
@@ -1169,11 +1405,13 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     auto run = [&](auto rpol) -> cudaError_t {
       using P = decltype(rpol);
       launch_pdl(k_bounds<P>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s, rpol, n_prune, n_tiles,
-                 const_cast<MkBound *>(rbnd));
+                 const_cast<MkBound *>(rbnd), (uint64_t *)nullptr, (uint32_t *)nullptr);
       cudaError_t r = cudaGetLastError();
       return r != cudaSuccess ? r
-                              : launch_merge(rpol, MkArgs{nnz, n_prune, nnz, rbnd, sums, row_guard, cbits, a.out_f, pl.rp},
-                                             row_direct, s);
+                              : launch_merge(rpol,
+                                             MkArgs{nnz, n_prune, nnz, rbnd, sums, row_guard, cbits, a.out_f, pl.rp,
+                                                    nullptr, nullptr, nullptr},
+                                             row_direct ? kMkDirect : kMkGiven, s);
     };
     (void)nix;
     TV *vo = reinterpret_cast<TV *>(a.val_out);
@@ -1195,12 +1433,16 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     const ColPol cpol{pl.cp, pl.row_t, pl.rowt16, pl.src_t, pl.newidx, rbits, a.in_f, pl.gc_key, pl.gc_q, pl.gq,
                       pl.row_t_alt, pl.src_t_alt, pl.rowt16_alt};
     MkBound *cbnd = reinterpret_cast<MkBound *>(pl.cv_bnd);
-    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s2, cpol, n_prune, n_tiles, cbnd);
-    bool cdirect = true;
-    err = keep_sums(ColKeep{pl.src_t, pl.newidx}, nnz, pl.cv_sums, s2, &cdirect);
+    uint64_t *status = pl.cv_sums;  // one word per tile, then the ticket
+    uint32_t *ticket = reinterpret_cast<uint32_t *>(pl.cv_sums + n_tiles);
+    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s2, cpol, n_prune, n_tiles, cbnd, status,
+               ticket);
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    err = launch_merge(cpol, MkArgs{nnz, n_prune, nnz, cbnd, pl.cv_sums, col_guard, rbits, a.in_f, pl.cp_alt},
-                       cdirect, s2);
+    err = launch_merge(cpol,
+                       MkArgs{nnz, n_prune, nnz, cbnd, nullptr, col_guard, rbits, a.in_f, pl.cp_alt, status, ticket,
+                              pl.flags + kPlanFlagLookBack},
+                       kMkLookBack, s2);
     if (err != cudaSuccess) return err;
     return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s2);
   };
@@ -1213,7 +1455,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   int64_t m = 0;
   e = cudaSuccess;
   if (n_prune > 0) {
-    launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, hkeys, hmin, (int64_t)W.cap, bcnt,
+    launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, tab, bcnt,
                (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0));
     m = chunk_size();
     e = draw_chunk(m, true);
@@ -1221,21 +1463,21 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       const bool k32 = kbits <= 32;
       if (buckets) {
         launch_pdl(k_bkt_rank, (br.nb + 7) / 8, 256, 0, s2, br, RankDst{B, nullptr, Bq}, n_prune, ds,
-                   update ? (uint32_t *)nullptr : a.counts_dev, k32);
+                   update ? (uint32_t *)nullptr : a.counts_dev, k32, lb_err);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = mark();
         if (e == cudaSuccess && update) {
           launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds,
                      n_prune, bc, 1, cbits, rbits, &ds->col_overflow);
           launch_pdl(k_bkt_rank, (bc.nb + 7) / 8, 256, 0, s2, bc, RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds,
-                     a.counts_dev, true);
+                     a.counts_dev, true, lb_err);
           e = cudaGetLastError();
         }
       } else {
         e = sort_rows_general();
         if (e == cudaSuccess) e = sort_cols_general();
         if (e == cudaSuccess) {
-          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1);
+          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1, lb_err);
           e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = mark();
@@ -1252,12 +1494,21 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low; keep counts per tile
   launch_pdl(k_sel_init, 1, 256, 0, s, st, (uint32_t)n_prune);
   if (n_prune > 0) {
-    const unsigned g = grid_for((nnz + 15) / 16, 256, 1184);
-    launch_pdl(k_sel_pass<TV, 0>, g, 256, 0, s, val, nnz, st);
-    launch_pdl(k_sel_pass<TV, 1>, g, 256, 0, s, val, nnz, st);
-    launch_pdl(k_sel_pass<TV, 2>, g, 256, 0, s, val, nnz, st);
+    // first digit over every key; the keys in its bucket listed while each
+    // tile counts those above it; the rest of the select and the tiles' keep
+    // counts from the list
+    launch_pdl(k_sel_pass<TV, 0>, grid_for((nnz + 15) / 16, 256, 1184), 256, 0, s, val, nnz, st);
+    uint64_t *scand = reinterpret_cast<uint64_t *>(b + W.scand);
+    launch_pdl(k_sel_bucket<TV>, (unsigned)n_tiles, kScanThreads, 0, s, val, nnz, st, sums, scand);
+    launch_pdl(k_sel_cand<1>, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, st);
+    launch_pdl(k_sel_cand<2>, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, st);
+    launch_pdl(k_sel_tiles, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, (const SelState *)st, sums);
+    row_direct = n_tiles <= kScanDirectTiles;
+    if (!row_direct) launch_pdl(k_scan_spine<uint64_t>, 1, kScanThreads, 0, s, sums, n_tiles, (uint64_t *)nullptr);
+    e = cudaGetLastError();
+  } else {
+    e = keep_sums(KeepVal<TV>{val, st}, nnz, sums, s, &row_direct);
   }
-  e = keep_sums(KeepVal<TV>{val, st}, nnz, sums, s, &row_direct);
   // With the update, 3 and 4 are queued at once behind the lists' flags (they
   // write nothing unless the first chunk's lists came out whole); a plan
   // rebuild on s cannot be undone, so without the update they wait for the
@@ -1280,6 +1531,10 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       join();
       return SNACK_ERR_WORKSPACE;
     }
+    if (a.host_counts[4]) {  // the previous column-view update gave up waiting (its view was wrong)
+      join();
+      return SNACK_ERR_TIMEOUT;
+    }
     acc = a.host_counts[0] < (uint32_t)n_prune ? (int64_t)a.host_counts[0] : n_prune;
     done = m;
     if (acc < n_prune || a.host_counts[2]) {
@@ -1297,7 +1552,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
           verdict = SNACK_ERR_CUDA;
           break;
         }
-        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0);
+        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0, (uint32_t *)nullptr);
         if (cudaGetLastError() != cudaSuccess || cudaEventRecord(a.counts_ready, s2) != cudaSuccess ||
             cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
           verdict = SNACK_ERR_CUDA;

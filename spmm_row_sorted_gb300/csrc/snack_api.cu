@@ -381,7 +381,7 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
 bool readback_ready(snack_handle h) {
   if (!h->host_counts) {  // mapped, so a kernel writes the words and the host reads them with no copy
     void *hp = nullptr, *dp = nullptr;
-    if (cudaHostAlloc(&hp, 4 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess) return false;
+    if (cudaHostAlloc(&hp, 8 * sizeof(uint32_t), cudaHostAllocMapped) != cudaSuccess) return false;
     if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess || !dp) {
       cudaFreeHost(hp);
       return false;
@@ -450,6 +450,7 @@ snack_status snack_create(snack_handle *out_handle, int32_t out_f, int32_t in_f,
   SNACK_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   PlanPtrs p = plan_ptrs(lay, plan);
+  SNACK_CUDA(cudaMemsetAsync(p.flags, 0, sizeof(uint32_t) * 64, s));  // every flag word starts clear
   if (validate) {
     SNACK_CUDA(validate_pattern(out_f, in_f, nnz, row, col, p.flags, s));
     uint32_t flag = 0;
