@@ -1018,15 +1018,13 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 
 
 def restructure_launches() -> int:
-    """Kernel launches of one restructure of the workload (one draw chunk)."""
-    draw_chunk = 1 + 1 + 1 + 2 + 1  # init, draws, accept flags, scan (+ bucket fill), bucket offsets (second stream)
-    sort_grown = 1  # rank inside each bucket (second stream)
-    select = 1 + 3  # init, three digit passes (the last block of each picks the digit)
-    keep_scan = 2
-    merge = 2  # split points, merge (also writes the row offsets)
-    col_offsets = 1 + 2  # column digit histogram from the split points + its scan (second stream, beside the merge)
-    plan = 1 + 1 + 1 + 1  # row tiles (second stream), column scatter, per-group column sort, column tiles
-    return draw_chunk + sort_grown + select + keep_scan + merge + col_offsets + plan
+    """Kernel launches of one restructure of the workload (one draw chunk; the column view updated)."""
+    regrow = 1 + 1 + 1 + 2 + 1 + 1  # init, draws, acceptance flags, acceptance scan, row-order placement, rank
+    col_list = 1 + 1  # column-order placement and rank (second stream, beside the merge)
+    select = 1 + 1 + 1 + 2 + 1  # init, first digit, bucket listing, two digits over the list, tile keep counts
+    merge = 1 + 1 + 1  # tile bounds, merge (also the row offsets), forward tiles
+    colview = 1 + 1 + 1  # tile bounds, column-view merge, column tiles (second stream, after the call)
+    return regrow + col_list + select + merge + colview
 
 
 # ----------------------------------------------------------------------------
