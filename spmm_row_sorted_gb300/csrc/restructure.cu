@@ -42,6 +42,52 @@ namespace {
 
 constexpr uint64_t kEmpty = ~0ull;
 
+// Decoupled look-back, by one full warp, for tile b of a pass whose tiles are
+// taken in ticket order (every earlier tile has a block running): publish the
+// tile's total `agg` (a 62-bit value whose fields add without carries), add up
+// the predecessors' published values going back from the nearest, 32 at a
+// time, until one that includes everything before it, publish b's inclusive
+// total and return the exclusive one (in every lane).  Words: flag in bits
+// 62..63 (1: the tile's own total, 2: everything up to it), value below.
+// Every wait is bounded: after kLbMaxSpins polls *err is set and the sum so
+// far is returned.
+constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
+constexpr uint32_t kLbMaxSpins = 1u << 20;  // about 0.1 s of polling
+__device__ __forceinline__ uint64_t lb_pack(uint64_t x) { return (x & 0x7FFFFFFFull) | ((x >> 32) << 31); }
+__device__ __forceinline__ uint64_t lb_unpack(uint64_t v) { return (v & 0x7FFFFFFFull) | (((v >> 31) & 0x7FFFFFFFull) << 32); }
+
+__device__ uint64_t look_back(uint64_t *status, int64_t b, uint64_t agg, uint32_t *err) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) *reinterpret_cast<volatile uint64_t *>(&status[b]) = (b == 0 ? kLbInclusive : kLbAggregate) | agg;
+  uint64_t excl = 0;
+  int64_t i = b - 1;
+  uint32_t spins = 0;
+  while (i >= 0) {
+    const int64_t idx = i - lane;
+    const uint64_t v = idx >= 0 ? *reinterpret_cast<const volatile uint64_t *>(&status[idx]) : kLbInclusive;
+    const unsigned incl = __ballot_sync(0xffffffffu, (v >> 62) == 2u);
+    const int first = incl ? __ffs(incl) - 1 : 31;
+    const unsigned upto = first == 31 ? 0xffffffffu : ((2u << first) - 1u);  // lanes 0 .. first
+    const unsigned missing = __ballot_sync(0xffffffffu, (v >> 62) == 0u) & upto;
+    if (missing) {
+      if (++spins > kLbMaxSpins) {
+        if (lane == 0) atomicOr(err, 1u);
+        break;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    uint64_t val = (unsigned)lane <= (unsigned)first ? (v & kLbValue) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) val += __shfl_down_sync(0xffffffffu, val, o);
+    excl += __shfl_sync(0xffffffffu, val, 0);
+    if (incl) break;
+    i -= 32;
+  }
+  if (lane == 0 && b > 0) *reinterpret_cast<volatile uint64_t *>(&status[b]) = kLbInclusive | ((excl + agg) & kLbValue);
+  return excl;
+}
+
 struct SelState {
   uint32_t prefix, remaining, n_prune, total;  // prefix = threshold key t, remaining = ties to prune
   uint32_t overflow;                           // a draw found the position table full
@@ -382,10 +428,10 @@ struct PosTable {
     }
     return false;
   }
-  __device__ uint32_t min_of(uint64_t key) const {
-    uint64_t h = sm64_finalise(key) & mask;
+  __device__ uint64_t home(uint64_t key) const { return sm64_finalise(key) & mask; }
+  // the smallest draw index recorded for key, probing from slot h whose word is k
+  __device__ uint32_t min_from(uint64_t key, uint64_t h, uint64_t k) const {
     for (uint64_t probe = 0; probe <= mask; ++probe) {
-      const uint64_t k = keys[h];
       if (k == kEmpty) return 0xFFFFFFFFu;
       if (packed) {
         if ((k >> 32) == key) return (uint32_t)k;
@@ -393,8 +439,13 @@ struct PosTable {
         return mins[h];
       }
       h = (h + 1) & mask;
+      k = keys[h];
     }
     return 0xFFFFFFFFu;
+  }
+  __device__ uint32_t min_of(uint64_t key) const {
+    const uint64_t h = home(key);
+    return min_from(key, h, keys[h]);
   }
 };
 
@@ -438,29 +489,6 @@ __global__ void k_draw(uint64_t base, uint64_t i0, int64_t m, uint64_t n_pos, in
   }
 }
 
-// flag[idx] = 1 when draw i0 + idx found an empty position and is that
-// position's first draw (the minimum index recorded for it); one thread per
-// draw, so the table lookups of all draws are in flight at once
-__global__ void k_accept_flags(const uint64_t *__restrict__ cand, int64_t m, uint64_t i0, PosTable tab,
-                               uint32_t *__restrict__ flags) {
-  pdl_wait();
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < m; idx += stride) {
-    const uint64_t p = cand[idx];
-    flags[idx] = (p != kEmpty && tab.min_of(p) == (uint32_t)(i0 + (uint64_t)idx)) ? 1u : 0u;
-  }
-}
-
-struct FlagRead {
-  const uint32_t *f;
-  __device__ uint32_t operator()(int64_t i) const { return f[i]; }
-};
-
-struct CandPayload {
-  const uint64_t *cand;
-  __device__ uint64_t operator()(int64_t idx) const { return cand[idx]; }
-};
-
 constexpr int kBktTarget = 64;               // positions expected per bucket
 constexpr int kBktCap = 256;                 // slots per bucket
 constexpr uint32_t kBktMaxBuckets = 16384;   // more buckets: the regrown positions take the general sort
@@ -500,23 +528,12 @@ __device__ __forceinline__ uint64_t col_major(uint64_t p, int cbits, int rbits) 
   return ((p & ((1ull << cbits) - 1ull)) << rbits) | (p >> cbits);
 }
 
-// Accepted draws in draw order: rank q among the accepted; the first n_prune
-// are the regrown positions, grown[q].
-struct AcceptOut {
-  uint64_t *grown;
-  int64_t before, n_prune;
-  __device__ void operator()(int64_t, uint32_t ex, uint32_t v, uint64_t p) const {
-    if (!v) return;
-    const int64_t q = before + (int64_t)ex;
-    if (q < n_prune) grown[q] = p;
-  }
-};
-
 // Counters of the regrow branch (it runs beside the select on a second stream).
 struct DrawState {
   uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
   uint32_t bucket_overflow;  // a row-order bucket of the regrown positions ran out of slots
   uint32_t col_overflow;     // a column-order bucket did
+  uint32_t lb_fail;          // the acceptance scan gave up waiting for a predecessor tile (never expected)
   uint32_t lists_ok;         // the row-order list is complete: the merge may write
   uint32_t col_ok;           // and the column-order list: the column-view update may write
 };
@@ -527,16 +544,17 @@ struct DrawState {
 __device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made,
                                         uint32_t *lb_err) {
   const uint32_t tot = ds->total, ovf = ds->overflow, bovf = ds->bucket_overflow, covf = ds->col_overflow;
+  const uint32_t lbf = ds->lb_fail;
   if (host_words) {
     volatile uint32_t *hw = host_words;
     hw[0] = tot;
     hw[1] = ovf;
     hw[2] = bovf;
     hw[3] = covf;
-    hw[4] = lb_err ? *lb_err : 0u;
+    hw[4] = (lb_err ? *lb_err : 0u) | lbf;
     if (lb_err) *lb_err = 0u;
   }
-  const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf;
+  const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf && !lbf;
   ds->lists_ok = ok ? 1u : 0u;
   ds->col_ok = ok && !covf ? 1u : 0u;
 }
@@ -553,7 +571,8 @@ __global__ void k_set_word(uint32_t *w, uint32_t v) {
 
 // Start of a restructure's regrow branch: counters and bucket counts to zero,
 // the position table to empty (one launch instead of several fills).
-__global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bcnt, int64_t nb) {
+__global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bcnt, int64_t nb,
+                          uint64_t *__restrict__ lb_status, int64_t n_lb, uint32_t *lb_ticket) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -562,8 +581,10 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
     ds->overflow = 0u;
     ds->bucket_overflow = 0u;
     ds->col_overflow = 0u;
+    ds->lb_fail = 0u;
     ds->lists_ok = 0u;
     ds->col_ok = 0u;
+    *lb_ticket = 0u;
   }
   const int64_t cap = (int64_t)tab.mask + 1;
   for (int64_t i = i0; i < cap; i += stride) {
@@ -571,6 +592,7 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
     if (!tab.packed) tab.mins[i] = 0xFFFFFFFFu;
   }
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
+  for (int64_t i = i0; i < n_lb; i += stride) lb_status[i] = 0ull;
 }
 
 // The first chunk's regrown positions into one order's buckets (row order:
@@ -584,6 +606,110 @@ __global__ void k_place(const uint64_t *__restrict__ grown, const DrawState *ds,
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
     const uint64_t p = grown[q];
     bs.place(col_order ? col_major(p, cbits, rbits) : p, (uint32_t)q, bovf);
+  }
+}
+
+// Acceptance of a draw chunk, its scan over draw order and (first chunk) the
+// row-order bucket placement of the regrown positions, in one pass: tiles of
+// kScanTile draws taken in ticket order.  A block flags its tile's draws (an
+// empty position, and that position's first draw), scans the flags, learns
+// the accepted draws before its tile by look-back, and writes the first
+// n_prune accepted positions in draw order: grown[q] for acceptance rank q,
+// and (key, q) into the position's bucket.  The last tile's block writes the
+// chunk's accepted count.
+struct AcceptArgs {
+  const uint64_t *cand;
+  int64_t m;
+  uint64_t i0;
+  PosTable tab;
+  uint64_t *grown;
+  int64_t before, n_prune;
+  BucketSet br;  // br.nb == 0: no placement (chunks after the first)
+  uint32_t *bovf;
+  uint64_t *status;  // [tiles], zero before the launch
+  uint32_t *ticket;  // zero before the launch
+  uint32_t *err;
+  uint32_t *total;
+};
+
+__global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
+  constexpr int kPadded = kScanTile + kScanTile / 32 + 1;
+  __shared__ uint32_t sF[kPadded];  // flags, then exclusive counts (one pad word per 32)
+  __shared__ int64_t s_tile;
+  __shared__ uint32_t s_tot;
+  __shared__ uint64_t s_pre;
+  auto pad = [](int e) { return e + (e >> 5); };
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = atomicAdd(a.ticket, 1u);
+  __syncthreads();
+  const int64_t t = s_tile, base = t * kScanTile;
+  uint64_t p[kScanItems], h[kScanItems], w[kScanItems];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t idx = base + i * kScanThreads + tid;
+    p[i] = idx < a.m ? a.cand[idx] : kEmpty;
+  }
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {  // every item's first probe in flight at once
+    h[i] = a.tab.home(p[i]);
+    w[i] = p[i] != kEmpty ? a.tab.keys[h[i]] : kEmpty;
+  }
+  uint32_t f[kScanItems];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    const int64_t idx = base + i * kScanThreads + tid;
+    f[i] = p[i] != kEmpty && a.tab.min_from(p[i], h[i], w[i]) == (uint32_t)(a.i0 + (uint64_t)idx) ? 1u : 0u;
+    sF[pad(i * kScanThreads + tid)] = f[i];
+  }
+  __syncthreads();
+  {
+    uint32_t v[kScanItems], tsum = 0;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      v[i] = sF[pad(tid * kScanItems + i)];
+      tsum += v[i];
+    }
+    uint32_t ex = block_exclusive_scan<uint32_t>(tsum, &s_tot);
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      sF[pad(tid * kScanItems + i)] = ex;
+      ex += v[i];
+    }
+  }
+  if (warp == 0) {  // accepted draws of the tiles before this one
+    const uint64_t excl = look_back(a.status, t, s_tot, a.err);
+    if (lane == 0) {
+      s_pre = excl;
+      if (t == ceil_div(a.m, kScanTile) - 1) *a.total = (uint32_t)(excl + s_tot);
+    }
+  }
+  __syncthreads();
+  int64_t q[kScanItems];
+  bool put[kScanItems];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    q[i] = a.before + (int64_t)s_pre + sF[pad(i * kScanThreads + tid)];
+    put[i] = f[i] && q[i] < a.n_prune;
+    if (put[i]) a.grown[q[i]] = p[i];
+  }
+  if (a.br.nb) {  // bucket slots: every atomic in flight before the stores that use them
+    uint32_t bk[kScanItems], slot[kScanItems];
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      bk[i] = put[i] ? (uint32_t)__umul64hi(p[i], a.br.mult) : 0u;
+      slot[i] = put[i] ? atomicAdd(&a.br.cnt[(size_t)bk[i] * kCntStride], 1u) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      if (!put[i]) continue;
+      if (slot[i] < (uint32_t)kBktCap) {
+        a.br.key[(size_t)bk[i] * kBktCap + slot[i]] = p[i];
+        a.br.q[(size_t)bk[i] * kBktCap + slot[i]] = (uint32_t)q[i];
+      } else {
+        atomicOr(a.bovf, 1u);
+      }
+    }
   }
 }
 
@@ -734,12 +860,6 @@ struct MkArgs {
 
 // How a merge block learns the keep counts before its tile.
 constexpr int kMkGiven = 0, kMkDirect = 1, kMkLookBack = 2;
-// Look-back words: flag in bits 62..63 (1: the tile's own total, 2: the total
-// of all tiles up to and including it), kept and tie counts in 31 bits each.
-constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
-constexpr uint32_t kLbMaxSpins = 1u << 20;  // about 0.1 s of polling before a wait gives up
-__device__ __forceinline__ uint64_t lb_pack(uint64_t x) { return (x & 0x7FFFFFFFull) | ((x >> 32) << 31); }
-__device__ __forceinline__ uint64_t lb_unpack(uint64_t v) { return (v & 0x7FFFFFFFull) | (((v >> 31) & 0x7FFFFFFFull) << 32); }
 
 // number of entries of an ascending sequence at(0..n) below v, by one warp:
 // each round probes 32 evenly spaced entries and keeps the bracket of the
@@ -908,41 +1028,10 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
     }
     if (tid == 0) sX[kpad<uint64_t>(kMkTile)] = s_tot;
   }
-  if (kMode == kMkLookBack && warp == 0) {
-    // publish this tile's kept and tie counts, then add up the predecessors'
-    // going back from the nearest, 32 tiles at a time, until a tile whose
-    // total includes everything before it
-    const uint64_t agg = lb_pack((s_tot & 0xFFFFull) | (((s_tot >> 16) & 0xFFFFull) << 32));
-    if (lane == 0) *reinterpret_cast<volatile uint64_t *>(&a.status[b]) = (b == 0 ? kLbInclusive : kLbAggregate) | agg;
-    uint64_t excl = 0;
-    int64_t i = b - 1;
-    uint32_t spins = 0;
-    while (i >= 0) {
-      const int64_t idx = i - lane;
-      const uint64_t v = idx >= 0 ? *reinterpret_cast<const volatile uint64_t *>(&a.status[idx]) : kLbInclusive;
-      const unsigned incl = __ballot_sync(0xffffffffu, (v >> 62) == 2u);
-      const int first = incl ? __ffs(incl) - 1 : 31;
-      const unsigned upto = first == 31 ? 0xffffffffu : ((2u << first) - 1u);  // lanes 0 .. first
-      const unsigned missing = __ballot_sync(0xffffffffu, (v >> 62) == 0u) & upto;
-      if (missing) {
-        if (++spins > kLbMaxSpins) {  // give up (the counts are then wrong; the error word says so)
-          if (lane == 0) atomicOr(a.err, 1u);
-          break;
-        }
-        __nanosleep(64);
-        continue;
-      }
-      uint64_t val = (unsigned)lane <= (unsigned)first ? (v & kLbValue) : 0ull;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) val += __shfl_down_sync(0xffffffffu, val, o);
-      excl += __shfl_sync(0xffffffffu, val, 0);
-      if (incl) break;
-      i -= 32;
-    }
-    if (lane == 0) {
-      if (b > 0) *reinterpret_cast<volatile uint64_t *>(&a.status[b]) = kLbInclusive | ((excl + agg) & kLbValue);
-      s_pre = lb_unpack(excl);
-    }
+  if (kMode == kMkLookBack && warp == 0) {  // the kept and tie counts of the tiles before this one
+    const uint64_t excl = look_back(a.status, b, lb_pack((s_tot & 0xFFFFull) | (((s_tot >> 16) & 0xFFFFull) << 32)),
+                                    a.err);
+    if (lane == 0) s_pre = lb_unpack(excl);
   }
   __syncthreads();
   const uint32_t preG = (uint32_t)s_pre, preE = (uint32_t)(s_pre >> 32), lo32 = (uint32_t)lo, c00 = s_c00;
@@ -1218,8 +1307,8 @@ double expected_draws(double n_pos, double empty, double need) {
 }
 
 struct RWs {
-  size_t state, dstate, sums, above, scand, scan2, grown_a, B, Bq, cand, flags, hkeys, hmin, bcnt, bnd, bkey, bq, rk0,
-      rv0, rk1, rv1, rtemp, plan, total;
+  size_t state, dstate, sums, above, scand, scan2, grown_a, B, Bq, cand, alb, hkeys, hmin, bcnt, bnd, bkey, bq,
+      rk0, rv0, rk1, rv1, rtemp, plan, total;
   int64_t d_max, cap;
   bool packed;     // positions below 2^32: one 64-bit word per table slot
   uint32_t n_bkt;  // buckets per order (row, column)
@@ -1258,8 +1347,8 @@ RWs rws_layout(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   o += align_up(4 * np, kAlign);
   w.cand = o;
   o += align_up(8 * dmx, kAlign);
-  w.flags = o;
-  o += align_up(4 * dmx, kAlign);
+  w.alb = o;  // the acceptance scan's look-back words (one per tile of draws) and its ticket
+  o += align_up(8 * ((size_t)ceil_div((int64_t)dmx, kScanTile) + 1), kAlign);
   w.packed = ((uint64_t)out_f << bits_for((uint64_t)(in_f - 1))) <= (1ull << 32);
   w.hkeys = o;
   o += align_up(8 * (size_t)cap, kAlign);
@@ -1309,7 +1398,6 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   uint64_t *B = reinterpret_cast<uint64_t *>(b + W.B);
   uint32_t *Bq = reinterpret_cast<uint32_t *>(b + W.Bq);
   uint64_t *cand = reinterpret_cast<uint64_t *>(b + W.cand);
-  uint32_t *flags = reinterpret_cast<uint32_t *>(b + W.flags);
   const PosTable tab{reinterpret_cast<uint64_t *>(b + W.hkeys), reinterpret_cast<uint32_t *>(b + W.hmin),
                      (uint64_t)(W.cap - 1), W.packed};
   uint32_t *bcnt = reinterpret_cast<uint32_t *>(b + W.bcnt);
@@ -1365,13 +1453,16 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     else
       launch_pdl(k_draw<int32_t>, grid_for(m, 256), 256, 0, s2, base, (uint64_t)done, m, n_pos, a.in_f, cbits, pl.rp,
                  a.col, cand, tab, &ds->overflow);
-    launch_pdl(k_accept_flags, grid_for(m, 256), 256, 0, s2, cand, m, (uint64_t)done, tab, flags);
-    cudaError_t err =
-        scan_apply_pl<uint32_t>(FlagRead{flags}, CandPayload{cand}, m, AcceptOut{grown_a, acc, n_prune}, &ds->total,
-                                stemp2, s2);
-    if (err != cudaSuccess || !first || !buckets) return err;
-    launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds, n_prune,
-               br, 0, cbits, rbits, &ds->bucket_overflow);
+    const int64_t n_at = ceil_div(m, kScanTile);
+    uint64_t *alb = reinterpret_cast<uint64_t *>(b + W.alb);
+    uint32_t *aticket = reinterpret_cast<uint32_t *>(alb + n_at);
+    if (!first) {  // the first chunk's words were cleared with the table
+      cudaError_t err = cudaMemsetAsync(alb, 0, sizeof(uint64_t) * (size_t)n_at + sizeof(uint32_t), s2);
+      if (err != cudaSuccess) return err;
+    }
+    const AcceptArgs aa{cand, m, (uint64_t)done, tab, grown_a, acc, n_prune, first && buckets ? br : BucketSet{},
+                        &ds->bucket_overflow, alb, aticket, &ds->lb_fail, &ds->total};
+    launch_pdl(k_accept_scan, (unsigned)n_at, kScanThreads, 0, s2, aa);
     return cudaGetLastError();
   };
   auto chunk_size = [&]() -> int64_t {
@@ -1455,8 +1546,11 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   int64_t m = 0;
   e = cudaSuccess;
   if (n_prune > 0) {
+    const int64_t n_at1 = ceil_div(chunk_size(), kScanTile);
+    uint64_t *alb = reinterpret_cast<uint64_t *>(b + W.alb);
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, tab, bcnt,
-               (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0));
+               (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0), alb, n_at1,
+               reinterpret_cast<uint32_t *>(alb + n_at1));
     m = chunk_size();
     e = draw_chunk(m, true);
     if (e == cudaSuccess) {
@@ -1531,8 +1625,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       join();
       return SNACK_ERR_WORKSPACE;
     }
-    if (a.host_counts[4]) {  // the previous column-view update gave up waiting (its view was wrong)
-      join();
+    if (a.host_counts[4]) {  // a wait for a predecessor tile gave up (this call's acceptance, or the
+      join();                 // previous column-view update): nothing trustworthy was written
       return SNACK_ERR_TIMEOUT;
     }
     acc = a.host_counts[0] < (uint32_t)n_prune ? (int64_t)a.host_counts[0] : n_prune;
@@ -1560,6 +1654,10 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
         }
         if (a.host_counts[1]) {
           verdict = SNACK_ERR_WORKSPACE;
+          break;
+        }
+        if (a.host_counts[4]) {
+          verdict = SNACK_ERR_TIMEOUT;
           break;
         }
         acc += a.host_counts[0];
