@@ -1215,23 +1215,32 @@ struct ColPol {
   __device__ bool keys_blocked(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next,
                                const PadKeys<uint32_t> &sK, Shared &ps) const {
     const int64_t ncp = (int64_t)(last ? (uint32_t)in_f - 1 : c_next) - c0 + 2;
-    const bool sm = ncp <= kCpCap;
-    auto cpx = [&](int64_t x) -> int64_t { return sm ? ps.cp[x] : cp[c0 + x]; };
     const int e0 = threadIdx.x * kMkItems;
     if (e0 >= len) return true;
     const int e1 = min(e0 + kMkItems, len);
-    int64_t lo = 0, hi = ncp - 1;  // last x with cpx(x) <= base + e0, in [0, ncp - 2]
-    while (hi - lo > 1) {
-      const int64_t md = (lo + hi) >> 1;
-      if (cpx(md) <= base + e0)
-        lo = md;
-      else
-        hi = md;
-    }
-    for (int e = e0; e < e1; ++e) {
-      while (cpx(lo + 1) <= base + e) ++lo;
-      sK[e] |= (c0 + (uint32_t)lo) << rbits;
-    }
+    // the last x in [0, ncp - 2] with off[x] <= base + e0, then forward steps
+    // (32-bit: positions are below 2^31)
+    auto walk = [&](const int32_t *off) {
+      const int32_t t0 = (int32_t)base + e0;
+      int lo = 0, hi = (int)ncp - 1;
+      while (hi - lo > 1) {
+        const int md = (lo + hi) >> 1;
+        if (off[md] <= t0)
+          lo = md;
+        else
+          hi = md;
+      }
+      int32_t nxt = off[lo + 1];
+      for (int e = e0; e < e1; ++e) {
+        const int32_t pos = (int32_t)base + e;
+        while (nxt <= pos) nxt = off[++lo + 1];
+        sK[e] |= (c0 + (uint32_t)lo) << rbits;
+      }
+    };
+    if (ncp <= kCpCap)
+      walk(ps.cp);
+    else
+      walk(cp + c0);
     return true;
   }
   // column of entry e: the number of columns c >= 1 whose offset cp[c] is at most e
