@@ -95,7 +95,7 @@ typedef enum snack_status {
   SNACK_ERR_OUT_OF_RANGE = 3, /* validation: an index outside [0,out_f) x [0,in_f) */
   SNACK_ERR_WORKSPACE = 4,    /* plan or workspace smaller than the call needs (the queried sizes always do) */
   SNACK_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
-  SNACK_ERR_TIMEOUT = 6,      /* reserved for bounded device-side waits (none today) */
+  SNACK_ERR_TIMEOUT = 6,      /* restructure: a bounded device-side wait gave up (not expected); nothing was changed */
   SNACK_ERR_UNSUPPORTED = 7,  /* val and act dtypes differ, or max(out_f, in_f) x padded batch >= 2^32 */
   SNACK_ERR_NO_SPACE = 8      /* restructure: too few empty positions, or draw budget spent */
 } snack_status;

@@ -16,7 +16,8 @@ struct PlanPtrs {
   int32_t *tiles_f;  // [(nt_f + 1) * 2] forward merge-path split points
   int32_t *cp;       // [in_f + 1]    column offsets of the column view
   int32_t *tiles_t;  // [(nt_t + 1) * 2] input-gradient split points
-  int32_t *row_t;    // [nnz]         row of each column-view entry
+  int32_t *row_t;    // [nnz]         row of each column-view entry (not kept up to date when rowt16 exists:
+                     //               every reader takes the 16-bit copy then)
   int32_t *src_t;    // [nnz]         storage index of each column-view entry
   uint32_t *flags;   // [64]          validation flags and small device scalars
   uint16_t *col16;   // [nnz]         16-bit copy of col (in_f <= 65536), else null
@@ -32,7 +33,8 @@ struct PlanPtrs {
   uint32_t *gq;       // [cv_pmax] output index of each regrown weight, by acceptance rank
   uint32_t *gc_key;   // [cv_pmax] regrown positions in column order, col << rbits | row
   uint32_t *gc_q;     // [cv_pmax] and their acceptance ranks
-  uint64_t *cv_sums;  // kept entries per column-view tile (scan_temp_bytes<uint64_t>(nnz))
+  uint32_t *cv_pcnt;  // [in_f] pruned weights per column (written by the restructure's merge)
+  uint32_t *cv_ppre;  // [in_f] their exclusive prefix (16-byte aligned)
   void *cv_bnd;       // bounds of the update's tiles of kScanTile entries (32 bytes per tile, and one more)
   int64_t cv_pmax;    // most weights a restructure may prune and still update (else rebuild)
   // Moderately sparse bf16 layers (dense_layer): per 64-column block and row,
@@ -41,14 +43,11 @@ struct PlanPtrs {
   void *tables;
 };
 
-// Words of PlanPtrs::flags: [0] pattern validation, [1] constant fan-in check,
-// [kPlanFlagLookBack] set when a column-view update gave up waiting for a
-// predecessor tile's counts.
-constexpr int kPlanFlagLookBack = 2;
+// Words of PlanPtrs::flags: [0] pattern validation, [1] constant fan-in check.
 
 struct PlanLayout {
   size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cpa, off_tta,
-      off_rowta, off_srcta, off_rowt16a, off_newidx, off_gq, off_gck, off_gcq, off_cvs, off_cvb, off_tab, total;
+      off_rowta, off_srcta, off_rowt16a, off_newidx, off_gq, off_gck, off_gcq, off_cvs, off_cvq, off_cvb, off_tab, total;
   bool c16, r16;  // the 16-bit index copies exist
   bool cv;        // the second column view and the incremental update's scratch exist
   int64_t cv_pmax;

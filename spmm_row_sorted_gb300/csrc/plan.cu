@@ -214,8 +214,10 @@ __global__ void __launch_bounds__(kRadixThreads) k_colview_bucket(const uint32_t
       const int c = s_col[e];
       const uint32_t pos = run[c] + (uint32_t)e - lstart[c];
       src_t[pos] = (int32_t)s_src[e];
-      row_t[pos] = (int32_t)s_row[e];
-      if (rowt16) rowt16[pos] = (uint16_t)s_row[e];
+      if (rowt16)
+        rowt16[pos] = (uint16_t)s_row[e];
+      else
+        row_t[pos] = (int32_t)s_row[e];
     }
     __syncthreads();
     for (int c = threadIdx.x; c < L; c += kRadixThreads) {  // advance each column by its count in the chunk
@@ -368,7 +370,7 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
   L.cv = colview_update_ok(out_f, in_f, nnz);
   L.cv_pmax = L.cv ? (nnz + 3) / 4 : 0;
   L.off_cpa = L.off_tta = L.off_rowta = L.off_srcta = L.off_rowt16a = L.off_newidx = L.off_gq = L.off_gck =
-      L.off_gcq = L.off_cvs = L.off_cvb = o;
+      L.off_gcq = L.off_cvs = L.off_cvq = L.off_cvb = o;
   if (L.cv) {
     const size_t n = (size_t)nnz, pm = (size_t)L.cv_pmax;
     L.off_cpa = o;
@@ -390,7 +392,9 @@ PlanLayout plan_layout(int32_t out_f, int32_t in_f, int64_t nnz, int bt_max, int
     L.off_gcq = o;
     o += align_up(sizeof(uint32_t) * pm, kAlign);
     L.off_cvs = o;
-    o += scan_temp_bytes<uint64_t>(nnz);
+    o += align_up(sizeof(uint32_t) * (size_t)in_f, kAlign);
+    L.off_cvq = o;
+    o += align_up(sizeof(uint32_t) * (size_t)in_f, kAlign);
     L.off_cvb = o;
     o += align_up(32 * (size_t)(ceil_div(nnz, kScanTile) + 1), kAlign);
   }
@@ -422,7 +426,8 @@ PlanPtrs plan_ptrs(const PlanLayout &L, void *base) {
   p.gq = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gq) : nullptr;
   p.gc_key = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gck) : nullptr;
   p.gc_q = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_gcq) : nullptr;
-  p.cv_sums = L.cv ? reinterpret_cast<uint64_t *>(b + L.off_cvs) : nullptr;
+  p.cv_pcnt = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvs) : nullptr;
+  p.cv_ppre = L.cv ? reinterpret_cast<uint32_t *>(b + L.off_cvq) : nullptr;
   p.cv_bnd = L.cv ? reinterpret_cast<void *>(b + L.off_cvb) : nullptr;
   p.cv_pmax = L.cv_pmax;
   p.tables = L.dense ? reinterpret_cast<void *>(b + L.off_tab) : nullptr;

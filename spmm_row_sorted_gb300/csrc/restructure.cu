@@ -53,8 +53,6 @@ constexpr uint64_t kEmpty = ~0ull;
 // far is returned.
 constexpr uint64_t kLbAggregate = 1ull << 62, kLbInclusive = 2ull << 62, kLbValue = (1ull << 62) - 1;
 constexpr uint32_t kLbMaxSpins = 1u << 20;  // about 0.1 s of polling
-__device__ __forceinline__ uint64_t lb_pack(uint64_t x) { return (x & 0x7FFFFFFFull) | ((x >> 32) << 31); }
-__device__ __forceinline__ uint64_t lb_unpack(uint64_t v) { return (v & 0x7FFFFFFFull) | (((v >> 31) & 0x7FFFFFFFull) << 32); }
 
 __device__ uint64_t look_back(uint64_t *status, int64_t b, uint64_t agg, uint32_t *err) {
   const int lane = threadIdx.x & 31;
@@ -443,10 +441,6 @@ struct PosTable {
     }
     return 0xFFFFFFFFu;
   }
-  __device__ uint32_t min_of(uint64_t key) const {
-    const uint64_t h = home(key);
-    return min_from(key, h, keys[h]);
-  }
 };
 
 __device__ __forceinline__ uint32_t mag_of(float v) { return canon_mag(__float_as_uint(v) & 0x7FFFFFFFu); }
@@ -539,10 +533,8 @@ struct DrawState {
 };
 
 // The lists' verdict and, with host_words, the chunk's counters to the host's
-// mapped words, with the plan's look-back error word (set by an earlier
-// column-view update that gave up waiting; read and cleared here).
-__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made,
-                                        uint32_t *lb_err) {
+// mapped words.
+__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made) {
   const uint32_t tot = ds->total, ovf = ds->overflow, bovf = ds->bucket_overflow, covf = ds->col_overflow;
   const uint32_t lbf = ds->lb_fail;
   if (host_words) {
@@ -551,17 +543,16 @@ __device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t
     hw[1] = ovf;
     hw[2] = bovf;
     hw[3] = covf;
-    hw[4] = (lb_err ? *lb_err : 0u) | lbf;
-    if (lb_err) *lb_err = 0u;
+    hw[4] = lbf;
   }
   const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf && !lbf;
   ds->lists_ok = ok ? 1u : 0u;
   ds->col_ok = ok && !covf ? 1u : 0u;
 }
 
-__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made, uint32_t *lb_err) {
+__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made) {
   pdl_wait();
-  publish(ds, n_prune, host_words, made != 0, lb_err);
+  publish(ds, n_prune, host_words, made != 0);
 }
 
 __global__ void k_set_word(uint32_t *w, uint32_t v) {
@@ -569,10 +560,12 @@ __global__ void k_set_word(uint32_t *w, uint32_t v) {
   *w = v;
 }
 
-// Start of a restructure's regrow branch: counters and bucket counts to zero,
-// the position table to empty (one launch instead of several fills).
+// Start of a restructure's regrow branch: counters, bucket counts and the
+// column-view update's pruned counts per column to zero, the position table
+// to empty (one launch instead of several fills).
 __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bcnt, int64_t nb,
-                          uint64_t *__restrict__ lb_status, int64_t n_lb, uint32_t *lb_ticket) {
+                          uint64_t *__restrict__ lb_status, int64_t n_lb, uint32_t *lb_ticket,
+                          uint32_t *__restrict__ pcnt, int64_t n_pc) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -593,6 +586,7 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
   }
   for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
   for (int64_t i = i0; i < n_lb; i += stride) lb_status[i] = 0ull;
+  for (int64_t i = i0; i < n_pc; i += stride) pcnt[i] = 0u;
 }
 
 // The first chunk's regrown positions into one order's buckets (row order:
@@ -725,12 +719,12 @@ struct RankDst {
 // bucket's keys (all distinct).  Block 0 first sets the lists' verdict (and,
 // with host_words, publishes the chunk's counters).
 __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet S, RankDst D, int64_t n_prune, DrawState *ds,
-                                                  uint32_t *host_words, bool k32, uint32_t *lb_err) {
+                                                  uint32_t *host_words, bool k32) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true, lb_err);
+  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true);
   const uint32_t b0 = blockIdx.x * 8;
   uint32_t part = 0;
   for (uint32_t i0 = threadIdx.x; i0 < b0; i0 += 256 * 8) {  // eight loads in flight per round
@@ -805,16 +799,14 @@ struct GrownColSrc {
 // major index (key >> minor_bits) is below M, written by the tile after
 // whose element major M starts.
 //
-// A block loads its tile striped (coalesced), scans the counts and walks the
-// tile against its list slice blocked (thread t: elements 8t .. 8t+7, one
-// binary search and then forward steps), and writes striped again, each
-// element's output index passed through shared memory.
+// A block loads its tile striped (coalesced), counts each of its list keys
+// on the last element below it (a binary search over the tile's keys in
+// shared memory), scans the counts blocked (thread t: elements 8t .. 8t+7)
+// and writes striped again.
 
 constexpr int kMkThreads = 256, kMkItems = 8, kMkTile = kMkThreads * kMkItems;
 static_assert(kMkTile == kScanTile, "a tile's keep counts are one scan tile's sum");
-constexpr int kMkListCap = 2048;                       // list keys of a tile staged in shared memory
-constexpr int kMkXWords = kMkTile + kMkTile / 32 + 1;  // padded local counts, index kMkTile included
-__device__ __forceinline__ int mk_pad(int e) { return e + (e >> 5); }
+constexpr int kMkListCap = 2048;  // list keys of a tile staged in shared memory
 // Tile arrays are read both striped (thread t: t, t + 256, ...) and blocked
 // (thread t: 8t .. 8t+7); one pad word per 32 words keeps both free of bank
 // conflicts (one 8-byte pad per 16 keys for 64-bit keys).
@@ -833,12 +825,12 @@ struct PadKeys {  // sK[e] through the padded index
 };
 
 // Bounds of tile t: its first key and the list keys below it (tile n_tiles:
-// key ~0, every list key), and the policy's note on the first element (the
-// column view: its column).
+// key ~0, every list key), and the policy's notes on the first element (the
+// column view: its column, and that column's first entry).
 struct MkBound {
   uint64_t key;
   int64_t lo;
-  uint32_t aux, pad;
+  uint32_t aux, aux2;
 };
 static_assert(sizeof(MkBound) <= 32, "the plan reserves 32 bytes per tile bound");
 
@@ -851,15 +843,17 @@ struct MkArgs {
   int minor_bits;
   int64_t n_major;
   int32_t *off;  // [n_major + 1]
-  // kMkLookBack: tiles are taken in ticket order and each block finds the
-  // counts before its tile from its predecessors' published totals
-  uint64_t *status;  // [n_tiles], zero before the launch
-  uint32_t *ticket;  // zero before the launch
-  uint32_t *err;     // set when a wait for a predecessor gave up (never expected)
+  // kMkByColumn: pruned entries in the columns before each column, exclusive
+  // prefix (null when nothing is pruned)
+  const uint32_t *col_pre;
 };
 
-// How a merge block learns the keep counts before its tile.
-constexpr int kMkGiven = 0, kMkDirect = 1, kMkLookBack = 2;
+// How a merge block learns the keep counts before its tile: given as
+// exclusive prefixes, added up from the per-tile counts, or (the column
+// view) its first entry's index less the pruned entries before it, which
+// are those of the columns before the tile's first column plus those of
+// that column ahead of the tile.
+constexpr int kMkGiven = 0, kMkDirect = 1, kMkByColumn = 2;
 
 // number of entries of an ascending sequence at(0..n) below v, by one warp:
 // each round probes 32 evenly spaced entries and keeps the bracket of the
@@ -902,22 +896,75 @@ constexpr size_t mk_smem_bytes() {
          sizeof(uint16_t) * kMkListCap + sizeof(typename Pol::Shared);
 }
 
+// Exclusive prefix sums pre[c] = cnt[0] + .. + cnt[c - 1], c < n, by one
+// block of kScanThreads, kPfxItems consecutive counts per thread a round:
+// added up, block-scanned, then read again (from L1) to write the prefixes,
+// so no thread holds its counts across the scan.
+constexpr int kPfxItems = 64;
+__device__ void block_prefix_u32(const uint32_t *cnt, uint32_t *pre, int64_t n) {
+  __shared__ uint32_t s_tot;
+  uint32_t carry = 0;
+  for (int64_t r0 = 0; r0 < n; r0 += (int64_t)kScanThreads * kPfxItems) {
+    const int64_t b = r0 + (int64_t)threadIdx.x * kPfxItems;
+    const bool whole = b + kPfxItems <= n;  // 16-byte aligned: b is a multiple of kPfxItems
+    uint32_t sum = 0;
+    if (whole) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(cnt + b);
+#pragma unroll
+      for (int i = 0; i < kPfxItems / 4; ++i) {
+        const uint4 q = p[i];
+        sum += q.x + q.y + q.z + q.w;
+      }
+    } else {
+      for (int i = 0; i < kPfxItems; ++i) sum += b + i < n ? cnt[b + i] : 0u;
+    }
+    uint32_t ex = carry + block_exclusive_scan<uint32_t>(sum, &s_tot);
+    if (whole) {
+      const uint4 *p = reinterpret_cast<const uint4 *>(cnt + b);
+      uint4 *o = reinterpret_cast<uint4 *>(pre + b);
+#pragma unroll 4
+      for (int i = 0; i < kPfxItems / 4; ++i) {
+        const uint4 q = p[i];
+        uint4 w;
+        w.x = ex;
+        w.y = w.x + q.x;
+        w.z = w.y + q.y;
+        w.w = w.z + q.z;
+        ex = w.w + q.w;
+        o[i] = w;
+      }
+    } else {
+      for (int i = 0; i < kPfxItems && b + i < n; ++i) {
+        const uint32_t x = cnt[b + i];
+        pre[b + i] = ex;
+        ex += x;
+      }
+    }
+    carry += s_tot;
+  }
+}
+
 // Tile bounds, one warp per tile t in [0, n_tiles], all at once (so the merge
 // blocks start with their bounds instead of searching the list themselves);
-// for a look-back merge also its per-tile words and ticket, cleared.
+// with pcnt, one more block (the last) writes the exclusive prefix of the
+// n_cols counts pcnt into ppre.
 template <class Pol>
-__global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd, uint64_t *status, uint32_t *ticket) {
+__global__ void k_bounds(Pol pol, int64_t n_list, int64_t n_tiles, MkBound *bnd, const uint32_t *pcnt,
+                         uint32_t *ppre, int64_t n_cols) {
   pdl_wait();
+  if constexpr (Pol::kByColumn) {
+    if (pcnt && blockIdx.x == gridDim.x - 1) {
+      block_prefix_u32(pcnt, ppre, n_cols);
+      return;
+    }
+  }
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t > n_tiles) return;
-  if (status && (threadIdx.x & 31) == 0) {  // a look-back merge's per-tile words and ticket, cleared
-    if (t < n_tiles) status[t] = 0ull;
-    if (t == 0) *ticket = 0u;
-  }
   MkBound r{~0ull, n_list, 0u, 0u};
   if (t < n_tiles) {
     r.key = pol.key_at_warp(t * (int64_t)kMkTile, &r.aux);
     r.lo = t == 0 ? 0 : lb_warp([&](int64_t j) { return pol.list_key(j); }, n_list, r.key);
+    if constexpr (Pol::kByColumn) r.aux2 = (uint32_t)pol.cp[r.aux];
   }
   if ((threadIdx.x & 31) == 0) bnd[t] = r;
 }
@@ -941,18 +988,11 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
   __shared__ uint64_t s_red[kMkThreads / 32];
   __shared__ uint64_t s_tot;
   __shared__ uint32_t s_c00;
-  __shared__ int64_t s_tile;
   pdl_wait();
   // every load of the tile's inputs is issued before the first wait on one
   const uint32_t go = a.guard ? *reinterpret_cast<const volatile uint32_t *>(a.guard) : 1u;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int64_t b = blockIdx.x;
-  if (kMode == kMkLookBack) {  // tiles in ticket order: every tile before this one has a block running
-    if (go == 0u) return;
-    if (tid == 0) s_tile = atomicAdd(a.ticket, 1u);
-    __syncthreads();
-    b = s_tile;
-  }
+  const int64_t b = blockIdx.x;
   const int64_t base = b * (int64_t)kMkTile;
   const int len = (int)(a.n - base < kMkTile ? a.n - base : kMkTile);
   const bool last = b == (int64_t)gridDim.x - 1;
@@ -960,7 +1000,15 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
   const uint32_t m = pol.ties_dropped();
   typename Pol::Item it[kMkItems];
   uint32_t fl[kMkItems];
-  pol.load(base, len, last, bd0.aux, bd1.aux, it, fl, sK, ps);
+  // (the column view: this thread's share of the pruned entries of the
+  // tile's first column ahead of the tile, and those of the columns before)
+  uint32_t ahead = pol.load(base, len, last, bd0, bd1.aux, it, fl, sK, ps);
+  const uint32_t col_pre = kMode == kMkByColumn && a.col_pre && tid == 0 ? a.col_pre[bd0.aux] : 0u;
+  if constexpr (kMode == kMkByColumn) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ahead += __shfl_down_sync(0xffffffffu, ahead, o);
+    if (lane == 0) s_red[warp] = ahead;
+  }
   const int64_t lo = bd0.lo, cnt = bd1.lo - bd0.lo;
   const bool lsm = cnt <= kMkListCap;
   if (lsm)
@@ -990,11 +1038,16 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
     s_c00 = 0u;
   }
   __syncthreads();
-  if (tid == 0 && kMode != kMkLookBack) {
+  if (tid == 0) {
     uint64_t p = 0;
     if (kDirect) {
 #pragma unroll
       for (int w = 0; w < kMkThreads / 32; ++w) p += s_red[w];
+    } else if (kMode == kMkByColumn) {  // kept entries before the tile (no ties in this order)
+      uint32_t np = col_pre;
+#pragma unroll
+      for (int w = 0; w < kMkThreads / 32; ++w) np += s_red[w];
+      p = (uint64_t)((uint32_t)base - np);
     } else {
       p = a.sums[b];
     }
@@ -1028,11 +1081,6 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
     }
     if (tid == 0) sX[kpad<uint64_t>(kMkTile)] = s_tot;
   }
-  if (kMode == kMkLookBack && warp == 0) {  // the kept and tie counts of the tiles before this one
-    const uint64_t excl = look_back(a.status, b, lb_pack((s_tot & 0xFFFFull) | (((s_tot >> 16) & 0xFFFFull) << 32)),
-                                    a.err);
-    if (lane == 0) s_pre = lb_unpack(excl);
-  }
   __syncthreads();
   const uint32_t preG = (uint32_t)s_pre, preE = (uint32_t)(s_pre >> 32), lo32 = (uint32_t)lo, c00 = s_c00;
   auto surv = [&](uint64_t x) -> uint32_t {  // kept elements below, from an exclusive count
@@ -1055,7 +1103,7 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
         const uint32_t pos = surv(x) + lo32 + below(x);
         if ((int64_t)pos < a.n_out) pol.write_kept(it[i], base + e, pos, key);
       } else {
-        pol.write_dropped(it[i], base + e);
+        pol.write_dropped(it[i], base + e, key);
       }
       const uint32_t maj = (uint32_t)(key >> mb);
       const uint32_t nxt = e + 1 == len && last ? nmaj : min((uint32_t)(sK[e + 1] >> mb), nmaj);
@@ -1082,11 +1130,13 @@ __global__ void __launch_bounds__(kMkThreads, 4) k_merge_kept(Pol pol, MkArgs a)
 // The stored weights (row order) merged with the regrown positions: writes
 // the output pattern, values (+0 for the regrown), sources (-1 for the
 // regrown), 16-bit columns, and -- for the column-view update -- the output
-// index of every old weight (~0u when pruned) and of every regrown position
-// (by acceptance rank).  K: 32-bit keys when row and column bits fit 31.
+// index of every old weight (~0u when pruned), of every regrown position (by
+// acceptance rank), and the pruned weights per column.  K: 32-bit keys when
+// row and column bits fit 31.
 template <typename TV, typename K>
 struct RowPol {
   using Key = K;
+  static constexpr bool kByColumn = false;
   const int32_t *row, *col;
   const TV *val;
   const SelState *st;
@@ -1099,6 +1149,7 @@ struct RowPol {
   uint16_t *col16;   // or null
   uint32_t *newidx;  // or null
   uint32_t *gq;      // or null
+  uint32_t *pcnt;    // or null: pruned weights per column, added to
   struct Shared {
     uint32_t unused;
   };
@@ -1106,8 +1157,8 @@ struct RowPol {
     TV v;
   };
   __device__ uint32_t ties_dropped() const { return st->remaining; }
-  __device__ void load(int64_t base, int len, bool, uint32_t, uint32_t, Item (&it)[kMkItems], uint32_t (&fl)[kMkItems],
-                       const PadKeys<K> &sK, Shared &) const {
+  __device__ uint32_t load(int64_t base, int len, bool, const MkBound &, uint32_t, Item (&it)[kMkItems],
+                           uint32_t (&fl)[kMkItems], const PadKeys<K> &sK, Shared &) const {
     const uint32_t t = st->prefix;
     uint32_t r[kMkItems], c[kMkItems];
 #pragma unroll
@@ -1129,6 +1180,7 @@ struct RowPol {
         fl[i] = (mk > t ? 1u : 0u) | (mk == t ? 0x10000u : 0u);
       }
     }
+    return 0u;
   }
   __device__ bool keys_blocked(int64_t, int, bool, uint32_t, uint32_t, const PadKeys<K> &, Shared &) const {
     return false;
@@ -1146,8 +1198,9 @@ struct RowPol {
     if (col16) col16[pos] = (uint16_t)c;
     if (newidx) newidx[k] = pos;
   }
-  __device__ void write_dropped(const Item &, int64_t k) const {
+  __device__ void write_dropped(const Item &, int64_t k, K key) const {
     if (newidx) newidx[k] = ~0u;
+    if (pcnt) atomicAdd(&pcnt[(uint32_t)(key & (((K)1 << cbits) - 1))], 1u);
   }
   __device__ void write_list(int64_t j, K key, uint32_t pos) const {
     const uint32_t c = (uint32_t)(key & (((K)1 << cbits) - 1));
@@ -1166,6 +1219,7 @@ struct RowPol {
 // storage index, regrown ones theirs.
 struct ColPol {
   using Key = uint32_t;
+  static constexpr bool kByColumn = true;
   const int32_t *cp;       // [in_f + 1] current column offsets
   const int32_t *row_t;    // current rows in column order
   const uint16_t *rowt16;  // or null
@@ -1174,8 +1228,8 @@ struct ColPol {
   int rbits;
   int32_t in_f;
   const uint32_t *gc_key, *gc_q, *gq;
-  int32_t *row_t_new, *src_t_new;
-  uint16_t *rowt16_new;  // or null
+  int32_t *row_t_new, *src_t_new;  // (the 32-bit rows only without the 16-bit copy)
+  uint16_t *rowt16_new;             // or null
   static constexpr int kCpCap = 1024;  // column offsets of a tile staged in shared memory
   struct Shared {
     int32_t cp[kCpCap];
@@ -1185,9 +1239,14 @@ struct ColPol {
   };
   __device__ uint32_t ties_dropped() const { return 0u; }
   // rows into sK (the columns follow, blocked), the tile's column offsets
-  // cp[c0 .. c1 + 1] into shared memory, each entry's weight's new index
-  __device__ void load(int64_t base, int len, bool last, uint32_t c0, uint32_t c_next, Item (&it)[kMkItems],
-                       uint32_t (&fl)[kMkItems], const PadKeys<uint32_t> &sK, Shared &ps) const {
+  // cp[c0 .. c1 + 1] into shared memory, each entry's weight's new index;
+  // returns this thread's count of the pruned entries of column c0 ahead of
+  // the tile (from the column's first entry up to base), whose loads travel
+  // with the tile's
+  __device__ uint32_t load(int64_t base, int len, bool last, const MkBound &bd, uint32_t c_next,
+                           Item (&it)[kMkItems], uint32_t (&fl)[kMkItems], const PadKeys<uint32_t> &sK,
+                           Shared &ps) const {
+    const uint32_t c0 = bd.aux;
     const int64_t ncp = (int64_t)(last ? (uint32_t)in_f - 1 : c_next) - c0 + 2;
     if (ncp <= kCpCap)
       for (int i = threadIdx.x; i < ncp; i += kMkThreads) ps.cp[i] = cp[c0 + i];
@@ -1200,6 +1259,8 @@ struct ColPol {
         sK[e] = rowt16 ? (uint32_t)ld_stream(rowt16 + base + e) : (uint32_t)ld_stream(row_t + base + e);
       }
     }
+    const int64_t ja = (int64_t)bd.aux2 + threadIdx.x;
+    const uint32_t qa = ja < base ? (uint32_t)src_t[ja] : ~0u;
 #pragma unroll
     for (int i = 0; i < kMkItems; ++i) {
       const int e = i * kMkThreads + threadIdx.x;
@@ -1209,6 +1270,10 @@ struct ColPol {
         fl[i] = it[i].nk != ~0u ? 1u : 0u;
       }
     }
+    uint32_t ahead = qa != ~0u && newidx[qa] == ~0u ? 1u : 0u;
+    for (int64_t j = ja + kMkThreads; j < base; j += kMkThreads)  // columns longer than a block
+      ahead += newidx[src_t[j]] == ~0u ? 1u : 0u;
+    return ahead;
   }
   // columns, blocked (thread t: entries 8t .. 8t+7): one search, then forward
   // steps; the block synchronises after it
@@ -1254,16 +1319,20 @@ struct ColPol {
   __device__ uint64_t list_key(int64_t j) const { return gc_key[j]; }
   __device__ void write_kept(const Item &x, int64_t, uint32_t pos, uint32_t key) const {
     const uint32_t r = key & ((1u << rbits) - 1u);
-    row_t_new[pos] = (int32_t)r;
     src_t_new[pos] = (int32_t)x.nk;
-    if (rowt16_new) rowt16_new[pos] = (uint16_t)r;
+    if (rowt16_new)
+      rowt16_new[pos] = (uint16_t)r;
+    else
+      row_t_new[pos] = (int32_t)r;
   }
-  __device__ void write_dropped(const Item &, int64_t) const {}
+  __device__ void write_dropped(const Item &, int64_t, uint32_t) const {}
   __device__ void write_list(int64_t j, uint32_t key, uint32_t pos) const {
     const uint32_t r = key & ((1u << rbits) - 1u);
-    row_t_new[pos] = (int32_t)r;
     src_t_new[pos] = (int32_t)gq[gc_q[j]];
-    if (rowt16_new) rowt16_new[pos] = (uint16_t)r;
+    if (rowt16_new)
+      rowt16_new[pos] = (uint16_t)r;
+    else
+      row_t_new[pos] = (int32_t)r;
   }
 };
 
@@ -1287,11 +1356,15 @@ cudaError_t launch_merge_mode(const Pol &pol, const MkArgs &a, cudaStream_t s) {
   return e;
 }
 
+// The column view is merged by column counts; the row order by tile counts.
 template <class Pol>
 cudaError_t launch_merge(const Pol &pol, const MkArgs &a, int mode, cudaStream_t s) {
-  if (mode == kMkDirect) return launch_merge_mode<Pol, kMkDirect>(pol, a, s);
-  if (mode == kMkLookBack) return launch_merge_mode<Pol, kMkLookBack>(pol, a, s);
-  return launch_merge_mode<Pol, kMkGiven>(pol, a, s);
+  if constexpr (Pol::kByColumn) {
+    return launch_merge_mode<Pol, kMkByColumn>(pol, a, s);
+  } else {
+    if (mode == kMkDirect) return launch_merge_mode<Pol, kMkDirect>(pol, a, s);
+    return launch_merge_mode<Pol, kMkGiven>(pol, a, s);
+  }
 }
 
 unsigned grid_for(int64_t n, int threads, int64_t cap = 65535 * 8) {
@@ -1495,7 +1568,6 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   const int64_t n_tiles = ceil_div(nnz, kMkTile);
   const uint32_t *row_guard = n_prune > 0 ? &ds->lists_ok : nullptr;
   const uint32_t *col_guard = n_prune > 0 ? &ds->col_ok : nullptr;
-  uint32_t *lb_err = pl.flags + kPlanFlagLookBack;
   // 3: the merge (after s waits for the row-order list) and the plan's row half
   bool row_direct = true;  // set with the keep counts below, before the first call
   auto queue_rows = [&]() -> cudaError_t {
@@ -1505,23 +1577,24 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     auto run = [&](auto rpol) -> cudaError_t {
       using P = decltype(rpol);
       launch_pdl(k_bounds<P>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s, rpol, n_prune, n_tiles,
-                 const_cast<MkBound *>(rbnd), (uint64_t *)nullptr, (uint32_t *)nullptr);
+                 const_cast<MkBound *>(rbnd), (const uint32_t *)nullptr, (uint32_t *)nullptr, (int64_t)0);
       cudaError_t r = cudaGetLastError();
       return r != cudaSuccess ? r
                               : launch_merge(rpol,
                                              MkArgs{nnz, n_prune, nnz, rbnd, sums, row_guard, cbits, a.out_f, pl.rp,
-                                                    nullptr, nullptr, nullptr},
+                                                    nullptr},
                                              row_direct ? kMkDirect : kMkGiven, s);
     };
     (void)nix;
     TV *vo = reinterpret_cast<TV *>(a.val_out);
     uint32_t *ni = update ? pl.newidx : nullptr, *gq = update ? pl.gq : nullptr;
+    uint32_t *pc = update && n_prune > 0 ? pl.cv_pcnt : nullptr;
     if (kbits <= 31)
       err = run(RowPol<TV, uint32_t>{a.row, a.col, val, st, cbits, B, Bq, a.row_out, a.col_out, vo, a.src_out,
-                                     pl.col16, ni, gq});
+                                     pl.col16, ni, gq, pc});
     else
       err = run(RowPol<TV, uint64_t>{a.row, a.col, val, st, cbits, B, Bq, a.row_out, a.col_out, vo, a.src_out,
-                                     pl.col16, ni, gq});
+                                     pl.col16, ni, gq, pc});
     if (err != cudaSuccess) return err;
     return build_plan(a.out_f, a.in_f, nnz, a.row_out, a.col_out, pl, a.gf, a.gt, b + W.plan, s, kPlanRowsReady,
                       !update);
@@ -1533,16 +1606,17 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     const ColPol cpol{pl.cp, pl.row_t, pl.rowt16, pl.src_t, pl.newidx, rbits, a.in_f, pl.gc_key, pl.gc_q, pl.gq,
                       pl.row_t_alt, pl.src_t_alt, pl.rowt16_alt};
     MkBound *cbnd = reinterpret_cast<MkBound *>(pl.cv_bnd);
-    uint64_t *status = pl.cv_sums;  // one word per tile, then the ticket
-    uint32_t *ticket = reinterpret_cast<uint32_t *>(pl.cv_sums + n_tiles);
-    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256), 256, 0, s2, cpol, n_prune, n_tiles, cbnd, status,
-               ticket);
+    // with pruned weights, one more block of the bounds launch turns their
+    // counts per column into exclusive prefixes
+    const bool pruned = n_prune > 0;
+    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256) + (pruned ? 1u : 0u), 256, 0, s2, cpol, n_prune,
+               n_tiles, cbnd, pruned ? (const uint32_t *)pl.cv_pcnt : nullptr, pl.cv_ppre, (int64_t)a.in_f);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     err = launch_merge(cpol,
-                       MkArgs{nnz, n_prune, nnz, cbnd, nullptr, col_guard, rbits, a.in_f, pl.cp_alt, status, ticket,
-                              pl.flags + kPlanFlagLookBack},
-                       kMkLookBack, s2);
+                       MkArgs{nnz, n_prune, nnz, cbnd, nullptr, col_guard, rbits, a.in_f, pl.cp_alt,
+                              pruned ? (const uint32_t *)pl.cv_ppre : nullptr},
+                       kMkByColumn, s2);
     if (err != cudaSuccess) return err;
     return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s2);
   };
@@ -1559,28 +1633,29 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     uint64_t *alb = reinterpret_cast<uint64_t *>(b + W.alb);
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, tab, bcnt,
                (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0), alb, n_at1,
-               reinterpret_cast<uint32_t *>(alb + n_at1));
+               reinterpret_cast<uint32_t *>(alb + n_at1), update ? pl.cv_pcnt : (uint32_t *)nullptr,
+               (int64_t)(update ? a.in_f : 0));
     m = chunk_size();
     e = draw_chunk(m, true);
     if (e == cudaSuccess) {
       const bool k32 = kbits <= 32;
       if (buckets) {
         launch_pdl(k_bkt_rank, (br.nb + 7) / 8, 256, 0, s2, br, RankDst{B, nullptr, Bq}, n_prune, ds,
-                   update ? (uint32_t *)nullptr : a.counts_dev, k32, lb_err);
+                   update ? (uint32_t *)nullptr : a.counts_dev, k32);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = mark();
         if (e == cudaSuccess && update) {
           launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds,
                      n_prune, bc, 1, cbits, rbits, &ds->col_overflow);
           launch_pdl(k_bkt_rank, (bc.nb + 7) / 8, 256, 0, s2, bc, RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds,
-                     a.counts_dev, true, lb_err);
+                     a.counts_dev, true);
           e = cudaGetLastError();
         }
       } else {
         e = sort_rows_general();
         if (e == cudaSuccess) e = sort_cols_general();
         if (e == cudaSuccess) {
-          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1, lb_err);
+          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1);
           e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = mark();
@@ -1634,8 +1709,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       join();
       return SNACK_ERR_WORKSPACE;
     }
-    if (a.host_counts[4]) {  // a wait for a predecessor tile gave up (this call's acceptance, or the
-      join();                 // previous column-view update): nothing trustworthy was written
+    if (a.host_counts[4]) {  // the acceptance scan gave up waiting for a predecessor tile: the
+      join();                 // lists were not made, so the queued passes wrote nothing
       return SNACK_ERR_TIMEOUT;
     }
     acc = a.host_counts[0] < (uint32_t)n_prune ? (int64_t)a.host_counts[0] : n_prune;
@@ -1655,7 +1730,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
           verdict = SNACK_ERR_CUDA;
           break;
         }
-        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0, (uint32_t *)nullptr);
+        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0);
         if (cudaGetLastError() != cudaSuccess || cudaEventRecord(a.counts_ready, s2) != cudaSuccess ||
             cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
           verdict = SNACK_ERR_CUDA;
