@@ -1019,12 +1019,12 @@ def _configs_markdown(records, clocks, peak, peak_kind, cores) -> str:
 
 def restructure_launches() -> int:
     """Kernel launches of one restructure of the workload (one draw chunk; the column view updated)."""
-    regrow = 1 + 1 + 1 + 1  # init, draws, acceptance (its scan and the row-order placement), rank
-    col_list = 1 + 1  # column-order placement and rank (second stream, beside the merge)
+    # init, draws, acceptance (its scan and the placement in both orders' buckets), rank (both lists)
+    regrow = 1 + 1 + 1 + 1
     select = 1 + 1 + 1 + 2 + 1  # init, first digit, bucket listing, two digits over the list, tile keep counts
     merge = 1 + 1 + 1  # tile bounds, merge (also the row offsets), forward tiles
     colview = 1 + 1 + 1  # tile bounds, column-view merge, column tiles (second stream, after the call)
-    return regrow + col_list + select + merge + colview
+    return regrow + select + merge + colview
 
 
 # ----------------------------------------------------------------------------

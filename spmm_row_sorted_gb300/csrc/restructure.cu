@@ -589,28 +589,15 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
   for (int64_t i = i0; i < n_pc; i += stride) pcnt[i] = 0u;
 }
 
-// The first chunk's regrown positions into one order's buckets (row order:
-// the key itself; column order: col << rbits | row), one thread per
-// position, so all atomics are in flight at once.
-__global__ void k_place(const uint64_t *__restrict__ grown, const DrawState *ds, int64_t n_prune, BucketSet bs,
-                        int col_order, int cbits, int rbits, uint32_t *bovf) {
-  pdl_wait();
-  const int64_t n = min((int64_t)ds->total, n_prune);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
-    const uint64_t p = grown[q];
-    bs.place(col_order ? col_major(p, cbits, rbits) : p, (uint32_t)q, bovf);
-  }
-}
-
 // Acceptance of a draw chunk, its scan over draw order and (first chunk) the
-// row-order bucket placement of the regrown positions, in one pass: tiles of
-// kScanTile draws taken in ticket order.  A block flags its tile's draws (an
-// empty position, and that position's first draw), scans the flags, learns
-// the accepted draws before its tile by look-back, and writes the first
-// n_prune accepted positions in draw order: grown[q] for acceptance rank q,
-// and (key, q) into the position's bucket.  The last tile's block writes the
-// chunk's accepted count.
+// bucket placement of the regrown positions, in one pass: tiles of kScanTile
+// draws taken in ticket order.  A block flags its tile's draws (an empty
+// position, and that position's first draw), scans the flags, learns the
+// accepted draws before its tile by look-back, and writes the first n_prune
+// accepted positions in draw order: grown[q] for acceptance rank q, and
+// (key, q) into the position's row-order bucket and, for the column-view
+// update, (col << rbits | row, q) into its column-order bucket.  The last
+// tile's block writes the chunk's accepted count.
 struct AcceptArgs {
   const uint64_t *cand;
   int64_t m;
@@ -620,6 +607,9 @@ struct AcceptArgs {
   int64_t before, n_prune;
   BucketSet br;  // br.nb == 0: no placement (chunks after the first)
   uint32_t *bovf;
+  BucketSet bc;  // bc.nb == 0: no column-order placement
+  uint32_t *covf;
+  int cbits, rbits;
   uint64_t *status;  // [tiles], zero before the launch
   uint32_t *ticket;  // zero before the launch
   uint32_t *err;
@@ -688,11 +678,15 @@ __global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
     if (put[i]) a.grown[q[i]] = p[i];
   }
   if (a.br.nb) {  // bucket slots: every atomic in flight before the stores that use them
-    uint32_t bk[kScanItems], slot[kScanItems];
+    const bool col = a.bc.nb != 0;
+    uint32_t bk[kScanItems], slot[kScanItems], ck[kScanItems], bkc[kScanItems], slotc[kScanItems];
 #pragma unroll
     for (int i = 0; i < kScanItems; ++i) {
       bk[i] = put[i] ? (uint32_t)__umul64hi(p[i], a.br.mult) : 0u;
       slot[i] = put[i] ? atomicAdd(&a.br.cnt[(size_t)bk[i] * kCntStride], 1u) : 0u;
+      ck[i] = put[i] && col ? (uint32_t)col_major(p[i], a.cbits, a.rbits) : 0u;
+      bkc[i] = put[i] && col ? (uint32_t)__umul64hi((uint64_t)ck[i], a.bc.mult) : 0u;
+      slotc[i] = put[i] && col ? atomicAdd(&a.bc.cnt[(size_t)bkc[i] * kCntStride], 1u) : 0u;
     }
 #pragma unroll
     for (int i = 0; i < kScanItems; ++i) {
@@ -702,6 +696,13 @@ __global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
         a.br.q[(size_t)bk[i] * kBktCap + slot[i]] = (uint32_t)q[i];
       } else {
         atomicOr(a.bovf, 1u);
+      }
+      if (!col) continue;
+      if (slotc[i] < (uint32_t)kBktCap) {
+        a.bc.key[(size_t)bkc[i] * kBktCap + slotc[i]] = ck[i];
+        a.bc.q[(size_t)bkc[i] * kBktCap + slotc[i]] = (uint32_t)q[i];
+      } else {
+        atomicOr(a.covf, 1u);
       }
     }
   }
@@ -713,19 +714,24 @@ struct RankDst {
   uint32_t *q;      // acceptance ranks
 };
 
-// A sorted list from the first chunk's buckets, one warp per bucket: the
+// The sorted lists from the first chunk's buckets, one warp per bucket: the
 // bucket's first slot is the number of keys in the buckets before it (its
 // block adds up those counts), and each key lands at its rank among the
-// bucket's keys (all distinct).  Block 0 first sets the lists' verdict (and,
-// with host_words, publishes the chunk's counters).
-__global__ void __launch_bounds__(256) k_bkt_rank(BucketSet S, RankDst D, int64_t n_prune, DrawState *ds,
-                                                  uint32_t *host_words, bool k32) {
+// bucket's keys (all distinct).  Blocks [0, nr) rank the row-order buckets
+// R, the others the column-order buckets C.  Block 0 first sets the lists'
+// verdict (and, with host_words, publishes the chunk's counters).
+__global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool k32r, uint32_t nr, BucketSet C,
+                                                  RankDst DC, int64_t n_prune, DrawState *ds, uint32_t *host_words) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true);
-  const uint32_t b0 = blockIdx.x * 8;
+  const bool rows = blockIdx.x < nr;
+  const BucketSet S = rows ? R : C;
+  const RankDst D = rows ? DR : DC;
+  const bool k32 = rows ? k32r : true;
+  const uint32_t b0 = (rows ? blockIdx.x : blockIdx.x - nr) * 8;
   uint32_t part = 0;
   for (uint32_t i0 = threadIdx.x; i0 < b0; i0 += 256 * 8) {  // eight loads in flight per round
     uint32_t c[8];
@@ -1388,6 +1394,17 @@ double expected_draws(double n_pos, double empty, double need) {
   return n_pos * log((empty + 0.5) / (empty - need + 0.5));
 }
 
+// Standard deviation of that number: the draws for the k-th new position are
+// geometric with success probability q = u / n_pos (u = empty - k positions
+// left), variance (1 - q) / q^2 = n_pos (n_pos - u) / u^2; summed over u from
+// empty - need + 1 to empty with the same half-step sums as above.
+double draws_sd(double n_pos, double empty, double need) {
+  if (need <= 0) return 0.0;
+  const double lo = empty - need + 0.5, hi = empty + 0.5;
+  const double var = n_pos * n_pos * (1.0 / lo - 1.0 / hi) - n_pos * log(hi / lo);
+  return var > 0.0 ? sqrt(var) : 0.0;
+}
+
 struct RWs {
   size_t state, dstate, sums, above, scand, scan2, grown_a, B, Bq, cand, alb, hkeys, hmin, bcnt, bnd, bkey, bq,
       rk0, rv0, rk1, rv1, rtemp, plan, total;
@@ -1542,13 +1559,34 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       cudaError_t err = cudaMemsetAsync(alb, 0, sizeof(uint64_t) * (size_t)n_at + sizeof(uint32_t), s2);
       if (err != cudaSuccess) return err;
     }
-    const AcceptArgs aa{cand, m, (uint64_t)done, tab, grown_a, acc, n_prune, first && buckets ? br : BucketSet{},
-                        &ds->bucket_overflow, alb, aticket, &ds->lb_fail, &ds->total};
+    const AcceptArgs aa{cand,
+                        m,
+                        (uint64_t)done,
+                        tab,
+                        grown_a,
+                        acc,
+                        n_prune,
+                        first && buckets ? br : BucketSet{},
+                        &ds->bucket_overflow,
+                        first && buckets && update ? bc : BucketSet{},
+                        &ds->col_overflow,
+                        cbits,
+                        rbits,
+                        alb,
+                        aticket,
+                        &ds->lb_fail,
+                        &ds->total};
     launch_pdl(k_accept_scan, (unsigned)n_at, kScanThreads, 0, s2, aa);
     return cudaGetLastError();
   };
   auto chunk_size = [&]() -> int64_t {
-    double want = 1.1 * expected_draws((double)n_pos, empty - (double)acc, (double)(n_prune - acc)) + 1024.0;
+    // the expected draws and eight standard deviations (then the chunk falls
+    // short with a probability far below 1e-9), or 1.1 x the expected draws
+    // where that is less (crowded layers: more chunks are cheaper than many
+    // wasted draws)
+    const double e_left = empty - (double)acc, need = (double)(n_prune - acc);
+    const double ex = expected_draws((double)n_pos, e_left, need);
+    const double want = fmin(ex + 8.0 * draws_sd((double)n_pos, e_left, need), 1.1 * ex) + 1024.0;
     int64_t m = (int64_t)ceil(want);
     return m > W.d_max - done ? W.d_max - done : m;
   };
@@ -1639,18 +1677,12 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     e = draw_chunk(m, true);
     if (e == cudaSuccess) {
       const bool k32 = kbits <= 32;
-      if (buckets) {
-        launch_pdl(k_bkt_rank, (br.nb + 7) / 8, 256, 0, s2, br, RankDst{B, nullptr, Bq}, n_prune, ds,
-                   update ? (uint32_t *)nullptr : a.counts_dev, k32);
+      if (buckets) {  // both orders' lists in one launch
+        const uint32_t nr = (br.nb + 7) / 8, nc = update ? (bc.nb + 7) / 8 : 0u;
+        launch_pdl(k_bkt_rank, nr + nc, 256, 0, s2, br, RankDst{B, nullptr, Bq}, k32, nr, bc,
+                   RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = mark();
-        if (e == cudaSuccess && update) {
-          launch_pdl(k_place, grid_for(n_prune, 256), 256, 0, s2, (const uint64_t *)grown_a, (const DrawState *)ds,
-                     n_prune, bc, 1, cbits, rbits, &ds->col_overflow);
-          launch_pdl(k_bkt_rank, (bc.nb + 7) / 8, 256, 0, s2, bc, RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds,
-                     a.counts_dev, true);
-          e = cudaGetLastError();
-        }
       } else {
         e = sort_rows_general();
         if (e == cudaSuccess) e = sort_cols_general();

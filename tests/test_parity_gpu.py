@@ -373,9 +373,13 @@ def test_restructure_bucket_overflow_general_sort():
 
 
 def first_chunk_draws(n_pos: int, nnz: int, n_prune: int) -> int:
-    # the library's first draw chunk: 1.1 x the expected draws + 1024
+    # the library's first draw chunk: the expected draws plus the lesser of
+    # eight standard deviations and a tenth of them, plus 1024
     empty = n_pos - nnz
-    return int(np.ceil(1.1 * n_pos * np.log((empty + 0.5) / (empty - n_prune + 0.5)) + 1024.0))
+    lo, hi = empty - n_prune + 0.5, empty + 0.5
+    ex = n_pos * np.log(hi / lo)
+    sd = np.sqrt(max(n_pos * n_pos * (1.0 / lo - 1.0 / hi) - n_pos * np.log(hi / lo), 0.0))
+    return int(np.ceil(min(ex + 8.0 * sd, 1.1 * ex) + 1024.0))
 
 
 def test_restructure_extra_draw_chunks():
@@ -916,6 +920,46 @@ def test_restructure_rows_full_row_is_no_space_like_the_oracle():
     got["dw"], got["db"] = L.grad_weight(x, dy)
     torch.cuda.synchronize()
     check_layer_ops(lay, acts, got=got)
+    # and the next unstructured restructure draws against the input pattern
+    # (the occupancy bits the finished rows had changed are restored)
+    src = L.restructure(900, seed=7, step=4)
+    torch.cuda.synchronize()
+    ro, co, so, _ = oracle.restructure(400, 600, lay.row, lay.col, oracle.as_f64(lay.val), 900, 7, 4)
+    assert np.array_equal(L.row.cpu().numpy(), ro) and np.array_equal(L.col.cpu().numpy(), co)
+    assert np.array_equal(src.cpu().numpy(), so.astype(np.int32))
+    L.close()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_restructure_mixed_chain(dtype):
+    # Per-row and unstructured restructures alternate on one handle (the
+    # unstructured ones pruning a tenth, updated in place, and a third,
+    # rebuilt): each draws against the pattern the one before left, as the
+    # oracle chain does, and every op of the last pattern matches the oracle.
+    out_f, in_f = 600, 800
+    lay = wl.make_layer(out_f, in_f, fan_in=40, val_std=0.5, val_dtype=dtype, seed=5, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=16)
+    r, c, v = lay.row, lay.col, lay.val
+    for step, (kind, n) in enumerate((("rows", 4), ("all", 2400), ("rows", 6), ("all", 8000), ("all", 2400))):
+        if kind == "rows":
+            src = L.restructure_rows(n, 3, step)
+            r, c, so, _ = oracle.restructure_rows(out_f, in_f, r, c, oracle.as_f64(v, dtype), n, 3, step)
+        else:
+            src = L.restructure(n, seed=3, step=step)
+            r, c, so, _ = oracle.restructure(out_f, in_f, r, c, oracle.as_f64(v, dtype), n, 3, step)
+        torch.cuda.synchronize()
+        v = oracle.restructure_values(v, so)
+        assert np.array_equal(L.row.cpu().numpy(), r) and np.array_equal(L.col.cpu().numpy(), c), step
+        assert np.array_equal(src.cpu().numpy(), so.astype(np.int32)), step
+    new = wl.Layer(out_f, in_f, r, c, v, lay.bias, dtype)
+    for batch in (4, 16):
+        acts = wl.make_acts(batch, in_f, out_f, dtype, seed=batch)
+        x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
+        got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+        got["dw"], got["db"] = L.grad_weight(x, dy)
+        torch.cuda.synchronize()
+        check_layer_ops(new, acts, got=got)
     L.close()
 
 
