@@ -79,8 +79,9 @@ def kernel_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(op: str):
-    """DRAM bytes per launch of `op` from the committed ncu summary, if the kernels are unchanged since."""
+def profiled_traffic(op: str, kernel: str = None):
+    """DRAM bytes per call of `op` (or, with `kernel`, of that kernel of the op per call) from the
+    committed ncu summary, if the kernels are unchanged since."""
     path = os.path.join(ROOT, "profiles", "traffic_c4.md")
     if not os.path.exists(path):
         return None
@@ -92,9 +93,21 @@ def profiled_traffic(op: str):
                     d = json.loads(line[len("traffic:"):])
                 except ValueError:
                     return None
-                if d.get("kernel_digest") == want and op in d.get("bytes_per_call", {}):
-                    return int(d["bytes_per_call"][op])
+                if d.get("kernel_digest") != want:
+                    return None
+                table, key = (d.get("kernel_bytes", {}), f"{op}:{kernel}") if kernel else (d.get("bytes_per_call", {}), op)
+                return int(table[key]) if key in table else None
     return None
+
+
+def kernel_ident(name: str) -> str:
+    """The kernel's identifier (k_...) from the name the CUDA runtime gives (mangled or not)."""
+    import re
+    m = re.search(r"(k_[A-Za-z0-9_]*?)(?:I|E|$|<|\()", name)
+    if m:
+        return m.group(1)
+    m = re.search(r"(k_[A-Za-z0-9_]+)", name)
+    return m.group(1) if m else name
 
 
 class ClockSampler:
@@ -504,17 +517,32 @@ def run_ours(args):
                          "gflops": (flops / (op_ms[op] / 1e3) / 1e9) if flops else None,
                          "us_in_timed_loop": overlapped_ms[op] * 1e3}
     op_report["restructure"]["us_until_return"] = restructure_on_stream_ms * 1e3
-    dominant = max(ops, key=lambda o: op_ms[o])
     launches = {"fwd": 3, "bwd": 3, "restructure": restructure_launches()}
-    roofline = {"bound": "hbm", "achieved": op_report[dominant]["gbs"], "peak": peak, "unit": "GB/s",
-                "frac": op_report[dominant]["gbs"] / peak, "traffic": profiled_traffic(dominant),
-                "kernel": f"op {dominant} ({launches[dominant]} launches; the op with the largest time share)",
-                "peak_kind": peak_kind,
-                # the largest single kernel of the step is the fused backward's tile kernel; its op time
-                # (both transposes, the tiles, the fix-up) bounds the kernel's time from above
-                "largest_kernel": {"name": "k_spmm_tiles<float, float, 4, 8, 1, 1> (fused backward, dX + dW)",
-                                   "achieved_op": op_report["bwd"]["gbs"], "frac_op": op_report["bwd"]["frac"],
-                                   "alg_bytes": byts["bwd"]}}
+    kern = kernel_times(snack, step, copies, stream, min(args.steps, 50), launches)
+    # the dominant kernel: the longest per step among those whose work has a
+    # scope-table byte count -- the forward's and the fused backward's tile
+    # kernels (their ops' other launches only transpose the activations and
+    # add split rows' partial sums) and the restructure's merge (it reads the
+    # old COO and writes the new one)
+    owns = {("fwd", "k_spmm_tiles"): "fwd", ("bwd", "k_spmm_tiles"): "bwd", ("restructure", "k_merge_kept:0"): "restructure"}
+    cands = [(k, v) for k, v in kern.items() if (k[0], k[1]) in owns]
+    (dop, dname), dk = max(cands, key=lambda kv: kv[1]["us_per_step"])
+    d_op = owns[(dop, dname)]
+    d_gbs = byts[d_op] / (dk["us_per_launch"] / 1e6) / 1e9
+    longest = max(kern.items(), key=lambda kv: kv[1]["us_per_step"])
+    dominant_op = max(ops, key=lambda o: op_ms[o])
+    roofline = {"bound": "hbm", "achieved": d_gbs, "peak": peak, "unit": "GB/s", "frac": d_gbs / peak,
+                "traffic": profiled_traffic(dop, dname),
+                "kernel": f"{dk['name']} ({d_op}; {dk['launches_per_step']} launch per step, "
+                          f"{dk['us_per_launch']:.1f} us per launch in the traced pass)",
+                "alg_bytes_per_launch": byts[d_op], "us_per_launch": dk["us_per_launch"], "peak_kind": peak_kind,
+                "longest_kernel": {"name": longest[1]["name"], "op": longest[0][0],
+                                   "us_per_step": longest[1]["us_per_step"]},
+                "op": {"name": f"{dominant_op} ({launches[dominant_op]} launches; the op with the largest time share)",
+                       "achieved": op_report[dominant_op]["gbs"], "frac": op_report[dominant_op]["frac"],
+                       "traffic": profiled_traffic(dominant_op)},
+                "kernels_us_per_step": {f"{k[0]}:{k[1]}": round(v["us_per_step"], 2) for k, v in
+                                        sorted(kern.items(), key=lambda kv: -kv[1]["us_per_step"])}}
 
     # end to end through the C ABI from pinned host buffers: every step's inputs
     # go host -> device and its results device -> host inside the timed region,
@@ -593,6 +621,45 @@ def run_ours(args):
     return 0
 
 
+def kernel_times(snack, step, copies, stream, n_steps: int, launches: dict) -> dict:
+    """Per-kernel device times from the library's kernel trace over n_steps steps (after the timed
+    region): every launch bracketed by two events, so each kernel runs alone and its time includes
+    its launch.  Keyed by (op, identifier), the restructure's two merges told apart as :0 and :1 in
+    launch order; values: name, launches and us per step, us per launch."""
+    per_step = sum(launches.values())
+    snack.snack_trace_start(per_step * n_steps + 64)
+    for i in range(n_steps):
+        for c2 in copies:
+            snack.snack_wait_plan(c2["h"], stream)
+        step(copies[i % len(copies)], 3 * 10**6 + i)
+    for cp in copies:
+        snack.snack_wait_plan(cp["h"], stream)
+    stream.synchronize()
+    recs = snack.snack_trace_read(per_step * n_steps + 64)
+    snack.snack_trace_stop()
+    recs = recs[-per_step * n_steps:]
+    bounds = [("fwd", launches["fwd"]), ("bwd", launches["bwd"]), ("restructure", launches["restructure"])]
+    out = {}
+    for s0 in range(0, len(recs), per_step):
+        block, pos = recs[s0:s0 + per_step], 0
+        for op, cnt in bounds:
+            seen = {}
+            for name, us in block[pos:pos + cnt]:
+                ident = kernel_ident(name)
+                if ident == "k_merge_kept":  # the row-order merge, then the column view's
+                    ident = f"k_merge_kept:{seen.setdefault('mk', 0)}"
+                    seen["mk"] += 1
+                d = out.setdefault((op, ident), {"name": ident.split(":")[0], "us": 0.0, "launches": 0})
+                d["us"] += us
+                d["launches"] += 1
+            pos += cnt
+    for d in out.values():
+        d["us_per_step"] = d["us"] / n_steps
+        d["launches_per_step"] = d["launches"] // n_steps
+        d["us_per_launch"] = d["us"] / d["launches"]
+    return out
+
+
 # ----------------------------------------------------------------------------
 # Per-workload sweep (--configs): every op of every workload, cold and warm,
 # beside same-run cuBLAS dense and Dense+Mask comparators and the oracle.
@@ -656,6 +723,34 @@ class _Timer:
         self.s.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
 
+    def time_restructure(self, snack, h, run, reps: int, cold: bool) -> tuple:
+        """A restructure call timed alone: each rep starts after the previous call's column-view
+        update (snack_wait_plan) and, cold, a read of 2x L2; the device sleeps briefly so the host
+        queues the call's first launches before they run.  Medians of the time until the call
+        returns and until its column-view update is done, in us."""
+        torch = self.torch
+        ret, done = [], []
+        with torch.cuda.stream(self.s):
+            for _ in range(3):
+                run()
+            for _ in range(reps):
+                snack.snack_wait_plan(h, self.s)
+                if cold:
+                    torch.sum(self.flush, dim=0, out=self.flush_out)
+                torch.cuda._sleep(int(1e5))
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(self.s)
+                run()
+                e1.record(self.s)
+                snack.snack_wait_plan(h, self.s)
+                e2.record(self.s)
+                ret.append((e0, e1))
+                done.append((e0, e2))
+            snack.snack_wait_plan(h, self.s)
+        self.s.synchronize()
+        return (statistics.median(a.elapsed_time(b) for a, b in ret) * 1e3,
+                statistics.median(a.elapsed_time(b) for a, b in done) * 1e3)
+
 
 def _oracle_us(oracle, lay, x64, dy64, op: str, budget_terms: float = 3e7) -> tuple:
     """Oracle time of `op` on the layer: the whole layer when nnz*batch is small,
@@ -692,11 +787,12 @@ def _layer_rows(name, lay, batch, ours, dense, mask, oracle_t, peak, cores):
     out = []
     for op, t in ours.items():
         cold, warm, graphed = t
+        base = op[:-4] if op.endswith("_all") else op  # restructure_all: the restructure's bytes
         flops = {"fwd": 2, "dx": 2, "dw": 2, "bwd": 4}.get(op, 0) * lay.nnz * batch
-        gbs = byts[op] / (cold * 1e-6) / 1e9
+        gbs = byts[base] / (cold * 1e-6) / 1e9
         rec = {"config": name, "layer": f"{lay.out_f}x{lay.in_f}", "nnz": lay.nnz, "batch": batch, "op": op,
                "dtype": lay.val_dtype, "us_cold": cold, "us_warm": warm, "graph": graphed,
-               "alg_bytes": byts[op], "gbs": gbs, "frac_measured": gbs / peak, "frac_nominal": gbs / NOMINAL_HBM_GBS,
+               "alg_bytes": byts[base], "gbs": gbs, "frac_measured": gbs / peak, "frac_nominal": gbs / NOMINAL_HBM_GBS,
                "gflops": flops / (cold * 1e-6) / 1e9 if flops else None,
                "frac_fma": (flops / (cold * 1e-6) / 1e12 / FMA_PEAK_TFLOPS) if flops else None,
                "dense_us": dense.get(op), "dense_mask_us": mask.get(op),
@@ -761,7 +857,9 @@ def _bench_layer(torch, F, snack, timer, name, lay, batch, ops, reps, dev, oracl
             state["i"] += 1
 
         rr = max(20, reps // 4)
-        ours["restructure"] = (timer.time(restructure, rr, True), timer.time(restructure, rr, False), False)
+        cold, warm = timer.time_restructure(snack, h, restructure, rr, True), timer.time_restructure(snack, h, restructure, rr, False)
+        ours["restructure"] = (cold[0], warm[0], False)  # until the call returns
+        ours["restructure_all"] = (cold[1], warm[1], False)  # until its column-view update is done
         if state["cur"] == 1:  # back on the first buffers
             restructure()
     # comparators: dense W (cuBLAS via F.linear / matmul) and Dense+Mask (W*M materialised every call)
@@ -912,9 +1010,13 @@ def _fanin_restructure(torch, snack, timer, dev, reps):
     out = []
     byts = alg_bytes(lay.nnz, 32, 16384, 16384)["restructure"]
     for name, fn in (("restructure_rows", per_row), ("restructure", unstructured)):
-        us = timer.time(fn, reps, True)
-        out.append({"config": "c4-fanin", "layer": "16384x16384", "nnz": lay.nnz, "batch": 0, "op": name,
-                    "dtype": "f32", "us_cold": us, "us_warm": timer.time(fn, reps, False), "graph": False,
+        cold, warm = timer.time_restructure(snack, h, fn, reps, True), timer.time_restructure(snack, h, fn, reps, False)
+        for op, k in ((name, 0), (name + "_all", 1)):
+            if op == "restructure_rows_all":
+                continue  # the per-row restructure rebuilds its column view before it returns
+            us = cold[k]
+            out.append({"config": "c4-fanin", "layer": "16384x16384", "nnz": lay.nnz, "batch": 0, "op": op,
+                    "dtype": "f32", "us_cold": us, "us_warm": warm[k], "graph": False,
                     "alg_bytes": byts, "gbs": byts / (us * 1e-6) / 1e9, "frac_measured": None, "frac_nominal": None,
                     "gflops": None, "frac_fma": None, "dense_us": None, "dense_mask_us": None, "oracle_us": None,
                     "oracle_full": None, "oracle_cores": None})

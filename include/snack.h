@@ -329,6 +329,29 @@ const char *snack_status_string(snack_status st);
 /* SNACK_VERSION of the built library. */
 int snack_version(void);
 
+/*
+ * Kernel trace of the calling host thread (a profiling aid).  While a trace
+ * is open, every kernel the library launches from this thread is bracketed by
+ * two CUDA events recorded on its stream, in a ring of `capacity` records:
+ * the event between two launches keeps the second from starting before the
+ * first ends, so a traced kernel's time includes its launch.  Events belong
+ * to the device current at snack_trace_start; trace launches on that device
+ * only.
+ *   snack_trace_start: open a ring of `capacity` >= 1 records (an open trace
+ *     is closed first).  SNACK_ERR_INVALID_ARG for capacity < 1,
+ *     SNACK_ERR_CUDA when an event cannot be created.
+ *   snack_trace_read: wait for the recorded launches to finish and return the
+ *     last min(recorded, capacity, max) of them, oldest first: names[i] the
+ *     kernel's name as the CUDA runtime gives it (mangled; owned by the
+ *     runtime), us[i] the time between its two events in microseconds; *n
+ *     the count.  The trace stays open.  SNACK_ERR_INVALID_ARG without an
+ *     open trace or for bad pointers.
+ *   snack_trace_stop: close the trace and free its events (no-op if none).
+ */
+snack_status snack_trace_start(int32_t capacity);
+snack_status snack_trace_read(const char **names, float *us, int32_t max, int32_t *n);
+snack_status snack_trace_stop(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,6 +29,21 @@ typedef __nv_bfloat16 bf16;
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ------------------------------------------------------------ kernel trace
+//
+// While the calling host thread has a trace open (snack_trace_start), every
+// launch is bracketed by two CUDA events recorded on its stream, kept with
+// the kernel's entry point in the next slot of a ring of `cap` slots.  (The
+// event between two launches also keeps the second from starting early, so a
+// traced kernel's time includes its launch.)
+struct KernelTrace {
+  const void **fn;
+  cudaEvent_t *ev;  // two per slot: before, after
+  int cap;
+  long long n;  // launches recorded; slot n % cap is next
+};
+extern thread_local KernelTrace *g_kernel_trace;
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
@@ -42,7 +57,19 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+  KernelTrace *tr = g_kernel_trace;
+  int slot = 0;
+  if (tr) {
+    slot = (int)(tr->n % tr->cap);
+    tr->fn[slot] = reinterpret_cast<const void *>(kernel);
+    cudaEventRecord(tr->ev[2 * slot], s);
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+  if (tr) {
+    cudaEventRecord(tr->ev[2 * slot + 1], s);
+    ++tr->n;
+  }
+  return e;
 }
 
 // ------------------------------------------------ shared-memory limits

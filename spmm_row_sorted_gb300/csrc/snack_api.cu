@@ -30,7 +30,29 @@ cudaError_t raise_smem_limit(const void *kernel, size_t bytes) {
   return e;
 }
 
+thread_local KernelTrace *g_kernel_trace = nullptr;
+
 }  // namespace snack
+
+namespace {
+
+// The calling thread's trace: the ring's storage and events (created on the
+// device current at snack_trace_start).
+struct TraceOwner {
+  KernelTrace t{};
+  ~TraceOwner() { release(); }
+  void release() {
+    if (t.ev)
+      for (int i = 0; i < 2 * t.cap; ++i)
+        if (t.ev[i]) cudaEventDestroy(t.ev[i]);
+    delete[] t.ev;
+    delete[] t.fn;
+    t = KernelTrace{};
+  }
+};
+thread_local TraceOwner g_trace_owner;
+
+}  // namespace
 
 namespace {
 
@@ -819,5 +841,55 @@ const char *snack_status_string(snack_status st) {
 }
 
 int snack_version(void) { return SNACK_VERSION; }
+
+snack_status snack_trace_start(int32_t capacity) {
+  if (capacity < 1) return SNACK_ERR_INVALID_ARG;
+  g_kernel_trace = nullptr;
+  g_trace_owner.release();
+  KernelTrace &t = g_trace_owner.t;
+  t.fn = new (std::nothrow) const void *[capacity]();
+  t.ev = new (std::nothrow) cudaEvent_t[2 * (size_t)capacity]();
+  t.cap = capacity;
+  t.n = 0;
+  if (!t.fn || !t.ev) {
+    g_trace_owner.release();
+    return SNACK_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < 2 * capacity; ++i)
+    if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
+      g_trace_owner.release();
+      return SNACK_ERR_CUDA;
+    }
+  g_kernel_trace = &t;
+  return SNACK_OK;
+}
+
+snack_status snack_trace_read(const char **names, float *us, int32_t max, int32_t *n) {
+  if (!n || max < 0 || (max > 0 && (!names || !us))) return SNACK_ERR_INVALID_ARG;
+  *n = 0;
+  const KernelTrace &t = g_trace_owner.t;
+  if (!t.fn) return SNACK_ERR_INVALID_ARG;
+  const long long have = t.n < t.cap ? t.n : t.cap;
+  const long long k = have < max ? have : max;
+  for (long long j = 0; j < k; ++j) {  // the last k records, oldest first
+    const int slot = (int)((t.n - k + j) % t.cap);
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.ev[2 * slot + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, t.ev[2 * slot], t.ev[2 * slot + 1]) != cudaSuccess)
+      return SNACK_ERR_CUDA;
+    const char *name = nullptr;
+    if (cudaFuncGetName(&name, t.fn[slot]) != cudaSuccess || !name) name = "?";
+    names[j] = name;
+    us[j] = 1000.f * ms;
+  }
+  *n = (int32_t)k;
+  return SNACK_OK;
+}
+
+snack_status snack_trace_stop(void) {
+  g_kernel_trace = nullptr;
+  g_trace_owner.release();
+  return SNACK_OK;
+}
 
 }  // extern "C"

@@ -31,7 +31,8 @@ SNACK_F32, SNACK_BF16 = 0, 1
 EXPORTED = ("snack_query_sizes", "snack_create", "snack_spmm_fwd", "snack_spmm_fwd_noalloc", "snack_spmm_dx",
             "snack_spmm_fwd_gelu", "snack_spmm_dx_gelu", "snack_sddmm_dw", "snack_backward",
             "snack_restructure_workspace_size", "snack_restructure", "snack_restructure_rows_workspace_size",
-            "snack_restructure_rows", "snack_wait_plan", "snack_destroy", "snack_status_string", "snack_version")
+            "snack_restructure_rows", "snack_wait_plan", "snack_destroy", "snack_status_string", "snack_version",
+            "snack_trace_start", "snack_trace_read", "snack_trace_stop")
 
 
 class SnackLibraryMissing(RuntimeError):
@@ -99,6 +100,13 @@ def load(path: Optional[str] = None):
         lib.snack_status_string.restype = ctypes.c_char_p
         lib.snack_version.argtypes = []
         lib.snack_version.restype = ctypes.c_int
+        lib.snack_trace_start.argtypes = [i32]
+        lib.snack_trace_start.restype = st
+        lib.snack_trace_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i32,
+                                         ctypes.POINTER(i32)]
+        lib.snack_trace_read.restype = st
+        lib.snack_trace_stop.argtypes = []
+        lib.snack_trace_stop.restype = st
         _lib = lib
         return lib
 
@@ -237,6 +245,23 @@ def snack_destroy(h: int) -> None:
 
 def snack_status_string(status: int) -> str:
     return load().snack_status_string(status).decode()
+
+
+def snack_trace_start(capacity: int) -> None:
+    _check("snack_trace_start", load().snack_trace_start(capacity))
+
+
+def snack_trace_read(max_records: int) -> list:
+    """The last records of the calling thread's trace, oldest first: (kernel name, microseconds)."""
+    names = (ctypes.c_char_p * max(max_records, 1))()
+    us = (ctypes.c_float * max(max_records, 1))()
+    n = ctypes.c_int32(0)
+    _check("snack_trace_read", load().snack_trace_read(names, us, max_records, ctypes.byref(n)))
+    return [(names[i].decode(), float(us[i])) for i in range(n.value)]
+
+
+def snack_trace_stop() -> None:
+    _check("snack_trace_stop", load().snack_trace_stop())
 
 
 def snack_version() -> int:

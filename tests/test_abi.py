@@ -100,3 +100,14 @@ def test_null_handle_rejected_without_gpu(lib):
     assert lib.snack_create(ctypes.byref(h), 4, 4, 2, 1, 0, 0, fake, fake, fake, 16, fake, 1 << 20, 0, None) == 4
     assert lib.snack_create(ctypes.byref(h), 4, 4, 2, 1, 0, 0, fake, fake, fake, 1 << 20, fake, 16, 0, None) == 4
     assert h.value is None
+
+
+def test_trace_rejects_bad_arguments_on_the_host(lib):
+    # capacity < 1, and a read without an open trace, fail before any CUDA call
+    assert lib.snack_trace_start(0) == 1
+    assert lib.snack_trace_start(-5) == 1
+    assert lib.snack_trace_stop() == 0
+    n = ctypes.c_int32(7)
+    assert lib.snack_trace_read(None, None, 0, ctypes.byref(n)) == 1 and n.value == 0
+    assert lib.snack_trace_read(None, None, 0, None) == 1
+    assert lib.snack_trace_stop() == 0  # closing twice is fine

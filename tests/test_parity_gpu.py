@@ -981,3 +981,43 @@ def test_restructure_rows_errors():
         L.restructure_rows(1, 0, 0)
     assert e.value.status == 7
     L.close()
+
+
+# ---------------------------------------------------------------- kernel trace
+
+def _ident(name: str) -> str:
+    import re
+    m = re.search(r"(k_[A-Za-z0-9_]*?)(?:I|E|$|<|\()", name)
+    return m.group(1) if m else name
+
+
+def test_kernel_trace_records_every_launch():
+    # The trace brackets every launch of the calling thread with two events:
+    # a small-batch forward is one kernel, a tile-path forward several
+    # (transpose, tiles, ...); a ring of two keeps the last two records; the
+    # results are bit-identical with and without the trace.
+    lay = wl.make_layer(300, 400, nnz=20000, val_std=0.3, val_dtype="f32", seed=3, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(300, 400, row, col, val, bias, max_batch=32)
+    x32 = act_tensor(wl.make_acts(32, 400, 300, "f32", seed=1).x, "f32")
+    x4 = act_tensor(wl.make_acts(4, 400, 300, "f32", seed=2).x, "f32")
+    ref32, ref4 = L.forward(x32), L.forward(x4)
+    torch.cuda.synchronize()
+    snack.snack_trace_start(64)
+    try:
+        y4 = L.forward(x4)
+        y32 = L.forward(x32)
+        recs = snack.snack_trace_read(64)
+        idents = [_ident(n) for n, _ in recs]
+        assert idents[0] == "k_spmm_small" and "k_spmm_tiles" in idents[1:] and "k_transpose" in idents[1:], idents
+        assert all(us > 0.0 for _, us in recs)
+        snack.snack_trace_start(2)  # restarts with an empty ring
+        for _ in range(3):
+            L.forward(x4)
+        recs2 = snack.snack_trace_read(10)
+        assert [_ident(n) for n, _ in recs2] == ["k_spmm_small"] * 2
+    finally:
+        snack.snack_trace_stop()
+    torch.cuda.synchronize()
+    assert torch.equal(y32, ref32) and torch.equal(y4, ref4)
+    L.close()
