@@ -257,12 +257,16 @@ def test_restructure_small(dtype, case):
 @pytest.mark.parametrize("case", [(500, 700, 30000, 3000, None), (64, 64, 3000, 1000, None), (7, 3, 10, 5, None),
                                   (2000, 3000, 200000, 20000, 1.2), (70000, 20, 3000, 300, None),
                                   (40, 30, 600, 0, None), (70000, 70000, 30000, 3000, None),
-                                  (300, 400, 40000, 20000, None)])
+                                  (300, 400, 40000, 20000, None), (65536, 32768, 20000, 2000, None),
+                                  (65536, 65536, 20000, 2000, None), (300, 5000, 2000, 300, None),
+                                  (200, 300, 8000, 2000, None), (200, 300, 8000, 2001, None)])
 def test_restructure_chain_plan_equals_fresh(dtype, case):
     # The restructure rebuilds the handle's plan in place: row offsets and the
     # 16-bit columns from its merge, and the column view updated into the
-    # plan's second view (row and column bits within 32, at most a quarter of
-    # the weights pruned) or rebuilt (70000^2; half pruned).  After three
+    # plan's second view (row and column bits within 31 -- 65536 x 32768 is at
+    # the limit --, at most a quarter of the weights pruned: 2000 of 8000 is,
+    # 2001 is not; mostly empty columns in 300 x 5000) or rebuilt (70000^2 and
+    # 65536^2; half pruned).  After three
     # restructures in a row the COO still
     # matches the oracle, and every op on the handle is bit-identical to the
     # same op on a new handle made for the final pattern, at a small-batch and
