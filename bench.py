@@ -410,7 +410,10 @@ def run_ours(args):
     byts = alg_bytes(nnz, BATCH, OUT_F, IN_F)
     step_bytes = sum(byts[op] for op in STEP_OPS)
 
-    stream = torch.cuda.Stream(device=dev)
+    # the step's stream above the lowest priority: the column-view update a
+    # restructure leaves running (on a stream of the lowest priority) then
+    # fills the gaps of the next step's kernels instead of competing with them
+    stream = torch.cuda.Stream(device=dev, priority=-1)
     plan_b, ws_b = snack.snack_query_sizes(OUT_F, IN_F, nnz, BATCH, 0, 0)
     copies = []
     with torch.cuda.stream(stream):

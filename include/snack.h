@@ -24,20 +24,23 @@
  * Memory ownership.  Every device buffer -- indices, values, activations,
  * outputs, the plan and the workspaces -- is allocated and freed by the
  * caller.  The library never allocates device memory.  A handle owns host
- * metadata, and after its first restructure also a second CUDA stream, four
- * events and 16 bytes of mapped pinned host memory; snack_destroy frees them.
+ * metadata, and after its first restructure also two CUDA streams, five
+ * events and 32 bytes of mapped pinned host memory; snack_destroy frees them.
  *
  * Streams.  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream), except snack_create with validate != 0, which
  * synchronises `stream`, and snack_restructure, which waits on the host for
  * its draw count (see there).  A plan and a workspace may be used by one call
- * in flight at a time.  After snack_restructure the rebuild of the plan's
- * column view may still be running on the handle's second stream; every call
+ * in flight at a time.  After snack_restructure the update of the plan's
+ * column view may still be running on a stream of the handle; every call
  * that reads the column view (snack_spmm_dx, snack_spmm_dx_gelu,
  * snack_sddmm_dw, snack_backward and both restructures) first makes its
  * stream wait for it, so results never depend on the timing.  The forward
  * reads only the row half of the plan and does not wait.  snack_wait_plan
- * orders any stream after that rebuild.
+ * orders any stream after that update.  The update's stream has the lowest
+ * stream priority: calls queued next on a stream of higher priority (see
+ * cudaStreamCreateWithPriority) run ahead of it, and it fills the gaps they
+ * leave.
  *
  * Host threads.  Calls may come from several host threads.  The launchers
  * raise a kernel's dynamic shared-memory limit (a per-process, per-device
@@ -262,11 +265,13 @@ snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, s
  * returns, the new COO, the source map and the row half of the plan are
  * ordered on `stream`; the workspace is free for the next call at once.  For
  * layers with the deferred scratch in their plan (see snack_query_sizes) the
- * column view is rebuilt from row_out/col_out on the handle's second stream
- * after `stream`'s work, overlapping whatever the caller queues next; the
- * calls that read it wait for it (see Streams), snack_wait_plan orders a
- * stream after it, and snack_destroy waits for it.  row_out and col_out must
- * not change while it runs (they are the layer's pattern from now on).
+ * column view is updated from the plan alone (the old view, each weight's new
+ * index, the regrown positions in column order) on a third stream of the
+ * handle, of the lowest priority, after `stream`'s work, overlapping whatever
+ * the caller queues next; the calls that read it wait for it (see Streams),
+ * snack_wait_plan orders a stream after it, and snack_destroy waits for it.
+ * It reads neither the workspace nor row_out/col_out; row_out and col_out
+ * are the layer's pattern from now on.
  * Returns SNACK_ERR_NO_SPACE when fewer than
  * n_prune positions are empty or the draw budget (sized in the workspace
  * query: twice the expected number of draws plus 4096) runs out; the handle's
@@ -309,12 +314,11 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
                                     snack_stream_t stream);
 
 /*
- * Order `stream` after every plan rebuild of the handle that may still be
- * running on its second stream (the column view of the last
- * snack_restructure); returns at once, asynchronous like every call.  Use it
- * before timing, freeing or reading anything that the rebuild touches (the
- * plan; row_out/col_out of the last restructure).  A handle that has not
- * restructured has nothing pending.
+ * Order `stream` after everything the last snack_restructure left running on
+ * the handle's own streams (the column-view update of the plan); returns at
+ * once, asynchronous like every call.  Use it before timing, freeing or
+ * reading anything that the update touches (the plan).  A handle that has
+ * not restructured has nothing pending.
  */
 snack_status snack_wait_plan(snack_handle h, snack_stream_t stream);
 

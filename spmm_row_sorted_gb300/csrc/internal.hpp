@@ -43,7 +43,12 @@ struct PlanPtrs {
   void *tables;
 };
 
-// Words of PlanPtrs::flags: [0] pattern validation, [1] constant fan-in check.
+// Words of PlanPtrs::flags: [0] pattern validation, [1] constant fan-in check,
+// [kPlanFlagColOk] set when the last restructure's column-order list of the
+// regrown positions is complete (its column-view update, which runs after
+// the call returns, may write; the word lives in the plan because the caller
+// may reuse the workspace by then).
+constexpr int kPlanFlagColOk = 2;
 
 struct PlanLayout {
   size_t off_rp, off_tf, off_cp, off_tt, off_rowt, off_srct, off_flags, off_col16, off_rowt16, off_cpa, off_tta,
@@ -108,17 +113,18 @@ struct RestructureArgs {
   // The plan of the input pattern: the draws read its row offsets and 16-bit
   // columns, the merge rewrites them (and the forward tiles) for the output;
   // when `update` is set the column view is updated into the plan's second
-  // view on `aux` after the call returns (the caller then swaps the views),
-  // else it is rebuilt on s.
+  // view on `aux_lo` after the call returns (the caller then swaps the
+  // views), else it is rebuilt on s.
   const PlanPtrs *plan;
   TileGeom gf, gt;
   bool update;
   uint32_t *host_counts;  // pinned, mapped host memory, 8 words: a draw chunk's accepted count, table and bucket
-                          // overflows, and the plan's look-back error
+                          // overflows, and the acceptance scan's look-back error
   uint32_t *counts_dev;   // the same words' device address (written by a kernel, no copy)
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
-  cudaStream_t aux;          // second stream of the handle (regrow branch, column-view update)
-  cudaEvent_t ev_fork, ev_join;
+  cudaStream_t aux;          // second stream of the handle (regrow branch), highest priority
+  cudaStream_t aux_lo;       // third stream (the deferred column-view update), lowest priority
+  cudaEvent_t ev_fork, ev_join, ev_aux;
 };
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune);
 // Returns SNACK_OK, SNACK_ERR_NO_SPACE, SNACK_ERR_WORKSPACE or SNACK_ERR_CUDA;
@@ -192,11 +198,13 @@ struct snack_layer {
   uint32_t *host_counts = nullptr;  // restructure read-back (pinned, mapped), made on first use
   uint32_t *host_counts_dev = nullptr;  // its device address
   cudaEvent_t counts_ready = nullptr;
-  cudaStream_t aux = nullptr;  // restructure's second stream and its fork/join events, made on first use
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  // The column view of the last restructure is updated on `aux` after the
-  // call returns; ev_colview marks its end and the calls that read the
-  // column view make their stream wait for it.
+  cudaStream_t aux = nullptr;     // restructure's second stream and its fork/join events, made on first use
+  cudaStream_t aux_lo = nullptr;  // and its third stream (lowest priority)
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_aux = nullptr;
+  // The column view of the last restructure is updated on `aux_lo` after the
+  // call returns; ev_colview marks the end of everything the call left on
+  // `aux` and `aux_lo`, and the calls that read the column view make their
+  // stream wait for it.
   cudaEvent_t ev_colview = nullptr;
   bool colview_pending = false;
   bool dense = false;   // the layer takes the tensor-core path for wide batches

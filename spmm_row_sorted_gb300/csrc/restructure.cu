@@ -529,12 +529,12 @@ struct DrawState {
   uint32_t col_overflow;     // a column-order bucket did
   uint32_t lb_fail;          // the acceptance scan gave up waiting for a predecessor tile (never expected)
   uint32_t lists_ok;         // the row-order list is complete: the merge may write
-  uint32_t col_ok;           // and the column-order list: the column-view update may write
 };
 
-// The lists' verdict and, with host_words, the chunk's counters to the host's
-// mapped words.
-__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made) {
+// The lists' verdict (the column-order one into the plan word col_ok) and,
+// with host_words, the chunk's counters to the host's mapped words.
+__device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, bool made,
+                                        uint32_t *col_ok) {
   const uint32_t tot = ds->total, ovf = ds->overflow, bovf = ds->bucket_overflow, covf = ds->col_overflow;
   const uint32_t lbf = ds->lb_fail;
   if (host_words) {
@@ -547,12 +547,12 @@ __device__ __forceinline__ void publish(DrawState *ds, int64_t n_prune, uint32_t
   }
   const bool ok = made && (int64_t)tot >= n_prune && !ovf && !bovf && !lbf;
   ds->lists_ok = ok ? 1u : 0u;
-  ds->col_ok = ok && !covf ? 1u : 0u;
+  *col_ok = ok && !covf ? 1u : 0u;
 }
 
-__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made) {
+__global__ void k_publish(DrawState *ds, int64_t n_prune, uint32_t *host_words, int made, uint32_t *col_ok) {
   pdl_wait();
-  publish(ds, n_prune, host_words, made != 0);
+  publish(ds, n_prune, host_words, made != 0, col_ok);
 }
 
 __global__ void k_set_word(uint32_t *w, uint32_t v) {
@@ -565,7 +565,7 @@ __global__ void k_set_word(uint32_t *w, uint32_t v) {
 // to empty (one launch instead of several fills).
 __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bcnt, int64_t nb,
                           uint64_t *__restrict__ lb_status, int64_t n_lb, uint32_t *lb_ticket,
-                          uint32_t *__restrict__ pcnt, int64_t n_pc) {
+                          uint32_t *__restrict__ pcnt, int64_t n_pc, uint32_t *col_ok) {
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -576,7 +576,7 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
     ds->col_overflow = 0u;
     ds->lb_fail = 0u;
     ds->lists_ok = 0u;
-    ds->col_ok = 0u;
+    *col_ok = 0u;
     *lb_ticket = 0u;
   }
   const int64_t cap = (int64_t)tab.mask + 1;
@@ -721,12 +721,13 @@ struct RankDst {
 // R, the others the column-order buckets C.  Block 0 first sets the lists'
 // verdict (and, with host_words, publishes the chunk's counters).
 __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool k32r, uint32_t nr, BucketSet C,
-                                                  RankDst DC, int64_t n_prune, DrawState *ds, uint32_t *host_words) {
+                                                  RankDst DC, int64_t n_prune, DrawState *ds, uint32_t *host_words,
+                                                  uint32_t *col_ok) {
   pdl_wait();
   __shared__ uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true);
+  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true, col_ok);
   const bool rows = blockIdx.x < nr;
   const BucketSet S = rows ? R : C;
   const RankDst D = rows ? DR : DC;
@@ -1605,7 +1606,8 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   };
   const int64_t n_tiles = ceil_div(nnz, kMkTile);
   const uint32_t *row_guard = n_prune > 0 ? &ds->lists_ok : nullptr;
-  const uint32_t *col_guard = n_prune > 0 ? &ds->col_ok : nullptr;
+  uint32_t *col_ok = pl.flags + kPlanFlagColOk;
+  const uint32_t *col_guard = n_prune > 0 ? col_ok : nullptr;
   // 3: the merge (after s waits for the row-order list) and the plan's row half
   bool row_direct = true;  // set with the keep counts below, before the first call
   auto queue_rows = [&]() -> cudaError_t {
@@ -1637,9 +1639,14 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     return build_plan(a.out_f, a.in_f, nnz, a.row_out, a.col_out, pl, a.gf, a.gt, b + W.plan, s, kPlanRowsReady,
                       !update);
   };
-  // 4: the column-view update, on s2 after s's work so far
+  // 4: the column-view update, on the third stream (lowest priority), after
+  // s's work so far and everything on s2
+  cudaStream_t s3 = a.aux_lo;
   auto queue_cols = [&]() -> cudaError_t {
-    cudaError_t err = fork();
+    cudaError_t err = cudaEventRecord(a.ev_fork, s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(s3, a.ev_fork, 0);
+    if (err == cudaSuccess) err = cudaEventRecord(a.ev_aux, s2);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(s3, a.ev_aux, 0);
     if (err != cudaSuccess) return err;
     const ColPol cpol{pl.cp, pl.row_t, pl.rowt16, pl.src_t, pl.newidx, rbits, a.in_f, pl.gc_key, pl.gc_q, pl.gq,
                       pl.row_t_alt, pl.src_t_alt, pl.rowt16_alt};
@@ -1647,16 +1654,16 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     // with pruned weights, one more block of the bounds launch turns their
     // counts per column into exclusive prefixes
     const bool pruned = n_prune > 0;
-    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256) + (pruned ? 1u : 0u), 256, 0, s2, cpol, n_prune,
+    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256) + (pruned ? 1u : 0u), 256, 0, s3, cpol, n_prune,
                n_tiles, cbnd, pruned ? (const uint32_t *)pl.cv_pcnt : nullptr, pl.cv_ppre, (int64_t)a.in_f);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     err = launch_merge(cpol,
                        MkArgs{nnz, n_prune, nnz, cbnd, nullptr, col_guard, rbits, a.in_f, pl.cp_alt,
                               pruned ? (const uint32_t *)pl.cv_ppre : nullptr},
-                       kMkByColumn, s2);
+                       kMkByColumn, s3);
     if (err != cudaSuccess) return err;
-    return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s2);
+    return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s3);
   };
   auto mark = [&]() -> cudaError_t { return cudaEventRecord(a.ev_join, s2); };  // s joins s2 here
   auto wait_mark = [&]() -> cudaError_t { return cudaStreamWaitEvent(s, a.ev_join, 0); };
@@ -1672,7 +1679,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     launch_pdl(k_rs_init, grid_for(W.cap, 256, 1184), 256, 0, s2, ds, tab, bcnt,
                (int64_t)(buckets ? 2 * (int64_t)W.n_bkt * kCntStride : 0), alb, n_at1,
                reinterpret_cast<uint32_t *>(alb + n_at1), update ? pl.cv_pcnt : (uint32_t *)nullptr,
-               (int64_t)(update ? a.in_f : 0));
+               (int64_t)(update ? a.in_f : 0), col_ok);
     m = chunk_size();
     e = draw_chunk(m, true);
     if (e == cudaSuccess) {
@@ -1680,14 +1687,14 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       if (buckets) {  // both orders' lists in one launch
         const uint32_t nr = (br.nb + 7) / 8, nc = update ? (bc.nb + 7) / 8 : 0u;
         launch_pdl(k_bkt_rank, nr + nc, 256, 0, s2, br, RankDst{B, nullptr, Bq}, k32, nr, bc,
-                   RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev);
+                   RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev, col_ok);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = mark();
       } else {
         e = sort_rows_general();
         if (e == cudaSuccess) e = sort_cols_general();
         if (e == cudaSuccess) {
-          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1);
+          launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1, col_ok);
           e = cudaGetLastError();
         }
         if (e == cudaSuccess) e = mark();
@@ -1762,7 +1769,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
           verdict = SNACK_ERR_CUDA;
           break;
         }
-        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0);
+        launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 0, col_ok);
         if (cudaGetLastError() != cudaSuccess || cudaEventRecord(a.counts_ready, s2) != cudaSuccess ||
             cudaEventSynchronize(a.counts_ready) != cudaSuccess) {
           verdict = SNACK_ERR_CUDA;
@@ -1783,7 +1790,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
         verdict = SNACK_ERR_CUDA;
       if (verdict == SNACK_OK) {
         launch_pdl(k_set_word, 1, 1, 0, s2, &ds->lists_ok, 1u);
-        launch_pdl(k_set_word, 1, 1, 0, s2, &ds->col_ok, 1u);
+        launch_pdl(k_set_word, 1, 1, 0, s2, col_ok, 1u);
         if (cudaGetLastError() != cudaSuccess) verdict = SNACK_ERR_CUDA;
       }
       if (join() != cudaSuccess && verdict == SNACK_OK) verdict = SNACK_ERR_CUDA;
@@ -1794,8 +1801,9 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       cols_queued = false;
       SNACK_TRY(fork());
       SNACK_TRY(sort_cols_general());
-      launch_pdl(k_set_word, 1, 1, 0, s2, &ds->col_ok, 1u);
+      launch_pdl(k_set_word, 1, 1, 0, s2, col_ok, 1u);
       SNACK_TRY(cudaGetLastError());
+      SNACK_TRY(join());  // the sort's scratch is in the workspace: done before the call returns
     }
   }
   if (!rows_queued) {

@@ -696,20 +696,30 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
     return SNACK_ERR_CUDA;
   if (!h->ev_colview && cudaEventCreateWithFlags(&h->ev_colview, cudaEventDisableTiming) != cudaSuccess)
     return SNACK_ERR_CUDA;
-  if (!h->aux) {
+  if (!h->ev_aux && cudaEventCreateWithFlags(&h->ev_aux, cudaEventDisableTiming) != cudaSuccess)
+    return SNACK_ERR_CUDA;
+  if (!h->aux || !h->aux_lo) {
     // The regrow branch (draws, acceptance, sort) is the longer of the two
     // that meet at the merge: its stream gets the highest priority, so its
     // blocks are scheduled ahead of the select's when both wait for SMs.
+    // The column-view update that runs on after the call returns gets the
+    // lowest, so the caller's next calls go ahead of it where their streams
+    // have a higher priority.
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SNACK_ERR_CUDA;
-    if (cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess) return SNACK_ERR_CUDA;
+    if (!h->aux && cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return SNACK_ERR_CUDA;
+    if (!h->aux_lo && cudaStreamCreateWithPriority(&h->aux_lo, cudaStreamNonBlocking, least) != cudaSuccess)
+      return SNACK_ERR_CUDA;
   }
   a.host_counts = h->host_counts;
   a.counts_dev = h->host_counts_dev;
   a.counts_ready = h->counts_ready;
   a.aux = h->aux;
+  a.aux_lo = h->aux_lo;
   a.ev_fork = h->ev_fork;
   a.ev_join = h->ev_join;
+  a.ev_aux = h->ev_aux;
   bool updated = false;
   snack_status st = run_restructure(a, ws, ws_bytes, s, &updated);
   if (st == SNACK_OK) h->fan_in = 0;  // regrowth lands in any row: row counts change
@@ -720,10 +730,13 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
     std::swap(h->p.src_t, h->p.src_t_alt);
     std::swap(h->p.rowt16, h->p.rowt16_alt);
   }
-  // Whatever is still queued on the second stream (the column-view update,
-  // or work an error left behind) is what the column-view readers wait for.
-  if (cudaEventRecord(h->ev_colview, h->aux) != cudaSuccess) {
+  // Whatever is still queued on the second and third streams (the
+  // column-view update, or work an error left behind) is what the
+  // column-view readers wait for.
+  if (cudaEventRecord(h->ev_aux, h->aux) != cudaSuccess || cudaStreamWaitEvent(h->aux_lo, h->ev_aux, 0) != cudaSuccess ||
+      cudaEventRecord(h->ev_colview, h->aux_lo) != cudaSuccess) {
     cudaStreamSynchronize(h->aux);
+    cudaStreamSynchronize(h->aux_lo);
     h->colview_pending = false;
     return SNACK_ERR_CUDA;
   }
@@ -807,7 +820,7 @@ snack_status snack_wait_plan(snack_handle h, snack_stream_t stream) {
 
 void snack_destroy(snack_handle h) {
   if (!h) return;
-  if (h->counts_ready || h->aux || h->ev_fork || h->ev_join || h->ev_colview) {
+  if (h->counts_ready || h->aux || h->aux_lo || h->ev_fork || h->ev_join || h->ev_aux || h->ev_colview) {
     int prev = -1;
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
@@ -815,6 +828,11 @@ void snack_destroy(snack_handle h) {
       cudaStreamSynchronize(h->aux);
       cudaStreamDestroy(h->aux);
     }
+    if (h->aux_lo) {
+      cudaStreamSynchronize(h->aux_lo);
+      cudaStreamDestroy(h->aux_lo);
+    }
+    if (h->ev_aux) cudaEventDestroy(h->ev_aux);
     if (h->counts_ready) cudaEventDestroy(h->counts_ready);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);

@@ -318,7 +318,7 @@ def test_restructure_deferred_column_view(dtype):
         x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
         M = snack.SparseLinear(out_f, in_f, row.clone(), col.clone(), val.clone(), bias, max_batch=32)
         M.restructure(30000, seed=3, step=4)
-        M.ws.fill_(255)  # the rebuild must not read the caller's workspace
+        M.ws.fill_(0)  # the rebuild must not read the caller's workspace (a zero there would stop it)
         got = {"y": M.forward(x)}
         other.wait_stream(torch.cuda.current_stream())  # inputs and the new COO, not the rebuild
         with torch.cuda.stream(other):
