@@ -424,12 +424,22 @@ def run_ours(args):
         x0 = torch.from_numpy(acts.x).to(dev)
         dy0 = torch.from_numpy(acts.dy).to(dev)
         for c in range(1 if args.profile else N_COPIES):
+            # a step's inputs (X, dY) and results (Y, dX, db, dW) each in one
+            # buffer, so the end-to-end loop moves them with one copy per
+            # direction (every part starts on a 16-byte boundary)
+            inp = torch.empty(BATCH * IN_F + BATCH * OUT_F, device=dev)
+            out = torch.empty(BATCH * OUT_F + BATCH * IN_F + OUT_F + nnz, device=dev)
             cp = {"row": [row0.clone(), torch.empty_like(row0)], "col": [col0.clone(), torch.empty_like(col0)],
                   "val": [val0.clone(), torch.empty_like(val0)], "cur": 0, "src": torch.empty_like(row0),
-                  "x": x0.clone(), "dy": dy0.clone(), "bias": bias.clone(),
-                  "y": torch.empty((BATCH, OUT_F), device=dev), "dx": torch.empty((BATCH, IN_F), device=dev),
-                  "dw": torch.empty(nnz, device=dev), "db": torch.empty(OUT_F, device=dev),
+                  "inp": inp, "out": out, "bias": bias.clone(),
+                  "x": inp[:BATCH * IN_F].view(BATCH, IN_F), "dy": inp[BATCH * IN_F:].view(BATCH, OUT_F),
+                  "y": out[:BATCH * OUT_F].view(BATCH, OUT_F),
+                  "dx": out[BATCH * OUT_F:BATCH * OUT_F + BATCH * IN_F].view(BATCH, IN_F),
+                  "db": out[BATCH * (OUT_F + IN_F):BATCH * (OUT_F + IN_F) + OUT_F],
+                  "dw": out[BATCH * (OUT_F + IN_F) + OUT_F:],
                   "plan": torch.empty(plan_b, dtype=torch.uint8, device=dev)}
+            cp["x"].copy_(x0)
+            cp["dy"].copy_(dy0)
             copies.append(cp)
         ws = torch.empty(ws_b, dtype=torch.uint8, device=dev)
     stream.synchronize()
@@ -554,13 +564,12 @@ def run_ours(args):
     # host buffers; events order a copy slot's transfers after the step that
     # last used it)
     e2e_steps = max(1, min(args.steps, 200))
-    hx = torch.from_numpy(acts.x).pin_memory()
-    hdy = torch.from_numpy(acts.dy).pin_memory()
-    host_out = [{"y": torch.empty((BATCH, OUT_F)).pin_memory(), "dx": torch.empty((BATCH, IN_F)).pin_memory(),
-                 "dw": torch.empty(nnz).pin_memory(), "db": torch.empty(OUT_F).pin_memory()}
-                for _ in range(min(N_COPIES, e2e_steps))]
-    h2d = hx.numel() * 4 + hdy.numel() * 4
-    d2h = sum(t.numel() for t in host_out[0].values()) * 4
+    # a step's inputs X and dY, and its results Y, dX, db and dW, each packed
+    # in one pinned host buffer: one copy per direction and step
+    hin = torch.cat([torch.from_numpy(acts.x).reshape(-1), torch.from_numpy(acts.dy).reshape(-1)]).pin_memory()
+    host_out = [torch.empty(copies[0]["out"].numel()).pin_memory() for _ in range(min(N_COPIES, e2e_steps))]
+    h2d = hin.numel() * 4
+    d2h = host_out[0].numel() * 4
     hs, ds = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     slots = len(host_out)
     ev = lambda: torch.cuda.Event()
@@ -577,8 +586,7 @@ def run_ours(args):
         if computed[c] is not None:
             hs.wait_event(computed[c])  # the slot's previous step has read its inputs
         with torch.cuda.stream(hs):
-            cp["x"].copy_(hx, non_blocking=True)
-            cp["dy"].copy_(hdy, non_blocking=True)
+            cp["inp"].copy_(hin, non_blocking=True)
         ready = ev()
         ready.record(hs)
         stream.wait_event(ready)
@@ -589,8 +597,7 @@ def run_ours(args):
         computed[c].record(stream)
         ds.wait_event(computed[c])
         with torch.cuda.stream(ds):
-            for k, t in host_out[c].items():
-                t.copy_(cp[k], non_blocking=True)
+            host_out[c].copy_(cp["out"], non_blocking=True)
         drained[c] = ev()
         drained[c].record(ds)
     for d in drained:
