@@ -572,7 +572,10 @@ def run_ours(args):
     d2h = host_out[0].numel() * 4
     hs, ds = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     slots = len(host_out)
-    ev = lambda: torch.cuda.Event()
+    # events made once: a slot's inputs landed, its step ran, its results reached the host
+    ready_ev = [torch.cuda.Event() for _ in range(slots)]
+    computed_ev = [torch.cuda.Event() for _ in range(slots)]
+    drained_ev = [torch.cuda.Event() for _ in range(slots)]
     computed = [None] * slots  # event after the last step that used a slot
     drained = [None] * slots   # event after that step's results reached the host
     stream.synchronize()
@@ -587,18 +590,18 @@ def run_ours(args):
             hs.wait_event(computed[c])  # the slot's previous step has read its inputs
         with torch.cuda.stream(hs):
             cp["inp"].copy_(hin, non_blocking=True)
-        ready = ev()
+        ready = ready_ev[c]
         ready.record(hs)
         stream.wait_event(ready)
         if drained[c] is not None:
             stream.wait_event(drained[c])  # the slot's previous results have left the device
         step(cp, 10**6 + i)
-        computed[c] = ev()
+        computed[c] = computed_ev[c]
         computed[c].record(stream)
         ds.wait_event(computed[c])
         with torch.cuda.stream(ds):
             host_out[c].copy_(cp["out"], non_blocking=True)
-        drained[c] = ev()
+        drained[c] = drained_ev[c]
         drained[c].record(ds)
     for d in drained:
         if d is not None:
