@@ -1025,8 +1025,6 @@ def _fanin_restructure(torch, snack, timer, dev, reps):
     for name, fn in (("restructure_rows", per_row), ("restructure", unstructured)):
         cold, warm = timer.time_restructure(snack, h, fn, reps, True), timer.time_restructure(snack, h, fn, reps, False)
         for op, k in ((name, 0), (name + "_all", 1)):
-            if op == "restructure_rows_all":
-                continue  # the per-row restructure rebuilds its column view before it returns
             us = cold[k]
             out.append({"config": "c4-fanin", "layer": "16384x16384", "nnz": lay.nnz, "batch": 0, "op": op,
                     "dtype": "f32", "us_cold": us, "us_warm": warm[k], "graph": False,

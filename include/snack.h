@@ -31,7 +31,7 @@
  * the legacy default stream), except snack_create with validate != 0, which
  * synchronises `stream`, and snack_restructure, which waits on the host for
  * its draw count (see there).  A plan and a workspace may be used by one call
- * in flight at a time.  After snack_restructure the update of the plan's
+ * in flight at a time.  After either restructure the update of the plan's
  * column view may still be running on a stream of the handle; every call
  * that reads the column view (snack_spmm_dx, snack_spmm_dx_gelu,
  * snack_sddmm_dw, snack_backward and both restructures) first makes its
@@ -302,11 +302,19 @@ snack_status snack_restructure_rows_workspace_size(snack_handle h, int64_t n_per
  * 0's stream is snack_restructure's stream.  Every row keeps its count and its
  * offsets, so the outputs (same meaning and rules as snack_restructure) hold
  * row r at the same index range as the input, and only the column view of the
- * plan is rebuilt.  Needs ws_bytes >= snack_restructure_rows_workspace_size.
+ * plan changes.  Needs ws_bytes >= snack_restructure_rows_workspace_size(h,
+ * n_per_row).  With the deferred scratch in the plan (see snack_query_sizes)
+ * and out_f * n_per_row within it (one quarter of nnz) and at most 2^20, the
+ * kernel also files the regrown positions into column-order buckets in the
+ * workspace; the call ranks them on `stream` and then updates the column
+ * view from the plan alone on the handle's lowest-priority stream, as
+ * snack_restructure does (it reads neither the workspace nor the outputs
+ * there).  Otherwise, or when a bucket ran out of slots (not expected), the
+ * column view is rebuilt on `stream` before the call returns.
  * Returns SNACK_ERR_UNSUPPORTED when n_per_row > 256 or in_f > 65536, and
  * SNACK_ERR_NO_SPACE when a row has fewer empty columns than it prunes or runs
  * out of draws (the outputs are then undefined and the plan is unchanged).
- * The host waits once for the device's error word.
+ * The host waits once for the device's error words.
  */
 snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const int32_t *col, const void *val,
                                     int64_t n_per_row, uint64_t seed, uint64_t step, int32_t *row_out,

@@ -169,11 +169,33 @@ struct RowsRestructureArgs {
   void *val_out;
   int32_t *src_out;   // may be null
   uint16_t *col16;    // plan's 16-bit column copy, or null
-  uint32_t *err;      // device word: nonzero after the kernel when a row cannot be restructured
+  // device words: err[0] nonzero after the kernel when a row cannot be
+  // restructured; with plan set also err[1] (a column-order bucket of the
+  // regrown positions ran out of slots) and err[2] (the regrown count)
+  uint32_t *err;
+  // With plan set, the kernel also writes the inputs of the incremental
+  // column-view update: each old weight's new index and the pruned weights
+  // per column into the plan, the regrown positions into column-order
+  // buckets in bws (rows_update_ws_bytes bytes, kAlign-aligned).
+  const PlanPtrs *plan = nullptr;
+  void *bws = nullptr;
 };
 // SNACK_OK, SNACK_ERR_UNSUPPORTED (n_per_row > 256 or in_f > 65536) or SNACK_ERR_CUDA; row
 // failures are reported through *err.
 snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s);
+// Bytes of the bucket region of a per-row restructure's column-view update;
+// 0 when the update does not apply (more regrown weights than the buckets
+// take).
+size_t rows_update_ws_bytes(int32_t out_f, int64_t n_per_row);
+// After run_restructure_rows with plan set: the regrown positions'
+// column-order list into the plan, on s (it reads bws; it writes nothing
+// when err[0] or err[1] is set).
+cudaError_t queue_rows_rank(const RowsRestructureArgs &a, cudaStream_t s);
+// After queue_rows_rank, with no row error and no bucket overflow: on s_lo,
+// once s reaches ev, the merge of the old column view with the n_grown
+// regrown positions into the plan's second view, and that view's tiles.
+cudaError_t queue_rows_colview(const RowsRestructureArgs &a, int64_t n_grown, const TileGeom &gt, cudaStream_t s,
+                               cudaStream_t s_lo, cudaEvent_t ev);
 
 // Host SplitMix64 (state increment and finaliser of Steele, Lea and Flood 2014).
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ULL;

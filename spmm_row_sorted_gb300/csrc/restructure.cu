@@ -719,15 +719,18 @@ struct RankDst {
 // block adds up those counts), and each key lands at its rank among the
 // bucket's keys (all distinct).  Blocks [0, nr) rank the row-order buckets
 // R, the others the column-order buckets C.  Block 0 first sets the lists'
-// verdict (and, with host_words, publishes the chunk's counters).
+// verdict (and, with host_words, publishes the chunk's counters); without ds
+// there is no verdict to set.  With stop set, the launch writes nothing when
+// stop[0] or stop[1] is nonzero.
 __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool k32r, uint32_t nr, BucketSet C,
                                                   RankDst DC, int64_t n_prune, DrawState *ds, uint32_t *host_words,
-                                                  uint32_t *col_ok) {
+                                                  uint32_t *col_ok, const uint32_t *stop) {
   pdl_wait();
+  if (stop && (stop[0] | stop[1])) return;
   __shared__ uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == 0 && threadIdx.x == 0) publish(ds, n_prune, host_words, true, col_ok);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && ds) publish(ds, n_prune, host_words, true, col_ok);
   const bool rows = blockIdx.x < nr;
   const BucketSet S = rows ? R : C;
   const RankDst D = rows ? DR : DC;
@@ -1387,6 +1390,33 @@ int bits_for(uint64_t v) {
   return b;
 }
 
+// The column-view update on stream s3: the old view merged with the n_list
+// regrown positions in column order (pl.gc_key, pl.gc_q, pl.gq), kept
+// entries taking pl.newidx, tile prefixes from the pruned counts per column
+// (pl.cv_pcnt, n_list > 0), into the plan's second view, then its column
+// tiles.  `guard`: when set and zero, the merge writes nothing.
+cudaError_t queue_colview_merge(const PlanPtrs &pl, int32_t in_f, int64_t nnz, int64_t n_list, int rbits,
+                                const uint32_t *guard, const TileGeom &gt, cudaStream_t s3) {
+  const int64_t n_tiles = ceil_div(nnz, kMkTile);
+  const ColPol cpol{pl.cp,     pl.row_t, pl.rowt16, pl.src_t,     pl.newidx,    rbits,
+                    in_f,      pl.gc_key, pl.gc_q,  pl.gq,        pl.row_t_alt, pl.src_t_alt,
+                    pl.rowt16_alt};
+  MkBound *cbnd = reinterpret_cast<MkBound *>(pl.cv_bnd);
+  // with pruned weights, one more block of the bounds launch turns their
+  // counts per column into exclusive prefixes
+  const bool pruned = n_list > 0;
+  launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256) + (pruned ? 1u : 0u), 256, 0, s3, cpol, n_list,
+             n_tiles, cbnd, pruned ? (const uint32_t *)pl.cv_pcnt : nullptr, pl.cv_ppre, (int64_t)in_f);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = launch_merge(cpol,
+                     MkArgs{nnz, n_list, nnz, cbnd, nullptr, guard, rbits, in_f, pl.cp_alt,
+                            pruned ? (const uint32_t *)pl.cv_ppre : nullptr},
+                     kMkByColumn, s3);
+  if (err != cudaSuccess) return err;
+  return cut_tiles(pl.cp_alt, in_f, nnz, gt, pl.tiles_t_alt, s3);
+}
+
 // Expected number of draws to accept `need` distinct positions out of `empty`
 // empty ones, among n_pos equally likely positions: n_pos * (H(empty) -
 // H(empty - need)), using ln((e + 1/2) / (e - need + 1/2)) for the difference.
@@ -1648,22 +1678,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
     if (err == cudaSuccess) err = cudaEventRecord(a.ev_aux, s2);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(s3, a.ev_aux, 0);
     if (err != cudaSuccess) return err;
-    const ColPol cpol{pl.cp, pl.row_t, pl.rowt16, pl.src_t, pl.newidx, rbits, a.in_f, pl.gc_key, pl.gc_q, pl.gq,
-                      pl.row_t_alt, pl.src_t_alt, pl.rowt16_alt};
-    MkBound *cbnd = reinterpret_cast<MkBound *>(pl.cv_bnd);
-    // with pruned weights, one more block of the bounds launch turns their
-    // counts per column into exclusive prefixes
-    const bool pruned = n_prune > 0;
-    launch_pdl(k_bounds<ColPol>, grid_for(32 * (n_tiles + 1), 256) + (pruned ? 1u : 0u), 256, 0, s3, cpol, n_prune,
-               n_tiles, cbnd, pruned ? (const uint32_t *)pl.cv_pcnt : nullptr, pl.cv_ppre, (int64_t)a.in_f);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    err = launch_merge(cpol,
-                       MkArgs{nnz, n_prune, nnz, cbnd, nullptr, col_guard, rbits, a.in_f, pl.cp_alt,
-                              pruned ? (const uint32_t *)pl.cv_ppre : nullptr},
-                       kMkByColumn, s3);
-    if (err != cudaSuccess) return err;
-    return cut_tiles(pl.cp_alt, a.in_f, nnz, a.gt, pl.tiles_t_alt, s3);
+    return queue_colview_merge(pl, a.in_f, nnz, n_prune, rbits, col_guard, a.gt, s3);
   };
   auto mark = [&]() -> cudaError_t { return cudaEventRecord(a.ev_join, s2); };  // s joins s2 here
   auto wait_mark = [&]() -> cudaError_t { return cudaStreamWaitEvent(s, a.ev_join, 0); };
@@ -1687,7 +1702,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       if (buckets) {  // both orders' lists in one launch
         const uint32_t nr = (br.nb + 7) / 8, nc = update ? (bc.nb + 7) / 8 : 0u;
         launch_pdl(k_bkt_rank, nr + nc, 256, 0, s2, br, RankDst{B, nullptr, Bq}, k32, nr, bc,
-                   RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev, col_ok);
+                   RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev, col_ok, (const uint32_t *)nullptr);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = mark();
       } else {
@@ -1849,6 +1864,15 @@ struct RowsArgs {
   int32_t *src_out;
   uint16_t *col16;
   uint32_t *err;  // bit 0: a row has fewer empty columns than it prunes; bit 1: a row ran out of draws
+  // With newidx set, the inputs of the incremental column-view update: each
+  // old weight's new index (~0u: pruned), the pruned weights per column, the
+  // new index of regrown weight q = row * n_per_row + g in gq, and (col <<
+  // rbits | row, q) of every regrown weight in its column-order bucket;
+  // *bovf set when a bucket ran out of slots; *n_grown the regrown count.
+  uint32_t *newidx, *pcnt, *gq;
+  BucketSet bc;
+  uint32_t *bovf, *n_grown;
+  int rbits;
 };
 
 // one warp: the digit d of hist (256 bins) where the running count reaches
@@ -2025,8 +2049,13 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
       val_out[o] = val[k0 + j];
       if (A.src_out) A.src_out[o] = (int32_t)(k0 + j);
       if (A.col16) A.col16[o] = (uint16_t)c;
-    } else if (in && !keep && n_pr + __popc(pb & lt) < (uint32_t)kRowsMaxPrune) {
-      pcol[n_pr + __popc(pb & lt)] = c;
+      if (A.newidx) A.newidx[k0 + j] = (uint32_t)o;
+    } else if (in && !keep) {
+      if (n_pr + __popc(pb & lt) < (uint32_t)kRowsMaxPrune) pcol[n_pr + __popc(pb & lt)] = c;
+      if (A.newidx) {
+        A.newidx[k0 + j] = ~0u;
+        atomicAdd(&A.pcnt[c], 1u);
+      }
     }
     carry_eq += __popc(eqb);
     carry_keep += __popc(kb);
@@ -2045,10 +2074,68 @@ __global__ void __launch_bounds__(kRowsWarps * 32) k_restructure_rows(RowsArgs A
     val_out[o] = from_f32<TV>(0.f);
     if (A.src_out) A.src_out[o] = -1;
     if (A.col16) A.col16[o] = (uint16_t)c;
+    if (A.gq) {
+      const uint32_t q = (uint32_t)r * (uint32_t)A.n_per_row + (uint32_t)g;
+      A.gq[q] = (uint32_t)o;
+      A.bc.place((uint64_t)((c << A.rbits) | (uint32_t)r), q, A.bovf);
+    }
   }
+  if (A.n_grown && lane == 0 && p > 0) atomicAdd(A.n_grown, (uint32_t)p);
+}
+
+// The column-order buckets of a per-row restructure's regrown positions
+// (out_f * n_per_row at most) in its workspace.
+struct RowsBkt {
+  uint32_t nb;
+  size_t cnt, key, q, total;
+};
+RowsBkt rows_bkt_layout(int32_t out_f, int64_t n_per_row) {
+  RowsBkt L{};
+  const int64_t np = (int64_t)out_f * n_per_row, nb = np / kBktTarget;
+  L.nb = (uint32_t)(nb < 1 ? 1 : nb > (int64_t)kBktMaxBuckets ? (int64_t)kBktMaxBuckets + 1 : nb);
+  size_t o = 0;
+  L.cnt = o;
+  o += align_up(4 * (size_t)L.nb * kCntStride, kAlign);
+  L.key = o;
+  o += align_up(8 * (size_t)L.nb * kBktCap, kAlign);
+  L.q = o;
+  o += align_up(4 * (size_t)L.nb * kBktCap, kAlign);
+  L.total = o;
+  return L;
+}
+
+BucketSet rows_buckets(const RowsBkt &L, void *bws, int32_t in_f, int rbits) {
+  uint8_t *b = reinterpret_cast<uint8_t *>(bws);
+  return BucketSet{reinterpret_cast<uint32_t *>(b + L.cnt), reinterpret_cast<uint64_t *>(b + L.key),
+                   reinterpret_cast<uint32_t *>(b + L.q), bucket_mult(L.nb, (uint64_t)in_f << rbits), L.nb};
 }
 
 }  // namespace
+
+size_t rows_update_ws_bytes(int32_t out_f, int64_t n_per_row) {
+  const RowsBkt L = rows_bkt_layout(out_f, n_per_row);
+  return L.nb > kBktMaxBuckets ? 0 : L.total;
+}
+
+cudaError_t queue_rows_rank(const RowsRestructureArgs &a, cudaStream_t s) {
+  const PlanPtrs &pl = *a.plan;
+  const int rbits = bits_for((uint64_t)(a.out_f - 1));
+  const BucketSet C = rows_buckets(rows_bkt_layout(a.out_f, a.n_per_row), a.bws, a.in_f, rbits);
+  launch_pdl(k_bkt_rank, (C.nb + 7) / 8, 256, 0, s, BucketSet{}, RankDst{nullptr, nullptr, nullptr}, true, 0u, C,
+             RankDst{nullptr, pl.gc_key, pl.gc_q}, (int64_t)a.out_f * a.n_per_row, (DrawState *)nullptr,
+             (uint32_t *)nullptr, (uint32_t *)nullptr, (const uint32_t *)a.err);
+  return cudaGetLastError();
+}
+
+cudaError_t queue_rows_colview(const RowsRestructureArgs &a, int64_t n_grown, const TileGeom &gt, cudaStream_t s,
+                               cudaStream_t s_lo, cudaEvent_t ev) {
+  const PlanPtrs &pl = *a.plan;
+  const int rbits = bits_for((uint64_t)(a.out_f - 1));
+  cudaError_t e = cudaEventRecord(ev, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_lo, ev, 0);
+  if (e != cudaSuccess) return e;
+  return queue_colview_merge(pl, a.in_f, a.nnz, n_grown, rbits, nullptr, gt, s_lo);
+}
 
 size_t restructure_ws_bytes(int32_t out_f, int32_t in_f, int64_t nnz, int64_t n_prune) {
   return align_up(rws_layout(out_f, in_f, nnz, n_prune).total, kAlign);
@@ -2072,7 +2159,24 @@ snack_status run_restructure_rows(const RowsRestructureArgs &a, cudaStream_t s) 
   A.src_out = a.src_out;
   A.col16 = a.col16;
   A.err = a.err;
-  if (cudaMemsetAsync(a.err, 0, sizeof(uint32_t), s) != cudaSuccess) return SNACK_ERR_CUDA;
+  A.newidx = A.pcnt = A.gq = A.bovf = A.n_grown = nullptr;
+  A.bc = BucketSet{};
+  A.rbits = 0;
+  if (cudaMemsetAsync(a.err, 0, sizeof(uint32_t) * (a.plan ? 3 : 1), s) != cudaSuccess) return SNACK_ERR_CUDA;
+  if (a.plan) {
+    const RowsBkt L = rows_bkt_layout(a.out_f, a.n_per_row);
+    if (L.nb > kBktMaxBuckets || !a.bws || !a.plan->newidx) return SNACK_ERR_INVALID_ARG;
+    A.rbits = bits_for((uint64_t)(a.out_f - 1));
+    A.bc = rows_buckets(L, a.bws, a.in_f, A.rbits);
+    A.newidx = a.plan->newidx;
+    A.pcnt = a.plan->cv_pcnt;
+    A.gq = a.plan->gq;
+    A.bovf = a.err + 1;
+    A.n_grown = a.err + 2;
+    if (cudaMemsetAsync(A.bc.cnt, 0, sizeof(uint32_t) * (size_t)L.nb * kCntStride, s) != cudaSuccess ||
+        cudaMemsetAsync(A.pcnt, 0, sizeof(uint32_t) * (size_t)a.in_f, s) != cudaSuccess)
+      return SNACK_ERR_CUDA;
+  }
   const unsigned grid = (unsigned)((a.out_f + kRowsWarps - 1) / kRowsWarps);
   if (a.val_t == SNACK_BF16)
     launch_pdl(k_restructure_rows<bf16>, grid, kRowsWarps * 32, 0, s, A);

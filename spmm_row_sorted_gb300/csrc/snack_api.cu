@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <new>
@@ -416,6 +417,27 @@ bool readback_ready(snack_handle h) {
   return true;
 }
 
+// The restructures' streams and events, made on first use.
+bool restructure_streams(snack_handle h) {
+  if (!h->ev_fork && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess) return false;
+  if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) return false;
+  if (!h->ev_colview && cudaEventCreateWithFlags(&h->ev_colview, cudaEventDisableTiming) != cudaSuccess) return false;
+  if (!h->ev_aux && cudaEventCreateWithFlags(&h->ev_aux, cudaEventDisableTiming) != cudaSuccess) return false;
+  if (!h->aux || !h->aux_lo) {
+    // The regrow branch (draws, acceptance, sort) is the longer of the two
+    // that meet at the merge: its stream gets the highest priority, so its
+    // blocks are scheduled ahead of the select's when both wait for SMs.
+    // The column-view update that runs on after the call returns gets the
+    // lowest, so the caller's next calls go ahead of it where their streams
+    // have a higher priority.
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+    if (!h->aux && cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
+    if (!h->aux_lo && cudaStreamCreateWithPriority(&h->aux_lo, cudaStreamNonBlocking, least) != cudaSuccess)
+      return false;
+  }
+  return true;
+}
 
 // The column view of a restructured handle may still be rebuilding on the
 // handle's second stream: order `s` after it.  The forward reads only the
@@ -689,29 +711,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
   a.gf = h->lay.gf;
   a.gt = h->lay.gt;
   a.update = h->lay.cv && n_prune <= h->lay.cv_pmax;
-  if (!readback_ready(h)) return SNACK_ERR_CUDA;
-  if (!h->ev_fork && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess)
-    return SNACK_ERR_CUDA;
-  if (!h->ev_join && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
-    return SNACK_ERR_CUDA;
-  if (!h->ev_colview && cudaEventCreateWithFlags(&h->ev_colview, cudaEventDisableTiming) != cudaSuccess)
-    return SNACK_ERR_CUDA;
-  if (!h->ev_aux && cudaEventCreateWithFlags(&h->ev_aux, cudaEventDisableTiming) != cudaSuccess)
-    return SNACK_ERR_CUDA;
-  if (!h->aux || !h->aux_lo) {
-    // The regrow branch (draws, acceptance, sort) is the longer of the two
-    // that meet at the merge: its stream gets the highest priority, so its
-    // blocks are scheduled ahead of the select's when both wait for SMs.
-    // The column-view update that runs on after the call returns gets the
-    // lowest, so the caller's next calls go ahead of it where their streams
-    // have a higher priority.
-    int least = 0, greatest = 0;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return SNACK_ERR_CUDA;
-    if (!h->aux && cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess)
-      return SNACK_ERR_CUDA;
-    if (!h->aux_lo && cudaStreamCreateWithPriority(&h->aux_lo, cudaStreamNonBlocking, least) != cudaSuccess)
-      return SNACK_ERR_CUDA;
-  }
+  if (!readback_ready(h) || !restructure_streams(h)) return SNACK_ERR_CUDA;
   a.host_counts = h->host_counts;
   a.counts_dev = h->host_counts_dev;
   a.counts_ready = h->counts_ready;
@@ -746,7 +746,7 @@ snack_status snack_restructure(snack_handle h, const int32_t *row, const int32_t
 
 snack_status snack_restructure_rows_workspace_size(snack_handle h, int64_t n_per_row, size_t *bytes) {
   if (!h || !bytes || n_per_row < 0) return SNACK_ERR_INVALID_ARG;
-  *bytes = kAlign + plan_build_ws_bytes(h->out_f, h->in_f, h->nnz);
+  *bytes = kAlign + std::max(plan_build_ws_bytes(h->out_f, h->in_f, h->nnz), rows_update_ws_bytes(h->out_f, n_per_row));
   return SNACK_OK;
 }
 
@@ -774,7 +774,14 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
   if (nnz == 0) return SNACK_OK;
   DevGuard g(h->device);
   if (!g.ok) return SNACK_ERR_CUDA;
-  if (!readback_ready(h)) return SNACK_ERR_CUDA;
+  // Every row keeps its length, so the row view stays; the column view is
+  // updated from the old one (after the call returns, on the lowest-priority
+  // stream) where the plan keeps a second view and the workspace holds the
+  // buckets of the regrown positions, else rebuilt before the call returns.
+  const size_t upd_bytes = rows_update_ws_bytes(h->out_f, n_per_row);
+  const bool update = h->lay.cv && (int64_t)h->out_f * n_per_row <= h->lay.cv_pmax && upd_bytes > 0 &&
+                      ws_bytes >= kAlign + upd_bytes;
+  if (!readback_ready(h) || (update && !restructure_streams(h))) return SNACK_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!wait_colview(h, s)) return SNACK_ERR_CUDA;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
@@ -795,16 +802,42 @@ snack_status snack_restructure_rows(snack_handle h, const int32_t *row, const in
   a.src_out = src_out;
   a.col16 = h->p.col16;
   a.err = reinterpret_cast<uint32_t *>(b);
+  if (update) {
+    a.plan = &h->p;
+    a.bws = b + kAlign;
+  }
   snack_status st = run_restructure_rows(a, s);
   if (st != SNACK_OK) return st;
-  SNACK_CUDA(cudaMemcpyAsync(h->host_counts, a.err, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+  const int n_words = update ? 3 : 1;
+  SNACK_CUDA(cudaMemcpyAsync(h->host_counts, a.err, sizeof(uint32_t) * n_words, cudaMemcpyDeviceToHost, s));
   SNACK_CUDA(cudaEventRecord(h->counts_ready, s));
+  // the column-order list runs while the host waits for the words (it
+  // writes nothing if they say the update will not be taken)
+  if (update) SNACK_CUDA(queue_rows_rank(a, s));
   SNACK_CUDA(cudaEventSynchronize(h->counts_ready));
   if (h->host_counts[0]) {
     // the rows that finished wrote their new columns into the plan's 16-bit
     // copy: put back the input's, so the plan still serves (row, col)
     SNACK_CUDA(pack16(col, nnz, h->p.col16, s));
     return SNACK_ERR_NO_SPACE;
+  }
+  if (update && !h->host_counts[1]) {
+    if (h->p.tables && h->p.col16) SNACK_CUDA(build_tables(h->p.rp, h->p.col16, h->out_f, h->in_f, h->p.tables, s));
+    const cudaError_t e = queue_rows_colview(a, (int64_t)h->host_counts[2], h->lay.gt, s, h->aux_lo, h->ev_fork);
+    if (e == cudaSuccess) {  // the second view becomes the current one
+      std::swap(h->p.cp, h->p.cp_alt);
+      std::swap(h->p.tiles_t, h->p.tiles_t_alt);
+      std::swap(h->p.row_t, h->p.row_t_alt);
+      std::swap(h->p.src_t, h->p.src_t_alt);
+      std::swap(h->p.rowt16, h->p.rowt16_alt);
+    }
+    if (e != cudaSuccess || cudaEventRecord(h->ev_colview, h->aux_lo) != cudaSuccess) {
+      cudaStreamSynchronize(h->aux_lo);
+      h->colview_pending = false;
+      return SNACK_ERR_CUDA;
+    }
+    h->colview_pending = true;
+    return SNACK_OK;
   }
   SNACK_CUDA(build_plan(h->out_f, h->in_f, nnz, row_out, col_out, h->p, h->lay.gf, h->lay.gt, b + kAlign, s,
                         kPlanRowTilesReady));

@@ -884,6 +884,45 @@ def test_restructure_rows_ties_nan_and_chain():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_restructure_rows_chain_column_view(dtype):
+    # Consecutive per-row restructures on one handle, each small enough for
+    # the incremental column-view update (out_f * n_per_row within a quarter
+    # of nnz): every update merges the view the one before left, and after
+    # each step every op that reads the column view matches the oracle.
+    out_f, in_f, K, n = 300, 500, 40, 6
+    lay = wl.make_layer(out_f, in_f, fan_in=K, val_std=0.5, val_dtype=dtype, seed=21, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(out_f, in_f, row, col, val, bias, max_batch=16)
+    r, c, v = lay.row, lay.col, lay.val
+    acts = wl.make_acts(16, in_f, out_f, dtype, seed=5)
+    x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
+    for step in range(5):
+        src = L.restructure_rows(n, 9, step)
+        r, c, so, _ = oracle.restructure_rows(out_f, in_f, r, c, oracle.as_f64(v, dtype), n, 9, step)
+        v = oracle.restructure_values(v, so)
+        got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+        got["dw"], got["db"] = L.grad_weight(x, dy)
+        torch.cuda.synchronize()
+        assert np.array_equal(L.col.cpu().numpy(), c) and np.array_equal(src.cpu().numpy(), so.astype(np.int32)), step
+        check_layer_ops(wl.Layer(out_f, in_f, r, c, v, lay.bias, dtype), acts, got=got)
+    L.close()
+
+
+def test_restructure_rows_bucket_overflow_rebuilds():
+    # Every row holds columns 0..999 of 1024 and regrows all of its 24 empty
+    # columns: the regrown positions all fall in the last of the column-order
+    # buckets, which overflows, and the column view is rebuilt instead of
+    # updated; the results are the same.
+    out_f, in_f, K = 32, 1024, 1000
+    rng = np.random.default_rng(4)
+    row = np.repeat(np.arange(out_f, dtype=np.int32), K)
+    col = np.tile(np.arange(K, dtype=np.int32), out_f)
+    val = rng.normal(0.0, 0.5, size=out_f * K).astype(np.float32)
+    lay = wl.Layer(out_f, in_f, row, col, val, rng.normal(size=out_f).astype(np.float32), "f32")
+    restructure_rows_and_check(lay, 24, seed=2, step=1, acts=wl.make_acts(8, in_f, out_f, "f32", seed=8))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", [(1024, 1024, 51), (768, 3072, 31), (3072, 768, 8), (300, 7000, 3)])
 def test_diagonal_patterns(dtype, shape):
     # A diagonal sparsity pattern (wrapped diagonals, the same column offsets
