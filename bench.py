@@ -736,18 +736,22 @@ class _Timer:
         self.s.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
 
-    def time_restructure(self, snack, h, run, reps: int, cold: bool) -> tuple:
+    def time_restructure(self, snack, h, run, reps: int, cold: bool, prep=None) -> tuple:
         """A restructure call timed alone: each rep starts after the previous call's column-view
-        update (snack_wait_plan) and, cold, a read of 2x L2; the device sleeps briefly so the host
-        queues the call's first launches before they run.  Medians of the time until the call
-        returns and until its column-view update is done, in us."""
+        update (snack_wait_plan), `prep` (untimed) and, cold, a read of 2x L2; the device sleeps
+        briefly so the host queues the call's first launches before they run.  Medians of the time
+        until the call returns and until its column-view update is done, in us."""
         torch = self.torch
         ret, done = [], []
         with torch.cuda.stream(self.s):
             for _ in range(3):
+                if prep is not None:
+                    prep()
                 run()
             for _ in range(reps):
                 snack.snack_wait_plan(h, self.s)
+                if prep is not None:
+                    prep()
                 if cold:
                     torch.sum(self.flush, dim=0, out=self.flush_out)
                 torch.cuda._sleep(int(1e5))
@@ -800,7 +804,7 @@ def _layer_rows(name, lay, batch, ours, dense, mask, oracle_t, peak, cores):
     out = []
     for op, t in ours.items():
         cold, warm, graphed = t
-        base = op[:-4] if op.endswith("_all") else op  # restructure_all: the restructure's bytes
+        base = "restructure" if op.startswith("restructure") else op  # every restructure row: its bytes
         flops = {"fwd": 2, "dx": 2, "dw": 2, "bwd": 4}.get(op, 0) * lay.nnz * batch
         gbs = byts[base] / (cold * 1e-6) / 1e9
         rec = {"config": name, "layer": f"{lay.out_f}x{lay.in_f}", "nnz": lay.nnz, "batch": batch, "op": op,
@@ -873,6 +877,18 @@ def _bench_layer(torch, F, snack, timer, name, lay, batch, ops, reps, dev, oracl
         cold, warm = timer.time_restructure(snack, h, restructure, rr, True), timer.time_restructure(snack, h, restructure, rr, False)
         ours["restructure"] = (cold[0], warm[0], False)  # until the call returns
         ours["restructure_all"] = (cold[1], warm[1], False)  # until its column-view update is done
+        # Back to back, each call prunes the previous call's regrown zeros (ties at |w| = 0).  With
+        # fresh values before every call (the layer's value distribution, as after an optimizer
+        # step; untimed) the select sees a continuous distribution instead.
+        fresh = torch.from_numpy(lay.val).to(dev)
+
+        def refill():
+            bufs[state["cur"]][2].copy_(fresh)
+
+        cold, warm = (timer.time_restructure(snack, h, restructure, rr, True, refill),
+                      timer.time_restructure(snack, h, restructure, rr, False, refill))
+        ours["restructure_fresh"] = (cold[0], warm[0], False)
+        ours["restructure_fresh_all"] = (cold[1], warm[1], False)
         if state["cur"] == 1:  # back on the first buffers
             restructure()
     # comparators: dense W (cuBLAS via F.linear / matmul) and Dense+Mask (W*M materialised every call)
