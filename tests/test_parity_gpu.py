@@ -561,6 +561,29 @@ def test_backward_workloads_c1_c4():
         check_layer_ops(lay, acts, ops=("dx", "dw"), got=run_backward(lay, acts))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_rows_repeated_calls(dtype):
+    # Rows split between tiles (long Zipf rows span several) leave partials
+    # that the fix-up adds in tile order: one handle, several batch sizes
+    # (one and several batch tiles), every tile-path op twice in a row, each
+    # call bit-identical to the one before and within the bound of the oracle.
+    lay = wl.make_layer(600, 900, nnz=60000, zipf_s=1.3, val_std=0.3, val_dtype=dtype, seed=17, bias="normal")
+    row, col, val, bias = layer_tensors(lay)
+    L = snack.SparseLinear(600, 900, row, col, val, bias, max_batch=300)
+    for batch in (9, 300, 33, 300, 9):
+        acts = wl.make_acts(batch, 900, 600, dtype, seed=batch)
+        x, dy = act_tensor(acts.x, dtype), act_tensor(acts.dy, dtype)
+        got = {"y": L.forward(x), "dx": L.grad_input(dy)}
+        got["dw"], got["db"] = L.grad_weight(x, dy)
+        dx_b, dw_b, _ = L.backward(x, dy)
+        again = (L.forward(x), L.grad_input(dy), L.backward(x, dy)[0])
+        torch.cuda.synchronize()
+        assert torch.equal(got["y"], again[0]) and torch.equal(got["dx"], again[1]), batch
+        assert torch.equal(dx_b, again[2]) and torch.equal(dx_b, got["dx"]), batch
+        check_layer_ops(lay, acts, got=got)
+    L.close()
+
+
 @pytest.mark.parametrize("batch,out_f,in_f,nnz", [(32, 300, 400, 20000), (5, 300, 400, 20000),
                                                   (8, 3000, 600, 900000)])
 def test_backward_equals_separate_calls_bitwise(batch, out_f, in_f, nnz):
