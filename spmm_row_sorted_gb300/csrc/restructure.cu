@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool 
                                                   uint32_t *col_ok, const uint32_t *stop) {
   pdl_wait();
   if (stop && (stop[0] | stop[1])) return;
-  __shared__ uint64_t sk[8][kBktCap];
+  __shared__ __align__(16) uint64_t sk[8][kBktCap];
   __shared__ uint32_t s_red[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (blockIdx.x == 0 && threadIdx.x == 0 && ds) publish(ds, n_prune, host_words, true, col_ok);
@@ -756,18 +756,7 @@ __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool 
   for (uint32_t w = 0; w < (uint32_t)warp; ++w) before += S.count(b0 + w);
   const uint32_t L = S.count(b);
   const size_t sb = (size_t)b * kBktCap;
-  for (uint32_t i = lane; i < L; i += 32) sk[warp][i] = S.key[sb + i];
-  __syncwarp();
-  for (uint32_t i = lane; i < L; i += 32) {
-    const uint64_t k = sk[warp][i];
-    uint32_t r = 0;
-    if (k32) {  // keys below 2^32: compare the low words
-      const uint32_t *s32 = reinterpret_cast<const uint32_t *>(sk[warp]);
-      const uint32_t k_lo = (uint32_t)k;
-      for (uint32_t j = 0; j < L; ++j) r += s32[2 * j] < k_lo ? 1u : 0u;
-    } else {
-      for (uint32_t j = 0; j < L; ++j) r += sk[warp][j] < k ? 1u : 0u;
-    }
+  auto put = [&](uint32_t i, uint64_t k, uint32_t r) {
     const int64_t dst = (int64_t)before + r;
     if (dst < n_prune) {  // always, unless a bucket ran over (then the lists are discarded)
       if (D.key64)
@@ -775,6 +764,36 @@ __global__ void __launch_bounds__(256) k_bkt_rank(BucketSet R, RankDst DR, bool 
       else
         D.key32[dst] = (uint32_t)k;
       D.q[dst] = S.q[sb + i];
+    }
+  };
+  if (k32) {
+    // keys below 2^32: staged as 32-bit words padded with ~0u (never below a
+    // key) to a multiple of four; a lane ranks two keys per sweep, reading
+    // four staged keys per 16-byte load
+    uint32_t *s32 = reinterpret_cast<uint32_t *>(sk[warp]);
+    const uint32_t L4 = (L + 3u) & ~3u;
+    for (uint32_t i = lane; i < L4; i += 32) s32[i] = i < L ? (uint32_t)S.key[sb + i] : ~0u;
+    __syncwarp();
+    for (uint32_t i = lane; i < L; i += 64) {
+      const bool two = i + 32 < L;
+      const uint32_t ka = s32[i], kb = two ? s32[i + 32] : 0u;
+      uint32_t ra = 0, rb = 0;
+      for (uint32_t j = 0; j < L4; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(s32 + j);
+        ra += (v.x < ka ? 1u : 0u) + (v.y < ka ? 1u : 0u) + (v.z < ka ? 1u : 0u) + (v.w < ka ? 1u : 0u);
+        rb += (v.x < kb ? 1u : 0u) + (v.y < kb ? 1u : 0u) + (v.z < kb ? 1u : 0u) + (v.w < kb ? 1u : 0u);
+      }
+      put(i, ka, ra);
+      if (two) put(i + 32, kb, rb);
+    }
+  } else {
+    for (uint32_t i = lane; i < L; i += 32) sk[warp][i] = S.key[sb + i];
+    __syncwarp();
+    for (uint32_t i = lane; i < L; i += 32) {
+      const uint64_t k = sk[warp][i];
+      uint32_t r = 0;
+      for (uint32_t j = 0; j < L; ++j) r += sk[warp][j] < k ? 1u : 0u;
+      put(i, k, r);
     }
   }
 }
