@@ -337,7 +337,8 @@ snack_status run_dw(snack_handle h, const int32_t *row, const int32_t *col, cons
 }
 
 // Fused backward: one pass over the column view gives dX and dW (one batch
-// tile); wider batches run the input gradient and the SDDMM separately.
+// tile); wider batches run the input gradient and the SDDMM separately, over
+// one transpose of dY and X.
 template <typename T>
 snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, const void *val, const void *x,
                      const void *dy, int32_t batch, void *dx, float *dw, float *db, void *ws, size_t ws_bytes,
@@ -351,11 +352,15 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
     return SNACK_OK;
   }
   BatchGeom bg = batch_geom(batch, h->act_t);
-  if (bg.n_btiles > 1 || h->nnz == 0) {
+  if (h->nnz == 0) {
     snack_status st = run_dx<T>(h, val, dy, batch, dx, ws, ws_bytes, s);
     if (st != SNACK_OK) return st;
     return run_dw<T>(h, row, col, x, dy, batch, dw, db, ws, ws_bytes, s);
   }
+  // one batch tile: dX and dW in one pass over the column view; wider
+  // batches: the input gradient's tiles, then the SDDMM, both reading the
+  // same transposed dY (and the SDDMM the transposed X)
+  const bool fused = bg.n_btiles == 1;
   BwdWs W = bwd_ws(h->out_f, h->in_f, h->lay.gt, bg, sizeof(T), batch);
   if (ws_bytes < W.total) return SNACK_ERR_WORKSPACE;
   uint8_t *b = reinterpret_cast<uint8_t *>(ws);
@@ -390,12 +395,13 @@ snack_status run_bwd(snack_handle h, const int32_t *row, const int32_t *col, con
   p.batch = batch;
   p.carry = reinterpret_cast<float *>(b + W.carry);
   p.head = reinterpret_cast<float *>(b + W.head);
-  p.xt_dw = xt;
-  p.dw = dw;
+  p.xt_dw = fused ? xt : nullptr;
+  p.dw = fused ? dw : nullptr;
   p.act = kActNone;
   p.pre_in = nullptr;
   p.pre_out = nullptr;
-  SNACK_CUDA(run_spmm<T>(p, bg, true, true, s));
+  SNACK_CUDA(run_spmm<T>(p, bg, true, fused, s));
+  if (!fused) SNACK_CUDA(run_sddmm<T>(h->nnz, row, col, h->out_f, h->in_f, xt, dyt, bg, dw, h->num_sms, s));
   return SNACK_OK;
 }
 
