@@ -533,8 +533,9 @@ __global__ void k_colsum(const T *__restrict__ a, int batch, int n, float *__res
 }
 
 // out[r] = sum_b at[r][b] over the feature-major copy (rows ldx apart): one
-// warp per row, lane-strided partial sums combined by a fixed shuffle tree,
-// so the result does not depend on scheduling.
+// warp per row, each lane adding 16-byte runs of the row (single elements,
+// lane-strided, when rows are not 16-byte aligned), the lanes' sums combined
+// by a fixed shuffle tree, so the result does not depend on scheduling.
 template <typename T>
 __global__ void __launch_bounds__(256) k_rowsum_t(const T *__restrict__ at, int ldx, int batch, int n,
                                                   float *__restrict__ out) {
@@ -543,8 +544,21 @@ __global__ void __launch_bounds__(256) k_rowsum_t(const T *__restrict__ at, int 
   if (r >= n) return;
   const T *p = at + (size_t)r * ldx;
   float s = 0.f;
+  constexpr int kV = 16 / (int)sizeof(T);  // elements per 16-byte load
+  if (ldx % kV == 0) {  // rows start on 16-byte boundaries: a lane adds kV consecutive elements per load
+    const int nv = batch / kV;
+#pragma unroll 2
+    for (int v = lane; v < nv; v += 32) {
+      const uint4 q = *reinterpret_cast<const uint4 *>(p + (size_t)v * kV);
+      const T *e = reinterpret_cast<const T *>(&q);
+#pragma unroll
+      for (int k = 0; k < kV; ++k) s += to_f32(e[k]);
+    }
+    for (int b = nv * kV + lane; b < batch; b += 32) s += to_f32(p[b]);
+  } else {
 #pragma unroll 4
-  for (int b = lane; b < batch; b += 32) s += to_f32(p[b]);
+    for (int b = lane; b < batch; b += 32) s += to_f32(p[b]);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) out[r] = s;
