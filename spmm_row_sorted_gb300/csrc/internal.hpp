@@ -26,7 +26,7 @@ struct PlanPtrs {
   // the row and column bits fit 31 together): a second column view, written
   // by the update while the current one is read (the handle swaps the two
   // when the update is queued), and the update's scratch, which must outlive
-  // the call because the update runs on the handle's second stream.
+  // the call because the update runs on a stream of the handle after it returns.
   int32_t *cp_alt, *tiles_t_alt, *row_t_alt, *src_t_alt;
   uint16_t *rowt16_alt;
   uint32_t *newidx;   // [nnz] output index of each stored weight (~0u: pruned)

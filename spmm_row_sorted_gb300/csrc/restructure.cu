@@ -21,8 +21,8 @@
 //     next tile's, so a survivor lands at (survivors before it) + (regrown
 //     below it) and a regrown position at (its rank) + (survivors below it);
 //     the same pass writes the row offsets and the 16-bit columns;
-//  4. the column view is updated the same way on the second stream after the
-//     call returns: the current view's kept entries (column order) merged with
+//  4. the column view is updated the same way on the handle's lowest-priority
+//     stream after the call returns: the current view's kept entries (column order) merged with
 //     the regrown positions in column order, into the plan's second view.
 // Steps 3 and 4 are queued before the host has read how many draws the first
 // chunk accepted, behind a device flag that step 2 sets only when the chunk

@@ -445,8 +445,8 @@ bool restructure_streams(snack_handle h) {
   return true;
 }
 
-// The column view of a restructured handle may still be rebuilding on the
-// handle's second stream: order `s` after it.  The forward reads only the
+// The column view of a restructured handle may still be updating on a
+// stream of the handle: order `s` after it.  The forward reads only the
 // row half of the plan and does not wait.
 bool wait_colview(snack_handle h, cudaStream_t s) {
   return !h->colview_pending || cudaStreamWaitEvent(s, h->ev_colview, 0) == cudaSuccess;
