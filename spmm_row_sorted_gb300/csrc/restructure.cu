@@ -579,12 +579,15 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
     *col_ok = 0u;
     *lb_ticket = 0u;
   }
+  // 16-byte stores: the table (a power of two of at least 16 slots) and the
+  // bucket counts (a multiple of 16 words) start on 16-byte boundaries
   const int64_t cap = (int64_t)tab.mask + 1;
-  for (int64_t i = i0; i < cap; i += stride) {
-    tab.keys[i] = kEmpty;
-    if (!tab.packed) tab.mins[i] = 0xFFFFFFFFu;
-  }
-  for (int64_t i = i0; i < nb; i += stride) bcnt[i] = 0u;
+  const uint4 ones = make_uint4(~0u, ~0u, ~0u, ~0u), zeros = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = i0; i < cap / 2; i += stride) reinterpret_cast<uint4 *>(tab.keys)[i] = ones;
+  if (!tab.packed)
+    for (int64_t i = i0; i < cap / 4; i += stride) reinterpret_cast<uint4 *>(tab.mins)[i] = ones;
+  for (int64_t i = i0; i < nb / 4; i += stride) reinterpret_cast<uint4 *>(bcnt)[i] = zeros;
+  for (int64_t i = (nb / 4) * 4 + i0; i < nb; i += stride) bcnt[i] = 0u;
   for (int64_t i = i0; i < n_lb; i += stride) lb_status[i] = 0ull;
   for (int64_t i = i0; i < n_pc; i += stride) pcnt[i] = 0u;
 }
