@@ -32,11 +32,11 @@ __device__ __forceinline__ T warp_inclusive_scan(T v) {
   return v;
 }
 
-// Exclusive scan across the block (blockDim.x == kScanThreads).  Returns the
-// thread's exclusive prefix; *total gets the block sum.
-template <typename T>
+// Exclusive scan across the block (blockDim.x == kThreads, at most 1024).
+// Returns the thread's exclusive prefix; *total gets the block sum.
+template <typename T, int kThreads = kScanThreads>
 __device__ __forceinline__ T block_exclusive_scan(T v, T *total) {
-  constexpr int kNW = kScanThreads / 32;
+  constexpr int kNW = kThreads / 32;
   __shared__ T warp_tot[kNW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   T inc = warp_inclusive_scan(v);

@@ -592,6 +592,12 @@ __global__ void k_rs_init(DrawState *ds, PosTable tab, uint32_t *__restrict__ bc
   for (int64_t i = i0; i < n_pc; i += stride) pcnt[i] = 0u;
 }
 
+// The acceptance scan's block: a scan tile of draws over 1024 threads, two
+// per thread (its phases are dependent round trips; more warps per tile keep
+// more of them in flight).
+constexpr int kAccThreads = 1024, kAccItems = kScanTile / kAccThreads;
+static_assert(kAccItems * kAccThreads == kScanTile, "one acceptance block per scan tile");
+
 // Acceptance of a draw chunk, its scan over draw order and (first chunk) the
 // bucket placement of the regrown positions, in one pass: tiles of kScanTile
 // draws taken in ticket order.  A block flags its tile's draws (an empty
@@ -619,7 +625,7 @@ struct AcceptArgs {
   uint32_t *total;
 };
 
-__global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
+__global__ void __launch_bounds__(kAccThreads) k_accept_scan(AcceptArgs a) {
   constexpr int kPadded = kScanTile + kScanTile / 32 + 1;
   __shared__ uint32_t sF[kPadded];  // flags, then exclusive counts (one pad word per 32)
   __shared__ int64_t s_tile;
@@ -631,36 +637,36 @@ __global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
   if (tid == 0) s_tile = atomicAdd(a.ticket, 1u);
   __syncthreads();
   const int64_t t = s_tile, base = t * kScanTile;
-  uint64_t p[kScanItems], h[kScanItems], w[kScanItems];
+  uint64_t p[kAccItems], h[kAccItems], w[kAccItems];
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    const int64_t idx = base + i * kScanThreads + tid;
+  for (int i = 0; i < kAccItems; ++i) {
+    const int64_t idx = base + i * kAccThreads + tid;
     p[i] = idx < a.m ? a.cand[idx] : kEmpty;
   }
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {  // every item's first probe in flight at once
+  for (int i = 0; i < kAccItems; ++i) {  // every item's first probe in flight at once
     h[i] = a.tab.home(p[i]);
     w[i] = p[i] != kEmpty ? a.tab.keys[h[i]] : kEmpty;
   }
-  uint32_t f[kScanItems];
+  uint32_t f[kAccItems];
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    const int64_t idx = base + i * kScanThreads + tid;
+  for (int i = 0; i < kAccItems; ++i) {
+    const int64_t idx = base + i * kAccThreads + tid;
     f[i] = p[i] != kEmpty && a.tab.min_from(p[i], h[i], w[i]) == (uint32_t)(a.i0 + (uint64_t)idx) ? 1u : 0u;
-    sF[pad(i * kScanThreads + tid)] = f[i];
+    sF[pad(i * kAccThreads + tid)] = f[i];
   }
   __syncthreads();
   {
-    uint32_t v[kScanItems], tsum = 0;
+    uint32_t v[kAccItems], tsum = 0;
 #pragma unroll
-    for (int i = 0; i < kScanItems; ++i) {
-      v[i] = sF[pad(tid * kScanItems + i)];
+    for (int i = 0; i < kAccItems; ++i) {
+      v[i] = sF[pad(tid * kAccItems + i)];
       tsum += v[i];
     }
-    uint32_t ex = block_exclusive_scan<uint32_t>(tsum, &s_tot);
+    uint32_t ex = block_exclusive_scan<uint32_t, kAccThreads>(tsum, &s_tot);
 #pragma unroll
-    for (int i = 0; i < kScanItems; ++i) {
-      sF[pad(tid * kScanItems + i)] = ex;
+    for (int i = 0; i < kAccItems; ++i) {
+      sF[pad(tid * kAccItems + i)] = ex;
       ex += v[i];
     }
   }
@@ -672,19 +678,19 @@ __global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
     }
   }
   __syncthreads();
-  int64_t q[kScanItems];
-  bool put[kScanItems];
+  int64_t q[kAccItems];
+  bool put[kAccItems];
 #pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    q[i] = a.before + (int64_t)s_pre + sF[pad(i * kScanThreads + tid)];
+  for (int i = 0; i < kAccItems; ++i) {
+    q[i] = a.before + (int64_t)s_pre + sF[pad(i * kAccThreads + tid)];
     put[i] = f[i] && q[i] < a.n_prune;
     if (put[i]) a.grown[q[i]] = p[i];
   }
   if (a.br.nb) {  // bucket slots: every atomic in flight before the stores that use them
     const bool col = a.bc.nb != 0;
-    uint32_t bk[kScanItems], slot[kScanItems], ck[kScanItems], bkc[kScanItems], slotc[kScanItems];
+    uint32_t bk[kAccItems], slot[kAccItems], ck[kAccItems], bkc[kAccItems], slotc[kAccItems];
 #pragma unroll
-    for (int i = 0; i < kScanItems; ++i) {
+    for (int i = 0; i < kAccItems; ++i) {
       bk[i] = put[i] ? (uint32_t)__umul64hi(p[i], a.br.mult) : 0u;
       slot[i] = put[i] ? atomicAdd(&a.br.cnt[(size_t)bk[i] * kCntStride], 1u) : 0u;
       ck[i] = put[i] && col ? (uint32_t)col_major(p[i], a.cbits, a.rbits) : 0u;
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(kScanThreads) k_accept_scan(AcceptArgs a) {
       slotc[i] = put[i] && col ? atomicAdd(&a.bc.cnt[(size_t)bkc[i] * kCntStride], 1u) : 0u;
     }
 #pragma unroll
-    for (int i = 0; i < kScanItems; ++i) {
+    for (int i = 0; i < kAccItems; ++i) {
       if (!put[i]) continue;
       if (slot[i] < (uint32_t)kBktCap) {
         a.br.key[(size_t)bk[i] * kBktCap + slot[i]] = p[i];
@@ -1629,7 +1635,7 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
                         aticket,
                         &ds->lb_fail,
                         &ds->total};
-    launch_pdl(k_accept_scan, (unsigned)n_at, kScanThreads, 0, s2, aa);
+    launch_pdl(k_accept_scan, (unsigned)n_at, kAccThreads, 0, s2, aa);
     return cudaGetLastError();
   };
   auto chunk_size = [&]() -> int64_t {
