@@ -258,10 +258,11 @@ snack_status snack_restructure_workspace_size(snack_handle h, int64_t n_prune, s
  * survivor, -1 for a regrown entry.  The handle's plan is rebuilt for the new
  * pattern; later calls must pass row_out/col_out.  Needs ws_bytes >=
  * snack_restructure_workspace_size(h, n_prune).  The regrow (draws,
- * acceptance, sort of the new positions) runs on the handle's second stream,
- * forked from and joined back into `stream`, concurrently with the prune
- * select; the host waits once per batch of draws (normally once) for that
- * batch's accepted count, while the device keeps working.  When the call
+ * acceptance, sort of the new positions) runs on `stream`; the prune select
+ * runs concurrently on the handle's second stream (lowest priority), forked
+ * from and joined back into `stream`; the host waits once per batch of
+ * draws (normally once) for that batch's accepted count, while the device
+ * keeps working.  When the call
  * returns, the new COO, the source map and the row half of the plan are
  * ordered on `stream`; the workspace is free for the next call at once.  For
  * layers with the deferred scratch in their plan (see snack_query_sizes) the

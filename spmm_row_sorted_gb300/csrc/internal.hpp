@@ -122,7 +122,7 @@ struct RestructureArgs {
                           // overflows, and the acceptance scan's look-back error
   uint32_t *counts_dev;   // the same words' device address (written by a kernel, no copy)
   cudaEvent_t counts_ready;  // recorded after the kernel that writes host_counts
-  cudaStream_t aux;          // second stream of the handle (regrow branch), highest priority
+  cudaStream_t aux;          // second stream of the handle (the prune select), lowest priority
   cudaStream_t aux_lo;       // third stream (the deferred column-view update), lowest priority
   cudaEvent_t ev_fork, ev_join, ev_aux;
 };

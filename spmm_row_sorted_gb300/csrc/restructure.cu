@@ -1587,17 +1587,20 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
   } while (0)
 
   // Two branches meet at the merge: the regrow (draws, acceptance, sort of
-  // the regrown positions) depends only on the old pattern and runs on the
-  // handle's second stream, beside the prune select on the caller's stream.
-  // The host reads each draw chunk's accepted count from mapped pinned words
-  // that a kernel writes (an event marks them ready).
-  cudaStream_t s2 = a.aux;
+  // the regrown positions) depends only on the old pattern; it is the longer
+  // of the two and runs on the caller's stream (s2 = s), while the prune
+  // select runs beside it on the handle's second stream ss, of the lowest
+  // priority (so the regrow's blocks go first), forked from s at the start
+  // and joined back before the merge.  The host reads each draw chunk's
+  // accepted count from mapped pinned words that a kernel writes (an event
+  // marks them ready).
+  cudaStream_t s2 = s, ss = a.aux;
   auto fork = [&]() -> cudaError_t {
     cudaError_t err = cudaEventRecord(a.ev_fork, s);
-    return err != cudaSuccess ? err : cudaStreamWaitEvent(s2, a.ev_fork, 0);
+    return err != cudaSuccess ? err : cudaStreamWaitEvent(ss, a.ev_fork, 0);
   };
   auto join = [&]() -> cudaError_t {
-    cudaError_t err = cudaEventRecord(a.ev_join, s2);
+    cudaError_t err = cudaEventRecord(a.ev_join, ss);
     return err != cudaSuccess ? err : cudaStreamWaitEvent(s, a.ev_join, 0);
   };
   SNACK_TRY(fork());
@@ -1698,22 +1701,19 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
                       !update);
   };
   // 4: the column-view update, on the third stream (lowest priority), after
-  // s's work so far and everything on s2
+  // s's work so far (which waits for the select)
   cudaStream_t s3 = a.aux_lo;
   auto queue_cols = [&]() -> cudaError_t {
     cudaError_t err = cudaEventRecord(a.ev_fork, s);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(s3, a.ev_fork, 0);
-    if (err == cudaSuccess) err = cudaEventRecord(a.ev_aux, s2);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(s3, a.ev_aux, 0);
     if (err != cudaSuccess) return err;
     return queue_colview_merge(pl, a.in_f, nnz, n_prune, rbits, col_guard, a.gt, s3);
   };
-  auto mark = [&]() -> cudaError_t { return cudaEventRecord(a.ev_join, s2); };  // s joins s2 here
+  auto mark = [&]() -> cudaError_t { return cudaEventRecord(a.ev_join, ss); };
   auto wait_mark = [&]() -> cudaError_t { return cudaStreamWaitEvent(s, a.ev_join, 0); };
 
-  // 2. regrow, first chunk, and its sorted lists (on s2): the row-order list
-  //    is what the merge waits for; the column-order list is made after it,
-  //    beside the merge
+  // 2. regrow, first chunk, and its sorted lists (on s2 = s): the merge
+  //    follows them in stream order
   int64_t m = 0;
   e = cudaSuccess;
   if (n_prune > 0) {
@@ -1732,7 +1732,6 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
         launch_pdl(k_bkt_rank, nr + nc, 256, 0, s2, br, RankDst{B, nullptr, Bq}, k32, nr, bc,
                    RankDst{nullptr, pl.gc_key, pl.gc_q}, n_prune, ds, a.counts_dev, col_ok, (const uint32_t *)nullptr);
         e = cudaGetLastError();
-        if (e == cudaSuccess) e = mark();
       } else {
         e = sort_rows_general();
         if (e == cudaSuccess) e = sort_cols_general();
@@ -1740,35 +1739,34 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
           launch_pdl(k_publish, 1, 1, 0, s2, ds, n_prune, a.counts_dev, 1, col_ok);
           e = cudaGetLastError();
         }
-        if (e == cudaSuccess) e = mark();
       }
     }
     if (e == cudaSuccess) e = cudaEventRecord(a.counts_ready, s2);
-  } else {
-    e = mark();
   }
   if (e != cudaSuccess) {
     join();
     return SNACK_ERR_CUDA;
   }
-  // 1. prune threshold: three digit passes (11, 10, 10 bits), high to low; keep counts per tile
-  launch_pdl(k_sel_init, 1, 256, 0, s, st, (uint32_t)n_prune);
+  // 1. prune threshold (on ss): three digit passes (11, 10, 10 bits), high to
+  //    low; keep counts per tile
+  launch_pdl(k_sel_init, 1, 256, 0, ss, st, (uint32_t)n_prune);
   if (n_prune > 0) {
     // first digit over every key; the keys in its bucket listed while each
     // tile counts those above it; the rest of the select and the tiles' keep
     // counts from the list
-    launch_pdl(k_sel_pass<TV, 0>, grid_for((nnz + 15) / 16, 256, 1184), 256, 0, s, val, nnz, st);
+    launch_pdl(k_sel_pass<TV, 0>, grid_for((nnz + 15) / 16, 256, 1184), 256, 0, ss, val, nnz, st);
     uint64_t *scand = reinterpret_cast<uint64_t *>(b + W.scand);
-    launch_pdl(k_sel_bucket<TV>, (unsigned)n_tiles, kScanThreads, 0, s, val, nnz, st, sums, scand);
-    launch_pdl(k_sel_cand<1>, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, st);
-    launch_pdl(k_sel_cand<2>, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, st);
-    launch_pdl(k_sel_tiles, kSelCandBlocks, 256, 0, s, (const uint64_t *)scand, (const SelState *)st, sums);
+    launch_pdl(k_sel_bucket<TV>, (unsigned)n_tiles, kScanThreads, 0, ss, val, nnz, st, sums, scand);
+    launch_pdl(k_sel_cand<1>, kSelCandBlocks, 256, 0, ss, (const uint64_t *)scand, st);
+    launch_pdl(k_sel_cand<2>, kSelCandBlocks, 256, 0, ss, (const uint64_t *)scand, st);
+    launch_pdl(k_sel_tiles, kSelCandBlocks, 256, 0, ss, (const uint64_t *)scand, (const SelState *)st, sums);
     row_direct = n_tiles <= kScanDirectTiles;
-    if (!row_direct) launch_pdl(k_scan_spine<uint64_t>, 1, kScanThreads, 0, s, sums, n_tiles, (uint64_t *)nullptr);
+    if (!row_direct) launch_pdl(k_scan_spine<uint64_t>, 1, kScanThreads, 0, ss, sums, n_tiles, (uint64_t *)nullptr);
     e = cudaGetLastError();
   } else {
-    e = keep_sums(KeepVal<TV>{val, st}, nnz, sums, s, &row_direct);
+    e = keep_sums(KeepVal<TV>{val, st}, nnz, sums, ss, &row_direct);
   }
+  if (e == cudaSuccess) e = mark();
   // With the update, 3 and 4 are queued at once behind the lists' flags (they
   // write nothing unless the first chunk's lists came out whole); a plan
   // rebuild on s cannot be undone, so without the update they wait for the
@@ -1801,7 +1799,6 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       // the first chunk fell short or a row-order bucket ran over: more draws
       // (after everything queued so far), the general sorts, and 3 and 4 again
       rows_queued = cols_queued = false;
-      SNACK_TRY(fork());
       while (acc < n_prune) {
         if (done >= W.d_max) {
           verdict = SNACK_ERR_NO_SPACE;
@@ -1842,7 +1839,6 @@ snack_status restructure_impl(const RestructureArgs &a, void *ws, size_t ws_byte
       // only a column-order bucket ran over: the merge has written the
       // output; the column-order list the general way and 4 again
       cols_queued = false;
-      SNACK_TRY(fork());
       SNACK_TRY(sort_cols_general());
       launch_pdl(k_set_word, 1, 1, 0, s2, col_ok, 1u);
       SNACK_TRY(cudaGetLastError());

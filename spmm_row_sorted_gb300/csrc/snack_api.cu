@@ -431,14 +431,16 @@ bool restructure_streams(snack_handle h) {
   if (!h->ev_aux && cudaEventCreateWithFlags(&h->ev_aux, cudaEventDisableTiming) != cudaSuccess) return false;
   if (!h->aux || !h->aux_lo) {
     // The regrow branch (draws, acceptance, sort) is the longer of the two
-    // that meet at the merge: its stream gets the highest priority, so its
-    // blocks are scheduled ahead of the select's when both wait for SMs.
-    // The column-view update that runs on after the call returns gets the
-    // lowest, so the caller's next calls go ahead of it where their streams
-    // have a higher priority.
+    // that meet at the merge and runs on the caller's stream; the select
+    // beside it gets the second stream at the lowest priority, so the
+    // regrow's blocks are scheduled ahead of the select's when both wait for
+    // SMs.  The column-view update that runs on after the call returns gets
+    // the third, also of the lowest priority, so the caller's next calls go
+    // ahead of it where their streams have a higher priority.
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-    if (!h->aux && cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
+    (void)greatest;
+    if (!h->aux && cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, least) != cudaSuccess) return false;
     if (!h->aux_lo && cudaStreamCreateWithPriority(&h->aux_lo, cudaStreamNonBlocking, least) != cudaSuccess)
       return false;
   }
