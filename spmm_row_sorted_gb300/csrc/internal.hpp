@@ -220,7 +220,7 @@ struct snack_layer {
   uint32_t *host_counts = nullptr;  // restructure read-back (pinned, mapped), made on first use
   uint32_t *host_counts_dev = nullptr;  // its device address
   cudaEvent_t counts_ready = nullptr;
-  cudaStream_t aux = nullptr;     // restructure's second stream and its fork/join events, made on first use
+  cudaStream_t aux = nullptr;     // restructure's second stream (its select) and fork/join events, made on first use
   cudaStream_t aux_lo = nullptr;  // and its third stream (lowest priority)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_aux = nullptr;
   // The column view of the last restructure is updated on `aux_lo` after the

@@ -1,12 +1,13 @@
 // Dynamic Sparse Training restructure on the GPU (prune smallest |w|, regrow
 // at random empty positions with value +0, re-sort the COO).
 //
-//  1. prune set: radix select (digits of 11, 10 and 10 bits, high to low) of
+//  1. prune set (on the handle's second stream, of the lowest priority,
+//     beside step 2): radix select (digits of 11, 10 and 10 bits, high to low) of
 //     the n_prune-th smallest magnitude key t; ties at t are pruned in
 //     storage order, so the pruned set is exactly the n_prune smallest
 //     (|w|, k); one more pass counts, per tile of stored weights, those above
 //     t and those equal to it;
-//  2. regrow, on the handle's second stream beside step 1: draws i of
+//  2. regrow, on the caller's stream beside step 1: draws i of
 //     SplitMix64 map to positions by multiply-high; a draw is a candidate when
 //     the position was empty (binary search in its old row), and is accepted
 //     when it is the first draw of its position -- a hash table keeps the
@@ -522,7 +523,7 @@ __device__ __forceinline__ uint64_t col_major(uint64_t p, int cbits, int rbits) 
   return ((p & ((1ull << cbits) - 1ull)) << rbits) | (p >> cbits);
 }
 
-// Counters of the regrow branch (it runs beside the select on a second stream).
+// Counters of the regrow branch (it runs beside the select, which has a stream of its own).
 struct DrawState {
   uint32_t total, overflow;  // accepted draws of the last chunk; a draw found the position table full
   uint32_t bucket_overflow;  // a row-order bucket of the regrown positions ran out of slots
